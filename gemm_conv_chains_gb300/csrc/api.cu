@@ -1,0 +1,607 @@
+// api.cu -- the extern "C" entry points of libb2b.so (declared in include/b2b.h).
+//
+// Host side only: argument validation (before anything touches the GPU), TMA tensor-map
+// encoding (cached), the shared-memory plan of each launch, and the launch itself on the
+// caller's stream.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
+#include <unordered_map>
+
+#include "b2b.h"
+#include "ptx.cuh"
+#include "launch.h"
+
+namespace b2b {
+namespace {
+
+// ------------------------------------------------------------------------------------
+// device state
+// ------------------------------------------------------------------------------------
+__device__ uint32_t g_error_word[4];   // {code, kernel id, wait site, tile}
+
+constexpr int kMaxDevices = 64;
+constexpr uint32_t kSmemLimit = 227u * 1024u;          // dynamic smem per CTA on sm_100/103
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;     // 1 s
+
+struct DeviceState {
+  std::once_flag once;
+  int num_sms = 0;
+  uint32_t* err = nullptr;                    // device address of g_error_word
+  cudaError_t init_error = cudaSuccess;
+  std::atomic<uint32_t> attr_done{0};         // bit v: smem attribute set for variant v
+};
+DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
+DeviceState* device_state(b2b_status* st) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *st = B2B_ERR_CUDA;
+    return nullptr;
+  }
+  DeviceState& d = g_dev[dev];
+  std::call_once(d.once, [&d, dev] {
+    int n = 0;
+    d.init_error = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (d.init_error == cudaSuccess) {
+      d.num_sms = n;
+      // The device address of the error word, with this device current.
+      d.init_error = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_error_word);
+    }
+    if (d.init_error != cudaSuccess) cudaGetLastError();
+  });
+  if (d.init_error != cudaSuccess) {
+    *st = B2B_ERR_CUDA;
+    return nullptr;
+  }
+  return &d;
+}
+
+// ------------------------------------------------------------------------------------
+// TMA tensor maps
+// ------------------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  uint32_t rank, is_bf16;
+  uint64_t dims[4];
+  uint64_t strides[3];
+  uint32_t box[4];
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(&k);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(MapKey) / 8; ++i) h = (h ^ w[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+// A tiled, 128B-swizzled map with zero fill outside the tensor.  dims[0] is the
+// contiguous dimension; strides are in bytes for dims 1..rank-1.
+bool make_map(CUtensorMap* out, const void* ptr, int is_bf16, uint32_t rank,
+              std::initializer_list<uint64_t> dims, std::initializer_list<uint64_t> strides,
+              std::initializer_list<uint32_t> box) {
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.ptr = ptr;
+  key.rank = rank;
+  key.is_bf16 = static_cast<uint32_t>(is_bf16);
+  std::copy(dims.begin(), dims.end(), key.dims);
+  std::copy(strides.begin(), strides.end(), key.strides);
+  std::copy(box.begin(), box.end(), key.box);
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return true;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t gdim[4], gstride[3];
+  cuuint32_t bdim[4], estride[4] = {1, 1, 1, 1};
+  for (uint32_t i = 0; i < rank; ++i) {
+    gdim[i] = key.dims[i];
+    bdim[i] = key.box[i];
+  }
+  for (uint32_t i = 0; i + 1 < rank; ++i) gstride[i] = key.strides[i];
+  CUtensorMap m;
+  const CUresult r = fn(&m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        rank, const_cast<void*>(ptr), gdim, gstride, bdim, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  if (g_maps.size() > 4096) g_maps.clear();
+  g_maps.emplace(key, m);
+  *out = m;
+  return true;
+}
+
+// ------------------------------------------------------------------------------------
+// helpers
+// ------------------------------------------------------------------------------------
+inline uint32_t round_up(uint32_t x, uint32_t m) { return (x + m - 1) / m * m; }
+inline int32_t ceil_div(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1) / b); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+inline uint32_t pow2_at_least(uint32_t x) {
+  uint32_t p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+inline bool valid_dtype(int dt) { return dt == B2B_F16 || dt == B2B_BF16; }
+inline bool valid_epi(int e) {
+  return e == B2B_EPI_NONE || e == B2B_EPI_RELU || e == B2B_EPI_HARDSWISH;
+}
+
+// Shared-memory plan: ring of A (and, when streamed, weight) chunks; resident weights;
+// P tile; output staging; biases (fp32); barriers.  Fills the offsets of p.
+bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_bytes) {
+  const uint32_t budget = kSmemLimit - 1024u;   // 1 KiB slack to align the base to 1024
+  const uint32_t n0blk = static_cast<uint32_t>((p.N0p + 63) / 64);
+  const uint32_t n1blk = static_cast<uint32_t>((p.N1p + 63) / 64);
+  p.w0_chunk_bytes = w0mn ? n0blk * 8192u : static_cast<uint32_t>(p.N0p) * 128u;
+  p.w1_chunk_bytes = mode == MODE_CHAIN ? (w1mn ? n1blk * 8192u : static_cast<uint32_t>(p.N1p) * 128u) : 0u;
+  const uint32_t p_bytes = mode == MODE_CHAIN ? n0blk * kPChunkBytes : 0u;
+  const uint32_t out_bytes = mode == MODE_CHAIN    ? n1blk * kPChunkBytes
+                             : mode == MODE_SINGLE ? n0blk * kPChunkBytes
+                                                   : n0blk * kPoolChunkBytes;
+  const uint32_t bias_bytes = round_up(static_cast<uint32_t>(p.N0p + p.N1p) * 4u, 1024u);
+  const uint32_t bar_bytes = 1024u;
+  const uint32_t w_res = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes +
+                         static_cast<uint32_t>(p.kchunks1) * p.w1_chunk_bytes;
+
+  struct Cand { int resident, alias; };
+  const Cand cands[4] = {{1, 0}, {1, 1}, {0, 0}, {0, 1}};
+  int chosen = -1;
+  uint32_t chosen_stages = 0, chosen_stage_bytes = 0;
+  for (int min_stages = 3; min_stages >= 2 && chosen < 0; --min_stages) {
+    for (int c = 0; c < 4; ++c) {
+      if (cands[c].alias && mode != MODE_CHAIN) continue;
+      const uint32_t stage_bytes =
+          cands[c].resident ? kABytes
+                            : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
+      const uint32_t fixed = (cands[c].resident ? w_res : 0u) + p_bytes +
+                             (cands[c].alias ? 0u : out_bytes) + bias_bytes + bar_bytes;
+      if (fixed >= budget) continue;
+      const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / stage_bytes);
+      if (stages < static_cast<uint32_t>(min_stages)) continue;
+      chosen = c;
+      chosen_stages = stages;
+      chosen_stage_bytes = stage_bytes;
+      break;
+    }
+  }
+  if (chosen < 0) return false;
+  p.resident = cands[chosen].resident;
+  p.out_alias_p = cands[chosen].alias;
+  p.num_stages = chosen_stages;
+  p.stage_bytes = chosen_stage_bytes;
+  uint32_t off = 0;
+  p.off_ring = off;
+  off += p.num_stages * p.stage_bytes;
+  p.off_w0 = off;
+  p.off_w1 = off + static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
+  if (p.resident) off += w_res;
+  p.off_p = off;
+  off += p_bytes;
+  p.off_out = p.out_alias_p ? p.off_p : off;
+  if (!p.out_alias_p) off += out_bytes;
+  p.off_bias = off;
+  off += bias_bytes;
+  p.off_bar = off;
+  off += bar_bytes;
+  *smem_bytes = off + 1024u;
+  return *smem_bytes <= kSmemLimit;
+}
+
+void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const void* b1,
+                 DeviceState* d, uint32_t kid) {
+  p.is_bf16 = dt == B2B_BF16 ? 1 : 0;
+  p.act0 = e0;
+  p.act1 = e1;
+  p.b0 = static_cast<const uint16_t*>(b0);
+  p.b1 = static_cast<const uint16_t*>(b1);
+  p.wait_limit_ns = g_wait_ns.load();
+  p.kernel_id = kid;
+  p.err = d->err;
+}
+
+void set_tmem(ChainParams& p, int mode) {
+  if (mode == MODE_CHAIN) {
+    p.acc_stride = round_up(static_cast<uint32_t>(p.N0p), 32u);
+    p.tmem_cols = pow2_at_least(p.acc_stride + static_cast<uint32_t>(p.N1p));
+  } else {
+    p.tmem_cols = pow2_at_least(2u * static_cast<uint32_t>(p.N0p));
+    p.acc_stride = p.tmem_cols / 2u;
+  }
+}
+
+b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtensorMap& w0,
+                  const CUtensorMap& w1, const CUtensorMap& out, ChainParams& p, size_t smem,
+                  void* stream) {
+  const uint32_t bit = 1u << static_cast<uint32_t>(v);
+  if ((d->attr_done.load() & bit) == 0u) {
+    if (cudaFuncSetAttribute(variant_func(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemLimit)) != cudaSuccess) {
+      cudaGetLastError();
+      return B2B_ERR_CUDA;
+    }
+    d->attr_done.fetch_or(bit);
+  }
+  const int grid = std::max(1, std::min(p.num_tiles, d->num_sms));
+  const cudaError_t e =
+      launch_variant(v, a, w0, w1, out, p, grid, smem, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
+// ------------------------------------------------------------------------------------
+// GEMM-shaped entry points (2-D A operand)
+// ------------------------------------------------------------------------------------
+// W0/W1 given as [K][N] row-major (w_mn = true) or as [N][K] (conv filters, w_mn = false).
+b2b_status run_gemm(int mode, bool w_mn, int dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
+                    const void* A, const void* W0, const void* b0, int e0, const void* W1,
+                    const void* b1, int e1, void* D, void* stream, uint32_t kid) {
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  if (d == nullptr) return st;
+  ChainParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = static_cast<int32_t>(M);
+  p.K0 = K0;
+  p.N0 = N0;
+  p.N1 = mode == MODE_CHAIN ? N1 : 0;
+  p.N0p = static_cast<int32_t>(round_up(static_cast<uint32_t>(N0), 16u));
+  p.N1p = mode == MODE_CHAIN ? static_cast<int32_t>(round_up(static_cast<uint32_t>(N1), 16u)) : 0;
+  p.kchunks0 = ceil_div(K0, kChunkK);
+  p.kc_per_tap = p.kchunks0;
+  p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
+  p.num_tiles = ceil_div(M, kBlockM);
+  fill_common(p, dt, e0, e1, b0, b1, d, kid);
+  set_tmem(p, mode);
+  size_t smem = 0;
+  if (!plan_smem(p, mode, w_mn, w_mn, &smem)) return B2B_ERR_UNSUPPORTED;
+
+  CUtensorMap ta, tw0, tw1, to;
+  const uint64_t e = 2;
+  bool ok = make_map(&ta, A, p.is_bf16, 2, {static_cast<uint64_t>(K0), static_cast<uint64_t>(M)},
+                     {K0 * e}, {kChunkK, kBlockM});
+  if (w_mn)
+    ok = ok && make_map(&tw0, W0, p.is_bf16, 2, {static_cast<uint64_t>(N0), static_cast<uint64_t>(K0)},
+                        {N0 * e}, {64, 64});
+  else
+    ok = ok && make_map(&tw0, W0, p.is_bf16, 2, {static_cast<uint64_t>(K0), static_cast<uint64_t>(N0)},
+                        {K0 * e}, {kChunkK, static_cast<uint32_t>(p.N0p)});
+  const int32_t Nout = mode == MODE_CHAIN ? N1 : N0;
+  if (mode == MODE_CHAIN) {
+    if (w_mn)
+      ok = ok && make_map(&tw1, W1, p.is_bf16, 2, {static_cast<uint64_t>(N1), static_cast<uint64_t>(N0)},
+                          {N1 * e}, {64, 64});
+    else
+      ok = ok && make_map(&tw1, W1, p.is_bf16, 2, {static_cast<uint64_t>(N0), static_cast<uint64_t>(N1)},
+                          {N0 * e}, {kChunkK, static_cast<uint32_t>(p.N1p)});
+  } else {
+    tw1 = tw0;
+  }
+  ok = ok && make_map(&to, D, p.is_bf16, 2, {static_cast<uint64_t>(Nout), static_cast<uint64_t>(M)},
+                      {Nout * e}, {64, kBlockM});
+  if (!ok) return B2B_ERR_CUDA;
+  Variant v;
+  if (mode == MODE_CHAIN) v = w_mn ? V_GEMM_CHAIN : V_CONV1X1_CHAIN;
+  else v = w_mn ? V_GEMM_SINGLE : V_CONV1X1_SINGLE;
+  return launch(v, d, ta, tw0, tw1, to, p, smem, stream);
+}
+
+// ------------------------------------------------------------------------------------
+// conv-shaped entry points (4-D implicit-GEMM A operand)
+// ------------------------------------------------------------------------------------
+b2b_status run_conv(int mode, int dt, int32_t N, int32_t H, int32_t W, int32_t C, const void* x,
+                    const void* W0, int32_t C0, int32_t R, int32_t S, int32_t pad, const void* b0,
+                    int e0, const void* W1, int32_t C1, const void* b1, int e1, void* y,
+                    void* stream, uint32_t kid) {
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  if (d == nullptr) return st;
+  const int32_t Ho = H + 2 * pad - R + 1, Wo = W + 2 * pad - S + 1;
+  ChainParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.K0 = C;
+  p.N0 = C0;
+  p.N1 = mode == MODE_CHAIN ? C1 : 0;
+  p.N0p = static_cast<int32_t>(round_up(static_cast<uint32_t>(C0), 16u));
+  p.N1p = mode == MODE_CHAIN ? static_cast<int32_t>(round_up(static_cast<uint32_t>(C1), 16u)) : 0;
+  p.kc_per_tap = ceil_div(C, kChunkK);
+  p.kchunks0 = R * S * p.kc_per_tap;
+  p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
+  p.R = R;
+  p.S = S;
+  p.pad = pad;
+  p.Ho = Ho;
+  p.Wo = Wo;
+  p.tiles_w = ceil_div(Wo, 16);
+  p.tiles_h = ceil_div(Ho, 8);
+  const int64_t tiles = static_cast<int64_t>(N) * p.tiles_w * p.tiles_h;
+  if (tiles > INT32_MAX) return B2B_ERR_UNSUPPORTED;
+  p.num_tiles = static_cast<int32_t>(tiles);
+  fill_common(p, dt, e0, e1, b0, b1, d, kid);
+  set_tmem(p, mode);
+  size_t smem = 0;
+  if (!plan_smem(p, mode, false, false, &smem)) return B2B_ERR_UNSUPPORTED;
+
+  const uint64_t e = 2;
+  CUtensorMap ta, tw0, tw1, to;
+  bool ok = make_map(&ta, x, p.is_bf16, 4,
+                     {static_cast<uint64_t>(C), static_cast<uint64_t>(W), static_cast<uint64_t>(H),
+                      static_cast<uint64_t>(N)},
+                     {C * e, static_cast<uint64_t>(W) * C * e, static_cast<uint64_t>(H) * W * C * e},
+                     {kChunkK, 16, 8, 1});
+  ok = ok && make_map(&tw0, W0, p.is_bf16, 3,
+                      {static_cast<uint64_t>(C), static_cast<uint64_t>(R) * S, static_cast<uint64_t>(C0)},
+                      {C * e, static_cast<uint64_t>(R) * S * C * e},
+                      {kChunkK, 1, static_cast<uint32_t>(p.N0p)});
+  if (mode == MODE_CHAIN)
+    ok = ok && make_map(&tw1, W1, p.is_bf16, 2, {static_cast<uint64_t>(C0), static_cast<uint64_t>(C1)},
+                        {C0 * e}, {kChunkK, static_cast<uint32_t>(p.N1p)});
+  else
+    tw1 = tw0;
+  if (mode == MODE_POOL) {
+    const int32_t Hp = H / 2, Wp = W / 2;
+    ok = ok && make_map(&to, y, p.is_bf16, 4,
+                        {static_cast<uint64_t>(C0), static_cast<uint64_t>(Wp), static_cast<uint64_t>(Hp),
+                         static_cast<uint64_t>(N)},
+                        {C0 * e, static_cast<uint64_t>(Wp) * C0 * e, static_cast<uint64_t>(Hp) * Wp * C0 * e},
+                        {64, 8, 4, 1});
+  } else {
+    const int32_t Cout = mode == MODE_CHAIN ? C1 : C0;
+    ok = ok && make_map(&to, y, p.is_bf16, 4,
+                        {static_cast<uint64_t>(Cout), static_cast<uint64_t>(Wo), static_cast<uint64_t>(Ho),
+                         static_cast<uint64_t>(N)},
+                        {Cout * e, static_cast<uint64_t>(Wo) * Cout * e, static_cast<uint64_t>(Ho) * Wo * Cout * e},
+                        {64, 16, 8, 1});
+  }
+  if (!ok) return B2B_ERR_CUDA;
+  const Variant v = mode == MODE_CHAIN ? V_CONV_CHAIN : mode == MODE_SINGLE ? V_CONV_SINGLE : V_CONV_POOL;
+  return launch(v, d, ta, tw0, tw1, to, p, smem, stream);
+}
+
+// Shared checks of a channel-like size: multiple of 8 (16 bytes), within [8, hi].
+b2b_status check_channels(int32_t c, int32_t hi) {
+  if (c < 8) return c <= 0 ? B2B_ERR_SHAPE : B2B_ERR_ALIGN;
+  if (c % 8 != 0) return B2B_ERR_ALIGN;
+  if (c > hi) return B2B_ERR_UNSUPPORTED;
+  return B2B_OK;
+}
+
+constexpr int32_t kMaxReduction = 1 << 16;   // K0 or C: keeps all index math in int32
+
+}  // namespace
+}  // namespace b2b
+
+using namespace b2b;
+
+extern "C" {
+
+b2b_status b2b_gemm(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1, const void* A,
+                    const void* W0, const void* b0, b2b_epilogue e0, const void* W1,
+                    const void* b1, b2b_epilogue e1, void* D, void* stream) {
+  if (!valid_dtype(dt) || !valid_epi(e0) || !valid_epi(e1)) return B2B_ERR_UNSUPPORTED;
+  if (M < 0 || K0 <= 0 || N0 <= 0 || N1 <= 0) return B2B_ERR_SHAPE;
+  b2b_status st;
+  if ((st = check_channels(K0, kMaxReduction)) != B2B_OK) return st;
+  if ((st = check_channels(N0, 256)) != B2B_OK) return st;
+  if ((st = check_channels(N1, 256)) != B2B_OK) return st;
+  if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
+  if (M == 0) return B2B_OK;
+  if (!A || !W0 || !W1 || !D) return B2B_ERR_NULL;
+  if (!aligned16(A) || !aligned16(W0) || !aligned16(W1) || !aligned16(D)) return B2B_ERR_ALIGN;
+  if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1))) return B2B_ERR_ALIGN;
+  return run_gemm(MODE_CHAIN, true, dt, M, K0, N0, N1, A, W0, b0, e0, W1, b1, e1, D, stream,
+                  KID_GEMM_CHAIN);
+}
+
+b2b_status gemm_bias_act(b2b_dtype dt, int64_t M, int32_t K, int32_t N, const void* A,
+                         const void* W, const void* b, b2b_epilogue e, void* D, void* stream) {
+  if (!valid_dtype(dt) || !valid_epi(e)) return B2B_ERR_UNSUPPORTED;
+  if (M < 0 || K <= 0 || N <= 0) return B2B_ERR_SHAPE;
+  b2b_status st;
+  if ((st = check_channels(K, kMaxReduction)) != B2B_OK) return st;
+  if ((st = check_channels(N, 256)) != B2B_OK) return st;
+  if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
+  if (M == 0) return B2B_OK;
+  if (!A || !W || !D) return B2B_ERR_NULL;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(D)) return B2B_ERR_ALIGN;
+  if (b && !aligned2(b)) return B2B_ERR_ALIGN;
+  return run_gemm(MODE_SINGLE, true, dt, M, K, N, 0, A, W, b, e, nullptr, nullptr, 0, D, stream,
+                  KID_GEMM_SINGLE);
+}
+
+static b2b_status check_conv_args(int32_t N, int32_t H, int32_t W, int32_t C, int32_t Co,
+                                  int32_t R, int32_t S, int32_t pad) {
+  if (N < 0 || H < 0 || W < 0) return B2B_ERR_SHAPE;
+  b2b_status st;
+  if ((st = check_channels(C, kMaxReduction)) != B2B_OK) return st;
+  if ((st = check_channels(Co, 256)) != B2B_OK) return st;
+  if (R < 1 || S < 1 || pad < 0) return B2B_ERR_SHAPE;
+  if (R > 7 || S > 7 || pad > 3) return B2B_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(R) * S * ((C + 63) / 64) > 4096) return B2B_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(N) * H * W > 0) {
+    if (H + 2 * pad - R + 1 < 1 || W + 2 * pad - S + 1 < 1) return B2B_ERR_SHAPE;
+  }
+  if (static_cast<int64_t>(N) * H * W * C > (int64_t{1} << 40)) return B2B_ERR_UNSUPPORTED;
+  return B2B_OK;
+}
+
+b2b_status b2b_conv_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C, const void* x,
+                         const void* W0, int32_t C0, int32_t R, int32_t S, int32_t pad,
+                         const void* b0, b2b_epilogue e0, const void* W1, int32_t C1,
+                         const void* b1, b2b_epilogue e1, void* y, void* stream) {
+  if (!valid_dtype(dt) || !valid_epi(e0) || !valid_epi(e1)) return B2B_ERR_UNSUPPORTED;
+  b2b_status st = check_conv_args(N, H, W, C, C0, R, S, pad);
+  if (st != B2B_OK) return st;
+  if ((st = check_channels(C1, 256)) != B2B_OK) return st;
+  if (static_cast<int64_t>(N) * H * W == 0) return B2B_OK;
+  if (!x || !W0 || !W1 || !y) return B2B_ERR_NULL;
+  if (!aligned16(x) || !aligned16(W0) || !aligned16(W1) || !aligned16(y)) return B2B_ERR_ALIGN;
+  if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1))) return B2B_ERR_ALIGN;
+  if (R == 1 && S == 1 && pad == 0) {
+    // A 1x1 conv is a GEMM over the N*H*W pixel rows (interview notes, "Conv
+    // optimisation", item 5): run the GEMM-shaped kernel with K-major filters.
+    const int64_t M = static_cast<int64_t>(N) * H * W;
+    if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
+    return run_gemm(MODE_CHAIN, false, dt, M, C, C0, C1, x, W0, b0, e0, W1, b1, e1, y, stream,
+                    KID_CONV1X1_CHAIN);
+  }
+  return run_conv(MODE_CHAIN, dt, N, H, W, C, x, W0, C0, R, S, pad, b0, e0, W1, C1, b1, e1, y,
+                  stream, KID_CONV_CHAIN);
+}
+
+b2b_status conv_bias_act_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                              const void* x, const void* Wt, int32_t Co, int32_t R, int32_t S,
+                              int32_t pad, const void* b, b2b_epilogue e, void* y, void* stream) {
+  if (!valid_dtype(dt) || !valid_epi(e)) return B2B_ERR_UNSUPPORTED;
+  b2b_status st = check_conv_args(N, H, W, C, Co, R, S, pad);
+  if (st != B2B_OK) return st;
+  if (static_cast<int64_t>(N) * H * W == 0) return B2B_OK;
+  if (!x || !Wt || !y) return B2B_ERR_NULL;
+  if (!aligned16(x) || !aligned16(Wt) || !aligned16(y)) return B2B_ERR_ALIGN;
+  if (b && !aligned2(b)) return B2B_ERR_ALIGN;
+  if (R == 1 && S == 1 && pad == 0) {
+    const int64_t M = static_cast<int64_t>(N) * H * W;
+    if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
+    return run_gemm(MODE_SINGLE, false, dt, M, C, Co, 0, x, Wt, b, e, nullptr, nullptr, 0, y,
+                    stream, KID_CONV1X1_SINGLE);
+  }
+  return run_conv(MODE_SINGLE, dt, N, H, W, C, x, Wt, Co, R, S, pad, b, e, nullptr, 0, nullptr, 0,
+                  y, stream, KID_CONV_SINGLE);
+}
+
+b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t Cin,
+                             const void* x, const void* Wt, const void* b, int32_t Cout, void* y,
+                             void* stream) {
+  if (!valid_dtype(dt)) return B2B_ERR_UNSUPPORTED;
+  if (N < 0 || H < 0 || W < 0) return B2B_ERR_SHAPE;
+  if (N > 0 && (H < 2 || W < 2)) return B2B_ERR_SHAPE;
+  b2b_status st = check_conv_args(N, H, W, Cin, Cout, 3, 3, 1);
+  if (st != B2B_OK) return st;
+  if (N == 0) return B2B_OK;
+  if (!x || !Wt || !y) return B2B_ERR_NULL;
+  if (!aligned16(x) || !aligned16(Wt) || !aligned16(y)) return B2B_ERR_ALIGN;
+  if (b && !aligned2(b)) return B2B_ERR_ALIGN;
+  return run_conv(MODE_POOL, dt, N, H, W, Cin, x, Wt, Cout, 3, 3, 1, b, B2B_EPI_RELU, nullptr, 0,
+                  nullptr, 0, y, stream, KID_CONV_POOL);
+}
+
+b2b_status maxpool2x2_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                           const void* x, void* y, void* stream) {
+  if (!valid_dtype(dt)) return B2B_ERR_UNSUPPORTED;
+  if (N < 0 || H < 0 || W < 0 || C <= 0) return B2B_ERR_SHAPE;
+  if (N > 0 && (H < 2 || W < 2)) return B2B_ERR_SHAPE;
+  if (C % 8 != 0) return B2B_ERR_ALIGN;
+  if (N == 0) return B2B_OK;
+  if (!x || !y) return B2B_ERR_NULL;
+  if (!aligned16(x) || !aligned16(y)) return B2B_ERR_ALIGN;
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  if (d == nullptr) return st;
+  if (launch_maxpool(dt == B2B_BF16, N, H, W, C, x, y, d->num_sms,
+                     static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
+const char* b2b_status_str(b2b_status s) {
+  switch (s) {
+    case B2B_OK: return "B2B_OK";
+    case B2B_ERR_NULL: return "B2B_ERR_NULL: a required pointer is NULL";
+    case B2B_ERR_SHAPE: return "B2B_ERR_SHAPE: invalid or inconsistent size";
+    case B2B_ERR_ALIGN: return "B2B_ERR_ALIGN: pointer not 16-byte aligned or size not a multiple of 8";
+    case B2B_ERR_UNSUPPORTED: return "B2B_ERR_UNSUPPORTED: outside the kernels' limits";
+    case B2B_ERR_CUDA: return "B2B_ERR_CUDA: a CUDA call failed";
+    case B2B_ERR_TIMEOUT: return "B2B_ERR_TIMEOUT: a kernel gave up waiting";
+    default: return "unknown b2b_status";
+  }
+}
+
+const char* b2b_version(void) { return "0.1.0"; }
+
+int32_t b2b_num_sms(void) {
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  return d ? d->num_sms : -1;
+}
+
+void b2b_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns); }
+
+b2b_status b2b_get_device_error(uint32_t info[4]) {
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  if (d == nullptr) return st;
+  uint32_t w[4] = {0, 0, 0, 0};
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(w, d->err, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  if (info) std::memcpy(info, w, sizeof(w));
+  if (w[0] == 0u) return B2B_OK;
+  const uint32_t zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(d->err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return w[0] == ERR_CODE_TIMEOUT ? B2B_ERR_TIMEOUT : B2B_ERR_CUDA;
+}
+
+b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream) {
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  if (d == nullptr) return st;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return B2B_ERR_SHAPE;
+  if (launch_probe_timeout(limit_ns, d->err, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
+}  // extern "C"

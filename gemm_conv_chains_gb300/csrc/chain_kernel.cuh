@@ -1,0 +1,622 @@
+// chain_kernel.cuh -- the persistent fused-chain kernel for sm_103a.
+//
+// One CTA per SM loops over 128-row output tiles (BOLT notes, "Persistent kernel
+// (GEMM/Conv) fusion").  The CTA owns every N0 and N1 column of its rows ("Threadblock
+// residence": ThreadBlock_N = GEMM_N), so GEMM1 never needs another block's data:
+//
+//   warp 0      TMA producer: A (or one conv tap of x) and weight K-chunks -> smem ring
+//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma (GEMM0 into TMEM, GEMM1 from P)
+//   warps 2..5  epilogue: TMEM -> registers -> bias + activation -> fp16/bf16 ->
+//               (chain) P tile in shared memory, the operand of GEMM1
+//               ("Shared-memory-resident fusion": the accumulator tile is staged in
+//               shared memory and read back by the second GEMM, Figure 7)
+//               (last stage) output tile in shared memory -> TMA store to global
+//
+// Modes
+//   MODE_CHAIN   GEMM0 -> epi0 -> P -> GEMM1 -> epi1 -> global
+//   MODE_SINGLE  GEMM0 -> epi0 -> global             (one operator of the unfused path)
+//   MODE_POOL    conv GEMM -> 2x2 max -> bias -> ReLU -> global (Welder notes, Figure 5:
+//                the (2,2,F) reuse tile is reduced in registers and never leaves the chip)
+//
+// A operand
+//   2-D: rows of A[M, K0] in 128 x 64 boxes.
+//   4-D (implicit GEMM, interview notes "Conv optimisation", item 2): for tap (r, s) and
+//   channel block cb, one box x[n, ho0+r-pad .. +8, wo0+s-pad .. +16, cb*64 .. +64] of
+//   an 8 x 16 output-pixel tile; coordinates outside the image read as zero, which is the
+//   conv's zero padding.  The box lands in shared memory as 128 rows x 128 B, exactly the
+//   K-major 128B-swizzled layout tcgen05 reads, so no im2col buffer exists anywhere.
+//
+// Every wait is bounded (see ptx.cuh); on a timeout all roles leave their loops, the MMA
+// issuer drains its MMAs, the producer drains its copies, and TMEM is freed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernel_params.h"
+#include "ptx.cuh"
+
+namespace b2b {
+
+// Barrier slots (8 bytes each) at p.off_bar.
+enum : uint32_t {
+  BAR_FULL0 = 0,
+  BAR_EMPTY0 = kMaxStages,
+  BAR_WFULL = 2 * kMaxStages,
+  BAR_ACC_FULL0 = BAR_WFULL + 1,
+  BAR_ACC_EMPTY0 = BAR_ACC_FULL0 + 2,
+  BAR_P_FULL = BAR_ACC_EMPTY0 + 2,
+  BAR_D1_FULL = BAR_P_FULL + 1,
+  BAR_MMA_DONE = BAR_D1_FULL + 1,
+  BAR_COUNT = BAR_MMA_DONE + 1,
+};
+constexpr uint32_t kBarRegionBytes = 512;   // barriers, then TMEM slot and abort flag
+
+struct TileCoord {
+  int32_t m0;              // 2-D: first row
+  int32_t n, ho0, wo0;     // 4-D: image, first output row, first output column
+};
+
+template <bool A4D>
+__device__ __forceinline__ TileCoord tile_coord(const ChainParams& p, int32_t t) {
+  TileCoord c{0, 0, 0, 0};
+  if constexpr (A4D) {
+    const int32_t per_img = p.tiles_h * p.tiles_w;
+    c.n = t / per_img;
+    const int32_t rem = t - c.n * per_img;
+    const int32_t th = rem / p.tiles_w;
+    c.ho0 = th * 8;
+    c.wo0 = (rem - th * p.tiles_w) * 16;
+  } else {
+    c.m0 = t * kBlockM;
+  }
+  return c;
+}
+
+// Number of 16-wide MMA K steps in GEMM0 chunk kc (a partial last chunk is zero-filled
+// by TMA up to the next multiple of 16).
+__device__ __forceinline__ int ksteps0(const ChainParams& p, int kc, bool a4d) {
+  const int cb = a4d ? (kc % p.kc_per_tap) : kc;
+  const int rem = p.K0 - cb * kChunkK;
+  const int s = (rem + 15) >> 4;
+  return s < 4 ? s : 4;
+}
+
+// ------------------------------------------------------------------------------------
+// producer (one thread)
+// ------------------------------------------------------------------------------------
+template <int MODE, bool A4D, bool W0MN, bool W1MN>
+__device__ __forceinline__ void load_a_chunk(const ChainParams& p, const CUtensorMap* tmA,
+                                             uint32_t dst, const TileCoord& tc, int kc,
+                                             uint32_t bar, uint64_t pol) {
+  if constexpr (A4D) {
+    const int t = kc / p.kc_per_tap;
+    const int cb = kc - t * p.kc_per_tap;
+    const int r = t / p.S;
+    const int s = t - r * p.S;
+    tma_load_4d(dst, tmA, bar, cb * kChunkK, tc.wo0 + s - p.pad, tc.ho0 + r - p.pad, tc.n, pol);
+  } else {
+    tma_load_2d(dst, tmA, bar, kc * kChunkK, tc.m0, pol);
+  }
+}
+
+template <bool A4D, bool W0MN>
+__device__ __forceinline__ void load_w0_chunk(const ChainParams& p, const CUtensorMap* tmW0,
+                                              uint32_t dst, int kc, uint32_t bar, uint64_t pol) {
+  if constexpr (W0MN) {
+    // W0[K0][N0] row-major: one 64 (N) x 64 (K) box per 64-wide N block, 8 KiB apart.
+    const int nblk = (p.N0p + 63) >> 6;
+    for (int nb = 0; nb < nblk; ++nb)
+      tma_load_2d(dst + nb * 8192u, tmW0, bar, nb * 64, kc * kChunkK, pol);
+  } else if constexpr (A4D) {
+    // W0[C0][R*S][C]: the 64-channel block cb of tap t for all C0 rows.
+    const int t = kc / p.kc_per_tap;
+    const int cb = kc - t * p.kc_per_tap;
+    tma_load_3d(dst, tmW0, bar, cb * kChunkK, t, 0, pol);
+  } else {
+    tma_load_2d(dst, tmW0, bar, kc * kChunkK, 0, pol);
+  }
+}
+
+template <bool W1MN>
+__device__ __forceinline__ void load_w1_chunk(const ChainParams& p, const CUtensorMap* tmW1,
+                                              uint32_t dst, int kc1, uint32_t bar, uint64_t pol) {
+  if constexpr (W1MN) {
+    const int nblk = (p.N1p + 63) >> 6;
+    for (int nb = 0; nb < nblk; ++nb)
+      tma_load_2d(dst + nb * 8192u, tmW1, bar, nb * 64, kc1 * kChunkK, pol);
+  } else {
+    tma_load_2d(dst, tmW1, bar, kc1 * kChunkK, 0, pol);
+  }
+}
+
+template <int MODE, bool A4D, bool W0MN, bool W1MN>
+__device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
+                              const CUtensorMap* tmW0, const CUtensorMap* tmW1, uint32_t base,
+                              uint32_t bars, volatile uint32_t* abort_flag) {
+  const uint64_t pol_stream = l2_policy_evict_first();
+  const uint64_t pol_keep = l2_policy_evict_last();
+  uint32_t issued = 0, issued_parity = 0;   // per-stage: a fill in flight, and its parity
+  bool w_issued = false;
+  bool ok = true;
+
+  if (p.resident) {
+    const uint32_t wbar = bars + 8u * BAR_WFULL;
+    uint32_t total = p.kchunks0 * p.w0_chunk_bytes;
+    if (MODE == MODE_CHAIN) total += p.kchunks1 * p.w1_chunk_bytes;
+    mbar_arrive_expect_tx(wbar, total);
+    for (int kc = 0; kc < p.kchunks0; ++kc)
+      load_w0_chunk<A4D, W0MN>(p, tmW0, base + p.off_w0 + kc * p.w0_chunk_bytes, kc, wbar,
+                               pol_keep);
+    if (MODE == MODE_CHAIN)
+      for (int kc1 = 0; kc1 < p.kchunks1; ++kc1)
+        load_w1_chunk<W1MN>(p, tmW1, base + p.off_w1 + kc1 * p.w1_chunk_bytes, kc1, wbar,
+                            pol_keep);
+    w_issued = true;
+  }
+
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+    const TileCoord tc = tile_coord<A4D>(p, t);
+    for (int kc = 0; kc < p.kchunks0; ++kc) {
+      if (!mbar_wait(bars + 8u * (BAR_EMPTY0 + stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
+                     p.err, p.kernel_id, SITE_PRODUCER_EMPTY, t)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
+      const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
+      mbar_arrive_expect_tx(fb, kABytes + (p.resident ? 0u : p.w0_chunk_bytes));
+      load_a_chunk<MODE, A4D, W0MN, W1MN>(p, tmA, sbase, tc, kc, fb, pol_stream);
+      if (!p.resident) load_w0_chunk<A4D, W0MN>(p, tmW0, sbase + kABytes, kc, fb, pol_keep);
+      issued |= 1u << stage;
+      issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok) break;
+    if (MODE == MODE_CHAIN && !p.resident) {
+      for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
+        if (!mbar_wait(bars + 8u * (BAR_EMPTY0 + stage), phase ^ 1u, p.wait_limit_ns,
+                       abort_flag, p.err, p.kernel_id, SITE_PRODUCER_EMPTY, t)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
+        mbar_arrive_expect_tx(fb, p.w1_chunk_bytes);
+        load_w1_chunk<W1MN>(p, tmW1, base + p.off_ring + stage * p.stage_bytes, kc1, fb,
+                            pol_keep);
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+      }
+    }
+  }
+
+  if (!ok) {
+    // Gave up: let the copies this thread started land before the CTA can exit.
+    const uint64_t drain_ns = 100000000ull;
+    for (uint32_t s = 0; s < p.num_stages; ++s)
+      if (issued & (1u << s))
+        (void)mbar_wait(bars + 8u * (BAR_FULL0 + s), (issued_parity >> s) & 1u, drain_ns,
+                        nullptr, p.err, p.kernel_id, SITE_PRODUCER_DRAIN, 0);
+    if (w_issued)
+      (void)mbar_wait(bars + 8u * BAR_WFULL, 0u, drain_ns, nullptr, p.err, p.kernel_id,
+                      SITE_PRODUCER_DRAIN, 0);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// MMA issuer (one thread)
+// ------------------------------------------------------------------------------------
+template <int MODE, bool A4D, bool W0MN, bool W1MN>
+__device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
+                         volatile uint32_t* abort_flag) {
+  const uint32_t idesc0 = idesc_f16_f32(p.is_bf16, W0MN ? 1u : 0u, kBlockM, p.N0p);
+  const uint32_t idesc1 = idesc_f16_f32(p.is_bf16, W1MN ? 1u : 0u, kBlockM, p.N1p);
+  bool ok = true;
+  if (p.resident)
+    ok = mbar_wait(bars + 8u * BAR_WFULL, 0u, p.wait_limit_ns, abort_flag, p.err, p.kernel_id,
+                   SITE_MMA_WEIGHTS, 0);
+
+  int stage = 0;
+  uint32_t phase = 0;
+  int it = 0;
+  for (int32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+    uint32_t d0 = tmem_base;
+    uint32_t acc_full = bars + 8u * BAR_ACC_FULL0;
+    if (MODE != MODE_CHAIN) {
+      // Two accumulator buffers: GEMM(i+1) runs while the epilogue drains buffer i.
+      const uint32_t as = it & 1;
+      if (!mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + as), ((it >> 1) & 1) ^ 1u, p.wait_limit_ns,
+                     abort_flag, p.err, p.kernel_id, SITE_MMA_ACC_EMPTY, t)) {
+        ok = false;
+        break;
+      }
+      d0 = tmem_base + as * p.acc_stride;
+      acc_full = bars + 8u * (BAR_ACC_FULL0 + as);
+    }
+    tc_fence_after_sync();
+
+    // GEMM0: D0 = A . W0 over all K chunks.
+    for (int kc = 0; kc < p.kchunks0; ++kc) {
+      if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag,
+                     p.err, p.kernel_id, SITE_MMA_FULL, t)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
+      const uint32_t wbase =
+          p.resident ? base + p.off_w0 + kc * p.w0_chunk_bytes : sbase + kABytes;
+      const int nks = ksteps0(p, kc, A4D);
+      for (int ks = 0; ks < nks; ++ks) {
+        const uint64_t adesc = sdesc_sw128(sbase + ks * 32u, 16u, 1024u);
+        const uint64_t bdesc = W0MN ? sdesc_sw128(wbase + ks * 2048u, 8192u, 1024u)
+                                    : sdesc_sw128(wbase + ks * 32u, 16u, 1024u);
+        mma_f16_ss(d0, adesc, bdesc, idesc0, (kc | ks) != 0 ? 1u : 0u);
+      }
+      mma_commit(bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
+      if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok) break;
+    mma_commit(acc_full);
+
+    if (MODE == MODE_CHAIN) {
+      // GEMM1: D1 = P . W1, P being the epilogue's fp16/bf16 tile in shared memory.
+      if (!mbar_wait(bars + 8u * BAR_P_FULL, it & 1, p.wait_limit_ns, abort_flag, p.err, p.kernel_id,
+                     SITE_MMA_P_FULL, t)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t d1 = tmem_base + p.acc_stride;
+      for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
+        uint32_t w1base;
+        if (p.resident) {
+          w1base = base + p.off_w1 + kc1 * p.w1_chunk_bytes;
+        } else {
+          if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag,
+                         p.err, p.kernel_id, SITE_MMA_FULL, t)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          w1base = base + p.off_ring + stage * p.stage_bytes;
+        }
+        const uint32_t pbase = base + p.off_p + kc1 * kPChunkBytes;
+        const int rem = p.N0p - kc1 * kChunkK;
+        const int nks = rem >= 64 ? 4 : (rem >> 4);
+        for (int ks = 0; ks < nks; ++ks) {
+          const uint64_t adesc = sdesc_sw128(pbase + ks * 32u, 16u, 1024u);
+          const uint64_t bdesc = W1MN ? sdesc_sw128(w1base + ks * 2048u, 8192u, 1024u)
+                                      : sdesc_sw128(w1base + ks * 32u, 16u, 1024u);
+          mma_f16_ss(d1, adesc, bdesc, idesc1, (kc1 | ks) != 0 ? 1u : 0u);
+        }
+        if (!p.resident) {
+          mma_commit(bars + 8u * (BAR_EMPTY0 + stage));
+          if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) break;
+      mma_commit(bars + 8u * BAR_D1_FULL);
+    }
+  }
+  // Whatever happened, no MMA may still be running when TMEM is released.
+  mma_commit(bars + 8u * BAR_MMA_DONE);
+  (void)mbar_wait(bars + 8u * BAR_MMA_DONE, 0u, p.wait_limit_ns, nullptr, p.err, p.kernel_id,
+                  SITE_MMA_DRAIN, 0);
+}
+
+// ------------------------------------------------------------------------------------
+// epilogue (4 warps, one TMEM lane = one tile row per thread)
+// ------------------------------------------------------------------------------------
+template <int ACT>
+__device__ __forceinline__ float act_fn(float x) {
+  if constexpr (ACT == 1) return fmaxf(x, 0.0f);
+  if constexpr (ACT == 2) return x * fminf(fmaxf(x + 3.0f, 0.0f), 6.0f) * (1.0f / 6.0f);
+  return x;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// Stores 16 consecutive columns [c0, c0+16) of row `row` into a K-major, 128B-swizzled
+// tile: 64-column chunks of `chunk_bytes`, 128 B per row, and the 16-byte unit j of row r
+// stored at unit j ^ (r & 7) -- the layout TMA writes with SWIZZLE_128B and tcgen05
+// reads through a SWIZZLE_128B descriptor.
+__device__ __forceinline__ void st_row16_sw128(uint32_t tile, int row, int c0,
+                                               uint32_t chunk_bytes, const uint32_t (&v)[8]) {
+  const uint32_t chunk = static_cast<uint32_t>(c0) >> 6;
+  const uint32_t j = (static_cast<uint32_t>(c0) & 63u) >> 3;
+  const uint32_t rb = tile + chunk * chunk_bytes + static_cast<uint32_t>(row) * 128u;
+  const uint32_t x = static_cast<uint32_t>(row) & 7u;
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + ((j ^ x) << 4)), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3])
+               : "memory");
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + (((j + 1) ^ x) << 4)),
+               "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+template <bool BF16, int ACT>
+__device__ __forceinline__ void convert16(const uint32_t (&r)[16], const float* bias, int c,
+                                          uint32_t (&out)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float lo = act_fn<ACT>(__uint_as_float(r[2 * j]) + bias[c + 2 * j]);
+    const float hi = act_fn<ACT>(__uint_as_float(r[2 * j + 1]) + bias[c + 2 * j + 1]);
+    out[j] = pack2<BF16>(lo, hi);
+  }
+}
+
+// TMEM columns [col0, col0 + ncols) of this thread's row -> bias -> act -> dtype -> smem.
+template <bool BF16, int ACT>
+__device__ __forceinline__ void drain_to_smem(uint32_t tm_lane, uint32_t col0, int ncols,
+                                              const float* bias, uint32_t tile, int row,
+                                              uint32_t chunk_bytes) {
+  for (int c = 0; c < ncols; c += 32) {
+    uint32_t r0[16], r1[16];
+    uint32_t v[8];
+    const bool two = c + 16 < ncols;
+    tmem_ld16(tm_lane + col0 + c, r0);
+    if (two) tmem_ld16(tm_lane + col0 + c + 16, r1);
+    tmem_wait_ld(r0, r1);
+    convert16<BF16, ACT>(r0, bias, c, v);
+    st_row16_sw128(tile, row, c, chunk_bytes, v);
+    if (two) {
+      convert16<BF16, ACT>(r1, bias, c + 16, v);
+      st_row16_sw128(tile, row, c + 16, chunk_bytes, v);
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void drain_to_smem_act(int act, uint32_t tm_lane, uint32_t col0,
+                                                  int ncols, const float* bias, uint32_t tile,
+                                                  int row, uint32_t chunk_bytes) {
+  if (act == 1)
+    drain_to_smem<BF16, 1>(tm_lane, col0, ncols, bias, tile, row, chunk_bytes);
+  else if (act == 2)
+    drain_to_smem<BF16, 2>(tm_lane, col0, ncols, bias, tile, row, chunk_bytes);
+  else
+    drain_to_smem<BF16, 0>(tm_lane, col0, ncols, bias, tile, row, chunk_bytes);
+}
+
+// Pool epilogue.  Tile row = 16 * h + w over an 8 x 16 conv-output tile, so warp q holds
+// conv rows 2q and 2q+1: the horizontal partner of a pixel sits in lane ^ 1 and the
+// vertical one in lane ^ 16.  The max of the four fp32 sums is taken first; adding the
+// bias, ReLU and rounding are monotone, so this equals pooling the rounded ReLU output.
+template <bool BF16>
+__device__ __forceinline__ void drain_pool(uint32_t tm_lane, uint32_t col0, int ncols,
+                                           const float* bias, uint32_t tile, int q, int lane) {
+  const bool owner = (lane & 17) == 0;
+  const int prow = q * 8 + (lane >> 1);
+  for (int c = 0; c < ncols; c += 16) {
+    uint32_t r[16];
+    tmem_ld16(tm_lane + col0 + c, r);
+    tmem_wait_ld(r);
+    float m[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float v = __uint_as_float(r[j]);
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      m[j] = v;
+    }
+    if (owner) {
+      uint32_t v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = pack2<BF16>(fmaxf(m[2 * j] + bias[c + 2 * j], 0.0f),
+                           fmaxf(m[2 * j + 1] + bias[c + 2 * j + 1], 0.0f));
+      st_row16_sw128(tile, prow, c, kPoolChunkBytes, v);
+    }
+  }
+}
+
+template <bool A4D>
+__device__ __forceinline__ void store_tile(const CUtensorMap* tmOut, uint32_t tile, int nchunks,
+                                           const TileCoord& tc) {
+  for (int nc = 0; nc < nchunks; ++nc) {
+    if constexpr (A4D)
+      tma_store_4d(tmOut, tile + nc * kPChunkBytes, nc * 64, tc.wo0, tc.ho0, tc.n);
+    else
+      tma_store_2d(tmOut, tile + nc * kPChunkBytes, nc * 64, tc.m0);
+  }
+}
+
+// Warp-uniform bounded wait: every lane acquires the barrier itself, and the warp agrees
+// on the outcome, so warp-collective tcgen05 loads and the named barriers below are
+// always executed by whole warps.
+__device__ __forceinline__ bool warp_wait(bool alive, uint32_t bar, uint32_t parity,
+                                          const ChainParams& p, volatile uint32_t* abort_flag,
+                                          uint32_t site, int32_t t) {
+  bool ok = alive && mbar_wait(bar, parity, p.wait_limit_ns, abort_flag, p.err, p.kernel_id, site, t);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int MODE, bool A4D, bool BF16>
+__device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, uint32_t base,
+                              uint32_t bars, uint32_t tmem_base, const float* bias_s,
+                              volatile uint32_t* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+  const int row = q * 32 + lane;
+  const uint32_t tm_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+  const bool elected = threadIdx.x == 64;
+  const uint32_t p_tile = base + p.off_p;
+  const uint32_t out_tile = base + p.off_out;
+  bool alive = true;
+  int it = 0;
+
+  for (int32_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+    const TileCoord tc = tile_coord<A4D>(p, t);
+    if (MODE == MODE_CHAIN) {
+      alive = warp_wait(alive, bars + 8u * BAR_ACC_FULL0, it & 1, p, abort_flag,
+                        SITE_EPI_ACC_FULL, t);
+      tc_fence_after_sync();
+      if (p.out_alias_p) {   // P doubles as the previous tile's output staging
+        if (elected) bulk_wait_read_all();
+        named_bar_sync(1, kNumEpiThreads);
+      }
+      if (alive)
+        drain_to_smem_act<BF16>(p.act0, tm_lane, 0, p.N0p, bias_s, p_tile, row, kPChunkBytes);
+      tc_fence_before_sync();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8u * BAR_P_FULL);
+
+      alive = warp_wait(alive, bars + 8u * BAR_D1_FULL, it & 1, p, abort_flag,
+                        SITE_EPI_D1_FULL, t);
+      tc_fence_after_sync();
+      if (!p.out_alias_p) {
+        if (elected) bulk_wait_read_all();
+        named_bar_sync(1, kNumEpiThreads);
+      }
+      if (alive)
+        drain_to_smem_act<BF16>(p.act1, tm_lane, p.acc_stride, p.N1p, bias_s + p.N0p, out_tile, row,
+                                kPChunkBytes);
+      tc_fence_before_sync();
+      fence_proxy_async_smem();
+      named_bar_sync(1, kNumEpiThreads);
+      if (elected && !*abort_flag) {
+        store_tile<A4D>(tmOut, out_tile, (p.N1p + 63) >> 6, tc);
+        bulk_commit_group();
+      }
+    } else {
+      const uint32_t as = it & 1;
+      alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + as), (it >> 1) & 1, p, abort_flag,
+                        SITE_EPI_ACC_FULL, t);
+      tc_fence_after_sync();
+      if (elected) bulk_wait_read_all();   // staging free again
+      named_bar_sync(1, kNumEpiThreads);
+      if (alive) {
+        if (MODE == MODE_POOL)
+          drain_pool<BF16>(tm_lane, as * p.acc_stride, p.N0p, bias_s, out_tile, q, lane);
+        else
+          drain_to_smem_act<BF16>(p.act0, tm_lane, as * p.acc_stride, p.N0p, bias_s, out_tile, row,
+                                  kPChunkBytes);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + as));
+      fence_proxy_async_smem();
+      named_bar_sync(1, kNumEpiThreads);
+      if (elected && !*abort_flag) {
+        if (MODE == MODE_POOL) {
+          const int nch = (p.N0p + 63) >> 6;
+          for (int nc = 0; nc < nch; ++nc)
+            tma_store_4d(tmOut, out_tile + nc * kPoolChunkBytes, nc * 64, tc.wo0 >> 1,
+                         tc.ho0 >> 1, tc.n);
+        } else {
+          store_tile<A4D>(tmOut, out_tile, (p.N0p + 63) >> 6, tc);
+        }
+        bulk_commit_group();
+      }
+    }
+  }
+  if (elected) bulk_wait_all();
+}
+
+// ------------------------------------------------------------------------------------
+// the kernel
+// ------------------------------------------------------------------------------------
+template <int MODE, bool A4D, bool W0MN, bool W1MN>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW0,
+                 const __grid_constant__ CUtensorMap tmW1,
+                 const __grid_constant__ CUtensorMap tmOut, const ChainParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bars = base + p.off_bar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + p.off_bar + 8u * BAR_COUNT);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+  float* bias_s = reinterpret_cast<float*>(base_ptr + p.off_bias);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < p.num_stages; ++s) {
+      mbar_init(bars + 8u * (BAR_FULL0 + s), 1);
+      mbar_init(bars + 8u * (BAR_EMPTY0 + s), 1);
+    }
+    mbar_init(bars + 8u * BAR_WFULL, 1);
+    for (uint32_t a = 0; a < 2; ++a) {
+      mbar_init(bars + 8u * (BAR_ACC_FULL0 + a), 1);
+      mbar_init(bars + 8u * (BAR_ACC_EMPTY0 + a), kNumEpiThreads / 32);
+    }
+    mbar_init(bars + 8u * BAR_P_FULL, kNumEpiThreads / 32);
+    mbar_init(bars + 8u * BAR_D1_FULL, 1);
+    mbar_init(bars + 8u * BAR_MMA_DONE, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmW0);
+    if (MODE == MODE_CHAIN) tma_prefetch_desc(&tmW1);
+    tma_prefetch_desc(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp >= 2) {
+    for (int i = threadIdx.x - 64; i < p.N0p + p.N1p; i += kNumEpiThreads) {
+      float v = 0.0f;
+      const uint16_t* src = nullptr;
+      int j = i;
+      if (i < p.N0p) {
+        if (i < p.N0) src = p.b0;
+      } else {
+        j = i - p.N0p;
+        if (j < p.N1) src = p.b1;
+      }
+      if (src != nullptr) {
+        const uint16_t bits = src[j];
+        v = p.is_bf16 ? __uint_as_float(static_cast<uint32_t>(bits) << 16)
+                      : __half2float(__ushort_as_half(bits));
+      }
+      bias_s[i] = v;
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) producer_role<MODE, A4D, W0MN, W1MN>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<MODE, A4D, W0MN, W1MN>(p, base, bars, tmem_base, abort_flag);
+    __syncwarp();
+  } else {
+    if (p.is_bf16)
+      epilogue_role<MODE, A4D, true>(p, &tmOut, base, bars, tmem_base, bias_s, abort_flag);
+    else
+      epilogue_role<MODE, A4D, false>(p, &tmOut, base, bars, tmem_base, bias_s, abort_flag);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace b2b

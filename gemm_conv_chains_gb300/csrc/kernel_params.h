@@ -1,0 +1,81 @@
+// kernel_params.h -- launch parameters shared by the host planner and the chain kernel.
+#pragma once
+
+#include <cstdint>
+
+namespace b2b {
+
+// What one launch of the chain kernel computes.
+enum ChainMode : int {
+  MODE_CHAIN = 0,   // GEMM0 -> epilogue0 -> P (smem) -> GEMM1 -> epilogue1 -> global
+  MODE_SINGLE = 1,  // GEMM0 -> epilogue0 -> global (one operator of the unfused path)
+  MODE_POOL = 2,    // GEMM0 (conv) -> 2x2 max -> bias -> ReLU -> global (pooled)
+};
+
+// Kernel ids recorded in the device error word.
+enum KernelId : uint32_t {
+  KID_GEMM_CHAIN = 1,
+  KID_CONV1X1_CHAIN = 2,
+  KID_CONV_CHAIN = 3,
+  KID_GEMM_SINGLE = 4,
+  KID_CONV1X1_SINGLE = 5,
+  KID_CONV_SINGLE = 6,
+  KID_CONV_POOL = 7,
+  KID_PROBE = 15,
+};
+
+// Wait sites recorded in the device error word.
+enum WaitSite : uint32_t {
+  SITE_PRODUCER_EMPTY = 1,
+  SITE_MMA_WEIGHTS = 2,
+  SITE_MMA_FULL = 3,
+  SITE_MMA_ACC_EMPTY = 4,
+  SITE_MMA_P_FULL = 5,
+  SITE_MMA_DRAIN = 6,
+  SITE_EPI_ACC_FULL = 7,
+  SITE_EPI_D1_FULL = 8,
+  SITE_PRODUCER_DRAIN = 9,
+  SITE_PROBE = 10,
+};
+
+constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M
+constexpr int kChunkK = 64;           // K elements per staged chunk (128 B rows, SW128)
+constexpr int kNumThreads = 192;      // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kNumEpiThreads = 128;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kABytes = kBlockM * kChunkK * 2;   // 16 KiB A chunk
+constexpr uint32_t kPChunkBytes = kBlockM * 128;      // 128 rows x 64 cols x 2 B
+constexpr uint32_t kPoolChunkBytes = 32 * 128;        // 4h x 8w pooled pixels x 64 ch
+
+struct ChainParams {
+  // --- problem -------------------------------------------------------------------
+  int32_t M;            // rows (2D A) -- unused for conv tiles
+  int32_t K0;           // GEMM0 reduction length (2D A) or input channels C (4D A)
+  int32_t N0, N1;       // true output widths of GEMM0 / GEMM1
+  int32_t N0p, N1p;     // padded to multiples of 16 (tcgen05 N granularity for M = 128)
+  int32_t kchunks0;     // 64-wide K chunks of GEMM0 (4D: taps * kc_per_tap)
+  int32_t kc_per_tap;   // 4D: ceil(C / 64)
+  int32_t kchunks1;     // 64-wide K chunks of GEMM1 (= ceil(N0p / 64))
+  int32_t R, S, pad;    // 4D filter
+  int32_t Ho, Wo;       // 4D output spatial size (before pooling)
+  int32_t tiles_w, tiles_h;  // 4D tiling: 16 output columns x 8 output rows per tile
+  int32_t num_tiles;
+  int32_t is_bf16;
+  int32_t act0, act1;
+  const uint16_t* b0;   // may be null
+  const uint16_t* b1;   // may be null
+  // --- shared-memory plan (byte offsets from the 1024-aligned dynamic base) -----------
+  uint32_t off_ring, stage_bytes, num_stages;
+  uint32_t w0_chunk_bytes, w1_chunk_bytes;
+  uint32_t off_w0, off_w1;      // resident weights (resident != 0)
+  uint32_t off_p, off_out, off_bias, off_bar;
+  int32_t resident;             // 1: W0/W1 loaded once per CTA; 0: streamed per tile
+  int32_t out_alias_p;          // 1: output staging shares the P buffer
+  uint32_t tmem_cols;
+  uint32_t acc_stride;          // TMEM column of D1 (chain) / of accumulator buffer 1
+  uint64_t wait_limit_ns;
+  uint32_t kernel_id;
+  uint32_t* err;                // device error word {code, kernel, site, tile}
+};
+
+}  // namespace b2b

@@ -1,0 +1,114 @@
+// kernels_misc.cu -- the plain max-pool operator of the unfused path, the timeout probe,
+// and the variant dispatch over the two chain-kernel units.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace b2b {
+
+const void* variant_func_a2d(Variant v);
+const void* variant_func_a4d(Variant v);
+cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
+                               const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
+                               int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
+                               const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
+                               int grid, size_t smem, cudaStream_t s);
+
+static bool is_a4d(Variant v) {
+  return v == V_CONV_CHAIN || v == V_CONV_SINGLE || v == V_CONV_POOL;
+}
+
+const void* variant_func(Variant v) {
+  return is_a4d(v) ? variant_func_a4d(v) : variant_func_a2d(v);
+}
+
+cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
+                           const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
+                           int grid, size_t smem, cudaStream_t stream) {
+  return is_a4d(v) ? launch_variant_a4d(v, a, w0, w1, out, p, grid, smem, stream)
+                   : launch_variant_a2d(v, a, w0, w1, out, p, grid, smem, stream);
+}
+
+// ------------------------------------------------------------------------------------
+// max-pool 2x2 / stride 2, floor mode, NHWC; one thread per 8-channel (16-byte) vector.
+// ------------------------------------------------------------------------------------
+template <bool BF16>
+__device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                               *reinterpret_cast<__nv_bfloat162*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+  } else {
+    __half2 r = __hmax2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint4 max4(const uint4& a, const uint4& b) {
+  return make_uint4(max2<BF16>(a.x, b.x), max2<BF16>(a.y, b.y), max2<BF16>(a.z, b.z),
+                    max2<BF16>(a.w, b.w));
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) maxpool2x2_kernel(const uint4* __restrict__ x,
+                                                         uint4* __restrict__ y, int H, int W,
+                                                         int Hp, int Wp, int C8, int64_t total) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const int c = static_cast<int>(idx % C8);
+    int64_t r = idx / C8;
+    const int j = static_cast<int>(r % Wp);
+    r /= Wp;
+    const int i = static_cast<int>(r % Hp);
+    const int64_t n = r / Hp;
+    const int64_t row0 = ((n * H + 2 * i) * W + 2 * j) * C8 + c;
+    const int64_t row1 = row0 + static_cast<int64_t>(W) * C8;
+    const uint4 a = __ldg(x + row0), b = __ldg(x + row0 + C8);
+    const uint4 d = __ldg(x + row1), e = __ldg(x + row1 + C8);
+    y[idx] = max4<BF16>(max4<BF16>(a, b), max4<BF16>(d, e));
+  }
+}
+
+cudaError_t launch_maxpool(int is_bf16, int N, int H, int W, int C, const void* x, void* y,
+                           int num_sms, cudaStream_t stream) {
+  const int Hp = H / 2, Wp = W / 2, C8 = C / 8;
+  const int64_t total = static_cast<int64_t>(N) * Hp * Wp * C8;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (is_bf16)
+    maxpool2x2_kernel<true><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const uint4*>(x), static_cast<uint4*>(y), H, W, Hp, Wp, C8, total);
+  else
+    maxpool2x2_kernel<false><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const uint4*>(x), static_cast<uint4*>(y), H, W, Hp, Wp, C8, total);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------
+// timeout probe: a barrier that expects one arrival which never comes
+// ------------------------------------------------------------------------------------
+__global__ void probe_timeout_kernel(uint64_t limit_ns, uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    (void)mbar_wait(b, 0u, limit_ns, nullptr, err, KID_PROBE, SITE_PROBE, 0);
+}
+
+cudaError_t launch_probe_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t stream) {
+  probe_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace b2b

@@ -1,0 +1,40 @@
+// launch.h -- internal interface between the host API (api.cu) and the kernel units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernel_params.h"
+
+namespace b2b {
+
+// The compiled instantiations of the chain kernel.
+//   GEMM_*     2-D A operand, weights W[K][N] row-major (MN-major B operand)
+//   CONV1X1_*  2-D A operand (NHWC pixels as rows), weights W[Cout][Cin] (K-major)
+//   CONV_*     4-D A operand (implicit GEMM per filter tap), weights W[Cout][R][S][Cin]
+enum Variant : int {
+  V_GEMM_CHAIN = 0,
+  V_CONV1X1_CHAIN,
+  V_CONV_CHAIN,
+  V_GEMM_SINGLE,
+  V_CONV1X1_SINGLE,
+  V_CONV_SINGLE,
+  V_CONV_POOL,
+  V_COUNT
+};
+
+// Kernel function pointer of a variant (for cudaFuncSetAttribute).
+const void* variant_func(Variant v);
+
+cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
+                           const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
+                           int grid, size_t smem, cudaStream_t stream);
+
+// Plain 2x2/2 max-pool over NHWC fp16/bf16 (the unfused pooling operator).
+cudaError_t launch_maxpool(int is_bf16, int N, int H, int W, int C, const void* x, void* y,
+                           int num_sms, cudaStream_t stream);
+
+// One-CTA kernel whose only wait can never complete; it must time out.
+cudaError_t launch_probe_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t stream);
+
+}  // namespace b2b

@@ -1,0 +1,285 @@
+"""Python binding of libb2b.so (include/b2b.h): argument marshalling only.
+
+Every function takes CUDA tensors, checks dtypes, shapes and contiguity (the C ABI sees
+only pointers and sizes), allocates the output with torch when none is given, and calls
+the entry point of the same name on the current torch stream.  All arithmetic runs in the
+library's kernels; there is no other code path, and a missing or unloadable library
+raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+EPILOGUES = {"none": 0, "relu": 1, "hardswish": 2}
+STATUS = {0: "B2B_OK", 1: "B2B_ERR_NULL", 2: "B2B_ERR_SHAPE", 3: "B2B_ERR_ALIGN",
+          4: "B2B_ERR_UNSUPPORTED", 5: "B2B_ERR_CUDA", 6: "B2B_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class B2BError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libb2b.so (building it first if it is absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        i32, i64, vp, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint64
+        ci = ctypes.c_int
+        L.b2b_gemm.argtypes = [ci, i64, i32, i32, i32, vp, vp, vp, ci, vp, vp, ci, vp, vp]
+        L.b2b_conv_nhwc.argtypes = [ci, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32, vp, ci,
+                                    vp, i32, vp, ci, vp, vp]
+        L.conv_relu_maxpool.argtypes = [ci, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp]
+        L.gemm_bias_act.argtypes = [ci, i64, i32, i32, vp, vp, vp, ci, vp, vp]
+        L.conv_bias_act_nhwc.argtypes = [ci, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32, vp,
+                                         ci, vp, vp]
+        L.maxpool2x2_nhwc.argtypes = [ci, i32, i32, i32, i32, vp, vp, vp]
+        for name in ("b2b_gemm", "b2b_conv_nhwc", "conv_relu_maxpool", "gemm_bias_act",
+                     "conv_bias_act_nhwc", "maxpool2x2_nhwc", "b2b_get_device_error",
+                     "b2b_probe_timeout"):
+            getattr(L, name).restype = ci
+        L.b2b_status_str.argtypes = [ci]
+        L.b2b_status_str.restype = ctypes.c_char_p
+        L.b2b_version.argtypes = []
+        L.b2b_version.restype = ctypes.c_char_p
+        L.b2b_num_sms.argtypes = []
+        L.b2b_num_sms.restype = i32
+        L.b2b_set_wait_limit_ns.argtypes = [u64]
+        L.b2b_set_wait_limit_ns.restype = None
+        L.b2b_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        L.b2b_probe_timeout.argtypes = [u64, vp]
+        _lib = L
+        return L
+
+
+# ------------------------------------------------------------------------------------
+# marshalling helpers
+# ------------------------------------------------------------------------------------
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"expected float16 or bfloat16, got {t.dtype}")
+
+
+def _epi(e) -> int:
+    if isinstance(e, int):
+        return e
+    try:
+        return EPILOGUES[e]
+    except KeyError:
+        raise ValueError(f"unknown epilogue {e!r}; expected one of {list(EPILOGUES)}") from None
+
+
+def _check_tensor(t: torch.Tensor, name: str, dtype, shape) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _raise(status: int, what: str) -> None:
+    if status != 0:
+        raise B2BError(status, what)
+
+
+# ------------------------------------------------------------------------------------
+# fused chains
+# ------------------------------------------------------------------------------------
+
+def b2b_gemm(A, W0, b0, W1, b1, epi0="relu", epi1="relu", out=None, stream=None):
+    """out[M,N1] = epi1(epi0(A[M,K0] @ W0[K0,N0] + b0) @ W1[N0,N1] + b1), one launch."""
+    dt = A.dtype
+    M, K0 = A.shape
+    N0, N1 = W0.shape[1], W1.shape[1]
+    _check_tensor(A, "A", dt, (M, K0))
+    _check_tensor(W0, "W0", dt, (K0, N0))
+    _check_tensor(W1, "W1", dt, (N0, N1))
+    if b0 is not None:
+        _check_tensor(b0, "b0", dt, (N0,))
+    if b1 is not None:
+        _check_tensor(b1, "b1", dt, (N1,))
+    if out is None:
+        out = torch.empty((M, N1), dtype=dt, device=A.device)
+    _check_tensor(out, "out", dt, (M, N1))
+    _raise(lib().b2b_gemm(_dtype_code(A), M, K0, N0, N1, _ptr(A), _ptr(W0), _ptr(b0), _epi(epi0),
+                          _ptr(W1), _ptr(b1), _epi(epi1), _ptr(out), _stream(stream)), "b2b_gemm")
+    return out
+
+
+def b2b_conv_nhwc(x, W0, b0, W1, b1, pad=1, epi0="relu", epi1="relu", out=None, stream=None):
+    """out = conv1x1(conv_RxS(x) + b0 -> epi0) + b1 -> epi1, NHWC, stride 1, one launch.
+    x [N,H,W,C], W0 [C0,R,S,C], W1 [C1,C0] -> out [N,Ho,Wo,C1]."""
+    dt = x.dtype
+    N, H, W, C = x.shape
+    C0, R, S = W0.shape[0], W0.shape[1], W0.shape[2]
+    C1 = W1.shape[0]
+    _check_tensor(x, "x", dt, (N, H, W, C))
+    _check_tensor(W0, "W0", dt, (C0, R, S, C))
+    _check_tensor(W1, "W1", dt, (C1, C0))
+    if b0 is not None:
+        _check_tensor(b0, "b0", dt, (C0,))
+    if b1 is not None:
+        _check_tensor(b1, "b1", dt, (C1,))
+    Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
+    if out is None:
+        out = torch.empty((N, max(Ho, 0), max(Wo, 0), C1), dtype=dt, device=x.device)
+    _check_tensor(out, "out", dt, (N, max(Ho, 0), max(Wo, 0), C1))
+    _raise(lib().b2b_conv_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(W0), C0, R, S, pad,
+                               _ptr(b0), _epi(epi0), _ptr(W1), C1, _ptr(b1), _epi(epi1),
+                               _ptr(out), _stream(stream)), "b2b_conv_nhwc")
+    return out
+
+
+def conv_relu_maxpool(x, Wt, b, out=None, stream=None):
+    """out = maxpool2x2(relu(conv3x3_pad1(x, Wt) + b)), NHWC, one launch.
+    x [N,H,W,Cin], Wt [Cout,3,3,Cin] -> out [N,H//2,W//2,Cout]."""
+    dt = x.dtype
+    N, H, W, Cin = x.shape
+    Cout = Wt.shape[0]
+    _check_tensor(x, "x", dt, (N, H, W, Cin))
+    _check_tensor(Wt, "Wt", dt, (Cout, 3, 3, Cin))
+    if b is not None:
+        _check_tensor(b, "b", dt, (Cout,))
+    if out is None:
+        out = torch.empty((N, H // 2, W // 2, Cout), dtype=dt, device=x.device)
+    _check_tensor(out, "out", dt, (N, H // 2, W // 2, Cout))
+    _raise(lib().conv_relu_maxpool(_dtype_code(x), N, H, W, Cin, _ptr(x), _ptr(Wt), _ptr(b), Cout,
+                                   _ptr(out), _stream(stream)), "conv_relu_maxpool")
+    return out
+
+
+# ------------------------------------------------------------------------------------
+# single operators (the unfused two-kernel path)
+# ------------------------------------------------------------------------------------
+
+def gemm_bias_act(A, W, b, epi="relu", out=None, stream=None):
+    """out[M,N] = epi(A[M,K] @ W[K,N] + b)."""
+    dt = A.dtype
+    M, K = A.shape
+    N = W.shape[1]
+    _check_tensor(A, "A", dt, (M, K))
+    _check_tensor(W, "W", dt, (K, N))
+    if b is not None:
+        _check_tensor(b, "b", dt, (N,))
+    if out is None:
+        out = torch.empty((M, N), dtype=dt, device=A.device)
+    _check_tensor(out, "out", dt, (M, N))
+    _raise(lib().gemm_bias_act(_dtype_code(A), M, K, N, _ptr(A), _ptr(W), _ptr(b), _epi(epi),
+                               _ptr(out), _stream(stream)), "gemm_bias_act")
+    return out
+
+
+def conv_bias_act_nhwc(x, Wt, b, pad=1, epi="relu", out=None, stream=None):
+    """out = epi(conv_RxS(x, Wt) + b); x [N,H,W,C], Wt [Co,R,S,C] -> [N,Ho,Wo,Co]."""
+    dt = x.dtype
+    N, H, W, C = x.shape
+    Co, R, S = Wt.shape[0], Wt.shape[1], Wt.shape[2]
+    _check_tensor(x, "x", dt, (N, H, W, C))
+    _check_tensor(Wt, "Wt", dt, (Co, R, S, C))
+    if b is not None:
+        _check_tensor(b, "b", dt, (Co,))
+    Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
+    if out is None:
+        out = torch.empty((N, max(Ho, 0), max(Wo, 0), Co), dtype=dt, device=x.device)
+    _check_tensor(out, "out", dt, (N, max(Ho, 0), max(Wo, 0), Co))
+    _raise(lib().conv_bias_act_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(Wt), Co, R, S, pad,
+                                    _ptr(b), _epi(epi), _ptr(out), _stream(stream)),
+           "conv_bias_act_nhwc")
+    return out
+
+
+def maxpool2x2_nhwc(x, out=None, stream=None):
+    """out[N,H//2,W//2,C] = max over 2x2 windows (stride 2, floor mode) of x[N,H,W,C]."""
+    dt = x.dtype
+    N, H, W, C = x.shape
+    _check_tensor(x, "x", dt, (N, H, W, C))
+    if out is None:
+        out = torch.empty((N, H // 2, W // 2, C), dtype=dt, device=x.device)
+    _check_tensor(out, "out", dt, (N, H // 2, W // 2, C))
+    _raise(lib().maxpool2x2_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(out), _stream(stream)),
+           "maxpool2x2_nhwc")
+    return out
+
+
+# ------------------------------------------------------------------------------------
+# diagnostics
+# ------------------------------------------------------------------------------------
+
+def version() -> str:
+    return lib().b2b_version().decode()
+
+
+def status_str(status: int) -> str:
+    return lib().b2b_status_str(status).decode()
+
+
+def num_sms() -> int:
+    return int(lib().b2b_num_sms())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib().b2b_set_wait_limit_ns(int(ns))
+
+
+def get_device_error():
+    """(status, info[4]); reads and clears the device error word (synchronises)."""
+    info = (ctypes.c_uint32 * 4)()
+    st = lib().b2b_get_device_error(info)
+    return int(st), [int(v) for v in info]
+
+
+def probe_timeout(limit_ns: int, stream=None) -> None:
+    _raise(lib().b2b_probe_timeout(int(limit_ns), _stream(stream)), "b2b_probe_timeout")
+
+
+def pad_channels(t: torch.Tensor, dim: int, multiple: int = 8) -> torch.Tensor:
+    """Zero-pads `dim` of t up to a multiple of `multiple` (BOLT's kernel padding to an
+    8-element, 128-bit alignment).  Padded inputs, weights and biases give padded output
+    channels that are exactly zero."""
+    size = t.shape[dim]
+    target = -(-size // multiple) * multiple
+    if target == size:
+        return t.contiguous()
+    pad_shape = list(t.shape)
+    pad_shape[dim] = target - size
+    return torch.cat([t, t.new_zeros(pad_shape)], dim=dim).contiguous()

@@ -1,0 +1,172 @@
+/*
+ * b2b.h -- C ABI of libb2b.so: fused GEMM/conv operator chains for one GB300 (sm_103a).
+ *
+ * Each fused entry point runs a whole operator chain in ONE kernel launch and keeps the
+ * chain's intermediate on chip:
+ *
+ *   b2b_gemm           GEMM0 -> bias + activation -> GEMM1 -> bias + activation
+ *   b2b_conv_nhwc      conv RxS (implicit GEMM) -> bias + act -> conv1x1 -> bias + act
+ *   conv_relu_maxpool  conv3x3 -> bias -> ReLU -> maxpool 2x2/2
+ *
+ * Sources (page title, section):
+ *   BOLT notes, "Enabling deeper operator fusion" / "Persistent kernel (GEMM/Conv)
+ *     fusion": several GEMMs/convs in one kernel, no load/store of the intermediate
+ *     through global memory, no second launch (Figure 4a/4b).
+ *   BOLT notes, "Threadblock residence": the block that computes a GEMM0 output tile also
+ *     computes the GEMM1 tile that consumes it, which needs ThreadBlock_N = GEMM_N (for a
+ *     conv: = output channels).  Here one CTA owns all N0 and N1 columns of its 128 rows,
+ *     hence the N0, N1 <= 256 limits below.
+ *   BOLT notes, "Shared-memory-resident fusion": GEMM0's accumulator tile is converted
+ *     and staged in shared memory, where GEMM1 reads it (Figure 7).
+ *   BOLT notes, "Prerequisite: Epilogue fusion" and "Graph Level" (Conv2D + BiasAdd +
+ *     Hardswish): column-broadcast bias, element-wise activation, dtype conversion.
+ *   BOLT notes, "Templated code generation": all convs in NHWC; tensors padded to an
+ *     alignment of 8 fp16 elements = 128 bits (errata note: "8 bit" means 8 elements).
+ *   Welder notes, "Operator-tile and Tile-graph" / "Tile-graph Scheduling" (Figure 5):
+ *     Conv + ReLU + MaxPool as one tile-graph; the (2,2,F) reuse tile stays on chip.
+ *   AI-Infra interview notes, "Conv optimisation": implicit GEMM (addresses computed on
+ *     the fly, no im2col buffer); a 1x1 conv is a GEMM.
+ *
+ * Conventions shared by every entry point
+ *   - Element type: dt selects fp16 or bf16 for every tensor argument (inputs, weights,
+ *     biases and outputs).  Products accumulate in fp32; bias and activation are applied
+ *     in fp32; each stored tensor (the on-chip intermediate included) is rounded to nearest
+ *     even into dt.
+ *   - Layouts are row-major / NHWC and dense (no strides): see each function.
+ *   - Pointers: tensor pointers are DEVICE pointers, 16-byte aligned.  Bias pointers are
+ *     device pointers (2-byte aligned) or NULL for "no bias".
+ *   - Channel / inner sizes (K0, N0, N1, C, C0, C1, Cin, Cout) are multiples of 8
+ *     elements (16 bytes).  Callers with other sizes zero-pad channels, weights and
+ *     biases up to the next multiple of 8; the padded output channels are then exactly 0.
+ *   - Ownership: the caller owns every buffer.  The library allocates no device memory per
+ *     call; its only state is a host-side cache of TMA tensor maps, a per-device record of
+ *     kernel attributes, and one small device error word per device.
+ *   - Asynchrony: calls enqueue work on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and return without synchronising.  Outputs must not alias inputs.
+ *   - Errors: argument errors are detected on the host before anything is launched and
+ *     returned as a status; launch failures return B2B_ERR_CUDA.  A kernel that waits
+ *     longer than the wait limit (b2b_set_wait_limit_ns) for an on-chip event gives up,
+ *     leaves its output incomplete and records B2B_ERR_TIMEOUT in the device error word,
+ *     read with b2b_get_device_error.  No call aborts, traps or throws.
+ *   - Empty problems (M == 0, N == 0) return B2B_OK and launch nothing.
+ */
+#ifndef B2B_H
+#define B2B_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum b2b_status {
+    B2B_OK = 0,
+    B2B_ERR_NULL = 1,         /* a required pointer is NULL */
+    B2B_ERR_SHAPE = 2,        /* a size is negative, or the output would be empty/invalid */
+    B2B_ERR_ALIGN = 3,        /* pointer not 16-byte aligned, or a channel size not % 8 */
+    B2B_ERR_UNSUPPORTED = 4,  /* outside the kernels' limits (e.g. N0 > 256) */
+    B2B_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed (no device, launch...) */
+    B2B_ERR_TIMEOUT = 6       /* a kernel gave up waiting (from b2b_get_device_error) */
+} b2b_status;
+
+typedef enum b2b_dtype { B2B_F16 = 0, B2B_BF16 = 1 } b2b_dtype;
+
+/* Element-wise operator of an epilogue, applied after the bias:
+ *   NONE: y = z;  RELU: y = max(z, 0);  HARDSWISH: y = z * min(max(z + 3, 0), 6) / 6. */
+typedef enum b2b_epilogue { B2B_EPI_NONE = 0, B2B_EPI_RELU = 1, B2B_EPI_HARDSWISH = 2 } b2b_epilogue;
+
+/* ------------------------------------------------------------------------------------ */
+/* Fused chains                                                                          */
+/* ------------------------------------------------------------------------------------ */
+
+/* D[M,N1] = e1( e0( A[M,K0] . W0[K0,N0] + b0 ) . W1[N0,N1] + b1 )
+ * (BOLT notes: "Persistent kernel (GEMM/Conv) fusion", "Threadblock residence",
+ *  "Shared-memory-resident fusion").
+ *   A  [M][K0]  row-major      W0 [K0][N0] row-major     b0 [N0] or NULL
+ *   W1 [N0][N1] row-major      b1 [N1] or NULL           D  [M][N1] row-major (output)
+ * Limits: M >= 0; K0 >= 8; 8 <= N0 <= 256; 8 <= N1 <= 256; K0, N0, N1 multiples of 8.
+ * The GEMM0 result tile (128 rows x N0) is rounded to dt and kept in shared memory. */
+b2b_status b2b_gemm(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
+                    const void* A, const void* W0, const void* b0, b2b_epilogue e0,
+                    const void* W1, const void* b1, b2b_epilogue e1,
+                    void* D, void* stream);
+
+/* y = conv1x1_{W1,b1,e1}( conv_{W0,b0,e0}(x) ), stride 1, dilation 1, zero padding `pad`,
+ * cross-correlation (implicit GEMM; interview notes "Conv optimisation", item 2; BOLT
+ * notes "Persistent kernel fusion" for the conv case, ThreadBlock_N = output channels).
+ *   x  [N][H][W][C]             W0 [C0][R][S][C]          b0 [C0] or NULL
+ *   W1 [C1][C0]  (the 1x1 filter, output-channel major)   b1 [C1] or NULL
+ *   y  [N][Ho][Wo][C1] with Ho = H + 2*pad - R + 1, Wo = W + 2*pad - S + 1 (output)
+ * Limits: N, H, W >= 0; Ho, Wo >= 1 when N*H*W > 0; 1 <= R, S <= 7; 0 <= pad <= 3;
+ * C >= 8, 8 <= C0 <= 256, 8 <= C1 <= 256, all multiples of 8. */
+b2b_status b2b_conv_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                         const void* x, const void* W0, int32_t C0, int32_t R, int32_t S,
+                         int32_t pad, const void* b0, b2b_epilogue e0,
+                         const void* W1, int32_t C1, const void* b1, b2b_epilogue e1,
+                         void* y, void* stream);
+
+/* y = maxpool2x2_stride2( ReLU( conv3x3_pad1(x, Wt) + b ) ), floor mode
+ * (Welder notes, "Tile-graph Scheduling", Figure 5: Conv+ReLU at registers, ReLU->MaxPool
+ * through the (2,2,F) reuse tile; the conv output never reaches global memory).
+ *   x  [N][H][W][Cin]     Wt [Cout][3][3][Cin]     b [Cout] or NULL
+ *   y  [N][H/2][W/2][Cout] (output; an odd last row/column of the conv is dropped)
+ * Limits: N >= 0; H, W >= 2; Cin >= 8; 8 <= Cout <= 256; Cin, Cout multiples of 8. */
+b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t Cin,
+                             const void* x, const void* Wt, const void* b, int32_t Cout,
+                             void* y, void* stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* Single operators: the unfused two-kernel path the fused chains are measured against   */
+/* ------------------------------------------------------------------------------------ */
+
+/* D[M,N] = e( A[M,K] . W[K,N] + b ); layouts and limits as GEMM0 of b2b_gemm. */
+b2b_status gemm_bias_act(b2b_dtype dt, int64_t M, int32_t K, int32_t N,
+                         const void* A, const void* W, const void* b, b2b_epilogue e,
+                         void* D, void* stream);
+
+/* y[N,Ho,Wo,Co] = e( conv_{R x S, pad}(x[N,H,W,C], Wt[Co][R][S][C]) + b );
+ * layouts and limits as the first conv of b2b_conv_nhwc. */
+b2b_status conv_bias_act_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                              const void* x, const void* Wt, int32_t Co, int32_t R, int32_t S,
+                              int32_t pad, const void* b, b2b_epilogue e,
+                              void* y, void* stream);
+
+/* y[N,H/2,W/2,C] = max over each 2x2 window (stride 2, floor mode) of x[N,H,W,C].
+ * Limits: H, W >= 2; C multiple of 8. */
+b2b_status maxpool2x2_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                           const void* x, void* y, void* stream);
+
+/* ------------------------------------------------------------------------------------ */
+/* Diagnostics                                                                           */
+/* ------------------------------------------------------------------------------------ */
+
+/* Static string naming a status. */
+const char* b2b_status_str(b2b_status s);
+
+/* Library version, e.g. "0.1.0". */
+const char* b2b_version(void);
+
+/* Number of SMs of the current device (the persistent grid size), or -1 on error. */
+int32_t b2b_num_sms(void);
+
+/* Wait limit, in nanoseconds, that later launches give each of their on-chip waits
+ * (default 1e9 = 1 s).  0 restores the default.  Host-side setting, not per stream. */
+void b2b_set_wait_limit_ns(uint64_t ns);
+
+/* Reads and clears the current device's error word.  Synchronises the current device.
+ * Returns B2B_OK if no kernel recorded an error, B2B_ERR_TIMEOUT if one gave up waiting
+ * (then info[0] = code, info[1] = kernel id, info[2] = wait site, info[3] = tile index),
+ * or B2B_ERR_CUDA if the word could not be read.  info may be NULL. */
+b2b_status b2b_get_device_error(uint32_t info[4]);
+
+/* Launches a one-CTA kernel that waits, with the given limit, on an on-chip barrier that
+ * nothing will ever signal, so that it takes its timeout path and records
+ * B2B_ERR_TIMEOUT.  Used by tests of the failure-detection path. */
+b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B2B_H */

@@ -1,0 +1,282 @@
+"""GPU parity: every entry point of libb2b.so against the CPU oracle, element by element.
+
+Shapes span several 128-row tiles with ragged tails, padded channel counts, odd spatial
+sizes, both storage types and every epilogue.  Integer-valued cases must match exactly
+(they pin layouts, swizzles, tap offsets, padding and pool windows bit for bit); random
+cases must be within 2e-2 * max(1, |ref|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_conv_chains_gb300 import ops
+from gemm_conv_chains_gb300 import workloads as wl
+
+from gpu_util import check_no_device_error, compare, run_b2b_gemm, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ops.lib()
+    ops.get_device_error()   # start from a clean error word
+
+
+# ------------------------------------------------------------------------------------
+# b2b GEMM
+# ------------------------------------------------------------------------------------
+GEMM_SHAPES = [
+    # dtype, M, K0, N0, N1
+    ("f16", 1, 64, 64, 64),
+    ("f16", 300, 64, 64, 64),
+    ("f16", 1000, 64, 64, 64),
+    ("bf16", 513, 256, 256, 128),
+    ("f16", 257, 72, 40, 24),
+    ("bf16", 129, 8, 8, 8),
+    ("f16", 640, 128, 128, 256),
+    ("f16", 200, 320, 96, 200),
+    ("bf16", 384, 64, 256, 256),
+]
+
+
+@pytest.mark.parametrize("shape", GEMM_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_b2b_gemm_integer_exact(shape):
+    dt, M, K0, N0, N1 = shape
+    for acts in (("relu", "none"), ("none", "relu")):
+        w = wl.GemmChain("int", dt, M, K0, N0, N1, *acts)
+        run_b2b_gemm(w, seed=M, integer=True)
+
+
+@pytest.mark.parametrize("shape", GEMM_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_b2b_gemm_random(shape):
+    dt, M, K0, N0, N1 = shape
+    w = wl.GemmChain("rnd", dt, M, K0, N0, N1, "hardswish", "relu")
+    run_b2b_gemm(w, seed=M + 1)
+
+
+def test_b2b_gemm_without_bias():
+    w = wl.GemmChain("nobias", "f16", 300, 64, 64, 64, "relu", "hardswish", bias=False)
+    run_b2b_gemm(w, seed=3)
+
+
+def test_b2b_gemm_small_workload_full():
+    run_b2b_gemm(wl.GEMM_SMALL, seed=0)
+
+
+def test_b2b_gemm_ffn_workload_sampled_rows():
+    # Full-size FFN-like chain in the benchmark's launch configuration; the oracle checks
+    # a sample of rows (rows are independent) including the first and last tiles.
+    w = wl.GEMM_FFN
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(128), np.arange(w.M - 128, w.M),
+                                     rng.choice(w.M, 1024, replace=False)]))
+    run_b2b_gemm(w, seed=0, rows=rows)
+
+
+# ------------------------------------------------------------------------------------
+# single GEMM stage (unfused path)
+# ------------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [("f16", 300, 64, 64), ("bf16", 513, 256, 256),
+                                   ("f16", 130, 24, 40), ("f16", 1, 8, 8)],
+                         ids=lambda s: "-".join(map(str, s)))
+@pytest.mark.parametrize("integer", [True, False])
+def test_gemm_bias_act(shape, integer):
+    dt, M, K, N = shape
+    w = wl.GemmChain("g", dt, M, K, N, 8, "relu" if integer else "hardswish", "none")
+    t = wl.gemm_inputs(w, seed=M, integer=integer)
+    out = ops.gemm_bias_act(to_dev(t["A"]), to_dev(t["W0"]), to_dev(t["b0"]), w.act0)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    ref = oracle.gemm_bias_act(dt, wl.to_bits(t["A"]), wl.to_bits(t["W0"]), wl.to_bits(t["b0"]),
+                               w.act0)
+    compare(dt, wl.to_bits(out.cpu()), ref, integer, "gemm_bias_act")
+
+
+# ------------------------------------------------------------------------------------
+# b2b conv
+# ------------------------------------------------------------------------------------
+CONV_SHAPES = [
+    # dtype, N, H, W, C, C0, R, S, pad, C1
+    ("f16", 2, 9, 9, 64, 64, 3, 3, 1, 128),
+    ("f16", 1, 17, 20, 16, 24, 3, 3, 1, 8),
+    ("bf16", 2, 8, 16, 64, 64, 3, 3, 1, 64),
+    ("f16", 1, 11, 13, 128, 64, 3, 3, 0, 64),
+    ("f16", 1, 10, 12, 32, 32, 5, 5, 2, 16),
+    ("f16", 2, 7, 9, 64, 64, 1, 1, 0, 64),     # the 1x1 path (GEMM over pixels)
+    ("f16", 1, 6, 6, 16, 16, 1, 3, 1, 16),     # non-square filter, wider output
+    ("bf16", 1, 5, 5, 8, 8, 1, 1, 1, 8),       # 1x1 with padding: zero border rows
+]
+
+
+def run_conv(dt, N, H, W, C, C0, R, S, pad, C1, act0, act1, integer, seed):
+    w = wl.ConvChain("c", dt, N, H, W, C, C0, R, S, pad, C1, act0, act1)
+    t = wl.conv_inputs(w, seed=seed, integer=integer)
+    out = ops.b2b_conv_nhwc(to_dev(t["x"]), to_dev(t["W0"]), to_dev(t["b0"]), to_dev(t["W1"]),
+                            to_dev(t["b1"]), pad, act0, act1)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    b = {k: wl.to_bits(v) for k, v in t.items()}
+    ref = oracle.b2b_conv_nhwc(dt, b["x"], b["W0"], b["b0"], b["W1"], b["b1"], pad, act0, act1)
+    return compare(dt, wl.to_bits(out.cpu()), ref, integer, "b2b_conv_nhwc")
+
+
+@pytest.mark.parametrize("shape", CONV_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_b2b_conv_integer_exact(shape):
+    run_conv(*shape, "relu", "none", True, seed=sum(shape[1:]))
+
+
+@pytest.mark.parametrize("shape", CONV_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_b2b_conv_random(shape):
+    run_conv(*shape, "hardswish", "none", False, seed=sum(shape[1:]) + 1)
+
+
+@pytest.mark.parametrize("shape", [("f16", 2, 9, 9, 64, 64, 3, 3, 1), ("f16", 1, 7, 5, 16, 24, 3, 3, 1),
+                                   ("f16", 2, 6, 6, 64, 64, 1, 1, 0)],
+                         ids=lambda s: "-".join(map(str, s)))
+@pytest.mark.parametrize("integer", [True, False])
+def test_conv_bias_act(shape, integer):
+    dt, N, H, W, C, Co, R, S, pad = shape
+    w = wl.ConvChain("c", dt, N, H, W, C, Co, R, S, pad, 8, "relu", "none")
+    t = wl.conv_inputs(w, seed=H * W, integer=integer)
+    act = "relu" if integer else "hardswish"
+    out = ops.conv_bias_act_nhwc(to_dev(t["x"]), to_dev(t["W0"]), to_dev(t["b0"]), pad, act)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    ref = oracle.conv2d_nhwc(dt, wl.to_bits(t["x"]), wl.to_bits(t["W0"]), wl.to_bits(t["b0"]),
+                             pad, act)
+    compare(dt, wl.to_bits(out.cpu()), ref, integer, "conv_bias_act_nhwc")
+
+
+def test_conv1x1_workload_sampled_images():
+    w = wl.CONV1X1
+    t = wl.conv_inputs(w, seed=0)
+    out = ops.b2b_conv_nhwc(*(to_dev(t[k]) for k in ("x", "W0", "b0", "W1", "b1")), w.pad,
+                            w.act0, w.act1)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    b = {k: wl.to_bits(v) for k, v in t.items()}
+    got = wl.to_bits(out.cpu())
+    for n in (0, 37, w.N - 1):
+        ref = oracle.b2b_conv_nhwc(w.dtype, b["x"][n:n + 1], b["W0"], b["b0"], b["W1"], b["b1"],
+                                   w.pad, w.act0, w.act1)
+        compare(w.dtype, got[n:n + 1], ref, False, f"conv1x1 image {n}")
+
+
+def test_conv3x3_1x1_workload_sampled_images():
+    w = wl.CONV3X3_1X1
+    t = wl.conv_inputs(w, seed=0)
+    out = ops.b2b_conv_nhwc(*(to_dev(t[k]) for k in ("x", "W0", "b0", "W1", "b1")), w.pad,
+                            w.act0, w.act1)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    b = {k: wl.to_bits(v) for k, v in t.items()}
+    got = wl.to_bits(out.cpu())
+    for n in (0, w.N - 1):
+        ref = oracle.b2b_conv_nhwc(w.dtype, b["x"][n:n + 1], b["W0"], b["b0"], b["W1"], b["b1"],
+                                   w.pad, w.act0, w.act1)
+        compare(w.dtype, got[n:n + 1], ref, False, f"conv3x3_1x1 image {n}")
+
+
+# ------------------------------------------------------------------------------------
+# conv + ReLU + maxpool
+# ------------------------------------------------------------------------------------
+POOL_SHAPES = [
+    # dtype, N, H, W, Cin, Cout
+    ("f16", 2, 16, 16, 64, 64),
+    ("f16", 1, 7, 9, 16, 8),
+    ("bf16", 1, 20, 34, 32, 64),
+    ("f16", 1, 2, 2, 8, 8),
+    ("f16", 2, 18, 40, 64, 128),
+]
+
+
+def run_pool(dt, N, H, W, Cin, Cout, integer, seed):
+    w = wl.ConvPool("p", dt, N, H, W, Cin, Cout)
+    t = wl.pool_inputs(w, seed=seed, integer=integer)
+    out = ops.conv_relu_maxpool(to_dev(t["x"]), to_dev(t["Wt"]), to_dev(t["b"]))
+    torch.cuda.synchronize()
+    check_no_device_error()
+    ref = oracle.conv_relu_maxpool(dt, wl.to_bits(t["x"]), wl.to_bits(t["Wt"]), wl.to_bits(t["b"]))
+    return compare(dt, wl.to_bits(out.cpu()), ref, integer, "conv_relu_maxpool")
+
+
+@pytest.mark.parametrize("shape", POOL_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_conv_relu_maxpool_integer_exact(shape):
+    run_pool(*shape, True, seed=sum(shape[1:]))
+
+
+@pytest.mark.parametrize("shape", POOL_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_conv_relu_maxpool_random(shape):
+    run_pool(*shape, False, seed=sum(shape[1:]) + 1)
+
+
+def test_conv_pool_workload_sampled_images():
+    w = wl.CONV_POOL
+    t = wl.pool_inputs(w, seed=0)
+    out = ops.conv_relu_maxpool(to_dev(t["x"]), to_dev(t["Wt"]), to_dev(t["b"]))
+    torch.cuda.synchronize()
+    check_no_device_error()
+    got = wl.to_bits(out.cpu())
+    b = {k: wl.to_bits(v) for k, v in t.items()}
+    for n in (0, w.N - 1):
+        ref = oracle.conv_relu_maxpool(w.dtype, b["x"][n:n + 1], b["Wt"], b["b"])
+        compare(w.dtype, got[n:n + 1], ref, False, f"conv_pool image {n}")
+
+
+@pytest.mark.parametrize("shape", [("f16", 2, 8, 8, 64), ("bf16", 1, 7, 9, 16), ("f16", 3, 2, 3, 8)])
+def test_maxpool2x2(shape):
+    dt, N, H, W, C = shape
+    g = torch.Generator().manual_seed(H * W)
+    x = (torch.rand((N, H, W, C), generator=g) * 8 - 4).to(wl.DTYPES[dt])
+    out = ops.maxpool2x2_nhwc(x.cuda())
+    torch.cuda.synchronize()
+    ref = oracle.maxpool2x2_nhwc(dt, wl.to_bits(x))
+    compare(dt, wl.to_bits(out.cpu()), ref, True, "maxpool2x2_nhwc")
+
+
+# ------------------------------------------------------------------------------------
+# unfused two-kernel path == fused chain (same tiles, same roundings)
+# ------------------------------------------------------------------------------------
+def test_unfused_gemm_chain_matches_fused_bitwise():
+    w = wl.GemmChain("u", "bf16", 1000, 256, 256, 128, "hardswish", "hardswish", a_dist="normal")
+    t = {k: to_dev(v) for k, v in wl.gemm_inputs(w, seed=4).items()}
+    fused = ops.b2b_gemm(t["A"], t["W0"], t["b0"], t["W1"], t["b1"], w.act0, w.act1)
+    h = ops.gemm_bias_act(t["A"], t["W0"], t["b0"], w.act0)
+    unfused = ops.gemm_bias_act(h, t["W1"], t["b1"], w.act1)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
+
+
+def test_unfused_conv_pool_matches_fused_bitwise():
+    w = wl.ConvPool("u", "f16", 2, 16, 24, 64, 64)
+    t = {k: to_dev(v) for k, v in wl.pool_inputs(w, seed=5).items()}
+    fused = ops.conv_relu_maxpool(t["x"], t["Wt"], t["b"])
+    c = ops.conv_bias_act_nhwc(t["x"], t["Wt"], t["b"], 1, "relu")
+    unfused = ops.maxpool2x2_nhwc(c)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.float(), unfused.float())
+
+
+# ------------------------------------------------------------------------------------
+# empty problems, failure detection
+# ------------------------------------------------------------------------------------
+def test_empty_problems_launch_nothing():
+    A = torch.empty((0, 64), dtype=torch.float16, device="cuda")
+    W = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
+    assert ops.b2b_gemm(A, W, None, W, None).shape == (0, 64)
+    x = torch.empty((0, 8, 8, 64), dtype=torch.float16, device="cuda")
+    Wt = torch.zeros((64, 3, 3, 64), dtype=torch.float16, device="cuda")
+    assert ops.conv_relu_maxpool(x, Wt, None).shape == (0, 4, 4, 64)
+
+
+def test_timeout_path_reports_and_context_survives():
+    ops.get_device_error()
+    ops.probe_timeout(20_000_000)            # 20 ms on a barrier nothing signals
+    st, info = ops.get_device_error()
+    assert st == 6 and info[0] == 6 and info[1] == 15, (st, info)
+    assert ops.get_device_error()[0] == 0    # read-and-clear
+    run_b2b_gemm(wl.GemmChain("after", "f16", 200, 64, 64, 64, "relu", "none"), integer=True)
