@@ -168,9 +168,16 @@ inline bool valid_epi(int e) {
   return e == B2B_EPI_NONE || e == B2B_EPI_RELU || e == B2B_EPI_HARDSWISH;
 }
 
+// Byte sizes of the shared-memory regions of one launch (for the plan and its checks).
+struct Regions {
+  uint32_t ring, w_res, p, out, bias, bar;
+};
+
 // Shared-memory plan: ring of A (and, when streamed, weight) chunks; resident weights;
-// P tile; output staging; biases (fp32); barriers.  Fills the offsets of p.
-bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_bytes) {
+// P tile; output staging; biases (fp32); barriers.  Fills the offsets of p.  When the
+// output staging shares the P buffer, that buffer is sized for the larger of the two.
+bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_bytes,
+               Regions* regions) {
   const uint32_t budget = kSmemLimit - 1024u;   // 1 KiB slack to align the base to 1024
   const uint32_t n0blk = static_cast<uint32_t>((p.N0p + 63) / 64);
   const uint32_t n1blk = static_cast<uint32_t>((p.N1p + 63) / 64);
@@ -195,8 +202,8 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
       const uint32_t stage_bytes =
           cands[c].resident ? kABytes
                             : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
-      const uint32_t fixed = (cands[c].resident ? w_res : 0u) + p_bytes +
-                             (cands[c].alias ? 0u : out_bytes) + bias_bytes + bar_bytes;
+      const uint32_t shared = cands[c].alias ? std::max(p_bytes, out_bytes) : p_bytes + out_bytes;
+      const uint32_t fixed = (cands[c].resident ? w_res : 0u) + shared + bias_bytes + bar_bytes;
       if (fixed >= budget) continue;
       const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / stage_bytes);
       if (stages < static_cast<uint32_t>(min_stages)) continue;
@@ -211,21 +218,29 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.out_alias_p = cands[chosen].alias;
   p.num_stages = chosen_stages;
   p.stage_bytes = chosen_stage_bytes;
+  Regions r;
+  r.ring = p.num_stages * p.stage_bytes;
+  r.w_res = p.resident ? w_res : 0u;
+  r.p = p.out_alias_p ? std::max(p_bytes, out_bytes) : p_bytes;
+  r.out = p.out_alias_p ? 0u : out_bytes;
+  r.bias = bias_bytes;
+  r.bar = bar_bytes;
   uint32_t off = 0;
   p.off_ring = off;
-  off += p.num_stages * p.stage_bytes;
+  off += r.ring;
   p.off_w0 = off;
   p.off_w1 = off + static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
-  if (p.resident) off += w_res;
+  off += r.w_res;
   p.off_p = off;
-  off += p_bytes;
+  off += r.p;
   p.off_out = p.out_alias_p ? p.off_p : off;
-  if (!p.out_alias_p) off += out_bytes;
+  off += r.out;
   p.off_bias = off;
-  off += bias_bytes;
+  off += r.bias;
   p.off_bar = off;
-  off += bar_bytes;
+  off += r.bar;
   *smem_bytes = off + 1024u;
+  if (regions) *regions = r;
   return *smem_bytes <= kSmemLimit;
 }
 
@@ -238,7 +253,7 @@ void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const v
   p.b1 = static_cast<const uint16_t*>(b1);
   p.wait_limit_ns = g_wait_ns.load();
   p.kernel_id = kid;
-  p.err = d->err;
+  p.err = d ? d->err : nullptr;
 }
 
 void set_tmem(ChainParams& p, int mode) {
@@ -274,16 +289,11 @@ b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtenso
 }
 
 // ------------------------------------------------------------------------------------
-// GEMM-shaped entry points (2-D A operand)
+// launch parameters (host only; no CUDA call)
 // ------------------------------------------------------------------------------------
-// W0/W1 given as [K][N] row-major (w_mn = true) or as [N][K] (conv filters, w_mn = false).
-b2b_status run_gemm(int mode, bool w_mn, int dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
-                    const void* A, const void* W0, const void* b0, int e0, const void* W1,
-                    const void* b1, int e1, void* D, void* stream, uint32_t kid) {
-  b2b_status st = B2B_OK;
-  DeviceState* d = device_state(&st);
-  if (d == nullptr) return st;
-  ChainParams p;
+// 2-D A operand.  W0/W1 are [K][N] row-major when w_mn, else [N][K] (conv filters).
+bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int32_t N0,
+                 int32_t N1, size_t* smem, Regions* regions) {
   std::memset(&p, 0, sizeof(p));
   p.M = static_cast<int32_t>(M);
   p.K0 = K0;
@@ -295,10 +305,50 @@ b2b_status run_gemm(int mode, bool w_mn, int dt, int64_t M, int32_t K0, int32_t 
   p.kc_per_tap = p.kchunks0;
   p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
   p.num_tiles = ceil_div(M, kBlockM);
-  fill_common(p, dt, e0, e1, b0, b1, d, kid);
   set_tmem(p, mode);
+  return plan_smem(p, mode, w_mn, w_mn, smem, regions);
+}
+
+// 4-D implicit-GEMM A operand (conv filters [Cout][R][S][Cin]).
+bool conv_params(ChainParams& p, int mode, int32_t N, int32_t H, int32_t W, int32_t C,
+                 int32_t C0, int32_t R, int32_t S, int32_t pad, int32_t C1, size_t* smem,
+                 Regions* regions) {
+  std::memset(&p, 0, sizeof(p));
+  p.K0 = C;
+  p.N0 = C0;
+  p.N1 = mode == MODE_CHAIN ? C1 : 0;
+  p.N0p = static_cast<int32_t>(round_up(static_cast<uint32_t>(C0), 16u));
+  p.N1p = mode == MODE_CHAIN ? static_cast<int32_t>(round_up(static_cast<uint32_t>(C1), 16u)) : 0;
+  p.kc_per_tap = ceil_div(C, kChunkK);
+  p.kchunks0 = R * S * p.kc_per_tap;
+  p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
+  p.R = R;
+  p.S = S;
+  p.pad = pad;
+  p.Ho = H + 2 * pad - R + 1;
+  p.Wo = W + 2 * pad - S + 1;
+  p.tiles_w = ceil_div(p.Wo, 16);
+  p.tiles_h = ceil_div(p.Ho, 8);
+  const int64_t tiles = static_cast<int64_t>(N) * p.tiles_w * p.tiles_h;
+  if (tiles > INT32_MAX) return false;
+  p.num_tiles = static_cast<int32_t>(tiles);
+  set_tmem(p, mode);
+  return plan_smem(p, mode, false, false, smem, regions);
+}
+
+// ------------------------------------------------------------------------------------
+// GEMM-shaped entry points (2-D A operand)
+// ------------------------------------------------------------------------------------
+b2b_status run_gemm(int mode, bool w_mn, int dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
+                    const void* A, const void* W0, const void* b0, int e0, const void* W1,
+                    const void* b1, int e1, void* D, void* stream, uint32_t kid) {
+  ChainParams p;
   size_t smem = 0;
-  if (!plan_smem(p, mode, w_mn, w_mn, &smem)) return B2B_ERR_UNSUPPORTED;
+  if (!gemm_params(p, mode, w_mn, M, K0, N0, N1, &smem, nullptr)) return B2B_ERR_UNSUPPORTED;
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  if (d == nullptr) return st;
+  fill_common(p, dt, e0, e1, b0, b1, d, kid);
 
   CUtensorMap ta, tw0, tw1, to;
   const uint64_t e = 2;
@@ -337,34 +387,15 @@ b2b_status run_conv(int mode, int dt, int32_t N, int32_t H, int32_t W, int32_t C
                     const void* W0, int32_t C0, int32_t R, int32_t S, int32_t pad, const void* b0,
                     int e0, const void* W1, int32_t C1, const void* b1, int e1, void* y,
                     void* stream, uint32_t kid) {
+  ChainParams p;
+  size_t smem = 0;
+  if (!conv_params(p, mode, N, H, W, C, C0, R, S, pad, C1, &smem, nullptr))
+    return B2B_ERR_UNSUPPORTED;
   b2b_status st = B2B_OK;
   DeviceState* d = device_state(&st);
   if (d == nullptr) return st;
-  const int32_t Ho = H + 2 * pad - R + 1, Wo = W + 2 * pad - S + 1;
-  ChainParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.K0 = C;
-  p.N0 = C0;
-  p.N1 = mode == MODE_CHAIN ? C1 : 0;
-  p.N0p = static_cast<int32_t>(round_up(static_cast<uint32_t>(C0), 16u));
-  p.N1p = mode == MODE_CHAIN ? static_cast<int32_t>(round_up(static_cast<uint32_t>(C1), 16u)) : 0;
-  p.kc_per_tap = ceil_div(C, kChunkK);
-  p.kchunks0 = R * S * p.kc_per_tap;
-  p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
-  p.R = R;
-  p.S = S;
-  p.pad = pad;
-  p.Ho = Ho;
-  p.Wo = Wo;
-  p.tiles_w = ceil_div(Wo, 16);
-  p.tiles_h = ceil_div(Ho, 8);
-  const int64_t tiles = static_cast<int64_t>(N) * p.tiles_w * p.tiles_h;
-  if (tiles > INT32_MAX) return B2B_ERR_UNSUPPORTED;
-  p.num_tiles = static_cast<int32_t>(tiles);
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
-  set_tmem(p, mode);
-  size_t smem = 0;
-  if (!plan_smem(p, mode, false, false, &smem)) return B2B_ERR_UNSUPPORTED;
+  const int32_t Ho = p.Ho, Wo = p.Wo;
 
   const uint64_t e = 2;
   CUtensorMap ta, tw0, tw1, to;
@@ -590,6 +621,71 @@ b2b_status b2b_get_device_error(uint32_t info[4]) {
     return B2B_ERR_CUDA;
   }
   return w[0] == ERR_CODE_TIMEOUT ? B2B_ERR_TIMEOUT : B2B_ERR_CUDA;
+}
+
+b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,
+                          int32_t out_len) {
+  static const int32_t need[5] = {4, 3, 9, 8, 5};
+  if (kind < 0 || kind > 4) return B2B_ERR_UNSUPPORTED;
+  if (dims == nullptr || out == nullptr) return B2B_ERR_NULL;
+  if (ndims < need[kind] || out_len < 28) return B2B_ERR_SHAPE;
+  for (int i = 0; i < need[kind]; ++i)
+    if (dims[i] < 0 || dims[i] > INT32_MAX) return B2B_ERR_SHAPE;
+  const int32_t d0 = static_cast<int32_t>(dims[0]), d1 = static_cast<int32_t>(dims[1]),
+                d2 = static_cast<int32_t>(dims[2]), d3 = static_cast<int32_t>(dims[3]);
+  ChainParams p;
+  Regions r;
+  size_t smem = 0;
+  bool ok = false;
+  b2b_status st = B2B_OK;
+  int32_t mode = MODE_CHAIN;
+  switch (kind) {
+    case 0:   // b2b_gemm: M, K0, N0, N1
+      if ((st = check_channels(d1, kMaxReduction)) != B2B_OK) return st;
+      if ((st = check_channels(d2, 256)) != B2B_OK) return st;
+      if ((st = check_channels(d3, 256)) != B2B_OK) return st;
+      ok = gemm_params(p, MODE_CHAIN, true, dims[0], d1, d2, d3, &smem, &r);
+      break;
+    case 1:   // gemm_bias_act: M, K, N
+      if ((st = check_channels(d1, kMaxReduction)) != B2B_OK) return st;
+      if ((st = check_channels(d2, 256)) != B2B_OK) return st;
+      mode = MODE_SINGLE;
+      ok = gemm_params(p, MODE_SINGLE, true, dims[0], d1, d2, 0, &smem, &r);
+      break;
+    case 2:
+    case 3: {  // b2b_conv_nhwc: N,H,W,C,C0,R,S,pad[,C1]; conv_bias_act_nhwc: N,H,W,C,Co,R,S,pad
+      const int32_t C0 = static_cast<int32_t>(dims[4]), R = static_cast<int32_t>(dims[5]),
+                    S = static_cast<int32_t>(dims[6]), pad = static_cast<int32_t>(dims[7]);
+      const int32_t C1 = kind == 2 ? static_cast<int32_t>(dims[8]) : 0;
+      if ((st = check_conv_args(d0, d1, d2, d3, C0, R, S, pad)) != B2B_OK) return st;
+      if (kind == 2 && (st = check_channels(C1, 256)) != B2B_OK) return st;
+      mode = kind == 2 ? MODE_CHAIN : MODE_SINGLE;
+      if (R == 1 && S == 1 && pad == 0)
+        ok = gemm_params(p, mode, false, static_cast<int64_t>(d0) * d1 * d2, d3, C0, C1, &smem, &r);
+      else
+        ok = conv_params(p, mode, d0, d1, d2, d3, C0, R, S, pad, C1, &smem, &r);
+      break;
+    }
+    case 4: { // conv_relu_maxpool: N, H, W, Cin, Cout
+      const int32_t Cout = static_cast<int32_t>(dims[4]);
+      if (d0 > 0 && (d1 < 2 || d2 < 2)) return B2B_ERR_SHAPE;
+      if ((st = check_conv_args(d0, d1, d2, d3, Cout, 3, 3, 1)) != B2B_OK) return st;
+      mode = MODE_POOL;
+      ok = conv_params(p, MODE_POOL, d0, d1, d2, d3, Cout, 3, 3, 1, 0, &smem, &r);
+      break;
+    }
+  }
+  if (!ok) return B2B_ERR_UNSUPPORTED;
+  const uint32_t v[28] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+                          static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
+                          p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
+                          p.w1_chunk_bytes, p.off_p, r.p, p.off_out, r.out, p.off_bias, r.bias,
+                          p.off_bar, r.bar, p.tmem_cols, p.acc_stride,
+                          static_cast<uint32_t>(p.num_tiles), static_cast<uint32_t>(p.kchunks0),
+                          static_cast<uint32_t>(p.kchunks1), static_cast<uint32_t>(p.N0p),
+                          static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode)};
+  std::memcpy(out, v, sizeof(v));
+  return B2B_OK;
 }
 
 b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream) {

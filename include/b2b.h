@@ -165,6 +165,24 @@ b2b_status b2b_get_device_error(uint32_t info[4]);
  * B2B_ERR_TIMEOUT.  Used by tests of the failure-detection path. */
 b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
 
+/* Describes, without any CUDA call, the launch an entry point would make for the given
+ * sizes: its shared-memory plan and TMEM use.  For tests and tuning.
+ *   kind 0 b2b_gemm            dims = {M, K0, N0, N1}
+ *   kind 1 gemm_bias_act       dims = {M, K, N}
+ *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1}
+ *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad}
+ *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
+ * out (out_len >= 28) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ * weights resident (0/1), output staging aliases P (0/1), then (offset, bytes) of the
+ * ring, the resident-weight region start, the W1 offset, resident bytes, W0 chunk bytes,
+ * W1 chunk bytes, (offset, bytes) of P, of the output staging, of the biases and of the
+ * barriers, TMEM columns, TMEM accumulator stride, tiles, GEMM0 K chunks, GEMM1 K chunks,
+ * padded N0, padded N1, and the kernel mode (0 chain, 1 single, 2 pool).
+ * Returns the status the entry point would return for these sizes (B2B_OK if it would
+ * launch). */
+b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,
+                          int32_t out_len);
+
 #ifdef __cplusplus
 }
 #endif

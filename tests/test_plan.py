@@ -1,0 +1,149 @@
+"""Launch plans on the host (no GPU): every shared-memory region the kernel touches lies
+inside the dynamic allocation, regions do not overlap, each is at least as large as the
+kernel's accesses into it, and TMEM accumulators fit the allocation.
+
+The sizes below are re-derived from what the kernel writes and reads, independently of
+the planner: A chunks are 128 rows x 128 B; a weight chunk is 64 K-rows x 128 B per
+64-wide N block (row-major weights) or N x 128 B (K-major filters); the P tile and the
+output staging hold 16 KiB per 64 columns; a pooled staging tile 4 KiB per 64 columns.
+"""
+import ctypes
+import itertools
+
+import pytest
+
+from gemm_conv_chains_gb300 import ops
+from gemm_conv_chains_gb300 import workloads as wl
+
+FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "ring", "off_w0",
+          "off_w1", "w_res", "w0_chunk", "w1_chunk", "off_p", "p", "off_out", "out", "off_bias",
+          "bias", "off_bar", "bar", "tmem_cols", "acc_stride", "tiles", "kchunks0", "kchunks1",
+          "N0p", "N1p", "mode"]
+SMEM_LIMIT = 227 * 1024
+KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
+        "conv_relu_maxpool": 4}
+
+
+def plan(kind, dims):
+    arr = (ctypes.c_int64 * len(dims))(*dims)
+    out = (ctypes.c_uint32 * 28)()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 28)
+    return st, dict(zip(FIELDS, list(out)))
+
+
+def rup(x, m):
+    return -(-x // m) * m
+
+
+def check(kind, dims, row_major_w):
+    st, p = plan(kind, dims)
+    assert st == 0, (kind, dims, st)
+    mode = p["mode"]
+    N0p, N1p = p["N0p"], p["N1p"]
+    n0blk, n1blk = -(-N0p // 64), -(-N1p // 64)
+    # what the kernel touches
+    w0_chunk = n0blk * 8192 if row_major_w else N0p * 128
+    w1_chunk = (n1blk * 8192 if row_major_w else N1p * 128) if mode == 0 else 0
+    p_need = n0blk * 16384 if mode == 0 else 0
+    out_need = {0: n1blk * 16384, 1: n0blk * 16384, 2: n0blk * 4096}[mode]
+    assert p["w0_chunk"] == w0_chunk and p["w1_chunk"] == w1_chunk
+    assert p["smem"] <= SMEM_LIMIT
+    assert 2 <= p["stages"] <= 8
+    assert p["ring"] == p["stages"] * p["stage_bytes"]
+    assert p["stage_bytes"] >= 16384 + (0 if p["resident"] else w0_chunk)
+    if not p["resident"]:
+        assert p["stage_bytes"] >= w1_chunk
+    regions = [("ring", p["off_ring"], p["ring"]), ("bias", p["off_bias"], p["bias"]),
+               ("bar", p["off_bar"], p["bar"])]
+    if p["resident"]:
+        assert p["w_res"] >= p["kchunks0"] * w0_chunk + p["kchunks1"] * w1_chunk
+        assert p["off_w1"] == p["off_w0"] + p["kchunks0"] * w0_chunk
+        regions.append(("w", p["off_w0"], p["w_res"]))
+    if mode == 0:
+        need_p = max(p_need, out_need) if p["alias"] else p_need
+        assert p["p"] >= need_p
+        regions.append(("p", p["off_p"], p["p"]))
+    if p["alias"]:
+        assert mode == 0 and p["off_out"] == p["off_p"]
+    else:
+        assert p["out"] >= out_need
+        regions.append(("out", p["off_out"], p["out"]))
+    assert p["bias"] >= 4 * (N0p + N1p)
+    assert p["bar"] >= 8 * 24 + 8
+    usable = p["smem"] - 1024                    # the rest aligns the base to 1024
+    for name, off, size in regions:
+        assert off % 1024 == 0, name
+        assert off + size <= usable, (name, off, size, usable)
+    for (a, oa, sa), (b, ob, sb) in itertools.combinations(regions, 2):
+        assert oa + sa <= ob or ob + sb <= oa, (a, b)
+    # TMEM
+    assert p["tmem_cols"] in (32, 64, 128, 256, 512)
+    assert p["acc_stride"] >= N0p
+    if mode == 0:
+        assert p["acc_stride"] + N1p <= p["tmem_cols"]
+    else:
+        assert 2 * p["acc_stride"] <= p["tmem_cols"]
+    assert N0p % 16 == 0 and 16 <= N0p <= 256 and N1p % 16 == 0 and N1p <= 256
+    return p
+
+
+GEMM = [(1, 64, 64, 64), (640, 128, 128, 256), (200, 320, 96, 200), (384, 64, 256, 256),
+        (32768, 256, 256, 128), (1024, 64, 64, 64), (129, 8, 8, 8), (257, 72, 40, 24),
+        (100, 2048, 256, 256), (100, 8, 256, 8)]
+
+
+@pytest.mark.parametrize("dims", GEMM)
+def test_b2b_gemm_plans(dims):
+    check("b2b_gemm", dims, True)
+
+
+def test_b2b_gemm_plan_sweep():
+    for n0 in range(8, 257, 24):
+        for n1 in range(8, 257, 40):
+            for k0 in (8, 64, 200, 512):
+                check("b2b_gemm", (1000, k0, n0, n1), True)
+
+
+def test_ffn_plan_streams_weights():
+    p = check("b2b_gemm", (32768, 256, 256, 128), True)
+    assert p["resident"] == 0      # 192 KiB of weights plus a 64 KiB P tile cannot all stay
+
+
+@pytest.mark.parametrize("dims", [(1000, 64, 64), (513, 256, 256), (130, 24, 40), (1, 8, 256)])
+def test_gemm_bias_act_plans(dims):
+    check("gemm_bias_act", dims, True)
+
+
+CONV = [(2, 9, 9, 64, 64, 3, 3, 1, 128), (1, 17, 20, 16, 24, 3, 3, 1, 8),
+        (1, 10, 12, 32, 32, 5, 5, 2, 16), (2, 7, 9, 64, 64, 1, 1, 0, 64),
+        (32, 56, 56, 64, 64, 3, 3, 1, 128), (64, 56, 56, 64, 64, 1, 1, 0, 64),
+        (1, 6, 6, 256, 256, 3, 3, 1, 256), (1, 6, 6, 16, 16, 1, 3, 1, 16)]
+
+
+@pytest.mark.parametrize("dims", CONV)
+def test_b2b_conv_plans(dims):
+    check("b2b_conv_nhwc", dims, False)
+
+
+@pytest.mark.parametrize("dims", [(2, 9, 9, 64, 64, 3, 3, 1), (1, 7, 5, 16, 24, 3, 3, 1),
+                                  (2, 6, 6, 64, 64, 1, 1, 0), (1, 8, 8, 256, 256, 7, 7, 3)])
+def test_conv_bias_act_plans(dims):
+    check("conv_bias_act_nhwc", dims, False)
+
+
+@pytest.mark.parametrize("dims", [(32, 112, 112, 64, 64), (1, 7, 9, 16, 8), (1, 2, 2, 8, 8),
+                                  (2, 18, 40, 64, 128), (1, 16, 16, 256, 256)])
+def test_conv_relu_maxpool_plans(dims):
+    check("conv_relu_maxpool", dims, False)
+
+
+def test_workload_tile_counts():
+    assert plan("b2b_gemm", (wl.GEMM_FFN.M, 256, 256, 128))[1]["tiles"] == 256
+    assert plan("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128))[1]["tiles"] == 32 * 7 * 4
+    assert plan("conv_relu_maxpool", (32, 112, 112, 64, 64))[1]["tiles"] == 32 * 14 * 7
+
+
+def test_plan_rejects_like_the_entry_points():
+    assert plan("b2b_gemm", (10, 12, 64, 64))[0] == 3        # K0 not a multiple of 8
+    assert plan("b2b_gemm", (10, 64, 264, 64))[0] == 4       # N0 > 256
+    assert plan("conv_relu_maxpool", (1, 1, 8, 8, 8))[0] == 2
