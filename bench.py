@@ -1,0 +1,524 @@
+"""Benchmark of the fused GEMM/conv chains on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload: the FFN-like b2b GEMM, bf16, A[32768,256] . W0[256,256] (+b0,
+Hardswish) . W1[256,128] (+b1, Hardswish).  One step = one fused launch over one batch.
+Prints ONE JSON line (rank 0).
+
+  value        whole-job TFLOP/s (MMA FLOPs 2*M*(K0*N0 + N0*N1) per step), inputs resident
+               in HBM; the K timed steps rotate through input/output sets whose total size
+               exceeds twice the L2, so every step streams its A from HBM.
+  roofline     the fused kernel's algorithmic bytes (A + W0 + b0 + W1 + b1 + out) per
+               launch over its average launch time, against the measured HBM copy rate.
+  pct_of_roofline  100 * max(FLOPs / tensor peak, bytes / HBM peak) / measured time.
+  unfused      the same chain as two launches (GEMM0 + epilogue -> HBM -> GEMM1), its
+               time and algorithmic bytes (the intermediate written and read back).
+  e2e          the same metric through the public API from pinned host buffers: every step
+               copies the inputs host->device and the result back.
+  cpu_baseline the CPU oracle (single thread) on a bounded sample of rows.
+  workloads    the other four workloads, fused and unfused, measured the same way.
+
+--impl reference times the CPU oracle instead (the method's plain unfused definition),
+on a per-step sample of the same workload sized so the whole run takes about a minute.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import platform
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from gemm_conv_chains_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "fused-chain TFLOPS and % of roofline; HBM bytes vs unfused 2-kernel path"
+UNIT = "TFLOP/s"
+HEADLINE = wl.GEMM_FFN
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for name in ("chain_kernel.cuh", "ptx.cuh", "kernel_params.h"):
+        with open(os.path.join(ROOT, "gemm_conv_chains_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    entry = d.get("workloads", {}).get(workload_name)
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for (t, line) in self.lines:
+            if any(a - 0.05 <= t <= b + 0.05 for a, b in self.windows):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[6 + i]
+                          and "Not" not in r[6 + i]})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------
+# workload runners: each returns (step(i) callable, flops, floor_bytes, unfused step,
+# unfused_bytes, bytes of one input/output set)
+# ------------------------------------------------------------------------------------
+def make_sets(nsets, make_one):
+    return [make_one(i) for i in range(nsets)]
+
+
+def l2_bytes(dev):
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+
+
+def rotation_sets(set_bytes, dev):
+    return max(2, math.ceil(2 * l2_bytes(dev) / set_bytes) + 1)
+
+
+def gemm_runner(w: wl.GemmChain, dev):
+    from gemm_conv_chains_gb300 import ops
+    t = wl.gemm_inputs(w, seed=0)
+    W0, b0, W1, b1 = (t[k].to(dev) for k in ("W0", "b0", "W1", "b1"))
+    set_bytes = 2 * w.M * (w.K0 + w.N1)
+    n = rotation_sets(set_bytes, dev)
+    A0 = t["A"].to(dev)
+    sets = []
+    for i in range(n):
+        A = A0 if i == 0 else A0.roll(i, dims=0).contiguous()
+        sets.append((A, torch.empty((w.M, w.N1), dtype=A0.dtype, device=dev),
+                     torch.empty((w.M, w.N0), dtype=A0.dtype, device=dev)))
+
+    def fused(i):
+        A, D, _ = sets[i % n]
+        ops.b2b_gemm(A, W0, b0, W1, b1, w.act0, w.act1, out=D)
+
+    def unfused(i):
+        A, D, H = sets[i % n]
+        ops.gemm_bias_act(A, W0, b0, w.act0, out=H)
+        ops.gemm_bias_act(H, W1, b1, w.act1, out=D)
+
+    return fused, unfused, n, set_bytes
+
+
+def conv_runner(w: wl.ConvChain, dev):
+    from gemm_conv_chains_gb300 import ops
+    t = wl.conv_inputs(w, seed=0)
+    W0, b0, W1, b1 = (t[k].to(dev) for k in ("W0", "b0", "W1", "b1"))
+    set_bytes = 2 * (w.N * w.H * w.W * w.C + w.M * w.C1)
+    n = rotation_sets(set_bytes, dev)
+    x0 = t["x"].to(dev)
+    sets = []
+    for i in range(n):
+        x = x0 if i == 0 else x0.roll(i, dims=0).contiguous()
+        sets.append((x, torch.empty((w.N, w.Ho, w.Wo, w.C1), dtype=x0.dtype, device=dev),
+                     torch.empty((w.N, w.Ho, w.Wo, w.C0), dtype=x0.dtype, device=dev)))
+    W1_as_conv = W1.view(w.C1, 1, 1, w.C0)
+
+    def fused(i):
+        x, y, _ = sets[i % n]
+        ops.b2b_conv_nhwc(x, W0, b0, W1, b1, w.pad, w.act0, w.act1, out=y)
+
+    def unfused(i):
+        x, y, h = sets[i % n]
+        ops.conv_bias_act_nhwc(x, W0, b0, w.pad, w.act0, out=h)
+        ops.conv_bias_act_nhwc(h, W1_as_conv, b1, 0, w.act1, out=y)
+
+    return fused, unfused, n, set_bytes
+
+
+def pool_runner(w: wl.ConvPool, dev):
+    from gemm_conv_chains_gb300 import ops
+    t = wl.pool_inputs(w, seed=0)
+    Wt, b = t["Wt"].to(dev), t["b"].to(dev)
+    set_bytes = 2 * (w.N * w.H * w.W * w.Cin + w.N * (w.H // 2) * (w.W // 2) * w.Cout)
+    n = rotation_sets(set_bytes, dev)
+    x0 = t["x"].to(dev)
+    sets = []
+    for i in range(n):
+        x = x0 if i == 0 else x0.roll(i, dims=0).contiguous()
+        sets.append((x, torch.empty((w.N, w.H // 2, w.W // 2, w.Cout), dtype=x0.dtype, device=dev),
+                     torch.empty((w.N, w.H, w.W, w.Cout), dtype=x0.dtype, device=dev)))
+
+    def fused(i):
+        x, y, _ = sets[i % n]
+        ops.conv_relu_maxpool(x, Wt, b, out=y)
+
+    def unfused(i):
+        x, y, c = sets[i % n]
+        ops.conv_bias_act_nhwc(x, Wt, b, 1, "relu", out=c)
+        ops.maxpool2x2_nhwc(c, out=y)
+
+    return fused, unfused, n, set_bytes
+
+
+def runner_for(w, dev):
+    if isinstance(w, wl.GemmChain):
+        return gemm_runner(w, dev)
+    if isinstance(w, wl.ConvChain):
+        return conv_runner(w, dev)
+    return pool_runner(w, dev)
+
+
+def time_steps(step, steps, warmup, nsets, dev, graph_len=None):
+    """Runs `warmup` untimed steps, then times exactly `steps` steps with CUDA events on
+    the current stream.  Steps are captured in CUDA graphs of up to `graph_len` launches
+    (a whole rotation of the input sets, repeated) and replayed; returns seconds."""
+    stream = torch.cuda.current_stream(dev)
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if graph_len is None:
+        graph_len = nsets * max(1, 96 // nsets)
+    graphs = {}
+
+    def graph_of(length):
+        if length not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(length):
+                    step(i)
+            graphs[length] = g
+        return graphs[length]
+
+    full, rem = divmod(steps, graph_len)
+    if full:
+        graph_of(graph_len)
+    if rem:
+        graph_of(rem)
+    # one untimed replay of each graph
+    for g in graphs.values():
+        g.replay()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(full):
+        graphs[graph_len].replay()
+    if rem:
+        graphs[rem].replay()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+# ------------------------------------------------------------------------------------
+# the oracle as CPU baseline
+# ------------------------------------------------------------------------------------
+def oracle_sample(w: wl.GemmChain, rows: int, seed: int = 0):
+    t = wl.gemm_inputs(w.with_m(rows), seed=seed)
+    return {k: wl.to_bits(v) for k, v in t.items()}
+
+
+def time_oracle(w: wl.GemmChain, rows: int, reps: int = 1):
+    import oracle
+    b = oracle_sample(w, rows)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.b2b_gemm(w.dtype, b["A"], b["W0"], b["b0"], b["W1"], b["b1"], w.act0, w.act1)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: wl.GemmChain, target_s: float = 10.0):
+    per_row_flops = w.flops / w.M
+    calib_rows = 256
+    t = time_oracle(w, calib_rows)
+    rows = int(min(w.M, max(calib_rows, target_s / max(t, 1e-9) * calib_rows)))
+    t = time_oracle(w, rows)
+    return {"value": rows * per_row_flops / t / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {w.M} rows of {w.name} (rows are independent), "
+                      f"{t:.1f} s single-threaded C, double-precision sums",
+            "host": platform.machine()}
+
+
+# ------------------------------------------------------------------------------------
+# end to end through the public API from host buffers
+# ------------------------------------------------------------------------------------
+def e2e_gemm(w: wl.GemmChain, dev, steps=20):
+    from gemm_conv_chains_gb300 import ops
+    t = wl.gemm_inputs(w, seed=0)
+    host = {k: v.pin_memory() for k, v in t.items()}
+    devb = {k: torch.empty_like(v, device=dev) for k, v in t.items()}
+    out_dev = torch.empty((w.M, w.N1), dtype=t["A"].dtype, device=dev)
+    out_host = torch.empty((w.M, w.N1), dtype=t["A"].dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in t.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        ops.b2b_gemm(devb["A"], devb["W0"], devb["b0"], devb["W1"], devb["b1"], w.act0, w.act1,
+                     out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    e.synchronize()
+    sec = s.elapsed_time(e) / 1e3 / steps
+    return {"value": w.flops / sec / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": sec * 1e3, "steps": steps}
+
+
+# ------------------------------------------------------------------------------------
+# arms
+# ------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def headline_config(world):
+    w = HEADLINE
+    return {"workload": f"{w.name}: b2b GEMM bf16 A[{w.M},{w.K0}] W0[{w.K0},{w.N0}] "
+                        f"W1[{w.N0},{w.N1}], bias+{w.act0}/bias+{w.act1}",
+            "M": w.M, "K0": w.K0, "N0": w.N0, "N1": w.N1, "dtype": w.dtype,
+            "parallelism": f"replicas{world}" if world > 1 else "single-gpu"}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    from gemm_conv_chains_gb300 import ops
+    ops.lib()
+    ops.get_device_error()
+    peaks = load_peaks()
+    w = HEADLINE
+    fused, unfused, nsets, set_bytes = gemm_runner(w, dev)
+    clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES")
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    sec = time_steps(fused, args.steps, args.warmup, nsets, dev)
+    clocks.mark(t_wall0, time.time())
+    if pg:
+        tt = torch.tensor([sec], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        sec = float(tt.item())
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    st, info = ops.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error word after the timed region: {st} {info}")
+    sec_unfused = time_steps(unfused, max(args.steps // 4, 8), args.warmup, nsets, dev)
+    unfused_steps = max(args.steps // 4, 8)
+    clocks.stop()
+
+    ms = sec / args.steps * 1e3
+    t_step = sec / args.steps
+    tflops = w.flops / t_step / 1e12
+    value = world * w.flops * args.steps / sec / 1e12
+    achieved_gbs = w.floor_bytes / t_step / 1e9
+    t_roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.floor_bytes / (peaks["hbm_gbs"] * 1e9))
+    t_unf = sec_unfused / unfused_steps
+    traffic = load_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; A ~ N(0,1), W ~ N(0, 1/K), b ~ U[-0.1, 0.1])",
+        "config": {**headline_config(world),
+                   "l2": f"{nsets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB "
+                         f"(> 2x L2) replayed in CUDA graphs"},
+        "pct_of_roofline": round(100.0 * t_roof / t_step, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": w.floor_bytes,
+                     "peak_source": peaks["source"],
+                     "tensor": {"achieved_tflops": round(tflops, 1), "peak": peaks["bf16_tflops"],
+                                "frac": round(tflops / peaks["bf16_tflops"], 4)}},
+        "unfused": {"ms_per_step": round(t_unf * 1e3, 6), "tflops": round(w.flops / t_unf / 1e12, 2),
+                    "algorithmic_bytes": w.unfused_bytes, "launches_per_step": 2,
+                    "fused_speedup": round(t_unf / t_step, 3)},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0:
+        line["e2e"] = e2e_gemm(w, dev)
+        if not args.skip_cpu:
+            line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
+        if not args.headline_only:
+            line["workloads"] = other_workloads(dev, peaks, max(args.steps // 8, 64), args.warmup)
+        line["clocks"] = clocks.summary()
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def other_workloads(dev, peaks, steps, warmup):
+    out = {}
+    for w in (wl.GEMM_SMALL, wl.GEMM_FFN, wl.CONV1X1, wl.CONV3X3_1X1, wl.CONV_POOL):
+        fused, unfused, nsets, _ = runner_for(w, dev)
+        s_f = time_steps(fused, steps, warmup, nsets, dev) / steps
+        s_u = time_steps(unfused, steps, warmup, nsets, dev) / steps
+        t_roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.floor_bytes / (peaks["hbm_gbs"] * 1e9))
+        out[w.name] = {"us_per_step": round(s_f * 1e6, 3), "tflops": round(w.flops / s_f / 1e12, 1),
+                       "pct_of_roofline": round(100 * t_roof / s_f, 1),
+                       "hbm_gbs_algorithmic": round(w.floor_bytes / s_f / 1e9, 1),
+                       "bound": "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) >
+                                w.floor_bytes / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                       "unfused_us_per_step": round(s_u * 1e6, 3),
+                       "fused_speedup": round(s_u / s_f, 3),
+                       "floor_bytes": w.floor_bytes, "unfused_bytes": w.unfused_bytes}
+        del fused, unfused
+        torch.cuda.empty_cache()
+    from gemm_conv_chains_gb300 import ops
+    st, info = ops.get_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error word: {st} {info}")
+    return out
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = HEADLINE
+    per_row = w.flops / w.M
+    t_cal = time_oracle(w, 128) / 128
+    budget = 60.0
+    rows = int(max(1, min(4096, budget / max(args.steps + args.warmup, 1) / max(t_cal, 1e-9))))
+    import oracle
+    b = oracle_sample(w, rows)
+    for _ in range(args.warmup):
+        oracle.b2b_gemm(w.dtype, b["A"], b["W0"], b["b0"], b["W1"], b["b1"], w.act0, w.act1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.b2b_gemm(w.dtype, b["A"], b["W0"], b["b0"], b["W1"], b["b1"], w.act0, w.act1)
+    sec = time.perf_counter() - t0
+    value = rows * per_row * args.steps / sec / 1e12
+    sample = (f"{rows} of {w.M} rows of {w.name} per step (rows are independent), "
+              f"single-threaded C oracle, double-precision sums")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": headline_config(world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[1])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the per-workload table")
+    ap.add_argument("--skip-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
