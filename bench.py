@@ -380,8 +380,8 @@ def run_ours(args):
     ops.lib()
     ops.get_device_error()
     peaks = load_peaks()
-    w = HEADLINE
-    fused, unfused, nsets, set_bytes = gemm_runner(w, dev)
+    w = wl.WORKLOADS[args.workload]
+    fused, unfused, nsets, set_bytes = runner_for(w, dev)
     clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES")
                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     clocks.start()
@@ -418,7 +418,9 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; A ~ N(0,1), W ~ N(0, 1/K), b ~ U[-0.1, 0.1])",
-        "config": {**headline_config(world),
+        "config": {**(headline_config(world) if w is HEADLINE else
+                      {"workload": w.name, "dtype": w.dtype,
+                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu"}),
                    "l2": f"{nsets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB "
                          f"(> 2x L2) replayed in CUDA graphs"},
         "pct_of_roofline": round(100.0 * t_roof / t_step, 2),
@@ -434,8 +436,9 @@ def run_ours(args):
         "gpu_launches": args.steps,
     }
     if rank == 0:
-        line["e2e"] = e2e_gemm(w, dev)
-        if not args.skip_cpu:
+        if isinstance(w, wl.GemmChain):
+            line["e2e"] = e2e_gemm(w, dev)
+        if not args.skip_cpu and isinstance(w, wl.GemmChain):
             line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
         if not args.headline_only:
             line["workloads"] = other_workloads(dev, peaks, max(args.steps // 8, 64), args.warmup)
@@ -511,6 +514,9 @@ def main():
                     help="skip the per-workload table")
     ap.add_argument("--skip-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", choices=sorted(wl.WORKLOADS), default=HEADLINE.name,
+                    help="workload of the timed line (default: the FFN-like chain); the "
+                         "others are for profiling single kernels")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -170,12 +170,34 @@ inline bool valid_epi(int e) {
 
 // Byte sizes of the shared-memory regions of one launch (for the plan and its checks).
 struct Regions {
-  uint32_t ring, w_res, p, out, bias, bar;
+  uint32_t ring, w_res, p_each, out_each, bias, bar;
 };
 
+// TMEM columns of the accumulators.  Chain: D0 buffers of round_up(N0p, 32) columns, then
+// D1 buffers of round_up(N1p, 32) columns (every buffer starts on a multiple of 32
+// columns); single/pool: two accumulator buffers.  `dual` selects two buffers per
+// accumulator (two tiles in flight).  Returns the power-of-two allocation.
+uint32_t tmem_layout(ChainParams& p, int mode, bool dual) {
+  const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
+  if (mode == MODE_CHAIN) {
+    const uint32_t s1 = round_up(static_cast<uint32_t>(p.N1p), 32u);
+    p.d0_col[0] = 0;
+    p.d0_col[1] = dual ? s0 : 0u;
+    p.d1_col[0] = dual ? 2u * s0 : s0;
+    p.d1_col[1] = dual ? 2u * s0 + s1 : s0;
+    return pow2_at_least(dual ? 2u * (s0 + s1) : s0 + s1);
+  }
+  const uint32_t cols = pow2_at_least(2u * s0);
+  p.d0_col[0] = 0;
+  p.d0_col[1] = cols / 2u;
+  p.d1_col[0] = p.d1_col[1] = 0;
+  return cols;
+}
+
 // Shared-memory plan: ring of A (and, when streamed, weight) chunks; resident weights;
-// P tile; output staging; biases (fp32); barriers.  Fills the offsets of p.  When the
-// output staging shares the P buffer, that buffer is sized for the larger of the two.
+// P tiles; output staging; biases (fp32); barriers.  Candidates are tried in order of
+// preference -- two tiles in flight, resident weights, separate staging -- and the first
+// that leaves at least three ring stages (else two) is taken.  Fills p's layout fields.
 bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_bytes,
                Regions* regions) {
   const uint32_t budget = kSmemLimit - 1024u;   // 1 KiB slack to align the base to 1024
@@ -192,18 +214,36 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   const uint32_t w_res = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes +
                          static_cast<uint32_t>(p.kchunks1) * p.w1_chunk_bytes;
 
-  struct Cand { int resident, alias; };
-  const Cand cands[4] = {{1, 0}, {1, 1}, {0, 0}, {0, 1}};
+  struct Cand { int dual, groups, resident, alias; };
+  Cand cands[8];
+  int ncand = 0;
+  if (mode == MODE_CHAIN) {
+    ChainParams probe = p;
+    const bool tmem_dual_ok = tmem_layout(probe, mode, true) <= 512u;
+    for (int dual = tmem_dual_ok ? 1 : 0; dual >= 0; --dual)
+      for (int resident = 1; resident >= 0; --resident)
+        for (int alias = 0; alias <= 1; ++alias)
+          cands[ncand++] = {dual, dual ? 2 : 1, resident, alias};
+  } else {
+    // Pool staging is small: the warpgroups always take alternate tiles.
+    const int gmin = mode == MODE_POOL ? 2 : 1;
+    for (int resident = 1; resident >= 0; --resident)
+      for (int groups = 2; groups >= gmin; --groups) cands[ncand++] = {1, groups, resident, 0};
+  }
+
   int chosen = -1;
   uint32_t chosen_stages = 0, chosen_stage_bytes = 0;
   for (int min_stages = 3; min_stages >= 2 && chosen < 0; --min_stages) {
-    for (int c = 0; c < 4; ++c) {
-      if (cands[c].alias && mode != MODE_CHAIN) continue;
+    for (int c = 0; c < ncand; ++c) {
+      const Cand& k = cands[c];
       const uint32_t stage_bytes =
-          cands[c].resident ? kABytes
-                            : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
-      const uint32_t shared = cands[c].alias ? std::max(p_bytes, out_bytes) : p_bytes + out_bytes;
-      const uint32_t fixed = (cands[c].resident ? w_res : 0u) + shared + bias_bytes + bar_bytes;
+          k.resident ? kABytes
+                     : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
+      const uint32_t pbufs = mode == MODE_CHAIN ? (k.dual ? 2u : 1u) : 0u;
+      const uint32_t obufs = k.groups == 2 ? 2u : 1u;
+      const uint32_t shared = k.alias ? pbufs * std::max(p_bytes, out_bytes)
+                                      : pbufs * p_bytes + obufs * out_bytes;
+      const uint32_t fixed = (k.resident ? w_res : 0u) + shared + bias_bytes + bar_bytes;
       if (fixed >= budget) continue;
       const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / stage_bytes);
       if (stages < static_cast<uint32_t>(min_stages)) continue;
@@ -214,34 +254,43 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
     }
   }
   if (chosen < 0) return false;
-  p.resident = cands[chosen].resident;
-  p.out_alias_p = cands[chosen].alias;
+  const Cand& k = cands[chosen];
+  p.acc_dual = k.dual;
+  p.epi_groups = k.groups;
+  p.resident = k.resident;
+  p.out_alias_p = k.alias;
   p.num_stages = chosen_stages;
   p.stage_bytes = chosen_stage_bytes;
+  p.tmem_cols = tmem_layout(p, mode, k.dual != 0);
   Regions r;
   r.ring = p.num_stages * p.stage_bytes;
   r.w_res = p.resident ? w_res : 0u;
-  r.p = p.out_alias_p ? std::max(p_bytes, out_bytes) : p_bytes;
-  r.out = p.out_alias_p ? 0u : out_bytes;
+  r.p_each = mode == MODE_CHAIN ? (p.out_alias_p ? std::max(p_bytes, out_bytes) : p_bytes) : 0u;
+  r.out_each = p.out_alias_p ? 0u : out_bytes;
   r.bias = bias_bytes;
   r.bar = bar_bytes;
+  const uint32_t pbufs = mode == MODE_CHAIN ? (k.dual ? 2u : 1u) : 0u;
+  const uint32_t obufs = k.groups == 2 ? 2u : 1u;
   uint32_t off = 0;
   p.off_ring = off;
   off += r.ring;
   p.off_w0 = off;
   p.off_w1 = off + static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
   off += r.w_res;
-  p.off_p = off;
-  off += r.p;
-  p.off_out = p.out_alias_p ? p.off_p : off;
-  off += r.out;
+  for (uint32_t b = 0; b < 2; ++b) p.off_p[b] = off + (b < pbufs ? b : 0u) * r.p_each;
+  off += pbufs * r.p_each;
+  for (uint32_t b = 0; b < 2; ++b) {
+    if (p.out_alias_p) p.off_out[b] = p.off_p[b];
+    else p.off_out[b] = off + (b < obufs ? b : 0u) * r.out_each;
+  }
+  if (!p.out_alias_p) off += obufs * r.out_each;
   p.off_bias = off;
   off += r.bias;
   p.off_bar = off;
   off += r.bar;
   *smem_bytes = off + 1024u;
   if (regions) *regions = r;
-  return *smem_bytes <= kSmemLimit;
+  return *smem_bytes <= kSmemLimit && p.tmem_cols <= 512u;
 }
 
 void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const void* b1,
@@ -254,16 +303,6 @@ void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const v
   p.wait_limit_ns = g_wait_ns.load();
   p.kernel_id = kid;
   p.err = d ? d->err : nullptr;
-}
-
-void set_tmem(ChainParams& p, int mode) {
-  if (mode == MODE_CHAIN) {
-    p.acc_stride = round_up(static_cast<uint32_t>(p.N0p), 32u);
-    p.tmem_cols = pow2_at_least(p.acc_stride + static_cast<uint32_t>(p.N1p));
-  } else {
-    p.tmem_cols = pow2_at_least(2u * static_cast<uint32_t>(p.N0p));
-    p.acc_stride = p.tmem_cols / 2u;
-  }
 }
 
 b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtensorMap& w0,
@@ -305,7 +344,6 @@ bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int
   p.kc_per_tap = p.kchunks0;
   p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
   p.num_tiles = ceil_div(M, kBlockM);
-  set_tmem(p, mode);
   return plan_smem(p, mode, w_mn, w_mn, smem, regions);
 }
 
@@ -332,7 +370,6 @@ bool conv_params(ChainParams& p, int mode, int32_t N, int32_t H, int32_t W, int3
   const int64_t tiles = static_cast<int64_t>(N) * p.tiles_w * p.tiles_h;
   if (tiles > INT32_MAX) return false;
   p.num_tiles = static_cast<int32_t>(tiles);
-  set_tmem(p, mode);
   return plan_smem(p, mode, false, false, smem, regions);
 }
 
@@ -628,7 +665,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   static const int32_t need[5] = {4, 3, 9, 8, 5};
   if (kind < 0 || kind > 4) return B2B_ERR_UNSUPPORTED;
   if (dims == nullptr || out == nullptr) return B2B_ERR_NULL;
-  if (ndims < need[kind] || out_len < 28) return B2B_ERR_SHAPE;
+  if (ndims < need[kind] || out_len < 36) return B2B_ERR_SHAPE;
   for (int i = 0; i < need[kind]; ++i)
     if (dims[i] < 0 || dims[i] > INT32_MAX) return B2B_ERR_SHAPE;
   const int32_t d0 = static_cast<int32_t>(dims[0]), d1 = static_cast<int32_t>(dims[1]),
@@ -676,14 +713,16 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
     }
   }
   if (!ok) return B2B_ERR_UNSUPPORTED;
-  const uint32_t v[28] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[36] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
-                          p.w1_chunk_bytes, p.off_p, r.p, p.off_out, r.out, p.off_bias, r.bias,
-                          p.off_bar, r.bar, p.tmem_cols, p.acc_stride,
+                          p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
+                          p.off_out[1], r.out_each, p.off_bias, r.bias, p.off_bar, r.bar,
+                          p.tmem_cols, p.d0_col[0], p.d0_col[1], p.d1_col[0], p.d1_col[1],
+                          static_cast<uint32_t>(p.acc_dual), static_cast<uint32_t>(p.epi_groups),
                           static_cast<uint32_t>(p.num_tiles), static_cast<uint32_t>(p.kchunks0),
                           static_cast<uint32_t>(p.kchunks1), static_cast<uint32_t>(p.N0p),
-                          static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode)};
+                          static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode), 0u};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

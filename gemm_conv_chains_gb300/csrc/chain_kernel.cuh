@@ -6,7 +6,7 @@
 //
 //   warp 0      TMA producer: A (or one conv tap of x) and weight K-chunks -> smem ring
 //   warp 1      TMEM allocator; lane 0 issues tcgen05.mma (GEMM0 into TMEM, GEMM1 from P)
-//   warps 2..5  epilogue: TMEM -> registers -> bias + activation -> fp16/bf16 ->
+//   warps 2..9  epilogue, two warpgroups: TMEM -> registers -> bias + act -> fp16/bf16 ->
 //               (chain) P tile in shared memory, the operand of GEMM1
 //               ("Shared-memory-resident fusion": the accumulator tile is staged in
 //               shared memory and read back by the second GEMM, Figure 7)
@@ -25,6 +25,13 @@
 //   an 8 x 16 output-pixel tile; coordinates outside the image read as zero, which is the
 //   conv's zero padding.  The box lands in shared memory as 128 rows x 128 B, exactly the
 //   K-major 128B-swizzled layout tcgen05 reads, so no im2col buffer exists anywhere.
+//
+// Two tiles in flight: when TMEM and shared memory allow (acc_dual), tile i uses
+// accumulator / P / staging buffer i & 1 and the two epilogue warpgroups take alternate
+// tiles, so GEMM0 of tile i+2 and GEMM1 of tile i+1 run while the epilogue of tile i
+// drains.  The MMA issue order is G0(0), G0(1), then G1(j), G0(j+2) for j = 0, 1, ...
+// Otherwise (one buffer) it is G0(0), then G1(j), G0(j+1), and both warpgroups split the
+// columns of every tile.
 //
 // Every wait is bounded (see ptx.cuh); on a timeout all roles leave their loops, the MMA
 // issuer drains its MMAs, the producer drains its copies, and TMEM is freed.
@@ -46,9 +53,9 @@ enum : uint32_t {
   BAR_WFULL = 2 * kMaxStages,
   BAR_ACC_FULL0 = BAR_WFULL + 1,
   BAR_ACC_EMPTY0 = BAR_ACC_FULL0 + 2,
-  BAR_P_FULL = BAR_ACC_EMPTY0 + 2,
-  BAR_D1_FULL = BAR_P_FULL + 1,
-  BAR_MMA_DONE = BAR_D1_FULL + 1,
+  BAR_P_FULL0 = BAR_ACC_EMPTY0 + 2,
+  BAR_D1_FULL0 = BAR_P_FULL0 + 2,
+  BAR_MMA_DONE = BAR_D1_FULL0 + 2,
   BAR_COUNT = BAR_MMA_DONE + 1,
 };
 constexpr uint32_t kBarRegionBytes = 512;   // barriers, then TMEM slot and abort flag
@@ -72,6 +79,12 @@ __device__ __forceinline__ TileCoord tile_coord(const ChainParams& p, int32_t t)
     c.m0 = t * kBlockM;
   }
   return c;
+}
+
+// Number of tiles this CTA processes (tiles blockIdx.x, blockIdx.x + gridDim.x, ...).
+__device__ __forceinline__ int local_tiles(const ChainParams& p) {
+  const int b = static_cast<int>(blockIdx.x), g = static_cast<int>(gridDim.x);
+  return b < p.num_tiles ? (p.num_tiles - 1 - b) / g + 1 : 0;
 }
 
 // Number of 16-wide MMA K steps in GEMM0 chunk kc (a partial last chunk is zero-filled
@@ -158,40 +171,55 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
 
   int stage = 0;
   uint32_t phase = 0;
-  for (int32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+  auto acquire = [&](int32_t t) -> bool {   // waits until ring slot `stage` is free
+    return mbar_wait(bars + 8u * (BAR_EMPTY0 + stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
+                     p.err, p.kernel_id, SITE_PRODUCER_EMPTY, t);
+  };
+  auto advance = [&]() {
+    issued |= 1u << stage;
+    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+    if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+  };
+  // A (and streamed W0) chunks of the it-th tile of this CTA.
+  auto load_g0 = [&](int it) -> bool {
+    const int32_t t = blockIdx.x + it * gridDim.x;
     const TileCoord tc = tile_coord<A4D>(p, t);
     for (int kc = 0; kc < p.kchunks0; ++kc) {
-      if (!mbar_wait(bars + 8u * (BAR_EMPTY0 + stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
-                     p.err, p.kernel_id, SITE_PRODUCER_EMPTY, t)) {
-        ok = false;
-        break;
-      }
+      if (!acquire(t)) return false;
       const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
       mbar_arrive_expect_tx(fb, kABytes + (p.resident ? 0u : p.w0_chunk_bytes));
       load_a_chunk<MODE, A4D, W0MN, W1MN>(p, tmA, sbase, tc, kc, fb, pol_stream);
       if (!p.resident) load_w0_chunk<A4D, W0MN>(p, tmW0, sbase + kABytes, kc, fb, pol_keep);
-      issued |= 1u << stage;
-      issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+      advance();
     }
-    if (!ok) break;
-    if (MODE == MODE_CHAIN && !p.resident) {
-      for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
-        if (!mbar_wait(bars + 8u * (BAR_EMPTY0 + stage), phase ^ 1u, p.wait_limit_ns,
-                       abort_flag, p.err, p.kernel_id, SITE_PRODUCER_EMPTY, t)) {
-          ok = false;
-          break;
-        }
-        const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
-        mbar_arrive_expect_tx(fb, p.w1_chunk_bytes);
-        load_w1_chunk<W1MN>(p, tmW1, base + p.off_ring + stage * p.stage_bytes, kc1, fb,
-                            pol_keep);
-        issued |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
-      }
+    return true;
+  };
+  // Streamed W1 chunks for GEMM1 of the it-th tile.
+  auto load_g1 = [&](int it) -> bool {
+    if (MODE != MODE_CHAIN || p.resident) return true;
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
+      if (!acquire(t)) return false;
+      const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
+      mbar_arrive_expect_tx(fb, p.w1_chunk_bytes);
+      load_w1_chunk<W1MN>(p, tmW1, base + p.off_ring + stage * p.stage_bytes, kc1, fb, pol_keep);
+      advance();
     }
+    return true;
+  };
+
+  const int ntiles = local_tiles(p);
+  if (MODE == MODE_CHAIN) {
+    // Same order as the MMA issuer consumes: G0(0..L-1), then G1(j), G0(j+L).
+    const int L = p.acc_dual ? 2 : 1;
+    for (int it = 0; ok && it < L && it < ntiles; ++it) ok = load_g0(it);
+    for (int j = 0; ok && j < ntiles; ++j) {
+      ok = load_g1(j);
+      if (ok && j + L < ntiles) ok = load_g0(j + L);
+    }
+  } else {
+    for (int it = 0; ok && it < ntiles; ++it) ok = load_g0(it);
   }
 
   if (!ok) {
@@ -222,30 +250,25 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
 
   int stage = 0;
   uint32_t phase = 0;
-  int it = 0;
-  for (int32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
-    uint32_t d0 = tmem_base;
-    uint32_t acc_full = bars + 8u * BAR_ACC_FULL0;
+  const int ntiles = local_tiles(p);
+
+  // GEMM0 of the it-th tile: D0[b] = A . W0 over all K chunks; commits ACC_FULL[b].
+  auto issue_g0 = [&](int it) -> bool {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    const uint32_t b = (MODE != MODE_CHAIN || p.acc_dual) ? static_cast<uint32_t>(it & 1) : 0u;
     if (MODE != MODE_CHAIN) {
-      // Two accumulator buffers: GEMM(i+1) runs while the epilogue drains buffer i.
-      const uint32_t as = it & 1;
-      if (!mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + as), ((it >> 1) & 1) ^ 1u, p.wait_limit_ns,
-                     abort_flag, p.err, p.kernel_id, SITE_MMA_ACC_EMPTY, t)) {
-        ok = false;
-        break;
-      }
-      d0 = tmem_base + as * p.acc_stride;
-      acc_full = bars + 8u * (BAR_ACC_FULL0 + as);
+      // The epilogue must have drained the buffer's previous tile.
+      const uint32_t u = static_cast<uint32_t>(it >> 1);
+      if (!mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), (u & 1u) ^ 1u, p.wait_limit_ns,
+                     abort_flag, p.err, p.kernel_id, SITE_MMA_ACC_EMPTY, t))
+        return false;
     }
     tc_fence_after_sync();
-
-    // GEMM0: D0 = A . W0 over all K chunks.
+    const uint32_t d0 = tmem_base + p.d0_col[b];
     for (int kc = 0; kc < p.kchunks0; ++kc) {
-      if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag,
-                     p.err, p.kernel_id, SITE_MMA_FULL, t)) {
-        ok = false;
-        break;
-      }
+      if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag, p.err,
+                     p.kernel_id, SITE_MMA_FULL, t))
+        return false;
       tc_fence_after_sync();
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
       const uint32_t wbase =
@@ -260,47 +283,61 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       mma_commit(bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
       if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
     }
-    if (!ok) break;
-    mma_commit(acc_full);
+    mma_commit(bars + 8u * (BAR_ACC_FULL0 + b));
+    return true;
+  };
 
+  // GEMM1 of the j-th tile: D1[b] = P[b] . W1, P[b] being the epilogue's fp16/bf16 tile.
+  auto issue_g1 = [&](int j) -> bool {
+    const int32_t t = blockIdx.x + j * gridDim.x;
+    const uint32_t b = p.acc_dual ? static_cast<uint32_t>(j & 1) : 0u;
+    const uint32_t u = p.acc_dual ? static_cast<uint32_t>(j >> 1) : static_cast<uint32_t>(j);
+    if (!mbar_wait(bars + 8u * (BAR_P_FULL0 + b), u & 1u, p.wait_limit_ns, abort_flag, p.err,
+                   p.kernel_id, SITE_MMA_P_FULL, t))
+      return false;
+    tc_fence_after_sync();
+    const uint32_t d1 = tmem_base + p.d1_col[b];
+    for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
+      uint32_t w1base;
+      if (p.resident) {
+        w1base = base + p.off_w1 + kc1 * p.w1_chunk_bytes;
+      } else {
+        if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag, p.err,
+                       p.kernel_id, SITE_MMA_FULL, t))
+          return false;
+        tc_fence_after_sync();
+        w1base = base + p.off_ring + stage * p.stage_bytes;
+      }
+      const uint32_t pbase = base + p.off_p[b] + kc1 * kPChunkBytes;
+      const int rem = p.N0p - kc1 * kChunkK;
+      const int nks = rem >= 64 ? 4 : (rem >> 4);
+      for (int ks = 0; ks < nks; ++ks) {
+        const uint64_t adesc = sdesc_sw128(pbase + ks * 32u, 16u, 1024u);
+        const uint64_t bdesc = W1MN ? sdesc_sw128(w1base + ks * 2048u, 8192u, 1024u)
+                                    : sdesc_sw128(w1base + ks * 32u, 16u, 1024u);
+        mma_f16_ss(d1, adesc, bdesc, idesc1, (kc1 | ks) != 0 ? 1u : 0u);
+      }
+      if (!p.resident) {
+        mma_commit(bars + 8u * (BAR_EMPTY0 + stage));
+        if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+      }
+    }
+    mma_commit(bars + 8u * (BAR_D1_FULL0 + b));
+    return true;
+  };
+
+  if (ok) {
     if (MODE == MODE_CHAIN) {
-      // GEMM1: D1 = P . W1, P being the epilogue's fp16/bf16 tile in shared memory.
-      if (!mbar_wait(bars + 8u * BAR_P_FULL, it & 1, p.wait_limit_ns, abort_flag, p.err, p.kernel_id,
-                     SITE_MMA_P_FULL, t)) {
-        ok = false;
-        break;
+      // A D0 buffer is free again once the epilogue has published that tile's P, so
+      // G0(j+L) follows G1(j); with two buffers (L = 2) two tiles are in flight.
+      const int L = p.acc_dual ? 2 : 1;
+      for (int it = 0; ok && it < L && it < ntiles; ++it) ok = issue_g0(it);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        ok = issue_g1(j);
+        if (ok && j + L < ntiles) ok = issue_g0(j + L);
       }
-      tc_fence_after_sync();
-      const uint32_t d1 = tmem_base + p.acc_stride;
-      for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
-        uint32_t w1base;
-        if (p.resident) {
-          w1base = base + p.off_w1 + kc1 * p.w1_chunk_bytes;
-        } else {
-          if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag,
-                         p.err, p.kernel_id, SITE_MMA_FULL, t)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          w1base = base + p.off_ring + stage * p.stage_bytes;
-        }
-        const uint32_t pbase = base + p.off_p + kc1 * kPChunkBytes;
-        const int rem = p.N0p - kc1 * kChunkK;
-        const int nks = rem >= 64 ? 4 : (rem >> 4);
-        for (int ks = 0; ks < nks; ++ks) {
-          const uint64_t adesc = sdesc_sw128(pbase + ks * 32u, 16u, 1024u);
-          const uint64_t bdesc = W1MN ? sdesc_sw128(w1base + ks * 2048u, 8192u, 1024u)
-                                      : sdesc_sw128(w1base + ks * 32u, 16u, 1024u);
-          mma_f16_ss(d1, adesc, bdesc, idesc1, (kc1 | ks) != 0 ? 1u : 0u);
-        }
-        if (!p.resident) {
-          mma_commit(bars + 8u * (BAR_EMPTY0 + stage));
-          if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
-        }
-      }
-      if (!ok) break;
-      mma_commit(bars + 8u * BAR_D1_FULL);
+    } else {
+      for (int it = 0; ok && it < ntiles; ++it) ok = issue_g0(it);
     }
   }
   // Whatever happened, no MMA may still be running when TMEM is released.
@@ -315,7 +352,9 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
 template <int ACT>
 __device__ __forceinline__ float act_fn(float x) {
   if constexpr (ACT == 1) return fmaxf(x, 0.0f);
-  if constexpr (ACT == 2) return x * fminf(fmaxf(x + 3.0f, 0.0f), 6.0f) * (1.0f / 6.0f);
+  // hardswish(x) = x * min(max(x + 3, 0), 6) / 6 = x * clamp(x / 6 + 1/2, 0, 1):
+  // one fused multiply-add with saturation and one multiply.
+  if constexpr (ACT == 2) return x * __saturatef(fmaf(x, 1.0f / 6.0f, 0.5f));
   return x;
 }
 
@@ -351,20 +390,24 @@ __device__ __forceinline__ void st_row16_sw128(uint32_t tile, int row, int c0,
 template <bool BF16, int ACT>
 __device__ __forceinline__ void convert16(const uint32_t (&r)[16], const float* bias, int c,
                                           uint32_t (&out)[8]) {
+  const float4* b4 = reinterpret_cast<const float4*>(bias + c);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float lo = act_fn<ACT>(__uint_as_float(r[2 * j]) + bias[c + 2 * j]);
-    const float hi = act_fn<ACT>(__uint_as_float(r[2 * j + 1]) + bias[c + 2 * j + 1]);
-    out[j] = pack2<BF16>(lo, hi);
+  for (int q = 0; q < 4; ++q) {
+    const float4 bb = b4[q];
+    out[2 * q] = pack2<BF16>(act_fn<ACT>(__uint_as_float(r[4 * q]) + bb.x),
+                             act_fn<ACT>(__uint_as_float(r[4 * q + 1]) + bb.y));
+    out[2 * q + 1] = pack2<BF16>(act_fn<ACT>(__uint_as_float(r[4 * q + 2]) + bb.z),
+                                 act_fn<ACT>(__uint_as_float(r[4 * q + 3]) + bb.w));
   }
 }
 
-// TMEM columns [col0, col0 + ncols) of this thread's row -> bias -> act -> dtype -> smem.
+// TMEM columns [col0 + c, col0 + c + 32) for c = c_first, c_first + c_step, ... below
+// ncols, of this thread's row -> bias -> act -> dtype -> smem tile.
 template <bool BF16, int ACT>
-__device__ __forceinline__ void drain_to_smem(uint32_t tm_lane, uint32_t col0, int ncols,
-                                              const float* bias, uint32_t tile, int row,
-                                              uint32_t chunk_bytes) {
-  for (int c = 0; c < ncols; c += 32) {
+__device__ __forceinline__ void drain_to_smem(uint32_t tm_lane, uint32_t col0, int c_first,
+                                              int c_step, int ncols, const float* bias,
+                                              uint32_t tile, int row, uint32_t chunk_bytes) {
+  for (int c = c_first; c < ncols; c += c_step) {
     uint32_t r0[16], r1[16];
     uint32_t v[8];
     const bool two = c + 16 < ncols;
@@ -382,14 +425,15 @@ __device__ __forceinline__ void drain_to_smem(uint32_t tm_lane, uint32_t col0, i
 
 template <bool BF16>
 __device__ __forceinline__ void drain_to_smem_act(int act, uint32_t tm_lane, uint32_t col0,
-                                                  int ncols, const float* bias, uint32_t tile,
-                                                  int row, uint32_t chunk_bytes) {
+                                                  int c_first, int c_step, int ncols,
+                                                  const float* bias, uint32_t tile, int row,
+                                                  uint32_t chunk_bytes) {
   if (act == 1)
-    drain_to_smem<BF16, 1>(tm_lane, col0, ncols, bias, tile, row, chunk_bytes);
+    drain_to_smem<BF16, 1>(tm_lane, col0, c_first, c_step, ncols, bias, tile, row, chunk_bytes);
   else if (act == 2)
-    drain_to_smem<BF16, 2>(tm_lane, col0, ncols, bias, tile, row, chunk_bytes);
+    drain_to_smem<BF16, 2>(tm_lane, col0, c_first, c_step, ncols, bias, tile, row, chunk_bytes);
   else
-    drain_to_smem<BF16, 0>(tm_lane, col0, ncols, bias, tile, row, chunk_bytes);
+    drain_to_smem<BF16, 0>(tm_lane, col0, c_first, c_step, ncols, bias, tile, row, chunk_bytes);
 }
 
 // Pool epilogue.  Tile row = 16 * h + w over an 8 x 16 conv-output tile, so warp q holds
@@ -445,73 +489,88 @@ __device__ __forceinline__ bool warp_wait(bool alive, uint32_t bar, uint32_t par
   return __all_sync(0xffffffffu, ok);
 }
 
+// Epilogue warps.  With epi_groups == 2 warpgroup g (warps 2+4g .. 5+4g) takes the
+// CTA's tiles i with i & 1 == g and owns buffer g; with epi_groups == 1 all eight warps
+// take every tile and warpgroup g drains the 32-column blocks 2k + g.
 template <int MODE, bool A4D, bool BF16>
 __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, uint32_t base,
                               uint32_t bars, uint32_t tmem_base, const float* bias_s,
                               volatile uint32_t* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+  const int wg = (warp - 2) >> 2;             // warpgroup 0 or 1
+  const int q = warp & 3;                     // TMEM lane quadrant this warp may access
   const int row = q * 32 + lane;
   const uint32_t tm_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-  const bool elected = threadIdx.x == 64;
-  const uint32_t p_tile = base + p.off_p;
-  const uint32_t out_tile = base + p.off_out;
+  const int groups = p.epi_groups;
+  const int g = groups == 2 ? wg : 0;         // which tiles
+  const int c_first = groups == 2 ? 0 : 32 * wg;   // which columns
+  const int c_step = groups == 2 ? 32 : 64;
+  const uint32_t group_threads = static_cast<uint32_t>(kNumEpiThreads / groups);
+  const uint32_t bar_id = 1u + static_cast<uint32_t>(g);
+  const bool elected = threadIdx.x == 64 + g * static_cast<int>(group_threads);
+  const bool dual = MODE != MODE_CHAIN || p.acc_dual;
   bool alive = true;
-  int it = 0;
 
-  for (int32_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+  const int ntiles = local_tiles(p);
+  for (int it = g; it < ntiles; it += groups) {
+    const int32_t t = blockIdx.x + it * gridDim.x;
     const TileCoord tc = tile_coord<A4D>(p, t);
+    const uint32_t b = dual ? static_cast<uint32_t>(it & 1) : 0u;
+    const uint32_t u = dual ? static_cast<uint32_t>(it >> 1) : static_cast<uint32_t>(it);
+    const uint32_t sb = groups == 2 ? static_cast<uint32_t>(g) : 0u;   // staging buffer
+    const uint32_t out_tile = base + p.off_out[sb];
     if (MODE == MODE_CHAIN) {
-      alive = warp_wait(alive, bars + 8u * BAR_ACC_FULL0, it & 1, p, abort_flag,
+      const uint32_t p_tile = base + p.off_p[b];
+      alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_ACC_FULL, t);
       tc_fence_after_sync();
-      if (p.out_alias_p) {   // P doubles as the previous tile's output staging
+      if (p.out_alias_p) {   // P[b] doubles as this group's previous output staging
         if (elected) bulk_wait_read_all();
-        named_bar_sync(1, kNumEpiThreads);
+        named_bar_sync(bar_id, group_threads);
       }
       if (alive)
-        drain_to_smem_act<BF16>(p.act0, tm_lane, 0, p.N0p, bias_s, p_tile, row, kPChunkBytes);
+        drain_to_smem_act<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, bias_s,
+                                p_tile, row, kPChunkBytes);
       tc_fence_before_sync();
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8u * BAR_P_FULL);
+      if (lane == 0) mbar_arrive(bars + 8u * (BAR_P_FULL0 + b));
 
-      alive = warp_wait(alive, bars + 8u * BAR_D1_FULL, it & 1, p, abort_flag,
+      alive = warp_wait(alive, bars + 8u * (BAR_D1_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_D1_FULL, t);
       tc_fence_after_sync();
       if (!p.out_alias_p) {
         if (elected) bulk_wait_read_all();
-        named_bar_sync(1, kNumEpiThreads);
+        named_bar_sync(bar_id, group_threads);
       }
       if (alive)
-        drain_to_smem_act<BF16>(p.act1, tm_lane, p.acc_stride, p.N1p, bias_s + p.N0p, out_tile, row,
-                                kPChunkBytes);
+        drain_to_smem_act<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p,
+                                bias_s + p.N0p, out_tile, row, kPChunkBytes);
       tc_fence_before_sync();
       fence_proxy_async_smem();
-      named_bar_sync(1, kNumEpiThreads);
+      named_bar_sync(bar_id, group_threads);
       if (elected && !*abort_flag) {
         store_tile<A4D>(tmOut, out_tile, (p.N1p + 63) >> 6, tc);
         bulk_commit_group();
       }
     } else {
-      const uint32_t as = it & 1;
-      alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + as), (it >> 1) & 1, p, abort_flag,
+      alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_ACC_FULL, t);
       tc_fence_after_sync();
-      if (elected) bulk_wait_read_all();   // staging free again
-      named_bar_sync(1, kNumEpiThreads);
+      if (elected) bulk_wait_read_all();   // this group's staging is free again
+      named_bar_sync(bar_id, group_threads);
       if (alive) {
         if (MODE == MODE_POOL)
-          drain_pool<BF16>(tm_lane, as * p.acc_stride, p.N0p, bias_s, out_tile, q, lane);
+          drain_pool<BF16>(tm_lane, p.d0_col[b], p.N0p, bias_s, out_tile, q, lane);
         else
-          drain_to_smem_act<BF16>(p.act0, tm_lane, as * p.acc_stride, p.N0p, bias_s, out_tile, row,
-                                  kPChunkBytes);
+          drain_to_smem_act<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, bias_s,
+                                  out_tile, row, kPChunkBytes);
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + as));
+      if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + b));
       fence_proxy_async_smem();
-      named_bar_sync(1, kNumEpiThreads);
+      named_bar_sync(bar_id, group_threads);
       if (elected && !*abort_flag) {
         if (MODE == MODE_POOL) {
           const int nch = (p.N0p + 63) >> 6;
@@ -546,6 +605,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   float* bias_s = reinterpret_cast<float*>(base_ptr + p.off_bias);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t warps_per_group = static_cast<uint32_t>(kNumEpiWarps / p.epi_groups);
 
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < p.num_stages; ++s) {
@@ -555,10 +615,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     mbar_init(bars + 8u * BAR_WFULL, 1);
     for (uint32_t a = 0; a < 2; ++a) {
       mbar_init(bars + 8u * (BAR_ACC_FULL0 + a), 1);
-      mbar_init(bars + 8u * (BAR_ACC_EMPTY0 + a), kNumEpiThreads / 32);
+      mbar_init(bars + 8u * (BAR_ACC_EMPTY0 + a), warps_per_group);
+      mbar_init(bars + 8u * (BAR_P_FULL0 + a), warps_per_group);
+      mbar_init(bars + 8u * (BAR_D1_FULL0 + a), 1);
     }
-    mbar_init(bars + 8u * BAR_P_FULL, kNumEpiThreads / 32);
-    mbar_init(bars + 8u * BAR_D1_FULL, 1);
     mbar_init(bars + 8u * BAR_MMA_DONE, 1);
     *abort_flag = 0u;
     fence_barrier_init();

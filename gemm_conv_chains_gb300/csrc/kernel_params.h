@@ -40,8 +40,9 @@ enum WaitSite : uint32_t {
 
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M
 constexpr int kChunkK = 64;           // K elements per staged chunk (128 B rows, SW128)
-constexpr int kNumThreads = 192;      // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr int kNumEpiThreads = 128;
+constexpr int kNumEpiWarps = 8;       // two warpgroups of four (one per TMEM lane quadrant)
+constexpr int kNumEpiThreads = 32 * kNumEpiWarps;
+constexpr int kNumThreads = 64 + kNumEpiThreads;   // warp 0 TMA, warp 1 MMA + TMEM, 2..9 epilogue
 constexpr int kMaxStages = 8;
 constexpr uint32_t kABytes = kBlockM * kChunkK * 2;   // 16 KiB A chunk
 constexpr uint32_t kPChunkBytes = kBlockM * 128;      // 128 rows x 64 cols x 2 B
@@ -68,11 +69,15 @@ struct ChainParams {
   uint32_t off_ring, stage_bytes, num_stages;
   uint32_t w0_chunk_bytes, w1_chunk_bytes;
   uint32_t off_w0, off_w1;      // resident weights (resident != 0)
-  uint32_t off_p, off_out, off_bias, off_bar;
+  uint32_t off_p[2], off_out[2], off_bias, off_bar;
   int32_t resident;             // 1: W0/W1 loaded once per CTA; 0: streamed per tile
-  int32_t out_alias_p;          // 1: output staging shares the P buffer
+  int32_t out_alias_p;          // 1: output staging b shares P buffer b
+  int32_t acc_dual;             // 1: accumulators (and, chained, P) double-buffered:
+                                //    tile i uses buffer i & 1, two tiles in flight
+  int32_t epi_groups;           // 2: the epilogue warpgroups take alternate tiles;
+                                // 1: both warpgroups split the columns of every tile
   uint32_t tmem_cols;
-  uint32_t acc_stride;          // TMEM column of D1 (chain) / of accumulator buffer 1
+  uint32_t d0_col[2], d1_col[2];  // TMEM columns of GEMM0 / GEMM1 accumulator buffers
   uint64_t wait_limit_ns;
   uint32_t kernel_id;
   uint32_t* err;                // device error word {code, kernel, site, tile}

@@ -172,12 +172,14 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1}
  *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
- * out (out_len >= 28) receives, in order: dynamic smem bytes, ring stages, stage bytes,
- * weights resident (0/1), output staging aliases P (0/1), then (offset, bytes) of the
- * ring, the resident-weight region start, the W1 offset, resident bytes, W0 chunk bytes,
- * W1 chunk bytes, (offset, bytes) of P, of the output staging, of the biases and of the
- * barriers, TMEM columns, TMEM accumulator stride, tiles, GEMM0 K chunks, GEMM1 K chunks,
- * padded N0, padded N1, and the kernel mode (0 chain, 1 single, 2 pool).
+ * out (out_len >= 36) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
+ * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
+ * P offsets [2], bytes per P buffer, staging offsets [2], bytes per staging buffer,
+ * bias offset, bias bytes, barrier offset, barrier bytes, TMEM columns, GEMM0 accumulator
+ * columns [2], GEMM1 accumulator columns [2], two tiles in flight (0/1), epilogue groups
+ * (1/2), tiles, GEMM0 K chunks, GEMM1 K chunks, padded N0, padded N1, kernel mode
+ * (0 chain, 1 single, 2 pool), 0.
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,

@@ -16,9 +16,10 @@ from gemm_conv_chains_gb300 import ops
 from gemm_conv_chains_gb300 import workloads as wl
 
 FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "ring", "off_w0",
-          "off_w1", "w_res", "w0_chunk", "w1_chunk", "off_p", "p", "off_out", "out", "off_bias",
-          "bias", "off_bar", "bar", "tmem_cols", "acc_stride", "tiles", "kchunks0", "kchunks1",
-          "N0p", "N1p", "mode"]
+          "off_w1", "w_res", "w0_chunk", "w1_chunk", "off_p0", "off_p1", "p", "off_out0",
+          "off_out1", "out", "off_bias", "bias", "off_bar", "bar", "tmem_cols", "d0_col0",
+          "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0", "kchunks1",
+          "N0p", "N1p", "mode", "zero"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4}
@@ -26,8 +27,8 @@ KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nh
 
 def plan(kind, dims):
     arr = (ctypes.c_int64 * len(dims))(*dims)
-    out = (ctypes.c_uint32 * 28)()
-    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 28)
+    out = (ctypes.c_uint32 * 36)()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 36)
     return st, dict(zip(FIELDS, list(out)))
 
 
@@ -59,30 +60,51 @@ def check(kind, dims, row_major_w):
         assert p["w_res"] >= p["kchunks0"] * w0_chunk + p["kchunks1"] * w1_chunk
         assert p["off_w1"] == p["off_w0"] + p["kchunks0"] * w0_chunk
         regions.append(("w", p["off_w0"], p["w_res"]))
+    dual = p["dual"] == 1
+    groups = p["groups"]
+    assert groups in (1, 2) and (groups == 1 or dual)
+    if mode == 2:
+        assert groups == 2                       # the pool epilogue needs whole rows per warp
+    # P buffers used: tile i -> P[i & 1] when dual, else P[0]
+    pbufs = (2 if dual else 1) if mode == 0 else 0
+    obufs = 2 if groups == 2 else 1
     if mode == 0:
         need_p = max(p_need, out_need) if p["alias"] else p_need
         assert p["p"] >= need_p
-        regions.append(("p", p["off_p"], p["p"]))
+        for b in range(pbufs):
+            regions.append((f"p{b}", p[f"off_p{b}"], p["p"]))
     if p["alias"]:
-        assert mode == 0 and p["off_out"] == p["off_p"]
+        assert mode == 0
+        # staging b (used by epilogue group b, which handles the tiles using P[b])
+        for b in range(obufs):
+            assert p[f"off_out{b}"] == p[f"off_p{b if dual else 0}"]
     else:
         assert p["out"] >= out_need
-        regions.append(("out", p["off_out"], p["out"]))
+        for b in range(obufs):
+            regions.append((f"out{b}", p[f"off_out{b}"], p["out"]))
     assert p["bias"] >= 4 * (N0p + N1p)
-    assert p["bar"] >= 8 * 24 + 8
+    assert p["bar"] >= 8 * 26 + 8
     usable = p["smem"] - 1024                    # the rest aligns the base to 1024
     for name, off, size in regions:
         assert off % 1024 == 0, name
         assert off + size <= usable, (name, off, size, usable)
     for (a, oa, sa), (b, ob, sb) in itertools.combinations(regions, 2):
         assert oa + sa <= ob or ob + sb <= oa, (a, b)
-    # TMEM
+    # TMEM: every accumulator buffer in range, 32-column aligned, distinct buffers disjoint
     assert p["tmem_cols"] in (32, 64, 128, 256, 512)
-    assert p["acc_stride"] >= N0p
-    if mode == 0:
-        assert p["acc_stride"] + N1p <= p["tmem_cols"]
+    accs = [("d0_0", p["d0_col0"], N0p)]
+    if mode != 0 or dual:
+        accs.append(("d0_1", p["d0_col1"], N0p))
     else:
-        assert 2 * p["acc_stride"] <= p["tmem_cols"]
+        assert p["d0_col1"] == p["d0_col0"]
+    if mode == 0:
+        accs.append(("d1_0", p["d1_col0"], N1p))
+        if dual:
+            accs.append(("d1_1", p["d1_col1"], N1p))
+    for name, col, n in accs:
+        assert col % 32 == 0 and col + n <= p["tmem_cols"], (name, col, n)
+    for (a, ca, na), (b, cb, nb) in itertools.combinations(accs, 2):
+        assert ca + na <= cb or cb + nb <= ca, (a, b)
     assert N0p % 16 == 0 and 16 <= N0p <= 256 and N1p % 16 == 0 and N1p <= 256
     return p
 
@@ -107,6 +129,15 @@ def test_b2b_gemm_plan_sweep():
 def test_ffn_plan_streams_weights():
     p = check("b2b_gemm", (32768, 256, 256, 128), True)
     assert p["resident"] == 0      # 192 KiB of weights plus a 64 KiB P tile cannot all stay
+    assert p["dual"] == 0          # 2 x (256 + 128) accumulator columns exceed 512
+
+
+def test_small_chains_keep_two_tiles_in_flight():
+    for dims in ((200704, 64, 64, 64), (1024, 64, 64, 64)):
+        p = check("b2b_gemm", dims, True)
+        assert p["dual"] == 1 and p["groups"] == 2 and p["resident"] == 1
+    p = check("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128), False)
+    assert p["dual"] == 1 and p["resident"] == 1
 
 
 @pytest.mark.parametrize("dims", [(1000, 64, 64), (513, 256, 256), (130, 24, 40), (1, 8, 256)])
