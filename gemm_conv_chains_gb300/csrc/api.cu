@@ -40,6 +40,11 @@ struct DeviceState {
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
+// Optional event trace (b2b_set_trace): caller-owned device buffer, read by later launches.
+std::mutex g_trace_mu;
+unsigned long long* g_trace_buf = nullptr;
+uint32_t g_trace_cap = 0, g_trace_cta = 0;
+
 DeviceState* device_state(b2b_status* st) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -303,6 +308,10 @@ void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const v
   p.wait_limit_ns = g_wait_ns.load();
   p.kernel_id = kid;
   p.err = d ? d->err : nullptr;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  p.trace = g_trace_buf;
+  p.trace_cap = g_trace_cap;
+  p.trace_cta = g_trace_cta;
 }
 
 b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtensorMap& w0,
@@ -639,6 +648,15 @@ int32_t b2b_num_sms(void) {
 }
 
 void b2b_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns); }
+
+b2b_status b2b_set_trace(void* buf, uint32_t capacity, uint32_t cta) {
+  if (buf != nullptr && (reinterpret_cast<uintptr_t>(buf) & 7u) != 0) return B2B_ERR_ALIGN;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_buf = static_cast<unsigned long long*>(buf);
+  g_trace_cap = buf ? capacity : 0u;
+  g_trace_cta = cta;
+  return B2B_OK;
+}
 
 b2b_status b2b_get_device_error(uint32_t info[4]) {
   b2b_status st = B2B_OK;

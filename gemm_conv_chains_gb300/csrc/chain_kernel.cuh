@@ -81,6 +81,17 @@ __device__ __forceinline__ TileCoord tile_coord(const ChainParams& p, int32_t t)
   return c;
 }
 
+// Optional event trace of one CTA: slot 0 counts events; event i occupies slots
+// 2i+1 (clock64) and 2i+2 (code | group << 8 | tile index << 16).
+__device__ __forceinline__ void trace(const ChainParams& p, uint32_t code, uint32_t group,
+                                      int it) {
+  if (p.trace == nullptr || blockIdx.x != p.trace_cta) return;
+  const unsigned long long idx = atomicAdd(p.trace, 1ull);
+  if (idx >= p.trace_cap) return;
+  p.trace[2 * idx + 1] = static_cast<unsigned long long>(clock64());
+  p.trace[2 * idx + 2] = code | (group << 8) | (static_cast<unsigned long long>(it) << 16);
+}
+
 // Number of tiles this CTA processes (tiles blockIdx.x, blockIdx.x + gridDim.x, ...).
 __device__ __forceinline__ int local_tiles(const ChainParams& p) {
   const int b = static_cast<int>(blockIdx.x), g = static_cast<int>(gridDim.x);
@@ -186,11 +197,13 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     const TileCoord tc = tile_coord<A4D>(p, t);
     for (int kc = 0; kc < p.kchunks0; ++kc) {
       if (!acquire(t)) return false;
+      trace(p, EV_PROD_ACQUIRE, kc, it);
       const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
       mbar_arrive_expect_tx(fb, kABytes + (p.resident ? 0u : p.w0_chunk_bytes));
       load_a_chunk<MODE, A4D, W0MN, W1MN>(p, tmA, sbase, tc, kc, fb, pol_stream);
       if (!p.resident) load_w0_chunk<A4D, W0MN>(p, tmW0, sbase + kABytes, kc, fb, pol_keep);
+      trace(p, EV_PROD_ISSUED, kc, it);
       advance();
     }
     return true;
@@ -262,6 +275,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       if (!mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), (u & 1u) ^ 1u, p.wait_limit_ns,
                      abort_flag, p.err, p.kernel_id, SITE_MMA_ACC_EMPTY, t))
         return false;
+      trace(p, EV_MMA_ACC_FREE, b, it);
     }
     tc_fence_after_sync();
     const uint32_t d0 = tmem_base + p.d0_col[b];
@@ -269,6 +283,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag, p.err,
                      p.kernel_id, SITE_MMA_FULL, t))
         return false;
+      trace(p, EV_MMA_FULL, kc, it);
       tc_fence_after_sync();
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
       const uint32_t wbase =
@@ -284,6 +299,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
     }
     mma_commit(bars + 8u * (BAR_ACC_FULL0 + b));
+    trace(p, EV_MMA_G0_DONE, b, it);
     return true;
   };
 
@@ -295,6 +311,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     if (!mbar_wait(bars + 8u * (BAR_P_FULL0 + b), u & 1u, p.wait_limit_ns, abort_flag, p.err,
                    p.kernel_id, SITE_MMA_P_FULL, t))
       return false;
+    trace(p, EV_MMA_P_READY, b, j);
     tc_fence_after_sync();
     const uint32_t d1 = tmem_base + p.d1_col[b];
     for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
@@ -323,6 +340,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       }
     }
     mma_commit(bars + 8u * (BAR_D1_FULL0 + b));
+    trace(p, EV_MMA_G1_DONE, b, j);
     return true;
   };
 
@@ -523,6 +541,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       const uint32_t p_tile = base + p.off_p[b];
       alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_ACC_FULL, t);
+      if (elected) trace(p, EV_EPI_ACC_READY, g, it);
       tc_fence_after_sync();
       if (p.out_alias_p) {   // P[b] doubles as this group's previous output staging
         if (elected) bulk_wait_read_all();
@@ -535,14 +554,17 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8u * (BAR_P_FULL0 + b));
+      if (elected) trace(p, EV_EPI_P_DONE, g, it);
 
       alive = warp_wait(alive, bars + 8u * (BAR_D1_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_D1_FULL, t);
+      if (elected) trace(p, EV_EPI_D1_READY, g, it);
       tc_fence_after_sync();
       if (!p.out_alias_p) {
         if (elected) bulk_wait_read_all();
         named_bar_sync(bar_id, group_threads);
       }
+      if (elected) trace(p, EV_EPI_STAGING, g, it);
       if (alive)
         drain_to_smem_act<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p,
                                 bias_s + p.N0p, out_tile, row, kPChunkBytes);
@@ -552,13 +574,16 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       if (elected && !*abort_flag) {
         store_tile<A4D>(tmOut, out_tile, (p.N1p + 63) >> 6, tc);
         bulk_commit_group();
+        trace(p, EV_EPI_STORED, g, it);
       }
     } else {
       alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_ACC_FULL, t);
+      if (elected) trace(p, EV_EPI_ACC_READY, g, it);
       tc_fence_after_sync();
       if (elected) bulk_wait_read_all();   // this group's staging is free again
       named_bar_sync(bar_id, group_threads);
+      if (elected) trace(p, EV_EPI_STAGING, g, it);
       if (alive) {
         if (MODE == MODE_POOL)
           drain_pool<BF16>(tm_lane, p.d0_col[b], p.N0p, bias_s, out_tile, q, lane);
@@ -581,6 +606,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
           store_tile<A4D>(tmOut, out_tile, (p.N0p + 63) >> 6, tc);
         }
         bulk_commit_group();
+        trace(p, EV_EPI_STORED, g, it);
       }
     }
   }

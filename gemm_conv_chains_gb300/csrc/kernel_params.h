@@ -38,6 +38,22 @@ enum WaitSite : uint32_t {
   SITE_PROBE = 10,
 };
 
+// Events of the optional trace: one CTA's roles stamp clock64() at these points.
+enum TraceEvent : uint32_t {
+  EV_PROD_ACQUIRE = 1,   // producer got a free ring slot
+  EV_PROD_ISSUED = 2,    // producer issued the slot's TMA loads
+  EV_MMA_FULL = 3,       // MMA issuer saw a ring slot filled
+  EV_MMA_G0_DONE = 4,    // GEMM0 of a tile issued and committed
+  EV_MMA_P_READY = 5,    // MMA issuer saw a P tile published
+  EV_MMA_G1_DONE = 6,    // GEMM1 of a tile issued and committed
+  EV_MMA_ACC_FREE = 7,   // MMA issuer saw an accumulator drained (single/pool)
+  EV_EPI_ACC_READY = 8,  // epilogue group saw GEMM0's accumulator complete
+  EV_EPI_P_DONE = 9,     // epilogue group published P
+  EV_EPI_D1_READY = 10,  // epilogue group saw GEMM1's accumulator complete
+  EV_EPI_STAGING = 11,   // epilogue group's output staging free
+  EV_EPI_STORED = 12,    // epilogue group issued the tile's TMA store
+};
+
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M
 constexpr int kChunkK = 64;           // K elements per staged chunk (128 B rows, SW128)
 constexpr int kNumEpiWarps = 8;       // two warpgroups of four (one per TMEM lane quadrant)
@@ -81,6 +97,9 @@ struct ChainParams {
   uint64_t wait_limit_ns;
   uint32_t kernel_id;
   uint32_t* err;                // device error word {code, kernel, site, tile}
+  unsigned long long* trace;    // optional event trace (see TraceEvent), or null
+  uint32_t trace_cap;           // capacity of `trace` in events
+  uint32_t trace_cta;           // the CTA whose events are recorded
 };
 
 }  // namespace b2b
