@@ -5,7 +5,8 @@
 // residence": ThreadBlock_N = GEMM_N), so GEMM1 never needs another block's data:
 //
 //   warp 0      TMA producer: A (or one conv tap of x) and weight K-chunks -> smem ring
-//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma (GEMM0 into TMEM, GEMM1 from P)
+//   warp 1      TMEM allocator and tcgen05.mma issuer (GEMM0 into TMEM, GEMM1 from P)
+//   (both run as converged warps; one elected lane issues each TMA / MMA / commit)
 //   warps 2..9  epilogue, two warpgroups: TMEM -> registers -> bias + act -> fp16/bf16 ->
 //               (chain) P tile in shared memory, the operand of GEMM1
 //               ("Shared-memory-resident fusion": the accumulator tile is staged in
@@ -81,16 +82,27 @@ __device__ __forceinline__ TileCoord tile_coord(const ChainParams& p, int32_t t)
   return c;
 }
 
-// Optional event trace of one CTA: slot 0 counts events; event i occupies slots
-// 2i+1 (clock64) and 2i+2 (code | group << 8 | tile index << 16).
-__device__ __forceinline__ void trace(const ChainParams& p, uint32_t code, uint32_t group,
-                                      int it) {
-  if (p.trace == nullptr || blockIdx.x != p.trace_cta) return;
-  const unsigned long long idx = atomicAdd(p.trace, 1ull);
-  if (idx >= p.trace_cap) return;
-  p.trace[2 * idx + 1] = static_cast<unsigned long long>(clock64());
-  p.trace[2 * idx + 2] = code | (group << 8) | (static_cast<unsigned long long>(it) << 16);
-}
+// Optional event trace of one CTA.  The buffer holds four regions of trace_cap / 4 events,
+// one per role (producer, MMA issuer, epilogue group 0, group 1); each role appends to its
+// own region with plain stores, so tracing costs a few instructions per event.  An event
+// is two words: clock64, and code | group << 8 | tile index << 16 | 1 << 63.
+struct Tracer {
+  unsigned long long* base = nullptr;
+  uint32_t n = 0, cap = 0;
+  __device__ __forceinline__ Tracer(const ChainParams& p, uint32_t region, uint32_t leader) {
+    if (p.trace != nullptr && blockIdx.x == p.trace_cta && leader != 0u) {
+      cap = p.trace_cap / 4u;
+      base = p.trace + 2ull * cap * region;
+    }
+  }
+  __device__ __forceinline__ void operator()(uint32_t code, uint32_t group, int it) {
+    if (base == nullptr || n >= cap) return;
+    base[2 * n] = static_cast<unsigned long long>(clock64());
+    base[2 * n + 1] = code | (group << 8) | (static_cast<unsigned long long>(it) << 16) |
+                      (1ull << 63);
+    ++n;
+  }
+};
 
 // Number of tiles this CTA processes (tiles blockIdx.x, blockIdx.x + gridDim.x, ...).
 __device__ __forceinline__ int local_tiles(const ChainParams& p) {
@@ -98,60 +110,65 @@ __device__ __forceinline__ int local_tiles(const ChainParams& p) {
   return b < p.num_tiles ? (p.num_tiles - 1 - b) / g + 1 : 0;
 }
 
-// Number of 16-wide MMA K steps in GEMM0 chunk kc (a partial last chunk is zero-filled
-// by TMA up to the next multiple of 16).
-__device__ __forceinline__ int ksteps0(const ChainParams& p, int kc, bool a4d) {
-  const int cb = a4d ? (kc % p.kc_per_tap) : kc;
-  const int rem = p.K0 - cb * kChunkK;
-  const int s = (rem + 15) >> 4;
-  return s < 4 ? s : 4;
+// Bounded wait executed by a whole warp; the lanes agree on the outcome.
+__device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity,
+                                               const ChainParams& p,
+                                               volatile uint32_t* abort_flag, uint32_t site,
+                                               int32_t t) {
+  const bool ok =
+      mbar_wait(bar, parity, p.wait_limit_ns, abort_flag, p.err, p.kernel_id, site, t);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ------------------------------------------------------------------------------------
-// producer (one thread)
+// producer (one warp; the elected lane issues)
 // ------------------------------------------------------------------------------------
 template <int MODE, bool A4D, bool W0MN, bool W1MN>
-__device__ __forceinline__ void load_a_chunk(const ChainParams& p, const CUtensorMap* tmA,
-                                             uint32_t dst, const TileCoord& tc, int kc,
-                                             uint32_t bar, uint64_t pol) {
+__device__ __forceinline__ void load_a_chunk(uint32_t lead, const ChainParams& p,
+                                             const CUtensorMap* tmA, uint32_t dst,
+                                             const TileCoord& tc, int kc, uint32_t bar,
+                                             uint64_t pol) {
   if constexpr (A4D) {
     const int t = kc / p.kc_per_tap;
     const int cb = kc - t * p.kc_per_tap;
     const int r = t / p.S;
     const int s = t - r * p.S;
-    tma_load_4d(dst, tmA, bar, cb * kChunkK, tc.wo0 + s - p.pad, tc.ho0 + r - p.pad, tc.n, pol);
+    tma_load_4d(lead, dst, tmA, bar, cb * kChunkK, tc.wo0 + s - p.pad, tc.ho0 + r - p.pad, tc.n,
+                pol);
   } else {
-    tma_load_2d(dst, tmA, bar, kc * kChunkK, tc.m0, pol);
+    tma_load_2d(lead, dst, tmA, bar, kc * kChunkK, tc.m0, pol);
   }
 }
 
 template <bool A4D, bool W0MN>
-__device__ __forceinline__ void load_w0_chunk(const ChainParams& p, const CUtensorMap* tmW0,
-                                              uint32_t dst, int kc, uint32_t bar, uint64_t pol) {
+__device__ __forceinline__ void load_w0_chunk(uint32_t lead, const ChainParams& p,
+                                              const CUtensorMap* tmW0, uint32_t dst, int kc,
+                                              uint32_t bar, uint64_t pol) {
   if constexpr (W0MN) {
     // W0[K0][N0] row-major: one 64 (N) x 64 (K) box per 64-wide N block, 8 KiB apart.
     const int nblk = (p.N0p + 63) >> 6;
     for (int nb = 0; nb < nblk; ++nb)
-      tma_load_2d(dst + nb * 8192u, tmW0, bar, nb * 64, kc * kChunkK, pol);
+      tma_load_2d(lead, dst + nb * 8192u, tmW0, bar, nb * 64, kc * kChunkK, pol);
   } else if constexpr (A4D) {
     // W0[C0][R*S][C]: the 64-channel block cb of tap t for all C0 rows.
     const int t = kc / p.kc_per_tap;
     const int cb = kc - t * p.kc_per_tap;
-    tma_load_3d(dst, tmW0, bar, cb * kChunkK, t, 0, pol);
+    tma_load_3d(lead, dst, tmW0, bar, cb * kChunkK, t, 0, pol);
   } else {
-    tma_load_2d(dst, tmW0, bar, kc * kChunkK, 0, pol);
+    tma_load_2d(lead, dst, tmW0, bar, kc * kChunkK, 0, pol);
   }
 }
 
 template <bool W1MN>
-__device__ __forceinline__ void load_w1_chunk(const ChainParams& p, const CUtensorMap* tmW1,
-                                              uint32_t dst, int kc1, uint32_t bar, uint64_t pol) {
+__device__ __forceinline__ void load_w1_chunk(uint32_t lead, const ChainParams& p,
+                                              const CUtensorMap* tmW1, uint32_t dst, int kc1,
+                                              uint32_t bar, uint64_t pol) {
   if constexpr (W1MN) {
     const int nblk = (p.N1p + 63) >> 6;
     for (int nb = 0; nb < nblk; ++nb)
-      tma_load_2d(dst + nb * 8192u, tmW1, bar, nb * 64, kc1 * kChunkK, pol);
+      tma_load_2d(lead, dst + nb * 8192u, tmW1, bar, nb * 64, kc1 * kChunkK, pol);
   } else {
-    tma_load_2d(dst, tmW1, bar, kc1 * kChunkK, 0, pol);
+    tma_load_2d(lead, dst, tmW1, bar, kc1 * kChunkK, 0, pol);
   }
 }
 
@@ -159,8 +176,10 @@ template <int MODE, bool A4D, bool W0MN, bool W1MN>
 __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
                               const CUtensorMap* tmW0, const CUtensorMap* tmW1, uint32_t base,
                               uint32_t bars, volatile uint32_t* abort_flag) {
+  const uint32_t lead = elect_one();
   const uint64_t pol_stream = l2_policy_evict_first();
   const uint64_t pol_keep = l2_policy_evict_last();
+  Tracer trace(p, 0, lead);
   uint32_t issued = 0, issued_parity = 0;   // per-stage: a fill in flight, and its parity
   bool w_issued = false;
   bool ok = true;
@@ -169,13 +188,13 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     const uint32_t wbar = bars + 8u * BAR_WFULL;
     uint32_t total = p.kchunks0 * p.w0_chunk_bytes;
     if (MODE == MODE_CHAIN) total += p.kchunks1 * p.w1_chunk_bytes;
-    mbar_arrive_expect_tx(wbar, total);
+    mbar_arrive_expect_tx_if(lead, wbar, total);
     for (int kc = 0; kc < p.kchunks0; ++kc)
-      load_w0_chunk<A4D, W0MN>(p, tmW0, base + p.off_w0 + kc * p.w0_chunk_bytes, kc, wbar,
+      load_w0_chunk<A4D, W0MN>(lead, p, tmW0, base + p.off_w0 + kc * p.w0_chunk_bytes, kc, wbar,
                                pol_keep);
     if (MODE == MODE_CHAIN)
       for (int kc1 = 0; kc1 < p.kchunks1; ++kc1)
-        load_w1_chunk<W1MN>(p, tmW1, base + p.off_w1 + kc1 * p.w1_chunk_bytes, kc1, wbar,
+        load_w1_chunk<W1MN>(lead, p, tmW1, base + p.off_w1 + kc1 * p.w1_chunk_bytes, kc1, wbar,
                             pol_keep);
     w_issued = true;
   }
@@ -183,8 +202,8 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
   int stage = 0;
   uint32_t phase = 0;
   auto acquire = [&](int32_t t) -> bool {   // waits until ring slot `stage` is free
-    return mbar_wait(bars + 8u * (BAR_EMPTY0 + stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
-                     p.err, p.kernel_id, SITE_PRODUCER_EMPTY, t);
+    return warp_mbar_wait(bars + 8u * (BAR_EMPTY0 + stage), phase ^ 1u, p, abort_flag,
+                          SITE_PRODUCER_EMPTY, t);
   };
   auto advance = [&]() {
     issued |= 1u << stage;
@@ -197,13 +216,14 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     const TileCoord tc = tile_coord<A4D>(p, t);
     for (int kc = 0; kc < p.kchunks0; ++kc) {
       if (!acquire(t)) return false;
-      trace(p, EV_PROD_ACQUIRE, kc, it);
+      trace(EV_PROD_ACQUIRE, kc, it);
       const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
-      mbar_arrive_expect_tx(fb, kABytes + (p.resident ? 0u : p.w0_chunk_bytes));
-      load_a_chunk<MODE, A4D, W0MN, W1MN>(p, tmA, sbase, tc, kc, fb, pol_stream);
-      if (!p.resident) load_w0_chunk<A4D, W0MN>(p, tmW0, sbase + kABytes, kc, fb, pol_keep);
-      trace(p, EV_PROD_ISSUED, kc, it);
+      mbar_arrive_expect_tx_if(lead, fb, kABytes + (p.resident ? 0u : p.w0_chunk_bytes));
+      load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, kc, fb, pol_stream);
+      if (!p.resident)
+        load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, kc, fb, pol_keep);
+      trace(EV_PROD_ISSUED, kc, it);
       advance();
     }
     return true;
@@ -215,8 +235,9 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
       if (!acquire(t)) return false;
       const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
-      mbar_arrive_expect_tx(fb, p.w1_chunk_bytes);
-      load_w1_chunk<W1MN>(p, tmW1, base + p.off_ring + stage * p.stage_bytes, kc1, fb, pol_keep);
+      mbar_arrive_expect_tx_if(lead, fb, p.w1_chunk_bytes);
+      load_w1_chunk<W1MN>(lead, p, tmW1, base + p.off_ring + stage * p.stage_bytes, kc1, fb,
+                          pol_keep);
       advance();
     }
     return true;
@@ -251,15 +272,57 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
 // ------------------------------------------------------------------------------------
 // MMA issuer (one thread)
 // ------------------------------------------------------------------------------------
+// Issues the MMAs of one 64-wide K chunk: D (+)= A . B over `nks` 16-wide K steps.  The
+// descriptors of consecutive K steps differ only in their start-address field (32 B per
+// step for K-major operands, 2 KiB for an MN-major one), so each step is one add; with
+// small N the single issuing thread is otherwise the bottleneck.
+template <bool BMN>
+__device__ __forceinline__ void issue_chunk(uint32_t lead, uint32_t d, uint64_t adesc,
+                                            uint64_t bdesc, uint32_t idesc, int nks,
+                                            bool first) {
+  constexpr uint64_t kAStep = 32u >> 4;
+  constexpr uint64_t kBStep = BMN ? (2048u >> 4) : (32u >> 4);
+  if (nks == 4) {
+    mma_f16_ss(lead, d, adesc, bdesc, idesc, first ? 0u : 1u);
+    mma_f16_ss(lead, d, adesc + kAStep, bdesc + kBStep, idesc, 1u);
+    mma_f16_ss(lead, d, adesc + 2 * kAStep, bdesc + 2 * kBStep, idesc, 1u);
+    mma_f16_ss(lead, d, adesc + 3 * kAStep, bdesc + 3 * kBStep, idesc, 1u);
+  } else {
+    for (int ks = 0; ks < nks; ++ks)
+      mma_f16_ss(lead, d, adesc + ks * kAStep, bdesc + ks * kBStep, idesc,
+                 (first && ks == 0) ? 0u : 1u);
+  }
+}
+
 template <int MODE, bool A4D, bool W0MN, bool W1MN>
 __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
                          volatile uint32_t* abort_flag) {
   const uint32_t idesc0 = idesc_f16_f32(p.is_bf16, W0MN ? 1u : 0u, kBlockM, p.N0p);
   const uint32_t idesc1 = idesc_f16_f32(p.is_bf16, W1MN ? 1u : 0u, kBlockM, p.N1p);
   bool ok = true;
+  const uint32_t lead = elect_one();
+  Tracer trace(p, 1, lead);
   if (p.resident)
-    ok = mbar_wait(bars + 8u * BAR_WFULL, 0u, p.wait_limit_ns, abort_flag, p.err, p.kernel_id,
-                   SITE_MMA_WEIGHTS, 0);
+    ok = warp_mbar_wait(bars + 8u * BAR_WFULL, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
+
+  // Descriptors of every operand region, built once; a ring stage / weight chunk / P
+  // chunk is then a multiple of its byte size (in 16-byte units) added to them.
+  const uint32_t w0_lbo = W0MN ? 8192u : 16u, w1_lbo = W1MN ? 8192u : 16u;
+  const uint64_t ring_a = sdesc_sw128(base + p.off_ring, 16u, 1024u);
+  const uint64_t ring_w0 = sdesc_sw128(base + p.off_ring + kABytes, w0_lbo, 1024u);
+  const uint64_t ring_w1 = sdesc_sw128(base + p.off_ring, w1_lbo, 1024u);
+  const uint64_t res_w0 = sdesc_sw128(base + p.off_w0, w0_lbo, 1024u);
+  const uint64_t res_w1 = sdesc_sw128(base + p.off_w1, w1_lbo, 1024u);
+  const uint64_t p_desc0 = sdesc_sw128(base + p.off_p[0], 16u, 1024u);
+  const uint64_t p_desc1 = sdesc_sw128(base + p.off_p[1], 16u, 1024u);
+  const uint32_t stage_step = p.stage_bytes >> 4;
+  const uint32_t w0_step = p.w0_chunk_bytes >> 4, w1_step = p.w1_chunk_bytes >> 4;
+  // K steps of GEMM0's chunks: full (4) except the last channel block of each tap / the
+  // last chunk of K0.
+  const int last_rem = p.K0 - (p.kc_per_tap - 1) * kChunkK;
+  const int last_nks = last_rem >= 64 ? 4 : (last_rem + 15) >> 4;
+  const int rem1 = p.N0p - (p.kchunks1 - 1) * kChunkK;
+  const int last_nks1 = rem1 >= 64 ? 4 : (rem1 >> 4);
 
   int stage = 0;
   uint32_t phase = 0;
@@ -272,34 +335,34 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     if (MODE != MODE_CHAIN) {
       // The epilogue must have drained the buffer's previous tile.
       const uint32_t u = static_cast<uint32_t>(it >> 1);
-      if (!mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), (u & 1u) ^ 1u, p.wait_limit_ns,
-                     abort_flag, p.err, p.kernel_id, SITE_MMA_ACC_EMPTY, t))
+      if (!warp_mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), (u & 1u) ^ 1u, p, abort_flag,
+                          SITE_MMA_ACC_EMPTY, t))
         return false;
-      trace(p, EV_MMA_ACC_FREE, b, it);
-    }
-    tc_fence_after_sync();
-    const uint32_t d0 = tmem_base + p.d0_col[b];
-    for (int kc = 0; kc < p.kchunks0; ++kc) {
-      if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag, p.err,
-                     p.kernel_id, SITE_MMA_FULL, t))
-        return false;
-      trace(p, EV_MMA_FULL, kc, it);
+      trace(EV_MMA_ACC_FREE, b, it);
+      // Orders these MMAs after the epilogue's TMEM reads of the buffer.  This fence costs
+      // hundreds of cycles while earlier MMAs are in flight, so it is taken once per tile,
+      // only where the wait synchronised with tcgen05 operations of another thread.
       tc_fence_after_sync();
-      const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
-      const uint32_t wbase =
-          p.resident ? base + p.off_w0 + kc * p.w0_chunk_bytes : sbase + kABytes;
-      const int nks = ksteps0(p, kc, A4D);
-      for (int ks = 0; ks < nks; ++ks) {
-        const uint64_t adesc = sdesc_sw128(sbase + ks * 32u, 16u, 1024u);
-        const uint64_t bdesc = W0MN ? sdesc_sw128(wbase + ks * 2048u, 8192u, 1024u)
-                                    : sdesc_sw128(wbase + ks * 32u, 16u, 1024u);
-        mma_f16_ss(d0, adesc, bdesc, idesc0, (kc | ks) != 0 ? 1u : 0u);
-      }
-      mma_commit(bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
+    }
+    const uint32_t d0 = tmem_base + p.d0_col[b];
+    int cb = 0;   // channel block within the tap (4-D) / chunk index (2-D)
+    for (int kc = 0; kc < p.kchunks0; ++kc) {
+      trace(EV_MMA_WAIT, kc, it);
+      if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL, t))
+        return false;
+      trace(EV_MMA_FULL, kc, it);   // TMA data: no tcgen05 ordering needed
+      const uint64_t adesc = ring_a + static_cast<uint64_t>(stage) * stage_step;
+      const uint64_t bdesc = p.resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
+                                        : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
+      const int nks = cb == p.kc_per_tap - 1 ? last_nks : 4;
+      if (++cb == p.kc_per_tap) cb = 0;
+      issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
+      trace(EV_MMA_ISSUED, kc, it);
+      mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
       if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
     }
-    mma_commit(bars + 8u * (BAR_ACC_FULL0 + b));
-    trace(p, EV_MMA_G0_DONE, b, it);
+    mma_commit(lead, bars + 8u * (BAR_ACC_FULL0 + b));
+    trace(EV_MMA_G0_DONE, b, it);
     return true;
   };
 
@@ -308,39 +371,31 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     const int32_t t = blockIdx.x + j * gridDim.x;
     const uint32_t b = p.acc_dual ? static_cast<uint32_t>(j & 1) : 0u;
     const uint32_t u = p.acc_dual ? static_cast<uint32_t>(j >> 1) : static_cast<uint32_t>(j);
-    if (!mbar_wait(bars + 8u * (BAR_P_FULL0 + b), u & 1u, p.wait_limit_ns, abort_flag, p.err,
-                   p.kernel_id, SITE_MMA_P_FULL, t))
+    if (!warp_mbar_wait(bars + 8u * (BAR_P_FULL0 + b), u & 1u, p, abort_flag, SITE_MMA_P_FULL, t))
       return false;
-    trace(p, EV_MMA_P_READY, b, j);
+    trace(EV_MMA_P_READY, b, j);
     tc_fence_after_sync();
     const uint32_t d1 = tmem_base + p.d1_col[b];
     for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
-      uint32_t w1base;
+      uint64_t bdesc;
       if (p.resident) {
-        w1base = base + p.off_w1 + kc1 * p.w1_chunk_bytes;
+        bdesc = res_w1 + static_cast<uint64_t>(kc1) * w1_step;
       } else {
-        if (!mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p.wait_limit_ns, abort_flag, p.err,
-                       p.kernel_id, SITE_MMA_FULL, t))
+        if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL,
+                            t))
           return false;
-        tc_fence_after_sync();
-        w1base = base + p.off_ring + stage * p.stage_bytes;
+        bdesc = ring_w1 + static_cast<uint64_t>(stage) * stage_step;
       }
-      const uint32_t pbase = base + p.off_p[b] + kc1 * kPChunkBytes;
-      const int rem = p.N0p - kc1 * kChunkK;
-      const int nks = rem >= 64 ? 4 : (rem >> 4);
-      for (int ks = 0; ks < nks; ++ks) {
-        const uint64_t adesc = sdesc_sw128(pbase + ks * 32u, 16u, 1024u);
-        const uint64_t bdesc = W1MN ? sdesc_sw128(w1base + ks * 2048u, 8192u, 1024u)
-                                    : sdesc_sw128(w1base + ks * 32u, 16u, 1024u);
-        mma_f16_ss(d1, adesc, bdesc, idesc1, (kc1 | ks) != 0 ? 1u : 0u);
-      }
+      const uint64_t adesc = (b ? p_desc1 : p_desc0) + static_cast<uint64_t>(kc1) * (kPChunkBytes >> 4);
+      issue_chunk<W1MN>(lead, d1, adesc, bdesc, idesc1, kc1 == p.kchunks1 - 1 ? last_nks1 : 4,
+                        kc1 == 0);
       if (!p.resident) {
-        mma_commit(bars + 8u * (BAR_EMPTY0 + stage));
+        mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));
         if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
       }
     }
-    mma_commit(bars + 8u * (BAR_D1_FULL0 + b));
-    trace(p, EV_MMA_G1_DONE, b, j);
+    mma_commit(lead, bars + 8u * (BAR_D1_FULL0 + b));
+    trace(EV_MMA_G1_DONE, b, j);
     return true;
   };
 
@@ -359,9 +414,10 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     }
   }
   // Whatever happened, no MMA may still be running when TMEM is released.
-  mma_commit(bars + 8u * BAR_MMA_DONE);
+  mma_commit(lead, bars + 8u * BAR_MMA_DONE);
   (void)mbar_wait(bars + 8u * BAR_MMA_DONE, 0u, p.wait_limit_ns, nullptr, p.err, p.kernel_id,
                   SITE_MMA_DRAIN, 0);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------------------------
@@ -528,6 +584,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
   const bool elected = threadIdx.x == 64 + g * static_cast<int>(group_threads);
   const bool dual = MODE != MODE_CHAIN || p.acc_dual;
   bool alive = true;
+  Tracer trace(p, 2u + static_cast<uint32_t>(g), elected ? 1u : 0u);
 
   const int ntiles = local_tiles(p);
   for (int it = g; it < ntiles; it += groups) {
@@ -541,7 +598,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       const uint32_t p_tile = base + p.off_p[b];
       alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_ACC_FULL, t);
-      if (elected) trace(p, EV_EPI_ACC_READY, g, it);
+      if (elected) trace(EV_EPI_ACC_READY, g, it);
       tc_fence_after_sync();
       if (p.out_alias_p) {   // P[b] doubles as this group's previous output staging
         if (elected) bulk_wait_read_all();
@@ -554,17 +611,17 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8u * (BAR_P_FULL0 + b));
-      if (elected) trace(p, EV_EPI_P_DONE, g, it);
+      if (elected) trace(EV_EPI_P_DONE, g, it);
 
       alive = warp_wait(alive, bars + 8u * (BAR_D1_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_D1_FULL, t);
-      if (elected) trace(p, EV_EPI_D1_READY, g, it);
+      if (elected) trace(EV_EPI_D1_READY, g, it);
       tc_fence_after_sync();
       if (!p.out_alias_p) {
         if (elected) bulk_wait_read_all();
         named_bar_sync(bar_id, group_threads);
       }
-      if (elected) trace(p, EV_EPI_STAGING, g, it);
+      if (elected) trace(EV_EPI_STAGING, g, it);
       if (alive)
         drain_to_smem_act<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p,
                                 bias_s + p.N0p, out_tile, row, kPChunkBytes);
@@ -574,16 +631,16 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       if (elected && !*abort_flag) {
         store_tile<A4D>(tmOut, out_tile, (p.N1p + 63) >> 6, tc);
         bulk_commit_group();
-        trace(p, EV_EPI_STORED, g, it);
+        trace(EV_EPI_STORED, g, it);
       }
     } else {
       alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u & 1u, p, abort_flag,
                         SITE_EPI_ACC_FULL, t);
-      if (elected) trace(p, EV_EPI_ACC_READY, g, it);
+      if (elected) trace(EV_EPI_ACC_READY, g, it);
       tc_fence_after_sync();
       if (elected) bulk_wait_read_all();   // this group's staging is free again
       named_bar_sync(bar_id, group_threads);
-      if (elected) trace(p, EV_EPI_STAGING, g, it);
+      if (elected) trace(EV_EPI_STAGING, g, it);
       if (alive) {
         if (MODE == MODE_POOL)
           drain_pool<BF16>(tm_lane, p.d0_col[b], p.N0p, bias_s, out_tile, q, lane);
@@ -606,7 +663,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
           store_tile<A4D>(tmOut, out_tile, (p.N0p + 63) >> 6, tc);
         }
         bulk_commit_group();
-        trace(p, EV_EPI_STORED, g, it);
+        trace(EV_EPI_STORED, g, it);
       }
     }
   }
@@ -685,10 +742,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<MODE, A4D, W0MN, W1MN>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
+    producer_role<MODE, A4D, W0MN, W1MN>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) mma_role<MODE, A4D, W0MN, W1MN>(p, base, bars, tmem_base, abort_flag);
+    mma_role<MODE, A4D, W0MN, W1MN>(p, base, bars, tmem_base, abort_flag);
     __syncwarp();
   } else {
     if (p.is_bf16)

@@ -52,6 +52,8 @@ enum TraceEvent : uint32_t {
   EV_EPI_D1_READY = 10,  // epilogue group saw GEMM1's accumulator complete
   EV_EPI_STAGING = 11,   // epilogue group's output staging free
   EV_EPI_STORED = 12,    // epilogue group issued the tile's TMA store
+  EV_MMA_WAIT = 13,      // MMA issuer starts waiting for a ring slot
+  EV_MMA_ISSUED = 14,    // MMA issuer issued a slot's MMAs
 };
 
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M

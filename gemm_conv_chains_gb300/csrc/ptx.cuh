@@ -59,6 +59,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(uint32_t pred, uint32_t bar,
+                                                         uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%1], %2;\n\t}" ::"r"(pred),
+      "r"(bar), "r"(bytes)
+      : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -71,17 +80,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware park the warp for up to `hint_ns` (it resumes as soon
+// as the phase completes), so that waiting warps take no issue slots from the warps that
+// share their scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  `abort_flag` (shared
-// memory, may be null) lets one role that gave up stop the others quickly.
+// memory, may be null) lets one role that gave up stop the others quickly.  Between
+// checks of the limit the warp sleeps in try_wait (at most 100 us at a time).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           volatile uint32_t* abort_flag, uint32_t* err,
                                           uint32_t kernel, uint32_t site, uint32_t tile) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (abort_flag != nullptr && *abort_flag != 0u) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       record_error(err, ERR_CODE_TIMEOUT, kernel, site, tile);
@@ -89,6 +113,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
       return false;
     }
   }
+}
+
+// ------------------------------------------------------------------------------------
+// warp-converged issue
+// ------------------------------------------------------------------------------------
+// Returns 1 in exactly one lane of the (fully converged) warp.  The producer and MMA
+// roles run as whole warps and predicate their single-thread instructions on this value,
+// so their loop state stays warp-uniform and the issue path stays short.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t is_leader;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(is_leader));
+  return is_leader;
 }
 
 // ------------------------------------------------------------------------------------
@@ -131,32 +171,38 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t c0, int32_t c1, uint64_t policy) {
+// TMA tile loads into shared memory, completing on `bar`; issued only where pred != 0.
+__device__ __forceinline__ void tma_load_2d(uint32_t pred, uint32_t dst, const CUtensorMap* map,
+                                            uint32_t bar, int32_t c0, int32_t c1, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%1], [%2, {%4, %5}], [%3], %6;\n\t}" ::"r"(pred),
+      "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t c0, int32_t c1, int32_t c2, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3,
+__device__ __forceinline__ void tma_load_3d(uint32_t pred, uint32_t dst, const CUtensorMap* map,
+                                            uint32_t bar, int32_t c0, int32_t c1, int32_t c2,
                                             uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%1], [%2, {%4, %5, %6}], [%3], %7;\n\t}" ::"r"(pred),
+      "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
       "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t pred, uint32_t dst, const CUtensorMap* map,
+                                            uint32_t bar, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%1], [%2, {%4, %5, %6, %7}], [%3], %8;\n\t}" ::"r"(pred),
+      "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "l"(policy)
       : "memory");
 }
 
@@ -237,22 +283,27 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t is_bf16, uint32_t 
          ((M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] x B[smem]; issued by one thread.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem] x B[smem]; issued only where pred != 0 (one lane).
+__device__ __forceinline__ void mma_f16_ss(uint32_t pred, uint32_t d_tmem, uint64_t a_desc,
+                                           uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 q, %0, 0;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, p;\n\t}" ::"r"(pred),
+      "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrives (once) on `bar` when every tcgen05.mma previously issued by this thread is done.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
-                   "r"(bar)
-               : "memory");
+// Arrives (once) on `bar` when every tcgen05.mma previously issued by this thread is done;
+// issued only where pred != 0 (the lane that issued the MMAs).
+__device__ __forceinline__ void mma_commit(uint32_t pred, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::
+          "r"(pred),
+      "r"(bar)
+      : "memory");
 }
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread t of the warp gets lane (base + t).

@@ -276,31 +276,31 @@ def probe_timeout(limit_ns: int, stream=None) -> None:
 
 TRACE_EVENTS = {1: "prod_acquire", 2: "prod_issued", 3: "mma_full", 4: "mma_g0_done",
                 5: "mma_p_ready", 6: "mma_g1_done", 7: "mma_acc_free", 8: "epi_acc_ready",
-                9: "epi_p_done", 10: "epi_d1_ready", 11: "epi_staging", 12: "epi_stored"}
+                9: "epi_p_done", 10: "epi_d1_ready", 11: "epi_staging", 12: "epi_stored",
+                13: "mma_wait", 14: "mma_issued"}
 
 
 def set_trace(buf, cta: int = 0) -> None:
-    """Records the per-step timeline of CTA `cta` of later launches into `buf` (a CUDA
-    int64 tensor of 1 + 2 * capacity words, zeroed by the caller); None turns it off."""
+    """Records the per-step timeline of CTA `cta` of later launches into `buf` (a zeroed,
+    contiguous CUDA int64 tensor of 2 * capacity words); None turns it off."""
     if buf is None:
         _raise(lib().b2b_set_trace(None, 0, 0), "b2b_set_trace")
         return
     if not (buf.is_cuda and buf.dtype == torch.int64 and buf.is_contiguous()):
         raise ValueError("trace buffer must be a contiguous CUDA int64 tensor")
-    _raise(lib().b2b_set_trace(_ptr(buf), (buf.numel() - 1) // 2, int(cta)), "b2b_set_trace")
+    _raise(lib().b2b_set_trace(_ptr(buf), buf.numel() // 2, int(cta)), "b2b_set_trace")
 
 
 def read_trace(buf):
-    """Decodes a trace buffer: list of (cycles since the first event, event, group, tile)."""
-    raw = buf.cpu().tolist()
-    n = min(raw[0], (len(raw) - 1) // 2)
-    ev = [(raw[2 * i + 1], raw[2 * i + 2]) for i in range(n)]
+    """Decodes a trace buffer into (cycles since the first event, event, group, tile),
+    sorted by time."""
+    raw = buf.cpu().view(-1, 2).tolist()
+    ev = [(c, w & ((1 << 63) - 1)) for c, w in raw if w != 0]
     if not ev:
         return []
     t0 = min(c for c, _ in ev)
-    out = [(c - t0, TRACE_EVENTS.get(w & 0xFF, str(w & 0xFF)), (w >> 8) & 0xFF, w >> 16)
-           for c, w in ev]
-    return sorted(out)
+    return sorted((c - t0, TRACE_EVENTS.get(w & 0xFF, str(w & 0xFF)), (w >> 8) & 0xFF,
+                   (w >> 16) & 0xFFFF) for c, w in ev)
 
 
 def pad_channels(t: torch.Tensor, dim: int, multiple: int = 8) -> torch.Tensor:

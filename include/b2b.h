@@ -156,12 +156,12 @@ void b2b_set_wait_limit_ns(uint64_t ns);
 
 /* Event trace for performance analysis.  When buf is not NULL, every later launch of a
  * chain kernel records, for its CTA number `cta` only, the time (clock64, SM cycles) at
- * which each role reached each step of each tile: buf is a caller-owned device array of
- * 1 + 2 * capacity uint64 words, buf[0] must be zeroed by the caller and counts events
- * (it keeps counting past capacity), event i is stored in buf[2i+1] (clock) and buf[2i+2]
- * (event code | group << 8 | tile index << 16; codes in kernel_params.h, TraceEvent).
- * buf = NULL turns tracing off.  buf must be 8-byte aligned and stay valid while traced
- * launches run. */
+ * which each role reached each step of each tile.  buf is a caller-owned, zero-filled
+ * device array of 2 * capacity uint64 words split into four equal regions (producer,
+ * MMA issuer, epilogue group 0, epilogue group 1); each role appends its events to its
+ * region: word 2i = clock, word 2i+1 = event code | group << 8 | tile index << 16 |
+ * 1 << 63 (codes: TraceEvent in kernel_params.h); unused words stay 0.  buf = NULL turns
+ * tracing off.  buf must be 8-byte aligned and stay valid while traced launches run. */
 b2b_status b2b_set_trace(void* buf, uint32_t capacity, uint32_t cta);
 
 /* Reads and clears the current device's error word.  Synchronises the current device.

@@ -21,7 +21,7 @@ def test_trace_of_a_chain_is_complete_and_causal():
     w = wl.GemmChain("t", "f16", 128 * 400, 64, 64, 64, "relu", "relu")
     t = {k: v.cuda() for k, v in wl.gemm_inputs(w, seed=1).items()}
     ref = ops.b2b_gemm(t["A"], t["W0"], t["b0"], t["W1"], t["b1"], "relu", "relu")
-    buf = torch.zeros(1 + 2 * 4096, dtype=torch.int64, device="cuda")
+    buf = torch.zeros(2 * 4096, dtype=torch.int64, device="cuda")
     ops.set_trace(buf, cta=3)
     out = ops.b2b_gemm(t["A"], t["W0"], t["b0"], t["W1"], t["b1"], "relu", "relu")
     ops.set_trace(None)
@@ -37,18 +37,17 @@ def test_trace_of_a_chain_is_complete_and_causal():
     when = {(e[1], e[3]): e[0] for e in ev}
     for it in range(ntiles):
         assert when[("mma_g0_done", it)] <= when[("epi_acc_ready", it)]
-        assert when[("epi_p_done", it)] <= when[("mma_p_ready", it)] or True  # different threads
         assert when[("mma_p_ready", it)] <= when[("mma_g1_done", it)]
         assert when[("mma_g1_done", it)] <= when[("epi_d1_ready", it)]
         assert when[("epi_d1_ready", it)] <= when[("epi_stored", it)]
 
 
 def test_trace_off_records_nothing():
-    buf = torch.zeros(1 + 2 * 64, dtype=torch.int64, device="cuda")
+    buf = torch.zeros(2 * 64, dtype=torch.int64, device="cuda")
     ops.set_trace(buf)
     ops.set_trace(None)
     w = wl.GemmChain("t", "bf16", 512, 64, 64, 64, "relu", "relu")
     t = {k: v.cuda() for k, v in wl.gemm_inputs(w, seed=2).items()}
     ops.b2b_gemm(t["A"], t["W0"], t["b0"], t["W1"], t["b1"])
     torch.cuda.synchronize()
-    assert int(buf[0]) == 0
+    assert int(torch.count_nonzero(buf)) == 0
