@@ -123,39 +123,47 @@ __device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity,
 // ------------------------------------------------------------------------------------
 // producer (one warp; the elected lane issues)
 // ------------------------------------------------------------------------------------
+// Position of a GEMM0 K chunk: filter tap (r, s), its index t = r * S + s, and the
+// channel block cb within the tap (2-D A: t = r = s = 0 and cb = chunk index).  Advanced
+// with counters so that the issue loops do no division.
+struct KPos {
+  int r = 0, s = 0, t = 0, cb = 0;
+  __device__ __forceinline__ void next(const ChainParams& p) {
+    if (++cb == p.kc_per_tap) {
+      cb = 0;
+      ++t;
+      if (++s == p.S) { s = 0; ++r; }
+    }
+  }
+};
+
 template <int MODE, bool A4D, bool W0MN, bool W1MN>
 __device__ __forceinline__ void load_a_chunk(uint32_t lead, const ChainParams& p,
                                              const CUtensorMap* tmA, uint32_t dst,
-                                             const TileCoord& tc, int kc, uint32_t bar,
+                                             const TileCoord& tc, const KPos& k, uint32_t bar,
                                              uint64_t pol) {
   if constexpr (A4D) {
-    const int t = kc / p.kc_per_tap;
-    const int cb = kc - t * p.kc_per_tap;
-    const int r = t / p.S;
-    const int s = t - r * p.S;
-    tma_load_4d(lead, dst, tmA, bar, cb * kChunkK, tc.wo0 + s - p.pad, tc.ho0 + r - p.pad, tc.n,
-                pol);
+    tma_load_4d(lead, dst, tmA, bar, k.cb * kChunkK, tc.wo0 + k.s - p.pad, tc.ho0 + k.r - p.pad,
+                tc.n, pol);
   } else {
-    tma_load_2d(lead, dst, tmA, bar, kc * kChunkK, tc.m0, pol);
+    tma_load_2d(lead, dst, tmA, bar, k.cb * kChunkK, tc.m0, pol);
   }
 }
 
 template <bool A4D, bool W0MN>
 __device__ __forceinline__ void load_w0_chunk(uint32_t lead, const ChainParams& p,
-                                              const CUtensorMap* tmW0, uint32_t dst, int kc,
-                                              uint32_t bar, uint64_t pol) {
+                                              const CUtensorMap* tmW0, uint32_t dst,
+                                              const KPos& k, uint32_t bar, uint64_t pol) {
   if constexpr (W0MN) {
     // W0[K0][N0] row-major: one 64 (N) x 64 (K) box per 64-wide N block, 8 KiB apart.
     const int nblk = (p.N0p + 63) >> 6;
     for (int nb = 0; nb < nblk; ++nb)
-      tma_load_2d(lead, dst + nb * 8192u, tmW0, bar, nb * 64, kc * kChunkK, pol);
+      tma_load_2d(lead, dst + nb * 8192u, tmW0, bar, nb * 64, k.cb * kChunkK, pol);
   } else if constexpr (A4D) {
     // W0[C0][R*S][C]: the 64-channel block cb of tap t for all C0 rows.
-    const int t = kc / p.kc_per_tap;
-    const int cb = kc - t * p.kc_per_tap;
-    tma_load_3d(lead, dst, tmW0, bar, cb * kChunkK, t, 0, pol);
+    tma_load_3d(lead, dst, tmW0, bar, k.cb * kChunkK, k.t, 0, pol);
   } else {
-    tma_load_2d(lead, dst, tmW0, bar, kc * kChunkK, 0, pol);
+    tma_load_2d(lead, dst, tmW0, bar, k.cb * kChunkK, 0, pol);
   }
 }
 
@@ -189,8 +197,9 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     uint32_t total = p.kchunks0 * p.w0_chunk_bytes;
     if (MODE == MODE_CHAIN) total += p.kchunks1 * p.w1_chunk_bytes;
     mbar_arrive_expect_tx_if(lead, wbar, total);
-    for (int kc = 0; kc < p.kchunks0; ++kc)
-      load_w0_chunk<A4D, W0MN>(lead, p, tmW0, base + p.off_w0 + kc * p.w0_chunk_bytes, kc, wbar,
+    KPos k;
+    for (int kc = 0; kc < p.kchunks0; ++kc, k.next(p))
+      load_w0_chunk<A4D, W0MN>(lead, p, tmW0, base + p.off_w0 + kc * p.w0_chunk_bytes, k, wbar,
                                pol_keep);
     if (MODE == MODE_CHAIN)
       for (int kc1 = 0; kc1 < p.kchunks1; ++kc1)
@@ -214,15 +223,16 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
   auto load_g0 = [&](int it) -> bool {
     const int32_t t = blockIdx.x + it * gridDim.x;
     const TileCoord tc = tile_coord<A4D>(p, t);
-    for (int kc = 0; kc < p.kchunks0; ++kc) {
+    KPos k;
+    for (int kc = 0; kc < p.kchunks0; ++kc, k.next(p)) {
       if (!acquire(t)) return false;
       trace(EV_PROD_ACQUIRE, kc, it);
       const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
       mbar_arrive_expect_tx_if(lead, fb, kABytes + (p.resident ? 0u : p.w0_chunk_bytes));
-      load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, kc, fb, pol_stream);
+      load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, k, fb, pol_stream);
       if (!p.resident)
-        load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, kc, fb, pol_keep);
+        load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, k, fb, pol_keep);
       trace(EV_PROD_ISSUED, kc, it);
       advance();
     }
@@ -475,25 +485,40 @@ __device__ __forceinline__ void convert16(const uint32_t (&r)[16], const float* 
   }
 }
 
-// TMEM columns [col0 + c, col0 + c + 32) for c = c_first, c_first + c_step, ... below
-// ncols, of this thread's row -> bias -> act -> dtype -> smem tile.
+template <bool BF16, int ACT>
+__device__ __forceinline__ void convert_store16(const uint32_t (&r)[16], const float* bias, int c,
+                                                uint32_t tile, int row, uint32_t chunk_bytes) {
+  uint32_t v[8];
+  convert16<BF16, ACT>(r, bias, c, v);
+  st_row16_sw128(tile, row, c, chunk_bytes, v);
+}
+
+// TMEM columns of this thread's row -> bias -> act -> dtype -> smem tile.  The columns are
+// the 16-wide units u = 0, 1, ... at c_first + (u / 2) * c_step + (u % 2) * 16 below ncols
+// (c_step = 32: all columns; 64: every other 32-column block).  Software-pipelined: the
+// TMEM load of unit u+1 is in flight while unit u is converted and stored.
 template <bool BF16, int ACT>
 __device__ __forceinline__ void drain_to_smem(uint32_t tm_lane, uint32_t col0, int c_first,
                                               int c_step, int ncols, const float* bias,
                                               uint32_t tile, int row, uint32_t chunk_bytes) {
-  for (int c = c_first; c < ncols; c += c_step) {
-    uint32_t r0[16], r1[16];
-    uint32_t v[8];
-    const bool two = c + 16 < ncols;
-    tmem_ld16(tm_lane + col0 + c, r0);
-    if (two) tmem_ld16(tm_lane + col0 + c + 16, r1);
-    tmem_wait_ld(r0, r1);
-    convert16<BF16, ACT>(r0, bias, c, v);
-    st_row16_sw128(tile, row, c, chunk_bytes, v);
-    if (two) {
-      convert16<BF16, ACT>(r1, bias, c + 16, v);
-      st_row16_sw128(tile, row, c + 16, chunk_bytes, v);
-    }
+  auto col = [&](int u) { return c_first + (u >> 1) * c_step + ((u & 1) << 4); };
+  int u = 0;
+  if (col(0) >= ncols) return;
+  uint32_t a[16], b[16];
+  tmem_ld16(tm_lane + col0 + col(0), a);
+  tmem_wait_ld(a);
+  while (true) {
+    const int ca = col(u), cb = col(u + 1);
+    if (cb < ncols) tmem_ld16(tm_lane + col0 + cb, b);
+    convert_store16<BF16, ACT>(a, bias, ca, tile, row, chunk_bytes);
+    if (cb >= ncols) break;
+    tmem_wait_ld(b);
+    const int cn = col(u + 2);
+    if (cn < ncols) tmem_ld16(tm_lane + col0 + cn, a);
+    convert_store16<BF16, ACT>(b, bias, cb, tile, row, chunk_bytes);
+    if (cn >= ncols) break;
+    tmem_wait_ld(a);
+    u += 2;
   }
 }
 
@@ -515,30 +540,50 @@ __device__ __forceinline__ void drain_to_smem_act(int act, uint32_t tm_lane, uin
 // vertical one in lane ^ 16.  The max of the four fp32 sums is taken first; adding the
 // bias, ReLU and rounding are monotone, so this equals pooling the rounded ReLU output.
 template <bool BF16>
+__device__ __forceinline__ void pool_store16(const uint32_t (&r)[16], const float* bias, int c,
+                                             uint32_t tile, int prow, bool owner) {
+  float m[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float v = __uint_as_float(r[j]);
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+    m[j] = v;
+  }
+  if (owner) {
+    uint32_t v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      v[j] = pack2<BF16>(fmaxf(m[2 * j] + bias[c + 2 * j], 0.0f),
+                         fmaxf(m[2 * j + 1] + bias[c + 2 * j + 1], 0.0f));
+    st_row16_sw128(tile, prow, c, kPoolChunkBytes, v);
+  }
+}
+
+// Pool epilogue.  Tile row = 16 * h + w over an 8 x 16 conv-output tile, so warp q holds
+// conv rows 2q and 2q+1: the horizontal partner of a pixel sits in lane ^ 1 and the
+// vertical one in lane ^ 16.  The max of the four fp32 sums is taken first; adding the
+// bias, ReLU and rounding are monotone, so this equals pooling the rounded ReLU output.
+// TMEM loads of the next 16 columns overlap the current ones' reduction.
+template <bool BF16>
 __device__ __forceinline__ void drain_pool(uint32_t tm_lane, uint32_t col0, int ncols,
                                            const float* bias, uint32_t tile, int q, int lane) {
   const bool owner = (lane & 17) == 0;
   const int prow = q * 8 + (lane >> 1);
-  for (int c = 0; c < ncols; c += 16) {
-    uint32_t r[16];
-    tmem_ld16(tm_lane + col0 + c, r);
-    tmem_wait_ld(r);
-    float m[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      float v = __uint_as_float(r[j]);
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      m[j] = v;
-    }
-    if (owner) {
-      uint32_t v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        v[j] = pack2<BF16>(fmaxf(m[2 * j] + bias[c + 2 * j], 0.0f),
-                           fmaxf(m[2 * j + 1] + bias[c + 2 * j + 1], 0.0f));
-      st_row16_sw128(tile, prow, c, kPoolChunkBytes, v);
-    }
+  uint32_t a[16], b[16];
+  tmem_ld16(tm_lane + col0, a);
+  tmem_wait_ld(a);
+  for (int c = 0; c < ncols; c += 32) {
+    const bool nb = c + 16 < ncols;
+    if (nb) tmem_ld16(tm_lane + col0 + c + 16, b);
+    pool_store16<BF16>(a, bias, c, tile, prow, owner);
+    if (!nb) break;
+    tmem_wait_ld(b);
+    const bool na = c + 32 < ncols;
+    if (na) tmem_ld16(tm_lane + col0 + c + 32, a);
+    pool_store16<BF16>(b, bias, c + 16, tile, prow, owner);
+    if (!na) break;
+    tmem_wait_ld(a);
   }
 }
 

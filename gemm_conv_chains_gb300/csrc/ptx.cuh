@@ -332,6 +332,13 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
                : "memory");
 }
 
+// 32 consecutive columns in two x16 loads (the second only if `two`).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, bool two, uint32_t (&r)[16],
+                                          uint32_t (&s)[16]) {
+  tmem_ld16(taddr, r);
+  if (two) tmem_ld16(taddr + 16, s);
+}
+
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16], uint32_t (&s)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
