@@ -35,7 +35,7 @@ struct DeviceState {
   int num_sms = 0;
   uint32_t* err = nullptr;                    // device address of g_error_word
   cudaError_t init_error = cudaSuccess;
-  std::atomic<uint32_t> attr_done{0};         // bit v: smem attribute set for variant v
+  std::atomic<uint32_t> attr_done{0};         // bit 2v + bf16: smem attribute set
 };
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
@@ -182,8 +182,18 @@ struct Regions {
 // D1 buffers of round_up(N1p, 32) columns (every buffer starts on a multiple of 32
 // columns); single/pool: two accumulator buffers.  `dual` selects two buffers per
 // accumulator (two tiles in flight).  Returns the power-of-two allocation.
-uint32_t tmem_layout(ChainParams& p, int mode, bool dual) {
+uint32_t tmem_layout(ChainParams& p, int mode, bool dual, bool p_tmem = false) {
   const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
+  if (mode == MODE_CHAIN && p_tmem) {
+    // Buffer b holds D0, then P (packed, N0p / 2 columns, over D0) and D1 after it.
+    const uint32_t d1off = round_up(static_cast<uint32_t>(p.N0p) / 2u, 32u);
+    const uint32_t buf = round_up(std::max(s0, d1off + static_cast<uint32_t>(p.N1p)), 32u);
+    p.d0_col[0] = 0;
+    p.d0_col[1] = buf;
+    p.d1_col[0] = d1off;
+    p.d1_col[1] = buf + d1off;
+    return pow2_at_least(2u * buf);
+  }
   if (mode == MODE_CHAIN) {
     const uint32_t s1 = round_up(static_cast<uint32_t>(p.N1p), 32u);
     p.d0_col[0] = 0;
@@ -200,7 +210,7 @@ uint32_t tmem_layout(ChainParams& p, int mode, bool dual) {
 }
 
 // Shared-memory plan: ring of A (and, when streamed, weight) chunks; resident weights;
-// P tiles; output staging; biases (fp32); barriers.  Candidates are tried in order of
+// P tiles; output staging; bias operands; barriers.  Candidates are tried in order of
 // preference -- two tiles in flight, resident weights, separate staging -- and the first
 // that leaves at least three ring stages (else two) is taken.  Fills p's layout fields.
 bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_bytes,
@@ -214,26 +224,35 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   const uint32_t out_bytes = mode == MODE_CHAIN    ? n1blk * kPChunkBytes
                              : mode == MODE_SINGLE ? n0blk * kPChunkBytes
                                                    : n0blk * kPoolChunkBytes;
-  const uint32_t bias_bytes = round_up(static_cast<uint32_t>(p.N0p + p.N1p) * 4u, 1024u);
+  // Bias operands: the ONES tile, then one BIAS block per 64-wide N block of each GEMM.
+  const uint32_t bias_bytes =
+      kOnesBytes + kBiasBlockBytes * (n0blk + (mode == MODE_CHAIN ? n1blk : 0u));
   const uint32_t bar_bytes = 1024u;
   const uint32_t w_res = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes +
                          static_cast<uint32_t>(p.kchunks1) * p.w1_chunk_bytes;
 
-  struct Cand { int dual, groups, resident, alias; };
-  Cand cands[8];
+  // Candidates in order of preference.  Chains: two tiles in flight with P in shared
+  // memory; else two tiles in flight with P in TMEM (wide N0, where two P tiles and two
+  // accumulator pairs do not fit); else one tile at a time.
+  struct Cand { int dual, groups, resident, alias, p_tmem; };
+  Cand cands[16];
   int ncand = 0;
   if (mode == MODE_CHAIN) {
     ChainParams probe = p;
     const bool tmem_dual_ok = tmem_layout(probe, mode, true) <= 512u;
-    for (int dual = tmem_dual_ok ? 1 : 0; dual >= 0; --dual)
+    const bool tmem_p_ok = tmem_layout(probe, mode, true, true) <= 512u;
+    if (tmem_dual_ok)
       for (int resident = 1; resident >= 0; --resident)
-        for (int alias = 0; alias <= 1; ++alias)
-          cands[ncand++] = {dual, dual ? 2 : 1, resident, alias};
+        for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {1, 2, resident, alias, 0};
+    if (tmem_p_ok)
+      for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {1, 2, resident, 0, 1};
+    for (int resident = 1; resident >= 0; --resident)
+      for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {0, 1, resident, alias, 0};
   } else {
     // Pool staging is small: the warpgroups always take alternate tiles.
     const int gmin = mode == MODE_POOL ? 2 : 1;
     for (int resident = 1; resident >= 0; --resident)
-      for (int groups = 2; groups >= gmin; --groups) cands[ncand++] = {1, groups, resident, 0};
+      for (int groups = 2; groups >= gmin; --groups) cands[ncand++] = {1, groups, resident, 0, 0};
   }
 
   int chosen = -1;
@@ -244,7 +263,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
       const uint32_t stage_bytes =
           k.resident ? kABytes
                      : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
-      const uint32_t pbufs = mode == MODE_CHAIN ? (k.dual ? 2u : 1u) : 0u;
+      const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? (k.dual ? 2u : 1u) : 0u;
       const uint32_t obufs = k.groups == 2 ? 2u : 1u;
       const uint32_t shared = k.alias ? pbufs * std::max(p_bytes, out_bytes)
                                       : pbufs * p_bytes + obufs * out_bytes;
@@ -264,17 +283,18 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.epi_groups = k.groups;
   p.resident = k.resident;
   p.out_alias_p = k.alias;
+  p.p_tmem = k.p_tmem;
   p.num_stages = chosen_stages;
   p.stage_bytes = chosen_stage_bytes;
-  p.tmem_cols = tmem_layout(p, mode, k.dual != 0);
+  p.tmem_cols = tmem_layout(p, mode, k.dual != 0, k.p_tmem != 0);
   Regions r;
   r.ring = p.num_stages * p.stage_bytes;
   r.w_res = p.resident ? w_res : 0u;
-  r.p_each = mode == MODE_CHAIN ? (p.out_alias_p ? std::max(p_bytes, out_bytes) : p_bytes) : 0u;
+  const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? (k.dual ? 2u : 1u) : 0u;
+  r.p_each = pbufs ? (p.out_alias_p ? std::max(p_bytes, out_bytes) : p_bytes) : 0u;
   r.out_each = p.out_alias_p ? 0u : out_bytes;
   r.bias = bias_bytes;
   r.bar = bar_bytes;
-  const uint32_t pbufs = mode == MODE_CHAIN ? (k.dual ? 2u : 1u) : 0u;
   const uint32_t obufs = k.groups == 2 ? 2u : 1u;
   uint32_t off = 0;
   p.off_ring = off;
@@ -317,9 +337,10 @@ void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const v
 b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtensorMap& w0,
                   const CUtensorMap& w1, const CUtensorMap& out, ChainParams& p, size_t smem,
                   void* stream) {
-  const uint32_t bit = 1u << static_cast<uint32_t>(v);
+  const uint32_t bit = 1u << (2u * static_cast<uint32_t>(v) + (p.is_bf16 ? 1u : 0u));
   if ((d->attr_done.load() & bit) == 0u) {
-    if (cudaFuncSetAttribute(variant_func(v), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(variant_func(v, p.is_bf16 != 0),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemLimit)) != cudaSuccess) {
       cudaGetLastError();
       return B2B_ERR_CUDA;
@@ -740,7 +761,8 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           static_cast<uint32_t>(p.acc_dual), static_cast<uint32_t>(p.epi_groups),
                           static_cast<uint32_t>(p.num_tiles), static_cast<uint32_t>(p.kchunks0),
                           static_cast<uint32_t>(p.kchunks1), static_cast<uint32_t>(p.N0p),
-                          static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode), 0u};
+                          static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode),
+                          static_cast<uint32_t>(p.p_tmem)};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

@@ -7,7 +7,7 @@
 //   warp 0      TMA producer: A (or one conv tap of x) and weight K-chunks -> smem ring
 //   warp 1      TMEM allocator and tcgen05.mma issuer (GEMM0 into TMEM, GEMM1 from P)
 //   (both run as converged warps; one elected lane issues each TMA / MMA / commit)
-//   warps 2..9  epilogue, two warpgroups: TMEM -> registers -> bias + act -> fp16/bf16 ->
+//   warps 2..9  epilogue, two warpgroups: TMEM -> registers -> act -> fp16/bf16 ->
 //               (chain) P tile in shared memory, the operand of GEMM1
 //               ("Shared-memory-resident fusion": the accumulator tile is staged in
 //               shared memory and read back by the second GEMM, Figure 7)
@@ -16,7 +16,7 @@
 // Modes
 //   MODE_CHAIN   GEMM0 -> epi0 -> P -> GEMM1 -> epi1 -> global
 //   MODE_SINGLE  GEMM0 -> epi0 -> global             (one operator of the unfused path)
-//   MODE_POOL    conv GEMM -> 2x2 max -> bias -> ReLU -> global (Welder notes, Figure 5:
+//   MODE_POOL    conv GEMM -> 2x2 max -> ReLU -> global (Welder notes, Figure 5:
 //                the (2,2,F) reuse tile is reduced in registers and never leaves the chip)
 //
 // A operand
@@ -26,6 +26,9 @@
 //   an 8 x 16 output-pixel tile; coordinates outside the image read as zero, which is the
 //   conv's zero padding.  The box lands in shared memory as 128 rows x 128 B, exactly the
 //   K-major 128B-swizzled layout tcgen05 reads, so no im2col buffer exists anywhere.
+//
+// Bias: each GEMM's first MMA writes the bias into its accumulator (D = ONES . BIAS, see
+// fill_bias_operands), so epilogues apply only the activation and the rounding.
 //
 // Two tiles in flight: when TMEM and shared memory allow (acc_dual), tile i uses
 // accumulator / P / staging buffer i & 1 and the two epilogue warpgroups take alternate
@@ -57,7 +60,8 @@ enum : uint32_t {
   BAR_P_FULL0 = BAR_ACC_EMPTY0 + 2,
   BAR_D1_FULL0 = BAR_P_FULL0 + 2,
   BAR_MMA_DONE = BAR_D1_FULL0 + 2,
-  BAR_COUNT = BAR_MMA_DONE + 1,
+  BAR_BIAS_READY = BAR_MMA_DONE + 1,
+  BAR_COUNT = BAR_BIAS_READY + 1,
 };
 constexpr uint32_t kBarRegionBytes = 512;   // barriers, then TMEM slot and abort flag
 
@@ -248,13 +252,23 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
       mbar_arrive_expect_tx_if(lead, fb, p.w1_chunk_bytes);
       load_w1_chunk<W1MN>(lead, p, tmW1, base + p.off_ring + stage * p.stage_bytes, kc1, fb,
                           pol_keep);
+      trace(EV_PROD_W1_ISSUED, kc1, it);
       advance();
     }
     return true;
   };
 
   const int ntiles = local_tiles(p);
-  if (MODE == MODE_CHAIN) {
+  if (MODE == MODE_CHAIN && p.p_tmem) {
+    // Pairs: G0(0), G0(1), then G1(k), G1(k+1), G0(k+2), G0(k+3) -- as the MMA issuer.
+    for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = load_g0(it);
+    for (int k = 0; ok && k < ntiles; k += 2) {
+      ok = load_g1(k);
+      if (ok && k + 1 < ntiles) ok = load_g1(k + 1);
+      if (ok && k + 2 < ntiles) ok = load_g0(k + 2);
+      if (ok && k + 3 < ntiles) ok = load_g0(k + 3);
+    }
+  } else if (MODE == MODE_CHAIN) {
     // Same order as the MMA issuer consumes: G0(0..L-1), then G1(j), G0(j+L).
     const int L = p.acc_dual ? 2 : 1;
     for (int it = 0; ok && it < L && it < ntiles; ++it) ok = load_g0(it);
@@ -282,38 +296,47 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
 // ------------------------------------------------------------------------------------
 // MMA issuer (one thread)
 // ------------------------------------------------------------------------------------
-// Issues the MMAs of one 64-wide K chunk: D (+)= A . B over `nks` 16-wide K steps.  The
+// Issues the MMAs of one 64-wide K chunk: D += A . B over `nks` 16-wide K steps (D was
+// initialised to the bias by the GEMM's first MMA).  The
 // descriptors of consecutive K steps differ only in their start-address field (32 B per
 // step for K-major operands, 2 KiB for an MN-major one), so each step is one add; with
 // small N the single issuing thread is otherwise the bottleneck.
 template <bool BMN>
 __device__ __forceinline__ void issue_chunk(uint32_t lead, uint32_t d, uint64_t adesc,
-                                            uint64_t bdesc, uint32_t idesc, int nks,
-                                            bool first) {
+                                            uint64_t bdesc, uint32_t idesc, int nks) {
   constexpr uint64_t kAStep = 32u >> 4;
   constexpr uint64_t kBStep = BMN ? (2048u >> 4) : (32u >> 4);
   if (nks == 4) {
-    mma_f16_ss(lead, d, adesc, bdesc, idesc, first ? 0u : 1u);
+    mma_f16_ss(lead, d, adesc, bdesc, idesc, 1u);
     mma_f16_ss(lead, d, adesc + kAStep, bdesc + kBStep, idesc, 1u);
     mma_f16_ss(lead, d, adesc + 2 * kAStep, bdesc + 2 * kBStep, idesc, 1u);
     mma_f16_ss(lead, d, adesc + 3 * kAStep, bdesc + 3 * kBStep, idesc, 1u);
   } else {
     for (int ks = 0; ks < nks; ++ks)
-      mma_f16_ss(lead, d, adesc + ks * kAStep, bdesc + ks * kBStep, idesc,
-                 (first && ks == 0) ? 0u : 1u);
+      mma_f16_ss(lead, d, adesc + ks * kAStep, bdesc + ks * kBStep, idesc, 1u);
   }
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN>
+// GEMM1 chunk with A (= P) in TMEM: 8 packed columns per 16-wide K step.
+template <bool BMN>
+__device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32_t a_tmem,
+                                               uint64_t bdesc, uint32_t idesc, int nks) {
+  constexpr uint64_t kBStep = BMN ? (2048u >> 4) : (32u >> 4);
+  for (int ks = 0; ks < nks; ++ks)
+    mma_f16_ts(lead, d, a_tmem + 8u * ks, bdesc + ks * kBStep, idesc, 1u);
+}
+
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16>
 __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
                          volatile uint32_t* abort_flag) {
-  const uint32_t idesc0 = idesc_f16_f32(p.is_bf16, W0MN ? 1u : 0u, kBlockM, p.N0p);
-  const uint32_t idesc1 = idesc_f16_f32(p.is_bf16, W1MN ? 1u : 0u, kBlockM, p.N1p);
+  const uint32_t idesc0 = idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p);
+  const uint32_t idesc1 = idesc_f16_f32(BF16 ? 1u : 0u, W1MN ? 1u : 0u, kBlockM, p.N1p);
   bool ok = true;
   const uint32_t lead = elect_one();
   Tracer trace(p, 1, lead);
   if (p.resident)
     ok = warp_mbar_wait(bars + 8u * BAR_WFULL, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
+  if (ok) ok = warp_mbar_wait(bars + 8u * BAR_BIAS_READY, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
 
   // Descriptors of every operand region, built once; a ring stage / weight chunk / P
   // chunk is then a multiple of its byte size (in 16-byte units) added to them.
@@ -325,6 +348,15 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const uint64_t res_w1 = sdesc_sw128(base + p.off_w1, w1_lbo, 1024u);
   const uint64_t p_desc0 = sdesc_sw128(base + p.off_p[0], 16u, 1024u);
   const uint64_t p_desc1 = sdesc_sw128(base + p.off_p[1], 16u, 1024u);
+  // Bias step operands (see fill_bias_operands): B is MN-major whatever the weights are.
+  const uint32_t ones_addr = base + p.off_bias;
+  const uint32_t n0blk = static_cast<uint32_t>((p.N0p + 63) >> 6);
+  const uint64_t ones_desc = sdesc_sw128(ones_addr, 16u, 0u);
+  const uint64_t bias0_desc = sdesc_sw128(ones_addr + kOnesBytes, kBiasBlockBytes, 1024u);
+  const uint64_t bias1_desc =
+      sdesc_sw128(ones_addr + kOnesBytes + n0blk * kBiasBlockBytes, kBiasBlockBytes, 1024u);
+  const uint32_t idesc_b0 = idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N0p);
+  const uint32_t idesc_b1 = idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N1p);
   const uint32_t stage_step = p.stage_bytes >> 4;
   const uint32_t w0_step = p.w0_chunk_bytes >> 4, w1_step = p.w1_chunk_bytes >> 4;
   // K steps of GEMM0's chunks: full (4) except the last channel block of each tap / the
@@ -342,8 +374,9 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   auto issue_g0 = [&](int it) -> bool {
     const int32_t t = blockIdx.x + it * gridDim.x;
     const uint32_t b = (MODE != MODE_CHAIN || p.acc_dual) ? static_cast<uint32_t>(it & 1) : 0u;
-    if (MODE != MODE_CHAIN) {
-      // The epilogue must have drained the buffer's previous tile.
+    if (MODE != MODE_CHAIN || p.p_tmem) {
+      // The epilogue must have drained the buffer's previous tile (with P in TMEM: its
+      // GEMM1 accumulator, the last thing read from the buffer).
       const uint32_t u = static_cast<uint32_t>(it >> 1);
       if (!warp_mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), (u & 1u) ^ 1u, p, abort_flag,
                           SITE_MMA_ACC_EMPTY, t))
@@ -355,6 +388,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       tc_fence_after_sync();
     }
     const uint32_t d0 = tmem_base + p.d0_col[b];
+    mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0, 0u);   // D0 = bias
     int cb = 0;   // channel block within the tap (4-D) / chunk index (2-D)
     for (int kc = 0; kc < p.kchunks0; ++kc) {
       trace(EV_MMA_WAIT, kc, it);
@@ -366,7 +400,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
                                         : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
       const int nks = cb == p.kc_per_tap - 1 ? last_nks : 4;
       if (++cb == p.kc_per_tap) cb = 0;
-      issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
+      issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks);
       trace(EV_MMA_ISSUED, kc, it);
       mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
       if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
@@ -386,6 +420,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     trace(EV_MMA_P_READY, b, j);
     tc_fence_after_sync();
     const uint32_t d1 = tmem_base + p.d1_col[b];
+    mma_f16_ss(lead, d1, ones_desc, bias1_desc, idesc_b1, 0u);   // D1 = bias
     for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
       uint64_t bdesc;
       if (p.resident) {
@@ -394,11 +429,17 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL,
                             t))
           return false;
+        trace(EV_MMA_W1_FULL, kc1, j);
         bdesc = ring_w1 + static_cast<uint64_t>(stage) * stage_step;
       }
-      const uint64_t adesc = (b ? p_desc1 : p_desc0) + static_cast<uint64_t>(kc1) * (kPChunkBytes >> 4);
-      issue_chunk<W1MN>(lead, d1, adesc, bdesc, idesc1, kc1 == p.kchunks1 - 1 ? last_nks1 : 4,
-                        kc1 == 0);
+      const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
+      if (p.p_tmem) {
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1);
+      } else {
+        const uint64_t adesc =
+            (b ? p_desc1 : p_desc0) + static_cast<uint64_t>(kc1) * (kPChunkBytes >> 4);
+        issue_chunk<W1MN>(lead, d1, adesc, bdesc, idesc1, nks1);
+      }
       if (!p.resident) {
         mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));
         if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
@@ -410,7 +451,16 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   };
 
   if (ok) {
-    if (MODE == MODE_CHAIN) {
+    if (MODE == MODE_CHAIN && p.p_tmem) {
+      // Pairs of tiles: while the epilogue of one tile drains, the other tile's MMAs run.
+      for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = issue_g0(it);
+      for (int k = 0; ok && k < ntiles; k += 2) {
+        ok = issue_g1(k);
+        if (ok && k + 1 < ntiles) ok = issue_g1(k + 1);
+        if (ok && k + 2 < ntiles) ok = issue_g0(k + 2);
+        if (ok && k + 3 < ntiles) ok = issue_g0(k + 3);
+      }
+    } else if (MODE == MODE_CHAIN) {
       // A D0 buffer is free again once the epilogue has published that tile's P, so
       // G0(j+L) follows G1(j); with two buffers (L = 2) two tiles are in flight.
       const int L = p.acc_dual ? 2 : 1;
@@ -435,22 +485,26 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
 // ------------------------------------------------------------------------------------
 template <int ACT>
 __device__ __forceinline__ float act_fn(float x) {
-  if constexpr (ACT == 1) return fmaxf(x, 0.0f);
   // hardswish(x) = x * min(max(x + 3, 0), 6) / 6 = x * clamp(x / 6 + 1/2, 0, 1):
   // one fused multiply-add with saturation and one multiply.
   if constexpr (ACT == 2) return x * __saturatef(fmaf(x, 1.0f / 6.0f, 0.5f));
   return x;
 }
 
-template <bool BF16>
+// Two fp32 values -> one packed fp16/bf16 pair (lo in the low half), round to nearest
+// even; RELU clamps negative results to zero in the same conversion.
+template <bool BF16, bool RELU>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (BF16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  } else {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
+  uint32_t r;
+  if constexpr (BF16 && RELU)
+    asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else if constexpr (BF16)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else if constexpr (RELU)
+    asm("cvt.rn.relu.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Stores 16 consecutive columns [c0, c0+16) of row `row` into a K-major, 128B-swizzled
@@ -471,77 +525,93 @@ __device__ __forceinline__ void st_row16_sw128(uint32_t tile, int row, int c0,
                : "memory");
 }
 
+// 16 accumulator columns (the bias is already in them) -> act -> 8 packed pairs.
 template <bool BF16, int ACT>
-__device__ __forceinline__ void convert16(const uint32_t (&r)[16], const float* bias, int c,
-                                          uint32_t (&out)[8]) {
-  const float4* b4 = reinterpret_cast<const float4*>(bias + c);
+__device__ __forceinline__ void convert16(const uint32_t (&r)[16], uint32_t (&out)[8]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 bb = b4[q];
-    out[2 * q] = pack2<BF16>(act_fn<ACT>(__uint_as_float(r[4 * q]) + bb.x),
-                             act_fn<ACT>(__uint_as_float(r[4 * q + 1]) + bb.y));
-    out[2 * q + 1] = pack2<BF16>(act_fn<ACT>(__uint_as_float(r[4 * q + 2]) + bb.z),
-                                 act_fn<ACT>(__uint_as_float(r[4 * q + 3]) + bb.w));
-  }
+  for (int j = 0; j < 8; ++j)
+    out[j] = pack2<BF16, ACT == 1>(act_fn<ACT>(__uint_as_float(r[2 * j])),
+                                   act_fn<ACT>(__uint_as_float(r[2 * j + 1])));
 }
 
-template <bool BF16, int ACT>
-__device__ __forceinline__ void convert_store16(const uint32_t (&r)[16], const float* bias, int c,
-                                                uint32_t tile, int row, uint32_t chunk_bytes) {
-  uint32_t v[8];
-  convert16<BF16, ACT>(r, bias, c, v);
-  st_row16_sw128(tile, row, c, chunk_bytes, v);
-}
+// The drains below walk a row's TMEM columns in steps of 32: both 16-column loads of a
+// step are issued together and waited for once, then converted.  This plain loop (no
+// loads carried across iterations, no early exits) measured faster than a software-
+// pipelined one whose exits depend on the run-time column count.  The drains are called,
+// not inlined: one inlined copy per activation pushed the kernel past its register
+// budget (168 per thread with ten warps) and made it spill.
 
-// TMEM columns of this thread's row -> bias -> act -> dtype -> smem tile.  The columns are
-// the 16-wide units u = 0, 1, ... at c_first + (u / 2) * c_step + (u % 2) * 16 below ncols
-// (c_step = 32: all columns; 64: every other 32-column block).  Software-pipelined: the
-// TMEM load of unit u+1 is in flight while unit u is converted and stored.
+// TMEM columns of this thread's row -> act -> dtype -> K-major 128B-swizzled smem
+// tile.  The 32-column blocks c_first, c_first + c_step, ... below ncols (c_step = 32:
+// all columns; 64: every other block).  ncols is a multiple of 16.
 template <bool BF16, int ACT>
-__device__ __forceinline__ void drain_to_smem(uint32_t tm_lane, uint32_t col0, int c_first,
-                                              int c_step, int ncols, const float* bias,
-                                              uint32_t tile, int row, uint32_t chunk_bytes) {
-  auto col = [&](int u) { return c_first + (u >> 1) * c_step + ((u & 1) << 4); };
-  int u = 0;
-  if (col(0) >= ncols) return;
-  uint32_t a[16], b[16];
-  tmem_ld16(tm_lane + col0 + col(0), a);
-  tmem_wait_ld(a);
-  while (true) {
-    const int ca = col(u), cb = col(u + 1);
-    if (cb < ncols) tmem_ld16(tm_lane + col0 + cb, b);
-    convert_store16<BF16, ACT>(a, bias, ca, tile, row, chunk_bytes);
-    if (cb >= ncols) break;
-    tmem_wait_ld(b);
-    const int cn = col(u + 2);
-    if (cn < ncols) tmem_ld16(tm_lane + col0 + cn, a);
-    convert_store16<BF16, ACT>(b, bias, cb, tile, row, chunk_bytes);
-    if (cn >= ncols) break;
-    tmem_wait_ld(a);
-    u += 2;
+__device__ __noinline__ void drain_to_smem_act(uint32_t tm_lane, uint32_t col0, int c_first,
+                                                  int c_step, int ncols, uint32_t tile,
+                                                  int row, uint32_t chunk_bytes) {
+  for (int c = c_first; c < ncols; c += c_step) {
+    const bool two = c + 16 < ncols;
+    uint32_t a[16], b[16], v[8];
+    tmem_ld32(tm_lane + col0 + c, two, a, b);
+    tmem_wait_ld(a, b);
+    convert16<BF16, ACT>(a, v);
+    st_row16_sw128(tile, row, c, chunk_bytes, v);
+    if (two) {
+      convert16<BF16, ACT>(b, v);
+      st_row16_sw128(tile, row, c + 16, chunk_bytes, v);
+    }
   }
 }
 
 template <bool BF16>
-__device__ __forceinline__ void drain_to_smem_act(int act, uint32_t tm_lane, uint32_t col0,
-                                                  int c_first, int c_step, int ncols,
-                                                  const float* bias, uint32_t tile, int row,
-                                                  uint32_t chunk_bytes) {
-  if (act == 1)
-    drain_to_smem<BF16, 1>(tm_lane, col0, c_first, c_step, ncols, bias, tile, row, chunk_bytes);
-  else if (act == 2)
-    drain_to_smem<BF16, 2>(tm_lane, col0, c_first, c_step, ncols, bias, tile, row, chunk_bytes);
+__device__ __forceinline__ void drain_to_smem(int act, uint32_t tm_lane, uint32_t col0,
+                                              int c_first, int c_step, int ncols, uint32_t tile,
+                                              int row, uint32_t chunk_bytes) {
+  if (act == 2)
+    drain_to_smem_act<BF16, 2>(tm_lane, col0, c_first, c_step, ncols, tile, row, chunk_bytes);
+  else if (act == 1)
+    drain_to_smem_act<BF16, 1>(tm_lane, col0, c_first, c_step, ncols, tile, row, chunk_bytes);
   else
-    drain_to_smem<BF16, 0>(tm_lane, col0, c_first, c_step, ncols, bias, tile, row, chunk_bytes);
+    drain_to_smem_act<BF16, 0>(tm_lane, col0, c_first, c_step, ncols, tile, row, chunk_bytes);
 }
 
-// Pool epilogue.  Tile row = 16 * h + w over an 8 x 16 conv-output tile, so warp q holds
-// conv rows 2q and 2q+1: the horizontal partner of a pixel sits in lane ^ 1 and the
-// vertical one in lane ^ 16.  The max of the four fp32 sums is taken first; adding the
-// bias, ReLU and rounding are monotone, so this equals pooling the rounded ReLU output.
+// GEMM0 accumulator columns [col0, col0 + ncols) of this thread's row -> act -> dtype -> packed pairs written back into TMEM at p_col0 + c / 2.  With p_col0 = col0, P
+// overwrites columns of D0 this thread has already read: the step at c writes columns
+// below col0 + c / 2 + 16 <= col0 + c + 32, the next step's first column.  Valid only
+// when one warpgroup owns the whole row.
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain_to_tmem_act(uint32_t tm_lane, uint32_t col0, int ncols,
+                                                  uint32_t p_col0) {
+  for (int c = 0; c < ncols; c += 32) {
+    const bool two = c + 16 < ncols;
+    uint32_t a[16], b[16], v[8];
+    tmem_ld32(tm_lane + col0 + c, two, a, b);
+    tmem_wait_ld(a, b);
+    convert16<BF16, ACT>(a, v);
+    tmem_st8(tm_lane + p_col0 + (c >> 1), v);
+    if (two) {
+      convert16<BF16, ACT>(b, v);
+      tmem_st8(tm_lane + p_col0 + ((c + 16) >> 1), v);
+    }
+  }
+  tmem_wait_st();
+}
+
 template <bool BF16>
-__device__ __forceinline__ void pool_store16(const uint32_t (&r)[16], const float* bias, int c,
-                                             uint32_t tile, int prow, bool owner) {
+__device__ __forceinline__ void drain_to_tmem(int act, uint32_t tm_lane, uint32_t col0,
+                                              int ncols, uint32_t p_col0) {
+  if (act == 2)
+    drain_to_tmem_act<BF16, 2>(tm_lane, col0, ncols, p_col0);
+  else if (act == 1)
+    drain_to_tmem_act<BF16, 1>(tm_lane, col0, ncols, p_col0);
+  else
+    drain_to_tmem_act<BF16, 0>(tm_lane, col0, ncols, p_col0);
+}
+
+// 2x2 max of 16 columns across the four lanes of each pooling window, then ReLU and
+// rounding by the window's owner lane, stored to the pooled staging tile.
+template <bool BF16>
+__device__ __forceinline__ void pool_store16(const uint32_t (&r)[16], int c, uint32_t tile,
+                                             int prow, bool owner) {
   float m[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -553,37 +623,29 @@ __device__ __forceinline__ void pool_store16(const uint32_t (&r)[16], const floa
   if (owner) {
     uint32_t v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      v[j] = pack2<BF16>(fmaxf(m[2 * j] + bias[c + 2 * j], 0.0f),
-                         fmaxf(m[2 * j + 1] + bias[c + 2 * j + 1], 0.0f));
+    for (int j = 0; j < 8; ++j) v[j] = pack2<BF16, true>(m[2 * j], m[2 * j + 1]);
     st_row16_sw128(tile, prow, c, kPoolChunkBytes, v);
   }
 }
 
 // Pool epilogue.  Tile row = 16 * h + w over an 8 x 16 conv-output tile, so warp q holds
 // conv rows 2q and 2q+1: the horizontal partner of a pixel sits in lane ^ 1 and the
-// vertical one in lane ^ 16.  The max of the four fp32 sums is taken first; adding the
-// bias, ReLU and rounding are monotone, so this equals pooling the rounded ReLU output.
-// TMEM loads of the next 16 columns overlap the current ones' reduction.
+// vertical one in lane ^ 16.  The accumulators already hold the bias, which is the same
+// for the four pixels of a window, so the max of the four sums equals the max of the
+// biased values; ReLU and rounding are monotone, so taking them after the max equals
+// pooling the rounded ReLU output.
 template <bool BF16>
-__device__ __forceinline__ void drain_pool(uint32_t tm_lane, uint32_t col0, int ncols,
-                                           const float* bias, uint32_t tile, int q, int lane) {
+__device__ __noinline__ void drain_pool(uint32_t tm_lane, uint32_t col0, int ncols,
+                                           uint32_t tile, int q, int lane) {
   const bool owner = (lane & 17) == 0;
   const int prow = q * 8 + (lane >> 1);
-  uint32_t a[16], b[16];
-  tmem_ld16(tm_lane + col0, a);
-  tmem_wait_ld(a);
   for (int c = 0; c < ncols; c += 32) {
-    const bool nb = c + 16 < ncols;
-    if (nb) tmem_ld16(tm_lane + col0 + c + 16, b);
-    pool_store16<BF16>(a, bias, c, tile, prow, owner);
-    if (!nb) break;
-    tmem_wait_ld(b);
-    const bool na = c + 32 < ncols;
-    if (na) tmem_ld16(tm_lane + col0 + c + 32, a);
-    pool_store16<BF16>(b, bias, c + 16, tile, prow, owner);
-    if (!na) break;
-    tmem_wait_ld(a);
+    const bool two = c + 16 < ncols;
+    uint32_t a[16], b[16];
+    tmem_ld32(tm_lane + col0 + c, two, a, b);
+    tmem_wait_ld(a, b);
+    pool_store16<BF16>(a, c, tile, prow, owner);
+    if (two) pool_store16<BF16>(b, c + 16, tile, prow, owner);
   }
 }
 
@@ -613,7 +675,7 @@ __device__ __forceinline__ bool warp_wait(bool alive, uint32_t bar, uint32_t par
 // take every tile and warpgroup g drains the 32-column blocks 2k + g.
 template <int MODE, bool A4D, bool BF16>
 __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, uint32_t base,
-                              uint32_t bars, uint32_t tmem_base, const float* bias_s,
+                              uint32_t bars, uint32_t tmem_base,
                               volatile uint32_t* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wg = (warp - 2) >> 2;             // warpgroup 0 or 1
@@ -649,9 +711,13 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
         if (elected) bulk_wait_read_all();
         named_bar_sync(bar_id, group_threads);
       }
-      if (alive)
-        drain_to_smem_act<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, bias_s,
-                                p_tile, row, kPChunkBytes);
+      if (alive) {
+        if (p.p_tmem)
+          drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b], p.N0p, p.d0_col[b]);
+        else
+          drain_to_smem<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, p_tile,
+                              row, kPChunkBytes);
+      }
       tc_fence_before_sync();
       fence_proxy_async_smem();
       __syncwarp();
@@ -668,9 +734,13 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       }
       if (elected) trace(EV_EPI_STAGING, g, it);
       if (alive)
-        drain_to_smem_act<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p,
-                                bias_s + p.N0p, out_tile, row, kPChunkBytes);
+        drain_to_smem<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p, out_tile,
+                            row, kPChunkBytes);
       tc_fence_before_sync();
+      if (p.p_tmem) {   // the buffer (D0 -> P + D1) may take tile i + 2
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + b));
+      }
       fence_proxy_async_smem();
       named_bar_sync(bar_id, group_threads);
       if (elected && !*abort_flag) {
@@ -688,10 +758,10 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       if (elected) trace(EV_EPI_STAGING, g, it);
       if (alive) {
         if (MODE == MODE_POOL)
-          drain_pool<BF16>(tm_lane, p.d0_col[b], p.N0p, bias_s, out_tile, q, lane);
+          drain_pool<BF16>(tm_lane, p.d0_col[b], p.N0p, out_tile, q, lane);
         else
-          drain_to_smem_act<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, bias_s,
-                                  out_tile, row, kPChunkBytes);
+          drain_to_smem<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, out_tile,
+                              row, kPChunkBytes);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -716,9 +786,56 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
 }
 
 // ------------------------------------------------------------------------------------
+// bias operands
+// ------------------------------------------------------------------------------------
+// The bias enters every GEMM as its first K step, D = ONES . BIAS (accumulate off), so the
+// epilogue never reads it.  ONES is a K-major 128B-swizzled A tile whose row m holds 1 at
+// k = 0 and 0 at k = 1..15; all its 8-row groups are equal, so the descriptor's group
+// stride is 0 and the tile is a single 1 KiB swizzle atom (row r, k = 0 sits at byte
+// r * 128 + (0 ^ r) * 16).  BIAS is an MN-major 128B-swizzled B tile with 16 k-rows per
+// 64-wide N block (2 KiB): k-row 0 holds the block's 64 biases (unswizzled, as row 0),
+// the other rows are 0.  The product is the bias broadcast to all 128 rows, exact in
+// fp32.  Written by the epilogue warps with generic stores.
+template <bool BF16>
+__device__ __forceinline__ void fill_bias_operands(const ChainParams& p, uint32_t* region,
+                                                   int tid, int nthreads, bool chain) {
+  const int n0blk = (p.N0p + 63) >> 6;
+  const int n1blk = chain ? (p.N1p + 63) >> 6 : 0;
+  const int b0_bytes = n0blk * static_cast<int>(kBiasBlockBytes);
+  const int nwords =
+      (static_cast<int>(kOnesBytes) + (n0blk + n1blk) * static_cast<int>(kBiasBlockBytes)) >> 2;
+  const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
+  for (int w = tid; w < nwords; w += nthreads) {
+    const int o = w << 2;
+    uint32_t v = 0;
+    if (o < static_cast<int>(kOnesBytes)) {
+      const int r = o >> 7;
+      if (o == r * 128 + r * 16) v = one;
+    } else {
+      int lo = o - static_cast<int>(kOnesBytes);
+      const uint16_t* src = p.b0;
+      int n_valid = p.N0;
+      if (lo >= b0_bytes) {
+        lo -= b0_bytes;
+        src = p.b1;
+        n_valid = p.N1;
+      }
+      const int within = lo & static_cast<int>(kBiasBlockBytes - 1);
+      if (within < 128 && src != nullptr) {
+        const int n = (lo / static_cast<int>(kBiasBlockBytes)) * 64 + (within >> 1);
+        const uint32_t e0 = n < n_valid ? src[n] : 0u;
+        const uint32_t e1 = n + 1 < n_valid ? src[n + 1] : 0u;
+        v = e0 | (e1 << 16);
+      }
+    }
+    region[w] = v;
+  }
+}
+
+// ------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------
-template <int MODE, bool A4D, bool W0MN, bool W1MN>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16>
 __global__ void __launch_bounds__(kNumThreads, 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW0,
                  const __grid_constant__ CUtensorMap tmW1,
@@ -730,7 +847,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const uint32_t bars = base + p.off_bar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + p.off_bar + 8u * BAR_COUNT);
   volatile uint32_t* abort_flag = tmem_slot + 1;
-  float* bias_s = reinterpret_cast<float*>(base_ptr + p.off_bias);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t warps_per_group = static_cast<uint32_t>(kNumEpiWarps / p.epi_groups);
@@ -748,9 +864,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars + 8u * (BAR_D1_FULL0 + a), 1);
     }
     mbar_init(bars + 8u * BAR_MMA_DONE, 1);
+    mbar_init(bars + 8u * BAR_BIAS_READY, kNumEpiWarps);
     *abort_flag = 0u;
     fence_barrier_init();
     fence_proxy_async_smem();
+    // This grid is resident in one wave, so the next kernel may be scheduled now; its
+    // CTAs take an SM as this grid's CTAs leave and wait for this grid before touching
+    // global memory.
+    grid_launch_dependents();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
@@ -762,41 +883,32 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
     tmem_relinquish();
   }
-  if (warp >= 2) {
-    for (int i = threadIdx.x - 64; i < p.N0p + p.N1p; i += kNumEpiThreads) {
-      float v = 0.0f;
-      const uint16_t* src = nullptr;
-      int j = i;
-      if (i < p.N0p) {
-        if (i < p.N0) src = p.b0;
-      } else {
-        j = i - p.N0p;
-        if (j < p.N1) src = p.b1;
-      }
-      if (src != nullptr) {
-        const uint16_t bits = src[j];
-        v = p.is_bf16 ? __uint_as_float(static_cast<uint32_t>(bits) << 16)
-                      : __half2float(__ushort_as_half(bits));
-      }
-      bias_s[i] = v;
-    }
-  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
+  // Global memory is touched only after the previous kernel of the stream has completed
+  // (inputs may be its outputs, outputs its inputs); the setup above overlaps its tail.
   if (warp == 0) {
+    grid_dependency_wait();
     producer_role<MODE, A4D, W0MN, W1MN>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    mma_role<MODE, A4D, W0MN, W1MN>(p, base, bars, tmem_base, abort_flag);
+    grid_dependency_wait();   // so that no bounded wait below runs while it is pending
+    mma_role<MODE, A4D, W0MN, W1MN, BF16>(p, base, bars, tmem_base, abort_flag);
     __syncwarp();
   } else {
-    if (p.is_bf16)
-      epilogue_role<MODE, A4D, true>(p, &tmOut, base, bars, tmem_base, bias_s, abort_flag);
-    else
-      epilogue_role<MODE, A4D, false>(p, &tmOut, base, bars, tmem_base, bias_s, abort_flag);
+    // The bias operands, off the producer's critical path; the MMA issuer waits for them
+    // before its first MMA.
+    grid_dependency_wait();
+    fill_bias_operands<BF16>(p, reinterpret_cast<uint32_t*>(base_ptr + p.off_bias),
+                             static_cast<int>(threadIdx.x) - 64, kNumEpiThreads,
+                             MODE == MODE_CHAIN);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8u * BAR_BIAS_READY);
+    epilogue_role<MODE, A4D, BF16>(p, &tmOut, base, bars, tmem_base, abort_flag);
   }
 
   tc_fence_before_sync();

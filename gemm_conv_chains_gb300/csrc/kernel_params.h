@@ -54,6 +54,8 @@ enum TraceEvent : uint32_t {
   EV_EPI_STORED = 12,    // epilogue group issued the tile's TMA store
   EV_MMA_WAIT = 13,      // MMA issuer starts waiting for a ring slot
   EV_MMA_ISSUED = 14,    // MMA issuer issued a slot's MMAs
+  EV_PROD_W1_ISSUED = 15,  // producer issued a streamed GEMM1 weight chunk
+  EV_MMA_W1_FULL = 16,     // MMA issuer saw a streamed GEMM1 weight chunk land
 };
 
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M
@@ -62,6 +64,10 @@ constexpr int kNumEpiWarps = 8;       // two warpgroups of four (one per TMEM la
 constexpr int kNumEpiThreads = 32 * kNumEpiWarps;
 constexpr int kNumThreads = 64 + kNumEpiThreads;   // warp 0 TMA, warp 1 MMA + TMEM, 2..9 epilogue
 constexpr int kMaxStages = 8;
+// Bias operands in shared memory (at off_bias): a 1 KiB ONES tile, then per GEMM one
+// 2 KiB BIAS block per 64-wide N block.
+constexpr uint32_t kOnesBytes = 1024;
+constexpr uint32_t kBiasBlockBytes = 2048;
 constexpr uint32_t kABytes = kBlockM * kChunkK * 2;   // 16 KiB A chunk
 constexpr uint32_t kPChunkBytes = kBlockM * 128;      // 128 rows x 64 cols x 2 B
 constexpr uint32_t kPoolChunkBytes = 32 * 128;        // 4h x 8w pooled pixels x 64 ch
@@ -92,6 +98,9 @@ struct ChainParams {
   int32_t out_alias_p;          // 1: output staging b shares P buffer b
   int32_t acc_dual;             // 1: accumulators (and, chained, P) double-buffered:
                                 //    tile i uses buffer i & 1, two tiles in flight
+  int32_t p_tmem;               // 1 (chain): P is written back into TMEM over the consumed
+                                //    GEMM0 columns and GEMM1 reads A from TMEM; tiles are
+                                //    processed in pairs, buffer b holds D0 -> P + D1
   int32_t epi_groups;           // 2: the epilogue warpgroups take alternate tiles;
                                 // 1: both warpgroups split the columns of every tile
   uint32_t tmem_cols;

@@ -1,0 +1,79 @@
+// kernel_units.cuh -- the compiled instantiations of the chain kernel, per operand dtype.
+// Each kernels_<a2d|a4d>_<dtype>.cu instantiates one group, so the units compile in
+// parallel and every kernel holds the epilogue of one dtype only.
+#pragma once
+
+#include "chain_kernel.cuh"
+#include "launch.h"
+
+namespace b2b {
+
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16>
+const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(&chain_kernel<MODE, A4D, W0MN, W1MN, BF16>);
+}
+
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1,
+                       const CUtensorMap& out, const ChainParams& p, int grid, size_t smem,
+                       cudaStream_t stream) {
+  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16>, a, w0, w1, out, p, grid, smem,
+                      stream);
+}
+
+// 2-D A operand: GEMM chains (row-major weights) and 1x1 convs (K-major filters).
+template <bool BF16>
+const void* variant_func_a2d(Variant v) {
+  switch (v) {
+    case V_GEMM_CHAIN: return kernel_ptr<MODE_CHAIN, false, true, true, BF16>();
+    case V_CONV1X1_CHAIN: return kernel_ptr<MODE_CHAIN, false, false, false, BF16>();
+    case V_GEMM_SINGLE: return kernel_ptr<MODE_SINGLE, false, true, false, BF16>();
+    case V_CONV1X1_SINGLE: return kernel_ptr<MODE_SINGLE, false, false, false, BF16>();
+    default: return nullptr;
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
+                               const CUtensorMap& w1, const CUtensorMap& out,
+                               const ChainParams& p, int grid, size_t smem, cudaStream_t s) {
+  switch (v) {
+    case V_GEMM_CHAIN:
+      return launch_one<MODE_CHAIN, false, true, true, BF16>(a, w0, w1, out, p, grid, smem, s);
+    case V_CONV1X1_CHAIN:
+      return launch_one<MODE_CHAIN, false, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    case V_GEMM_SINGLE:
+      return launch_one<MODE_SINGLE, false, true, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    case V_CONV1X1_SINGLE:
+      return launch_one<MODE_SINGLE, false, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// 4-D A operand: implicit-GEMM convs (chain, single, conv + max-pool).
+template <bool BF16>
+const void* variant_func_a4d(Variant v) {
+  switch (v) {
+    case V_CONV_CHAIN: return kernel_ptr<MODE_CHAIN, true, false, false, BF16>();
+    case V_CONV_SINGLE: return kernel_ptr<MODE_SINGLE, true, false, false, BF16>();
+    case V_CONV_POOL: return kernel_ptr<MODE_POOL, true, false, false, BF16>();
+    default: return nullptr;
+  }
+}
+
+template <bool BF16>
+cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
+                               const CUtensorMap& w1, const CUtensorMap& out,
+                               const ChainParams& p, int grid, size_t smem, cudaStream_t s) {
+  switch (v) {
+    case V_CONV_CHAIN:
+      return launch_one<MODE_CHAIN, true, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    case V_CONV_SINGLE:
+      return launch_one<MODE_SINGLE, true, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    case V_CONV_POOL:
+      return launch_one<MODE_POOL, true, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace b2b

@@ -8,11 +8,15 @@
 
 namespace b2b {
 
+template <bool BF16>
 const void* variant_func_a2d(Variant v);
+template <bool BF16>
 const void* variant_func_a4d(Variant v);
+template <bool BF16>
 cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
                                const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
                                int grid, size_t smem, cudaStream_t s);
+template <bool BF16>
 cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
                                const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
                                int grid, size_t smem, cudaStream_t s);
@@ -21,15 +25,19 @@ static bool is_a4d(Variant v) {
   return v == V_CONV_CHAIN || v == V_CONV_SINGLE || v == V_CONV_POOL;
 }
 
-const void* variant_func(Variant v) {
-  return is_a4d(v) ? variant_func_a4d(v) : variant_func_a2d(v);
+const void* variant_func(Variant v, bool bf16) {
+  if (is_a4d(v)) return bf16 ? variant_func_a4d<true>(v) : variant_func_a4d<false>(v);
+  return bf16 ? variant_func_a2d<true>(v) : variant_func_a2d<false>(v);
 }
 
 cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
                            const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
                            int grid, size_t smem, cudaStream_t stream) {
-  return is_a4d(v) ? launch_variant_a4d(v, a, w0, w1, out, p, grid, smem, stream)
-                   : launch_variant_a2d(v, a, w0, w1, out, p, grid, smem, stream);
+  if (is_a4d(v))
+    return p.is_bf16 ? launch_variant_a4d<true>(v, a, w0, w1, out, p, grid, smem, stream)
+                     : launch_variant_a4d<false>(v, a, w0, w1, out, p, grid, smem, stream);
+  return p.is_bf16 ? launch_variant_a2d<true>(v, a, w0, w1, out, p, grid, smem, stream)
+                   : launch_variant_a2d<false>(v, a, w0, w1, out, p, grid, smem, stream);
 }
 
 // ------------------------------------------------------------------------------------

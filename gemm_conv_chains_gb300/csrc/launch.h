@@ -23,9 +23,32 @@ enum Variant : int {
   V_COUNT
 };
 
-// Kernel function pointer of a variant (for cudaFuncSetAttribute).
-const void* variant_func(Variant v);
+using ChainKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, ChainParams);
 
+// Launches a chain kernel with programmatic stream serialisation: the kernel may be
+// scheduled while the previous kernel of the stream finishes, and it waits for that
+// kernel (griddepcontrol.wait) before it touches global memory.
+inline cudaError_t launch_chain(ChainKernelFn fn, const CUtensorMap& a, const CUtensorMap& w0,
+                                const CUtensorMap& w1, const CUtensorMap& out,
+                                const ChainParams& p, int grid, size_t smem,
+                                cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(kNumThreads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, a, w0, w1, out, p);
+}
+
+// Kernel function pointer of a variant and operand dtype (for cudaFuncSetAttribute).
+const void* variant_func(Variant v, bool bf16);
+
+// Launches the variant's kernel for p.is_bf16.
 cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
                            const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
                            int grid, size_t smem, cudaStream_t stream);

@@ -152,6 +152,17 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the stream
+// (launched with programmatic stream serialisation) be scheduled while this grid still
+// runs; dependency_wait blocks until every prerequisite grid has completed and its memory
+// is visible, and returns at once when the kernel was launched without a prerequisite.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------
 // TMA
 // ------------------------------------------------------------------------------------
@@ -295,6 +306,19 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t pred, uint32_t d_tmem, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem] ("TS" form): A is 128 lanes (rows) x 16 K elements packed
+// two per 32-bit column, 8 columns per K step.  Issued only where pred != 0.
+__device__ __forceinline__ void mma_f16_ts(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem,
+                                           uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 q, %0, 0;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p;\n\t}" ::"r"(pred),
+      "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives (once) on `bar` when every tcgen05.mma previously issued by this thread is done;
 // issued only where pred != 0 (the lane that issued the MMAs).
 __device__ __forceinline__ void mma_commit(uint32_t pred, uint32_t bar) {
@@ -315,6 +339,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+
+// 32 lanes x 32 bits, 8 consecutive columns from registers (thread t -> lane base + t).
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -277,7 +277,8 @@ def probe_timeout(limit_ns: int, stream=None) -> None:
 TRACE_EVENTS = {1: "prod_acquire", 2: "prod_issued", 3: "mma_full", 4: "mma_g0_done",
                 5: "mma_p_ready", 6: "mma_g1_done", 7: "mma_acc_free", 8: "epi_acc_ready",
                 9: "epi_p_done", 10: "epi_d1_ready", 11: "epi_staging", 12: "epi_stored",
-                13: "mma_wait", 14: "mma_issued"}
+                13: "mma_wait", 14: "mma_issued",
+                15: "prod_w1_issued", 16: "mma_w1_full"}
 
 
 def set_trace(buf, cta: int = 0) -> None:

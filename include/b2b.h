@@ -189,7 +189,8 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * bias offset, bias bytes, barrier offset, barrier bytes, TMEM columns, GEMM0 accumulator
  * columns [2], GEMM1 accumulator columns [2], two tiles in flight (0/1), epilogue groups
  * (1/2), tiles, GEMM0 K chunks, GEMM1 K chunks, padded N0, padded N1, kernel mode
- * (0 chain, 1 single, 2 pool), 0.
+ * (0 chain, 1 single, 2 pool), and 1 if the chain's intermediate is kept in TMEM instead
+ * of shared memory (wide N0: GEMM1 then reads its A operand from TMEM).
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,

@@ -40,6 +40,10 @@ GEMM_SHAPES = [
     ("f16", 640, 128, 128, 256),
     ("f16", 200, 320, 96, 200),
     ("bf16", 384, 64, 256, 256),
+    # wide N0: the intermediate is kept in TMEM (checked by test_plan)
+    ("f16", 300, 128, 256, 64),
+    ("bf16", 257, 72, 200, 72),
+    ("f16", 1000, 64, 224, 96),
 ]
 
 

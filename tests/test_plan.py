@@ -5,7 +5,8 @@ kernel's accesses into it, and TMEM accumulators fit the allocation.
 The sizes below are re-derived from what the kernel writes and reads, independently of
 the planner: A chunks are 128 rows x 128 B; a weight chunk is 64 K-rows x 128 B per
 64-wide N block (row-major weights) or N x 128 B (K-major filters); the P tile and the
-output staging hold 16 KiB per 64 columns; a pooled staging tile 4 KiB per 64 columns.
+output staging hold 16 KiB per 64 columns; a pooled staging tile 4 KiB per 64 columns;
+the bias operands of the MMA 1 KiB plus 2 KiB per 64 columns of each GEMM.
 """
 import ctypes
 import itertools
@@ -19,7 +20,7 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "off_w1", "w_res", "w0_chunk", "w1_chunk", "off_p0", "off_p1", "p", "off_out0",
           "off_out1", "out", "off_bias", "bias", "off_bar", "bar", "tmem_cols", "d0_col0",
           "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0", "kchunks1",
-          "N0p", "N1p", "mode", "zero"]
+          "N0p", "N1p", "mode", "p_tmem"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4}
@@ -65,10 +66,12 @@ def check(kind, dims, row_major_w):
     assert groups in (1, 2) and (groups == 1 or dual)
     if mode == 2:
         assert groups == 2                       # the pool epilogue needs whole rows per warp
-    # P buffers used: tile i -> P[i & 1] when dual, else P[0]
-    pbufs = (2 if dual else 1) if mode == 0 else 0
+    p_tmem = p["p_tmem"] == 1
+    assert not p_tmem or (mode == 0 and dual and groups == 2 and not p["alias"])
+    # P buffers used: tile i -> P[i & 1] when dual, else P[0]; none when P is in TMEM
+    pbufs = 0 if p_tmem else ((2 if dual else 1) if mode == 0 else 0)
     obufs = 2 if groups == 2 else 1
-    if mode == 0:
+    if mode == 0 and not p_tmem:
         need_p = max(p_need, out_need) if p["alias"] else p_need
         assert p["p"] >= need_p
         for b in range(pbufs):
@@ -82,8 +85,9 @@ def check(kind, dims, row_major_w):
         assert p["out"] >= out_need
         for b in range(obufs):
             regions.append((f"out{b}", p[f"off_out{b}"], p["out"]))
-    assert p["bias"] >= 4 * (N0p + N1p)
-    assert p["bar"] >= 8 * 26 + 8
+    # bias operands: a 1 KiB ONES tile and a 2 KiB BIAS block per 64-wide N block of each GEMM
+    assert p["bias"] >= 1024 + 2048 * (n0blk + (n1blk if mode == 0 else 0))
+    assert p["bar"] >= 8 * 27 + 8                # 27 barriers, then the TMEM slot and flag
     usable = p["smem"] - 1024                    # the rest aligns the base to 1024
     for name, off, size in regions:
         assert off % 1024 == 0, name
@@ -92,6 +96,18 @@ def check(kind, dims, row_major_w):
         assert oa + sa <= ob or ob + sb <= oa, (a, b)
     # TMEM: every accumulator buffer in range, 32-column aligned, distinct buffers disjoint
     assert p["tmem_cols"] in (32, 64, 128, 256, 512)
+    if p_tmem:
+        # buffer b: D0 [d0, d0 + N0p); P (packed) [d0, d0 + N0p/2); D1 [d1, d1 + N1p) after P
+        spans = []
+        for b in range(2):
+            d0, d1 = p[f"d0_col{b}"], p[f"d1_col{b}"]
+            assert d0 % 32 == 0 and d1 % 32 == 0
+            assert d1 >= d0 + N0p // 2                  # D1 never overwrites P
+            lo, hi = d0, max(d0 + N0p, d1 + N1p)
+            assert hi <= p["tmem_cols"]
+            spans.append((lo, hi))
+        assert spans[0][1] <= spans[1][0] or spans[1][1] <= spans[0][0]
+        return p
     accs = [("d0_0", p["d0_col0"], N0p)]
     if mode != 0 or dual:
         accs.append(("d0_1", p["d0_col1"], N0p))
@@ -126,10 +142,12 @@ def test_b2b_gemm_plan_sweep():
                 check("b2b_gemm", (1000, k0, n0, n1), True)
 
 
-def test_ffn_plan_streams_weights():
+def test_ffn_plan_keeps_p_in_tmem():
     p = check("b2b_gemm", (32768, 256, 256, 128), True)
-    assert p["resident"] == 0      # 192 KiB of weights plus a 64 KiB P tile cannot all stay
-    assert p["dual"] == 0          # 2 x (256 + 128) accumulator columns exceed 512
+    assert p["resident"] == 0      # 192 KiB of weights cannot stay beside the ring
+    # 2 x (256 + 128) accumulator columns exceed 512, but D0 -> P + D1 in one 256-column
+    # buffer per tile gives two tiles in flight with P in TMEM
+    assert p["p_tmem"] == 1 and p["dual"] == 1
 
 
 def test_small_chains_keep_two_tiles_in_flight():
@@ -178,3 +196,8 @@ def test_plan_rejects_like_the_entry_points():
     assert plan("b2b_gemm", (10, 12, 64, 64))[0] == 3        # K0 not a multiple of 8
     assert plan("b2b_gemm", (10, 64, 264, 64))[0] == 4       # N0 > 256
     assert plan("conv_relu_maxpool", (1, 1, 8, 8, 8))[0] == 2
+
+
+def test_wide_chains_keep_p_in_tmem():
+    for dims in ((300, 128, 256, 64), (257, 72, 200, 72), (1000, 64, 224, 96)):
+        assert check("b2b_gemm", dims, True)["p_tmem"] == 1
