@@ -287,6 +287,18 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.num_stages = chosen_stages;
   p.stage_bytes = chosen_stage_bytes;
   p.tmem_cols = tmem_layout(p, mode, k.dual != 0, k.p_tmem != 0);
+  // P in TMEM with streamed weights: W1 is packed into as few ring stages as possible and
+  // shared by the two tiles of a pair -- if those stages fit the ring at once.
+  p.w1_group = 0;
+  p.w1_per_stage = 1;
+  if (mode == MODE_CHAIN && k.p_tmem && !k.resident) {
+    const uint32_t per = std::max(1u, p.stage_bytes / p.w1_chunk_bytes);
+    const uint32_t stages = (static_cast<uint32_t>(p.kchunks1) + per - 1) / per;
+    if (stages <= p.num_stages) {
+      p.w1_group = 1;
+      p.w1_per_stage = per;
+    }
+  }
   Regions r;
   r.ring = p.num_stages * p.stage_bytes;
   r.w_res = p.resident ? w_res : 0u;
@@ -421,25 +433,41 @@ b2b_status run_gemm(int mode, bool w_mn, int dt, int64_t M, int32_t K0, int32_t 
   const uint64_t e = 2;
   bool ok = make_map(&ta, A, p.is_bf16, 2, {static_cast<uint64_t>(K0), static_cast<uint64_t>(M)},
                      {K0 * e}, {kChunkK, kBlockM});
-  if (w_mn)
-    ok = ok && make_map(&tw0, W0, p.is_bf16, 2, {static_cast<uint64_t>(N0), static_cast<uint64_t>(K0)},
-                        {N0 * e}, {64, 64});
-  else
+  // A row-major [rows][N] tensor with N a multiple of 64 viewed as [N/64][rows][64]: one
+  // box then covers every 64-wide column block of `box_rows` rows, laid out block after
+  // block exactly as the kernel's per-block boxes land.  Returns false (and the caller
+  // keeps the per-block 2-D map) if N is ragged or the driver refuses the view.
+  auto map3 = [&](CUtensorMap* m, const void* ptr, uint64_t rows, int32_t N, uint32_t box_rows) {
+    if (N % 64 != 0) return false;
+    return make_map(m, ptr, p.is_bf16, 3, {64, rows, static_cast<uint64_t>(N / 64)},
+                    {N * e, 128}, {64, box_rows, static_cast<uint32_t>(N / 64)});
+  };
+  if (w_mn) {
+    p.w0_box3 = map3(&tw0, W0, static_cast<uint64_t>(K0), N0, 64) ? 1 : 0;
+    if (!p.w0_box3)
+      ok = ok && make_map(&tw0, W0, p.is_bf16, 2,
+                          {static_cast<uint64_t>(N0), static_cast<uint64_t>(K0)}, {N0 * e}, {64, 64});
+  } else
     ok = ok && make_map(&tw0, W0, p.is_bf16, 2, {static_cast<uint64_t>(K0), static_cast<uint64_t>(N0)},
                         {K0 * e}, {kChunkK, static_cast<uint32_t>(p.N0p)});
   const int32_t Nout = mode == MODE_CHAIN ? N1 : N0;
   if (mode == MODE_CHAIN) {
-    if (w_mn)
-      ok = ok && make_map(&tw1, W1, p.is_bf16, 2, {static_cast<uint64_t>(N1), static_cast<uint64_t>(N0)},
-                          {N1 * e}, {64, 64});
-    else
+    if (w_mn) {
+      p.w1_box3 = map3(&tw1, W1, static_cast<uint64_t>(N0), N1, 64) ? 1 : 0;
+      if (!p.w1_box3)
+        ok = ok && make_map(&tw1, W1, p.is_bf16, 2,
+                            {static_cast<uint64_t>(N1), static_cast<uint64_t>(N0)}, {N1 * e}, {64, 64});
+    } else
       ok = ok && make_map(&tw1, W1, p.is_bf16, 2, {static_cast<uint64_t>(N0), static_cast<uint64_t>(N1)},
                           {N0 * e}, {kChunkK, static_cast<uint32_t>(p.N1p)});
   } else {
     tw1 = tw0;
   }
-  ok = ok && make_map(&to, D, p.is_bf16, 2, {static_cast<uint64_t>(Nout), static_cast<uint64_t>(M)},
-                      {Nout * e}, {64, kBlockM});
+  p.out_box3 = map3(&to, D, static_cast<uint64_t>(M), Nout, kBlockM) ? 1 : 0;
+  if (!p.out_box3)
+    ok = ok && make_map(&to, D, p.is_bf16, 2,
+                        {static_cast<uint64_t>(Nout), static_cast<uint64_t>(M)}, {Nout * e},
+                        {64, kBlockM});
   if (!ok) return B2B_ERR_CUDA;
   Variant v;
   if (mode == MODE_CHAIN) v = w_mn ? V_GEMM_CHAIN : V_CONV1X1_CHAIN;
@@ -704,7 +732,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   static const int32_t need[5] = {4, 3, 9, 8, 5};
   if (kind < 0 || kind > 4) return B2B_ERR_UNSUPPORTED;
   if (dims == nullptr || out == nullptr) return B2B_ERR_NULL;
-  if (ndims < need[kind] || out_len < 36) return B2B_ERR_SHAPE;
+  if (ndims < need[kind] || out_len < 38) return B2B_ERR_SHAPE;
   for (int i = 0; i < need[kind]; ++i)
     if (dims[i] < 0 || dims[i] > INT32_MAX) return B2B_ERR_SHAPE;
   const int32_t d0 = static_cast<int32_t>(dims[0]), d1 = static_cast<int32_t>(dims[1]),
@@ -752,7 +780,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
     }
   }
   if (!ok) return B2B_ERR_UNSUPPORTED;
-  const uint32_t v[36] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[38] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -762,7 +790,8 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           static_cast<uint32_t>(p.num_tiles), static_cast<uint32_t>(p.kchunks0),
                           static_cast<uint32_t>(p.kchunks1), static_cast<uint32_t>(p.N0p),
                           static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode),
-                          static_cast<uint32_t>(p.p_tmem)};
+                          static_cast<uint32_t>(p.p_tmem), static_cast<uint32_t>(p.w1_group),
+                          p.w1_per_stage};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

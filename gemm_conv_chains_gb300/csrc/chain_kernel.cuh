@@ -89,19 +89,22 @@ __device__ __forceinline__ TileCoord tile_coord(const ChainParams& p, int32_t t)
 // Optional event trace of one CTA.  The buffer holds four regions of trace_cap / 4 events,
 // one per role (producer, MMA issuer, epilogue group 0, group 1); each role appends to its
 // own region with plain stores, so tracing costs a few instructions per event.  An event
-// is two words: clock64, and code | group << 8 | tile index << 16 | 1 << 63.
+// is two words: %globaltimer (ns; one clock for all warps and SMs), and
+// code | group << 8 | tile index << 16 | 1 << 63.
 struct Tracer {
   unsigned long long* base = nullptr;
   uint32_t n = 0, cap = 0;
-  __device__ __forceinline__ Tracer(const ChainParams& p, uint32_t region, uint32_t leader) {
+  __device__ __forceinline__ Tracer(const ChainParams& p, uint32_t region, uint32_t leader,
+                                    uint32_t first = 0) {
     if (p.trace != nullptr && blockIdx.x == p.trace_cta && leader != 0u) {
       cap = p.trace_cap / 4u;
       base = p.trace + 2ull * cap * region;
+      n = first;
     }
   }
   __device__ __forceinline__ void operator()(uint32_t code, uint32_t group, int it) {
     if (base == nullptr || n >= cap) return;
-    base[2 * n] = static_cast<unsigned long long>(clock64());
+    base[2 * n] = static_cast<unsigned long long>(global_timer_ns());
     base[2 * n + 1] = code | (group << 8) | (static_cast<unsigned long long>(it) << 16) |
                       (1ull << 63);
     ++n;
@@ -159,7 +162,12 @@ __device__ __forceinline__ void load_w0_chunk(uint32_t lead, const ChainParams& 
                                               const CUtensorMap* tmW0, uint32_t dst,
                                               const KPos& k, uint32_t bar, uint64_t pol) {
   if constexpr (W0MN) {
-    // W0[K0][N0] row-major: one 64 (N) x 64 (K) box per 64-wide N block, 8 KiB apart.
+    // W0[K0][N0] row-major: a 64 (N) x 64 (K) box per 64-wide N block, 8 KiB apart; with
+    // the [N0/64][K0][64] view, all blocks in one box.
+    if (p.w0_box3) {
+      tma_load_3d(lead, dst, tmW0, bar, 0, k.cb * kChunkK, 0, pol);
+      return;
+    }
     const int nblk = (p.N0p + 63) >> 6;
     for (int nb = 0; nb < nblk; ++nb)
       tma_load_2d(lead, dst + nb * 8192u, tmW0, bar, nb * 64, k.cb * kChunkK, pol);
@@ -176,6 +184,10 @@ __device__ __forceinline__ void load_w1_chunk(uint32_t lead, const ChainParams& 
                                               const CUtensorMap* tmW1, uint32_t dst, int kc1,
                                               uint32_t bar, uint64_t pol) {
   if constexpr (W1MN) {
+    if (p.w1_box3) {
+      tma_load_3d(lead, dst, tmW1, bar, 0, kc1 * kChunkK, 0, pol);
+      return;
+    }
     const int nblk = (p.N1p + 63) >> 6;
     for (int nb = 0; nb < nblk; ++nb)
       tma_load_2d(lead, dst + nb * 8192u, tmW1, bar, nb * 64, kc1 * kChunkK, pol);
@@ -258,13 +270,35 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     return true;
   };
 
+  // W1 once for the pair of tiles it, it + 1: w1_per_stage chunks per ring stage.
+  auto load_w1_group = [&](int it) -> bool {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    for (int kc1 = 0; kc1 < p.kchunks1;) {
+      if (!acquire(t)) return false;
+      const int n = min(static_cast<int>(p.w1_per_stage), p.kchunks1 - kc1);
+      const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
+      const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
+      mbar_arrive_expect_tx_if(lead, fb, static_cast<uint32_t>(n) * p.w1_chunk_bytes);
+      for (int j = 0; j < n; ++j)
+        load_w1_chunk<W1MN>(lead, p, tmW1, sbase + j * p.w1_chunk_bytes, kc1 + j, fb, pol_keep);
+      trace(EV_PROD_W1_ISSUED, kc1, it);
+      advance();
+      kc1 += n;
+    }
+    return true;
+  };
+
   const int ntiles = local_tiles(p);
   if (MODE == MODE_CHAIN && p.p_tmem) {
     // Pairs: G0(0), G0(1), then G1(k), G1(k+1), G0(k+2), G0(k+3) -- as the MMA issuer.
     for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = load_g0(it);
     for (int k = 0; ok && k < ntiles; k += 2) {
-      ok = load_g1(k);
-      if (ok && k + 1 < ntiles) ok = load_g1(k + 1);
+      if (p.w1_group) {
+        ok = load_w1_group(k);
+      } else {
+        ok = load_g1(k);
+        if (ok && k + 1 < ntiles) ok = load_g1(k + 1);
+      }
       if (ok && k + 2 < ntiles) ok = load_g0(k + 2);
       if (ok && k + 3 < ntiles) ok = load_g0(k + 3);
     }
@@ -333,7 +367,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const uint32_t idesc1 = idesc_f16_f32(BF16 ? 1u : 0u, W1MN ? 1u : 0u, kBlockM, p.N1p);
   bool ok = true;
   const uint32_t lead = elect_one();
-  Tracer trace(p, 1, lead);
+  Tracer trace(p, 1, lead, 1);   // slot 0: the kernel's entry event
   if (p.resident)
     ok = warp_mbar_wait(bars + 8u * BAR_WFULL, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
   if (ok) ok = warp_mbar_wait(bars + 8u * BAR_BIAS_READY, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
@@ -450,13 +484,62 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     return true;
   };
 
+  // GEMM1 of the tiles j and (if `two`) j + 1 from one group of W1 stages (w1_group):
+  // the first tile waits for the stages, the second reads the same ones, and the stages
+  // are released after both.
+  auto issue_g1_pair = [&](int j, bool two) -> bool {
+    const int per = static_cast<int>(p.w1_per_stage);
+    const int s_first = stage;
+    const uint32_t ph_first = phase;
+    for (int r = 0; r < (two ? 2 : 1); ++r) {
+      const int jj = j + r;
+      const int32_t t = blockIdx.x + jj * gridDim.x;
+      const uint32_t b = static_cast<uint32_t>(jj & 1), u = static_cast<uint32_t>(jj >> 1);
+      if (!warp_mbar_wait(bars + 8u * (BAR_P_FULL0 + b), u & 1u, p, abort_flag, SITE_MMA_P_FULL,
+                          t))
+        return false;
+      trace(EV_MMA_P_READY, b, jj);
+      tc_fence_after_sync();
+      const uint32_t d1 = tmem_base + p.d1_col[b];
+      mma_f16_ss(lead, d1, ones_desc, bias1_desc, idesc_b1, 0u);   // D1 = bias
+      int s = s_first, slot = 0;
+      uint32_t ph = ph_first;
+      for (int kc1 = 0; kc1 < p.kchunks1; ++kc1, ++slot) {
+        if (slot == per) {
+          slot = 0;
+          if (++s == static_cast<int>(p.num_stages)) { s = 0; ph ^= 1u; }
+        }
+        if (r == 0 && slot == 0) {
+          if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + s), ph, p, abort_flag, SITE_MMA_FULL, t))
+            return false;
+          trace(EV_MMA_W1_FULL, kc1, jj);
+        }
+        const uint64_t bdesc = ring_w1 + static_cast<uint64_t>(s) * stage_step +
+                               static_cast<uint64_t>(slot) * w1_step;
+        const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1);
+      }
+      mma_commit(lead, bars + 8u * (BAR_D1_FULL0 + b));
+      trace(EV_MMA_G1_DONE, b, jj);
+    }
+    for (int i = 0; i < (p.kchunks1 + per - 1) / per; ++i) {
+      mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));
+      if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+    }
+    return true;
+  };
+
   if (ok) {
     if (MODE == MODE_CHAIN && p.p_tmem) {
       // Pairs of tiles: while the epilogue of one tile drains, the other tile's MMAs run.
       for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = issue_g0(it);
       for (int k = 0; ok && k < ntiles; k += 2) {
-        ok = issue_g1(k);
-        if (ok && k + 1 < ntiles) ok = issue_g1(k + 1);
+        if (p.w1_group) {
+          ok = issue_g1_pair(k, k + 1 < ntiles);
+        } else {
+          ok = issue_g1(k);
+          if (ok && k + 1 < ntiles) ok = issue_g1(k + 1);
+        }
         if (ok && k + 2 < ntiles) ok = issue_g0(k + 2);
         if (ok && k + 3 < ntiles) ok = issue_g0(k + 3);
       }
@@ -650,8 +733,12 @@ __device__ __noinline__ void drain_pool(uint32_t tm_lane, uint32_t col0, int nco
 }
 
 template <bool A4D>
-__device__ __forceinline__ void store_tile(const CUtensorMap* tmOut, uint32_t tile, int nchunks,
-                                           const TileCoord& tc) {
+__device__ __forceinline__ void store_tile(const ChainParams& p, const CUtensorMap* tmOut,
+                                           uint32_t tile, int nchunks, const TileCoord& tc) {
+  if (!A4D && p.out_box3) {   // [N/64][M][64] view: the whole tile in one box
+    tma_store_3d(tmOut, tile, 0, tc.m0, 0);
+    return;
+  }
   for (int nc = 0; nc < nchunks; ++nc) {
     if constexpr (A4D)
       tma_store_4d(tmOut, tile + nc * kPChunkBytes, nc * 64, tc.wo0, tc.ho0, tc.n);
@@ -744,7 +831,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       fence_proxy_async_smem();
       named_bar_sync(bar_id, group_threads);
       if (elected && !*abort_flag) {
-        store_tile<A4D>(tmOut, out_tile, (p.N1p + 63) >> 6, tc);
+        store_tile<A4D>(p, tmOut, out_tile, (p.N1p + 63) >> 6, tc);
         bulk_commit_group();
         trace(EV_EPI_STORED, g, it);
       }
@@ -775,14 +862,16 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
             tma_store_4d(tmOut, out_tile + nc * kPoolChunkBytes, nc * 64, tc.wo0 >> 1,
                          tc.ho0 >> 1, tc.n);
         } else {
-          store_tile<A4D>(tmOut, out_tile, (p.N0p + 63) >> 6, tc);
+          store_tile<A4D>(p, tmOut, out_tile, (p.N0p + 63) >> 6, tc);
         }
         bulk_commit_group();
         trace(EV_EPI_STORED, g, it);
       }
     }
   }
-  if (elected) bulk_wait_all();
+  // The staging tiles must outlive the stores' reads of them; the writes themselves are
+  // complete when the grid is.
+  if (elected) bulk_wait_read_all();
 }
 
 // ------------------------------------------------------------------------------------
@@ -797,39 +886,31 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
 // the other rows are 0.  The product is the bias broadcast to all 128 rows, exact in
 // fp32.  Written by the epilogue warps with generic stores.
 template <bool BF16>
-__device__ __forceinline__ void fill_bias_operands(const ChainParams& p, uint32_t* region,
+__device__ __forceinline__ void fill_bias_operands(const ChainParams& p, uint8_t* region,
                                                    int tid, int nthreads, bool chain) {
   const int n0blk = (p.N0p + 63) >> 6;
   const int n1blk = chain ? (p.N1p + 63) >> 6 : 0;
-  const int b0_bytes = n0blk * static_cast<int>(kBiasBlockBytes);
+  // Each thread fetches its element of both bias rows first (N <= 256 <= nthreads), so
+  // the global loads overlap the fill below instead of following one another.
+  const uint16_t v0 = (tid < p.N0 && p.b0 != nullptr) ? p.b0[tid] : uint16_t(0);
+  const uint16_t v1 = (chain && tid < p.N1 && p.b1 != nullptr) ? p.b1[tid] : uint16_t(0);
+  // ONES, and every byte of the BIAS blocks but their k-row 0 (bytes [0, 128) of a block).
+  uint32_t* words = reinterpret_cast<uint32_t*>(region);
   const int nwords =
       (static_cast<int>(kOnesBytes) + (n0blk + n1blk) * static_cast<int>(kBiasBlockBytes)) >> 2;
   const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
   for (int w = tid; w < nwords; w += nthreads) {
     const int o = w << 2;
-    uint32_t v = 0;
-    if (o < static_cast<int>(kOnesBytes)) {
-      const int r = o >> 7;
-      if (o == r * 128 + r * 16) v = one;
-    } else {
-      int lo = o - static_cast<int>(kOnesBytes);
-      const uint16_t* src = p.b0;
-      int n_valid = p.N0;
-      if (lo >= b0_bytes) {
-        lo -= b0_bytes;
-        src = p.b1;
-        n_valid = p.N1;
-      }
-      const int within = lo & static_cast<int>(kBiasBlockBytes - 1);
-      if (within < 128 && src != nullptr) {
-        const int n = (lo / static_cast<int>(kBiasBlockBytes)) * 64 + (within >> 1);
-        const uint32_t e0 = n < n_valid ? src[n] : 0u;
-        const uint32_t e1 = n + 1 < n_valid ? src[n + 1] : 0u;
-        v = e0 | (e1 << 16);
-      }
-    }
-    region[w] = v;
+    if (o < static_cast<int>(kOnesBytes))
+      words[w] = o == (o >> 7) * 144 ? one : 0u;   // row r: byte r * 128 + r * 16
+    else if (((o - static_cast<int>(kOnesBytes)) & static_cast<int>(kBiasBlockBytes - 1)) >= 128)
+      words[w] = 0u;
   }
+  // k-row 0 of block n / 64 holds element n at byte 2 * (n % 64); zero beyond N.
+  uint16_t* halves = reinterpret_cast<uint16_t*>(region + kOnesBytes);
+  constexpr int kBlockHalves = static_cast<int>(kBiasBlockBytes / 2);
+  if (tid < n0blk * 64) halves[(tid >> 6) * kBlockHalves + (tid & 63)] = v0;
+  if (tid < n1blk * 64) halves[(n0blk + (tid >> 6)) * kBlockHalves + (tid & 63)] = v1;
 }
 
 // ------------------------------------------------------------------------------------
@@ -850,6 +931,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t warps_per_group = static_cast<uint32_t>(kNumEpiWarps / p.epi_groups);
+  Tracer ktrace(p, 1, threadIdx.x == 32 ? 1u : 0u);
+  ktrace(EV_KERNEL_ENTRY, 0, 0);
 
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < p.num_stages; ++s) {
@@ -902,9 +985,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // The bias operands, off the producer's critical path; the MMA issuer waits for them
     // before its first MMA.
     grid_dependency_wait();
-    fill_bias_operands<BF16>(p, reinterpret_cast<uint32_t*>(base_ptr + p.off_bias),
-                             static_cast<int>(threadIdx.x) - 64, kNumEpiThreads,
-                             MODE == MODE_CHAIN);
+    fill_bias_operands<BF16>(p, base_ptr + p.off_bias, static_cast<int>(threadIdx.x) - 64,
+                             kNumEpiThreads, MODE == MODE_CHAIN);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8u * BAR_BIAS_READY);

@@ -56,6 +56,7 @@ enum TraceEvent : uint32_t {
   EV_MMA_ISSUED = 14,    // MMA issuer issued a slot's MMAs
   EV_PROD_W1_ISSUED = 15,  // producer issued a streamed GEMM1 weight chunk
   EV_MMA_W1_FULL = 16,     // MMA issuer saw a streamed GEMM1 weight chunk land
+  EV_KERNEL_ENTRY = 17,    // first instruction of the CTA
 };
 
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M
@@ -101,6 +102,14 @@ struct ChainParams {
   int32_t p_tmem;               // 1 (chain): P is written back into TMEM over the consumed
                                 //    GEMM0 columns and GEMM1 reads A from TMEM; tiles are
                                 //    processed in pairs, buffer b holds D0 -> P + D1
+  int32_t w0_box3, w1_box3;     // 1: a row-major weight (N a multiple of 64) is mapped as
+                                //    [N/64][K][64], so one 3-D box loads a whole K chunk
+  int32_t out_box3;             // 1: the 2-D output (N a multiple of 64) is mapped the same
+                                //    way and a tile is stored by one 3-D box
+  int32_t w1_group;             // 1 (P in TMEM, streamed weights): W1 is loaded once per
+                                //    pair of tiles, w1_per_stage chunks per ring stage,
+                                //    and both tiles' GEMM1 read it from the same stages
+  uint32_t w1_per_stage;        // W1 chunks per ring stage when w1_group
   int32_t epi_groups;           // 2: the epilogue warpgroups take alternate tiles;
                                 // 1: both warpgroups split the columns of every tile
   uint32_t tmem_cols;

@@ -278,7 +278,8 @@ TRACE_EVENTS = {1: "prod_acquire", 2: "prod_issued", 3: "mma_full", 4: "mma_g0_d
                 5: "mma_p_ready", 6: "mma_g1_done", 7: "mma_acc_free", 8: "epi_acc_ready",
                 9: "epi_p_done", 10: "epi_d1_ready", 11: "epi_staging", 12: "epi_stored",
                 13: "mma_wait", 14: "mma_issued",
-                15: "prod_w1_issued", 16: "mma_w1_full"}
+                15: "prod_w1_issued", 16: "mma_w1_full",
+                17: "kernel_entry"}
 
 
 def set_trace(buf, cta: int = 0) -> None:
@@ -293,7 +294,7 @@ def set_trace(buf, cta: int = 0) -> None:
 
 
 def read_trace(buf):
-    """Decodes a trace buffer into (cycles since the first event, event, group, tile),
+    """Decodes a trace buffer into (nanoseconds since the first event, event, group, tile),
     sorted by time."""
     raw = buf.cpu().view(-1, 2).tolist()
     ev = [(c, w & ((1 << 63) - 1)) for c, w in raw if w != 0]

@@ -155,11 +155,11 @@ int32_t b2b_num_sms(void);
 void b2b_set_wait_limit_ns(uint64_t ns);
 
 /* Event trace for performance analysis.  When buf is not NULL, every later launch of a
- * chain kernel records, for its CTA number `cta` only, the time (clock64, SM cycles) at
+ * chain kernel records, for its CTA number `cta` only, the time (%globaltimer, ns) at
  * which each role reached each step of each tile.  buf is a caller-owned, zero-filled
  * device array of 2 * capacity uint64 words split into four equal regions (producer,
  * MMA issuer, epilogue group 0, epilogue group 1); each role appends its events to its
- * region: word 2i = clock, word 2i+1 = event code | group << 8 | tile index << 16 |
+ * region: word 2i = time, word 2i+1 = event code | group << 8 | tile index << 16 |
  * 1 << 63 (codes: TraceEvent in kernel_params.h); unused words stay 0.  buf = NULL turns
  * tracing off.  buf must be 8-byte aligned and stay valid while traced launches run. */
 b2b_status b2b_set_trace(void* buf, uint32_t capacity, uint32_t cta);
@@ -182,15 +182,16 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1}
  *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
- * out (out_len >= 36) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ * out (out_len >= 38) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
  * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
  * P offsets [2], bytes per P buffer, staging offsets [2], bytes per staging buffer,
  * bias offset, bias bytes, barrier offset, barrier bytes, TMEM columns, GEMM0 accumulator
  * columns [2], GEMM1 accumulator columns [2], two tiles in flight (0/1), epilogue groups
  * (1/2), tiles, GEMM0 K chunks, GEMM1 K chunks, padded N0, padded N1, kernel mode
- * (0 chain, 1 single, 2 pool), and 1 if the chain's intermediate is kept in TMEM instead
- * of shared memory (wide N0: GEMM1 then reads its A operand from TMEM).
+ * (0 chain, 1 single, 2 pool), 1 if the chain's intermediate is kept in TMEM instead
+ * of shared memory (wide N0: GEMM1 then reads its A operand from TMEM), 1 if W1 is then
+ * loaded once per pair of tiles into shared ring stages, and the W1 chunks per stage.
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,

@@ -20,7 +20,7 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "off_w1", "w_res", "w0_chunk", "w1_chunk", "off_p0", "off_p1", "p", "off_out0",
           "off_out1", "out", "off_bias", "bias", "off_bar", "bar", "tmem_cols", "d0_col0",
           "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0", "kchunks1",
-          "N0p", "N1p", "mode", "p_tmem"]
+          "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4}
@@ -28,8 +28,8 @@ KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nh
 
 def plan(kind, dims):
     arr = (ctypes.c_int64 * len(dims))(*dims)
-    out = (ctypes.c_uint32 * 36)()
-    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 36)
+    out = (ctypes.c_uint32 * 38)()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 38)
     return st, dict(zip(FIELDS, list(out)))
 
 
@@ -68,6 +68,12 @@ def check(kind, dims, row_major_w):
         assert groups == 2                       # the pool epilogue needs whole rows per warp
     p_tmem = p["p_tmem"] == 1
     assert not p_tmem or (mode == 0 and dual and groups == 2 and not p["alias"])
+    if p["w1_group"]:
+        # W1 packed w1_per_stage chunks per ring stage; all its stages in the ring at once
+        assert p_tmem and not p["resident"]
+        per = p["w1_per_stage"]
+        assert per >= 1 and per * w1_chunk <= p["stage_bytes"]
+        assert -(-p["kchunks1"] // per) <= p["stages"]
     # P buffers used: tile i -> P[i & 1] when dual, else P[0]; none when P is in TMEM
     pbufs = 0 if p_tmem else ((2 if dual else 1) if mode == 0 else 0)
     obufs = 2 if groups == 2 else 1
@@ -148,6 +154,8 @@ def test_ffn_plan_keeps_p_in_tmem():
     # 2 x (256 + 128) accumulator columns exceed 512, but D0 -> P + D1 in one 256-column
     # buffer per tile gives two tiles in flight with P in TMEM
     assert p["p_tmem"] == 1 and p["dual"] == 1
+    # W1 (4 chunks of 16 KiB) fits in two 48 KiB stages, loaded once per pair of tiles
+    assert p["w1_group"] == 1 and p["w1_per_stage"] == 3
 
 
 def test_small_chains_keep_two_tiles_in_flight():

@@ -1,5 +1,5 @@
 """The optional per-CTA event trace: it records every step of every tile of the chosen CTA,
-in causal order, and leaves the results unchanged."""
+in causal order (one global clock for all warps), and leaves the results unchanged."""
 import pytest
 import torch
 
@@ -40,6 +40,9 @@ def test_trace_of_a_chain_is_complete_and_causal():
         assert when[("mma_p_ready", it)] <= when[("mma_g1_done", it)]
         assert when[("mma_g1_done", it)] <= when[("epi_d1_ready", it)]
         assert when[("epi_d1_ready", it)] <= when[("epi_stored", it)]
+    # the CTA's entry event comes first
+    assert names.count("kernel_entry") == 1
+    assert all(when[("kernel_entry", 0)] <= e[0] for e in ev)
 
 
 def test_trace_off_records_nothing():
