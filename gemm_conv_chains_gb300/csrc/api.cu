@@ -469,6 +469,13 @@ b2b_status run_gemm(int mode, bool w_mn, int dt, int64_t M, int32_t K0, int32_t 
                         {static_cast<uint64_t>(Nout), static_cast<uint64_t>(M)}, {Nout * e},
                         {64, kBlockM});
   if (!ok) return B2B_ERR_CUDA;
+  p.pf_a = static_cast<const uint8_t*>(A);
+  p.pf_a_bytes = static_cast<uint64_t>(M) * K0 * e;
+  p.pf_a_tile_bytes = static_cast<uint32_t>(kBlockM * K0 * e);
+  p.pf_w0 = static_cast<const uint8_t*>(W0);
+  p.pf_w0_bytes = static_cast<uint32_t>(static_cast<uint64_t>(K0) * N0 * e);
+  p.pf_w1 = static_cast<const uint8_t*>(W1);
+  p.pf_w1_bytes = mode == MODE_CHAIN ? static_cast<uint32_t>(static_cast<uint64_t>(N0) * N1 * e) : 0u;
   Variant v;
   if (mode == MODE_CHAIN) v = w_mn ? V_GEMM_CHAIN : V_CONV1X1_CHAIN;
   else v = w_mn ? V_GEMM_SINGLE : V_CONV1X1_SINGLE;
@@ -524,6 +531,10 @@ b2b_status run_conv(int mode, int dt, int32_t N, int32_t H, int32_t W, int32_t C
                         {64, 16, 8, 1});
   }
   if (!ok) return B2B_ERR_CUDA;
+  p.pf_w0 = static_cast<const uint8_t*>(W0);
+  p.pf_w0_bytes = static_cast<uint32_t>(static_cast<uint64_t>(C0) * R * S * C * e);
+  p.pf_w1 = static_cast<const uint8_t*>(W1);
+  p.pf_w1_bytes = mode == MODE_CHAIN ? static_cast<uint32_t>(static_cast<uint64_t>(C1) * C0 * e) : 0u;
   const Variant v = mode == MODE_CHAIN ? V_CONV_CHAIN : mode == MODE_SINGLE ? V_CONV_SINGLE : V_CONV_POOL;
   return launch(v, d, ta, tw0, tw1, to, p, smem, stream);
 }

@@ -27,7 +27,7 @@
 //   conv's zero padding.  The box lands in shared memory as 128 rows x 128 B, exactly the
 //   K-major 128B-swizzled layout tcgen05 reads, so no im2col buffer exists anywhere.
 //
-// Bias: each GEMM's first MMA writes the bias into its accumulator (D = ONES . BIAS, see
+// Bias: each GEMM's last MMA adds the bias to its accumulator (D += ONES . BIAS, see
 // fill_bias_operands), so epilogues apply only the activation and the rounding.
 //
 // Two tiles in flight: when TMEM and shared memory allow (acc_dual), tile i uses
@@ -196,6 +196,16 @@ __device__ __forceinline__ void load_w1_chunk(uint32_t lead, const ChainParams& 
   }
 }
 
+// L2 prefetch of tile t's rows of a 2-D A (contiguous, row-major).  Prefetches only warm
+// L2, so they may run before the previous kernel's writes are visible: L2 is where those
+// writes land.  The implicit-GEMM conv A has no per-tile contiguous range and is skipped.
+__device__ __forceinline__ void prefetch_a_tile(const ChainParams& p, int32_t t) {
+  if (p.pf_a == nullptr || t >= p.num_tiles) return;
+  const uint64_t off = static_cast<uint64_t>(t) * p.pf_a_tile_bytes;
+  const uint64_t n = min(static_cast<uint64_t>(p.pf_a_tile_bytes), p.pf_a_bytes - off);
+  bulk_prefetch_l2(p.pf_a + off, static_cast<uint32_t>(n));
+}
+
 template <int MODE, bool A4D, bool W0MN, bool W1MN>
 __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
                               const CUtensorMap* tmW0, const CUtensorMap* tmW1, uint32_t base,
@@ -249,6 +259,9 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
       load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, k, fb, pol_stream);
       if (!p.resident)
         load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, k, fb, pol_keep);
+      // Tile it + 2's A into L2 behind this tile's first chunk (tiles 0 and 1 were
+      // prefetched at the start), so that HBM stays busy ahead of the ring.
+      if (kc == 0 && lead) prefetch_a_tile(p, t + 2 * static_cast<int32_t>(gridDim.x));
       trace(EV_PROD_ISSUED, kc, it);
       advance();
     }
@@ -330,34 +343,37 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
 // ------------------------------------------------------------------------------------
 // MMA issuer (one thread)
 // ------------------------------------------------------------------------------------
-// Issues the MMAs of one 64-wide K chunk: D += A . B over `nks` 16-wide K steps (D was
-// initialised to the bias by the GEMM's first MMA).  The
+// Issues the MMAs of one 64-wide K chunk: D (+)= A . B over `nks` 16-wide K steps (the
+// first chunk of a GEMM overwrites D; the bias is added by the GEMM's last MMA).  The
 // descriptors of consecutive K steps differ only in their start-address field (32 B per
 // step for K-major operands, 2 KiB for an MN-major one), so each step is one add; with
 // small N the single issuing thread is otherwise the bottleneck.
 template <bool BMN>
 __device__ __forceinline__ void issue_chunk(uint32_t lead, uint32_t d, uint64_t adesc,
-                                            uint64_t bdesc, uint32_t idesc, int nks) {
+                                            uint64_t bdesc, uint32_t idesc, int nks, bool first) {
   constexpr uint64_t kAStep = 32u >> 4;
   constexpr uint64_t kBStep = BMN ? (2048u >> 4) : (32u >> 4);
   if (nks == 4) {
-    mma_f16_ss(lead, d, adesc, bdesc, idesc, 1u);
+    mma_f16_ss(lead, d, adesc, bdesc, idesc, first ? 0u : 1u);
     mma_f16_ss(lead, d, adesc + kAStep, bdesc + kBStep, idesc, 1u);
     mma_f16_ss(lead, d, adesc + 2 * kAStep, bdesc + 2 * kBStep, idesc, 1u);
     mma_f16_ss(lead, d, adesc + 3 * kAStep, bdesc + 3 * kBStep, idesc, 1u);
   } else {
     for (int ks = 0; ks < nks; ++ks)
-      mma_f16_ss(lead, d, adesc + ks * kAStep, bdesc + ks * kBStep, idesc, 1u);
+      mma_f16_ss(lead, d, adesc + ks * kAStep, bdesc + ks * kBStep, idesc,
+                 (first && ks == 0) ? 0u : 1u);
   }
 }
 
 // GEMM1 chunk with A (= P) in TMEM: 8 packed columns per 16-wide K step.
 template <bool BMN>
 __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32_t a_tmem,
-                                               uint64_t bdesc, uint32_t idesc, int nks) {
+                                               uint64_t bdesc, uint32_t idesc, int nks,
+                                               bool first) {
   constexpr uint64_t kBStep = BMN ? (2048u >> 4) : (32u >> 4);
   for (int ks = 0; ks < nks; ++ks)
-    mma_f16_ts(lead, d, a_tmem + 8u * ks, bdesc + ks * kBStep, idesc, 1u);
+    mma_f16_ts(lead, d, a_tmem + 8u * ks, bdesc + ks * kBStep, idesc,
+               (first && ks == 0) ? 0u : 1u);
 }
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16>
@@ -370,7 +386,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   Tracer trace(p, 1, lead, 1);   // slot 0: the kernel's entry event
   if (p.resident)
     ok = warp_mbar_wait(bars + 8u * BAR_WFULL, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
-  if (ok) ok = warp_mbar_wait(bars + 8u * BAR_BIAS_READY, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
+  bool bias_ready = false;   // the epilogue warps write the bias operands at the start
 
   // Descriptors of every operand region, built once; a ring stage / weight chunk / P
   // chunk is then a multiple of its byte size (in 16-byte units) added to them.
@@ -422,7 +438,6 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       tc_fence_after_sync();
     }
     const uint32_t d0 = tmem_base + p.d0_col[b];
-    mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0, 0u);   // D0 = bias
     int cb = 0;   // channel block within the tap (4-D) / chunk index (2-D)
     for (int kc = 0; kc < p.kchunks0; ++kc) {
       trace(EV_MMA_WAIT, kc, it);
@@ -434,11 +449,19 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
                                         : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
       const int nks = cb == p.kc_per_tap - 1 ? last_nks : 4;
       if (++cb == p.kc_per_tap) cb = 0;
-      issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks);
+      issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
       trace(EV_MMA_ISSUED, kc, it);
       mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
       if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
     }
+    // The bias step comes last, so the epilogue warps' first write of its operands
+    // overlaps the first tile's MMAs.
+    if (!bias_ready) {
+      if (!warp_mbar_wait(bars + 8u * BAR_BIAS_READY, 0u, p, abort_flag, SITE_MMA_WEIGHTS, t))
+        return false;
+      bias_ready = true;
+    }
+    mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0, 1u);   // D0 += bias
     mma_commit(lead, bars + 8u * (BAR_ACC_FULL0 + b));
     trace(EV_MMA_G0_DONE, b, it);
     return true;
@@ -454,7 +477,6 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     trace(EV_MMA_P_READY, b, j);
     tc_fence_after_sync();
     const uint32_t d1 = tmem_base + p.d1_col[b];
-    mma_f16_ss(lead, d1, ones_desc, bias1_desc, idesc_b1, 0u);   // D1 = bias
     for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
       uint64_t bdesc;
       if (p.resident) {
@@ -468,17 +490,19 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       }
       const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
       if (p.p_tmem) {
-        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1);
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1,
+                             kc1 == 0);
       } else {
         const uint64_t adesc =
             (b ? p_desc1 : p_desc0) + static_cast<uint64_t>(kc1) * (kPChunkBytes >> 4);
-        issue_chunk<W1MN>(lead, d1, adesc, bdesc, idesc1, nks1);
+        issue_chunk<W1MN>(lead, d1, adesc, bdesc, idesc1, nks1, kc1 == 0);
       }
       if (!p.resident) {
         mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));
         if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
       }
     }
+    mma_f16_ss(lead, d1, ones_desc, bias1_desc, idesc_b1, 1u);   // D1 += bias
     mma_commit(lead, bars + 8u * (BAR_D1_FULL0 + b));
     trace(EV_MMA_G1_DONE, b, j);
     return true;
@@ -501,7 +525,6 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       trace(EV_MMA_P_READY, b, jj);
       tc_fence_after_sync();
       const uint32_t d1 = tmem_base + p.d1_col[b];
-      mma_f16_ss(lead, d1, ones_desc, bias1_desc, idesc_b1, 0u);   // D1 = bias
       int s = s_first, slot = 0;
       uint32_t ph = ph_first;
       for (int kc1 = 0; kc1 < p.kchunks1; ++kc1, ++slot) {
@@ -517,8 +540,10 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         const uint64_t bdesc = ring_w1 + static_cast<uint64_t>(s) * stage_step +
                                static_cast<uint64_t>(slot) * w1_step;
         const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
-        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1);
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1,
+                             kc1 == 0);
       }
+      mma_f16_ss(lead, d1, ones_desc, bias1_desc, idesc_b1, 1u);   // D1 += bias
       mma_commit(lead, bars + 8u * (BAR_D1_FULL0 + b));
       trace(EV_MMA_G1_DONE, b, jj);
     }
@@ -690,45 +715,52 @@ __device__ __forceinline__ void drain_to_tmem(int act, uint32_t tm_lane, uint32_
     drain_to_tmem_act<BF16, 0>(tm_lane, col0, ncols, p_col0);
 }
 
-// 2x2 max of 16 columns across the four lanes of each pooling window, then ReLU and
-// rounding by the window's owner lane, stored to the pooled staging tile.
+// Elementwise max of two packed fp16/bf16 pairs.
 template <bool BF16>
-__device__ __forceinline__ void pool_store16(const uint32_t (&r)[16], int c, uint32_t tile,
-                                             int prow, bool owner) {
-  float m[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float v = __uint_as_float(r[j]);
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-    m[j] = v;
-  }
-  if (owner) {
-    uint32_t v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = pack2<BF16, true>(m[2 * j], m[2 * j + 1]);
-    st_row16_sw128(tile, prow, c, kPoolChunkBytes, v);
-  }
+__device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if constexpr (BF16)
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  else
+    asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // Pool epilogue.  Tile row = 16 * h + w over an 8 x 16 conv-output tile, so warp q holds
 // conv rows 2q and 2q+1: the horizontal partner of a pixel sits in lane ^ 1 and the
-// vertical one in lane ^ 16.  The accumulators already hold the bias, which is the same
-// for the four pixels of a window, so the max of the four sums equals the max of the
-// biased values; ReLU and rounding are monotone, so taking them after the max equals
-// pooling the rounded ReLU output.
+// vertical one in lane ^ 16.  Each pixel's biased accumulators are rounded with ReLU to
+// packed pairs first -- exactly the unfused operator's output -- and the 2x2 max is taken
+// over those pairs (two shuffles and two packed maxes per pair of channels); the lane
+// owning the window's top-left pixel stores the pooled pixel.
 template <bool BF16>
 __device__ __noinline__ void drain_pool(uint32_t tm_lane, uint32_t col0, int ncols,
-                                           uint32_t tile, int q, int lane) {
+                                        uint32_t tile, int q, int lane) {
   const bool owner = (lane & 17) == 0;
   const int prow = q * 8 + (lane >> 1);
   for (int c = 0; c < ncols; c += 32) {
     const bool two = c + 16 < ncols;
-    uint32_t a[16], b[16];
+    uint32_t a[16], b[16], v[8], w[8];
     tmem_ld32(tm_lane + col0 + c, two, a, b);
     tmem_wait_ld(a, b);
-    pool_store16<BF16>(a, c, tile, prow, owner);
-    if (two) pool_store16<BF16>(b, c + 16, tile, prow, owner);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = pack2<BF16, true>(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
+      w[j] = pack2<BF16, true>(__uint_as_float(b[2 * j]), __uint_as_float(b[2 * j + 1]));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = max2<BF16>(v[j], __shfl_xor_sync(0xffffffffu, v[j], 1));
+      w[j] = max2<BF16>(w[j], __shfl_xor_sync(0xffffffffu, w[j], 1));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = max2<BF16>(v[j], __shfl_xor_sync(0xffffffffu, v[j], 16));
+      w[j] = max2<BF16>(w[j], __shfl_xor_sync(0xffffffffu, w[j], 16));
+    }
+    if (owner) {
+      st_row16_sw128(tile, prow, c, kPoolChunkBytes, v);
+      if (two) st_row16_sw128(tile, prow, c + 16, kPoolChunkBytes, w);
+    }
   }
 }
 
@@ -877,8 +909,8 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
 // ------------------------------------------------------------------------------------
 // bias operands
 // ------------------------------------------------------------------------------------
-// The bias enters every GEMM as its first K step, D = ONES . BIAS (accumulate off), so the
-// epilogue never reads it.  ONES is a K-major 128B-swizzled A tile whose row m holds 1 at
+// The bias enters every GEMM as one more K step after the last chunk, D += ONES . BIAS, so
+// the epilogue never reads it.  ONES is a K-major 128B-swizzled A tile whose row m holds 1 at
 // k = 0 and 0 at k = 1..15; all its 8-row groups are equal, so the descriptor's group
 // stride is 0 and the tile is a single 1 KiB swizzle atom (row r, k = 0 sits at byte
 // r * 128 + (0 ^ r) * 16).  BIAS is an MN-major 128B-swizzled B tile with 16 k-rows per
@@ -974,6 +1006,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   // Global memory is touched only after the previous kernel of the stream has completed
   // (inputs may be its outputs, outputs its inputs); the setup above overlaps its tail.
   if (warp == 0) {
+    // The first two tiles' A and (from one CTA) the weights into L2 while the previous
+    // kernel finishes.
+    if (lane == 0) {
+      prefetch_a_tile(p, blockIdx.x);
+      prefetch_a_tile(p, blockIdx.x + gridDim.x);
+      if (blockIdx.x == 0) {
+        bulk_prefetch_l2(p.pf_w0, p.pf_w0_bytes);
+        if (MODE == MODE_CHAIN) bulk_prefetch_l2(p.pf_w1, p.pf_w1_bytes);
+      }
+    }
+    __syncwarp();
     grid_dependency_wait();
     producer_role<MODE, A4D, W0MN, W1MN>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
     __syncwarp();

@@ -90,6 +90,14 @@ struct ChainParams {
   int32_t act0, act1;
   const uint16_t* b0;   // may be null
   const uint16_t* b1;   // may be null
+  // L2 prefetch (warming only): 2-D A (null for the implicit-GEMM conv A) with the bytes of
+  // one 128-row tile and of the whole tensor, and the weights' bytes.
+  const uint8_t* pf_a;
+  uint64_t pf_a_bytes;
+  uint32_t pf_a_tile_bytes;
+  const uint8_t* pf_w0;
+  const uint8_t* pf_w1;
+  uint32_t pf_w0_bytes, pf_w1_bytes;
   // --- shared-memory plan (byte offsets from the 1024-aligned dynamic base) -----------
   uint32_t off_ring, stage_bytes, num_stages;
   uint32_t w0_chunk_bytes, w1_chunk_bytes;

@@ -217,6 +217,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t pred, uint32_t dst, const C
       : "memory");
 }
 
+// L2 prefetch of `bytes` contiguous bytes at a 16-byte aligned global address (bytes a
+// multiple of 16): no shared memory, no barrier; it only warms L2 for later loads.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0,
                                              int32_t c1) {
   asm volatile(
