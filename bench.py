@@ -64,7 +64,7 @@ def load_peaks():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for name in ("chain_kernel.cuh", "ptx.cuh", "kernel_params.h"):
+    for name in ("chain_kernel.cuh", "ptx.cuh", "kernel_params.h", "kernel_units.cuh", "api.cu"):
         with open(os.path.join(ROOT, "gemm_conv_chains_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
