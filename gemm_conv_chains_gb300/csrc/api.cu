@@ -260,8 +260,12 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   for (int min_stages = 3; min_stages >= 2 && chosen < 0; --min_stages) {
     for (int c = 0; c < ncand; ++c) {
       const Cand& k = cands[c];
+      // Resident filters of an R > 1 conv: one halo box of (8 + R - 1) x 16 pixels per
+      // column tap and channel block feeds all R row taps.
+      const uint32_t a_bytes = (k.resident && p.R > 1) ? (7u + static_cast<uint32_t>(p.R)) * 2048u
+                                                       : kABytes;
       const uint32_t stage_bytes =
-          k.resident ? kABytes
+          k.resident ? a_bytes
                      : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
       const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? (k.dual ? 2u : 1u) : 0u;
       const uint32_t obufs = k.groups == 2 ? 2u : 1u;
@@ -286,6 +290,9 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.p_tmem = k.p_tmem;
   p.num_stages = chosen_stages;
   p.stage_bytes = chosen_stage_bytes;
+  p.halo = (k.resident && p.R > 1) ? 1 : 0;
+  p.a_stage_bytes = p.halo ? (7u + static_cast<uint32_t>(p.R)) * 2048u : kABytes;
+  p.kstages0 = p.halo ? p.S * p.kc_per_tap : p.kchunks0;
   p.tmem_cols = tmem_layout(p, mode, k.dual != 0, k.p_tmem != 0);
   // P in TMEM with streamed weights: W1 is packed into as few ring stages as possible and
   // shared by the two tiles of a pair -- if those stages fit the ring at once.
@@ -505,7 +512,7 @@ b2b_status run_conv(int mode, int dt, int32_t N, int32_t H, int32_t W, int32_t C
                      {static_cast<uint64_t>(C), static_cast<uint64_t>(W), static_cast<uint64_t>(H),
                       static_cast<uint64_t>(N)},
                      {C * e, static_cast<uint64_t>(W) * C * e, static_cast<uint64_t>(H) * W * C * e},
-                     {kChunkK, 16, 8, 1});
+                     {kChunkK, 16, static_cast<uint32_t>(p.halo ? 8 + R - 1 : 8), 1});
   ok = ok && make_map(&tw0, W0, p.is_bf16, 3,
                       {static_cast<uint64_t>(C), static_cast<uint64_t>(R) * S, static_cast<uint64_t>(C0)},
                       {C * e, static_cast<uint64_t>(R) * S * C * e},
@@ -743,7 +750,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   static const int32_t need[5] = {4, 3, 9, 8, 5};
   if (kind < 0 || kind > 4) return B2B_ERR_UNSUPPORTED;
   if (dims == nullptr || out == nullptr) return B2B_ERR_NULL;
-  if (ndims < need[kind] || out_len < 38) return B2B_ERR_SHAPE;
+  if (ndims < need[kind] || out_len < 40) return B2B_ERR_SHAPE;
   for (int i = 0; i < need[kind]; ++i)
     if (dims[i] < 0 || dims[i] > INT32_MAX) return B2B_ERR_SHAPE;
   const int32_t d0 = static_cast<int32_t>(dims[0]), d1 = static_cast<int32_t>(dims[1]),
@@ -791,7 +798,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
     }
   }
   if (!ok) return B2B_ERR_UNSUPPORTED;
-  const uint32_t v[38] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[40] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -802,7 +809,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           static_cast<uint32_t>(p.kchunks1), static_cast<uint32_t>(p.N0p),
                           static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode),
                           static_cast<uint32_t>(p.p_tmem), static_cast<uint32_t>(p.w1_group),
-                          p.w1_per_stage};
+                          p.w1_per_stage, static_cast<uint32_t>(p.halo), p.a_stage_bytes};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

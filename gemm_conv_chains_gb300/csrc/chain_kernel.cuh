@@ -142,6 +142,10 @@ struct KPos {
       if (++s == p.S) { s = 0; ++r; }
     }
   }
+  // Halo stages: channel block fastest, then the column tap s (all row taps at once).
+  __device__ __forceinline__ void next_halo(const ChainParams& p) {
+    if (++cb == p.kc_per_tap) { cb = 0; ++s; }
+  }
 };
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN>
@@ -250,15 +254,16 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     const int32_t t = blockIdx.x + it * gridDim.x;
     const TileCoord tc = tile_coord<A4D>(p, t);
     KPos k;
-    for (int kc = 0; kc < p.kchunks0; ++kc, k.next(p)) {
+    for (int kc = 0; kc < p.kstages0; ++kc) {
       if (!acquire(t)) return false;
       trace(EV_PROD_ACQUIRE, kc, it);
       const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
-      mbar_arrive_expect_tx_if(lead, fb, kABytes + (p.resident ? 0u : p.w0_chunk_bytes));
+      mbar_arrive_expect_tx_if(lead, fb, p.a_stage_bytes + (p.resident ? 0u : p.w0_chunk_bytes));
       load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, k, fb, pol_stream);
       if (!p.resident)
         load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, k, fb, pol_keep);
+      if (A4D && p.halo) k.next_halo(p); else k.next(p);
       // Tile it + 2's A into L2 behind this tile's first chunk (tiles 0 and 1 were
       // prefetched at the start), so that HBM stays busy ahead of the ring.
       if (kc == 0 && lead) prefetch_a_tile(p, t + 2 * static_cast<int32_t>(gridDim.x));
@@ -438,18 +443,31 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       tc_fence_after_sync();
     }
     const uint32_t d0 = tmem_base + p.d0_col[b];
-    int cb = 0;   // channel block within the tap (4-D) / chunk index (2-D)
-    for (int kc = 0; kc < p.kchunks0; ++kc) {
+    int cb = 0;       // channel block within the tap (4-D) / chunk index (2-D)
+    int s_tap = 0;    // halo: the column tap of the stage
+    for (int kc = 0; kc < p.kstages0; ++kc) {
       trace(EV_MMA_WAIT, kc, it);
       if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL, t))
         return false;
       trace(EV_MMA_FULL, kc, it);   // TMA data: no tcgen05 ordering needed
       const uint64_t adesc = ring_a + static_cast<uint64_t>(stage) * stage_step;
-      const uint64_t bdesc = p.resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
-                                        : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
       const int nks = cb == p.kc_per_tap - 1 ? last_nks : 4;
-      if (++cb == p.kc_per_tap) cb = 0;
-      issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
+      if (A4D && p.halo) {
+        // The stage holds rows ho0 - pad .. + 8 + R - 1 (16 pixels each): row tap r starts
+        // 16 rows = 2 KiB (two swizzle atoms) further in.
+        for (int r = 0; r < p.R; ++r) {
+          const int wchunk = (r * p.S + s_tap) * p.kc_per_tap + cb;
+          issue_chunk<W0MN>(lead, d0, adesc + static_cast<uint64_t>(r) * (2048u >> 4),
+                            res_w0 + static_cast<uint64_t>(wchunk) * w0_step, idesc0, nks,
+                            kc == 0 && r == 0);
+        }
+        if (++cb == p.kc_per_tap) { cb = 0; ++s_tap; }
+      } else {
+        const uint64_t bdesc = p.resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
+                                          : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
+        if (++cb == p.kc_per_tap) cb = 0;
+        issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
+      }
       trace(EV_MMA_ISSUED, kc, it);
       mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
       if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }

@@ -81,6 +81,10 @@ struct ChainParams {
   int32_t N0p, N1p;     // padded to multiples of 16 (tcgen05 N granularity for M = 128)
   int32_t kchunks0;     // 64-wide K chunks of GEMM0 (4D: taps * kc_per_tap)
   int32_t kc_per_tap;   // 4D: ceil(C / 64)
+  int32_t halo;         // 4D, resident filters, R > 1: one box of (8 + R - 1) x 16 pixels per
+                        //   (column tap s, channel block) serves the R row taps
+  int32_t kstages0;     // ring stages per tile for GEMM0 (halo: S * kc_per_tap; else kchunks0)
+  uint32_t a_stage_bytes;   // A bytes per ring stage (16 KiB; halo: (8 + R - 1) * 2 KiB)
   int32_t kchunks1;     // 64-wide K chunks of GEMM1 (= ceil(N0p / 64))
   int32_t R, S, pad;    // 4D filter
   int32_t Ho, Wo;       // 4D output spatial size (before pooling)

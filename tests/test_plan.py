@@ -20,7 +20,7 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "off_w1", "w_res", "w0_chunk", "w1_chunk", "off_p0", "off_p1", "p", "off_out0",
           "off_out1", "out", "off_bias", "bias", "off_bar", "bar", "tmem_cols", "d0_col0",
           "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0", "kchunks1",
-          "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage"]
+          "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4}
@@ -28,8 +28,8 @@ KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nh
 
 def plan(kind, dims):
     arr = (ctypes.c_int64 * len(dims))(*dims)
-    out = (ctypes.c_uint32 * 38)()
-    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 38)
+    out = (ctypes.c_uint32 * 40)()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 40)
     return st, dict(zip(FIELDS, list(out)))
 
 
@@ -39,6 +39,10 @@ def rup(x, m):
 
 def check(kind, dims, row_major_w):
     st, p = plan(kind, dims)
+    R = {"b2b_conv_nhwc": dims[5] if len(dims) > 5 else 1, "conv_bias_act_nhwc": dims[5] if len(dims) > 5 else 1,
+         "conv_relu_maxpool": 3}.get(kind, 1)
+    if kind in ("b2b_conv_nhwc", "conv_bias_act_nhwc") and dims[5] == 1 and dims[6] == 1 and dims[7] == 0:
+        R = 1   # a 1x1 pad-0 conv runs as a GEMM
     assert st == 0, (kind, dims, st)
     mode = p["mode"]
     N0p, N1p = p["N0p"], p["N1p"]
@@ -52,7 +56,12 @@ def check(kind, dims, row_major_w):
     assert p["smem"] <= SMEM_LIMIT
     assert 2 <= p["stages"] <= 8
     assert p["ring"] == p["stages"] * p["stage_bytes"]
-    assert p["stage_bytes"] >= 16384 + (0 if p["resident"] else w0_chunk)
+    assert p["stage_bytes"] >= p["a_stage_bytes"] + (0 if p["resident"] else w0_chunk)
+    if p["halo"]:
+        # one box of (8 + R - 1) x 16 pixels x 64 channels per column tap feeds all row taps
+        assert p["resident"] and p["a_stage_bytes"] == (8 + R - 1) * 16 * 128
+    else:
+        assert p["a_stage_bytes"] == 128 * 128
     if not p["resident"]:
         assert p["stage_bytes"] >= w1_chunk
     regions = [("ring", p["off_ring"], p["ring"]), ("bias", p["off_bias"], p["bias"]),
@@ -192,6 +201,13 @@ def test_conv_bias_act_plans(dims):
                                   (2, 18, 40, 64, 128), (1, 16, 16, 256, 256)])
 def test_conv_relu_maxpool_plans(dims):
     check("conv_relu_maxpool", dims, False)
+
+
+def test_resident_3x3_convs_use_halo_boxes():
+    for kind, dims in (("conv_relu_maxpool", (32, 112, 112, 64, 64)),
+                       ("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128))):
+        p = check(kind, dims, False)
+        assert p["resident"] == 1 and p["halo"] == 1 and p["a_stage_bytes"] == 10 * 16 * 128
 
 
 def test_workload_tile_counts():
