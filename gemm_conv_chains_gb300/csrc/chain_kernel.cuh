@@ -873,6 +873,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       if (alive)
         drain_to_smem<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p, out_tile,
                             row, kPChunkBytes);
+      if (elected) trace(EV_EPI_DRAINED, g, it);
       tc_fence_before_sync();
       if (p.p_tmem) {   // the buffer (D0 -> P + D1) may take tile i + 2
         __syncwarp();

@@ -57,6 +57,7 @@ enum TraceEvent : uint32_t {
   EV_PROD_W1_ISSUED = 15,  // producer issued a streamed GEMM1 weight chunk
   EV_MMA_W1_FULL = 16,     // MMA issuer saw a streamed GEMM1 weight chunk land
   EV_KERNEL_ENTRY = 17,    // first instruction of the CTA
+  EV_EPI_DRAINED = 18,     // epilogue group's elected thread finished its output drain
 };
 
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M

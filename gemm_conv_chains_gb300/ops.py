@@ -279,7 +279,7 @@ TRACE_EVENTS = {1: "prod_acquire", 2: "prod_issued", 3: "mma_full", 4: "mma_g0_d
                 9: "epi_p_done", 10: "epi_d1_ready", 11: "epi_staging", 12: "epi_stored",
                 13: "mma_wait", 14: "mma_issued",
                 15: "prod_w1_issued", 16: "mma_w1_full",
-                17: "kernel_entry"}
+                17: "kernel_entry", 18: "epi_drained"}
 
 
 def set_trace(buf, cta: int = 0) -> None:
