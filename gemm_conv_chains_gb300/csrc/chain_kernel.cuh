@@ -560,6 +560,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
         issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1,
                              kc1 == 0);
+        trace(EV_MMA_ISSUED, 8 + kc1, jj);   // GEMM1 chunks: group 8 + chunk
       }
       mma_f16_ss(lead, d1, ones_desc, bias1_desc, idesc_b1, 1u);   // D1 += bias
       mma_commit(lead, bars + 8u * (BAR_D1_FULL0 + b));

@@ -82,13 +82,29 @@ def test_b2b_gemm_ffn_workload_sampled_rows():
 
 
 @pytest.mark.parametrize("integer", [True, False])
+def test_b2b_gemm_wide_streamed_pairs_sampled_rows(integer):
+    # K0 = 256 streams the weights, so GEMM0 of each tile pair runs interleaved (one W0
+    # chunk per stage for both tiles); 3 x SMs + 1 tiles give CTA 0 two pairs, the second
+    # with one ragged tile.
+    nsm = ops.num_sms()
+    M = 128 * nsm * 3 + 77
+    acts = ("relu", "none") if integer else ("hardswish", "hardswish")   # exact: no fractions
+    w = wl.GemmChain("spairs", "bf16", M, 256, 256, 128, *acts)
+    rng = np.random.default_rng(6)
+    cta0 = np.concatenate([np.arange(128 * t, min(128 * t + 128, M)) for t in range(0, 3 * nsm + 1, nsm)])
+    rows = np.unique(np.concatenate([cta0, rng.choice(M, 512, replace=False)]))
+    run_b2b_gemm(w, seed=12, integer=integer, rows=rows)
+
+
+@pytest.mark.parametrize("integer", [True, False])
 def test_b2b_gemm_wide_many_pairs_sampled_rows(integer):
     # N0 = 256 keeps P in TMEM and processes tiles in pairs; with 5 x SMs + 1 tiles, CTA 0
     # runs three pairs (W1 reloaded into the output staging between them, the last pair
     # with one ragged tile).  Rows of every tile of CTA 0 plus a random sample.
     nsm = ops.num_sms()
     M = 128 * nsm * 5 + 77
-    w = wl.GemmChain("pairs", "bf16", M, 64, 256, 128, "hardswish", "relu")
+    acts = ("relu", "none") if integer else ("hardswish", "relu")   # exact: no fractions
+    w = wl.GemmChain("pairs", "bf16", M, 64, 256, 128, *acts)
     rng = np.random.default_rng(5)
     cta0 = np.concatenate([np.arange(128 * t, min(128 * t + 128, M)) for t in range(0, 5 * nsm + 1, nsm)])
     rows = np.unique(np.concatenate([cta0, rng.choice(M, 512, replace=False)]))
