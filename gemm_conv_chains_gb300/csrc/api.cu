@@ -178,12 +178,12 @@ struct Regions {
   uint32_t ring, w_res, p_each, out_each, bias, bar;
 };
 
-// TMEM columns of the accumulators.  Chain: D0 buffers of round_up(N0p, 32) columns, then
-// D1 buffers of round_up(N1p, 32) columns (every buffer starts on a multiple of 32
-// columns); single/pool: two accumulator buffers.  `dual` selects two buffers per
-// accumulator (two tiles in flight).  Returns the power-of-two allocation.
-uint32_t tmem_layout(ChainParams& p, int mode, bool dual, bool p_tmem = false) {
+// TMEM columns of the accumulators.  Chain: nbuf D0 buffers of round_up(N0p, 32) columns,
+// then nbuf D1 buffers of round_up(N1p, 32) columns (every buffer starts on a multiple of
+// 32 columns); single/pool: two accumulator buffers.  Returns the power-of-two allocation.
+uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = false) {
   const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
+  for (uint32_t b = 0; b < kMaxBufs; ++b) p.d0_col[b] = p.d1_col[b] = 0;
   if (mode == MODE_CHAIN && p_tmem) {
     // Buffer b holds D0, then P (packed, N0p / 2 columns, over D0) and D1 after it.
     const uint32_t d1off = round_up(static_cast<uint32_t>(p.N0p) / 2u, 32u);
@@ -196,16 +196,15 @@ uint32_t tmem_layout(ChainParams& p, int mode, bool dual, bool p_tmem = false) {
   }
   if (mode == MODE_CHAIN) {
     const uint32_t s1 = round_up(static_cast<uint32_t>(p.N1p), 32u);
-    p.d0_col[0] = 0;
-    p.d0_col[1] = dual ? s0 : 0u;
-    p.d1_col[0] = dual ? 2u * s0 : s0;
-    p.d1_col[1] = dual ? 2u * s0 + s1 : s0;
-    return pow2_at_least(dual ? 2u * (s0 + s1) : s0 + s1);
+    for (uint32_t b = 0; b < nbuf; ++b) {
+      p.d0_col[b] = b * s0;
+      p.d1_col[b] = nbuf * s0 + b * s1;
+    }
+    return pow2_at_least(nbuf * (s0 + s1));
   }
   const uint32_t cols = pow2_at_least(2u * s0);
   p.d0_col[0] = 0;
   p.d0_col[1] = cols / 2u;
-  p.d1_col[0] = p.d1_col[1] = 0;
   return cols;
 }
 
@@ -234,25 +233,30 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   // Candidates in order of preference.  Chains: two tiles in flight with P in shared
   // memory; else two tiles in flight with P in TMEM (wide N0, where two P tiles and two
   // accumulator pairs do not fit); else one tile at a time.
+  // dual: chain accumulator / P buffers (1, 2 or 4); single/pool always have two.
   struct Cand { int dual, groups, resident, alias, p_tmem; };
   Cand cands[16];
   int ncand = 0;
   if (mode == MODE_CHAIN) {
     ChainParams probe = p;
-    const bool tmem_dual_ok = tmem_layout(probe, mode, true) <= 512u;
-    const bool tmem_p_ok = tmem_layout(probe, mode, true, true) <= 512u;
+    const bool tmem_quad_ok = tmem_layout(probe, mode, 4u) <= 512u;
+    const bool tmem_dual_ok = tmem_layout(probe, mode, 2u) <= 512u;
+    const bool tmem_p_ok = tmem_layout(probe, mode, 2u, true) <= 512u;
+    // Four tiles in flight (narrow chains): each epilogue group one tile ahead.
+    if (tmem_quad_ok)
+      for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {4, 2, resident, 0, 0};
     if (tmem_dual_ok)
       for (int resident = 1; resident >= 0; --resident)
-        for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {1, 2, resident, alias, 0};
+        for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {2, 2, resident, alias, 0};
     if (tmem_p_ok)
-      for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {1, 2, resident, 0, 1};
+      for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {2, 2, resident, 0, 1};
     for (int resident = 1; resident >= 0; --resident)
-      for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {0, 1, resident, alias, 0};
+      for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {1, 1, resident, alias, 0};
   } else {
     // Pool staging is small: the warpgroups always take alternate tiles.
     const int gmin = mode == MODE_POOL ? 2 : 1;
     for (int resident = 1; resident >= 0; --resident)
-      for (int groups = 2; groups >= gmin; --groups) cands[ncand++] = {1, groups, resident, 0, 0};
+      for (int groups = 2; groups >= gmin; --groups) cands[ncand++] = {2, groups, resident, 0, 0};
   }
 
   int chosen = -1;
@@ -267,7 +271,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
       const uint32_t stage_bytes =
           k.resident ? a_bytes
                      : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
-      const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? (k.dual ? 2u : 1u) : 0u;
+      const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? static_cast<uint32_t>(k.dual) : 0u;
       const uint32_t obufs = k.groups == 2 ? 2u : 1u;
       const uint32_t shared = k.alias ? pbufs * std::max(p_bytes, out_bytes)
                                       : pbufs * p_bytes + obufs * out_bytes;
@@ -283,7 +287,8 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   }
   if (chosen < 0) return false;
   const Cand& k = cands[chosen];
-  p.acc_dual = k.dual;
+  p.acc_dual = k.dual >= 2 ? 1 : 0;
+  p.nbuf_log2 = mode != MODE_CHAIN ? 1 : (k.dual == 4 ? 2 : (k.dual == 2 ? 1 : 0));
   p.epi_groups = k.groups;
   p.resident = k.resident;
   p.out_alias_p = k.alias;
@@ -293,7 +298,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.halo = (k.resident && p.R > 1) ? 1 : 0;
   p.a_stage_bytes = p.halo ? (7u + static_cast<uint32_t>(p.R)) * 2048u : kABytes;
   p.kstages0 = p.halo ? p.S * p.kc_per_tap : p.kchunks0;
-  p.tmem_cols = tmem_layout(p, mode, k.dual != 0, k.p_tmem != 0);
+  p.tmem_cols = tmem_layout(p, mode, static_cast<uint32_t>(k.dual), k.p_tmem != 0);
   // P in TMEM with streamed weights: W1 is packed into as few ring stages as possible and
   // shared by the two tiles of a pair -- if those stages fit the ring at once.
   p.w1_group = 0;
@@ -309,7 +314,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   Regions r;
   r.ring = p.num_stages * p.stage_bytes;
   r.w_res = p.resident ? w_res : 0u;
-  const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? (k.dual ? 2u : 1u) : 0u;
+  const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? static_cast<uint32_t>(k.dual) : 0u;
   r.p_each = pbufs ? (p.out_alias_p ? std::max(p_bytes, out_bytes) : p_bytes) : 0u;
   r.out_each = p.out_alias_p ? 0u : out_bytes;
   r.bias = bias_bytes;
@@ -321,7 +326,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.off_w0 = off;
   p.off_w1 = off + static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
   off += r.w_res;
-  for (uint32_t b = 0; b < 2; ++b) p.off_p[b] = off + (b < pbufs ? b : 0u) * r.p_each;
+  for (uint32_t b = 0; b < kMaxBufs; ++b) p.off_p[b] = off + (b < pbufs ? b : 0u) * r.p_each;
   off += pbufs * r.p_each;
   for (uint32_t b = 0; b < 2; ++b) {
     if (p.out_alias_p) p.off_out[b] = p.off_p[b];
@@ -750,7 +755,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   static const int32_t need[5] = {4, 3, 9, 8, 5};
   if (kind < 0 || kind > 4) return B2B_ERR_UNSUPPORTED;
   if (dims == nullptr || out == nullptr) return B2B_ERR_NULL;
-  if (ndims < need[kind] || out_len < 40) return B2B_ERR_SHAPE;
+  if (ndims < need[kind] || out_len < 47) return B2B_ERR_SHAPE;
   for (int i = 0; i < need[kind]; ++i)
     if (dims[i] < 0 || dims[i] > INT32_MAX) return B2B_ERR_SHAPE;
   const int32_t d0 = static_cast<int32_t>(dims[0]), d1 = static_cast<int32_t>(dims[1]),
@@ -798,7 +803,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
     }
   }
   if (!ok) return B2B_ERR_UNSUPPORTED;
-  const uint32_t v[40] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[47] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -809,7 +814,9 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           static_cast<uint32_t>(p.kchunks1), static_cast<uint32_t>(p.N0p),
                           static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode),
                           static_cast<uint32_t>(p.p_tmem), static_cast<uint32_t>(p.w1_group),
-                          p.w1_per_stage, static_cast<uint32_t>(p.halo), p.a_stage_bytes};
+                          p.w1_per_stage, static_cast<uint32_t>(p.halo), p.a_stage_bytes,
+                          1u << p.nbuf_log2, p.off_p[2], p.off_p[3], p.d0_col[2], p.d0_col[3],
+                          p.d1_col[2], p.d1_col[3]};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

@@ -56,10 +56,10 @@ enum : uint32_t {
   BAR_EMPTY0 = kMaxStages,
   BAR_WFULL = 2 * kMaxStages,
   BAR_ACC_FULL0 = BAR_WFULL + 1,
-  BAR_ACC_EMPTY0 = BAR_ACC_FULL0 + 2,
-  BAR_P_FULL0 = BAR_ACC_EMPTY0 + 2,
-  BAR_D1_FULL0 = BAR_P_FULL0 + 2,
-  BAR_MMA_DONE = BAR_D1_FULL0 + 2,
+  BAR_ACC_EMPTY0 = BAR_ACC_FULL0 + kMaxBufs,
+  BAR_P_FULL0 = BAR_ACC_EMPTY0 + kMaxBufs,
+  BAR_D1_FULL0 = BAR_P_FULL0 + kMaxBufs,
+  BAR_MMA_DONE = BAR_D1_FULL0 + kMaxBufs,
   BAR_BIAS_READY = BAR_MMA_DONE + 1,
   BAR_COUNT = BAR_BIAS_READY + 1,
 };
@@ -115,6 +115,14 @@ struct Tracer {
 __device__ __forceinline__ int local_tiles(const ChainParams& p) {
   const int b = static_cast<int>(blockIdx.x), g = static_cast<int>(gridDim.x);
   return b < p.num_tiles ? (p.num_tiles - 1 - b) / g + 1 : 0;
+}
+
+// Buffer of the CTA's it-th tile and the phase parity of its barriers.
+__device__ __forceinline__ uint32_t buf_of(const ChainParams& p, int it) {
+  return static_cast<uint32_t>(it) & ((1u << p.nbuf_log2) - 1u);
+}
+__device__ __forceinline__ uint32_t use_of(const ChainParams& p, int it) {
+  return (static_cast<uint32_t>(it) >> p.nbuf_log2) & 1u;
 }
 
 // Bounded wait executed by a whole warp; the lanes agree on the outcome.
@@ -322,7 +330,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     }
   } else if (MODE == MODE_CHAIN) {
     // Same order as the MMA issuer consumes: G0(0..L-1), then G1(j), G0(j+L).
-    const int L = p.acc_dual ? 2 : 1;
+    const int L = 1 << p.nbuf_log2;
     for (int it = 0; ok && it < L && it < ntiles; ++it) ok = load_g0(it);
     for (int j = 0; ok && j < ntiles; ++j) {
       ok = load_g1(j);
@@ -402,7 +410,6 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const uint64_t res_w0 = sdesc_sw128(base + p.off_w0, w0_lbo, 1024u);
   const uint64_t res_w1 = sdesc_sw128(base + p.off_w1, w1_lbo, 1024u);
   const uint64_t p_desc0 = sdesc_sw128(base + p.off_p[0], 16u, 1024u);
-  const uint64_t p_desc1 = sdesc_sw128(base + p.off_p[1], 16u, 1024u);
   // Bias step operands (see fill_bias_operands): B is MN-major whatever the weights are.
   const uint32_t ones_addr = base + p.off_bias;
   const uint32_t n0blk = static_cast<uint32_t>((p.N0p + 63) >> 6);
@@ -428,12 +435,11 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   // GEMM0 of the it-th tile: D0[b] = A . W0 over all K chunks; commits ACC_FULL[b].
   auto issue_g0 = [&](int it) -> bool {
     const int32_t t = blockIdx.x + it * gridDim.x;
-    const uint32_t b = (MODE != MODE_CHAIN || p.acc_dual) ? static_cast<uint32_t>(it & 1) : 0u;
+    const uint32_t b = buf_of(p, it);
     if (MODE != MODE_CHAIN || p.p_tmem) {
       // The epilogue must have drained the buffer's previous tile (with P in TMEM: its
       // GEMM1 accumulator, the last thing read from the buffer).
-      const uint32_t u = static_cast<uint32_t>(it >> 1);
-      if (!warp_mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), (u & 1u) ^ 1u, p, abort_flag,
+      if (!warp_mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), use_of(p, it) ^ 1u, p, abort_flag,
                           SITE_MMA_ACC_EMPTY, t))
         return false;
       trace(EV_MMA_ACC_FREE, b, it);
@@ -488,9 +494,8 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   // GEMM1 of the j-th tile: D1[b] = P[b] . W1, P[b] being the epilogue's fp16/bf16 tile.
   auto issue_g1 = [&](int j) -> bool {
     const int32_t t = blockIdx.x + j * gridDim.x;
-    const uint32_t b = p.acc_dual ? static_cast<uint32_t>(j & 1) : 0u;
-    const uint32_t u = p.acc_dual ? static_cast<uint32_t>(j >> 1) : static_cast<uint32_t>(j);
-    if (!warp_mbar_wait(bars + 8u * (BAR_P_FULL0 + b), u & 1u, p, abort_flag, SITE_MMA_P_FULL, t))
+    const uint32_t b = buf_of(p, j);
+    if (!warp_mbar_wait(bars + 8u * (BAR_P_FULL0 + b), use_of(p, j), p, abort_flag, SITE_MMA_P_FULL, t))
       return false;
     trace(EV_MMA_P_READY, b, j);
     tc_fence_after_sync();
@@ -511,8 +516,9 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1,
                              kc1 == 0);
       } else {
-        const uint64_t adesc =
-            (b ? p_desc1 : p_desc0) + static_cast<uint64_t>(kc1) * (kPChunkBytes >> 4);
+        // P buffer b, chunk kc1 (P buffers are whole 1 KiB multiples apart)
+        const uint64_t adesc = p_desc0 + ((p.off_p[b] - p.off_p[0]) >> 4) +
+                               static_cast<uint64_t>(kc1) * (kPChunkBytes >> 4);
         issue_chunk<W1MN>(lead, d1, adesc, bdesc, idesc1, nks1, kc1 == 0);
       }
       if (!p.resident) {
@@ -589,8 +595,8 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       }
     } else if (MODE == MODE_CHAIN) {
       // A D0 buffer is free again once the epilogue has published that tile's P, so
-      // G0(j+L) follows G1(j); with two buffers (L = 2) two tiles are in flight.
-      const int L = p.acc_dual ? 2 : 1;
+      // G0(j+L) follows G1(j); with L buffers, L tiles are in flight.
+      const int L = 1 << p.nbuf_log2;
       for (int it = 0; ok && it < L && it < ntiles; ++it) ok = issue_g0(it);
       for (int j = 0; ok && j < ntiles; ++j) {
         ok = issue_g1(j);
@@ -827,68 +833,90 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
   const uint32_t group_threads = static_cast<uint32_t>(kNumEpiThreads / groups);
   const uint32_t bar_id = 1u + static_cast<uint32_t>(g);
   const bool elected = threadIdx.x == 64 + g * static_cast<int>(group_threads);
-  const bool dual = MODE != MODE_CHAIN || p.acc_dual;
   bool alive = true;
   Tracer trace(p, 2u + static_cast<uint32_t>(g), elected ? 1u : 0u);
+  const uint32_t sb = groups == 2 ? static_cast<uint32_t>(g) : 0u;   // staging buffer
+  const uint32_t out_tile = base + p.off_out[sb];
 
-  const int ntiles = local_tiles(p);
-  for (int it = g; it < ntiles; it += groups) {
+  // Chain, first half: GEMM0's accumulator -> P (shared memory or TMEM) -> P_FULL.
+  auto epi0 = [&](int it) {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    const uint32_t b = buf_of(p, it), u = use_of(p, it);
+    const uint32_t p_tile = base + p.off_p[b];
+    alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u, p, abort_flag,
+                      SITE_EPI_ACC_FULL, t);
+    if (elected) trace(EV_EPI_ACC_READY, g, it);
+    tc_fence_after_sync();
+    if (p.out_alias_p) {   // P[b] doubles as this group's previous output staging
+      if (elected) bulk_wait_read_all();
+      named_bar_sync(bar_id, group_threads);
+    }
+    if (alive) {
+      if (p.p_tmem)
+        drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b], p.N0p, p.d0_col[b]);
+      else
+        drain_to_smem<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, p_tile,
+                            row, kPChunkBytes);
+    }
+    tc_fence_before_sync();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8u * (BAR_P_FULL0 + b));
+    if (elected) trace(EV_EPI_P_DONE, g, it);
+  };
+
+  // Chain, second half: GEMM1's accumulator -> output staging -> TMA store.
+  auto epi1 = [&](int it) {
     const int32_t t = blockIdx.x + it * gridDim.x;
     const TileCoord tc = tile_coord<A4D>(p, t);
-    const uint32_t b = dual ? static_cast<uint32_t>(it & 1) : 0u;
-    const uint32_t u = dual ? static_cast<uint32_t>(it >> 1) : static_cast<uint32_t>(it);
-    const uint32_t sb = groups == 2 ? static_cast<uint32_t>(g) : 0u;   // staging buffer
-    const uint32_t out_tile = base + p.off_out[sb];
-    if (MODE == MODE_CHAIN) {
-      const uint32_t p_tile = base + p.off_p[b];
-      alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u & 1u, p, abort_flag,
-                        SITE_EPI_ACC_FULL, t);
-      if (elected) trace(EV_EPI_ACC_READY, g, it);
-      tc_fence_after_sync();
-      if (p.out_alias_p) {   // P[b] doubles as this group's previous output staging
-        if (elected) bulk_wait_read_all();
-        named_bar_sync(bar_id, group_threads);
-      }
-      if (alive) {
-        if (p.p_tmem)
-          drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b], p.N0p, p.d0_col[b]);
-        else
-          drain_to_smem<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, p_tile,
-                              row, kPChunkBytes);
-      }
-      tc_fence_before_sync();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8u * (BAR_P_FULL0 + b));
-      if (elected) trace(EV_EPI_P_DONE, g, it);
-
-      alive = warp_wait(alive, bars + 8u * (BAR_D1_FULL0 + b), u & 1u, p, abort_flag,
-                        SITE_EPI_D1_FULL, t);
-      if (elected) trace(EV_EPI_D1_READY, g, it);
-      tc_fence_after_sync();
-      if (!p.out_alias_p) {
-        if (elected) bulk_wait_read_all();
-        named_bar_sync(bar_id, group_threads);
-      }
-      if (elected) trace(EV_EPI_STAGING, g, it);
-      if (alive)
-        drain_to_smem<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p, out_tile,
-                            row, kPChunkBytes);
-      if (elected) trace(EV_EPI_DRAINED, g, it);
-      tc_fence_before_sync();
-      if (p.p_tmem) {   // the buffer (D0 -> P + D1) may take tile i + 2
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + b));
-      }
-      fence_proxy_async_smem();
+    const uint32_t b = buf_of(p, it), u = use_of(p, it);
+    alive = warp_wait(alive, bars + 8u * (BAR_D1_FULL0 + b), u, p, abort_flag,
+                      SITE_EPI_D1_FULL, t);
+    if (elected) trace(EV_EPI_D1_READY, g, it);
+    tc_fence_after_sync();
+    if (!p.out_alias_p) {
+      if (elected) bulk_wait_read_all();
       named_bar_sync(bar_id, group_threads);
-      if (elected && !*abort_flag) {
-        store_tile<A4D>(p, tmOut, out_tile, (p.N1p + 63) >> 6, tc);
-        bulk_commit_group();
-        trace(EV_EPI_STORED, g, it);
-      }
-    } else {
-      alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u & 1u, p, abort_flag,
+    }
+    if (elected) trace(EV_EPI_STAGING, g, it);
+    if (alive)
+      drain_to_smem<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p, out_tile,
+                          row, kPChunkBytes);
+    if (elected) trace(EV_EPI_DRAINED, g, it);
+    tc_fence_before_sync();
+    if (p.p_tmem) {   // the buffer (D0 -> P + D1) may take tile i + 2
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + b));
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(bar_id, group_threads);
+    if (elected && !*abort_flag) {
+      store_tile<A4D>(p, tmOut, out_tile, (p.N1p + 63) >> 6, tc);
+      bulk_commit_group();
+      trace(EV_EPI_STORED, g, it);
+    }
+  };
+
+  const int ntiles = local_tiles(p);
+  if (MODE == MODE_CHAIN && p.nbuf_log2 == 2) {
+    // Four buffers: the group runs the first half of its next tile before the second half
+    // of the current one, so that it drains GEMM0 while GEMM1 of the current tile runs.
+    if (g < ntiles) epi0(g);
+    for (int it = g; it < ntiles; it += groups) {
+      if (it + groups < ntiles) epi0(it + groups);
+      epi1(it);
+    }
+  } else if (MODE == MODE_CHAIN) {
+    for (int it = g; it < ntiles; it += groups) {
+      epi0(it);
+      epi1(it);
+    }
+  } else {
+    for (int it = g; it < ntiles; it += groups) {
+      const int32_t t = blockIdx.x + it * gridDim.x;
+      const TileCoord tc = tile_coord<A4D>(p, t);
+      const uint32_t b = buf_of(p, it), u = use_of(p, it);
+      alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + b), u, p, abort_flag,
                         SITE_EPI_ACC_FULL, t);
       if (elected) trace(EV_EPI_ACC_READY, g, it);
       tc_fence_after_sync();
@@ -992,7 +1020,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars + 8u * (BAR_EMPTY0 + s), 1);
     }
     mbar_init(bars + 8u * BAR_WFULL, 1);
-    for (uint32_t a = 0; a < 2; ++a) {
+    for (uint32_t a = 0; a < kMaxBufs; ++a) {
       mbar_init(bars + 8u * (BAR_ACC_FULL0 + a), 1);
       mbar_init(bars + 8u * (BAR_ACC_EMPTY0 + a), warps_per_group);
       mbar_init(bars + 8u * (BAR_P_FULL0 + a), warps_per_group);

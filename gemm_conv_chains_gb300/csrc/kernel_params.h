@@ -66,6 +66,7 @@ constexpr int kNumEpiWarps = 8;       // two warpgroups of four (one per TMEM la
 constexpr int kNumEpiThreads = 32 * kNumEpiWarps;
 constexpr int kNumThreads = 64 + kNumEpiThreads;   // warp 0 TMA, warp 1 MMA + TMEM, 2..9 epilogue
 constexpr int kMaxStages = 8;
+constexpr int kMaxBufs = 4;          // accumulator / P buffers per CTA
 // Bias operands in shared memory (at off_bias): a 1 KiB ONES tile, then per GEMM one
 // 2 KiB BIAS block per 64-wide N block.
 constexpr uint32_t kOnesBytes = 1024;
@@ -107,9 +108,12 @@ struct ChainParams {
   uint32_t off_ring, stage_bytes, num_stages;
   uint32_t w0_chunk_bytes, w1_chunk_bytes;
   uint32_t off_w0, off_w1;      // resident weights (resident != 0)
-  uint32_t off_p[2], off_out[2], off_bias, off_bar;
+  uint32_t off_p[kMaxBufs], off_out[2], off_bias, off_bar;
   int32_t resident;             // 1: W0/W1 loaded once per CTA; 0: streamed per tile
   int32_t out_alias_p;          // 1: output staging b shares P buffer b
+  int32_t nbuf_log2;            // log2 of the accumulator (and, chained, P) buffers: tile i
+                                //    of the CTA uses buffer i mod 2^nbuf_log2 (4 buffers:
+                                //    narrow smem-P chains, each epilogue group one tile ahead)
   int32_t acc_dual;             // 1: accumulators (and, chained, P) double-buffered:
                                 //    tile i uses buffer i & 1, two tiles in flight
   int32_t p_tmem;               // 1 (chain): P is written back into TMEM over the consumed
@@ -126,7 +130,7 @@ struct ChainParams {
   int32_t epi_groups;           // 2: the epilogue warpgroups take alternate tiles;
                                 // 1: both warpgroups split the columns of every tile
   uint32_t tmem_cols;
-  uint32_t d0_col[2], d1_col[2];  // TMEM columns of GEMM0 / GEMM1 accumulator buffers
+  uint32_t d0_col[kMaxBufs], d1_col[kMaxBufs];  // TMEM columns of the accumulator buffers
   uint64_t wait_limit_ns;
   uint32_t kernel_id;
   uint32_t* err;                // device error word {code, kernel, site, tile}

@@ -182,7 +182,7 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1}
  *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
- * out (out_len >= 40) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ * out (out_len >= 47) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
  * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
  * P offsets [2], bytes per P buffer, staging offsets [2], bytes per staging buffer,
@@ -192,7 +192,9 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * (0 chain, 1 single, 2 pool), 1 if the chain's intermediate is kept in TMEM instead
  * of shared memory (wide N0: GEMM1 then reads its A operand from TMEM), 1 if W1 is then
  * loaded once per pair of tiles into shared ring stages, the W1 chunks per stage, 1 if a
- * conv loads one halo box per column tap for all row taps, and the A bytes per ring stage.
+ * conv loads one halo box per column tap for all row taps, the A bytes per ring stage, the
+ * number of accumulator buffers (tiles in flight: 1, 2 or 4), P offsets [2..3], GEMM0
+ * accumulator columns [2..3] and GEMM1 accumulator columns [2..3].
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,

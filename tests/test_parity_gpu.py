@@ -82,6 +82,20 @@ def test_b2b_gemm_ffn_workload_sampled_rows():
 
 
 @pytest.mark.parametrize("integer", [True, False])
+def test_b2b_gemm_narrow_four_buffers_sampled_rows(integer):
+    # 64 -> 64 -> 64 keeps four tiles in flight (each epilogue group one tile ahead); with
+    # 5 x SMs + 1 tiles CTA 0 cycles through the four buffers 1.5 times, the last tile ragged.
+    nsm = ops.num_sms()
+    M = 128 * nsm * 5 + 77
+    acts = ("relu", "none") if integer else ("hardswish", "relu")
+    w = wl.GemmChain("quad", "f16", M, 64, 64, 64, *acts)
+    rng = np.random.default_rng(7)
+    cta0 = np.concatenate([np.arange(128 * t, min(128 * t + 128, M)) for t in range(0, 5 * nsm + 1, nsm)])
+    rows = np.unique(np.concatenate([cta0, rng.choice(M, 512, replace=False)]))
+    run_b2b_gemm(w, seed=13, integer=integer, rows=rows)
+
+
+@pytest.mark.parametrize("integer", [True, False])
 def test_b2b_gemm_wide_streamed_pairs_sampled_rows(integer):
     # K0 = 256 streams the weights, so GEMM0 of each tile pair runs interleaved (one W0
     # chunk per stage for both tiles); 3 x SMs + 1 tiles give CTA 0 two pairs, the second

@@ -20,7 +20,8 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "off_w1", "w_res", "w0_chunk", "w1_chunk", "off_p0", "off_p1", "p", "off_out0",
           "off_out1", "out", "off_bias", "bias", "off_bar", "bar", "tmem_cols", "d0_col0",
           "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0", "kchunks1",
-          "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes"]
+          "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes",
+          "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2", "d1_col3"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4}
@@ -28,8 +29,8 @@ KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nh
 
 def plan(kind, dims):
     arr = (ctypes.c_int64 * len(dims))(*dims)
-    out = (ctypes.c_uint32 * 40)()
-    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 40)
+    out = (ctypes.c_uint32 * 47)()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 47)
     return st, dict(zip(FIELDS, list(out)))
 
 
@@ -83,8 +84,11 @@ def check(kind, dims, row_major_w):
         per = p["w1_per_stage"]
         assert per >= 1 and per * w1_chunk <= p["stage_bytes"]
         assert -(-p["kchunks1"] // per) <= p["stages"]
-    # P buffers used: tile i -> P[i & 1] when dual, else P[0]; none when P is in TMEM
-    pbufs = 0 if p_tmem else ((2 if dual else 1) if mode == 0 else 0)
+    nbuf = p["nbuf"]
+    assert nbuf in (1, 2, 4) and (nbuf > 1) == dual and (mode == 0 or nbuf == 2)
+    assert nbuf != 4 or (mode == 0 and not p_tmem and groups == 2 and not p["alias"])
+    # P buffers used: tile i -> P[i mod nbuf]; none when P is in TMEM
+    pbufs = 0 if p_tmem else (nbuf if mode == 0 else 0)
     obufs = 2 if groups == 2 else 1
     if mode == 0 and not p_tmem:
         need_p = max(p_need, out_need) if p["alias"] else p_need
@@ -123,15 +127,9 @@ def check(kind, dims, row_major_w):
             spans.append((lo, hi))
         assert spans[0][1] <= spans[1][0] or spans[1][1] <= spans[0][0]
         return p
-    accs = [("d0_0", p["d0_col0"], N0p)]
-    if mode != 0 or dual:
-        accs.append(("d0_1", p["d0_col1"], N0p))
-    else:
-        assert p["d0_col1"] == p["d0_col0"]
+    accs = [(f"d0_{b}", p[f"d0_col{b}"], N0p) for b in range(nbuf if mode == 0 else 2)]
     if mode == 0:
-        accs.append(("d1_0", p["d1_col0"], N1p))
-        if dual:
-            accs.append(("d1_1", p["d1_col1"], N1p))
+        accs += [(f"d1_{b}", p[f"d1_col{b}"], N1p) for b in range(nbuf)]
     for name, col, n in accs:
         assert col % 32 == 0 and col + n <= p["tmem_cols"], (name, col, n)
     for (a, ca, na), (b, cb, nb) in itertools.combinations(accs, 2):
@@ -167,10 +165,11 @@ def test_ffn_plan_keeps_p_in_tmem():
     assert p["w1_group"] == 1 and p["w1_per_stage"] == 3
 
 
-def test_small_chains_keep_two_tiles_in_flight():
+def test_small_chains_keep_four_tiles_in_flight():
+    # 64 -> 64 -> 64: four (D0 + D1) buffers of 64 + 64 columns fill the 512 TMEM columns
     for dims in ((200704, 64, 64, 64), (1024, 64, 64, 64)):
         p = check("b2b_gemm", dims, True)
-        assert p["dual"] == 1 and p["groups"] == 2 and p["resident"] == 1
+        assert p["nbuf"] == 4 and p["groups"] == 2 and p["resident"] == 1
     p = check("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128), False)
     assert p["dual"] == 1 and p["resident"] == 1
 
