@@ -247,6 +247,28 @@ def maxpool2x2_nhwc(x, out=None, stream=None):
 # diagnostics
 # ------------------------------------------------------------------------------------
 
+# Field names of b2b_debug_plan's output, in order (see include/b2b.h).
+PLAN_FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "ring", "off_w0",
+               "off_w1", "w_res", "w0_chunk", "w1_chunk", "off_p0", "off_p1", "p", "off_out0",
+               "off_out1", "out", "off_bias", "bias", "off_bar", "bar", "tmem_cols", "d0_col0",
+               "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0",
+               "kchunks1", "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo",
+               "a_stage_bytes", "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2",
+               "d1_col3"]
+PLAN_KINDS = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
+              "conv_relu_maxpool": 4}
+
+
+def debug_plan(kind: str, dims) -> dict:
+    """The launch plan the entry point `kind` would use for `dims` (b2b_debug_plan; no CUDA
+    call).  Raises B2BError with the entry point's status if it would not launch."""
+    arr = (ctypes.c_int64 * len(dims))(*[int(d) for d in dims])
+    out = (ctypes.c_uint32 * len(PLAN_FIELDS))()
+    _raise(lib().b2b_debug_plan(PLAN_KINDS[kind], arr, len(dims), out, len(PLAN_FIELDS)),
+           "b2b_debug_plan")
+    return dict(zip(PLAN_FIELDS, [int(v) for v in out]))
+
+
 def version() -> str:
     return lib().b2b_version().decode()
 

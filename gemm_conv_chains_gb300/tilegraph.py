@@ -1,0 +1,282 @@
+"""Tile-graph model of the fused chains, on the host (no CUDA).
+
+Welder notes, "Operator-tile and Tile-graph": once two operators are connected through a
+reuse tile, every tile of the connected graph follows from the output tile (tile
+propagation; for a convolution the input tile is the output tile plus the filter halo,
+an upper bound on the region read), the memory traffic of a level is the sum of the
+tiles it moves, and the footprint is what a best-fit allocation of the live buffers,
+in topological order, needs.  Here the model is applied to the chain kernels of this
+package: `propagate` gives the operand tiles of one output tile, `dram_traffic` the
+unique bytes of a launch, `l2_to_smem_traffic` the bytes the kernel's TMA and global
+loads move from L2 into the SMs for a given launch plan (`ops.debug_plan`), and
+`smem_footprint` a best-fit allocation of buffers by lifetime.  Predictions are compared
+with the ncu counters of the same launches in the profile summaries.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Iterable, List, Optional, Sequence, Tuple
+
+from . import workloads as wl
+
+ELEM = 2          # fp16 / bf16 bytes
+TILE_M = 128      # rows of a 2-D tile = TMEM lanes
+TILE_H, TILE_W = 8, 16   # output pixels of a conv tile
+
+
+# ------------------------------------------------------------------------------------
+# propagation
+# ------------------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class TileGraph:
+    """Operand tiles (element shapes) of one output tile of a fused chain."""
+    kind: str
+    tiles: Dict[str, Tuple[int, ...]]
+
+    def bytes(self, name: str) -> int:
+        return math.prod(self.tiles[name]) * ELEM
+
+
+def propagate(w) -> TileGraph:
+    """Every operand tile of the chain from its output tile.
+
+    b2b GEMM: out (128, N1) <- P (128, N0), W1 (N0, N1) <- A (128, K0), W0 (K0, N0).
+    Conv chain: out (8, 16, C1) <- P (8, 16, C0), W1 (C1, C0) <- x (8+R-1, 16+S-1, C),
+    W0 (C0, R, S, C).  Conv + pool: pooled (4, 8, F) <- conv out (8, 16, F) (the (2,2,F)
+    reuse tile per pooled pixel) <- x (10, 18, C), W (F, 3, 3, C)."""
+    if isinstance(w, wl.GemmChain):
+        return TileGraph("gemm_chain", {"out": (TILE_M, w.N1), "P": (TILE_M, w.N0),
+                                        "W1": (w.N0, w.N1), "A": (TILE_M, w.K0),
+                                        "W0": (w.K0, w.N0)})
+    if isinstance(w, wl.ConvChain):
+        return TileGraph("conv_chain", {"out": (TILE_H, TILE_W, w.C1),
+                                        "P": (TILE_H, TILE_W, w.C0), "W1": (w.C1, w.C0),
+                                        "x": (TILE_H + w.R - 1, TILE_W + w.S - 1, w.C),
+                                        "W0": (w.C0, w.R, w.S, w.C)})
+    if isinstance(w, wl.ConvPool):
+        return TileGraph("conv_pool", {"out": (TILE_H // 2, TILE_W // 2, w.Cout),
+                                       "conv": (TILE_H, TILE_W, w.Cout),
+                                       "x": (TILE_H + 2, TILE_W + 2, w.Cin),
+                                       "W": (w.Cout, 3, 3, w.Cin)})
+    raise TypeError(w)
+
+
+# ------------------------------------------------------------------------------------
+# traffic
+# ------------------------------------------------------------------------------------
+def dram_traffic(w, fused: bool = True) -> int:
+    """Unique bytes of one launch: each tensor read or written once (the sum of the
+    chain's input and output tensors).  Unfused, the intermediate is written by the first
+    operator and read back by the second."""
+    return w.floor_bytes if fused else w.unfused_bytes
+
+
+def plan_of(w) -> dict:
+    """The C planner's launch plan for a workload."""
+    from . import ops
+    if isinstance(w, wl.GemmChain):
+        return ops.debug_plan("b2b_gemm", (w.M, w.K0, w.N0, w.N1))
+    if isinstance(w, wl.ConvChain):
+        return ops.debug_plan("b2b_conv_nhwc", (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1))
+    return ops.debug_plan("conv_relu_maxpool", (w.N, w.H, w.W, w.Cin, w.Cout))
+
+
+def tiles_per_cta(num_tiles: int, num_sms: int) -> List[int]:
+    """Tiles of each CTA of the persistent grid (CTA b takes tiles b, b + grid, ...)."""
+    grid = max(1, min(num_tiles, num_sms))
+    return [len(range(b, num_tiles, grid)) for b in range(grid)]
+
+
+def _overlap(lo: int, n: int, extent: int) -> int:
+    """Length of [lo, lo + n) inside [0, extent): TMA fetches only in-bounds elements."""
+    return max(0, min(lo + n, extent) - max(lo, 0))
+
+
+def _conv_tile_input_bytes(N, H, W, C, R, S, pad, halo: bool) -> int:
+    """Input bytes all tiles of an RxS conv (8 x 16 output tiles) load from L2: one box of
+    (8 + R - 1) x 16 pixels per column tap with halo loads, else one 8 x 16 box per tap,
+    each clipped to the image and to the C channels of its 64-channel block."""
+    Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
+    tiles_h, tiles_w = -(-Ho // TILE_H), -(-Wo // TILE_W)
+    rows_per_box = TILE_H + R - 1 if halo else TILE_H
+    row_offsets = [0] if halo else list(range(R))
+    total = 0
+    for th in range(tiles_h):
+        for tw in range(tiles_w):
+            for s in range(S):
+                cols = _overlap(tw * TILE_W + s - pad, TILE_W, W)
+                for r in row_offsets:
+                    rows = _overlap(th * TILE_H + r - pad, rows_per_box, H)
+                    total += rows * cols
+    return N * total * C * ELEM
+
+
+def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Dict[str, int]:
+    """Bytes one fused launch moves from L2 into the SMs, by operand, for `plan`.
+
+    A: every tile's rows (2-D) or input boxes (conv), clipped to the tensor.  Weights:
+    once per CTA when resident; when streamed, W0 once per tile and W1 once per tile, or
+    once per pair of tiles when the plan groups W1 (P in TMEM).  Biases: once per CTA
+    (plain loads by the epilogue warps)."""
+    plan = plan or plan_of(w)
+    per_cta = tiles_per_cta(plan["tiles"], num_sms)
+    ctas = len(per_cta)
+    out: Dict[str, int] = {}
+    if isinstance(w, wl.GemmChain):
+        out["A"] = w.M * w.K0 * ELEM
+        w0, w1 = w.K0 * w.N0 * ELEM, w.N0 * w.N1 * ELEM
+        if plan["resident"]:
+            out["W0"], out["W1"] = ctas * w0, ctas * w1
+        else:
+            out["W0"] = plan["tiles"] * w0
+            loads_w1 = sum(-(-n // 2) for n in per_cta) if plan["w1_group"] else plan["tiles"]
+            out["W1"] = loads_w1 * w1
+        out["bias"] = ctas * (w.N0 + w.N1) * ELEM
+    elif isinstance(w, wl.ConvChain):
+        if w.R == 1 and w.S == 1 and w.pad == 0:   # runs as a GEMM over the pixels
+            out["A"] = w.N * w.H * w.W * w.C * ELEM
+        else:
+            out["A"] = _conv_tile_input_bytes(w.N, w.H, w.W, w.C, w.R, w.S, w.pad,
+                                              bool(plan["halo"]))
+        w0, w1 = w.C0 * w.R * w.S * w.C * ELEM, w.C1 * w.C0 * ELEM
+        if plan["resident"]:
+            out["W0"], out["W1"] = ctas * w0, ctas * w1
+        else:
+            out["W0"], out["W1"] = plan["tiles"] * w0, plan["tiles"] * w1
+        out["bias"] = ctas * (w.C0 + w.C1) * ELEM
+    else:
+        out["A"] = _conv_tile_input_bytes(w.N, w.H, w.W, w.Cin, 3, 3, 1, bool(plan["halo"]))
+        wt = w.Cout * 9 * w.Cin * ELEM
+        out["W0"] = ctas * wt if plan["resident"] else plan["tiles"] * wt
+        out["bias"] = ctas * w.Cout * ELEM
+    out["total"] = sum(out.values())
+    return out
+
+
+# ------------------------------------------------------------------------------------
+# footprint
+# ------------------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class Buffer:
+    name: str
+    size: int
+    live: Tuple[int, int]        # [first step, last step] in topological order
+    align: int = 1024
+
+
+def best_fit(buffers: Sequence[Buffer]) -> Tuple[int, Dict[str, int]]:
+    """Offsets of `buffers` such that two buffers live at a common step never overlap:
+    buffers are placed largest first, each at the lowest aligned offset that fits beside
+    the already placed buffers whose lifetimes intersect its own.  Returns (extent,
+    offsets)."""
+    placed: List[Tuple[Buffer, int]] = []
+    offsets: Dict[str, int] = {}
+    for b in sorted(buffers, key=lambda b: (-b.size, b.name)):
+        busy = sorted((off, off + o.size) for o, off in placed
+                      if not (o.live[1] < b.live[0] or b.live[1] < o.live[0]))
+        off = 0
+        for lo, hi in busy:
+            if off + b.size <= lo:
+                break
+            off = max(off, -(-hi // b.align) * b.align)
+        placed.append((b, off))
+        offsets[b.name] = off
+    extent = max((off + b.size for b, off in placed), default=0)
+    return extent, offsets
+
+
+def chain_buffers(plan: dict) -> List[Buffer]:
+    """Shared-memory buffers of a launch plan, with lifetimes over the steps of one tile:
+    0 load, 1 GEMM0, 2 epilogue 0 (writes P), 3 GEMM1 (reads P), 4 epilogue 1 (writes the
+    output staging), 5 store.  The ring, resident weights, bias operands and barriers live
+    throughout.  When every P slot belongs to one epilogue group and that group's staging
+    (as many P slots as staging buffers), a slot's P and its staging are used one after
+    the other by the same tiles, so their lifetimes are disjoint; otherwise the tiles in
+    flight keep every buffer live at every step."""
+    whole = (0, 5)
+    bufs = [Buffer("ring", plan["ring"], whole), Buffer("bias", plan["bias"], whole),
+            Buffer("bar", plan["bar"], whole)]
+    if plan["resident"]:
+        bufs.append(Buffer("weights", plan["w_res"], whole))
+    chain = plan["mode"] == 0
+    pbufs = plan["nbuf"] if (chain and not plan["p_tmem"]) else 0
+    p_bytes = (plan["N0p"] + 63) // 64 * 128 * 128
+    out_cols = plan["N1p"] if chain else plan["N0p"]
+    per_chunk = 32 * 128 if plan["mode"] == 2 else 128 * 128   # pooled: 4 x 8 pixels per tile
+    out_bytes = (out_cols + 63) // 64 * per_chunk
+    obufs = 2 if plan["groups"] == 2 else 1
+    paired = pbufs == obufs
+    for i in range(pbufs):
+        bufs.append(Buffer(f"P{i}", p_bytes, (2, 3) if paired else whole))
+    for i in range(obufs):
+        bufs.append(Buffer(f"out{i}", out_bytes, (4, 5) if paired else whole))
+    return bufs
+
+
+def smem_footprint(plan: dict) -> int:
+    """Best-fit shared-memory extent of a plan's buffers (without the 1 KiB the kernel
+    adds to align its base)."""
+    return best_fit(chain_buffers(plan))[0]
+
+
+# ------------------------------------------------------------------------------------
+# model vs. counters
+# ------------------------------------------------------------------------------------
+NCU_L2_TO_SM = "l1tex__m_xbar2l1tex_read_bytes.sum"
+NCU_DRAM = ("dram__bytes_read.sum", "dram__bytes_write.sum")
+
+
+def read_ncu_raw_csv(path: str) -> Dict[str, float]:
+    """First launch of an `ncu -i <report> --page raw --csv` export, metric -> value in
+    bytes where the unit is a byte multiple."""
+    import csv
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    with open(path, newline="") as f:
+        rows = list(csv.reader(f))
+    hdr = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
+    names, units, vals = rows[hdr], rows[hdr + 1], rows[hdr + 2]
+    out: Dict[str, float] = {}
+    for n, u, v in zip(names, units, vals):
+        try:
+            x = float(v.replace(",", ""))
+        except ValueError:
+            continue
+        out[n] = x * scale.get(u, 1)
+    return out
+
+
+def report(ncu: Optional[Dict[str, str]] = None) -> str:
+    """Markdown table of the model for every workload, beside the counters of one
+    captured launch per workload where an export is given (name -> csv path)."""
+    ncu = ncu or {}
+    lines = ["| workload | plan | DRAM unique MB | DRAM unfused MB | L2->SM model MB "
+             "| L2->SM ncu MB | model/ncu | smem model | smem planner |",
+             "|---|---|---|---|---|---|---|---|---|"]
+    for name, w in wl.WORKLOADS.items():
+        plan = plan_of(w)
+        t = l2_to_smem_traffic(w, plan)
+        desc = ("resident" if plan["resident"] else "streamed") + \
+            (", P in TMEM" if plan["p_tmem"] else f", {plan['nbuf']} P buffers") * (plan["mode"] == 0) + \
+            (", halo" if plan["halo"] else "") + (", alias" if plan["alias"] else "")
+        got = read_ncu_raw_csv(ncu[name]).get(NCU_L2_TO_SM) if name in ncu else None
+        t_total = t["total"]
+        lines.append(
+            f"| {name} | {desc} | {dram_traffic(w) / 1e6:.2f} | {dram_traffic(w, False) / 1e6:.2f} "
+            f"| {t['total'] / 1e6:.3f} | {'' if got is None else f'{got / 1e6:.3f}'} "
+            f"| {'' if not got else f'{t_total / got:.3f}'} "
+            f"| {smem_footprint(plan) + 1024} | {plan['smem']} |")
+    return "\n".join(lines)
+
+
+def main(argv: Optional[Sequence[str]] = None) -> None:
+    import argparse
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--ncu", nargs="*", default=[], metavar="WORKLOAD=CSV",
+                    help="raw-page csv export of one captured chain launch per workload")
+    args = ap.parse_args(argv)
+    print(report(dict(a.split("=", 1) for a in args.ncu)))
+
+
+if __name__ == "__main__":
+    main()

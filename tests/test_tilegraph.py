@@ -1,0 +1,109 @@
+"""The host-side tile-graph model: propagation, traffic and footprint (CPU only).
+
+Expected values are derived by hand from the tile shapes and the kernel's load schedule,
+not from the model's own code: a 3x3 conv's interior tile reads a 10 x 18 input tile; the
+FFN launch streams W0 once per tile and W1 once per tile pair on 152 CTAs; a best-fit
+allocation lets buffers with disjoint lifetimes share an offset.
+"""
+import pytest
+
+from gemm_conv_chains_gb300 import tilegraph as tg
+from gemm_conv_chains_gb300 import workloads as wl
+
+
+def test_propagation_shapes():
+    g = tg.propagate(wl.GEMM_FFN)
+    assert g.tiles == {"out": (128, 128), "P": (128, 256), "W1": (256, 128),
+                       "A": (128, 256), "W0": (256, 256)}
+    c = tg.propagate(wl.CONV3X3_1X1)
+    assert c.tiles["x"] == (10, 18, 64) and c.tiles["P"] == (8, 16, 64)
+    assert c.tiles["out"] == (8, 16, 128)
+    p = tg.propagate(wl.CONV_POOL)
+    # the (2,2,F) reuse tile per pooled pixel: 4 x 8 pooled pixels need 8 x 16 conv pixels
+    assert p.tiles["out"] == (4, 8, 64) and p.tiles["conv"] == (8, 16, 64)
+    assert p.tiles["x"] == (10, 18, 64)
+    assert p.bytes("x") == 10 * 18 * 64 * 2
+
+
+def test_dram_traffic_is_the_sum_of_tensors():
+    w = wl.GEMM_FFN
+    assert tg.dram_traffic(w) == 2 * (32768 * 256 + 256 * 256 + 256 * 128 + 32768 * 128
+                                      + 256 + 128)
+    assert tg.dram_traffic(w, fused=False) - tg.dram_traffic(w) == 2 * 2 * 32768 * 256
+
+
+def test_tiles_per_cta():
+    n = tg.tiles_per_cta(256, 152)
+    assert len(n) == 152 and sum(n) == 256 and n.count(2) == 104 and n.count(1) == 48
+    assert tg.tiles_per_cta(7, 152) == [1] * 7
+
+
+def test_ffn_l2_traffic_by_hand():
+    # 256 tiles on 152 CTAs (104 with 2 tiles, 48 with 1): W0 streamed per tile, W1 once
+    # per pair of tiles (P in TMEM), biases once per CTA.
+    t = tg.l2_to_smem_traffic(wl.GEMM_FFN)
+    assert t["A"] == 32768 * 256 * 2
+    assert t["W0"] == 256 * 256 * 256 * 2
+    assert t["W1"] == 152 * 256 * 128 * 2
+    assert t["bias"] == 152 * (256 + 128) * 2
+    assert t["total"] == 16_777_216 + 33_554_432 + 9_961_472 + 116_736   # 60.41 MB
+
+
+def test_conv_halo_boxes_read_less():
+    # interior tiles of a 3x3 conv: halo loads move 3 boxes of 10 x 16 pixels, per-tap
+    # loads 9 boxes of 8 x 16 pixels, per 64-channel block
+    halo = tg._conv_tile_input_bytes(1, 64, 64, 64, 3, 3, 1, halo=True)
+    taps = tg._conv_tile_input_bytes(1, 64, 64, 64, 3, 3, 1, halo=False)
+    assert halo < taps
+    interior_halo = 3 * 10 * 16 * 64 * 2
+    interior_taps = 9 * 8 * 16 * 64 * 2
+    assert interior_halo * 72 == interior_taps * 30
+    # a 1-pixel image (pad 1): the pixel lies in the boxes of taps r, s in {0, 1} (4 per-tap
+    # boxes) and in the halo boxes of column taps 0 and 1 (2 boxes); out-of-bounds fill is
+    # not fetched
+    assert tg._conv_tile_input_bytes(1, 1, 1, 8, 3, 3, 1, halo=False) == 4 * 8 * 2
+    assert tg._conv_tile_input_bytes(1, 1, 1, 8, 3, 3, 1, halo=True) == 2 * 8 * 2
+
+
+def test_best_fit_shares_offsets_by_lifetime():
+    B = tg.Buffer
+    ext, off = tg.best_fit([B("a", 4096, (0, 1)), B("b", 4096, (2, 3)), B("c", 1024, (0, 3))])
+    assert off["a"] == off["b"] and ext == 5120       # a and b never live together
+    ext, off = tg.best_fit([B("a", 4096, (0, 2)), B("b", 4096, (2, 3))])
+    assert off["a"] != off["b"] and ext == 8192       # both live at step 2
+    ext, off = tg.best_fit([B("a", 100, (0, 1)), B("b", 100, (0, 1))])
+    assert sorted(off.values()) == [0, 1024] and ext == 1124   # 1 KiB alignment
+
+
+@pytest.mark.parametrize("name", sorted(wl.WORKLOADS))
+def test_footprint_matches_the_planner(name):
+    # the C planner's layout is tight: the best-fit extent of the same buffers plus the
+    # 1 KiB base alignment reproduces its dynamic shared memory size
+    plan = tg.plan_of(wl.WORKLOADS[name])
+    assert tg.smem_footprint(plan) + 1024 == plan["smem"]
+
+
+def test_aliased_plan_needs_the_lifetime_analysis():
+    # conv3x3 -> 1x1: the planner aliases each P buffer with its group's output staging;
+    # without lifetimes the buffers would not fit in 227 KiB
+    plan = tg.plan_of(wl.CONV3X3_1X1)
+    assert plan["alias"] == 1
+    bufs = tg.chain_buffers(plan)
+    no_reuse = sum(-(-b.size // 1024) * 1024 for b in bufs)
+    assert no_reuse + 1024 > 227 * 1024 >= tg.smem_footprint(plan) + 1024
+
+
+def test_read_ncu_raw_csv(tmp_path):
+    # the raw page: a header row, a units row, then one row per launch
+    p = tmp_path / "raw.csv"
+    p.write_text('"ID","Kernel Name","l1tex__m_xbar2l1tex_read_bytes.sum","dram__bytes_read.sum",'
+                 '"launch__grid_size"\n'
+                 '"","","Mbyte","Kbyte",""\n'
+                 '"0","chain_kernel","60.41","17,074.43","152"\n'
+                 '"1","chain_kernel","1.00","2.00","152"\n')
+    d = tg.read_ncu_raw_csv(str(p))
+    assert d[tg.NCU_L2_TO_SM] == pytest.approx(60.41e6)
+    assert d["dram__bytes_read.sum"] == pytest.approx(17_074_430)
+    assert d["launch__grid_size"] == 152 and "Kernel Name" not in d
+    table = tg.report({"gemm_ffn": str(p)})
+    assert "| gemm_ffn |" in table and "60.410 | 60.410 | 1.000" in table
