@@ -8,7 +8,8 @@ tiles it moves, and the footprint is what a best-fit allocation of the live buff
 in topological order, needs.  Here the model is applied to the chain kernels of this
 package: `propagate` gives the operand tiles of one output tile, `dram_traffic` the
 unique bytes of a launch, `l2_to_smem_traffic` the bytes the kernel's TMA and global
-loads move from L2 into the SMs for a given launch plan (`ops.debug_plan`), and
+loads move from L2 into the SMs for a given launch plan (`ops.debug_plan`; whole boxes,
+out-of-bounds fill included), and
 `smem_footprint` a best-fit allocation of buffers by lifetime.  Predictions are compared
 with the ncu counters of the same launches in the profile summaries.
 """
@@ -94,9 +95,9 @@ def _overlap(lo: int, n: int, extent: int) -> int:
 
 
 def _conv_tile_input_bytes(N, H, W, C, R, S, pad, halo: bool) -> int:
-    """Input bytes all tiles of an RxS conv (8 x 16 output tiles) load from L2: one box of
-    (8 + R - 1) x 16 pixels per column tap with halo loads, else one 8 x 16 box per tap,
-    each clipped to the image and to the C channels of its 64-channel block."""
+    """Input bytes inside the image that all tiles of an RxS conv (8 x 16 output tiles)
+    read: one box of (8 + R - 1) x 16 pixels per column tap with halo loads, else one
+    8 x 16 box per tap, each clipped to the image (the useful part of the boxes)."""
     Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
     tiles_h, tiles_w = -(-Ho // TILE_H), -(-Wo // TILE_W)
     rows_per_box = TILE_H + R - 1 if halo else TILE_H
@@ -112,45 +113,54 @@ def _conv_tile_input_bytes(N, H, W, C, R, S, pad, halo: bool) -> int:
     return N * total * C * ELEM
 
 
+A_BOX = TILE_M * 64 * ELEM   # one 128-row x 64-element A box (16 KiB)
+
+
 def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Dict[str, int]:
     """Bytes one fused launch moves from L2 into the SMs, by operand, for `plan`.
 
-    A: every tile's rows (2-D) or input boxes (conv), clipped to the tensor.  Weights:
-    once per CTA when resident; when streamed, W0 once per tile and W1 once per tile, or
-    once per pair of tiles when the plan groups W1 (P in TMEM).  Biases: once per CTA
-    (plain loads by the epilogue warps)."""
+    Every TMA load moves its whole box: elements outside the tensor are filled with zeros
+    in shared memory but cross the L2 -> SM crossbar all the same (ncu's
+    l1tex__m_xbar2l1tex_read_bytes of the 3x3 conv chains on 56 x 56 and 64 x 64 images
+    and of conv + pool equals the whole-box sum to the byte).  A: per tile, one box per
+    K chunk (2-D), or per column tap and channel block (halo boxes of (8 + R - 1) x 16
+    pixels), or per tap and channel block (8 x 16 pixels).  Weights: once per CTA when
+    resident; when streamed, W0 once per tile and W1 once per tile, or once per pair of
+    tiles when the plan groups W1 (P in TMEM).  Biases: once per CTA (plain loads by the
+    epilogue warps).  `A_in_bounds` (not in the total) is the part of A inside the
+    tensor; A / A_in_bounds is the waste of ragged and halo tiles."""
     plan = plan or plan_of(w)
     per_cta = tiles_per_cta(plan["tiles"], num_sms)
     ctas = len(per_cta)
+    tiles = plan["tiles"]
     out: Dict[str, int] = {}
-    if isinstance(w, wl.GemmChain):
-        out["A"] = w.M * w.K0 * ELEM
-        w0, w1 = w.K0 * w.N0 * ELEM, w.N0 * w.N1 * ELEM
-        if plan["resident"]:
-            out["W0"], out["W1"] = ctas * w0, ctas * w1
-        else:
-            out["W0"] = plan["tiles"] * w0
-            loads_w1 = sum(-(-n // 2) for n in per_cta) if plan["w1_group"] else plan["tiles"]
-            out["W1"] = loads_w1 * w1
-        out["bias"] = ctas * (w.N0 + w.N1) * ELEM
-    elif isinstance(w, wl.ConvChain):
-        if w.R == 1 and w.S == 1 and w.pad == 0:   # runs as a GEMM over the pixels
-            out["A"] = w.N * w.H * w.W * w.C * ELEM
-        else:
-            out["A"] = _conv_tile_input_bytes(w.N, w.H, w.W, w.C, w.R, w.S, w.pad,
-                                              bool(plan["halo"]))
-        w0, w1 = w.C0 * w.R * w.S * w.C * ELEM, w.C1 * w.C0 * ELEM
-        if plan["resident"]:
-            out["W0"], out["W1"] = ctas * w0, ctas * w1
-        else:
-            out["W0"], out["W1"] = plan["tiles"] * w0, plan["tiles"] * w1
-        out["bias"] = ctas * (w.C0 + w.C1) * ELEM
+    R = getattr(w, "R", 3 if isinstance(w, wl.ConvPool) else 1)
+    a_tile = (plan["kchunks0"] // R * plan["a_stage_bytes"] if plan["halo"]
+              else plan["kchunks0"] * A_BOX)
+    out["A"] = tiles * a_tile
+    w0 = plan["kchunks0"] * plan["w0_chunk"]
+    w1 = plan["kchunks1"] * plan["w1_chunk"]
+    if plan["resident"]:
+        out["W0"] = ctas * w0
+        if w1:
+            out["W1"] = ctas * w1
     else:
-        out["A"] = _conv_tile_input_bytes(w.N, w.H, w.W, w.Cin, 3, 3, 1, bool(plan["halo"]))
-        wt = w.Cout * 9 * w.Cin * ELEM
-        out["W0"] = ctas * wt if plan["resident"] else plan["tiles"] * wt
+        out["W0"] = tiles * w0
+        if w1:
+            loads_w1 = sum(-(-n // 2) for n in per_cta) if plan["w1_group"] else tiles
+            out["W1"] = loads_w1 * w1
+    if isinstance(w, wl.GemmChain):
+        out["bias"] = ctas * (w.N0 + w.N1) * ELEM
+        useful = w.M * w.K0 * ELEM
+    elif isinstance(w, wl.ConvChain):
+        out["bias"] = ctas * (w.C0 + w.C1) * ELEM
+        useful = (w.N * w.H * w.W * w.C * ELEM if (w.R, w.S, w.pad) == (1, 1, 0) else
+                  _conv_tile_input_bytes(w.N, w.H, w.W, w.C, w.R, w.S, w.pad, bool(plan["halo"])))
+    else:
         out["bias"] = ctas * w.Cout * ELEM
+        useful = _conv_tile_input_bytes(w.N, w.H, w.W, w.Cin, 3, 3, 1, bool(plan["halo"]))
     out["total"] = sum(out.values())
+    out["A_in_bounds"] = useful
     return out
 
 
@@ -251,8 +261,8 @@ def report(ncu: Optional[Dict[str, str]] = None) -> str:
     captured launch per workload where an export is given (name -> csv path)."""
     ncu = ncu or {}
     lines = ["| workload | plan | DRAM unique MB | DRAM unfused MB | L2->SM model MB "
-             "| L2->SM ncu MB | model/ncu | smem model | smem planner |",
-             "|---|---|---|---|---|---|---|---|---|"]
+             "| A boxes / A in bounds | L2->SM ncu MB | model/ncu | smem model | smem planner |",
+             "|---|---|---|---|---|---|---|---|---|---|"]
     for name, w in wl.WORKLOADS.items():
         plan = plan_of(w)
         t = l2_to_smem_traffic(w, plan)
@@ -263,7 +273,8 @@ def report(ncu: Optional[Dict[str, str]] = None) -> str:
         t_total = t["total"]
         lines.append(
             f"| {name} | {desc} | {dram_traffic(w) / 1e6:.2f} | {dram_traffic(w, False) / 1e6:.2f} "
-            f"| {t['total'] / 1e6:.3f} | {'' if got is None else f'{got / 1e6:.3f}'} "
+            f"| {t['total'] / 1e6:.3f} | {t['A'] / t['A_in_bounds']:.3f} "
+            f"| {'' if got is None else f'{got / 1e6:.3f}'} "
             f"| {'' if not got else f'{t_total / got:.3f}'} "
             f"| {smem_footprint(plan) + 1024} | {plan['smem']} |")
     return "\n".join(lines)

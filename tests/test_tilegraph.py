@@ -49,6 +49,23 @@ def test_ffn_l2_traffic_by_hand():
     assert t["total"] == 16_777_216 + 33_554_432 + 9_961_472 + 116_736   # 60.41 MB
 
 
+def test_conv_boxes_are_moved_whole():
+    # conv3x3 -> 1x1 on 56 x 56 images: 32 x 7 x 4 tiles of 8 x 16 pixels (the fourth tile
+    # column is half outside the image), 3 halo boxes of 10 x 16 pixels x 64 channels each;
+    # resident filters once per CTA.  ncu's l1tex__m_xbar2l1tex_read_bytes.sum of one launch
+    # reads 68,805,632: out-of-bounds fill crosses the crossbar like data.
+    t = tg.l2_to_smem_traffic(wl.CONV3X3_1X1)
+    assert t["A"] == 896 * 3 * 10 * 16 * 64 * 2
+    assert t["W0"] == 152 * 9 * 64 * 64 * 2 and t["W1"] == 152 * 64 * 128 * 2
+    assert t["bias"] == 152 * (64 + 128) * 2
+    assert t["total"] == 68_805_632
+    assert t["A"] > t["A_in_bounds"]
+    # 112 x 112 images tile exactly; only the padding rows and columns are fill
+    p = tg.l2_to_smem_traffic(wl.CONV_POOL)
+    assert p["A"] == 32 * 14 * 7 * 3 * 10 * 16 * 64 * 2
+    assert p["A_in_bounds"] < p["A"] < 1.07 * p["A_in_bounds"]
+
+
 def test_conv_halo_boxes_read_less():
     # interior tiles of a 3x3 conv: halo loads move 3 boxes of 10 x 16 pixels, per-tap
     # loads 9 boxes of 8 x 16 pixels, per 64-channel block
@@ -106,4 +123,4 @@ def test_read_ncu_raw_csv(tmp_path):
     assert d["dram__bytes_read.sum"] == pytest.approx(17_074_430)
     assert d["launch__grid_size"] == 152 and "Kernel Name" not in d
     table = tg.report({"gemm_ffn": str(p)})
-    assert "| gemm_ffn |" in table and "60.410 | 60.410 | 1.000" in table
+    assert "| gemm_ffn |" in table and "60.410 | 1.000 | 60.410 | 1.000" in table
