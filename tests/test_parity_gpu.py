@@ -40,10 +40,14 @@ GEMM_SHAPES = [
     ("f16", 640, 128, 128, 256),
     ("f16", 200, 320, 96, 200),
     ("bf16", 384, 64, 256, 256),
-    # wide N0: the intermediate is kept in TMEM (checked by test_plan)
+    # wide N0: the intermediate is kept in TMEM (checked by test_plan), D1 after P or,
+    # for N1 > N0 / 2, past the end of D0
     ("f16", 300, 128, 256, 64),
     ("bf16", 257, 72, 200, 72),
     ("f16", 1000, 64, 224, 96),
+    ("f16", 300, 128, 160, 128),
+    ("bf16", 257, 72, 200, 120),
+    ("f16", 640, 128, 144, 96),
 ]
 
 
