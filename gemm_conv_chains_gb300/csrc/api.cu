@@ -11,8 +11,10 @@
 #include <cstdint>
 #include <cstring>
 #include <initializer_list>
+#include <map>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "b2b.h"
 #include "ptx.cuh"
@@ -176,6 +178,7 @@ inline bool valid_epi(int e) {
 // Byte sizes of the shared-memory regions of one launch (for the plan and its checks).
 struct Regions {
   uint32_t ring, w_res, p_each, out_each, bias, bar;
+  int32_t cand = 0, ncand = 0;   // the layout taken, as an index into the feasible ones
 };
 
 // TMEM columns of the accumulators.  Chain: nbuf D0 buffers of round_up(N0p, 32) columns,
@@ -209,11 +212,13 @@ uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = fals
 }
 
 // Shared-memory plan: ring of A (and, when streamed, weight) chunks; resident weights;
-// P tiles; output staging; bias operands; barriers.  Candidates are tried in order of
-// preference -- two tiles in flight, resident weights, separate staging -- and the first
-// that leaves at least three ring stages (else two) is taken.  Fills p's layout fields.
+// P tiles; output staging; bias operands; barriers.  The candidates that leave at least two
+// ring stages are feasible, in order of preference -- more tiles in flight, resident
+// weights, separate staging.  By default the first feasible one with three or more stages
+// is taken (else the first feasible one); `forced` >= 0 takes that feasible candidate
+// instead.  Fills p's layout fields.
 bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_bytes,
-               Regions* regions) {
+               Regions* regions, int forced = -1) {
   const uint32_t budget = kSmemLimit - 1024u;   // 1 KiB slack to align the base to 1024
   const uint32_t n0blk = static_cast<uint32_t>((p.N0p + 63) / 64);
   const uint32_t n1blk = static_cast<uint32_t>((p.N1p + 63) / 64);
@@ -259,9 +264,10 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
       for (int groups = 2; groups >= gmin; --groups) cands[ncand++] = {2, groups, resident, 0, 0};
   }
 
-  int chosen = -1;
-  uint32_t chosen_stages = 0, chosen_stage_bytes = 0;
-  for (int min_stages = 3; min_stages >= 2 && chosen < 0; --min_stages) {
+  int feas[16];
+  uint32_t feas_stages[16], feas_stage_bytes[16];
+  int nfeas = 0;
+  {
     for (int c = 0; c < ncand; ++c) {
       const Cand& k = cands[c];
       // Resident filters of an R > 1 conv: one halo box of (8 + R - 1) x 16 pixels per
@@ -278,14 +284,23 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
       const uint32_t fixed = (k.resident ? w_res : 0u) + shared + bias_bytes + bar_bytes;
       if (fixed >= budget) continue;
       const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / stage_bytes);
-      if (stages < static_cast<uint32_t>(min_stages)) continue;
-      chosen = c;
-      chosen_stages = stages;
-      chosen_stage_bytes = stage_bytes;
-      break;
+      if (stages < 2u) continue;
+      feas[nfeas] = c;
+      feas_stages[nfeas] = stages;
+      feas_stage_bytes[nfeas++] = stage_bytes;
     }
   }
-  if (chosen < 0) return false;
+  int pick = -1;
+  if (forced >= 0) {
+    pick = forced < nfeas ? forced : -1;
+  } else {
+    for (int i = 0; i < nfeas && pick < 0; ++i)
+      if (feas_stages[i] >= 3u) pick = i;
+    if (pick < 0 && nfeas > 0) pick = 0;
+  }
+  if (pick < 0) return false;
+  const int chosen = feas[pick];
+  const uint32_t chosen_stages = feas_stages[pick], chosen_stage_bytes = feas_stage_bytes[pick];
   const Cand& k = cands[chosen];
   p.acc_dual = k.dual >= 2 ? 1 : 0;
   p.nbuf_log2 = mode != MODE_CHAIN ? 1 : (k.dual == 4 ? 2 : (k.dual == 2 ? 1 : 0));
@@ -312,6 +327,8 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
     }
   }
   Regions r;
+  r.cand = pick;
+  r.ncand = nfeas;
   r.ring = p.num_stages * p.stage_bytes;
   r.w_res = p.resident ? w_res : 0u;
   const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? static_cast<uint32_t>(k.dual) : 0u;
@@ -360,7 +377,7 @@ void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const v
 
 b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtensorMap& w0,
                   const CUtensorMap& w1, const CUtensorMap& out, ChainParams& p, size_t smem,
-                  void* stream) {
+                  int grid, void* stream) {
   const uint32_t bit = 1u << (2u * static_cast<uint32_t>(v) + (p.is_bf16 ? 1u : 0u));
   if ((d->attr_done.load() & bit) == 0u) {
     if (cudaFuncSetAttribute(variant_func(v, p.is_bf16 != 0),
@@ -371,7 +388,6 @@ b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtenso
     }
     d->attr_done.fetch_or(bit);
   }
-  const int grid = std::max(1, std::min(p.num_tiles, d->num_sms));
   const cudaError_t e =
       launch_variant(v, a, w0, w1, out, p, grid, smem, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
@@ -386,7 +402,7 @@ b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtenso
 // ------------------------------------------------------------------------------------
 // 2-D A operand.  W0/W1 are [K][N] row-major when w_mn, else [N][K] (conv filters).
 bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int32_t N0,
-                 int32_t N1, size_t* smem, Regions* regions) {
+                 int32_t N1, size_t* smem, Regions* regions, int forced = -1) {
   std::memset(&p, 0, sizeof(p));
   p.M = static_cast<int32_t>(M);
   p.K0 = K0;
@@ -398,13 +414,13 @@ bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int
   p.kc_per_tap = p.kchunks0;
   p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
   p.num_tiles = ceil_div(M, kBlockM);
-  return plan_smem(p, mode, w_mn, w_mn, smem, regions);
+  return plan_smem(p, mode, w_mn, w_mn, smem, regions, forced);
 }
 
 // 4-D implicit-GEMM A operand (conv filters [Cout][R][S][Cin]).
 bool conv_params(ChainParams& p, int mode, int32_t N, int32_t H, int32_t W, int32_t C,
                  int32_t C0, int32_t R, int32_t S, int32_t pad, int32_t C1, size_t* smem,
-                 Regions* regions) {
+                 Regions* regions, int forced = -1) {
   std::memset(&p, 0, sizeof(p));
   p.K0 = C;
   p.N0 = C0;
@@ -424,22 +440,62 @@ bool conv_params(ChainParams& p, int mode, int32_t N, int32_t H, int32_t W, int3
   const int64_t tiles = static_cast<int64_t>(N) * p.tiles_w * p.tiles_h;
   if (tiles > INT32_MAX) return false;
   p.num_tiles = static_cast<int32_t>(tiles);
-  return plan_smem(p, mode, false, false, smem, regions);
+  return plan_smem(p, mode, false, false, smem, regions, forced);
+}
+
+// ------------------------------------------------------------------------------------
+// launch choices
+// ------------------------------------------------------------------------------------
+// What a launch of one problem may vary without changing its results (the same MMAs in
+// the same order, the same roundings): the shared-memory / TMEM layout (an index into the
+// planner's feasible candidates), the grid (0: one CTA per SM, or per tile if fewer;
+// 1: the fewest CTAs that keep the busiest CTA's tile count) and whether each CTA's
+// second tile's A rows are prefetched into L2 at the start.  -1 leaves a field to the
+// planner's default.
+struct Choice {
+  int32_t cand = -1, grid = -1, pf2 = -1;
+};
+
+// What one launch looked like, for the profiler's enumeration.
+struct Info {
+  int32_t ncand = 0, grid_full = 0, grid_balanced = 0, tiles = 0, can_prefetch = 0;
+};
+
+int grid_for(int32_t tiles, int sms, int32_t mode) {
+  const int full = std::max(1, std::min<int>(tiles, sms));
+  if (mode != 1) return full;
+  const int per = (tiles + full - 1) / full;
+  return std::max(1, (tiles + per - 1) / per);
+}
+
+// Default: prefetch the second tile too when a CTA has more than two tiles -- then the
+// rolling prefetch (two tiles ahead) starts from the third; with one or two tiles per
+// CTA the second tile's prefetch competed with the first tile's loads (measured on the
+// FFN-shaped chain: 1 % slower with it).
+int32_t pf_second_for(int32_t tiles, int grid, int32_t pf2) {
+  if (pf2 >= 0) return pf2 != 0 ? 1 : 0;
+  return (tiles + grid - 1) / grid > 2 ? 1 : 0;
 }
 
 // ------------------------------------------------------------------------------------
 // GEMM-shaped entry points (2-D A operand)
 // ------------------------------------------------------------------------------------
-b2b_status run_gemm(int mode, bool w_mn, int dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
-                    const void* A, const void* W0, const void* b0, int e0, const void* W1,
-                    const void* b1, int e1, void* D, void* stream, uint32_t kid) {
+b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int dt, int64_t M,
+                         int32_t K0, int32_t N0, int32_t N1, const void* A, const void* W0,
+                         const void* b0, int e0, const void* W1, const void* b1, int e1, void* D,
+                         void* stream, uint32_t kid) {
   ChainParams p;
   size_t smem = 0;
-  if (!gemm_params(p, mode, w_mn, M, K0, N0, N1, &smem, nullptr)) return B2B_ERR_UNSUPPORTED;
+  Regions r;
+  if (!gemm_params(p, mode, w_mn, M, K0, N0, N1, &smem, &r, ch.cand)) return B2B_ERR_UNSUPPORTED;
   b2b_status st = B2B_OK;
   DeviceState* d = device_state(&st);
   if (d == nullptr) return st;
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
+  const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
+  p.pf_second = pf_second_for(p.num_tiles, grid, ch.pf2);
+  if (info) *info = {r.ncand, grid_for(p.num_tiles, d->num_sms, 0),
+                     grid_for(p.num_tiles, d->num_sms, 1), p.num_tiles, 1};
 
   CUtensorMap ta, tw0, tw1, to;
   const uint64_t e = 2;
@@ -491,24 +547,30 @@ b2b_status run_gemm(int mode, bool w_mn, int dt, int64_t M, int32_t K0, int32_t 
   Variant v;
   if (mode == MODE_CHAIN) v = w_mn ? V_GEMM_CHAIN : V_CONV1X1_CHAIN;
   else v = w_mn ? V_GEMM_SINGLE : V_CONV1X1_SINGLE;
-  return launch(v, d, ta, tw0, tw1, to, p, smem, stream);
+  return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
 }
 
 // ------------------------------------------------------------------------------------
 // conv-shaped entry points (4-D implicit-GEMM A operand)
 // ------------------------------------------------------------------------------------
-b2b_status run_conv(int mode, int dt, int32_t N, int32_t H, int32_t W, int32_t C, const void* x,
-                    const void* W0, int32_t C0, int32_t R, int32_t S, int32_t pad, const void* b0,
-                    int e0, const void* W1, int32_t C1, const void* b1, int e1, void* y,
-                    void* stream, uint32_t kid) {
+b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t N, int32_t H,
+                         int32_t W, int32_t C, const void* x, const void* W0, int32_t C0,
+                         int32_t R, int32_t S, int32_t pad, const void* b0, int e0,
+                         const void* W1, int32_t C1, const void* b1, int e1, void* y,
+                         void* stream, uint32_t kid) {
   ChainParams p;
   size_t smem = 0;
-  if (!conv_params(p, mode, N, H, W, C, C0, R, S, pad, C1, &smem, nullptr))
+  Regions r;
+  if (!conv_params(p, mode, N, H, W, C, C0, R, S, pad, C1, &smem, &r, ch.cand))
     return B2B_ERR_UNSUPPORTED;
   b2b_status st = B2B_OK;
   DeviceState* d = device_state(&st);
   if (d == nullptr) return st;
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
+  const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
+  p.pf_second = 0;   // the implicit-GEMM A has no per-tile contiguous range to prefetch
+  if (info) *info = {r.ncand, grid_for(p.num_tiles, d->num_sms, 0),
+                     grid_for(p.num_tiles, d->num_sms, 1), p.num_tiles, 0};
   const int32_t Ho = p.Ho, Wo = p.Wo;
 
   const uint64_t e = 2;
@@ -548,7 +610,143 @@ b2b_status run_conv(int mode, int dt, int32_t N, int32_t H, int32_t W, int32_t C
   p.pf_w1 = static_cast<const uint8_t*>(W1);
   p.pf_w1_bytes = mode == MODE_CHAIN ? static_cast<uint32_t>(static_cast<uint64_t>(C1) * C0 * e) : 0u;
   const Variant v = mode == MODE_CHAIN ? V_CONV_CHAIN : mode == MODE_SINGLE ? V_CONV_SINGLE : V_CONV_POOL;
-  return launch(v, d, ta, tw0, tw1, to, p, smem, stream);
+  return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
+}
+
+// ------------------------------------------------------------------------------------
+// light-weight profiler (BOLT notes, "Light-weight performance profiler": a search over
+// launch parameters by timing): per problem, time every launch choice once, keep the fastest
+// ------------------------------------------------------------------------------------
+// Problems are keyed by the entry point and its sizes, as b2b_debug_plan takes them.
+using TuneKey = std::vector<int64_t>;
+
+struct Tuned {
+  Choice c;
+  int32_t source = 0;   // 1 pinned by b2b_set_choice, 2 measured
+  uint32_t best_ns = 0, default_ns = 0, timed = 0;
+};
+
+std::mutex g_tune_mu;
+std::map<TuneKey, Tuned> g_tuned;
+std::atomic<int> g_autotune{0};
+// Per choice: kTuneWarm untimed launches, then kTuneRounds rounds of kTuneReps launches;
+// a choice's time is its fastest round.  Another choice replaces the default only when
+// it is faster by more than kTuneMargin (timing noise must not pick a layout).
+constexpr int kTuneWarm = 2, kTuneReps = 10, kTuneRounds = 3;
+constexpr float kTuneMargin = 0.02f;
+
+bool find_choice(const TuneKey& key, Choice* c) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  const auto it = g_tuned.find(key);
+  if (it == g_tuned.end()) return false;
+  *c = it->second.c;
+  return true;
+}
+
+// Times `go(choice)` for the default and for every layout x grid x prefetch choice that
+// differs from it in effect, on the caller's stream (which it synchronises), records the
+// fastest and launches it for the caller.
+template <class Go>
+b2b_status tune(const TuneKey& key, void* stream, Go&& go) {
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Info info;
+  b2b_status st = go(Choice{}, &info);
+  if (st != B2B_OK) return st;
+  cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+  if (cudaEventCreate(&ev0) != cudaSuccess || cudaEventCreate(&ev1) != cudaSuccess) {
+    cudaGetLastError();
+    if (ev0) cudaEventDestroy(ev0);
+    return B2B_ERR_CUDA;
+  }
+  auto time_of = [&](const Choice& c, float* us) -> b2b_status {
+    for (int i = 0; i < kTuneWarm; ++i)
+      if (b2b_status e = go(c, nullptr); e != B2B_OK) return e;
+    for (int round = 0; round < kTuneRounds; ++round) {
+      if (cudaEventRecord(ev0, s) != cudaSuccess) return B2B_ERR_CUDA;
+      for (int i = 0; i < kTuneReps; ++i)
+        if (b2b_status e = go(c, nullptr); e != B2B_OK) return e;
+      float ms = 0.f;
+      if (cudaEventRecord(ev1, s) != cudaSuccess || cudaEventSynchronize(ev1) != cudaSuccess ||
+          cudaEventElapsedTime(&ms, ev0, ev1) != cudaSuccess)
+        return B2B_ERR_CUDA;
+      const float t = ms * 1000.f / kTuneReps;
+      if (round == 0 || t < *us) *us = t;
+    }
+    return B2B_OK;
+  };
+  float def_us = 0.f, best_us = 0.f;
+  Choice best;
+  uint32_t timed = 0;
+  st = time_of(Choice{}, &def_us);
+  if (st == B2B_OK) {
+    best_us = def_us;
+    timed = 1;
+    const int grids = info.grid_balanced != info.grid_full ? 2 : 1;
+    const int pfs = (info.can_prefetch && info.tiles > info.grid_balanced) ? 2 : 1;
+    for (int32_t cand = 0; cand < info.ncand && st == B2B_OK; ++cand)
+      for (int32_t grid = 0; grid < grids && st == B2B_OK; ++grid)
+        for (int32_t pf = 0; pf < pfs && st == B2B_OK; ++pf) {
+          const Choice c{cand, grid, pfs == 2 ? pf : 0};
+          float us = 0.f;
+          st = time_of(c, &us);
+          if (st == B2B_OK) {
+            ++timed;
+            if (us < best_us && us < def_us * (1.f - kTuneMargin)) {
+              best = c;
+              best_us = us;
+            }
+          }
+        }
+  }
+  if (st == B2B_ERR_CUDA) cudaGetLastError();
+  cudaEventDestroy(ev0);
+  cudaEventDestroy(ev1);
+  if (st != B2B_OK) return st;
+  {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    Tuned& t = g_tuned[key];
+    t.c = best;
+    t.source = 2;
+    t.best_ns = static_cast<uint32_t>(best_us * 1000.f);
+    t.default_ns = static_cast<uint32_t>(def_us * 1000.f);
+    t.timed = timed;
+  }
+  return go(best, nullptr);
+}
+
+// The launch choice of a problem: pinned or measured before, else (with the profiler on,
+// outside stream capture) measured now, else the planner's default.
+template <class Go>
+b2b_status dispatch(const TuneKey& key, void* stream, Go&& go) {
+  Choice c;
+  if (find_choice(key, &c)) return go(c, nullptr);
+  if (g_autotune.load() == 0) return go(Choice{}, nullptr);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return go(Choice{}, nullptr);
+  return tune(key, stream, go);
+}
+
+b2b_status run_gemm(const TuneKey& key, int mode, bool w_mn, int dt, int64_t M, int32_t K0,
+                    int32_t N0, int32_t N1, const void* A, const void* W0, const void* b0, int e0,
+                    const void* W1, const void* b1, int e1, void* D, void* stream, uint32_t kid) {
+  return dispatch(key, stream, [&](const Choice& c, Info* info) {
+    return run_gemm_with(c, info, mode, w_mn, dt, M, K0, N0, N1, A, W0, b0, e0, W1, b1, e1, D,
+                         stream, kid);
+  });
+}
+
+b2b_status run_conv(const TuneKey& key, int mode, int dt, int32_t N, int32_t H, int32_t W,
+                    int32_t C, const void* x, const void* W0, int32_t C0, int32_t R, int32_t S,
+                    int32_t pad, const void* b0, int e0, const void* W1, int32_t C1,
+                    const void* b1, int e1, void* y, void* stream, uint32_t kid) {
+  return dispatch(key, stream, [&](const Choice& c, Info* info) {
+    return run_conv_with(c, info, mode, dt, N, H, W, C, x, W0, C0, R, S, pad, b0, e0, W1, C1, b1,
+                         e1, y, stream, kid);
+  });
 }
 
 // Shared checks of a channel-like size: multiple of 8 (16 bytes), within [8, hi].
@@ -582,8 +780,8 @@ b2b_status b2b_gemm(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
   if (!A || !W0 || !W1 || !D) return B2B_ERR_NULL;
   if (!aligned16(A) || !aligned16(W0) || !aligned16(W1) || !aligned16(D)) return B2B_ERR_ALIGN;
   if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1))) return B2B_ERR_ALIGN;
-  return run_gemm(MODE_CHAIN, true, dt, M, K0, N0, N1, A, W0, b0, e0, W1, b1, e1, D, stream,
-                  KID_GEMM_CHAIN);
+  return run_gemm({0, M, K0, N0, N1}, MODE_CHAIN, true, dt, M, K0, N0, N1, A, W0, b0, e0, W1, b1,
+                  e1, D, stream, KID_GEMM_CHAIN);
 }
 
 b2b_status gemm_bias_act(b2b_dtype dt, int64_t M, int32_t K, int32_t N, const void* A,
@@ -598,8 +796,8 @@ b2b_status gemm_bias_act(b2b_dtype dt, int64_t M, int32_t K, int32_t N, const vo
   if (!A || !W || !D) return B2B_ERR_NULL;
   if (!aligned16(A) || !aligned16(W) || !aligned16(D)) return B2B_ERR_ALIGN;
   if (b && !aligned2(b)) return B2B_ERR_ALIGN;
-  return run_gemm(MODE_SINGLE, true, dt, M, K, N, 0, A, W, b, e, nullptr, nullptr, 0, D, stream,
-                  KID_GEMM_SINGLE);
+  return run_gemm({1, M, K, N}, MODE_SINGLE, true, dt, M, K, N, 0, A, W, b, e, nullptr, nullptr, 0,
+                  D, stream, KID_GEMM_SINGLE);
 }
 
 static b2b_status check_conv_args(int32_t N, int32_t H, int32_t W, int32_t C, int32_t Co,
@@ -635,11 +833,11 @@ b2b_status b2b_conv_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t 
     // optimisation", item 5): run the GEMM-shaped kernel with K-major filters.
     const int64_t M = static_cast<int64_t>(N) * H * W;
     if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
-    return run_gemm(MODE_CHAIN, false, dt, M, C, C0, C1, x, W0, b0, e0, W1, b1, e1, y, stream,
-                    KID_CONV1X1_CHAIN);
+    return run_gemm({2, N, H, W, C, C0, R, S, pad, C1}, MODE_CHAIN, false, dt, M, C, C0, C1, x, W0,
+                    b0, e0, W1, b1, e1, y, stream, KID_CONV1X1_CHAIN);
   }
-  return run_conv(MODE_CHAIN, dt, N, H, W, C, x, W0, C0, R, S, pad, b0, e0, W1, C1, b1, e1, y,
-                  stream, KID_CONV_CHAIN);
+  return run_conv({2, N, H, W, C, C0, R, S, pad, C1}, MODE_CHAIN, dt, N, H, W, C, x, W0, C0, R, S,
+                  pad, b0, e0, W1, C1, b1, e1, y, stream, KID_CONV_CHAIN);
 }
 
 b2b_status conv_bias_act_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
@@ -655,11 +853,11 @@ b2b_status conv_bias_act_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int
   if (R == 1 && S == 1 && pad == 0) {
     const int64_t M = static_cast<int64_t>(N) * H * W;
     if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
-    return run_gemm(MODE_SINGLE, false, dt, M, C, Co, 0, x, Wt, b, e, nullptr, nullptr, 0, y,
-                    stream, KID_CONV1X1_SINGLE);
+    return run_gemm({3, N, H, W, C, Co, R, S, pad}, MODE_SINGLE, false, dt, M, C, Co, 0, x, Wt, b,
+                    e, nullptr, nullptr, 0, y, stream, KID_CONV1X1_SINGLE);
   }
-  return run_conv(MODE_SINGLE, dt, N, H, W, C, x, Wt, Co, R, S, pad, b, e, nullptr, 0, nullptr, 0,
-                  y, stream, KID_CONV_SINGLE);
+  return run_conv({3, N, H, W, C, Co, R, S, pad}, MODE_SINGLE, dt, N, H, W, C, x, Wt, Co, R, S,
+                  pad, b, e, nullptr, 0, nullptr, 0, y, stream, KID_CONV_SINGLE);
 }
 
 b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t Cin,
@@ -674,8 +872,8 @@ b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int3
   if (!x || !Wt || !y) return B2B_ERR_NULL;
   if (!aligned16(x) || !aligned16(Wt) || !aligned16(y)) return B2B_ERR_ALIGN;
   if (b && !aligned2(b)) return B2B_ERR_ALIGN;
-  return run_conv(MODE_POOL, dt, N, H, W, Cin, x, Wt, Cout, 3, 3, 1, b, B2B_EPI_RELU, nullptr, 0,
-                  nullptr, 0, y, stream, KID_CONV_POOL);
+  return run_conv({4, N, H, W, Cin, Cout}, MODE_POOL, dt, N, H, W, Cin, x, Wt, Cout, 3, 3, 1, b,
+                  B2B_EPI_RELU, nullptr, 0, nullptr, 0, y, stream, KID_CONV_POOL);
 }
 
 b2b_status maxpool2x2_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
@@ -750,34 +948,45 @@ b2b_status b2b_get_device_error(uint32_t info[4]) {
   return w[0] == ERR_CODE_TIMEOUT ? B2B_ERR_TIMEOUT : B2B_ERR_CUDA;
 }
 
-b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,
-                          int32_t out_len) {
-  static const int32_t need[5] = {4, 3, 9, 8, 5};
+// Sizes an entry point takes, per kind (b2b_debug_plan's numbering).
+static const int32_t kPlanDims[5] = {4, 3, 9, 8, 5};
+
+static b2b_status check_plan_args(int32_t kind, const int64_t* dims, int32_t ndims) {
   if (kind < 0 || kind > 4) return B2B_ERR_UNSUPPORTED;
-  if (dims == nullptr || out == nullptr) return B2B_ERR_NULL;
-  if (ndims < need[kind] || out_len < 47) return B2B_ERR_SHAPE;
-  for (int i = 0; i < need[kind]; ++i)
+  if (dims == nullptr) return B2B_ERR_NULL;
+  if (ndims < kPlanDims[kind]) return B2B_ERR_SHAPE;
+  for (int i = 0; i < kPlanDims[kind]; ++i)
     if (dims[i] < 0 || dims[i] > INT32_MAX) return B2B_ERR_SHAPE;
+  return B2B_OK;
+}
+
+static TuneKey plan_key(int32_t kind, const int64_t* dims) {
+  TuneKey k{kind};
+  k.insert(k.end(), dims, dims + kPlanDims[kind]);
+  return k;
+}
+
+// The launch plan entry point `kind` makes for `dims` with layout candidate `forced`
+// (-1: the planner's default); validated like the entry point itself.
+static b2b_status plan_for_kind(int32_t kind, const int64_t* dims, int forced, ChainParams& p,
+                                Regions& r, size_t& smem, int32_t& mode) {
   const int32_t d0 = static_cast<int32_t>(dims[0]), d1 = static_cast<int32_t>(dims[1]),
                 d2 = static_cast<int32_t>(dims[2]), d3 = static_cast<int32_t>(dims[3]);
-  ChainParams p;
-  Regions r;
-  size_t smem = 0;
   bool ok = false;
   b2b_status st = B2B_OK;
-  int32_t mode = MODE_CHAIN;
+  mode = MODE_CHAIN;
   switch (kind) {
     case 0:   // b2b_gemm: M, K0, N0, N1
       if ((st = check_channels(d1, kMaxReduction)) != B2B_OK) return st;
       if ((st = check_channels(d2, 256)) != B2B_OK) return st;
       if ((st = check_channels(d3, 256)) != B2B_OK) return st;
-      ok = gemm_params(p, MODE_CHAIN, true, dims[0], d1, d2, d3, &smem, &r);
+      ok = gemm_params(p, MODE_CHAIN, true, dims[0], d1, d2, d3, &smem, &r, forced);
       break;
     case 1:   // gemm_bias_act: M, K, N
       if ((st = check_channels(d1, kMaxReduction)) != B2B_OK) return st;
       if ((st = check_channels(d2, 256)) != B2B_OK) return st;
       mode = MODE_SINGLE;
-      ok = gemm_params(p, MODE_SINGLE, true, dims[0], d1, d2, 0, &smem, &r);
+      ok = gemm_params(p, MODE_SINGLE, true, dims[0], d1, d2, 0, &smem, &r, forced);
       break;
     case 2:
     case 3: {  // b2b_conv_nhwc: N,H,W,C,C0,R,S,pad[,C1]; conv_bias_act_nhwc: N,H,W,C,Co,R,S,pad
@@ -788,9 +997,10 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
       if (kind == 2 && (st = check_channels(C1, 256)) != B2B_OK) return st;
       mode = kind == 2 ? MODE_CHAIN : MODE_SINGLE;
       if (R == 1 && S == 1 && pad == 0)
-        ok = gemm_params(p, mode, false, static_cast<int64_t>(d0) * d1 * d2, d3, C0, C1, &smem, &r);
+        ok = gemm_params(p, mode, false, static_cast<int64_t>(d0) * d1 * d2, d3, C0, C1, &smem, &r,
+                         forced);
       else
-        ok = conv_params(p, mode, d0, d1, d2, d3, C0, R, S, pad, C1, &smem, &r);
+        ok = conv_params(p, mode, d0, d1, d2, d3, C0, R, S, pad, C1, &smem, &r, forced);
       break;
     }
     case 4: { // conv_relu_maxpool: N, H, W, Cin, Cout
@@ -798,12 +1008,27 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
       if (d0 > 0 && (d1 < 2 || d2 < 2)) return B2B_ERR_SHAPE;
       if ((st = check_conv_args(d0, d1, d2, d3, Cout, 3, 3, 1)) != B2B_OK) return st;
       mode = MODE_POOL;
-      ok = conv_params(p, MODE_POOL, d0, d1, d2, d3, Cout, 3, 3, 1, 0, &smem, &r);
+      ok = conv_params(p, MODE_POOL, d0, d1, d2, d3, Cout, 3, 3, 1, 0, &smem, &r, forced);
       break;
     }
   }
-  if (!ok) return B2B_ERR_UNSUPPORTED;
-  const uint32_t v[47] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  return ok ? B2B_OK : B2B_ERR_UNSUPPORTED;
+}
+
+b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,
+                          int32_t out_len) {
+  b2b_status st = check_plan_args(kind, dims, ndims);
+  if (st != B2B_OK) return st;
+  if (out == nullptr) return B2B_ERR_NULL;
+  if (out_len < 51) return B2B_ERR_SHAPE;
+  Choice c;
+  find_choice(plan_key(kind, dims), &c);
+  ChainParams p;
+  Regions r;
+  size_t smem = 0;
+  int32_t mode = MODE_CHAIN;
+  if ((st = plan_for_kind(kind, dims, c.cand, p, r, smem, mode)) != B2B_OK) return st;
+  const uint32_t v[51] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -816,9 +1041,55 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           static_cast<uint32_t>(p.p_tmem), static_cast<uint32_t>(p.w1_group),
                           p.w1_per_stage, static_cast<uint32_t>(p.halo), p.a_stage_bytes,
                           1u << p.nbuf_log2, p.off_p[2], p.off_p[3], p.d0_col[2], p.d0_col[3],
-                          p.d1_col[2], p.d1_col[3]};
+                          p.d1_col[2], p.d1_col[3], static_cast<uint32_t>(r.cand),
+                          static_cast<uint32_t>(r.ncand), static_cast<uint32_t>(c.grid),
+                          static_cast<uint32_t>(c.pf2)};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
+}
+
+b2b_status b2b_set_choice(int32_t kind, const int64_t* dims, int32_t ndims, int32_t cand,
+                          int32_t grid, int32_t prefetch_second) {
+  b2b_status st = check_plan_args(kind, dims, ndims);
+  if (st != B2B_OK) return st;
+  if (cand < -1 || grid < -1 || grid > 1 || prefetch_second < -1 || prefetch_second > 1)
+    return B2B_ERR_SHAPE;
+  ChainParams p;
+  Regions r;
+  size_t smem = 0;
+  int32_t mode = MODE_CHAIN;
+  if ((st = plan_for_kind(kind, dims, cand, p, r, smem, mode)) != B2B_OK) return st;
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  Tuned& t = g_tuned[plan_key(kind, dims)];
+  t = Tuned{};
+  t.c = Choice{cand, grid, prefetch_second};
+  t.source = 1;
+  return B2B_OK;
+}
+
+b2b_status b2b_get_choice(int32_t kind, const int64_t* dims, int32_t ndims, int32_t* out,
+                          int32_t out_len) {
+  b2b_status st = check_plan_args(kind, dims, ndims);
+  if (st != B2B_OK) return st;
+  if (out == nullptr) return B2B_ERR_NULL;
+  if (out_len < 7) return B2B_ERR_SHAPE;
+  Tuned t;
+  {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    const auto it = g_tuned.find(plan_key(kind, dims));
+    if (it != g_tuned.end()) t = it->second;
+  }
+  const int32_t v[7] = {t.source, t.c.cand, t.c.grid, t.c.pf2, static_cast<int32_t>(t.best_ns),
+                        static_cast<int32_t>(t.default_ns), static_cast<int32_t>(t.timed)};
+  std::memcpy(out, v, sizeof(v));
+  return B2B_OK;
+}
+
+void b2b_set_autotune(int32_t on) { g_autotune.store(on != 0 ? 1 : 0); }
+
+void b2b_autotune_reset(void) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tuned.clear();
 }
 
 b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream) {

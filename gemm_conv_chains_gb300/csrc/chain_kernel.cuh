@@ -272,8 +272,9 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
       if (!p.resident)
         load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, k, fb, pol_keep);
       if (A4D && p.halo) k.next_halo(p); else k.next(p);
-      // Tile it + 2's A into L2 behind this tile's first chunk (tiles 0 and 1 were
-      // prefetched at the start), so that HBM stays busy ahead of the ring.
+      // Tile it + 2's A into L2 behind this tile's first chunk (tile 0, and tile 1 when
+      // the CTA has more tiles, were prefetched at the start), so that HBM stays busy
+      // ahead of the ring.
       if (kc == 0 && lead) prefetch_a_tile(p, t + 2 * static_cast<int32_t>(gridDim.x));
       trace(EV_PROD_ISSUED, kc, it);
       advance();
@@ -396,7 +397,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const uint32_t idesc1 = idesc_f16_f32(BF16 ? 1u : 0u, W1MN ? 1u : 0u, kBlockM, p.N1p);
   bool ok = true;
   const uint32_t lead = elect_one();
-  Tracer trace(p, 1, lead, 1);   // slot 0: the kernel's entry event
+  Tracer trace(p, 1, lead, 3);   // slots 0..2: the kernel's entry, setup and dependency events
   if (p.resident)
     ok = warp_mbar_wait(bars + 8u * BAR_WFULL, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
   bool bias_ready = false;   // the epilogue warps write the bias operands at the start
@@ -1050,15 +1051,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  ktrace(EV_SETUP_DONE, 0, 0);
 
   // Global memory is touched only after the previous kernel of the stream has completed
   // (inputs may be its outputs, outputs its inputs); the setup above overlaps its tail.
   if (warp == 0) {
-    // The first two tiles' A and (from one CTA) the weights into L2 while the previous
-    // kernel finishes.
+    // The first tile's A (and, if the plan asks, the second's) and (from one CTA) the
+    // weights into L2 while the previous kernel finishes.
     if (lane == 0) {
       prefetch_a_tile(p, blockIdx.x);
-      prefetch_a_tile(p, blockIdx.x + gridDim.x);
+      if (p.pf_second) prefetch_a_tile(p, blockIdx.x + gridDim.x);
       if (blockIdx.x == 0) {
         bulk_prefetch_l2(p.pf_w0, p.pf_w0_bytes);
         if (MODE == MODE_CHAIN) bulk_prefetch_l2(p.pf_w1, p.pf_w1_bytes);
@@ -1070,6 +1072,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     grid_dependency_wait();   // so that no bounded wait below runs while it is pending
+    ktrace(EV_DEP_READY, 0, 0);
     mma_role<MODE, A4D, W0MN, W1MN, BF16>(p, base, bars, tmem_base, abort_flag);
     __syncwarp();
   } else {

@@ -58,6 +58,8 @@ enum TraceEvent : uint32_t {
   EV_MMA_W1_FULL = 16,     // MMA issuer saw a streamed GEMM1 weight chunk land
   EV_KERNEL_ENTRY = 17,    // first instruction of the CTA
   EV_EPI_DRAINED = 18,     // epilogue group's elected thread finished its output drain
+  EV_SETUP_DONE = 19,      // barriers initialised and TMEM allocated (after __syncthreads)
+  EV_DEP_READY = 20,       // the MMA warp's wait for the previous grid returned
 };
 
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M
@@ -101,6 +103,7 @@ struct ChainParams {
   const uint8_t* pf_a;
   uint64_t pf_a_bytes;
   uint32_t pf_a_tile_bytes;
+  int32_t pf_second;    // 1: the CTA's second tile's A rows too, at the start
   const uint8_t* pf_w0;
   const uint8_t* pf_w1;
   uint32_t pf_w0_bytes, pf_w1_bytes;

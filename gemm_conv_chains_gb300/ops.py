@@ -69,6 +69,15 @@ def lib() -> ctypes.CDLL:
         L.b2b_probe_timeout.argtypes = [u64, vp]
         L.b2b_set_trace.argtypes = [vp, ctypes.c_uint32, ctypes.c_uint32]
         L.b2b_set_trace.restype = ci
+        p64 = ctypes.POINTER(i64)
+        L.b2b_set_autotune.argtypes = [i32]
+        L.b2b_set_autotune.restype = None
+        L.b2b_autotune_reset.argtypes = []
+        L.b2b_autotune_reset.restype = None
+        L.b2b_set_choice.argtypes = [i32, p64, i32, i32, i32, i32]
+        L.b2b_set_choice.restype = ci
+        L.b2b_get_choice.argtypes = [i32, p64, i32, ctypes.POINTER(i32), i32]
+        L.b2b_get_choice.restype = ci
         _lib = L
         return L
 
@@ -254,7 +263,8 @@ PLAN_FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring",
                "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0",
                "kchunks1", "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo",
                "a_stage_bytes", "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2",
-               "d1_col3"]
+               "d1_col3", "cand", "ncand", "grid_choice", "pf_choice"]
+_SIGNED_PLAN_FIELDS = ("grid_choice", "pf_choice")
 PLAN_KINDS = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
               "conv_relu_maxpool": 4}
 
@@ -266,7 +276,40 @@ def debug_plan(kind: str, dims) -> dict:
     out = (ctypes.c_uint32 * len(PLAN_FIELDS))()
     _raise(lib().b2b_debug_plan(PLAN_KINDS[kind], arr, len(dims), out, len(PLAN_FIELDS)),
            "b2b_debug_plan")
-    return dict(zip(PLAN_FIELDS, [int(v) for v in out]))
+    plan = dict(zip(PLAN_FIELDS, [int(v) for v in out]))
+    for k in _SIGNED_PLAN_FIELDS:
+        plan[k] = ctypes.c_int32(plan[k]).value
+    return plan
+
+
+# ------------------------------------------------------------------------------------
+# launch choices and the light-weight profiler (b2b_set_autotune and friends)
+# ------------------------------------------------------------------------------------
+
+def set_autotune(on: bool) -> None:
+    """With the profiler on, the first call of an entry point for new sizes times every
+    launch choice on the caller's stream and keeps the fastest (b2b_set_autotune)."""
+    lib().b2b_set_autotune(1 if on else 0)
+
+
+def autotune_reset() -> None:
+    lib().b2b_autotune_reset()
+
+
+def set_choice(kind: str, dims, cand: int = -1, grid: int = -1, prefetch_second: int = -1) -> None:
+    """Pins the launch choice of entry point `kind` for `dims` (b2b_set_choice)."""
+    arr = (ctypes.c_int64 * len(dims))(*[int(d) for d in dims])
+    _raise(lib().b2b_set_choice(PLAN_KINDS[kind], arr, len(dims), int(cand), int(grid),
+                                int(prefetch_second)), "b2b_set_choice")
+
+
+def get_choice(kind: str, dims) -> dict:
+    """The pinned or measured choice for `dims` (b2b_get_choice); source 0 = none."""
+    arr = (ctypes.c_int64 * len(dims))(*[int(d) for d in dims])
+    out = (ctypes.c_int32 * 7)()
+    _raise(lib().b2b_get_choice(PLAN_KINDS[kind], arr, len(dims), out, 7), "b2b_get_choice")
+    keys = ("source", "cand", "grid", "prefetch_second", "best_ns", "default_ns", "timed")
+    return dict(zip(keys, [int(v) for v in out]))
 
 
 def version() -> str:
@@ -301,7 +344,7 @@ TRACE_EVENTS = {1: "prod_acquire", 2: "prod_issued", 3: "mma_full", 4: "mma_g0_d
                 9: "epi_p_done", 10: "epi_d1_ready", 11: "epi_staging", 12: "epi_stored",
                 13: "mma_wait", 14: "mma_issued",
                 15: "prod_w1_issued", 16: "mma_w1_full",
-                17: "kernel_entry", 18: "epi_drained"}
+                17: "kernel_entry", 18: "epi_drained", 19: "setup_done", 20: "dep_ready"}
 
 
 def set_trace(buf, cta: int = 0) -> None:

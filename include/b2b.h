@@ -182,7 +182,7 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1}
  *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
- * out (out_len >= 47) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ * out (out_len >= 51) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
  * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
  * P offsets [2], bytes per P buffer, staging offsets [2], bytes per staging buffer,
@@ -194,10 +194,53 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * loaded once per pair of tiles into shared ring stages, the W1 chunks per stage, 1 if a
  * conv loads one halo box per column tap for all row taps, the A bytes per ring stage, the
  * number of accumulator buffers (tiles in flight: 1, 2 or 4), P offsets [2..3], GEMM0
- * accumulator columns [2..3] and GEMM1 accumulator columns [2..3].
+ * accumulator columns [2..3], GEMM1 accumulator columns [2..3], the layout taken (an
+ * index into the feasible layouts, in the planner's order of preference), the number of
+ * feasible layouts, and the pinned or measured grid and second-tile-prefetch choices
+ * (b2b_set_choice; -1, as a two's-complement word, for the default).  A choice pinned or
+ * measured for these sizes is reflected.
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,
+                          int32_t out_len);
+
+/* Launch choices and the light-weight profiler (BOLT notes, "Light-weight performance
+ * profiler" under "Automating templated code generation": a profiler picks among
+ * template configurations by timing them; here the configurations are launch choices of
+ * one kernel, which compute the same products with the same
+ * roundings: results are bit-identical, except that an R x S conv (R > 1) sums its taps
+ * in another fp32 order when its filters are resident (halo loads) than when they are
+ * streamed).
+ * A problem is an entry point (kind, as for b2b_debug_plan) and its sizes (dims).  Its
+ * launch may vary: the shared-memory / TMEM layout (cand: an index into the feasible
+ * layouts, 0 = most preferred), the grid (0: one CTA per SM, or per tile when there are
+ * fewer tiles; 1: the fewest CTAs that give no CTA more tiles than grid 0 does) and
+ * whether each CTA also prefetches its second tile's A rows into L2 at the start
+ * (prefetch_second 0/1; 2-D A operands only).  -1 leaves a field to the default.
+ *
+ * b2b_set_autotune(1): from then on, the first call of an entry point for a problem with
+ * no pinned or measured choice times the default and every choice (2 warm-up launches,
+ * then the fastest of 3 rounds of 10, CUDA events on the caller's stream, which it
+ * synchronises; the outputs are overwritten with the same values each time; the inputs
+ * are the caller's, so a problem smaller than L2 is timed with its inputs in L2), keeps
+ * the fastest for later calls of that problem -- the default unless another choice is
+ * more than 2 % faster -- and then runs it for the caller.  Calls on a stream being captured into a
+ * CUDA graph use the current choice or the default and never time.  Off by default.
+ * b2b_autotune_reset forgets every pinned and measured choice.  Host state shared by all
+ * devices and threads of the process. */
+void b2b_set_autotune(int32_t on);
+void b2b_autotune_reset(void);
+
+/* Pins a launch choice for a problem (no CUDA call).  B2B_ERR_UNSUPPORTED if cand is not
+ * a feasible layout for these sizes, B2B_ERR_SHAPE for a field out of range, otherwise the
+ * status b2b_debug_plan would return. */
+b2b_status b2b_set_choice(int32_t kind, const int64_t* dims, int32_t ndims, int32_t cand,
+                          int32_t grid, int32_t prefetch_second);
+
+/* The choice recorded for a problem (no CUDA call): out (out_len >= 7) = {source (0 none,
+ * 1 pinned, 2 measured), cand, grid, prefetch_second, fastest time in ns, default's time
+ * in ns, choices timed} (times 0 unless measured). */
+b2b_status b2b_get_choice(int32_t kind, const int64_t* dims, int32_t ndims, int32_t* out,
                           int32_t out_len);
 
 #ifdef __cplusplus

@@ -1,0 +1,120 @@
+"""Launch choices on the GPU: every layout x grid x prefetch choice of a problem computes
+bit-identical results, and the profiler keeps a choice no slower than the default.
+
+The choices change where tiles run and what sits where on chip, not the products or the
+roundings, so any difference is a layout or scheduling bug.  One thing may change: an
+R x S conv with resident filters (halo loads) sums its taps column tap by column tap,
+with streamed filters tap by tap, a different fp32 summation order; its cases use
+integer-valued inputs, whose sums are exact in any order.
+"""
+import pytest
+import torch
+
+from gemm_conv_chains_gb300 import ops
+from gemm_conv_chains_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ops.lib()
+    ops.get_device_error()
+    ops.set_autotune(False)
+    ops.autotune_reset()
+    yield
+    ops.set_autotune(False)
+    ops.autotune_reset()
+
+
+def _gemm(w, seed=5):
+    t = {k: (v.cuda() if v is not None else None) for k, v in wl.gemm_inputs(w, seed=seed).items()}
+    dims = (w.M, w.K0, w.N0, w.N1)
+    return "b2b_gemm", dims, lambda: ops.b2b_gemm(t["A"], t["W0"], t["b0"], t["W1"], t["b1"],
+                                                  w.act0, w.act1)
+
+
+def _conv(w, seed=6):
+    t = {k: v.cuda() for k, v in wl.conv_inputs(w, seed=seed, integer=w.R > 1).items()}
+    dims = (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1)
+    return "b2b_conv_nhwc", dims, lambda: ops.b2b_conv_nhwc(
+        t["x"], t["W0"], t["b0"], t["W1"], t["b1"], pad=w.pad, epi0=w.act0, epi1=w.act1)
+
+
+def _pool(w, seed=7):
+    t = {k: v.cuda() for k, v in wl.pool_inputs(w, seed=seed, integer=True).items()}
+    dims = (w.N, w.H, w.W, w.Cin, w.Cout)
+    return "conv_relu_maxpool", dims, lambda: ops.conv_relu_maxpool(t["x"], t["Wt"], t["b"])
+
+
+PROBLEMS = {
+    # 256 tiles: grids 152 and 128, P in TMEM by default
+    "ffn": lambda: _gemm(wl.GEMM_FFN),
+    # 313 tiles: three per CTA on 152 or 105 CTAs; every smem / TMEM layout of a wide chain
+    "wide": lambda: _gemm(wl.GemmChain("w", "f16", 40000, 128, 256, 64, "relu", "hardswish")),
+    "small": lambda: _gemm(wl.GemmChain("s", "f16", 1000, 64, 64, 64, "hardswish", "relu")),
+    "conv1x1": lambda: _conv(wl.ConvChain("c1", "f16", 8, 56, 56, 64, 64, 1, 1, 0, 64,
+                                          "relu", "relu")),
+    "conv3x3": lambda: _conv(wl.ConvChain("c3", "bf16", 4, 56, 56, 64, 64, 3, 3, 1, 128,
+                                          "hardswish", "none")),
+    "pool": lambda: _pool(wl.ConvPool("p", "f16", 4, 112, 112, 64, 64)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PROBLEMS))
+def test_every_choice_is_bit_identical(name):
+    kind, dims, call = PROBLEMS[name]()
+    ref = call().clone()
+    n = ops.debug_plan(kind, dims)["ncand"]
+    for cand in range(n):
+        for grid in (0, 1):
+            for pf in (0, 1):
+                ops.set_choice(kind, dims, cand=cand, grid=grid, prefetch_second=pf)
+                out = call()
+                torch.cuda.synchronize()
+                assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), \
+                    (name, cand, grid, pf)
+    st, info = ops.get_device_error()
+    assert st == 0, info
+
+
+def test_profiler_keeps_the_fastest_choice():
+    kind, dims, call = PROBLEMS["ffn"]()
+    ref = call().clone()
+    ops.set_autotune(True)
+    out = call()                      # times every choice, then runs the fastest
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    c = ops.get_choice(kind, dims)
+    n = ops.debug_plan(kind, dims)["ncand"]
+    assert c["source"] == 2
+    assert c["timed"] == 1 + n * 2 * 2            # the default, then every distinct choice
+    assert 0 < c["best_ns"] <= c["default_ns"]
+    if c["cand"] == -1:               # the default was kept
+        assert c["best_ns"] == c["default_ns"]
+    else:                             # another choice won by more than the 2 % margin
+        assert c["best_ns"] < 0.98 * c["default_ns"] + 1
+    # later calls reuse the choice without timing again
+    again = call()
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
+    assert ops.get_choice(kind, dims) == c
+
+
+def test_profiler_does_not_time_inside_graph_capture():
+    kind, dims, call = PROBLEMS["small"]()
+    ref = call().clone()
+    ops.set_autotune(True)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        call()                        # warm the caching allocator outside the capture
+        ops.autotune_reset()
+        with torch.cuda.graph(g, stream=stream):
+            out = call()
+    assert ops.get_choice(kind, dims)["source"] == 0
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

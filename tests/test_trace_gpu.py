@@ -40,9 +40,12 @@ def test_trace_of_a_chain_is_complete_and_causal():
         assert when[("mma_p_ready", it)] <= when[("mma_g1_done", it)]
         assert when[("mma_g1_done", it)] <= when[("epi_d1_ready", it)]
         assert when[("epi_d1_ready", it)] <= when[("epi_stored", it)]
-    # the CTA's entry event comes first
-    assert names.count("kernel_entry") == 1
+    # the CTA's entry event comes first, then the end of its setup, then the end of the
+    # wait for the previous grid; the first MMA follows both
+    for name in ("kernel_entry", "setup_done", "dep_ready"):
+        assert names.count(name) == 1, name
     assert all(when[("kernel_entry", 0)] <= e[0] for e in ev)
+    assert when[("setup_done", 0)] <= when[("dep_ready", 0)] <= when[("mma_g0_done", 0)]
 
 
 def test_trace_off_records_nothing():
