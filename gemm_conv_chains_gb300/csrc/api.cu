@@ -449,23 +449,35 @@ bool conv_params(ChainParams& p, int mode, int32_t N, int32_t H, int32_t W, int3
 // What a launch of one problem may vary without changing its results (the same MMAs in
 // the same order, the same roundings): the shared-memory / TMEM layout (an index into the
 // planner's feasible candidates), the grid (0: one CTA per SM, or per tile if fewer;
-// 1: the fewest CTAs that keep the busiest CTA's tile count) and whether each CTA's
-// second tile's A rows are prefetched into L2 at the start.  -1 leaves a field to the
-// planner's default.
+// 1: the fewest CTAs that keep the busiest CTA's tile count; 2: one CTA per tile, in
+// waves) and whether each CTA's second tile's A rows are prefetched into L2 at the start.
+// -1 leaves a field to the planner's default.
 struct Choice {
   int32_t cand = -1, grid = -1, pf2 = -1;
 };
 
 // What one launch looked like, for the profiler's enumeration.
+constexpr int kGridModes = 3;
 struct Info {
-  int32_t ncand = 0, grid_full = 0, grid_balanced = 0, tiles = 0, can_prefetch = 0;
+  int32_t ncand = 0, tiles = 0, can_prefetch = 0;
+  int32_t grid[kGridModes] = {0, 0, 0};   // the grid of each mode
 };
 
 int grid_for(int32_t tiles, int sms, int32_t mode) {
   const int full = std::max(1, std::min<int>(tiles, sms));
+  if (mode == 2) return std::max(1, tiles);
   if (mode != 1) return full;
   const int per = (tiles + full - 1) / full;
   return std::max(1, (tiles + per - 1) / per);
+}
+
+Info info_for(int32_t ncand, int32_t tiles, int sms, bool can_prefetch) {
+  Info i;
+  i.ncand = ncand;
+  i.tiles = tiles;
+  i.can_prefetch = can_prefetch ? 1 : 0;
+  for (int m = 0; m < kGridModes; ++m) i.grid[m] = grid_for(tiles, sms, m);
+  return i;
 }
 
 // Default: prefetch the second tile too when a CTA has more than two tiles -- then the
@@ -494,8 +506,7 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = pf_second_for(p.num_tiles, grid, ch.pf2);
-  if (info) *info = {r.ncand, grid_for(p.num_tiles, d->num_sms, 0),
-                     grid_for(p.num_tiles, d->num_sms, 1), p.num_tiles, 1};
+  if (info) *info = info_for(r.ncand, p.num_tiles, d->num_sms, true);
 
   CUtensorMap ta, tw0, tw1, to;
   const uint64_t e = 2;
@@ -569,8 +580,7 @@ b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = 0;   // the implicit-GEMM A has no per-tile contiguous range to prefetch
-  if (info) *info = {r.ncand, grid_for(p.num_tiles, d->num_sms, 0),
-                     grid_for(p.num_tiles, d->num_sms, 1), p.num_tiles, 0};
+  if (info) *info = info_for(r.ncand, p.num_tiles, d->num_sms, false);
   const int32_t Ho = p.Ho, Wo = p.Wo;
 
   const uint64_t e = 2;
@@ -681,10 +691,13 @@ b2b_status tune(const TuneKey& key, void* stream, Go&& go) {
   if (st == B2B_OK) {
     best_us = def_us;
     timed = 1;
-    const int grids = info.grid_balanced != info.grid_full ? 2 : 1;
-    const int pfs = (info.can_prefetch && info.tiles > info.grid_balanced) ? 2 : 1;
     for (int32_t cand = 0; cand < info.ncand && st == B2B_OK; ++cand)
-      for (int32_t grid = 0; grid < grids && st == B2B_OK; ++grid)
+      for (int32_t grid = 0; grid < kGridModes && st == B2B_OK; ++grid) {
+        bool same = false;   // a grid mode that gives an earlier mode's grid is skipped
+        for (int m = 0; m < grid; ++m) same = same || info.grid[m] == info.grid[grid];
+        if (same) continue;
+        // the second-tile prefetch matters only where some CTA has a second tile
+        const int pfs = (info.can_prefetch && info.tiles > info.grid[grid]) ? 2 : 1;
         for (int32_t pf = 0; pf < pfs && st == B2B_OK; ++pf) {
           const Choice c{cand, grid, pfs == 2 ? pf : 0};
           float us = 0.f;
@@ -697,6 +710,7 @@ b2b_status tune(const TuneKey& key, void* stream, Go&& go) {
             }
           }
         }
+      }
   }
   if (st == B2B_ERR_CUDA) cudaGetLastError();
   cudaEventDestroy(ev0);
@@ -1052,7 +1066,7 @@ b2b_status b2b_set_choice(int32_t kind, const int64_t* dims, int32_t ndims, int3
                           int32_t grid, int32_t prefetch_second) {
   b2b_status st = check_plan_args(kind, dims, ndims);
   if (st != B2B_OK) return st;
-  if (cand < -1 || grid < -1 || grid > 1 || prefetch_second < -1 || prefetch_second > 1)
+  if (cand < -1 || grid < -1 || grid > 2 || prefetch_second < -1 || prefetch_second > 1)
     return B2B_ERR_SHAPE;
   ChainParams p;
   Regions r;

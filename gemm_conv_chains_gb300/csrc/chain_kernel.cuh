@@ -1032,9 +1032,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     *abort_flag = 0u;
     fence_barrier_init();
     fence_proxy_async_smem();
-    // This grid is resident in one wave, so the next kernel may be scheduled now; its
-    // CTAs take an SM as this grid's CTAs leave and wait for this grid before touching
-    // global memory.
+    // Once every CTA of this grid has passed this point, the next kernel may be
+    // scheduled; its CTAs take an SM as this grid's CTAs leave and wait for this grid
+    // before touching global memory.
     grid_launch_dependents();
   }
   if (warp == 0 && lane == 0) {

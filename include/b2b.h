@@ -214,7 +214,8 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
  * A problem is an entry point (kind, as for b2b_debug_plan) and its sizes (dims).  Its
  * launch may vary: the shared-memory / TMEM layout (cand: an index into the feasible
  * layouts, 0 = most preferred), the grid (0: one CTA per SM, or per tile when there are
- * fewer tiles; 1: the fewest CTAs that give no CTA more tiles than grid 0 does) and
+ * fewer tiles; 1: the fewest CTAs that give no CTA more tiles than grid 0 does; 2: one
+ * CTA per tile, in as many waves as it takes) and
  * whether each CTA also prefetches its second tile's A rows into L2 at the start
  * (prefetch_second 0/1; 2-D A operands only).  -1 leaves a field to the default.
  *

@@ -58,7 +58,7 @@ def test_infeasible_and_out_of_range_choices_are_refused():
     with pytest.raises(ops.B2BError) as e:
         ops.set_choice(kind, dims, cand=n)
     assert e.value.status == 4          # B2B_ERR_UNSUPPORTED
-    for bad in (dict(grid=2), dict(prefetch_second=2), dict(cand=-2), dict(grid=-3)):
+    for bad in (dict(grid=3), dict(prefetch_second=2), dict(cand=-2), dict(grid=-3)):
         with pytest.raises(ops.B2BError) as e:
             ops.set_choice(kind, dims, **bad)
         assert e.value.status == 2      # B2B_ERR_SHAPE

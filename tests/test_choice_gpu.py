@@ -50,9 +50,10 @@ def _pool(w, seed=7):
 
 
 PROBLEMS = {
-    # 256 tiles: grids 152 and 128, P in TMEM by default
+    # 256 tiles: grids 152, 128 and 256, P in TMEM by default
     "ffn": lambda: _gemm(wl.GEMM_FFN),
-    # 313 tiles: three per CTA on 152 or 105 CTAs; every smem / TMEM layout of a wide chain
+    # 313 tiles: three per CTA on 152 or 105 CTAs, or one on 313; every smem / TMEM layout
+    # of a wide chain
     "wide": lambda: _gemm(wl.GemmChain("w", "f16", 40000, 128, 256, 64, "relu", "hardswish")),
     "small": lambda: _gemm(wl.GemmChain("s", "f16", 1000, 64, 64, 64, "hardswish", "relu")),
     "conv1x1": lambda: _conv(wl.ConvChain("c1", "f16", 8, 56, 56, 64, 64, 1, 1, 0, 64,
@@ -69,7 +70,7 @@ def test_every_choice_is_bit_identical(name):
     ref = call().clone()
     n = ops.debug_plan(kind, dims)["ncand"]
     for cand in range(n):
-        for grid in (0, 1):
+        for grid in (0, 1, 2):
             for pf in (0, 1):
                 ops.set_choice(kind, dims, cand=cand, grid=grid, prefetch_second=pf)
                 out = call()
@@ -90,7 +91,9 @@ def test_profiler_keeps_the_fastest_choice():
     c = ops.get_choice(kind, dims)
     n = ops.debug_plan(kind, dims)["ncand"]
     assert c["source"] == 2
-    assert c["timed"] == 1 + n * 2 * 2            # the default, then every distinct choice
+    # the default, then per layout: grids of 152 and 128 CTAs with and without the
+    # second-tile prefetch, and 256 CTAs (one tile each, nothing to prefetch)
+    assert c["timed"] == 1 + n * (2 + 2 + 1)
     assert 0 < c["best_ns"] <= c["default_ns"]
     if c["cand"] == -1:               # the default was kept
         assert c["best_ns"] == c["default_ns"]
