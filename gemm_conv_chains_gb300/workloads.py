@@ -71,7 +71,7 @@ class GemmChain:
 
 @dataclasses.dataclass(frozen=True)
 class ConvChain:
-    """conv RxS (stride 1, pad) + b0 + act0 -> conv1x1 + b1 + act1, NHWC."""
+    """conv RxS (pad, stride) + b0 + act0 -> conv1x1 + b1 + act1, NHWC."""
     name: str
     dtype: str
     N: int
@@ -85,14 +85,15 @@ class ConvChain:
     C1: int
     act0: str
     act1: str
+    stride: int = 1
 
     @property
     def Ho(self) -> int:
-        return self.H + 2 * self.pad - self.R + 1
+        return max(0, (self.H + 2 * self.pad - self.R) // self.stride + 1)
 
     @property
     def Wo(self) -> int:
-        return self.W + 2 * self.pad - self.S + 1
+        return max(0, (self.W + 2 * self.pad - self.S) // self.stride + 1)
 
     @property
     def M(self) -> int:

@@ -86,9 +86,18 @@ def _load():
                                              i64, u16p, ci, u16p, i64, u16p, ci, u16p]
         lib.oracle_conv_relu_maxpool.argtypes = [ci, i64, i64, i64, i64, u16p, u16p, u16p, i64,
                                                  u16p]
+        lib.oracle_conv2d_nhwc_strided.argtypes = [ci, i64, i64, i64, i64, u16p, i64, i64, i64,
+                                                   i64, i64, u16p, u16p, ci, u16p]
+        lib.oracle_b2b_conv_nhwc_strided.argtypes = [ci, i64, i64, i64, i64, u16p, u16p, i64,
+                                                     i64, i64, i64, i64, u16p, ci, u16p, i64,
+                                                     u16p, ci, u16p]
+        f32p = ctypes.POINTER(ctypes.c_float)
+        lib.oracle_fold_batchnorm.argtypes = [ci, i64, i64, ci, u16p, u16p, f32p, f32p, f32p,
+                                              f32p, ctypes.c_double, u16p, u16p]
         for name in ("oracle_gemm_bias_act", "oracle_b2b_gemm", "oracle_conv2d_nhwc",
                      "oracle_maxpool2x2_nhwc", "oracle_b2b_conv_nhwc",
-                     "oracle_conv_relu_maxpool"):
+                     "oracle_conv_relu_maxpool", "oracle_conv2d_nhwc_strided",
+                     "oracle_b2b_conv_nhwc_strided", "oracle_fold_batchnorm"):
             getattr(lib, name).restype = ci
         _lib = lib
         return lib
@@ -190,7 +199,12 @@ def b2b_gemm(dtype, A, W0, b0, W1, b1, act0, act1):
     return out
 
 
-def conv2d_nhwc(dtype, x, Wt, b, pad, act):
+def conv_out_size(n, pad, k, stride=1):
+    """Output length of a conv along one axis: floor((n + 2 pad - k) / stride) + 1."""
+    return 0 if n + 2 * pad < k else (n + 2 * pad - k) // stride + 1
+
+
+def conv2d_nhwc(dtype, x, Wt, b, pad, act, stride=1):
     """Direct convolution. x [N,H,W,C], Wt [Co,R,S,C] -> out [N,Ho,Wo,Co]."""
     lib = _load()
     x, px = _u16(x, "x")
@@ -199,11 +213,12 @@ def conv2d_nhwc(dtype, x, Wt, b, pad, act):
     N, H, W, C = x.shape
     Co, R, S, C2 = Wt.shape
     assert C == C2
-    Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
-    out = np.empty((N, max(Ho, 0), max(Wo, 0), Co), dtype=np.uint16)
-    _check(lib.oracle_conv2d_nhwc(_dt(dtype), N, H, W, C, px, Co, R, S, pad, pW, pb,
-                                  _act(act), out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))),
-           "oracle_conv2d_nhwc")
+    Ho, Wo = conv_out_size(H, pad, R, stride), conv_out_size(W, pad, S, stride)
+    out = np.empty((N, Ho, Wo, Co), dtype=np.uint16)
+    _check(lib.oracle_conv2d_nhwc_strided(_dt(dtype), N, H, W, C, px, Co, R, S, pad, stride, pW,
+                                          pb, _act(act),
+                                          out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))),
+           "oracle_conv2d_nhwc_strided")
     return out
 
 
@@ -218,8 +233,8 @@ def maxpool2x2_nhwc(dtype, x):
     return out
 
 
-def b2b_conv_nhwc(dtype, x, W0, b0, W1, b1, pad, act0, act1):
-    """conv RxS (+bias, act0) -> intermediate -> 1x1 conv (+bias, act1).
+def b2b_conv_nhwc(dtype, x, W0, b0, W1, b1, pad, act0, act1, stride=1):
+    """conv RxS, stride `stride` (+bias, act0) -> intermediate -> 1x1 conv (+bias, act1).
     x [N,H,W,C], W0 [C0,R,S,C], W1 [C1,C0] -> out [N,Ho,Wo,C1]."""
     lib = _load()
     x, px = _u16(x, "x")
@@ -232,13 +247,35 @@ def b2b_conv_nhwc(dtype, x, W0, b0, W1, b1, pad, act0, act1):
     assert C == C2
     C1, C0b = W1.shape
     assert C0b == C0
-    Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
-    out = np.empty((N, max(Ho, 0), max(Wo, 0), C1), dtype=np.uint16)
-    _check(lib.oracle_b2b_conv_nhwc(_dt(dtype), N, H, W, C, px, pW0, C0, R, S, pad, pb0,
-                                    _act(act0), pW1, C1, pb1, _act(act1),
-                                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))),
-           "oracle_b2b_conv_nhwc")
+    Ho, Wo = conv_out_size(H, pad, R, stride), conv_out_size(W, pad, S, stride)
+    out = np.empty((N, Ho, Wo, C1), dtype=np.uint16)
+    _check(lib.oracle_b2b_conv_nhwc_strided(_dt(dtype), N, H, W, C, px, pW0, C0, R, S, pad,
+                                            stride, pb0, _act(act0), pW1, C1, pb1, _act(act1),
+                                            out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))),
+           "oracle_b2b_conv_nhwc_strided")
     return out
+
+
+def fold_batchnorm(dtype, Wt, b, gamma, beta, mean, var, eps, out_inner=False):
+    """Batch normalisation folded into the preceding operator's weights and bias
+    (interview notes, SimplifyInference: BN -> scale + bias).  Wt [Co, ...] (conv filters,
+    out_inner False) or [K, Co] (row-major GEMM weights, out_inner True); b [Co] or None;
+    gamma, beta, mean, var float32 [Co].  Returns (W', b') in the storage type."""
+    lib = _load()
+    Wt, pW = _u16(Wt, "Wt")
+    b, pb = _u16(b, "b")
+    Co = Wt.shape[-1] if out_inner else Wt.shape[0]
+    K = Wt.size // max(Co, 1)
+    f32 = [np.ascontiguousarray(np.asarray(v, dtype=np.float32)) for v in (gamma, beta, mean, var)]
+    assert all(v.shape == (Co,) for v in f32)
+    fp = [v.ctypes.data_as(ctypes.POINTER(ctypes.c_float)) for v in f32]
+    W_out = np.empty_like(Wt)
+    b_out = np.empty((Co,), dtype=np.uint16)
+    _check(lib.oracle_fold_batchnorm(_dt(dtype), Co, K, 1 if out_inner else 0, pW, pb, *fp,
+                                     float(eps), W_out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)),
+                                     b_out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))),
+           "oracle_fold_batchnorm")
+    return W_out, b_out
 
 
 def conv_relu_maxpool(dtype, x, Wt, b):

@@ -18,6 +18,11 @@
  *       (Figure 5): Conv computes a 1x1xC output from a 3x3xC input tile; ReLU; MaxPool
  *       reduces a 2x2xF reuse tile to 1x1xF.
  *   Interview notes, "Conv optimisation", item 5: a 1x1 conv is a GEMM.
+ *   Welder notes, "Operator-tile and Tile-graph", tile propagation: a strided conv reads
+ *       a strided (non-contiguous) input region.
+ *   Interview notes, TVM Relay vs. TIR scheduling primitives, SimplifyInference: batch
+ *       normalisation becomes a scale and a bias at inference, which folded into the
+ *       preceding conv's weights and bias is the chain's bias epilogue.
  *
  * Arithmetic:
  *   - every stored tensor is fp16 or bf16 (bit patterns in uint16_t);
@@ -29,7 +34,8 @@
  *     of what the fused kernel computes: it writes an fp16/bf16 tile on chip).
  *
  * Readings where the pages are silent (each is listed in the design notes):
- *   - conv is cross-correlation, stride 1, dilation 1, zero padding `pad`;
+ *   - conv is cross-correlation, dilation 1, zero padding `pad`, stride `stride` in both
+ *     spatial dimensions (1 unless given);
  *   - weight layouts: GEMM W[K][N] row-major; conv W[Cout][R][S][Cin];
  *   - hardswish(x) = x * min(max(x + 3, 0), 6) / 6;
  *   - max-pool 2x2, stride 2, floor mode (odd trailing row/column dropped).
@@ -227,20 +233,28 @@ int oracle_b2b_gemm(int dt, int64_t M, int64_t K0, int64_t N0, int64_t N1,
 }
 
 /* ------------------------------------------------------------------------------------ */
-/* Direct 2-D convolution, NHWC, stride 1, zero padding `pad`, cross-correlation:          */
+/* Direct 2-D convolution, NHWC, stride st, zero padding `pad`, cross-correlation:        */
 /*   z[n][h][w][co] = b[co] + sum_{r<R} sum_{s<S} sum_{ci<C}                              */
-/*                      x[n][h+r-pad][w+s-pad][ci] * Wt[co][r][s][ci]                      */
+/*                      x[n][st*h+r-pad][st*w+s-pad][ci] * Wt[co][r][s][ci]                */
 /* with x taken as 0 outside [0,H) x [0,W).  The sum runs r, then s, then ci.             */
-/* Output spatial size Ho = H + 2*pad - R + 1, Wo = W + 2*pad - S + 1.                    */
+/* Output spatial size Ho = (H + 2*pad - R) / st + 1, Wo = (W + 2*pad - S) / st + 1       */
+/* (floor; no output if H + 2*pad < R or W + 2*pad < S).                                  */
 /* out[n][h][w][co] = rnd(act(z)).                                                        */
 /* ------------------------------------------------------------------------------------ */
-int oracle_conv2d_nhwc(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
-                       const uint16_t* x, int64_t Co, int64_t R, int64_t S, int64_t pad,
-                       const uint16_t* Wt, const uint16_t* b, int act, uint16_t* out)
+static int64_t conv_out_size(int64_t in, int64_t pad, int64_t k, int64_t st)
 {
-    const int64_t Ho = H + 2 * pad - R + 1, Wo = W + 2 * pad - S + 1;
+    return in + 2 * pad < k ? 0 : (in + 2 * pad - k) / st + 1;
+}
+
+int oracle_conv2d_nhwc_strided(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
+                               const uint16_t* x, int64_t Co, int64_t R, int64_t S, int64_t pad,
+                               int64_t st, const uint16_t* Wt, const uint16_t* b, int act,
+                               uint16_t* out)
+{
+    const int64_t Ho = conv_out_size(H, pad, R, st), Wo = conv_out_size(W, pad, S, st);
     double *wt, *img, *acc;
-    if (N < 0 || H < 0 || W < 0 || C < 0 || Co < 0 || R < 1 || S < 1 || pad < 0) return OR_BAD_ARG;
+    if (N < 0 || H < 0 || W < 0 || C < 0 || Co < 0 || R < 1 || S < 1 || pad < 0 || st < 1)
+        return OR_BAD_ARG;
     if (!x || !Wt || !out) return OR_BAD_ARG;
     if (Ho <= 0 || Wo <= 0) return OR_OK;
     wt = decode_alloc(dt, Co * R * S * C, Wt);
@@ -255,10 +269,10 @@ int oracle_conv2d_nhwc(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
                 for (int64_t co = 0; co < Co; ++co) {
                     double s_acc = 0.0;
                     for (int64_t r = 0; r < R; ++r) {
-                        const int64_t hi = ho + r - pad;
+                        const int64_t hi = st * ho + r - pad;
                         if (hi < 0 || hi >= H) continue;      /* zero padding row */
                         for (int64_t s = 0; s < S; ++s) {
-                            const int64_t wi = wo + s - pad;
+                            const int64_t wi = st * wo + s - pad;
                             const double* xp;
                             const double* wp;
                             if (wi < 0 || wi >= W) continue;  /* zero padding column */
@@ -278,6 +292,13 @@ int oracle_conv2d_nhwc(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
     }
     free(wt); free(img); free(acc);
     return OR_OK;
+}
+
+int oracle_conv2d_nhwc(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
+                       const uint16_t* x, int64_t Co, int64_t R, int64_t S, int64_t pad,
+                       const uint16_t* Wt, const uint16_t* b, int act, uint16_t* out)
+{
+    return oracle_conv2d_nhwc_strided(dt, N, H, W, C, x, Co, R, S, pad, 1, Wt, b, act, out);
 }
 
 /* Max-pool 2x2, stride 2, floor mode, NHWC: out [N][H/2][W/2][C].  The maximum of
@@ -304,29 +325,70 @@ int oracle_maxpool2x2_nhwc(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
     return OR_OK;
 }
 
-/* conv(R x S, pad) + bias + act0 -> intermediate (storage type) -> 1x1 conv + bias + act1.
- * x [N][H][W][C], W0 [C0][R][S][C], W1 [C1][C0], out [N][Ho][Wo][C1].
- * Images are independent, so the intermediate is formed one image at a time. */
-int oracle_b2b_conv_nhwc(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
-                         const uint16_t* x, const uint16_t* W0, int64_t C0, int64_t R, int64_t S,
-                         int64_t pad, const uint16_t* b0, int act0,
-                         const uint16_t* W1, int64_t C1, const uint16_t* b1, int act1,
-                         uint16_t* out)
+/* conv(R x S, pad, stride st) + bias + act0 -> intermediate (storage type) -> 1x1 conv
+ * (stride 1) + bias + act1.  x [N][H][W][C], W0 [C0][R][S][C], W1 [C1][C0],
+ * out [N][Ho][Wo][C1].  Images are independent, so the intermediate is formed one image
+ * at a time. */
+int oracle_b2b_conv_nhwc_strided(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
+                                 const uint16_t* x, const uint16_t* W0, int64_t C0, int64_t R,
+                                 int64_t S, int64_t pad, int64_t st, const uint16_t* b0, int act0,
+                                 const uint16_t* W1, int64_t C1, const uint16_t* b1, int act1,
+                                 uint16_t* out)
 {
-    const int64_t Ho = H + 2 * pad - R + 1, Wo = W + 2 * pad - S + 1;
+    const int64_t Ho = st >= 1 ? conv_out_size(H, pad, R, st) : 0;
+    const int64_t Wo = st >= 1 ? conv_out_size(W, pad, S, st) : 0;
     uint16_t* h;
-    if (N < 0 || !x || !W0 || !W1 || !out) return OR_BAD_ARG;
+    if (N < 0 || st < 1 || !x || !W0 || !W1 || !out) return OR_BAD_ARG;
     if (Ho <= 0 || Wo <= 0) return OR_OK;
     h = (uint16_t*)malloc((size_t)((Ho * Wo * C0) > 0 ? Ho * Wo * C0 : 1) * sizeof(uint16_t));
     if (!h) return OR_NO_MEM;
     for (int64_t n = 0; n < N; ++n) {
-        int rc = oracle_conv2d_nhwc(dt, 1, H, W, C, x + n * H * W * C, C0, R, S, pad, W0, b0, act0, h);
+        int rc = oracle_conv2d_nhwc_strided(dt, 1, H, W, C, x + n * H * W * C, C0, R, S, pad, st,
+                                            W0, b0, act0, h);
         if (rc == OR_OK)
             rc = oracle_conv2d_nhwc(dt, 1, Ho, Wo, C0, h, C1, 1, 1, 0, W1, b1, act1,
                                     out + n * Ho * Wo * C1);
         if (rc != OR_OK) { free(h); return rc; }
     }
     free(h);
+    return OR_OK;
+}
+
+int oracle_b2b_conv_nhwc(int dt, int64_t N, int64_t H, int64_t W, int64_t C,
+                         const uint16_t* x, const uint16_t* W0, int64_t C0, int64_t R, int64_t S,
+                         int64_t pad, const uint16_t* b0, int act0,
+                         const uint16_t* W1, int64_t C1, const uint16_t* b1, int act1,
+                         uint16_t* out)
+{
+    return oracle_b2b_conv_nhwc_strided(dt, N, H, W, C, x, W0, C0, R, S, pad, 1, b0, act0, W1, C1,
+                                        b1, act1, out);
+}
+
+/* Batch normalisation folded into the weights and bias of the operator before it
+ * (interview notes, SimplifyInference: BN becomes scale and bias at inference):
+ *   y = gamma * (z - mean) / sqrt(var + eps) + beta,   z = sum_k W[co][k] x[k] + b[co]
+ *     = sum_k (W[co][k] * s[co]) x[k] + ((b[co] - mean[co]) * s[co] + beta[co]),
+ *   s[co] = gamma[co] / sqrt(var[co] + eps).
+ * W is [Co][K] (out_inner = 0: conv filters [Co][R][S][Cin], K = R*S*Cin) or [K][Co]
+ * (out_inner = 1: row-major GEMM weights); gamma, beta, mean, var are fp32 (float), b
+ * may be NULL (0).  Each folded value is formed in double and rounded once to the
+ * storage type. */
+int oracle_fold_batchnorm(int dt, int64_t Co, int64_t K, int out_inner, const uint16_t* Wt,
+                          const uint16_t* b, const float* gamma, const float* beta,
+                          const float* mean, const float* var, double eps, uint16_t* W_out,
+                          uint16_t* b_out)
+{
+    if (Co < 0 || K < 0 || !Wt || !gamma || !beta || !mean || !var || !W_out || !b_out)
+        return OR_BAD_ARG;
+    for (int64_t co = 0; co < Co; ++co) {
+        const double s = (double)gamma[co] / sqrt((double)var[co] + eps);
+        const double bias = b ? oracle_decode(dt, b[co]) : 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t i = out_inner ? k * Co + co : co * K + k;
+            W_out[i] = oracle_encode(dt, oracle_decode(dt, Wt[i]) * s);
+        }
+        b_out[co] = oracle_encode(dt, (bias - (double)mean[co]) * s + (double)beta[co]);
+    }
     return OR_OK;
 }
 

@@ -219,12 +219,12 @@ def test_b2b_equals_two_stages(oracle_mod):
 # convolution
 # ------------------------------------------------------------------------------------
 
-def _torch_conv_nhwc(x, Wt, b, pad):
+def _torch_conv_nhwc(x, Wt, b, pad, stride=1):
     """float64 library convolution (cross-correlation) on NHWC data."""
     xt = torch.from_numpy(x).permute(0, 3, 1, 2)
     wt = torch.from_numpy(Wt).permute(0, 3, 1, 2)
     bt = torch.from_numpy(b) if b is not None else None
-    return F.conv2d(xt, wt, bt, padding=pad).permute(0, 2, 3, 1).numpy()
+    return F.conv2d(xt, wt, bt, padding=pad, stride=stride).permute(0, 2, 3, 1).numpy()
 
 
 def _im2col_conv_nhwc(x, Wt, b, pad):
@@ -331,6 +331,134 @@ def test_b2b_conv_equals_conv_then_pointwise(oracle_mod):
     y = oracle_mod.b2b_conv_nhwc("f16", t["x"], t["W0"], t["b0"], t["W1"], t["b1"], 1,
                                  "hardswish", "none")
     assert np.array_equal(y, y2)
+
+
+# ------------------------------------------------------------------------------------
+# strided conv (Welder notes, tile propagation: a strided conv reads a strided region)
+# ------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape", [
+    # N, H, W, C, Co, R, S, pad, stride
+    (2, 9, 8, 3, 4, 3, 3, 1, 2),
+    (1, 7, 7, 8, 5, 3, 3, 1, 2),     # odd size: the last window ends at the padding
+    (1, 10, 6, 2, 3, 1, 1, 0, 2),    # 1x1 stride 2 (a downsampling projection)
+    (1, 11, 9, 4, 2, 5, 3, 2, 3),
+])
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_strided_conv_integer_exact_vs_torch(oracle_mod, shape, dt):
+    N, H, W, C, Co, R, S, pad, st = shape
+    rng = np.random.default_rng(sum(shape) + 100)
+    x = rng.integers(-3, 4, (N, H, W, C)).astype(np.float64)
+    Wt = rng.integers(-3, 4, (Co, R, S, C)).astype(np.float64)
+    b = rng.integers(-2, 3, (Co,)).astype(np.float64)
+    enc = f16_bits if dt == "f16" else bf16_bits
+    got = oracle_mod.decode(dt, oracle_mod.conv2d_nhwc(dt, enc(x), enc(Wt), enc(b), pad, "none",
+                                                       stride=st))
+    ref = _torch_conv_nhwc(x, Wt, b, pad, stride=st)
+    Ho, Wo = (H + 2 * pad - R) // st + 1, (W + 2 * pad - S) // st + 1
+    assert got.shape == ref.shape == (N, Ho, Wo, Co)
+    assert np.array_equal(got, ref)
+
+
+def test_strided_conv_brute_force(oracle_mod):
+    # every output element from its own window, by plain loops over the definition
+    rng = np.random.default_rng(31)
+    N, H, W, C, Co, R, S, pad, st = 1, 6, 7, 2, 2, 3, 2, 1, 2
+    x = rng.integers(-3, 4, (N, H, W, C)).astype(np.float64)
+    Wt = rng.integers(-3, 4, (Co, R, S, C)).astype(np.float64)
+    got = oracle_mod.decode("f16", oracle_mod.conv2d_nhwc("f16", f16_bits(x), f16_bits(Wt), None,
+                                                          pad, "none", stride=st))
+    Ho, Wo = (H + 2 * pad - R) // st + 1, (W + 2 * pad - S) // st + 1
+    for ho in range(Ho):
+        for wo in range(Wo):
+            for co in range(Co):
+                acc = 0.0
+                for r in range(R):
+                    for s_ in range(S):
+                        hi, wi = ho * st + r - pad, wo * st + s_ - pad
+                        if 0 <= hi < H and 0 <= wi < W:
+                            acc += float(np.dot(x[0, hi, wi], Wt[co, r, s_]))
+                assert got[0, ho, wo, co] == acc, (ho, wo, co)
+
+
+def test_strided_conv_is_the_stride_one_conv_subsampled(oracle_mod):
+    # output (ho, wo) of a stride-2 conv is output (2 ho, 2 wo) of the stride-1 conv with
+    # the same padding: the same window, the same sum in the same order, bit for bit
+    w = wl.ConvChain("t", "bf16", 2, 9, 10, 8, 16, 3, 3, 1, 8, "hardswish", "none")
+    t = {k: wl.to_bits(v) for k, v in wl.conv_inputs(w, seed=12).items()}
+    one = oracle_mod.conv2d_nhwc("bf16", t["x"], t["W0"], t["b0"], 1, "hardswish")
+    two = oracle_mod.conv2d_nhwc("bf16", t["x"], t["W0"], t["b0"], 1, "hardswish", stride=2)
+    assert two.shape == (2, 5, 5, 16)
+    assert np.array_equal(two, one[:, ::2, ::2, :])
+
+
+def test_strided_b2b_conv_equals_conv_then_pointwise(oracle_mod):
+    w = wl.ConvChain("t", "f16", 2, 9, 7, 8, 16, 3, 3, 1, 24, "relu", "none")
+    t = {k: wl.to_bits(v) for k, v in wl.conv_inputs(w, seed=13).items()}
+    h = oracle_mod.conv2d_nhwc("f16", t["x"], t["W0"], t["b0"], 1, "relu", stride=2)
+    y2 = oracle_mod.conv2d_nhwc("f16", h, t["W1"].reshape(w.C1, 1, 1, w.C0), t["b1"], 0, "none")
+    y = oracle_mod.b2b_conv_nhwc("f16", t["x"], t["W0"], t["b0"], t["W1"], t["b1"], 1, "relu",
+                                 "none", stride=2)
+    assert y.shape == (2, 5, 4, 24)
+    assert np.array_equal(y, y2)
+
+
+# ------------------------------------------------------------------------------------
+# batch normalisation folded into weights and bias (interview notes, SimplifyInference)
+# ------------------------------------------------------------------------------------
+
+def test_fold_batchnorm_power_of_two_scale_is_exact(oracle_mod):
+    # gamma / sqrt(var + eps) = 2 and 0.5: scaling by a power of two is exact, and
+    # (b - mean) * s + beta is exact for these small integers
+    rng = np.random.default_rng(40)
+    W = rng.integers(-8, 9, (2, 3, 3, 4)).astype(np.float64)
+    b = np.array([3.0, -2.0])
+    gamma = np.array([4.0, 1.0], np.float32)
+    var = np.array([3.0, 3.0], np.float32)         # sqrt(var + 1) = 2
+    mean = np.array([1.0, -4.0], np.float32)
+    beta = np.array([0.5, -1.0], np.float32)
+    Wf, bf = oracle_mod.fold_batchnorm("f16", f16_bits(W), f16_bits(b), gamma, beta, mean, var,
+                                       1.0)
+    s = np.array([2.0, 0.5])
+    assert np.array_equal(oracle_mod.decode("f16", Wf), W * s[:, None, None, None])
+    assert np.array_equal(oracle_mod.decode("f16", bf), (b - mean) * s + beta)
+
+
+def test_fold_batchnorm_equals_conv_then_batchnorm(oracle_mod):
+    # conv with folded weights and bias == batch norm applied to the conv's fp64 output,
+    # up to the rounding of the folded weights to fp16 (checked in float64 by torch)
+    rng = np.random.default_rng(41)
+    x = oracle_mod.decode("f16", f16_bits(rng.uniform(-1, 1, (1, 6, 5, 8))))
+    W = oracle_mod.decode("f16", f16_bits(rng.normal(0, 0.3, (4, 3, 3, 8))))
+    b = oracle_mod.decode("f16", f16_bits(rng.uniform(-0.1, 0.1, (4,))))
+    gamma = rng.uniform(0.5, 2.0, 4).astype(np.float32)
+    beta = rng.uniform(-0.5, 0.5, 4).astype(np.float32)
+    mean = rng.uniform(-0.2, 0.2, 4).astype(np.float32)
+    var = rng.uniform(0.5, 2.0, 4).astype(np.float32)
+    eps = 1e-5
+    Wf, bf = oracle_mod.fold_batchnorm("f16", f16_bits(W), f16_bits(b), gamma, beta, mean, var,
+                                       eps)
+    z = _torch_conv_nhwc(x, W, b, 1)
+    bn = (z - mean) * (gamma / np.sqrt(var.astype(np.float64) + eps)) + beta
+    folded = _torch_conv_nhwc(x, oracle_mod.decode("f16", Wf), oracle_mod.decode("f16", bf), 1)
+    assert np.max(np.abs(folded - bn)) < 2e-2 * max(1.0, np.max(np.abs(bn)))
+    # each folded weight is the nearest fp16 value of the exact product
+    s = gamma.astype(np.float64) / np.sqrt(var.astype(np.float64) + eps)
+    assert np.array_equal(Wf, f16_bits(W * s[:, None, None, None]))
+
+
+def test_fold_batchnorm_layouts_agree(oracle_mod):
+    # [Co][K] filters and [K][Co] row-major GEMM weights fold per output channel alike
+    rng = np.random.default_rng(42)
+    W = f16_bits(rng.normal(0, 1, (5, 12)))
+    gamma, beta, mean, var = (rng.uniform(0.5, 1.5, 5).astype(np.float32) for _ in range(4))
+    Wa, ba = oracle_mod.fold_batchnorm("f16", W, None, gamma, beta, mean, var, 1e-3)
+    Wb, bb = oracle_mod.fold_batchnorm("f16", np.ascontiguousarray(W.T), None, gamma, beta, mean,
+                                       var, 1e-3, out_inner=True)
+    assert np.array_equal(Wa, Wb.T) and np.array_equal(ba, bb)
+    assert np.array_equal(oracle_mod.decode("f16", ba), oracle_mod.decode(
+        "f16", f16_bits(-mean.astype(np.float64) * gamma / np.sqrt(var.astype(np.float64) + 1e-3)
+                        + beta)))
 
 
 # ------------------------------------------------------------------------------------
