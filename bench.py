@@ -202,11 +202,17 @@ def conv_runner(w: wl.ConvChain, dev):
 
     def fused(i):
         x, y, _ = sets[i % n]
-        ops.b2b_conv_nhwc(x, W0, b0, W1, b1, w.pad, w.act0, w.act1, out=y)
+        if w.stride == 1:
+            ops.b2b_conv_nhwc(x, W0, b0, W1, b1, w.pad, w.act0, w.act1, out=y)
+        else:
+            ops.b2b_conv_nhwc_strided(x, W0, b0, W1, b1, w.pad, w.stride, w.act0, w.act1, out=y)
 
     def unfused(i):
         x, y, h = sets[i % n]
-        ops.conv_bias_act_nhwc(x, W0, b0, w.pad, w.act0, out=h)
+        if w.stride == 1:
+            ops.conv_bias_act_nhwc(x, W0, b0, w.pad, w.act0, out=h)
+        else:
+            ops.conv_bias_act_nhwc_strided(x, W0, b0, w.pad, w.stride, w.act0, out=h)
         ops.conv_bias_act_nhwc(h, W1_as_conv, b1, 0, w.act1, out=y)
 
     return fused, unfused, n, set_bytes

@@ -102,6 +102,7 @@ struct MapKey {
   uint64_t dims[4];
   uint64_t strides[3];
   uint32_t box[4];
+  uint32_t elem_strides[4];
   bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 struct MapKeyHash {
@@ -116,10 +117,13 @@ std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
 // A tiled, 128B-swizzled map with zero fill outside the tensor.  dims[0] is the
-// contiguous dimension; strides are in bytes for dims 1..rank-1.
+// contiguous dimension; strides are in bytes for dims 1..rank-1.  elem_strides: the box
+// takes every elem_strides[i]-th element along dimension i (box[i] / elem_strides[i] of
+// them land in shared memory).
 bool make_map(CUtensorMap* out, const void* ptr, int is_bf16, uint32_t rank,
               std::initializer_list<uint64_t> dims, std::initializer_list<uint64_t> strides,
-              std::initializer_list<uint32_t> box) {
+              std::initializer_list<uint32_t> box,
+              std::initializer_list<uint32_t> elem_strides = {1, 1, 1, 1}) {
   MapKey key;
   std::memset(&key, 0, sizeof(key));
   key.ptr = ptr;
@@ -128,6 +132,7 @@ bool make_map(CUtensorMap* out, const void* ptr, int is_bf16, uint32_t rank,
   std::copy(dims.begin(), dims.end(), key.dims);
   std::copy(strides.begin(), strides.end(), key.strides);
   std::copy(box.begin(), box.end(), key.box);
+  std::copy(elem_strides.begin(), elem_strides.end(), key.elem_strides);
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_maps.find(key);
@@ -143,6 +148,7 @@ bool make_map(CUtensorMap* out, const void* ptr, int is_bf16, uint32_t rank,
   for (uint32_t i = 0; i < rank; ++i) {
     gdim[i] = key.dims[i];
     bdim[i] = key.box[i];
+    estride[i] = key.elem_strides[i] != 0 ? key.elem_strides[i] : 1u;
   }
   for (uint32_t i = 0; i + 1 < rank; ++i) gstride[i] = key.strides[i];
   CUtensorMap m;
@@ -272,8 +278,9 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
       const Cand& k = cands[c];
       // Resident filters of an R > 1 conv: one halo box of (8 + R - 1) x 16 pixels per
       // column tap and channel block feeds all R row taps.
-      const uint32_t a_bytes = (k.resident && p.R > 1) ? (7u + static_cast<uint32_t>(p.R)) * 2048u
-                                                       : kABytes;
+      const uint32_t a_bytes = (k.resident && p.R > 1 && p.stride == 1)
+                                   ? (7u + static_cast<uint32_t>(p.R)) * 2048u
+                                   : kABytes;
       const uint32_t stage_bytes =
           k.resident ? a_bytes
                      : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
@@ -310,7 +317,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.p_tmem = k.p_tmem;
   p.num_stages = chosen_stages;
   p.stage_bytes = chosen_stage_bytes;
-  p.halo = (k.resident && p.R > 1) ? 1 : 0;
+  p.halo = (k.resident && p.R > 1 && p.stride == 1) ? 1 : 0;
   p.a_stage_bytes = p.halo ? (7u + static_cast<uint32_t>(p.R)) * 2048u : kABytes;
   p.kstages0 = p.halo ? p.S * p.kc_per_tap : p.kchunks0;
   p.tmem_cols = tmem_layout(p, mode, static_cast<uint32_t>(k.dual), k.p_tmem != 0);
@@ -414,13 +421,14 @@ bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int
   p.kc_per_tap = p.kchunks0;
   p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
   p.num_tiles = ceil_div(M, kBlockM);
+  p.stride = 1;
   return plan_smem(p, mode, w_mn, w_mn, smem, regions, forced);
 }
 
 // 4-D implicit-GEMM A operand (conv filters [Cout][R][S][Cin]).
 bool conv_params(ChainParams& p, int mode, int32_t N, int32_t H, int32_t W, int32_t C,
                  int32_t C0, int32_t R, int32_t S, int32_t pad, int32_t C1, size_t* smem,
-                 Regions* regions, int forced = -1) {
+                 Regions* regions, int forced = -1, int32_t stride = 1) {
   std::memset(&p, 0, sizeof(p));
   p.K0 = C;
   p.N0 = C0;
@@ -433,8 +441,9 @@ bool conv_params(ChainParams& p, int mode, int32_t N, int32_t H, int32_t W, int3
   p.R = R;
   p.S = S;
   p.pad = pad;
-  p.Ho = H + 2 * pad - R + 1;
-  p.Wo = W + 2 * pad - S + 1;
+  p.stride = stride;
+  p.Ho = (H + 2 * pad - R) / stride + 1;
+  p.Wo = (W + 2 * pad - S) / stride + 1;
   p.tiles_w = ceil_div(p.Wo, 16);
   p.tiles_h = ceil_div(p.Ho, 8);
   const int64_t tiles = static_cast<int64_t>(N) * p.tiles_w * p.tiles_h;
@@ -566,13 +575,13 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
 // ------------------------------------------------------------------------------------
 b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t N, int32_t H,
                          int32_t W, int32_t C, const void* x, const void* W0, int32_t C0,
-                         int32_t R, int32_t S, int32_t pad, const void* b0, int e0,
+                         int32_t R, int32_t S, int32_t pad, int32_t stride, const void* b0, int e0,
                          const void* W1, int32_t C1, const void* b1, int e1, void* y,
                          void* stream, uint32_t kid) {
   ChainParams p;
   size_t smem = 0;
   Regions r;
-  if (!conv_params(p, mode, N, H, W, C, C0, R, S, pad, C1, &smem, &r, ch.cand))
+  if (!conv_params(p, mode, N, H, W, C, C0, R, S, pad, C1, &smem, &r, ch.cand, stride))
     return B2B_ERR_UNSUPPORTED;
   b2b_status st = B2B_OK;
   DeviceState* d = device_state(&st);
@@ -585,11 +594,16 @@ b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t
 
   const uint64_t e = 2;
   CUtensorMap ta, tw0, tw1, to;
+  // One box per (tap, channel block): 8 x 16 output pixels, i.e. input pixels `stride`
+  // apart (the box spans 8 * stride x 16 * stride pixels and takes every stride-th); halo
+  // boxes (stride 1, resident filters) take 8 + R - 1 rows for all row taps.
+  const uint32_t sd = static_cast<uint32_t>(stride);
   bool ok = make_map(&ta, x, p.is_bf16, 4,
                      {static_cast<uint64_t>(C), static_cast<uint64_t>(W), static_cast<uint64_t>(H),
                       static_cast<uint64_t>(N)},
                      {C * e, static_cast<uint64_t>(W) * C * e, static_cast<uint64_t>(H) * W * C * e},
-                     {kChunkK, 16, static_cast<uint32_t>(p.halo ? 8 + R - 1 : 8), 1});
+                     {kChunkK, 16 * sd, static_cast<uint32_t>(p.halo ? 8 + R - 1 : 8 * sd), 1},
+                     {1, sd, sd, 1});
   ok = ok && make_map(&tw0, W0, p.is_bf16, 3,
                       {static_cast<uint64_t>(C), static_cast<uint64_t>(R) * S, static_cast<uint64_t>(C0)},
                       {C * e, static_cast<uint64_t>(R) * S * C * e},
@@ -755,11 +769,11 @@ b2b_status run_gemm(const TuneKey& key, int mode, bool w_mn, int dt, int64_t M, 
 
 b2b_status run_conv(const TuneKey& key, int mode, int dt, int32_t N, int32_t H, int32_t W,
                     int32_t C, const void* x, const void* W0, int32_t C0, int32_t R, int32_t S,
-                    int32_t pad, const void* b0, int e0, const void* W1, int32_t C1,
-                    const void* b1, int e1, void* y, void* stream, uint32_t kid) {
+                    int32_t pad, int32_t stride, const void* b0, int e0, const void* W1,
+                    int32_t C1, const void* b1, int e1, void* y, void* stream, uint32_t kid) {
   return dispatch(key, stream, [&](const Choice& c, Info* info) {
-    return run_conv_with(c, info, mode, dt, N, H, W, C, x, W0, C0, R, S, pad, b0, e0, W1, C1, b1,
-                         e1, y, stream, kid);
+    return run_conv_with(c, info, mode, dt, N, H, W, C, x, W0, C0, R, S, pad, stride, b0, e0, W1,
+                         C1, b1, e1, y, stream, kid);
   });
 }
 
@@ -815,13 +829,13 @@ b2b_status gemm_bias_act(b2b_dtype dt, int64_t M, int32_t K, int32_t N, const vo
 }
 
 static b2b_status check_conv_args(int32_t N, int32_t H, int32_t W, int32_t C, int32_t Co,
-                                  int32_t R, int32_t S, int32_t pad) {
+                                  int32_t R, int32_t S, int32_t pad, int32_t stride = 1) {
   if (N < 0 || H < 0 || W < 0) return B2B_ERR_SHAPE;
   b2b_status st;
   if ((st = check_channels(C, kMaxReduction)) != B2B_OK) return st;
   if ((st = check_channels(Co, 256)) != B2B_OK) return st;
-  if (R < 1 || S < 1 || pad < 0) return B2B_ERR_SHAPE;
-  if (R > 7 || S > 7 || pad > 3) return B2B_ERR_UNSUPPORTED;
+  if (R < 1 || S < 1 || pad < 0 || stride < 1) return B2B_ERR_SHAPE;
+  if (R > 7 || S > 7 || pad > 3 || stride > 4) return B2B_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(R) * S * ((C + 63) / 64) > 4096) return B2B_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(N) * H * W > 0) {
     if (H + 2 * pad - R + 1 < 1 || W + 2 * pad - S + 1 < 1) return B2B_ERR_SHAPE;
@@ -830,48 +844,66 @@ static b2b_status check_conv_args(int32_t N, int32_t H, int32_t W, int32_t C, in
   return B2B_OK;
 }
 
-b2b_status b2b_conv_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C, const void* x,
-                         const void* W0, int32_t C0, int32_t R, int32_t S, int32_t pad,
-                         const void* b0, b2b_epilogue e0, const void* W1, int32_t C1,
-                         const void* b1, b2b_epilogue e1, void* y, void* stream) {
+b2b_status b2b_conv_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                                 const void* x, const void* W0, int32_t C0, int32_t R, int32_t S,
+                                 int32_t pad, int32_t stride, const void* b0, b2b_epilogue e0,
+                                 const void* W1, int32_t C1, const void* b1, b2b_epilogue e1,
+                                 void* y, void* stream) {
   if (!valid_dtype(dt) || !valid_epi(e0) || !valid_epi(e1)) return B2B_ERR_UNSUPPORTED;
-  b2b_status st = check_conv_args(N, H, W, C, C0, R, S, pad);
+  b2b_status st = check_conv_args(N, H, W, C, C0, R, S, pad, stride);
   if (st != B2B_OK) return st;
   if ((st = check_channels(C1, 256)) != B2B_OK) return st;
   if (static_cast<int64_t>(N) * H * W == 0) return B2B_OK;
   if (!x || !W0 || !W1 || !y) return B2B_ERR_NULL;
   if (!aligned16(x) || !aligned16(W0) || !aligned16(W1) || !aligned16(y)) return B2B_ERR_ALIGN;
   if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1))) return B2B_ERR_ALIGN;
-  if (R == 1 && S == 1 && pad == 0) {
+  const TuneKey key{2, N, H, W, C, C0, R, S, pad, C1, stride};
+  if (R == 1 && S == 1 && pad == 0 && stride == 1) {
     // A 1x1 conv is a GEMM over the N*H*W pixel rows (interview notes, "Conv
     // optimisation", item 5): run the GEMM-shaped kernel with K-major filters.
     const int64_t M = static_cast<int64_t>(N) * H * W;
     if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
-    return run_gemm({2, N, H, W, C, C0, R, S, pad, C1}, MODE_CHAIN, false, dt, M, C, C0, C1, x, W0,
-                    b0, e0, W1, b1, e1, y, stream, KID_CONV1X1_CHAIN);
+    return run_gemm(key, MODE_CHAIN, false, dt, M, C, C0, C1, x, W0, b0, e0, W1, b1, e1, y, stream,
+                    KID_CONV1X1_CHAIN);
   }
-  return run_conv({2, N, H, W, C, C0, R, S, pad, C1}, MODE_CHAIN, dt, N, H, W, C, x, W0, C0, R, S,
-                  pad, b0, e0, W1, C1, b1, e1, y, stream, KID_CONV_CHAIN);
+  return run_conv(key, MODE_CHAIN, dt, N, H, W, C, x, W0, C0, R, S, pad, stride, b0, e0, W1, C1, b1,
+                  e1, y, stream, KID_CONV_CHAIN);
 }
 
-b2b_status conv_bias_act_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
-                              const void* x, const void* Wt, int32_t Co, int32_t R, int32_t S,
-                              int32_t pad, const void* b, b2b_epilogue e, void* y, void* stream) {
+b2b_status b2b_conv_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C, const void* x,
+                         const void* W0, int32_t C0, int32_t R, int32_t S, int32_t pad,
+                         const void* b0, b2b_epilogue e0, const void* W1, int32_t C1,
+                         const void* b1, b2b_epilogue e1, void* y, void* stream) {
+  return b2b_conv_nhwc_strided(dt, N, H, W, C, x, W0, C0, R, S, pad, 1, b0, e0, W1, C1, b1, e1, y,
+                               stream);
+}
+
+b2b_status conv_bias_act_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                                      const void* x, const void* Wt, int32_t Co, int32_t R,
+                                      int32_t S, int32_t pad, int32_t stride, const void* b,
+                                      b2b_epilogue e, void* y, void* stream) {
   if (!valid_dtype(dt) || !valid_epi(e)) return B2B_ERR_UNSUPPORTED;
-  b2b_status st = check_conv_args(N, H, W, C, Co, R, S, pad);
+  b2b_status st = check_conv_args(N, H, W, C, Co, R, S, pad, stride);
   if (st != B2B_OK) return st;
   if (static_cast<int64_t>(N) * H * W == 0) return B2B_OK;
   if (!x || !Wt || !y) return B2B_ERR_NULL;
   if (!aligned16(x) || !aligned16(Wt) || !aligned16(y)) return B2B_ERR_ALIGN;
   if (b && !aligned2(b)) return B2B_ERR_ALIGN;
-  if (R == 1 && S == 1 && pad == 0) {
+  const TuneKey key{3, N, H, W, C, Co, R, S, pad, stride};
+  if (R == 1 && S == 1 && pad == 0 && stride == 1) {
     const int64_t M = static_cast<int64_t>(N) * H * W;
     if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
-    return run_gemm({3, N, H, W, C, Co, R, S, pad}, MODE_SINGLE, false, dt, M, C, Co, 0, x, Wt, b,
-                    e, nullptr, nullptr, 0, y, stream, KID_CONV1X1_SINGLE);
+    return run_gemm(key, MODE_SINGLE, false, dt, M, C, Co, 0, x, Wt, b, e, nullptr, nullptr, 0, y,
+                    stream, KID_CONV1X1_SINGLE);
   }
-  return run_conv({3, N, H, W, C, Co, R, S, pad}, MODE_SINGLE, dt, N, H, W, C, x, Wt, Co, R, S,
-                  pad, b, e, nullptr, 0, nullptr, 0, y, stream, KID_CONV_SINGLE);
+  return run_conv(key, MODE_SINGLE, dt, N, H, W, C, x, Wt, Co, R, S, pad, stride, b, e, nullptr, 0,
+                  nullptr, 0, y, stream, KID_CONV_SINGLE);
+}
+
+b2b_status conv_bias_act_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                              const void* x, const void* Wt, int32_t Co, int32_t R, int32_t S,
+                              int32_t pad, const void* b, b2b_epilogue e, void* y, void* stream) {
+  return conv_bias_act_nhwc_strided(dt, N, H, W, C, x, Wt, Co, R, S, pad, 1, b, e, y, stream);
 }
 
 b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t Cin,
@@ -886,7 +918,7 @@ b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int3
   if (!x || !Wt || !y) return B2B_ERR_NULL;
   if (!aligned16(x) || !aligned16(Wt) || !aligned16(y)) return B2B_ERR_ALIGN;
   if (b && !aligned2(b)) return B2B_ERR_ALIGN;
-  return run_conv({4, N, H, W, Cin, Cout}, MODE_POOL, dt, N, H, W, Cin, x, Wt, Cout, 3, 3, 1, b,
+  return run_conv({4, N, H, W, Cin, Cout}, MODE_POOL, dt, N, H, W, Cin, x, Wt, Cout, 3, 3, 1, 1, b,
                   B2B_EPI_RELU, nullptr, 0, nullptr, 0, y, stream, KID_CONV_POOL);
 }
 
@@ -965,25 +997,34 @@ b2b_status b2b_get_device_error(uint32_t info[4]) {
 // Sizes an entry point takes, per kind (b2b_debug_plan's numbering).
 static const int32_t kPlanDims[5] = {4, 3, 9, 8, 5};
 
+// The convs (kinds 2 and 3) take an optional stride after their sizes (default 1).
+static int64_t plan_stride(int32_t kind, const int64_t* dims, int32_t ndims) {
+  return ((kind == 2 || kind == 3) && ndims > kPlanDims[kind]) ? dims[kPlanDims[kind]] : 1;
+}
+
 static b2b_status check_plan_args(int32_t kind, const int64_t* dims, int32_t ndims) {
   if (kind < 0 || kind > 4) return B2B_ERR_UNSUPPORTED;
   if (dims == nullptr) return B2B_ERR_NULL;
   if (ndims < kPlanDims[kind]) return B2B_ERR_SHAPE;
   for (int i = 0; i < kPlanDims[kind]; ++i)
     if (dims[i] < 0 || dims[i] > INT32_MAX) return B2B_ERR_SHAPE;
+  const int64_t st = plan_stride(kind, dims, ndims);
+  if (st < 1 || st > INT32_MAX) return B2B_ERR_SHAPE;
   return B2B_OK;
 }
 
-static TuneKey plan_key(int32_t kind, const int64_t* dims) {
+// The key the entry point files its launch choice under (the convs' with their stride).
+static TuneKey plan_key(int32_t kind, const int64_t* dims, int32_t ndims) {
   TuneKey k{kind};
   k.insert(k.end(), dims, dims + kPlanDims[kind]);
+  if (kind == 2 || kind == 3) k.push_back(plan_stride(kind, dims, ndims));
   return k;
 }
 
 // The launch plan entry point `kind` makes for `dims` with layout candidate `forced`
 // (-1: the planner's default); validated like the entry point itself.
-static b2b_status plan_for_kind(int32_t kind, const int64_t* dims, int forced, ChainParams& p,
-                                Regions& r, size_t& smem, int32_t& mode) {
+static b2b_status plan_for_kind(int32_t kind, const int64_t* dims, int32_t ndims, int forced,
+                                ChainParams& p, Regions& r, size_t& smem, int32_t& mode) {
   const int32_t d0 = static_cast<int32_t>(dims[0]), d1 = static_cast<int32_t>(dims[1]),
                 d2 = static_cast<int32_t>(dims[2]), d3 = static_cast<int32_t>(dims[3]);
   bool ok = false;
@@ -1007,14 +1048,15 @@ static b2b_status plan_for_kind(int32_t kind, const int64_t* dims, int forced, C
       const int32_t C0 = static_cast<int32_t>(dims[4]), R = static_cast<int32_t>(dims[5]),
                     S = static_cast<int32_t>(dims[6]), pad = static_cast<int32_t>(dims[7]);
       const int32_t C1 = kind == 2 ? static_cast<int32_t>(dims[8]) : 0;
-      if ((st = check_conv_args(d0, d1, d2, d3, C0, R, S, pad)) != B2B_OK) return st;
+      const int32_t stride = static_cast<int32_t>(plan_stride(kind, dims, ndims));
+      if ((st = check_conv_args(d0, d1, d2, d3, C0, R, S, pad, stride)) != B2B_OK) return st;
       if (kind == 2 && (st = check_channels(C1, 256)) != B2B_OK) return st;
       mode = kind == 2 ? MODE_CHAIN : MODE_SINGLE;
-      if (R == 1 && S == 1 && pad == 0)
+      if (R == 1 && S == 1 && pad == 0 && stride == 1)
         ok = gemm_params(p, mode, false, static_cast<int64_t>(d0) * d1 * d2, d3, C0, C1, &smem, &r,
                          forced);
       else
-        ok = conv_params(p, mode, d0, d1, d2, d3, C0, R, S, pad, C1, &smem, &r, forced);
+        ok = conv_params(p, mode, d0, d1, d2, d3, C0, R, S, pad, C1, &smem, &r, forced, stride);
       break;
     }
     case 4: { // conv_relu_maxpool: N, H, W, Cin, Cout
@@ -1036,12 +1078,12 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   if (out == nullptr) return B2B_ERR_NULL;
   if (out_len < 51) return B2B_ERR_SHAPE;
   Choice c;
-  find_choice(plan_key(kind, dims), &c);
+  find_choice(plan_key(kind, dims, ndims), &c);
   ChainParams p;
   Regions r;
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
-  if ((st = plan_for_kind(kind, dims, c.cand, p, r, smem, mode)) != B2B_OK) return st;
+  if ((st = plan_for_kind(kind, dims, ndims, c.cand, p, r, smem, mode)) != B2B_OK) return st;
   const uint32_t v[51] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
@@ -1072,9 +1114,9 @@ b2b_status b2b_set_choice(int32_t kind, const int64_t* dims, int32_t ndims, int3
   Regions r;
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
-  if ((st = plan_for_kind(kind, dims, cand, p, r, smem, mode)) != B2B_OK) return st;
+  if ((st = plan_for_kind(kind, dims, ndims, cand, p, r, smem, mode)) != B2B_OK) return st;
   std::lock_guard<std::mutex> lk(g_tune_mu);
-  Tuned& t = g_tuned[plan_key(kind, dims)];
+  Tuned& t = g_tuned[plan_key(kind, dims, ndims)];
   t = Tuned{};
   t.c = Choice{cand, grid, prefetch_second};
   t.source = 1;
@@ -1090,7 +1132,7 @@ b2b_status b2b_get_choice(int32_t kind, const int64_t* dims, int32_t ndims, int3
   Tuned t;
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
-    const auto it = g_tuned.find(plan_key(kind, dims));
+    const auto it = g_tuned.find(plan_key(kind, dims, ndims));
     if (it != g_tuned.end()) t = it->second;
   }
   const int32_t v[7] = {t.source, t.c.cand, t.c.grid, t.c.pf2, static_cast<int32_t>(t.best_ns),

@@ -162,8 +162,10 @@ __device__ __forceinline__ void load_a_chunk(uint32_t lead, const ChainParams& p
                                              const TileCoord& tc, const KPos& k, uint32_t bar,
                                              uint64_t pol) {
   if constexpr (A4D) {
-    tma_load_4d(lead, dst, tmA, bar, k.cb * kChunkK, tc.wo0 + k.s - p.pad, tc.ho0 + k.r - p.pad,
-                tc.n, pol);
+    // output pixel (ho, wo) reads input (stride * ho + r - pad, stride * wo + s - pad); the
+    // map's element strides make the box take every stride-th pixel
+    tma_load_4d(lead, dst, tmA, bar, k.cb * kChunkK, tc.wo0 * p.stride + k.s - p.pad,
+                tc.ho0 * p.stride + k.r - p.pad, tc.n, pol);
   } else {
     tma_load_2d(lead, dst, tmA, bar, k.cb * kChunkK, tc.m0, pol);
   }

@@ -91,6 +91,7 @@ struct ChainParams {
   uint32_t a_stage_bytes;   // A bytes per ring stage (16 KiB; halo: (8 + R - 1) * 2 KiB)
   int32_t kchunks1;     // 64-wide K chunks of GEMM1 (= ceil(N0p / 64))
   int32_t R, S, pad;    // 4D filter
+  int32_t stride;       // 4D: spatial stride of the first conv (halo loads only at 1)
   int32_t Ho, Wo;       // 4D output spatial size (before pooling)
   int32_t tiles_w, tiles_h;  // 4D tiling: 16 output columns x 8 output rows per tile
   int32_t num_tiles;

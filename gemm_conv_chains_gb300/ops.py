@@ -70,6 +70,12 @@ def lib() -> ctypes.CDLL:
         L.b2b_set_trace.argtypes = [vp, ctypes.c_uint32, ctypes.c_uint32]
         L.b2b_set_trace.restype = ci
         p64 = ctypes.POINTER(i64)
+        L.b2b_conv_nhwc_strided.argtypes = [ci, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32,
+                                            i32, vp, ci, vp, i32, vp, ci, vp, vp]
+        L.b2b_conv_nhwc_strided.restype = ci
+        L.conv_bias_act_nhwc_strided.argtypes = [ci, i32, i32, i32, i32, vp, vp, i32, i32, i32,
+                                                 i32, i32, vp, ci, vp, vp]
+        L.conv_bias_act_nhwc_strided.restype = ci
         L.b2b_set_autotune.argtypes = [i32]
         L.b2b_set_autotune.restype = None
         L.b2b_autotune_reset.argtypes = []
@@ -157,9 +163,24 @@ def b2b_gemm(A, W0, b0, W1, b1, epi0="relu", epi1="relu", out=None, stream=None)
     return out
 
 
+def _conv_out(n, pad, k, stride):
+    return 0 if n + 2 * pad < k else (n + 2 * pad - k) // stride + 1
+
+
 def b2b_conv_nhwc(x, W0, b0, W1, b1, pad=1, epi0="relu", epi1="relu", out=None, stream=None):
     """out = conv1x1(conv_RxS(x) + b0 -> epi0) + b1 -> epi1, NHWC, stride 1, one launch.
     x [N,H,W,C], W0 [C0,R,S,C], W1 [C1,C0] -> out [N,Ho,Wo,C1]."""
+    return _b2b_conv(x, W0, b0, W1, b1, pad, 1, epi0, epi1, out, stream)
+
+
+def b2b_conv_nhwc_strided(x, W0, b0, W1, b1, pad=1, stride=2, epi0="relu", epi1="relu",
+                          out=None, stream=None):
+    """b2b_conv_nhwc with the first conv at spatial stride `stride` (1..4):
+    out [N, (H+2pad-R)//stride+1, (W+2pad-S)//stride+1, C1]."""
+    return _b2b_conv(x, W0, b0, W1, b1, pad, stride, epi0, epi1, out, stream)
+
+
+def _b2b_conv(x, W0, b0, W1, b1, pad, stride, epi0, epi1, out, stream):
     dt = x.dtype
     N, H, W, C = x.shape
     C0, R, S = W0.shape[0], W0.shape[1], W0.shape[2]
@@ -171,13 +192,19 @@ def b2b_conv_nhwc(x, W0, b0, W1, b1, pad=1, epi0="relu", epi1="relu", out=None, 
         _check_tensor(b0, "b0", dt, (C0,))
     if b1 is not None:
         _check_tensor(b1, "b1", dt, (C1,))
-    Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
+    Ho, Wo = _conv_out(H, pad, R, stride), _conv_out(W, pad, S, stride)
     if out is None:
-        out = torch.empty((N, max(Ho, 0), max(Wo, 0), C1), dtype=dt, device=x.device)
-    _check_tensor(out, "out", dt, (N, max(Ho, 0), max(Wo, 0), C1))
-    _raise(lib().b2b_conv_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(W0), C0, R, S, pad,
-                               _ptr(b0), _epi(epi0), _ptr(W1), C1, _ptr(b1), _epi(epi1),
-                               _ptr(out), _stream(stream)), "b2b_conv_nhwc")
+        out = torch.empty((N, Ho, Wo, C1), dtype=dt, device=x.device)
+    _check_tensor(out, "out", dt, (N, Ho, Wo, C1))
+    if stride == 1:
+        _raise(lib().b2b_conv_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(W0), C0, R, S, pad,
+                                   _ptr(b0), _epi(epi0), _ptr(W1), C1, _ptr(b1), _epi(epi1),
+                                   _ptr(out), _stream(stream)), "b2b_conv_nhwc")
+    else:
+        _raise(lib().b2b_conv_nhwc_strided(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(W0), C0, R, S,
+                                           pad, stride, _ptr(b0), _epi(epi0), _ptr(W1), C1,
+                                           _ptr(b1), _epi(epi1), _ptr(out), _stream(stream)),
+               "b2b_conv_nhwc_strided")
     return out
 
 
@@ -222,6 +249,15 @@ def gemm_bias_act(A, W, b, epi="relu", out=None, stream=None):
 
 def conv_bias_act_nhwc(x, Wt, b, pad=1, epi="relu", out=None, stream=None):
     """out = epi(conv_RxS(x, Wt) + b); x [N,H,W,C], Wt [Co,R,S,C] -> [N,Ho,Wo,Co]."""
+    return _conv_single(x, Wt, b, pad, 1, epi, out, stream)
+
+
+def conv_bias_act_nhwc_strided(x, Wt, b, pad=1, stride=2, epi="relu", out=None, stream=None):
+    """conv_bias_act_nhwc at spatial stride `stride` (1..4)."""
+    return _conv_single(x, Wt, b, pad, stride, epi, out, stream)
+
+
+def _conv_single(x, Wt, b, pad, stride, epi, out, stream):
     dt = x.dtype
     N, H, W, C = x.shape
     Co, R, S = Wt.shape[0], Wt.shape[1], Wt.shape[2]
@@ -229,13 +265,18 @@ def conv_bias_act_nhwc(x, Wt, b, pad=1, epi="relu", out=None, stream=None):
     _check_tensor(Wt, "Wt", dt, (Co, R, S, C))
     if b is not None:
         _check_tensor(b, "b", dt, (Co,))
-    Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
+    Ho, Wo = _conv_out(H, pad, R, stride), _conv_out(W, pad, S, stride)
     if out is None:
-        out = torch.empty((N, max(Ho, 0), max(Wo, 0), Co), dtype=dt, device=x.device)
-    _check_tensor(out, "out", dt, (N, max(Ho, 0), max(Wo, 0), Co))
-    _raise(lib().conv_bias_act_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(Wt), Co, R, S, pad,
-                                    _ptr(b), _epi(epi), _ptr(out), _stream(stream)),
-           "conv_bias_act_nhwc")
+        out = torch.empty((N, Ho, Wo, Co), dtype=dt, device=x.device)
+    _check_tensor(out, "out", dt, (N, Ho, Wo, Co))
+    if stride == 1:
+        _raise(lib().conv_bias_act_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(Wt), Co, R, S,
+                                        pad, _ptr(b), _epi(epi), _ptr(out), _stream(stream)),
+               "conv_bias_act_nhwc")
+    else:
+        _raise(lib().conv_bias_act_nhwc_strided(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(Wt), Co,
+                                                R, S, pad, stride, _ptr(b), _epi(epi), _ptr(out),
+                                                _stream(stream)), "conv_bias_act_nhwc_strided")
     return out
 
 

@@ -43,8 +43,9 @@ def propagate(w) -> TileGraph:
     """Every operand tile of the chain from its output tile.
 
     b2b GEMM: out (128, N1) <- P (128, N0), W1 (N0, N1) <- A (128, K0), W0 (K0, N0).
-    Conv chain: out (8, 16, C1) <- P (8, 16, C0), W1 (C1, C0) <- x (8+R-1, 16+S-1, C),
-    W0 (C0, R, S, C).  Conv + pool: pooled (4, 8, F) <- conv out (8, 16, F) (the (2,2,F)
+    Conv chain: out (8, 16, C1) <- P (8, 16, C0), W1 (C1, C0) <- x (7 st + R, 15 st + S, C)
+    (the region an 8 x 16 output tile reads at stride st, an upper bound: every st-th pixel
+    of it is used), W0 (C0, R, S, C).  Conv + pool: pooled (4, 8, F) <- conv out (8, 16, F) (the (2,2,F)
     reuse tile per pooled pixel) <- x (10, 18, C), W (F, 3, 3, C)."""
     if isinstance(w, wl.GemmChain):
         return TileGraph("gemm_chain", {"out": (TILE_M, w.N1), "P": (TILE_M, w.N0),
@@ -53,7 +54,8 @@ def propagate(w) -> TileGraph:
     if isinstance(w, wl.ConvChain):
         return TileGraph("conv_chain", {"out": (TILE_H, TILE_W, w.C1),
                                         "P": (TILE_H, TILE_W, w.C0), "W1": (w.C1, w.C0),
-                                        "x": (TILE_H + w.R - 1, TILE_W + w.S - 1, w.C),
+                                        "x": ((TILE_H - 1) * w.stride + w.R,
+                                              (TILE_W - 1) * w.stride + w.S, w.C),
                                         "W0": (w.C0, w.R, w.S, w.C)})
     if isinstance(w, wl.ConvPool):
         return TileGraph("conv_pool", {"out": (TILE_H // 2, TILE_W // 2, w.Cout),
@@ -79,7 +81,8 @@ def plan_of(w) -> dict:
     if isinstance(w, wl.GemmChain):
         return ops.debug_plan("b2b_gemm", (w.M, w.K0, w.N0, w.N1))
     if isinstance(w, wl.ConvChain):
-        return ops.debug_plan("b2b_conv_nhwc", (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1))
+        return ops.debug_plan("b2b_conv_nhwc", (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1,
+                                                w.stride))
     return ops.debug_plan("conv_relu_maxpool", (w.N, w.H, w.W, w.Cin, w.Cout))
 
 
@@ -94,11 +97,19 @@ def _overlap(lo: int, n: int, extent: int) -> int:
     return max(0, min(lo + n, extent) - max(lo, 0))
 
 
-def _conv_tile_input_bytes(N, H, W, C, R, S, pad, halo: bool) -> int:
+def _strided_overlap(lo: int, n: int, step: int, extent: int) -> int:
+    """How many of lo, lo + step, ..., lo + (n - 1) step lie in [0, extent)."""
+    if step == 1:
+        return _overlap(lo, n, extent)
+    return sum(1 for i in range(n) if 0 <= lo + i * step < extent)
+
+
+def _conv_tile_input_bytes(N, H, W, C, R, S, pad, halo: bool, stride: int = 1) -> int:
     """Input bytes inside the image that all tiles of an RxS conv (8 x 16 output tiles)
     read: one box of (8 + R - 1) x 16 pixels per column tap with halo loads, else one
-    8 x 16 box per tap, each clipped to the image (the useful part of the boxes)."""
-    Ho, Wo = H + 2 * pad - R + 1, W + 2 * pad - S + 1
+    8 x 16 box per tap (pixels `stride` apart), each clipped to the image (the useful part
+    of the boxes)."""
+    Ho, Wo = (H + 2 * pad - R) // stride + 1, (W + 2 * pad - S) // stride + 1
     tiles_h, tiles_w = -(-Ho // TILE_H), -(-Wo // TILE_W)
     rows_per_box = TILE_H + R - 1 if halo else TILE_H
     row_offsets = [0] if halo else list(range(R))
@@ -106,9 +117,9 @@ def _conv_tile_input_bytes(N, H, W, C, R, S, pad, halo: bool) -> int:
     for th in range(tiles_h):
         for tw in range(tiles_w):
             for s in range(S):
-                cols = _overlap(tw * TILE_W + s - pad, TILE_W, W)
+                cols = _strided_overlap(tw * TILE_W * stride + s - pad, TILE_W, stride, W)
                 for r in row_offsets:
-                    rows = _overlap(th * TILE_H + r - pad, rows_per_box, H)
+                    rows = _strided_overlap(th * TILE_H * stride + r - pad, rows_per_box, stride, H)
                     total += rows * cols
     return N * total * C * ELEM
 
@@ -154,8 +165,9 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
         useful = w.M * w.K0 * ELEM
     elif isinstance(w, wl.ConvChain):
         out["bias"] = ctas * (w.C0 + w.C1) * ELEM
-        useful = (w.N * w.H * w.W * w.C * ELEM if (w.R, w.S, w.pad) == (1, 1, 0) else
-                  _conv_tile_input_bytes(w.N, w.H, w.W, w.C, w.R, w.S, w.pad, bool(plan["halo"])))
+        useful = (w.N * w.H * w.W * w.C * ELEM if (w.R, w.S, w.pad, w.stride) == (1, 1, 0, 1) else
+                  _conv_tile_input_bytes(w.N, w.H, w.W, w.C, w.R, w.S, w.pad, bool(plan["halo"]),
+                                         w.stride))
     else:
         out["bias"] = ctas * w.Cout * ELEM
         useful = _conv_tile_input_bytes(w.N, w.H, w.W, w.Cin, 3, 3, 1, bool(plan["halo"]))
@@ -200,10 +212,11 @@ def chain_buffers(plan: dict) -> List[Buffer]:
     """Shared-memory buffers of a launch plan, with lifetimes over the steps of one tile:
     0 load, 1 GEMM0, 2 epilogue 0 (writes P), 3 GEMM1 (reads P), 4 epilogue 1 (writes the
     output staging), 5 store.  The ring, resident weights, bias operands and barriers live
-    throughout.  When every P slot belongs to one epilogue group and that group's staging
-    (as many P slots as staging buffers), a slot's P and its staging are used one after
-    the other by the same tiles, so their lifetimes are disjoint; otherwise the tiles in
-    flight keep every buffer live at every step."""
+    throughout.  When the plan lets the output staging reuse the P buffers (`alias`: the
+    epilogue waits for the previous store's reads before it writes P), a slot's P and its
+    staging are used one after the other by the same tiles, so their lifetimes are
+    disjoint; otherwise the tiles in flight (and the TMA store still reading a staging
+    buffer while the next tile's P is written) keep every buffer live at every step."""
     whole = (0, 5)
     bufs = [Buffer("ring", plan["ring"], whole), Buffer("bias", plan["bias"], whole),
             Buffer("bar", plan["bar"], whole)]
@@ -216,7 +229,7 @@ def chain_buffers(plan: dict) -> List[Buffer]:
     per_chunk = 32 * 128 if plan["mode"] == 2 else 128 * 128   # pooled: 4 x 8 pixels per tile
     out_bytes = (out_cols + 63) // 64 * per_chunk
     obufs = 2 if plan["groups"] == 2 else 1
-    paired = pbufs == obufs
+    paired = bool(plan["alias"]) and pbufs == obufs
     for i in range(pbufs):
         bufs.append(Buffer(f"P{i}", p_bytes, (2, 3) if paired else whole))
     for i in range(obufs):

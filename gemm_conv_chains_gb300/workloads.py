@@ -148,8 +148,12 @@ CONV1X1 = ConvChain("conv1x1", "f16", 64, 56, 56, 64, 64, 1, 1, 0, 64, "relu", "
 CONV3X3_1X1 = ConvChain("conv3x3_1x1", "f16", 32, 56, 56, 64, 64, 3, 3, 1, 128,
                         "hardswish", "none")
 CONV_POOL = ConvPool("conv_pool", "f16", 32, 112, 112, 64, 64)
+# A downsampling stage: 3x3 stride 2 conv (56 -> 28, 64 -> 128 channels) + 1x1 (128 -> 128).
+CONV3X3S2_1X1 = ConvChain("conv3x3s2_1x1", "f16", 32, 56, 56, 64, 128, 3, 3, 1, 128, "relu",
+                          "none", stride=2)
 
-WORKLOADS = {w.name: w for w in (GEMM_SMALL, GEMM_FFN, CONV1X1, CONV3X3_1X1, CONV_POOL)}
+WORKLOADS = {w.name: w for w in (GEMM_SMALL, GEMM_FFN, CONV1X1, CONV3X3_1X1, CONV_POOL,
+                                 CONV3X3S2_1X1)}
 FFN_SWEEP_M = [4096, 8192, 16384, 32768, 65536, 131072, 262144]
 
 

@@ -106,6 +106,22 @@ b2b_status b2b_conv_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t 
                          const void* W1, int32_t C1, const void* b1, b2b_epilogue e1,
                          void* y, void* stream);
 
+/* b2b_conv_nhwc with the first conv at spatial stride `stride` in both dimensions (Welder
+ * notes, "Operator-tile and Tile-graph", tile propagation: a strided conv reads a strided
+ * input region, so each output tile's input tile is (8 - 1) * stride + R rows by
+ * (16 - 1) * stride + S columns, of which every stride-th pixel is used):
+ *   h[n,ho,wo,:] = e0( sum_{r,s} x[n, stride*ho + r - pad, stride*wo + s - pad, :] . W0 + b0 )
+ * with Ho = (H + 2 pad - R) / stride + 1, Wo = (W + 2 pad - S) / stride + 1 (floor); the
+ * 1x1 conv that follows has stride 1.  y [N][Ho][Wo][C1].  1 <= stride <= 4
+ * (B2B_ERR_UNSUPPORTED above); other arguments and limits as b2b_conv_nhwc, which is this
+ * call with stride 1.  A strided 1x1 conv (pad 0) runs as an implicit GEMM, not as a GEMM
+ * over the pixel rows. */
+b2b_status b2b_conv_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                                 const void* x, const void* W0, int32_t C0, int32_t R,
+                                 int32_t S, int32_t pad, int32_t stride, const void* b0,
+                                 b2b_epilogue e0, const void* W1, int32_t C1, const void* b1,
+                                 b2b_epilogue e1, void* y, void* stream);
+
 /* y = maxpool2x2_stride2( ReLU( conv3x3_pad1(x, Wt) + b ) ), floor mode
  * (Welder notes, "Tile-graph Scheduling", Figure 5: Conv+ReLU at registers, ReLU->MaxPool
  * through the (2,2,F) reuse tile; the conv output never reaches global memory).
@@ -131,6 +147,13 @@ b2b_status conv_bias_act_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int
                               const void* x, const void* Wt, int32_t Co, int32_t R, int32_t S,
                               int32_t pad, const void* b, b2b_epilogue e,
                               void* y, void* stream);
+
+/* conv_bias_act_nhwc at spatial stride `stride` (1 to 4), as the first conv of
+ * b2b_conv_nhwc_strided. */
+b2b_status conv_bias_act_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
+                                      const void* x, const void* Wt, int32_t Co, int32_t R,
+                                      int32_t S, int32_t pad, int32_t stride, const void* b,
+                                      b2b_epilogue e, void* y, void* stream);
 
 /* y[N,H/2,W/2,C] = max over each 2x2 window (stride 2, floor mode) of x[N,H,W,C].
  * Limits: H, W >= 2; C multiple of 8. */
@@ -179,8 +202,8 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * sizes: its shared-memory plan and TMEM use.  For tests and tuning.
  *   kind 0 b2b_gemm            dims = {M, K0, N0, N1}
  *   kind 1 gemm_bias_act       dims = {M, K, N}
- *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1}
- *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad}
+ *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1[, stride]}
+ *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad[, stride]}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
  * out (out_len >= 51) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,

@@ -34,7 +34,9 @@ def L():
 def test_header_declares_the_entry_points():
     names = header_functions()
     for n in ("b2b_gemm", "b2b_conv_nhwc", "conv_relu_maxpool", "gemm_bias_act",
-              "conv_bias_act_nhwc", "maxpool2x2_nhwc", "b2b_status_str", "b2b_get_device_error"):
+              "conv_bias_act_nhwc", "maxpool2x2_nhwc", "b2b_status_str", "b2b_get_device_error",
+              "b2b_conv_nhwc_strided", "conv_bias_act_nhwc_strided", "b2b_set_autotune",
+              "b2b_set_choice", "b2b_get_choice"):
         assert n in names
 
 
@@ -84,6 +86,25 @@ def conv(L, dt=F16, N=2, H=8, W=8, C=64, x=FAKE, W0=FAKE, C0=64, R=3, S=3, pad=1
 ])
 def test_b2b_conv_argument_checks(L, kw, expect):
     assert conv(L, **kw) == expect
+
+
+@pytest.mark.parametrize("stride,kw,expect", [
+    (0, {}, SHAPE), (-1, {}, SHAPE), (5, {}, UNSUP),
+    (2, dict(H=1, pad=0), SHAPE),                       # H + 2 pad < R: no output
+    (2, dict(C1=264), UNSUP), (3, dict(x=None), NULL), (2, dict(N=0, x=None, y=None), OK),
+])
+def test_strided_conv_argument_checks(L, stride, kw, expect):
+    a = dict(dt=F16, N=2, H=9, W=9, C=64, x=FAKE, W0=FAKE, C0=64, R=3, S=3, pad=1, b0=None,
+             e0=1, W1=FAKE, C1=64, b1=None, e1=1, y=FAKE)
+    a.update(kw)
+    assert L.b2b_conv_nhwc_strided(a["dt"], a["N"], a["H"], a["W"], a["C"], a["x"], a["W0"],
+                                   a["C0"], a["R"], a["S"], a["pad"], stride, a["b0"], a["e0"],
+                                   a["W1"], a["C1"], a["b1"], a["e1"], a["y"], None) == expect
+    single = L.conv_bias_act_nhwc_strided(a["dt"], a["N"], a["H"], a["W"], a["C"], a["x"],
+                                          a["W0"], a["C0"], a["R"], a["S"], a["pad"], stride,
+                                          a["b0"], a["e0"], a["y"], None)
+    if "C1" not in kw:
+        assert single == expect
 
 
 @pytest.mark.parametrize("args,expect", [

@@ -164,15 +164,20 @@ CONV_SHAPES = [
 ]
 
 
-def run_conv(dt, N, H, W, C, C0, R, S, pad, C1, act0, act1, integer, seed):
-    w = wl.ConvChain("c", dt, N, H, W, C, C0, R, S, pad, C1, act0, act1)
+def run_conv(dt, N, H, W, C, C0, R, S, pad, C1, act0, act1, integer, seed, stride=1):
+    w = wl.ConvChain("c", dt, N, H, W, C, C0, R, S, pad, C1, act0, act1, stride=stride)
     t = wl.conv_inputs(w, seed=seed, integer=integer)
-    out = ops.b2b_conv_nhwc(to_dev(t["x"]), to_dev(t["W0"]), to_dev(t["b0"]), to_dev(t["W1"]),
-                            to_dev(t["b1"]), pad, act0, act1)
+    args = [to_dev(t[k]) for k in ("x", "W0", "b0", "W1", "b1")]
+    if stride == 1:
+        out = ops.b2b_conv_nhwc(*args, pad, act0, act1)
+    else:
+        out = ops.b2b_conv_nhwc_strided(*args, pad, stride, act0, act1)
     torch.cuda.synchronize()
     check_no_device_error()
+    assert out.shape == (N, w.Ho, w.Wo, C1)
     b = {k: wl.to_bits(v) for k, v in t.items()}
-    ref = oracle.b2b_conv_nhwc(dt, b["x"], b["W0"], b["b0"], b["W1"], b["b1"], pad, act0, act1)
+    ref = oracle.b2b_conv_nhwc(dt, b["x"], b["W0"], b["b0"], b["W1"], b["b1"], pad, act0, act1,
+                               stride=stride)
     return compare(dt, wl.to_bits(out.cpu()), ref, integer, "b2b_conv_nhwc")
 
 
@@ -201,6 +206,62 @@ def test_conv_bias_act(shape, integer):
     ref = oracle.conv2d_nhwc(dt, wl.to_bits(t["x"]), wl.to_bits(t["W0"]), wl.to_bits(t["b0"]),
                              pad, act)
     compare(dt, wl.to_bits(out.cpu()), ref, integer, "conv_bias_act_nhwc")
+
+
+# strided first conv (Welder notes, tile propagation: a strided conv's input region)
+STRIDED_SHAPES = [
+    # dtype, N, H, W, C, C0, R, S, pad, C1, stride
+    ("f16", 2, 9, 9, 64, 64, 3, 3, 1, 128, 2),       # resident filters, ragged 5 x 5 output
+    ("bf16", 1, 17, 35, 16, 24, 3, 3, 1, 8, 2),      # narrow channels, two tile columns
+    ("f16", 2, 28, 28, 64, 128, 1, 1, 0, 64, 2),     # strided 1x1 (a projection shortcut)
+    ("f16", 1, 23, 19, 32, 32, 5, 5, 2, 16, 3),
+    ("f16", 1, 30, 40, 64, 64, 3, 3, 1, 64, 4),
+    ("f16", 2, 56, 56, 64, 128, 3, 3, 1, 128, 2),    # streamed filters (the workload's layers)
+]
+
+
+@pytest.mark.parametrize("shape", STRIDED_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_strided_conv_integer_exact(shape):
+    run_conv(*shape[:10], "relu", "none", True, seed=sum(shape[1:]) + 5, stride=shape[10])
+
+
+@pytest.mark.parametrize("shape", STRIDED_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_strided_conv_random(shape):
+    run_conv(*shape[:10], "hardswish", "relu", False, seed=sum(shape[1:]) + 6, stride=shape[10])
+
+
+@pytest.mark.parametrize("shape", [("f16", 2, 9, 9, 64, 64, 3, 3, 1, 2),
+                                   ("bf16", 1, 14, 20, 16, 8, 1, 1, 0, 2),
+                                   ("f16", 1, 13, 13, 32, 24, 3, 3, 1, 3)],
+                         ids=lambda s: "-".join(map(str, s)))
+@pytest.mark.parametrize("integer", [True, False])
+def test_strided_conv_bias_act(shape, integer):
+    dt, N, H, W, C, Co, R, S, pad, st = shape
+    w = wl.ConvChain("c", dt, N, H, W, C, Co, R, S, pad, 8, "relu", "none", stride=st)
+    t = wl.conv_inputs(w, seed=H * W + st, integer=integer)
+    act = "relu" if integer else "hardswish"
+    out = ops.conv_bias_act_nhwc_strided(to_dev(t["x"]), to_dev(t["W0"]), to_dev(t["b0"]), pad,
+                                         st, act)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    ref = oracle.conv2d_nhwc(dt, wl.to_bits(t["x"]), wl.to_bits(t["W0"]), wl.to_bits(t["b0"]),
+                             pad, act, stride=st)
+    compare(dt, wl.to_bits(out.cpu()), ref, integer, "conv_bias_act_nhwc_strided")
+
+
+def test_conv3x3s2_1x1_workload_sampled_images():
+    w = wl.CONV3X3S2_1X1
+    t = wl.conv_inputs(w, seed=0)
+    out = ops.b2b_conv_nhwc_strided(*(to_dev(t[k]) for k in ("x", "W0", "b0", "W1", "b1")),
+                                    w.pad, w.stride, w.act0, w.act1)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    b = {k: wl.to_bits(v) for k, v in t.items()}
+    got = wl.to_bits(out.cpu())
+    for n in (0, 17, w.N - 1):
+        ref = oracle.b2b_conv_nhwc(w.dtype, b["x"][n:n + 1], b["W0"], b["b0"], b["W1"], b["b1"],
+                                   w.pad, w.act0, w.act1, stride=w.stride)
+        compare(w.dtype, got[n:n + 1], ref, False, f"conv3x3s2_1x1 image {n}")
 
 
 def test_conv1x1_workload_sampled_images():

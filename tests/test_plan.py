@@ -225,3 +225,27 @@ def test_plan_rejects_like_the_entry_points():
 def test_wide_chains_keep_p_in_tmem():
     for dims in ((300, 128, 256, 64), (257, 72, 200, 72), (1000, 64, 224, 96)):
         assert check("b2b_gemm", dims, True)["p_tmem"] == 1
+
+
+def test_strided_conv_plans():
+    # stride s: an 8 x 16 output tile's boxes take every s-th input pixel; no halo boxes
+    # (the row taps are not whole box rows apart), tiles over the strided output
+    for dims in ((32, 56, 56, 64, 128, 3, 3, 1, 256, 2), (2, 9, 9, 64, 64, 3, 3, 1, 128, 2),
+                 (4, 28, 28, 64, 128, 1, 1, 0, 64, 2), (1, 17, 11, 16, 24, 5, 5, 2, 8, 3),
+                 (1, 30, 33, 32, 16, 3, 3, 1, 16, 4)):
+        p = check("b2b_conv_nhwc", dims, False)
+        N, H, W = dims[:3]
+        R, S, pad, st = dims[5], dims[6], dims[7], dims[9]
+        Ho, Wo = (H + 2 * pad - R) // st + 1, (W + 2 * pad - S) // st + 1
+        assert p["tiles"] == N * -(-Ho // 8) * -(-Wo // 16)
+        assert p["halo"] == 0 and p["kchunks0"] == R * S * -(-dims[3] // 64)
+        check("conv_bias_act_nhwc", dims[:8] + (st,), False)
+    # an explicit stride 1 is the unstrided launch
+    assert plan("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128, 1)) == \
+        plan("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128))
+    # a 1x1 pad-0 conv runs as a GEMM over the pixel rows at stride 1, as a strided
+    # implicit GEMM at stride 2
+    assert plan("b2b_conv_nhwc", (4, 28, 28, 64, 128, 1, 1, 0, 64))[1]["tiles"] == -(-4 * 28 * 28 // 128)
+    assert plan("b2b_conv_nhwc", (4, 28, 28, 64, 128, 1, 1, 0, 64, 2))[1]["tiles"] == 4 * 2 * 1
+    assert plan("b2b_conv_nhwc", (1, 9, 9, 64, 64, 3, 3, 1, 64, 5))[0] == 4     # stride > 4
+    assert plan("b2b_conv_nhwc", (1, 9, 9, 64, 64, 3, 3, 1, 64, 0))[0] == 2
