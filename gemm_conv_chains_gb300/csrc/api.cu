@@ -922,6 +922,29 @@ b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int3
                   B2B_EPI_RELU, nullptr, 0, nullptr, 0, y, stream, KID_CONV_POOL);
 }
 
+b2b_status b2b_fold_batchnorm(b2b_dtype dt, int64_t Co, int64_t K, int32_t out_inner,
+                              const void* Wt, const void* b, const float* gamma,
+                              const float* beta, const float* mean, const float* var, float eps,
+                              void* W_out, void* b_out, void* stream) {
+  if (!valid_dtype(dt) || (out_inner != 0 && out_inner != 1)) return B2B_ERR_UNSUPPORTED;
+  if (Co <= 0 || K <= 0 || !(eps >= 0.f) || Co > (int64_t{1} << 40) / K) return B2B_ERR_SHAPE;
+  if (!Wt || !gamma || !beta || !mean || !var || !W_out || !b_out) return B2B_ERR_NULL;
+  auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  if (!al(Wt, 2) || !al(W_out, 2) || !al(b_out, 2) || (b && !al(b, 2)) || !al(gamma, 4) ||
+      !al(beta, 4) || !al(mean, 4) || !al(var, 4))
+    return B2B_ERR_ALIGN;
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  if (d == nullptr) return st;
+  if (launch_fold_batchnorm(dt == B2B_BF16, Co, K, out_inner, Wt, b, gamma, beta, mean, var, eps,
+                            W_out, b_out, d->num_sms, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
 b2b_status maxpool2x2_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,
                            const void* x, void* y, void* stream) {
   if (!valid_dtype(dt)) return B2B_ERR_UNSUPPORTED;

@@ -100,6 +100,67 @@ cudaError_t launch_maxpool(int is_bf16, int N, int H, int W, int C, const void* 
 }
 
 // ------------------------------------------------------------------------------------
+// batch normalisation folded into the preceding operator's weights and bias
+// ------------------------------------------------------------------------------------
+// One thread per weight element (grid-stride): W'[i] = rnd(W[i] * s[co]) with
+// s[co] = gamma[co] / sqrt(var[co] + eps) in fp32, and for i < Co also
+// b'[i] = rnd((b[i] - mean[i]) * s[i] + beta[i]).  Element-wise, so W_out may be W and
+// b_out may be b.
+template <bool BF16>
+__device__ __forceinline__ float widen(uint16_t v) {
+  if constexpr (BF16) return __bfloat162float(__ushort_as_bfloat16(v));
+  else return __half2float(__ushort_as_half(v));
+}
+template <bool BF16>
+__device__ __forceinline__ uint16_t narrow(float v) {
+  if constexpr (BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  else return __half_as_ushort(__float2half_rn(v));
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) fold_bn_kernel(
+    const uint16_t* __restrict__ Wt, const uint16_t* __restrict__ b, const float* gamma,
+    const float* beta, const float* mean, const float* var, float eps, int64_t Co, int64_t K,
+    int out_inner, uint16_t* W_out, uint16_t* b_out) {
+  const int64_t total = Co * K;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += step) {
+    const int64_t co = out_inner ? i % Co : i / K;
+    const float s = gamma[co] / sqrtf(var[co] + eps);
+    W_out[i] = narrow<BF16>(widen<BF16>(Wt[i]) * s);
+    if (i < Co) {
+      const float si = gamma[i] / sqrtf(var[i] + eps);
+      const float bi = b != nullptr ? widen<BF16>(b[i]) : 0.f;
+      b_out[i] = narrow<BF16>((bi - mean[i]) * si + beta[i]);
+    }
+  }
+}
+
+cudaError_t launch_fold_batchnorm(int is_bf16, int64_t Co, int64_t K, int out_inner,
+                                  const void* Wt, const void* b, const float* gamma,
+                                  const float* beta, const float* mean, const float* var,
+                                  float eps, void* W_out, void* b_out, int num_sms,
+                                  cudaStream_t stream) {
+  const int64_t total = Co * K;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  auto* w = static_cast<const uint16_t*>(Wt);
+  auto* bb = static_cast<const uint16_t*>(b);
+  auto* wo = static_cast<uint16_t*>(W_out);
+  auto* bo = static_cast<uint16_t*>(b_out);
+  if (is_bf16)
+    fold_bn_kernel<true><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        w, bb, gamma, beta, mean, var, eps, Co, K, out_inner, wo, bo);
+  else
+    fold_bn_kernel<false><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        w, bb, gamma, beta, mean, var, eps, Co, K, out_inner, wo, bo);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------
 // timeout probe: a barrier that expects one arrival which never comes
 // ------------------------------------------------------------------------------------
 __global__ void probe_timeout_kernel(uint64_t limit_ns, uint32_t* err) {

@@ -57,6 +57,14 @@ cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w
 cudaError_t launch_maxpool(int is_bf16, int N, int H, int W, int C, const void* x, void* y,
                            int num_sms, cudaStream_t stream);
 
+// Batch normalisation folded into weights [Co][K] (out_inner 0) or [K][Co] (out_inner 1)
+// and bias [Co]; fp32 arithmetic, one rounding per stored value.
+cudaError_t launch_fold_batchnorm(int is_bf16, int64_t Co, int64_t K, int out_inner,
+                                  const void* Wt, const void* b, const float* gamma,
+                                  const float* beta, const float* mean, const float* var,
+                                  float eps, void* W_out, void* b_out, int num_sms,
+                                  cudaStream_t stream);
+
 // One-CTA kernel whose only wait can never complete; it must time out.
 cudaError_t launch_probe_timeout(uint64_t limit_ns, uint32_t* err, cudaStream_t stream);
 

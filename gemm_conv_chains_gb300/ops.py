@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.conv_bias_act_nhwc_strided.argtypes = [ci, i32, i32, i32, i32, vp, vp, i32, i32, i32,
                                                  i32, i32, vp, ci, vp, vp]
         L.conv_bias_act_nhwc_strided.restype = ci
+        L.b2b_fold_batchnorm.argtypes = [ci, i64, i64, i32, vp, vp, vp, vp, vp, vp,
+                                         ctypes.c_float, vp, vp, vp]
+        L.b2b_fold_batchnorm.restype = ci
         L.b2b_set_autotune.argtypes = [i32]
         L.b2b_set_autotune.restype = None
         L.b2b_autotune_reset.argtypes = []
@@ -278,6 +281,31 @@ def _conv_single(x, Wt, b, pad, stride, epi, out, stream):
                                                 R, S, pad, stride, _ptr(b), _epi(epi), _ptr(out),
                                                 _stream(stream)), "conv_bias_act_nhwc_strided")
     return out
+
+
+def fold_batchnorm(W, b, gamma, beta, mean, var, eps=1e-5, out_inner=False, W_out=None,
+                   b_out=None, stream=None):
+    """Batch norm folded into the preceding operator's weights and bias
+    (b2b_fold_batchnorm): W [Co, ...] (conv filters, out_inner False) or [K, Co] (row-major
+    GEMM weights, out_inner True), b [Co] or None, gamma/beta/mean/var float32 [Co].
+    Returns (W', b') in W's dtype; W_out / b_out may be W / b."""
+    dt = W.dtype
+    Co = W.shape[-1] if out_inner else W.shape[0]
+    K = W.numel() // max(Co, 1)
+    _check_tensor(W, "W", dt, tuple(W.shape))
+    if b is not None:
+        _check_tensor(b, "b", dt, (Co,))
+    for name, v in (("gamma", gamma), ("beta", beta), ("mean", mean), ("var", var)):
+        _check_tensor(v, name, torch.float32, (Co,))
+    W_out = torch.empty_like(W) if W_out is None else W_out
+    b_out = torch.empty((Co,), dtype=dt, device=W.device) if b_out is None else b_out
+    _check_tensor(W_out, "W_out", dt, tuple(W.shape))
+    _check_tensor(b_out, "b_out", dt, (Co,))
+    _raise(lib().b2b_fold_batchnorm(_dtype_code(W), Co, K, 1 if out_inner else 0, _ptr(W), _ptr(b),
+                                    _ptr(gamma), _ptr(beta), _ptr(mean), _ptr(var), float(eps),
+                                    _ptr(W_out), _ptr(b_out), _stream(stream)),
+           "b2b_fold_batchnorm")
+    return W_out, b_out
 
 
 def maxpool2x2_nhwc(x, out=None, stream=None):

@@ -155,6 +155,24 @@ b2b_status conv_bias_act_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_
                                       int32_t S, int32_t pad, int32_t stride, const void* b,
                                       b2b_epilogue e, void* y, void* stream);
 
+/* Batch normalisation folded into the weights and bias of the operator before it
+ * (interview notes, "阿里巴巴 AI Infra (2)", TVM Relay scheduling primitives,
+ * SimplifyInference: at inference BN is a per-channel scale and bias, which folded into
+ * the preceding conv or GEMM makes the chain's bias epilogue):
+ *   s[co]  = gamma[co] / sqrt(var[co] + eps)
+ *   W'[..] = rnd(W[..] * s[co]),   b'[co] = rnd((b[co] - mean[co]) * s[co] + beta[co])
+ * in fp32, one round-to-nearest-even per stored value.  W is [Co][K] (out_inner = 0: conv
+ * filters [Co][R][S][Cin], K = R*S*Cin; b2b_conv_nhwc's W1 [C1][C0]) or [K][Co]
+ * (out_inner = 1: b2b_gemm's row-major W0/W1).  gamma, beta, mean, var: fp32 device
+ * arrays [Co]; b [Co] or NULL (0); W_out / b_out may be W / b (in place).  Device
+ * pointers; asynchronous on `stream`.  Errors: B2B_ERR_SHAPE (Co or K < 1, eps < 0),
+ * B2B_ERR_NULL, B2B_ERR_ALIGN (fp16/bf16 arrays 2-byte, fp32 arrays 4-byte aligned),
+ * B2B_ERR_UNSUPPORTED (dtype, out_inner), B2B_ERR_CUDA. */
+b2b_status b2b_fold_batchnorm(b2b_dtype dt, int64_t Co, int64_t K, int32_t out_inner,
+                              const void* Wt, const void* b, const float* gamma,
+                              const float* beta, const float* mean, const float* var, float eps,
+                              void* W_out, void* b_out, void* stream);
+
 /* y[N,H/2,W/2,C] = max over each 2x2 window (stride 2, floor mode) of x[N,H,W,C].
  * Limits: H, W >= 2; C multiple of 8. */
 b2b_status maxpool2x2_nhwc(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t C,

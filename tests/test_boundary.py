@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
     for n in ("b2b_gemm", "b2b_conv_nhwc", "conv_relu_maxpool", "gemm_bias_act",
               "conv_bias_act_nhwc", "maxpool2x2_nhwc", "b2b_status_str", "b2b_get_device_error",
               "b2b_conv_nhwc_strided", "conv_bias_act_nhwc_strided", "b2b_set_autotune",
-              "b2b_set_choice", "b2b_get_choice"):
+              "b2b_set_choice", "b2b_get_choice", "b2b_fold_batchnorm"):
         assert n in names
 
 
@@ -126,9 +126,25 @@ def test_single_operator_argument_checks(L):
     assert L.maxpool2x2_nhwc(F16, 1, 1, 4, 16, FAKE, FAKE, None) == SHAPE
 
 
+def fold(L, dt=F16, Co=64, K=576, out_inner=0, W=FAKE, b=None, g=FAKE, be=FAKE, m=FAKE, v=FAKE,
+         eps=1e-5, Wo=FAKE, bo=FAKE):
+    return L.b2b_fold_batchnorm(dt, Co, K, out_inner, W, b, g, be, m, v, eps, Wo, bo, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dt=2), UNSUP), (dict(out_inner=2), UNSUP), (dict(Co=0), SHAPE), (dict(K=-1), SHAPE),
+    (dict(eps=-1.0), SHAPE), (dict(eps=float("nan")), SHAPE), (dict(g=None), NULL),
+    (dict(Wo=None), NULL), (dict(W=FAKE + 1), ALIGN), (dict(v=FAKE + 2), ALIGN),
+    (dict(b=FAKE + 1), ALIGN),
+])
+def test_fold_batchnorm_argument_checks(L, kw, expect):
+    assert fold(L, **kw) == expect
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
 def test_valid_call_without_device_reports_cuda_error(L):
     assert gemm(L) == CUDA
+    assert fold(L) == CUDA
     assert L.b2b_num_sms() == -1
 
 
