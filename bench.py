@@ -18,7 +18,7 @@ Prints ONE JSON line (rank 0).
                uploads its activations and downloads its result (weights resident), the
                upload of step i+1, compute of step i and download of step i-1 overlapping.
   cpu_baseline the CPU oracle (single thread) on a bounded sample of rows.
-  workloads    the other four workloads, fused and unfused, measured the same way.
+  workloads    every workload (the headline too), fused and unfused, measured the same way.
 
 --impl reference times the CPU oracle instead (the method's plain unfused definition),
 on a per-step sample of the same workload sized so the whole run takes about a minute.
@@ -491,7 +491,7 @@ def run_ours(args):
 
 def other_workloads(dev, peaks, steps, warmup):
     out = {}
-    for w in (wl.GEMM_SMALL, wl.GEMM_FFN, wl.CONV1X1, wl.CONV3X3_1X1, wl.CONV_POOL):
+    for w in wl.WORKLOADS.values():
         fused, unfused, nsets, _ = runner_for(w, dev)
         s_f = time_steps(fused, steps, warmup, nsets, dev) / steps
         s_u = time_steps(unfused, steps, warmup, nsets, dev) / steps
