@@ -185,6 +185,7 @@ inline bool valid_epi(int e) {
 struct Regions {
   uint32_t ring, w_res, p_each, out_each, bias, bar;
   int32_t cand = 0, ncand = 0;   // the layout taken, as an index into the feasible ones
+  uint32_t extend = 0;           // ring stages that may run on into the output staging
 };
 
 // TMEM columns of the accumulators.  Chain: nbuf D0 buffers of round_up(N0p, 32) columns,
@@ -361,6 +362,24 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   off += r.bias;
   p.off_bar = off;
   off += r.bar;
+  // When the output staging directly follows the ring (streamed weights, P in TMEM) and W1
+  // is loaded once per tile pair, a CTA with at most two tiles never fills the ring after
+  // its second tile's GEMM0 except with W1, so stages that run on into the staging are
+  // free before any epilogue writes it (the epilogue waits for GEMM1, which follows every
+  // GEMM0 chunk).  The extra stages are counted here and taken at launch when the grid
+  // gives no CTA a third tile, provided that W1's stages of the pair miss them.
+  r.extend = 0;
+  if (mode == MODE_CHAIN && k.p_tmem && !k.resident && p.w1_group &&
+      p.off_out[0] == p.off_ring + r.ring) {
+    const uint32_t span = r.ring + obufs * r.out_each;
+    const uint32_t total = std::min<uint32_t>(kMaxStages, span / p.stage_bytes);
+    const uint32_t w1_stages = (static_cast<uint32_t>(p.kchunks1) + p.w1_per_stage - 1) /
+                               p.w1_per_stage;
+    bool clear = total > p.num_stages;
+    for (uint32_t j = 0; j < w1_stages && clear; ++j)
+      clear = (2u * static_cast<uint32_t>(p.kstages0) + j) % total < p.num_stages;
+    if (clear) r.extend = total - p.num_stages;
+  }
   *smem_bytes = off + 1024u;
   if (regions) *regions = r;
   return *smem_bytes <= kSmemLimit && p.tmem_cols <= 512u;
@@ -515,6 +534,7 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = pf_second_for(p.num_tiles, grid, ch.pf2);
+  if (r.extend > 0 && (p.num_tiles + grid - 1) / grid <= 2) p.num_stages += r.extend;
   if (info) *info = info_for(r.ncand, p.num_tiles, d->num_sms, true);
 
   CUtensorMap ta, tw0, tw1, to;
@@ -589,6 +609,7 @@ b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = 0;   // the implicit-GEMM A has no per-tile contiguous range to prefetch
+  if (r.extend > 0 && (p.num_tiles + grid - 1) / grid <= 2) p.num_stages += r.extend;
   if (info) *info = info_for(r.ncand, p.num_tiles, d->num_sms, false);
   const int32_t Ho = p.Ho, Wo = p.Wo;
 
@@ -1099,7 +1120,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   b2b_status st = check_plan_args(kind, dims, ndims);
   if (st != B2B_OK) return st;
   if (out == nullptr) return B2B_ERR_NULL;
-  if (out_len < 51) return B2B_ERR_SHAPE;
+  if (out_len < 52) return B2B_ERR_SHAPE;
   Choice c;
   find_choice(plan_key(kind, dims, ndims), &c);
   ChainParams p;
@@ -1107,7 +1128,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
   if ((st = plan_for_kind(kind, dims, ndims, c.cand, p, r, smem, mode)) != B2B_OK) return st;
-  const uint32_t v[51] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[52] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -1122,7 +1143,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           1u << p.nbuf_log2, p.off_p[2], p.off_p[3], p.d0_col[2], p.d0_col[3],
                           p.d1_col[2], p.d1_col[3], static_cast<uint32_t>(r.cand),
                           static_cast<uint32_t>(r.ncand), static_cast<uint32_t>(c.grid),
-                          static_cast<uint32_t>(c.pf2)};
+                          static_cast<uint32_t>(c.pf2), r.extend};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

@@ -223,7 +223,7 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1[, stride]}
  *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad[, stride]}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
- * out (out_len >= 51) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ * out (out_len >= 52) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
  * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
  * P offsets [2], bytes per P buffer, staging offsets [2], bytes per staging buffer,
@@ -238,8 +238,10 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * accumulator columns [2..3], GEMM1 accumulator columns [2..3], the layout taken (an
  * index into the feasible layouts, in the planner's order of preference), the number of
  * feasible layouts, and the pinned or measured grid and second-tile-prefetch choices
- * (b2b_set_choice; -1, as a two's-complement word, for the default).  A choice pinned or
- * measured for these sizes is reflected.
+ * (b2b_set_choice; -1, as a two's-complement word, for the default), and the ring stages
+ * a launch adds over the output staging when no CTA gets more than two tiles (P in TMEM,
+ * streamed weights; the staging is first written after the pair's last GEMM0).  A choice
+ * pinned or measured for these sizes is reflected.
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,

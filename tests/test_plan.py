@@ -22,7 +22,7 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0", "kchunks1",
           "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes",
           "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2", "d1_col3", "cand", "ncand",
-          "grid_choice", "pf_choice"]
+          "grid_choice", "pf_choice", "ring_extend"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4}
@@ -30,8 +30,8 @@ KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nh
 
 def plan(kind, dims):
     arr = (ctypes.c_int64 * len(dims))(*dims)
-    out = (ctypes.c_uint32 * 51)()
-    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 51)
+    out = (ctypes.c_uint32 * 52)()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 52)
     return st, dict(zip(FIELDS, list(out)))
 
 
@@ -109,6 +109,18 @@ def check(kind, dims, row_major_w):
     assert p["bias"] >= 1024 + 2048 * (n0blk + (n1blk if mode == 0 else 0))
     assert p["bar"] >= 8 * 27 + 8                # 27 barriers, then the TMEM slot and flag
     usable = p["smem"] - 1024                    # the rest aligns the base to 1024
+    if p["ring_extend"]:
+        # extra ring stages run on into the output staging, never past it, and W1's stages
+        # of a tile pair (after both tiles' GEMM0 chunks) stay out of them
+        ext_end = p["off_ring"] + (p["stages"] + p["ring_extend"]) * p["stage_bytes"]
+        assert p["p_tmem"] and not p["resident"] and p["w1_group"] and p["stages"] + p["ring_extend"] <= 8
+        assert p["off_out0"] == p["off_ring"] + p["ring"]
+        assert ext_end <= p["off_out0"] + (2 if groups == 2 else 1) * p["out"] <= p["off_bias"]
+        total = p["stages"] + p["ring_extend"]
+        per = p["w1_per_stage"]
+        kst = p["kchunks0"] // (R if p["halo"] else 1)
+        for j in range(-(-p["kchunks1"] // per)):
+            assert (2 * kst + j) % total < p["stages"]
     for name, off, size in regions:
         assert off % 1024 == 0, name
         assert off + size <= usable, (name, off, size, usable)
@@ -164,6 +176,9 @@ def test_ffn_plan_keeps_p_in_tmem():
     assert p["p_tmem"] == 1 and p["dual"] == 1
     # W1 (4 chunks of 16 KiB) fits in two 48 KiB stages, loaded once per pair of tiles
     assert p["w1_group"] == 1 and p["w1_per_stage"] == 3
+    # three 48 KiB stages, and a fourth over the two 32 KiB output staging buffers when no
+    # CTA has a third tile (W1's stages of the pair, fills 8 and 9, land on stages 0 and 1)
+    assert p["stages"] == 3 and p["ring_extend"] == 1
 
 
 def test_small_chains_keep_four_tiles_in_flight():
