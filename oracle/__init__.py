@@ -199,6 +199,16 @@ def b2b_gemm(dtype, A, W0, b0, W1, b1, act0, act1):
     return out
 
 
+def b2b_gemm3(dtype, A, W0, b0, W1, b1, W2, b2, act0, act1, act2):
+    """A three-operator chain (BOLT notes, "Enabling deeper operator fusion": several GEMMs
+    in one persistent kernel), written as its definition: three GEMM + bias + activation
+    operators one after another, each intermediate stored in the storage type.
+    A [M,K0], W0 [K0,N0], W1 [N0,N1], W2 [N1,N2] (row-major) -> out [M,N2]."""
+    h0 = gemm_bias_act(dtype, A, W0, b0, act0)
+    h1 = gemm_bias_act(dtype, h0, W1, b1, act1)
+    return gemm_bias_act(dtype, h1, W2, b2, act2)
+
+
 def conv_out_size(n, pad, k, stride=1):
     """Output length of a conv along one axis: floor((n + 2 pad - k) / stride) + 1."""
     return 0 if n + 2 * pad < k else (n + 2 * pad - k) // stride + 1

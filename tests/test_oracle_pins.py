@@ -334,6 +334,50 @@ def test_b2b_conv_equals_conv_then_pointwise(oracle_mod):
 
 
 # ------------------------------------------------------------------------------------
+# three-operator chain (BOLT notes, "Enabling deeper operator fusion")
+# ------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+def test_gemm3_integer_exact_vs_numpy(oracle_mod, dt):
+    # integer data in {-1, 0, 1}: every sum is an exact integer far below 2^24 and every
+    # intermediate is exactly representable, so float64 numpy with the same roundings
+    # (identity on these integers) gives the same values
+    rng = np.random.default_rng(50)
+    A = rng.integers(-1, 2, (37, 64)).astype(np.float64)
+    W0 = rng.integers(-1, 2, (64, 48)).astype(np.float64)
+    W1 = rng.integers(-1, 2, (48, 32)).astype(np.float64)
+    W2 = rng.integers(-1, 2, (32, 24)).astype(np.float64)
+    b0, b1, b2 = (rng.integers(-2, 3, (n,)).astype(np.float64) for n in (48, 32, 24))
+    enc = f16_bits if dt == "f16" else bf16_bits
+    got = oracle_mod.decode(dt, oracle_mod.b2b_gemm3(dt, enc(A), enc(W0), enc(b0), enc(W1),
+                                                     enc(b1), enc(W2), enc(b2), "relu", "relu",
+                                                     "none"))
+    h0 = np.maximum(A @ W0 + b0, 0)
+    h1 = np.maximum(h0 @ W1 + b1, 0)
+    ref = h1 @ W2 + b2
+    if dt == "bf16":      # bf16 keeps 8 significant bits: round the larger integers as it does
+        ref = oracle_mod.decode("bf16", bf16_bits(ref))
+    assert np.all(np.abs(ref) < 65504)
+    assert np.array_equal(got, ref)
+
+
+def test_gemm3_is_b2b_then_one_more_operator(oracle_mod):
+    # the first two operators are the two-operator chain, the third one more GEMM + bias +
+    # act on its stored output
+    w = wl.GemmChain("t", "bf16", 70, 32, 40, 24, "hardswish", "relu")
+    t = {k: wl.to_bits(v) for k, v in wl.gemm_inputs(w, seed=51).items()}
+    rng = np.random.default_rng(52)
+    W2 = bf16_bits(rng.normal(0, 0.2, (24, 16)))
+    b2 = bf16_bits(rng.uniform(-0.1, 0.1, 16))
+    two = oracle_mod.b2b_gemm("bf16", t["A"], t["W0"], t["b0"], t["W1"], t["b1"], "hardswish",
+                              "relu")
+    three = oracle_mod.b2b_gemm3("bf16", t["A"], t["W0"], t["b0"], t["W1"], t["b1"], W2, b2,
+                                 "hardswish", "relu", "hardswish")
+    assert three.shape == (70, 16)
+    assert np.array_equal(three, oracle_mod.gemm_bias_act("bf16", two, W2, b2, "hardswish"))
+
+
+# ------------------------------------------------------------------------------------
 # strided conv (Welder notes, tile propagation: a strided conv reads a strided region)
 # ------------------------------------------------------------------------------------
 
