@@ -186,6 +186,34 @@ def gemm_runner(w: wl.GemmChain, dev):
     return fused, unfused, n, set_bytes
 
 
+def gemm3_runner(w: wl.GemmChain3, dev):
+    from gemm_conv_chains_gb300 import ops
+    t = wl.gemm3_inputs(w, seed=0)
+    W = [(t[f"W{i}"].to(dev), t[f"b{i}"].to(dev)) for i in range(3)]
+    acts = (w.act0, w.act1, w.act2)
+    set_bytes = 2 * w.M * (w.K0 + w.N2)
+    n = rotation_sets(set_bytes, dev)
+    A0 = t["A"].to(dev)
+    sets = []
+    for i in range(n):
+        A = A0 if i == 0 else A0.roll(i, dims=0).contiguous()
+        sets.append((A, torch.empty((w.M, w.N2), dtype=A0.dtype, device=dev),
+                     torch.empty((w.M, w.N0), dtype=A0.dtype, device=dev),
+                     torch.empty((w.M, w.N1), dtype=A0.dtype, device=dev)))
+
+    def fused(i):
+        A, D, _, _ = sets[i % n]
+        ops.b2b_gemm3(A, W[0][0], W[0][1], W[1][0], W[1][1], W[2][0], W[2][1], *acts, out=D)
+
+    def unfused(i):
+        A, D, H0, H1 = sets[i % n]
+        ops.gemm_bias_act(A, W[0][0], W[0][1], acts[0], out=H0)
+        ops.gemm_bias_act(H0, W[1][0], W[1][1], acts[1], out=H1)
+        ops.gemm_bias_act(H1, W[2][0], W[2][1], acts[2], out=D)
+
+    return fused, unfused, n, set_bytes
+
+
 def conv_runner(w: wl.ConvChain, dev):
     from gemm_conv_chains_gb300 import ops
     t = wl.conv_inputs(w, seed=0)
@@ -246,6 +274,8 @@ def pool_runner(w: wl.ConvPool, dev):
 def runner_for(w, dev):
     if isinstance(w, wl.GemmChain):
         return gemm_runner(w, dev)
+    if isinstance(w, wl.GemmChain3):
+        return gemm3_runner(w, dev)
     if isinstance(w, wl.ConvChain):
         return conv_runner(w, dev)
     return pool_runner(w, dev)
@@ -485,7 +515,8 @@ def run_ours(args):
                      "tensor": {"achieved_tflops": round(tflops, 1), "peak": peaks["bf16_tflops"],
                                 "frac": round(tflops / peaks["bf16_tflops"], 4)}},
         "unfused": {"ms_per_step": round(t_unf * 1e3, 6), "tflops": round(w.flops / t_unf / 1e12, 2),
-                    "algorithmic_bytes": w.unfused_bytes, "launches_per_step": 2,
+                    "algorithmic_bytes": w.unfused_bytes,
+                    "launches_per_step": 3 if isinstance(w, wl.GemmChain3) else 2,
                     "fused_speedup": round(t_unf / t_step, 3)},
         "gpu_launches": args.steps,
     }

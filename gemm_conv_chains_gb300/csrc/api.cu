@@ -194,6 +194,18 @@ struct Regions {
 uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = false) {
   const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
   for (uint32_t b = 0; b < kMaxBufs; ++b) p.d0_col[b] = p.d1_col[b] = 0;
+  p.d2_col[0] = p.d2_col[1] = 0;
+  if (mode == MODE_CHAIN3) {
+    // Two buffers of D0, D1, D2 each: tile i uses buffer i & 1.
+    const uint32_t s1 = round_up(static_cast<uint32_t>(p.N1p), 32u);
+    const uint32_t s2 = round_up(static_cast<uint32_t>(p.N2p), 32u);
+    for (uint32_t b = 0; b < 2; ++b) {
+      p.d0_col[b] = b * s0;
+      p.d1_col[b] = 2u * s0 + b * s1;
+      p.d2_col[b] = 2u * (s0 + s1) + b * s2;
+    }
+    return pow2_at_least(2u * (s0 + s1 + s2));
+  }
   if (mode == MODE_CHAIN && p_tmem) {
     // Buffer b holds D0, then P (packed, N0p / 2 columns, over D0) and D1 after it.
     const uint32_t d1off = round_up(static_cast<uint32_t>(p.N0p) / 2u, 32u);
@@ -385,6 +397,77 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   return *smem_bytes <= kSmemLimit && p.tmem_cols <= 512u;
 }
 
+// Shared-memory plan of the three-operator chain: ring of A chunks; W0, W1, W2 resident
+// (W2 written by the epilogue warps in the same MN-major layout as a TMA load of W1);
+// two P0, two P1 and two output staging buffers (tile i uses buffer i & 1); bias operands
+// of the three GEMMs; barriers.  At least two ring stages, else the chain does not fit.
+bool plan_smem_chain3(ChainParams& p, size_t* smem_bytes, Regions* regions) {
+  const uint32_t budget = kSmemLimit - 1024u;
+  const uint32_t n0blk = static_cast<uint32_t>((p.N0p + 63) / 64);
+  const uint32_t n1blk = static_cast<uint32_t>((p.N1p + 63) / 64);
+  const uint32_t n2blk = static_cast<uint32_t>((p.N2p + 63) / 64);
+  p.w0_chunk_bytes = n0blk * 8192u;
+  p.w1_chunk_bytes = n1blk * 8192u;
+  p.w2_chunk_bytes = n2blk * 8192u;
+  const uint32_t p0_bytes = n0blk * kPChunkBytes, p1_bytes = n1blk * kPChunkBytes;
+  const uint32_t out_bytes = n2blk * kPChunkBytes;
+  const uint32_t bias_bytes = kOnesBytes + kBiasBlockBytes * (n0blk + n1blk + n2blk);
+  const uint32_t bar_bytes = 1024u;
+  const uint32_t w_res = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes +
+                         static_cast<uint32_t>(p.kchunks1) * p.w1_chunk_bytes +
+                         static_cast<uint32_t>(p.kchunks2) * p.w2_chunk_bytes;
+  const uint64_t fixed = uint64_t{w_res} + 2u * (p0_bytes + p1_bytes + out_bytes) + bias_bytes +
+                         bar_bytes;
+  if (fixed >= budget) return false;
+  const uint32_t stages =
+      std::min<uint32_t>(kMaxStages, (budget - static_cast<uint32_t>(fixed)) / kABytes);
+  if (stages < 2u) return false;
+  p.tmem_cols = tmem_layout(p, MODE_CHAIN3, 2u);
+  if (p.tmem_cols > 512u) return false;
+  p.acc_dual = 1;
+  p.nbuf_log2 = 1;
+  p.epi_groups = 2;
+  p.resident = 1;
+  p.out_alias_p = 0;
+  p.p_tmem = 0;
+  p.halo = 0;
+  p.num_stages = stages;
+  p.stage_bytes = kABytes;
+  p.a_stage_bytes = kABytes;
+  p.kstages0 = p.kchunks0;
+  p.w1_group = 0;
+  p.w1_per_stage = 1;
+  Regions r;
+  r.cand = 0;
+  r.ncand = 1;
+  r.ring = stages * kABytes;
+  r.w_res = w_res;
+  r.p_each = p0_bytes;
+  r.out_each = out_bytes;
+  r.bias = bias_bytes;
+  r.bar = bar_bytes;
+  uint32_t off = 0;
+  p.off_ring = off;
+  off += r.ring;
+  p.off_w0 = off;
+  p.off_w1 = p.off_w0 + static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
+  p.off_w2 = p.off_w1 + static_cast<uint32_t>(p.kchunks1) * p.w1_chunk_bytes;
+  off += w_res;
+  for (uint32_t b = 0; b < kMaxBufs; ++b) p.off_p[b] = off + (b & 1u) * p0_bytes;
+  off += 2u * p0_bytes;
+  for (uint32_t b = 0; b < 2; ++b) p.off_p1[b] = off + b * p1_bytes;
+  off += 2u * p1_bytes;
+  for (uint32_t b = 0; b < 2; ++b) p.off_out[b] = off + b * out_bytes;
+  off += 2u * out_bytes;
+  p.off_bias = off;
+  off += bias_bytes;
+  p.off_bar = off;
+  off += bar_bytes;
+  *smem_bytes = off + 1024u;
+  if (regions) *regions = r;
+  return *smem_bytes <= kSmemLimit;
+}
+
 void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const void* b1,
                  DeviceState* d, uint32_t kid) {
   p.is_bf16 = dt == B2B_BF16 ? 1 : 0;
@@ -442,6 +525,28 @@ bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int
   p.num_tiles = ceil_div(M, kBlockM);
   p.stride = 1;
   return plan_smem(p, mode, w_mn, w_mn, smem, regions, forced);
+}
+
+// Three-operator chain over a 2-D A with row-major W0 [K0][N0], W1 [N0][N1], W2 [N1][N2].
+bool gemm3_params(ChainParams& p, int64_t M, int32_t K0, int32_t N0, int32_t N1, int32_t N2,
+                  size_t* smem, Regions* regions, int forced = -1) {
+  std::memset(&p, 0, sizeof(p));
+  if (forced > 0) return false;   // one layout
+  p.M = static_cast<int32_t>(M);
+  p.K0 = K0;
+  p.N0 = N0;
+  p.N1 = N1;
+  p.N2 = N2;
+  p.N0p = static_cast<int32_t>(round_up(static_cast<uint32_t>(N0), 16u));
+  p.N1p = static_cast<int32_t>(round_up(static_cast<uint32_t>(N1), 16u));
+  p.N2p = static_cast<int32_t>(round_up(static_cast<uint32_t>(N2), 16u));
+  p.kchunks0 = ceil_div(K0, kChunkK);
+  p.kc_per_tap = p.kchunks0;
+  p.kchunks1 = ceil_div(p.N0p, kChunkK);
+  p.kchunks2 = ceil_div(p.N1p, kChunkK);
+  p.num_tiles = ceil_div(M, kBlockM);
+  p.stride = 1;
+  return plan_smem_chain3(p, smem, regions);
 }
 
 // 4-D implicit-GEMM A operand (conv filters [Cout][R][S][Cin]).
@@ -588,6 +693,59 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   if (mode == MODE_CHAIN) v = w_mn ? V_GEMM_CHAIN : V_CONV1X1_CHAIN;
   else v = w_mn ? V_GEMM_SINGLE : V_CONV1X1_SINGLE;
   return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
+}
+
+// Three-operator chain (2-D A, row-major weights).
+b2b_status run_gemm3_with(const Choice& ch, Info* info, int dt, int64_t M, int32_t K0, int32_t N0,
+                          int32_t N1, int32_t N2, const void* A, const void* W0, const void* b0,
+                          int e0, const void* W1, const void* b1, int e1, const void* W2,
+                          const void* b2, int e2, void* D, void* stream) {
+  ChainParams p;
+  size_t smem = 0;
+  Regions r;
+  if (!gemm3_params(p, M, K0, N0, N1, N2, &smem, &r, ch.cand)) return B2B_ERR_UNSUPPORTED;
+  b2b_status st = B2B_OK;
+  DeviceState* d = device_state(&st);
+  if (d == nullptr) return st;
+  fill_common(p, dt, e0, e1, b0, b1, d, KID_GEMM_CHAIN3);
+  p.act2 = e2;
+  p.b2 = static_cast<const uint16_t*>(b2);
+  p.w2 = static_cast<const uint16_t*>(W2);
+  const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
+  p.pf_second = pf_second_for(p.num_tiles, grid, ch.pf2);
+  if (info) *info = info_for(r.ncand, p.num_tiles, d->num_sms, true);
+
+  CUtensorMap ta, tw0, tw1, to;
+  const uint64_t e = 2;
+  bool ok = make_map(&ta, A, p.is_bf16, 2, {static_cast<uint64_t>(K0), static_cast<uint64_t>(M)},
+                     {K0 * e}, {kChunkK, kBlockM});
+  // Row-major [rows][N] viewed as [N/64][rows][64] when N is a multiple of 64 (one box per
+  // K chunk), else one 2-D box per 64-wide column block.
+  auto wmap = [&](CUtensorMap* m, const void* ptr, uint64_t rows, int32_t N, uint32_t box_rows,
+                  int32_t* box3) {
+    *box3 = 0;
+    if (N % 64 == 0 && make_map(m, ptr, p.is_bf16, 3, {64, rows, static_cast<uint64_t>(N / 64)},
+                                {N * e, 128}, {64, box_rows, static_cast<uint32_t>(N / 64)})) {
+      *box3 = 1;
+      return true;
+    }
+    return make_map(m, ptr, p.is_bf16, 2, {static_cast<uint64_t>(N), rows}, {N * e},
+                    {64, box_rows});
+  };
+  int32_t out3 = 0;
+  ok = ok && wmap(&tw0, W0, static_cast<uint64_t>(K0), N0, 64, &p.w0_box3);
+  ok = ok && wmap(&tw1, W1, static_cast<uint64_t>(N0), N1, 64, &p.w1_box3);
+  ok = ok && wmap(&to, D, static_cast<uint64_t>(M), N2, kBlockM, &out3);
+  p.out_box3 = out3;
+  if (!ok) return B2B_ERR_CUDA;
+  p.pf_a = static_cast<const uint8_t*>(A);
+  p.pf_a_bytes = static_cast<uint64_t>(M) * K0 * e;
+  p.pf_a_tile_bytes = static_cast<uint32_t>(kBlockM * K0 * e);
+  p.pf_w0 = static_cast<const uint8_t*>(W0);
+  p.pf_w0_bytes = static_cast<uint32_t>(static_cast<uint64_t>(K0) * N0 * e);
+  p.pf_w1 = static_cast<const uint8_t*>(W1);
+  p.pf_w1_bytes = static_cast<uint32_t>(static_cast<uint64_t>(N0) * N1 * e);
+  return launch(V_GEMM_CHAIN3, d, ta, tw0, tw1, to, p, smem, grid, stream);
 }
 
 // ------------------------------------------------------------------------------------
@@ -788,6 +946,16 @@ b2b_status run_gemm(const TuneKey& key, int mode, bool w_mn, int dt, int64_t M, 
   });
 }
 
+b2b_status run_gemm3(const TuneKey& key, int dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
+                     int32_t N2, const void* A, const void* W0, const void* b0, int e0,
+                     const void* W1, const void* b1, int e1, const void* W2, const void* b2,
+                     int e2, void* D, void* stream) {
+  return dispatch(key, stream, [&](const Choice& c, Info* info) {
+    return run_gemm3_with(c, info, dt, M, K0, N0, N1, N2, A, W0, b0, e0, W1, b1, e1, W2, b2, e2,
+                          D, stream);
+  });
+}
+
 b2b_status run_conv(const TuneKey& key, int mode, int dt, int32_t N, int32_t H, int32_t W,
                     int32_t C, const void* x, const void* W0, int32_t C0, int32_t R, int32_t S,
                     int32_t pad, int32_t stride, const void* b0, int e0, const void* W1,
@@ -831,6 +999,29 @@ b2b_status b2b_gemm(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
   if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1))) return B2B_ERR_ALIGN;
   return run_gemm({0, M, K0, N0, N1}, MODE_CHAIN, true, dt, M, K0, N0, N1, A, W0, b0, e0, W1, b1,
                   e1, D, stream, KID_GEMM_CHAIN);
+}
+
+b2b_status b2b_gemm3(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1, int32_t N2,
+                     const void* A, const void* W0, const void* b0, b2b_epilogue e0,
+                     const void* W1, const void* b1, b2b_epilogue e1, const void* W2,
+                     const void* b2, b2b_epilogue e2, void* D, void* stream) {
+  if (!valid_dtype(dt) || !valid_epi(e0) || !valid_epi(e1) || !valid_epi(e2))
+    return B2B_ERR_UNSUPPORTED;
+  if (M < 0 || K0 <= 0 || N0 <= 0 || N1 <= 0 || N2 <= 0) return B2B_ERR_SHAPE;
+  b2b_status st;
+  if ((st = check_channels(K0, kMaxReduction)) != B2B_OK) return st;
+  if ((st = check_channels(N0, 256)) != B2B_OK) return st;
+  if ((st = check_channels(N1, 256)) != B2B_OK) return st;
+  if ((st = check_channels(N2, 256)) != B2B_OK) return st;
+  if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
+  if (M == 0) return B2B_OK;
+  if (!A || !W0 || !W1 || !W2 || !D) return B2B_ERR_NULL;
+  if (!aligned16(A) || !aligned16(W0) || !aligned16(W1) || !aligned16(W2) || !aligned16(D))
+    return B2B_ERR_ALIGN;
+  if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1)) || (b2 && !aligned2(b2)))
+    return B2B_ERR_ALIGN;
+  return run_gemm3({5, M, K0, N0, N1, N2}, dt, M, K0, N0, N1, N2, A, W0, b0, e0, W1, b1, e1, W2,
+                   b2, e2, D, stream);
 }
 
 b2b_status gemm_bias_act(b2b_dtype dt, int64_t M, int32_t K, int32_t N, const void* A,
@@ -1039,7 +1230,7 @@ b2b_status b2b_get_device_error(uint32_t info[4]) {
 }
 
 // Sizes an entry point takes, per kind (b2b_debug_plan's numbering).
-static const int32_t kPlanDims[5] = {4, 3, 9, 8, 5};
+static const int32_t kPlanDims[6] = {4, 3, 9, 8, 5, 5};
 
 // The convs (kinds 2 and 3) take an optional stride after their sizes (default 1).
 static int64_t plan_stride(int32_t kind, const int64_t* dims, int32_t ndims) {
@@ -1047,7 +1238,7 @@ static int64_t plan_stride(int32_t kind, const int64_t* dims, int32_t ndims) {
 }
 
 static b2b_status check_plan_args(int32_t kind, const int64_t* dims, int32_t ndims) {
-  if (kind < 0 || kind > 4) return B2B_ERR_UNSUPPORTED;
+  if (kind < 0 || kind > 5) return B2B_ERR_UNSUPPORTED;
   if (dims == nullptr) return B2B_ERR_NULL;
   if (ndims < kPlanDims[kind]) return B2B_ERR_SHAPE;
   for (int i = 0; i < kPlanDims[kind]; ++i)
@@ -1103,6 +1294,14 @@ static b2b_status plan_for_kind(int32_t kind, const int64_t* dims, int32_t ndims
         ok = conv_params(p, mode, d0, d1, d2, d3, C0, R, S, pad, C1, &smem, &r, forced, stride);
       break;
     }
+    case 5:   // b2b_gemm3: M, K0, N0, N1, N2
+      if ((st = check_channels(d1, kMaxReduction)) != B2B_OK) return st;
+      if ((st = check_channels(d2, 256)) != B2B_OK) return st;
+      if ((st = check_channels(d3, 256)) != B2B_OK) return st;
+      if ((st = check_channels(static_cast<int32_t>(dims[4]), 256)) != B2B_OK) return st;
+      mode = MODE_CHAIN3;
+      ok = gemm3_params(p, dims[0], d1, d2, d3, static_cast<int32_t>(dims[4]), &smem, &r, forced);
+      break;
     case 4: { // conv_relu_maxpool: N, H, W, Cin, Cout
       const int32_t Cout = static_cast<int32_t>(dims[4]);
       if (d0 > 0 && (d1 < 2 || d2 < 2)) return B2B_ERR_SHAPE;
@@ -1120,7 +1319,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   b2b_status st = check_plan_args(kind, dims, ndims);
   if (st != B2B_OK) return st;
   if (out == nullptr) return B2B_ERR_NULL;
-  if (out_len < 52) return B2B_ERR_SHAPE;
+  if (out_len < 57) return B2B_ERR_SHAPE;
   Choice c;
   find_choice(plan_key(kind, dims, ndims), &c);
   ChainParams p;
@@ -1128,7 +1327,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
   if ((st = plan_for_kind(kind, dims, ndims, c.cand, p, r, smem, mode)) != B2B_OK) return st;
-  const uint32_t v[52] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[57] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -1143,7 +1342,8 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           1u << p.nbuf_log2, p.off_p[2], p.off_p[3], p.d0_col[2], p.d0_col[3],
                           p.d1_col[2], p.d1_col[3], static_cast<uint32_t>(r.cand),
                           static_cast<uint32_t>(r.ncand), static_cast<uint32_t>(c.grid),
-                          static_cast<uint32_t>(c.pf2), r.extend};
+                          static_cast<uint32_t>(c.pf2), r.extend, p.off_w2, p.off_p1[0],
+                          p.off_p1[1], p.d2_col[0], p.d2_col[1]};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

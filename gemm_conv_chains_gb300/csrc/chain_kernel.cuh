@@ -18,6 +18,9 @@
 //   MODE_SINGLE  GEMM0 -> epi0 -> global             (one operator of the unfused path)
 //   MODE_POOL    conv GEMM -> 2x2 max -> ReLU -> global (Welder notes, Figure 5:
 //                the (2,2,F) reuse tile is reduced in registers and never leaves the chip)
+//   MODE_CHAIN3  GEMM0 -> epi0 -> P0 -> GEMM1 -> epi1 -> P1 -> GEMM2 -> epi2 -> global
+//                (BOLT notes, "Enabling deeper operator fusion": more than two GEMMs in
+//                one persistent kernel); weights resident, two tiles in flight
 //
 // A operand
 //   2-D: rows of A[M, K0] in 128 x 64 boxes.
@@ -59,7 +62,9 @@ enum : uint32_t {
   BAR_ACC_EMPTY0 = BAR_ACC_FULL0 + kMaxBufs,
   BAR_P_FULL0 = BAR_ACC_EMPTY0 + kMaxBufs,
   BAR_D1_FULL0 = BAR_P_FULL0 + kMaxBufs,
-  BAR_MMA_DONE = BAR_D1_FULL0 + kMaxBufs,
+  BAR_P1_FULL0 = BAR_D1_FULL0 + kMaxBufs,   // three-operator chain: P1 published
+  BAR_D2_FULL0 = BAR_P1_FULL0 + kMaxBufs,   // three-operator chain: GEMM2 accumulator ready
+  BAR_MMA_DONE = BAR_D2_FULL0 + kMaxBufs,
   BAR_BIAS_READY = BAR_MMA_DONE + 1,
   BAR_COUNT = BAR_BIAS_READY + 1,
 };
@@ -235,13 +240,13 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
   if (p.resident) {
     const uint32_t wbar = bars + 8u * BAR_WFULL;
     uint32_t total = p.kchunks0 * p.w0_chunk_bytes;
-    if (MODE == MODE_CHAIN) total += p.kchunks1 * p.w1_chunk_bytes;
+    if (MODE == MODE_CHAIN || MODE == MODE_CHAIN3) total += p.kchunks1 * p.w1_chunk_bytes;
     mbar_arrive_expect_tx_if(lead, wbar, total);
     KPos k;
     for (int kc = 0; kc < p.kchunks0; ++kc, k.next(p))
       load_w0_chunk<A4D, W0MN>(lead, p, tmW0, base + p.off_w0 + kc * p.w0_chunk_bytes, k, wbar,
                                pol_keep);
-    if (MODE == MODE_CHAIN)
+    if (MODE == MODE_CHAIN || MODE == MODE_CHAIN3)
       for (int kc1 = 0; kc1 < p.kchunks1; ++kc1)
         load_w1_chunk<W1MN>(lead, p, tmW1, base + p.off_w1 + kc1 * p.w1_chunk_bytes, kc1, wbar,
                             pol_keep);
@@ -430,6 +435,17 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const int last_nks = last_rem >= 64 ? 4 : (last_rem + 15) >> 4;
   const int rem1 = p.N0p - (p.kchunks1 - 1) * kChunkK;
   const int last_nks1 = rem1 >= 64 ? 4 : (rem1 >> 4);
+  // Three-operator chain: GEMM2 reads P1 (K-major, as P) and the resident W2 (MN-major).
+  const uint32_t idesc2 = idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N2p);
+  const uint64_t p1_desc0 = sdesc_sw128(base + p.off_p1[0], 16u, 1024u);
+  const uint64_t res_w2 = sdesc_sw128(base + p.off_w2, 8192u, 1024u);
+  const uint32_t n1blk = static_cast<uint32_t>((p.N1p + 63) >> 6);
+  const uint64_t bias2_desc = sdesc_sw128(
+      ones_addr + kOnesBytes + (n0blk + n1blk) * kBiasBlockBytes, kBiasBlockBytes, 1024u);
+  const uint32_t idesc_b2 = idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N2p);
+  const uint32_t w2_step = p.w2_chunk_bytes >> 4;
+  const int rem2 = p.N1p - (p.kchunks2 - 1) * kChunkK;
+  const int last_nks2 = rem2 >= 64 ? 4 : (rem2 >> 4);
 
   int stage = 0;
   uint32_t phase = 0;
@@ -439,7 +455,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   auto issue_g0 = [&](int it) -> bool {
     const int32_t t = blockIdx.x + it * gridDim.x;
     const uint32_t b = buf_of(p, it);
-    if (MODE != MODE_CHAIN || p.p_tmem) {
+    if ((MODE != MODE_CHAIN && MODE != MODE_CHAIN3) || p.p_tmem) {
       // The epilogue must have drained the buffer's previous tile (with P in TMEM: its
       // GEMM1 accumulator, the last thing read from the buffer).
       if (!warp_mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), use_of(p, it) ^ 1u, p, abort_flag,
@@ -535,6 +551,29 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     return true;
   };
 
+  // GEMM2 of the j-th tile (three-operator chain): D2[b] = P1[b] . W2, both resident in
+  // shared memory; commits D2_FULL[b].
+  auto issue_g2 = [&](int j) -> bool {
+    const int32_t t = blockIdx.x + j * gridDim.x;
+    const uint32_t b = buf_of(p, j);
+    if (!warp_mbar_wait(bars + 8u * (BAR_P1_FULL0 + b), use_of(p, j), p, abort_flag,
+                        SITE_MMA_P1_FULL, t))
+      return false;
+    tc_fence_after_sync();
+    const uint32_t d2 = tmem_base + p.d2_col[b];
+    for (int kc2 = 0; kc2 < p.kchunks2; ++kc2) {
+      const uint64_t adesc = p1_desc0 + ((p.off_p1[b] - p.off_p1[0]) >> 4) +
+                             static_cast<uint64_t>(kc2) * (kPChunkBytes >> 4);
+      const uint64_t bdesc = res_w2 + static_cast<uint64_t>(kc2) * w2_step;
+      issue_chunk<true>(lead, d2, adesc, bdesc, idesc2, kc2 == p.kchunks2 - 1 ? last_nks2 : 4,
+                        kc2 == 0);
+    }
+    mma_f16_ss(lead, d2, ones_desc, bias2_desc, idesc_b2, 1u);   // D2 += bias
+    mma_commit(lead, bars + 8u * (BAR_D2_FULL0 + b));
+    trace(EV_MMA_G2_DONE, b, j);
+    return true;
+  };
+
   // GEMM1 of the tiles j and (if `two`) j + 1 from one group of W1 stages (w1_group):
   // the first tile waits for the stages, the second reads the same ones, and the stages
   // are released after both.
@@ -595,6 +634,20 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         }
         if (ok && k + 2 < ntiles) ok = issue_g0(k + 2);
         if (ok && k + 3 < ntiles) ok = issue_g0(k + 3);
+      }
+    } else if (MODE == MODE_CHAIN3) {
+      // Pairs of tiles, each GEMM for both tiles before the next GEMM: while one tile's
+      // epilogue drains an accumulator, the other tile's MMAs run.  Buffer b's D0, D1, D2
+      // and P0, P1 are free again for tile k + 2 because the group that drains them works
+      // through its tiles in order and the MMAs complete in issue order.
+      for (int k = 0; ok && k < ntiles; k += 2) {
+        const bool two = k + 1 < ntiles;
+        ok = issue_g0(k);
+        if (ok && two) ok = issue_g0(k + 1);
+        if (ok) ok = issue_g1(k);
+        if (ok && two) ok = issue_g1(k + 1);
+        if (ok) ok = issue_g2(k);
+        if (ok && two) ok = issue_g2(k + 1);
       }
     } else if (MODE == MODE_CHAIN) {
       // A D0 buffer is free again once the epilogue has published that tile's P, so
@@ -900,8 +953,56 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
     }
   };
 
+  // Three-operator chain, middle: GEMM1's accumulator -> P1 (shared memory) -> P1_FULL.
+  auto epi1_p1 = [&](int it) {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    const uint32_t b = buf_of(p, it), u = use_of(p, it);
+    alive = warp_wait(alive, bars + 8u * (BAR_D1_FULL0 + b), u, p, abort_flag,
+                      SITE_EPI_D1_FULL, t);
+    if (elected) trace(EV_EPI_D1_READY, g, it);
+    tc_fence_after_sync();
+    if (alive)
+      drain_to_smem<BF16>(p.act1, tm_lane, p.d1_col[b], c_first, c_step, p.N1p,
+                          base + p.off_p1[b], row, kPChunkBytes);
+    tc_fence_before_sync();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8u * (BAR_P1_FULL0 + b));
+    if (elected) trace(EV_EPI_P1_DONE, g, it);
+  };
+
+  // Three-operator chain, last: GEMM2's accumulator -> output staging -> TMA store.
+  auto epi2 = [&](int it) {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    const TileCoord tc = tile_coord<A4D>(p, t);
+    const uint32_t b = buf_of(p, it), u = use_of(p, it);
+    alive = warp_wait(alive, bars + 8u * (BAR_D2_FULL0 + b), u, p, abort_flag,
+                      SITE_EPI_D2_FULL, t);
+    tc_fence_after_sync();
+    if (elected) bulk_wait_read_all();   // this group's staging is free again
+    named_bar_sync(bar_id, group_threads);
+    if (elected) trace(EV_EPI_STAGING, g, it);
+    if (alive)
+      drain_to_smem<BF16>(p.act2, tm_lane, p.d2_col[b], c_first, c_step, p.N2p, out_tile, row,
+                          kPChunkBytes);
+    tc_fence_before_sync();
+    fence_proxy_async_smem();
+    named_bar_sync(bar_id, group_threads);
+    if (elected && !*abort_flag) {
+      store_tile<A4D>(p, tmOut, out_tile, (p.N2p + 63) >> 6, tc);
+      bulk_commit_group();
+      trace(EV_EPI_STORED, g, it);
+    }
+  };
+
   const int ntiles = local_tiles(p);
-  if (MODE == MODE_CHAIN && p.nbuf_log2 == 2) {
+  if (MODE == MODE_CHAIN3) {
+    for (int it = g; it < ntiles; it += groups) {
+      epi0(it);
+      epi1_p1(it);
+      epi2(it);
+    }
+  } else if (MODE == MODE_CHAIN && p.nbuf_log2 == 2) {
     // Four buffers: the group runs the first half of its next tile before the second half
     // of the current one, so that it drains GEMM0 while GEMM1 of the current tile runs.
     if (g < ntiles) epi0(g);
@@ -970,17 +1071,19 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
 // fp32.  Written by the epilogue warps with generic stores.
 template <bool BF16>
 __device__ __forceinline__ void fill_bias_operands(const ChainParams& p, uint8_t* region,
-                                                   int tid, int nthreads, bool chain) {
+                                                   int tid, int nthreads, int ngemms) {
   const int n0blk = (p.N0p + 63) >> 6;
-  const int n1blk = chain ? (p.N1p + 63) >> 6 : 0;
-  // Each thread fetches its element of both bias rows first (N <= 256 <= nthreads), so
+  const int n1blk = ngemms >= 2 ? (p.N1p + 63) >> 6 : 0;
+  const int n2blk = ngemms >= 3 ? (p.N2p + 63) >> 6 : 0;
+  // Each thread fetches its element of every bias row first (N <= 256 <= nthreads), so
   // the global loads overlap the fill below instead of following one another.
   const uint16_t v0 = (tid < p.N0 && p.b0 != nullptr) ? p.b0[tid] : uint16_t(0);
-  const uint16_t v1 = (chain && tid < p.N1 && p.b1 != nullptr) ? p.b1[tid] : uint16_t(0);
+  const uint16_t v1 = (ngemms >= 2 && tid < p.N1 && p.b1 != nullptr) ? p.b1[tid] : uint16_t(0);
+  const uint16_t v2 = (ngemms >= 3 && tid < p.N2 && p.b2 != nullptr) ? p.b2[tid] : uint16_t(0);
   // ONES, and every byte of the BIAS blocks but their k-row 0 (bytes [0, 128) of a block).
   uint32_t* words = reinterpret_cast<uint32_t*>(region);
-  const int nwords =
-      (static_cast<int>(kOnesBytes) + (n0blk + n1blk) * static_cast<int>(kBiasBlockBytes)) >> 2;
+  const int nwords = (static_cast<int>(kOnesBytes) +
+                      (n0blk + n1blk + n2blk) * static_cast<int>(kBiasBlockBytes)) >> 2;
   const uint32_t one = BF16 ? 0x3F80u : 0x3C00u;
   for (int w = tid; w < nwords; w += nthreads) {
     const int o = w << 2;
@@ -994,6 +1097,29 @@ __device__ __forceinline__ void fill_bias_operands(const ChainParams& p, uint8_t
   constexpr int kBlockHalves = static_cast<int>(kBiasBlockBytes / 2);
   if (tid < n0blk * 64) halves[(tid >> 6) * kBlockHalves + (tid & 63)] = v0;
   if (tid < n1blk * 64) halves[(n0blk + (tid >> 6)) * kBlockHalves + (tid & 63)] = v1;
+  if (tid < n2blk * 64) halves[(n0blk + n1blk + (tid >> 6)) * kBlockHalves + (tid & 63)] = v2;
+}
+
+// W2 [N1][N2] (row-major, global) -> the resident MN-major layout GEMM2 reads, as a TMA
+// load with 128-byte swizzle would lay it out: per 64-row K chunk kc and 64-wide N block
+// nb an 8 KiB block, K-row r at r * 128 bytes, its 16-byte unit j (columns 8j..8j+7) at
+// unit j ^ (r % 8); rows beyond N1 and columns beyond N2 are zero.  Generic stores by the
+// epilogue warps, before they release the bias operands (the MMA issuer waits for those
+// before the first MMA that could read W2).
+__device__ __forceinline__ void fill_w2(const ChainParams& p, uint8_t* dst, int tid,
+                                        int nthreads) {
+  const int nblk = (p.N2p + 63) >> 6;
+  const int units = p.kchunks2 * nblk * 64 * 8;   // 16-byte units
+  for (int u = tid; u < units; u += nthreads) {
+    const int j = u & 7, r = (u >> 3) & 63, blk = u >> 9;
+    const int nb = blk % nblk, kc = blk / nblk;
+    const int k = kc * 64 + r, n = nb * 64 + j * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (k < p.N1 && n < p.N2)
+      v = *reinterpret_cast<const uint4*>(p.w2 + static_cast<size_t>(k) * p.N2 + n);
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(kc) * p.w2_chunk_bytes + nb * 8192 +
+                              r * 128 + ((j ^ (r & 7)) << 4)) = v;
+  }
 }
 
 // ------------------------------------------------------------------------------------
@@ -1028,6 +1154,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars + 8u * (BAR_ACC_EMPTY0 + a), warps_per_group);
       mbar_init(bars + 8u * (BAR_P_FULL0 + a), warps_per_group);
       mbar_init(bars + 8u * (BAR_D1_FULL0 + a), 1);
+      mbar_init(bars + 8u * (BAR_P1_FULL0 + a), warps_per_group);
+      mbar_init(bars + 8u * (BAR_D2_FULL0 + a), 1);
     }
     mbar_init(bars + 8u * BAR_MMA_DONE, 1);
     mbar_init(bars + 8u * BAR_BIAS_READY, kNumEpiWarps);
@@ -1042,7 +1170,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmW0);
-    if (MODE == MODE_CHAIN) tma_prefetch_desc(&tmW1);
+    if (MODE == MODE_CHAIN || MODE == MODE_CHAIN3) tma_prefetch_desc(&tmW1);
     tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
@@ -1065,7 +1193,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (p.pf_second) prefetch_a_tile(p, blockIdx.x + gridDim.x);
       if (blockIdx.x == 0) {
         bulk_prefetch_l2(p.pf_w0, p.pf_w0_bytes);
-        if (MODE == MODE_CHAIN) bulk_prefetch_l2(p.pf_w1, p.pf_w1_bytes);
+        if (MODE == MODE_CHAIN || MODE == MODE_CHAIN3) bulk_prefetch_l2(p.pf_w1, p.pf_w1_bytes);
       }
     }
     __syncwarp();
@@ -1082,7 +1210,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // before its first MMA.
     grid_dependency_wait();
     fill_bias_operands<BF16>(p, base_ptr + p.off_bias, static_cast<int>(threadIdx.x) - 64,
-                             kNumEpiThreads, MODE == MODE_CHAIN);
+                             kNumEpiThreads,
+                             MODE == MODE_CHAIN3 ? 3 : (MODE == MODE_CHAIN ? 2 : 1));
+    if (MODE == MODE_CHAIN3)
+      fill_w2(p, base_ptr + p.off_w2, static_cast<int>(threadIdx.x) - 64, kNumEpiThreads);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8u * BAR_BIAS_READY);

@@ -10,6 +10,7 @@ enum ChainMode : int {
   MODE_CHAIN = 0,   // GEMM0 -> epilogue0 -> P (smem) -> GEMM1 -> epilogue1 -> global
   MODE_SINGLE = 1,  // GEMM0 -> epilogue0 -> global (one operator of the unfused path)
   MODE_POOL = 2,    // GEMM0 (conv) -> 2x2 max -> bias -> ReLU -> global (pooled)
+  MODE_CHAIN3 = 3,  // GEMM0 -> P0 (smem) -> GEMM1 -> P1 (smem) -> GEMM2 -> global
 };
 
 // Kernel ids recorded in the device error word.
@@ -21,6 +22,7 @@ enum KernelId : uint32_t {
   KID_CONV1X1_SINGLE = 5,
   KID_CONV_SINGLE = 6,
   KID_CONV_POOL = 7,
+  KID_GEMM_CHAIN3 = 8,
   KID_PROBE = 15,
 };
 
@@ -36,6 +38,8 @@ enum WaitSite : uint32_t {
   SITE_EPI_D1_FULL = 8,
   SITE_PRODUCER_DRAIN = 9,
   SITE_PROBE = 10,
+  SITE_MMA_P1_FULL = 11,
+  SITE_EPI_D2_FULL = 12,
 };
 
 // Events of the optional trace: one CTA's roles stamp clock64() at these points.
@@ -60,6 +64,8 @@ enum TraceEvent : uint32_t {
   EV_EPI_DRAINED = 18,     // epilogue group's elected thread finished its output drain
   EV_SETUP_DONE = 19,      // barriers initialised and TMEM allocated (after __syncthreads)
   EV_DEP_READY = 20,       // the MMA warp's wait for the previous grid returned
+  EV_EPI_P1_DONE = 21,     // three-operator chain: epilogue group published P1
+  EV_MMA_G2_DONE = 22,     // three-operator chain: GEMM2 of a tile issued and committed
 };
 
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M
@@ -99,6 +105,16 @@ struct ChainParams {
   int32_t act0, act1;
   const uint16_t* b0;   // may be null
   const uint16_t* b1;   // may be null
+  // --- three-operator chain (MODE_CHAIN3): GEMM2 over P1 = act1(D1) ------------------
+  int32_t N2, N2p;      // GEMM2 output width, padded to 16
+  int32_t kchunks2;     // 64-wide K chunks of GEMM2 (= ceil(N1p / 64))
+  int32_t act2;
+  const uint16_t* b2;   // may be null
+  const uint16_t* w2;   // W2 [N1][N2] row-major in global memory; the epilogue warps copy
+                        //    it into the swizzled resident layout at off_w2
+  uint32_t w2_chunk_bytes, off_w2;
+  uint32_t off_p1[2];   // P1 buffers (K-major, swizzled like P)
+  uint32_t d2_col[2];   // TMEM columns of the GEMM2 accumulators
   // L2 prefetch (warming only): 2-D A (null for the implicit-GEMM conv A) with the bytes of
   // one 128-row tile and of the whole tensor, and the weights' bytes.
   const uint8_t* pf_a;

@@ -29,6 +29,7 @@ const void* variant_func_a2d(Variant v) {
     case V_CONV1X1_CHAIN: return kernel_ptr<MODE_CHAIN, false, false, false, BF16>();
     case V_GEMM_SINGLE: return kernel_ptr<MODE_SINGLE, false, true, false, BF16>();
     case V_CONV1X1_SINGLE: return kernel_ptr<MODE_SINGLE, false, false, false, BF16>();
+    case V_GEMM_CHAIN3: return kernel_ptr<MODE_CHAIN3, false, true, true, BF16>();
     default: return nullptr;
   }
 }
@@ -46,6 +47,8 @@ cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMa
       return launch_one<MODE_SINGLE, false, true, false, BF16>(a, w0, w1, out, p, grid, smem, s);
     case V_CONV1X1_SINGLE:
       return launch_one<MODE_SINGLE, false, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    case V_GEMM_CHAIN3:
+      return launch_one<MODE_CHAIN3, false, true, true, BF16>(a, w0, w1, out, p, grid, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -20,6 +20,7 @@ enum Variant : int {
   V_CONV1X1_SINGLE,
   V_CONV_SINGLE,
   V_CONV_POOL,
+  V_GEMM_CHAIN3,
   V_COUNT
 };
 

@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
         L.b2b_set_trace.argtypes = [vp, ctypes.c_uint32, ctypes.c_uint32]
         L.b2b_set_trace.restype = ci
         p64 = ctypes.POINTER(i64)
+        L.b2b_gemm3.argtypes = [ci, i64, i32, i32, i32, i32, vp, vp, vp, ci, vp, vp, ci, vp, vp,
+                                ci, vp, vp]
+        L.b2b_gemm3.restype = ci
         L.b2b_conv_nhwc_strided.argtypes = [ci, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32,
                                             i32, vp, ci, vp, i32, vp, ci, vp, vp]
         L.b2b_conv_nhwc_strided.restype = ci
@@ -168,6 +171,29 @@ def b2b_gemm(A, W0, b0, W1, b1, epi0="relu", epi1="relu", out=None, stream=None)
 
 def _conv_out(n, pad, k, stride):
     return 0 if n + 2 * pad < k else (n + 2 * pad - k) // stride + 1
+
+
+def b2b_gemm3(A, W0, b0, W1, b1, W2, b2, epi0="relu", epi1="relu", epi2="relu", out=None,
+              stream=None):
+    """out = epi2(epi1(epi0(A @ W0 + b0) @ W1 + b1) @ W2 + b2) in one launch (b2b_gemm3).
+    A [M,K0], W0 [K0,N0], W1 [N0,N1], W2 [N1,N2] -> out [M,N2]."""
+    dt = A.dtype
+    M, K0 = A.shape
+    N0, N1, N2 = W0.shape[1], W1.shape[1], W2.shape[1]
+    _check_tensor(A, "A", dt, (M, K0))
+    _check_tensor(W0, "W0", dt, (K0, N0))
+    _check_tensor(W1, "W1", dt, (N0, N1))
+    _check_tensor(W2, "W2", dt, (N1, N2))
+    for name, b, n in (("b0", b0, N0), ("b1", b1, N1), ("b2", b2, N2)):
+        if b is not None:
+            _check_tensor(b, name, dt, (n,))
+    if out is None:
+        out = torch.empty((M, N2), dtype=dt, device=A.device)
+    _check_tensor(out, "out", dt, (M, N2))
+    _raise(lib().b2b_gemm3(_dtype_code(A), M, K0, N0, N1, N2, _ptr(A), _ptr(W0), _ptr(b0),
+                           _epi(epi0), _ptr(W1), _ptr(b1), _epi(epi1), _ptr(W2), _ptr(b2),
+                           _epi(epi2), _ptr(out), _stream(stream)), "b2b_gemm3")
+    return out
 
 
 def b2b_conv_nhwc(x, W0, b0, W1, b1, pad=1, epi0="relu", epi1="relu", out=None, stream=None):
@@ -332,10 +358,11 @@ PLAN_FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring",
                "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0",
                "kchunks1", "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo",
                "a_stage_bytes", "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2",
-               "d1_col3", "cand", "ncand", "grid_choice", "pf_choice", "ring_extend"]
+               "d1_col3", "cand", "ncand", "grid_choice", "pf_choice", "ring_extend", "off_w2",
+               "off_p1_0", "off_p1_1", "d2_col0", "d2_col1"]
 _SIGNED_PLAN_FIELDS = ("grid_choice", "pf_choice")
 PLAN_KINDS = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
-              "conv_relu_maxpool": 4}
+              "conv_relu_maxpool": 4, "b2b_gemm3": 5}
 
 
 def debug_plan(kind: str, dims) -> dict:
@@ -413,7 +440,8 @@ TRACE_EVENTS = {1: "prod_acquire", 2: "prod_issued", 3: "mma_full", 4: "mma_g0_d
                 9: "epi_p_done", 10: "epi_d1_ready", 11: "epi_staging", 12: "epi_stored",
                 13: "mma_wait", 14: "mma_issued",
                 15: "prod_w1_issued", 16: "mma_w1_full",
-                17: "kernel_entry", 18: "epi_drained", 19: "setup_done", 20: "dep_ready"}
+                17: "kernel_entry", 18: "epi_drained", 19: "setup_done", 20: "dep_ready",
+                21: "epi_p1_done", 22: "mma_g2_done"}
 
 
 def set_trace(buf, cta: int = 0) -> None:

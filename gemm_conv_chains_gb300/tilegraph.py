@@ -51,6 +51,11 @@ def propagate(w) -> TileGraph:
         return TileGraph("gemm_chain", {"out": (TILE_M, w.N1), "P": (TILE_M, w.N0),
                                         "W1": (w.N0, w.N1), "A": (TILE_M, w.K0),
                                         "W0": (w.K0, w.N0)})
+    if isinstance(w, wl.GemmChain3):
+        return TileGraph("gemm_chain3", {"out": (TILE_M, w.N2), "P1": (TILE_M, w.N1),
+                                         "W2": (w.N1, w.N2), "P0": (TILE_M, w.N0),
+                                         "W1": (w.N0, w.N1), "A": (TILE_M, w.K0),
+                                         "W0": (w.K0, w.N0)})
     if isinstance(w, wl.ConvChain):
         return TileGraph("conv_chain", {"out": (TILE_H, TILE_W, w.C1),
                                         "P": (TILE_H, TILE_W, w.C0), "W1": (w.C1, w.C0),
@@ -80,6 +85,8 @@ def plan_of(w) -> dict:
     from . import ops
     if isinstance(w, wl.GemmChain):
         return ops.debug_plan("b2b_gemm", (w.M, w.K0, w.N0, w.N1))
+    if isinstance(w, wl.GemmChain3):
+        return ops.debug_plan("b2b_gemm3", (w.M, w.K0, w.N0, w.N1, w.N2))
     if isinstance(w, wl.ConvChain):
         return ops.debug_plan("b2b_conv_nhwc", (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1,
                                                 w.stride))
@@ -151,6 +158,15 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
     out["A"] = tiles * a_tile
     w0 = plan["kchunks0"] * plan["w0_chunk"]
     w1 = plan["kchunks1"] * plan["w1_chunk"]
+    if isinstance(w, wl.GemmChain3):
+        # W0, W1 by TMA boxes and W2 by the epilogue warps' loads (its bytes, unpadded),
+        # once per CTA
+        out["W0"], out["W1"] = ctas * w0, ctas * w1
+        out["W2"] = ctas * w.N1 * w.N2 * ELEM
+        out["bias"] = ctas * (w.N0 + w.N1 + w.N2) * ELEM
+        out["total"] = sum(out.values())
+        out["A_in_bounds"] = w.M * w.K0 * ELEM
+        return out
     if plan["resident"]:
         out["W0"] = ctas * w0
         if w1:
@@ -222,6 +238,13 @@ def chain_buffers(plan: dict) -> List[Buffer]:
             Buffer("bar", plan["bar"], whole)]
     if plan["resident"]:
         bufs.append(Buffer("weights", plan["w_res"], whole))
+    if plan["mode"] == 3:
+        # three-operator chain: two tiles in flight hold P0, P1 and the staging of both
+        p1 = (plan["off_p1_1"] - plan["off_p1_0"])
+        for b in range(2):
+            bufs += [Buffer(f"P0{b}", plan["p"], whole), Buffer(f"P1{b}", p1, whole),
+                     Buffer(f"out{b}", plan["out"], whole)]
+        return bufs
     chain = plan["mode"] == 0
     pbufs = plan["nbuf"] if (chain and not plan["p_tmem"]) else 0
     p_bytes = (plan["N0p"] + 63) // 64 * 128 * 128

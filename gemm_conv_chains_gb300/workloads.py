@@ -70,6 +70,36 @@ class GemmChain:
 
 
 @dataclasses.dataclass(frozen=True)
+class GemmChain3:
+    """Three-operator chain: out[M,N2] = act2(act1(act0(A W0 + b0) W1 + b1) W2 + b2)."""
+    name: str
+    dtype: str
+    M: int
+    K0: int
+    N0: int
+    N1: int
+    N2: int
+    act0: str
+    act1: str
+    act2: str
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * (self.K0 * self.N0 + self.N0 * self.N1 + self.N1 * self.N2)
+
+    @property
+    def floor_bytes(self) -> int:
+        e = 2
+        return e * (self.M * self.K0 + self.K0 * self.N0 + self.N0 * self.N1 + self.N1 * self.N2
+                    + self.N0 + self.N1 + self.N2 + self.M * self.N2)
+
+    @property
+    def unfused_bytes(self) -> int:
+        """Floor plus both intermediates written and read back."""
+        return self.floor_bytes + 2 * 2 * self.M * (self.N0 + self.N1)
+
+
+@dataclasses.dataclass(frozen=True)
 class ConvChain:
     """conv RxS (pad, stride) + b0 + act0 -> conv1x1 + b1 + act1, NHWC."""
     name: str
@@ -152,8 +182,11 @@ CONV_POOL = ConvPool("conv_pool", "f16", 32, 112, 112, 64, 64)
 CONV3X3S2_1X1 = ConvChain("conv3x3s2_1x1", "f16", 32, 56, 56, 64, 128, 3, 3, 1, 128, "relu",
                           "none", stride=2)
 
+# A three-operator MLP head: 128 -> 128 -> 64 -> 64 over 32768 rows, bf16.
+MLP3 = GemmChain3("mlp3", "bf16", 32768, 128, 128, 64, 64, "hardswish", "hardswish", "none")
+
 WORKLOADS = {w.name: w for w in (GEMM_SMALL, GEMM_FFN, CONV1X1, CONV3X3_1X1, CONV_POOL,
-                                 CONV3X3S2_1X1)}
+                                 CONV3X3S2_1X1, MLP3)}
 FFN_SWEEP_M = [4096, 8192, 16384, 32768, 65536, 131072, 262144]
 
 
@@ -201,6 +234,24 @@ def gemm_inputs(w: GemmChain, seed: int = 0, integer: bool = False) -> Dict[str,
         out["b0"] = None
         out["b1"] = None
     return {k: (v.to(dt).contiguous() if v is not None else None) for k, v in out.items()}
+
+
+def gemm3_inputs(w: GemmChain3, seed: int = 0, integer: bool = False) -> Dict[str, torch.Tensor]:
+    """A [M,K0], W0 [K0,N0], b0, W1 [N0,N1], b1, W2 [N1,N2], b2 on the CPU, storage dtype.
+    Integer data are in {-1, 0, 1} (biases too), so that three layers of sums stay exact
+    and, for these sizes, finite in fp16."""
+    g = _gen(seed)
+    dt = DTYPES[w.dtype]
+    dims = [(w.K0, w.N0), (w.N0, w.N1), (w.N1, w.N2)]
+    if integer:
+        A = _ints(g, (w.M, w.K0), -1, 1)
+        ws = [(_ints(g, d, -1, 1), _ints(g, (d[1],), -1, 1)) for d in dims]
+    else:
+        A = _uniform(g, (w.M, w.K0), -1, 1)
+        ws = [(_normal(g, d, 1.0 / math.sqrt(d[0])), _uniform(g, (d[1],), -0.1, 0.1)) for d in dims]
+    out = {"A": A, "W0": ws[0][0], "b0": ws[0][1], "W1": ws[1][0], "b1": ws[1][1],
+           "W2": ws[2][0], "b2": ws[2][1]}
+    return {k: v.to(dt).contiguous() for k, v in out.items()}
 
 
 def conv_inputs(w: ConvChain, seed: int = 0, integer: bool = False) -> Dict[str, torch.Tensor]:

@@ -92,6 +92,21 @@ b2b_status b2b_gemm(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
                     const void* W1, const void* b1, b2b_epilogue e1,
                     void* D, void* stream);
 
+/* D[M,N2] = e2( e1( e0( A . W0 + b0 ) . W1 + b1 ) . W2 + b2 ): three operators in one
+ * persistent kernel (BOLT notes, "Enabling deeper operator fusion": more GEMMs fused into
+ * one operator, no load or store of the intermediates).  Both intermediates are rounded
+ * to dt and kept in shared memory; the three weights stay resident in shared memory.
+ *   A  [M][K0]  row-major      W0 [K0][N0] row-major     b0 [N0] or NULL
+ *   W1 [N0][N1] row-major      b1 [N1] or NULL
+ *   W2 [N1][N2] row-major      b2 [N2] or NULL           D  [M][N2] row-major (output)
+ * Limits as b2b_gemm for each size, and two tiles of D0, D1, D2 accumulators must fit the
+ * 512 TMEM columns (N0 + N1 + N2 <= 256 once each is rounded up to 32) and the resident
+ * weights beside two ring stages of A: B2B_ERR_UNSUPPORTED otherwise. */
+b2b_status b2b_gemm3(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1, int32_t N2,
+                     const void* A, const void* W0, const void* b0, b2b_epilogue e0,
+                     const void* W1, const void* b1, b2b_epilogue e1, const void* W2,
+                     const void* b2, b2b_epilogue e2, void* D, void* stream);
+
 /* y = conv1x1_{W1,b1,e1}( conv_{W0,b0,e0}(x) ), stride 1, dilation 1, zero padding `pad`,
  * cross-correlation (implicit GEMM; interview notes "Conv optimisation", item 2; BOLT
  * notes "Persistent kernel fusion" for the conv case, ThreadBlock_N = output channels).
@@ -223,7 +238,8 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  *   kind 2 b2b_conv_nhwc       dims = {N, H, W, C, C0, R, S, pad, C1[, stride]}
  *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad[, stride]}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
- * out (out_len >= 52) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ *   kind 5 b2b_gemm3           dims = {M, K0, N0, N1, N2}
+ * out (out_len >= 57) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
  * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
  * P offsets [2], bytes per P buffer, staging offsets [2], bytes per staging buffer,
@@ -240,8 +256,9 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * feasible layouts, and the pinned or measured grid and second-tile-prefetch choices
  * (b2b_set_choice; -1, as a two's-complement word, for the default), and the ring stages
  * a launch adds over the output staging when no CTA gets more than two tiles (P in TMEM,
- * streamed weights; the staging is first written after the pair's last GEMM0).  A choice
- * pinned or measured for these sizes is reflected.
+ * streamed weights; the staging is first written after the pair's last GEMM0), then, for
+ * the three-operator chain, the resident W2 offset, P1 offsets [2] and GEMM2 accumulator
+ * columns [2] (0 otherwise).  A choice pinned or measured for these sizes is reflected.
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,

@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
     for n in ("b2b_gemm", "b2b_conv_nhwc", "conv_relu_maxpool", "gemm_bias_act",
               "conv_bias_act_nhwc", "maxpool2x2_nhwc", "b2b_status_str", "b2b_get_device_error",
               "b2b_conv_nhwc_strided", "conv_bias_act_nhwc_strided", "b2b_set_autotune",
-              "b2b_set_choice", "b2b_get_choice", "b2b_fold_batchnorm"):
+              "b2b_set_choice", "b2b_get_choice", "b2b_fold_batchnorm", "b2b_gemm3"):
         assert n in names
 
 
@@ -124,6 +124,21 @@ def test_single_operator_argument_checks(L):
     assert L.conv_bias_act_nhwc(F16, 1, 4, 4, 64, FAKE, FAKE, 64, 3, 3, 5, None, 1, FAKE, None) == UNSUP
     assert L.maxpool2x2_nhwc(F16, 1, 4, 4, 12, FAKE, FAKE, None) == ALIGN
     assert L.maxpool2x2_nhwc(F16, 1, 1, 4, 16, FAKE, FAKE, None) == SHAPE
+
+
+def gemm3(L, dt=F16, M=256, K0=64, N0=64, N1=64, N2=64, A=FAKE, W0=FAKE, b0=None, e0=1, W1=FAKE,
+          b1=None, e1=1, W2=FAKE, b2=None, e2=0, D=FAKE):
+    return L.b2b_gemm3(dt, M, K0, N0, N1, N2, A, W0, b0, e0, W1, b1, e1, W2, b2, e2, D, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(e2=3), UNSUP), (dict(N2=0), SHAPE), (dict(N2=12), ALIGN), (dict(N2=264), UNSUP),
+    (dict(N0=128, N1=128), UNSUP),            # two tiles of D0, D1, D2 exceed 512 columns
+    (dict(W2=None), NULL), (dict(W2=MIS), ALIGN), (dict(b2=FAKE + 1), ALIGN),
+    (dict(M=0, A=None, D=None), OK),
+])
+def test_b2b_gemm3_argument_checks(L, kw, expect):
+    assert gemm3(L, **kw) == expect
 
 
 def fold(L, dt=F16, Co=64, K=576, out_inner=0, W=FAKE, b=None, g=FAKE, be=FAKE, m=FAKE, v=FAKE,

@@ -36,6 +36,13 @@ def _gemm(w, seed=5):
                                                   w.act0, w.act1)
 
 
+def _gemm3(w, seed=8):
+    t = {k: v.cuda() for k, v in wl.gemm3_inputs(w, seed=seed).items()}
+    dims = (w.M, w.K0, w.N0, w.N1, w.N2)
+    return "b2b_gemm3", dims, lambda: ops.b2b_gemm3(
+        *(t[k] for k in ("A", "W0", "b0", "W1", "b1", "W2", "b2")), w.act0, w.act1, w.act2)
+
+
 def _conv(w, seed=6):
     t = {k: v.cuda() for k, v in wl.conv_inputs(w, seed=seed, integer=w.R > 1).items()}
     dims = (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1)
@@ -61,6 +68,9 @@ PROBLEMS = {
     "conv3x3": lambda: _conv(wl.ConvChain("c3", "bf16", 4, 56, 56, 64, 64, 3, 3, 1, 128,
                                           "hardswish", "none")),
     "pool": lambda: _pool(wl.ConvPool("p", "f16", 4, 112, 112, 64, 64)),
+    # three-operator chain, 313 tiles (pairs and an odd last tile per CTA)
+    "gemm3": lambda: _gemm3(wl.GemmChain3("g3", "bf16", 40000, 128, 128, 64, 64, "hardswish",
+                                          "relu", "none")),
 }
 
 

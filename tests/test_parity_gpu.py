@@ -149,6 +149,52 @@ def test_gemm_bias_act(shape, integer):
 
 
 # ------------------------------------------------------------------------------------
+# three-operator chain (BOLT notes, "Enabling deeper operator fusion")
+# ------------------------------------------------------------------------------------
+GEMM3_SHAPES = [
+    # dtype, M, K0, N0, N1, N2
+    ("f16", 1, 64, 64, 64, 64),
+    ("bf16", 1000, 64, 64, 64, 64),
+    ("f16", 257, 72, 40, 24, 96),        # padded widths, ragged rows
+    ("bf16", 129, 8, 8, 8, 8),
+    ("f16", 40000, 128, 128, 64, 64),    # 313 tiles: pairs and an odd last tile per CTA
+    ("bf16", 300, 128, 96, 64, 64),
+]
+
+
+def run_gemm3(shape, acts, integer, seed, rows=None):
+    dt, M, K0, N0, N1, N2 = shape
+    w = wl.GemmChain3("g3", dt, M, K0, N0, N1, N2, *acts)
+    t = wl.gemm3_inputs(w, seed=seed, integer=integer)
+    out = ops.b2b_gemm3(*(to_dev(t[k]) for k in ("A", "W0", "b0", "W1", "b1", "W2", "b2")), *acts)
+    torch.cuda.synchronize()
+    check_no_device_error()
+    b = {k: wl.to_bits(v) for k, v in t.items()}
+    sel = slice(None) if rows is None else rows
+    ref = oracle.b2b_gemm3(dt, b["A"][sel], b["W0"], b["b0"], b["W1"], b["b1"], b["W2"], b["b2"],
+                           *acts)
+    return compare(dt, wl.to_bits(out.cpu())[sel], ref, integer, "b2b_gemm3")
+
+
+@pytest.mark.parametrize("shape", GEMM3_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_b2b_gemm3_integer_exact(shape):
+    rows = np.r_[0:600, 39400:40000] if shape[1] > 5000 else None
+    run_gemm3(shape, ("relu", "relu", "none"), True, seed=shape[1] + 3, rows=rows)
+
+
+@pytest.mark.parametrize("shape", GEMM3_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_b2b_gemm3_random(shape):
+    rows = np.r_[0:600, 19000:19300, 39400:40000] if shape[1] > 5000 else None
+    run_gemm3(shape, ("hardswish", "relu", "hardswish"), False, seed=shape[1] + 4, rows=rows)
+
+
+def test_mlp3_workload_sampled_rows():
+    w = wl.MLP3
+    run_gemm3(("bf16", w.M, w.K0, w.N0, w.N1, w.N2), (w.act0, w.act1, w.act2), False, seed=0,
+              rows=np.r_[0:256, 16000:16128, w.M - 256:w.M])
+
+
+# ------------------------------------------------------------------------------------
 # b2b conv
 # ------------------------------------------------------------------------------------
 CONV_SHAPES = [

@@ -22,16 +22,17 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "d0_col1", "d1_col0", "d1_col1", "dual", "groups", "tiles", "kchunks0", "kchunks1",
           "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes",
           "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2", "d1_col3", "cand", "ncand",
-          "grid_choice", "pf_choice", "ring_extend"]
+          "grid_choice", "pf_choice", "ring_extend", "off_w2", "off_p1_0", "off_p1_1", "d2_col0",
+          "d2_col1"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
-        "conv_relu_maxpool": 4}
+        "conv_relu_maxpool": 4, "b2b_gemm3": 5}
 
 
 def plan(kind, dims):
     arr = (ctypes.c_int64 * len(dims))(*dims)
-    out = (ctypes.c_uint32 * 52)()
-    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 52)
+    out = (ctypes.c_uint32 * 57)()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 57)
     return st, dict(zip(FIELDS, list(out)))
 
 
@@ -264,3 +265,43 @@ def test_strided_conv_plans():
     assert plan("b2b_conv_nhwc", (4, 28, 28, 64, 128, 1, 1, 0, 64, 2))[1]["tiles"] == 4 * 2 * 1
     assert plan("b2b_conv_nhwc", (1, 9, 9, 64, 64, 3, 3, 1, 64, 5))[0] == 4     # stride > 4
     assert plan("b2b_conv_nhwc", (1, 9, 9, 64, 64, 3, 3, 1, 64, 0))[0] == 2
+
+
+@pytest.mark.parametrize("dims", [(1000, 64, 64, 64, 64), (32768, 128, 128, 64, 64),
+                                  (257, 72, 40, 24, 96), (129, 8, 8, 8, 8), (300, 128, 96, 64, 64)])
+def test_gemm3_plans(dims):
+    # three-operator chain: ring of A chunks, W0/W1/W2 resident, two P0, P1 and output
+    # buffers, bias blocks of three GEMMs; two tiles of D0, D1, D2 in TMEM
+    st, p = plan("b2b_gemm3", dims)
+    assert st == 0, st
+    M, K0, N0, N1, N2 = dims
+    r16 = lambda n: -(-n // 16) * 16
+    r32 = lambda n: -(-n // 32) * 32
+    n0b, n1b, n2b = (-(-r16(n) // 64) for n in (N0, N1, N2))
+    assert p["mode"] == 3 and p["resident"] == 1 and p["dual"] == 1 and p["groups"] == 2
+    assert p["stages"] >= 2 and p["stage_bytes"] == 16384 and p["smem"] <= SMEM_LIMIT
+    k0, k1, k2 = -(-K0 // 64), -(-r16(N0) // 64), -(-r16(N1) // 64)
+    assert p["kchunks0"] == k0 and p["kchunks1"] == k1
+    regions = [("ring", p["off_ring"], p["ring"]),
+               ("w0", p["off_w0"], k0 * n0b * 8192), ("w1", p["off_w1"], k1 * n1b * 8192),
+               ("w2", p["off_w2"], k2 * n2b * 8192),
+               ("p0a", p["off_p0"], n0b * 16384), ("p0b", p["off_p1"], n0b * 16384),
+               ("p1a", p["off_p1_0"], n1b * 16384), ("p1b", p["off_p1_1"], n1b * 16384),
+               ("outa", p["off_out0"], n2b * 16384), ("outb", p["off_out1"], n2b * 16384),
+               ("bias", p["off_bias"], 1024 + 2048 * (n0b + n1b + n2b)),
+               ("bar", p["off_bar"], 8 * 43 + 8)]
+    for name, off, size in regions:
+        assert off % 1024 == 0 and off + size <= p["smem"] - 1024, name
+    for (a, oa, sa), (b, ob, sb) in itertools.combinations(regions, 2):
+        assert oa + sa <= ob or ob + sb <= oa, (a, b)
+    cols = [(p[f"d{i}_col{b}"], r32(n)) for i, n in enumerate((N0, N1, N2)) for b in range(2)]
+    for c, n in cols:
+        assert c % 32 == 0 and c + n <= p["tmem_cols"] <= 512
+    for (ca, na), (cb, nb) in itertools.combinations(cols, 2):
+        assert ca + na <= cb or cb + nb <= ca
+
+
+def test_gemm3_limits():
+    assert plan("b2b_gemm3", (1000, 64, 128, 128, 64))[0] == 4   # 2 x (128 + 128 + 64) > 512
+    assert plan("b2b_gemm3", (1000, 64, 64, 64, 12))[0] == 3     # N2 not a multiple of 8
+    assert plan("b2b_gemm3", (1000, 8192, 128, 64, 64))[0] == 4  # W0 does not fit
