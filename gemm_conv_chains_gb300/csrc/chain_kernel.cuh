@@ -436,15 +436,19 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const int rem1 = p.N0p - (p.kchunks1 - 1) * kChunkK;
   const int last_nks1 = rem1 >= 64 ? 4 : (rem1 >> 4);
   // Three-operator chain: GEMM2 reads P1 (K-major, as P) and the resident W2 (MN-major).
-  const uint32_t idesc2 = idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N2p);
-  const uint64_t p1_desc0 = sdesc_sw128(base + p.off_p1[0], 16u, 1024u);
-  const uint64_t res_w2 = sdesc_sw128(base + p.off_w2, 8192u, 1024u);
+  // Other modes never read these (zero, so that they cost nothing).
+  constexpr bool kThree = MODE == MODE_CHAIN3;
+  const uint32_t idesc2 = kThree ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N2p) : 0u;
+  const uint64_t p1_desc0 = kThree ? sdesc_sw128(base + p.off_p1[0], 16u, 1024u) : 0u;
+  const uint64_t res_w2 = kThree ? sdesc_sw128(base + p.off_w2, 8192u, 1024u) : 0u;
   const uint32_t n1blk = static_cast<uint32_t>((p.N1p + 63) >> 6);
-  const uint64_t bias2_desc = sdesc_sw128(
-      ones_addr + kOnesBytes + (n0blk + n1blk) * kBiasBlockBytes, kBiasBlockBytes, 1024u);
-  const uint32_t idesc_b2 = idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N2p);
-  const uint32_t w2_step = p.w2_chunk_bytes >> 4;
-  const int rem2 = p.N1p - (p.kchunks2 - 1) * kChunkK;
+  const uint64_t bias2_desc =
+      kThree ? sdesc_sw128(ones_addr + kOnesBytes + (n0blk + n1blk) * kBiasBlockBytes,
+                           kBiasBlockBytes, 1024u)
+             : 0u;
+  const uint32_t idesc_b2 = kThree ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N2p) : 0u;
+  const uint32_t w2_step = kThree ? p.w2_chunk_bytes >> 4 : 0u;
+  const int rem2 = kThree ? p.N1p - (p.kchunks2 - 1) * kChunkK : 64;
   const int last_nks2 = rem2 >= 64 ? 4 : (rem2 >> 4);
 
   int stage = 0;
@@ -1154,8 +1158,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars + 8u * (BAR_ACC_EMPTY0 + a), warps_per_group);
       mbar_init(bars + 8u * (BAR_P_FULL0 + a), warps_per_group);
       mbar_init(bars + 8u * (BAR_D1_FULL0 + a), 1);
-      mbar_init(bars + 8u * (BAR_P1_FULL0 + a), warps_per_group);
-      mbar_init(bars + 8u * (BAR_D2_FULL0 + a), 1);
+      if (MODE == MODE_CHAIN3) {
+        mbar_init(bars + 8u * (BAR_P1_FULL0 + a), warps_per_group);
+        mbar_init(bars + 8u * (BAR_D2_FULL0 + a), 1);
+      }
     }
     mbar_init(bars + 8u * BAR_MMA_DONE, 1);
     mbar_init(bars + 8u * BAR_BIAS_READY, kNumEpiWarps);
