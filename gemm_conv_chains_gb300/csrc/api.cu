@@ -195,6 +195,17 @@ uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = fals
   const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
   for (uint32_t b = 0; b < kMaxBufs; ++b) p.d0_col[b] = p.d1_col[b] = 0;
   p.d2_col[0] = p.d2_col[1] = 0;
+  p.p_split = 0;
+  p.p_hi = 0;
+  if (mode == MODE_CHAIN && p_tmem && p.N0p > 256) {
+    // Wide: one buffer of 512 columns.  D0 = [0, N0p); P's halves pack in place into
+    // [0, 128) and [256, 256 + (N0p - 256) / 2); D1 = [128, 128 + N1p) between them.
+    p.p_split = 256u;
+    p.p_hi = 256u;
+    p.d0_col[0] = 0;
+    p.d1_col[0] = 128u;
+    return 512u;
+  }
   if (mode == MODE_CHAIN3) {
     // Two buffers of D0, D1, D2 each: tile i uses buffer i & 1.
     const uint32_t s1 = round_up(static_cast<uint32_t>(p.N1p), 32u);
@@ -266,16 +277,22 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
     const bool tmem_quad_ok = tmem_layout(probe, mode, 4u) <= 512u;
     const bool tmem_dual_ok = tmem_layout(probe, mode, 2u) <= 512u;
     const bool tmem_p_ok = tmem_layout(probe, mode, 2u, true) <= 512u;
-    // Four tiles in flight (narrow chains): each epilogue group one tile ahead.
-    if (tmem_quad_ok)
-      for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {4, 2, resident, 0, 0};
-    if (tmem_dual_ok)
+    if (p.N0p > 256) {
+      // Wide (256 < N0 <= 512, N1 <= 128): one tile in flight, P in TMEM, both
+      // warpgroups on every tile, weights streamed.
+      if (p.N1p <= 128) cands[ncand++] = {1, 1, 0, 0, 1};
+    } else {
+      // Four tiles in flight (narrow chains): each epilogue group one tile ahead.
+      if (tmem_quad_ok)
+        for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {4, 2, resident, 0, 0};
+      if (tmem_dual_ok)
+        for (int resident = 1; resident >= 0; --resident)
+          for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {2, 2, resident, alias, 0};
+      if (tmem_p_ok)
+        for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {2, 2, resident, 0, 1};
       for (int resident = 1; resident >= 0; --resident)
-        for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {2, 2, resident, alias, 0};
-    if (tmem_p_ok)
-      for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {2, 2, resident, 0, 1};
-    for (int resident = 1; resident >= 0; --resident)
-      for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {1, 1, resident, alias, 0};
+        for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {1, 1, resident, alias, 0};
+    }
   } else {
     // Pool staging is small: the warpgroups always take alternate tiles.
     const int gmin = mode == MODE_POOL ? 2 : 1;
@@ -338,7 +355,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   // shared by the two tiles of a pair -- if those stages fit the ring at once.
   p.w1_group = 0;
   p.w1_per_stage = 1;
-  if (mode == MODE_CHAIN && k.p_tmem && !k.resident) {
+  if (mode == MODE_CHAIN && k.p_tmem && !k.resident && p.p_split == 0u) {
     const uint32_t per = std::max(1u, p.stage_bytes / p.w1_chunk_bytes);
     const uint32_t stages = (static_cast<uint32_t>(p.kchunks1) + per - 1) / per;
     if (stages <= p.num_stages) {
@@ -990,7 +1007,7 @@ b2b_status b2b_gemm(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
   if (M < 0 || K0 <= 0 || N0 <= 0 || N1 <= 0) return B2B_ERR_SHAPE;
   b2b_status st;
   if ((st = check_channels(K0, kMaxReduction)) != B2B_OK) return st;
-  if ((st = check_channels(N0, 256)) != B2B_OK) return st;
+  if ((st = check_channels(N0, 512)) != B2B_OK) return st;
   if ((st = check_channels(N1, 256)) != B2B_OK) return st;
   if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
   if (M == 0) return B2B_OK;
@@ -1268,7 +1285,7 @@ static b2b_status plan_for_kind(int32_t kind, const int64_t* dims, int32_t ndims
   switch (kind) {
     case 0:   // b2b_gemm: M, K0, N0, N1
       if ((st = check_channels(d1, kMaxReduction)) != B2B_OK) return st;
-      if ((st = check_channels(d2, 256)) != B2B_OK) return st;
+      if ((st = check_channels(d2, 512)) != B2B_OK) return st;
       if ((st = check_channels(d3, 256)) != B2B_OK) return st;
       ok = gemm_params(p, MODE_CHAIN, true, dims[0], d1, d2, d3, &smem, &r, forced);
       break;
@@ -1319,7 +1336,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   b2b_status st = check_plan_args(kind, dims, ndims);
   if (st != B2B_OK) return st;
   if (out == nullptr) return B2B_ERR_NULL;
-  if (out_len < 57) return B2B_ERR_SHAPE;
+  if (out_len < 58) return B2B_ERR_SHAPE;
   Choice c;
   find_choice(plan_key(kind, dims, ndims), &c);
   ChainParams p;
@@ -1327,7 +1344,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
   if ((st = plan_for_kind(kind, dims, ndims, c.cand, p, r, smem, mode)) != B2B_OK) return st;
-  const uint32_t v[57] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[58] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -1343,7 +1360,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           p.d1_col[2], p.d1_col[3], static_cast<uint32_t>(r.cand),
                           static_cast<uint32_t>(r.ncand), static_cast<uint32_t>(c.grid),
                           static_cast<uint32_t>(c.pf2), r.extend, p.off_w2, p.off_p1[0],
-                          p.off_p1[1], p.d2_col[0], p.d2_col[1]};
+                          p.off_p1[1], p.d2_col[0], p.d2_col[1], p.p_split};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

@@ -323,7 +323,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
   };
 
   const int ntiles = local_tiles(p);
-  if (MODE == MODE_CHAIN && p.p_tmem) {
+  if (MODE == MODE_CHAIN && p.p_tmem && p.p_split == 0u) {
     // Pairs: G0(0), G0(1), then G1(k), G1(k+1), G0(k+2), G0(k+3) -- as the MMA issuer.
     for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = load_g0(it);
     for (int k = 0; ok && k < ntiles; k += 2) {
@@ -386,6 +386,14 @@ __device__ __forceinline__ void issue_chunk(uint32_t lead, uint32_t d, uint64_t 
   }
 }
 
+// TMEM column (from its buffer's start) of GEMM1's A operand, K chunk kc1, when P is kept
+// in TMEM: packed pairs, 32 columns per 64-wide chunk; for wide chains the chunks from
+// p_split on sit in P's upper half at p_hi.
+__device__ __forceinline__ uint32_t p_col_of(const ChainParams& p, int kc1) {
+  const uint32_t k = static_cast<uint32_t>(kc1) * 64u;
+  return (p.p_split == 0u || k < p.p_split) ? (k >> 1) : p.p_hi + ((k - p.p_split) >> 1);
+}
+
 // GEMM1 chunk with A (= P) in TMEM: 8 packed columns per 16-wide K step.
 template <bool BMN>
 __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32_t a_tmem,
@@ -435,6 +443,15 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const int last_nks = last_rem >= 64 ? 4 : (last_rem + 15) >> 4;
   const int rem1 = p.N0p - (p.kchunks1 - 1) * kChunkK;
   const int last_nks1 = rem1 >= 64 ? 4 : (rem1 >> 4);
+  // Wide chains: GEMM0 as two MMAs of N = 256 and N0p - 256; the upper half's B starts
+  // four 64-wide blocks (32 KiB, MN-major) into the W0 chunk, its bias four blocks in.
+  const bool wide = p.p_split != 0u;
+  const uint32_t idesc0_lo = wide ? idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, 256) : 0u;
+  const uint32_t idesc0_hi =
+      wide ? idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p - 256) : 0u;
+  const uint32_t idesc_b0_lo = wide ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, 256) : 0u;
+  const uint32_t idesc_b0_hi = wide ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N0p - 256) : 0u;
+  const uint64_t w0_hi_step = (4u * 8192u) >> 4;
   // Three-operator chain: GEMM2 reads P1 (K-major, as P) and the resident W2 (MN-major).
   // Other modes never read these (zero, so that they cost nothing).
   constexpr bool kThree = MODE == MODE_CHAIN3;
@@ -495,7 +512,12 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         const uint64_t bdesc = p.resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
                                           : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
         if (++cb == p.kc_per_tap) cb = 0;
-        issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
+        if (p.p_split != 0u) {   // wide: D0 columns [0, 256) and [256, N0p)
+          issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0_lo, nks, kc == 0);
+          issue_chunk<W0MN>(lead, d0 + 256u, adesc, bdesc + w0_hi_step, idesc0_hi, nks, kc == 0);
+        } else {
+          issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
+        }
       }
       trace(EV_MMA_ISSUED, kc, it);
       mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
@@ -508,7 +530,13 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         return false;
       bias_ready = true;
     }
-    mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0, 1u);   // D0 += bias
+    if (p.p_split != 0u) {
+      mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0_lo, 1u);
+      mma_f16_ss(lead, d0 + 256u, ones_desc, bias0_desc + ((4u * kBiasBlockBytes) >> 4),
+                 idesc_b0_hi, 1u);
+    } else {
+      mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0, 1u);   // D0 += bias
+    }
     mma_commit(lead, bars + 8u * (BAR_ACC_FULL0 + b));
     trace(EV_MMA_G0_DONE, b, it);
     return true;
@@ -536,8 +564,8 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       }
       const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
       if (p.p_tmem) {
-        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1,
-                             kc1 == 0);
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + p_col_of(p, kc1), bdesc, idesc1,
+                             nks1, kc1 == 0);
       } else {
         // P buffer b, chunk kc1 (P buffers are whole 1 KiB multiples apart)
         const uint64_t adesc = p_desc0 + ((p.off_p[b] - p.off_p[0]) >> 4) +
@@ -626,7 +654,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   };
 
   if (ok) {
-    if (MODE == MODE_CHAIN && p.p_tmem) {
+    if (MODE == MODE_CHAIN && p.p_tmem && p.p_split == 0u) {
       // Pairs of tiles: while the epilogue of one tile drains, the other tile's MMAs run.
       for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = issue_g0(it);
       for (int k = 0; ok && k < ntiles; k += 2) {
@@ -912,7 +940,13 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       named_bar_sync(bar_id, group_threads);
     }
     if (alive) {
-      if (p.p_tmem)
+      if (p.p_tmem && p.p_split != 0u) {
+        // wide: warpgroup wg packs D0 columns [wg * p_split, ...) in place
+        const int c0 = wg * static_cast<int>(p.p_split);
+        const int n = min(static_cast<int>(p.p_split), p.N0p - c0);
+        if (n > 0)
+          drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b] + c0, n, p.d0_col[b] + c0);
+      } else if (p.p_tmem)
         drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b], p.N0p, p.d0_col[b]);
       else
         drain_to_smem<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, p_tile,
@@ -1079,8 +1113,9 @@ __device__ __forceinline__ void fill_bias_operands(const ChainParams& p, uint8_t
   const int n0blk = (p.N0p + 63) >> 6;
   const int n1blk = ngemms >= 2 ? (p.N1p + 63) >> 6 : 0;
   const int n2blk = ngemms >= 3 ? (p.N2p + 63) >> 6 : 0;
-  // Each thread fetches its element of every bias row first (N <= 256 <= nthreads), so
-  // the global loads overlap the fill below instead of following one another.
+  // Each thread fetches its first element of every bias row before the fill below, so the
+  // global loads overlap it instead of following one another (rows longer than nthreads,
+  // N0 up to 512, finish in the loop at the end).
   const uint16_t v0 = (tid < p.N0 && p.b0 != nullptr) ? p.b0[tid] : uint16_t(0);
   const uint16_t v1 = (ngemms >= 2 && tid < p.N1 && p.b1 != nullptr) ? p.b1[tid] : uint16_t(0);
   const uint16_t v2 = (ngemms >= 3 && tid < p.N2 && p.b2 != nullptr) ? p.b2[tid] : uint16_t(0);
@@ -1102,6 +1137,9 @@ __device__ __forceinline__ void fill_bias_operands(const ChainParams& p, uint8_t
   if (tid < n0blk * 64) halves[(tid >> 6) * kBlockHalves + (tid & 63)] = v0;
   if (tid < n1blk * 64) halves[(n0blk + (tid >> 6)) * kBlockHalves + (tid & 63)] = v1;
   if (tid < n2blk * 64) halves[(n0blk + n1blk + (tid >> 6)) * kBlockHalves + (tid & 63)] = v2;
+  for (int n = tid + nthreads; n < n0blk * 64; n += nthreads)   // wide N0
+    halves[(n >> 6) * kBlockHalves + (n & 63)] =
+        (n < p.N0 && p.b0 != nullptr) ? p.b0[n] : uint16_t(0);
 }
 
 // W2 [N1][N2] (row-major, global) -> the resident MN-major layout GEMM2 reads, as a TMA

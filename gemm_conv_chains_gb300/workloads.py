@@ -182,11 +182,14 @@ CONV_POOL = ConvPool("conv_pool", "f16", 32, 112, 112, 64, 64)
 CONV3X3S2_1X1 = ConvChain("conv3x3s2_1x1", "f16", 32, 56, 56, 64, 128, 3, 3, 1, 128, "relu",
                           "none", stride=2)
 
+# A wide chain: 256 -> 512 -> 128 over 32768 rows, bf16 (GEMM0 wider than one MMA).
+GEMM_WIDE = GemmChain("gemm_wide", "bf16", 32768, 256, 512, 128, "hardswish", "hardswish",
+                      a_dist="normal")
 # A three-operator MLP head: 128 -> 128 -> 64 -> 64 over 32768 rows, bf16.
 MLP3 = GemmChain3("mlp3", "bf16", 32768, 128, 128, 64, 64, "hardswish", "hardswish", "none")
 
 WORKLOADS = {w.name: w for w in (GEMM_SMALL, GEMM_FFN, CONV1X1, CONV3X3_1X1, CONV_POOL,
-                                 CONV3X3S2_1X1, MLP3)}
+                                 CONV3X3S2_1X1, MLP3, GEMM_WIDE)}
 FFN_SWEEP_M = [4096, 8192, 16384, 32768, 65536, 131072, 262144]
 
 

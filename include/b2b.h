@@ -65,7 +65,7 @@ typedef enum b2b_status {
     B2B_ERR_NULL = 1,         /* a required pointer is NULL */
     B2B_ERR_SHAPE = 2,        /* a size is negative, or the output would be empty/invalid */
     B2B_ERR_ALIGN = 3,        /* pointer not 16-byte aligned, or a channel size not % 8 */
-    B2B_ERR_UNSUPPORTED = 4,  /* outside the kernels' limits (e.g. N0 > 256) */
+    B2B_ERR_UNSUPPORTED = 4,  /* outside the kernels' limits (e.g. N0 > 512) */
     B2B_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed (no device, launch...) */
     B2B_ERR_TIMEOUT = 6       /* a kernel gave up waiting (from b2b_get_device_error) */
 } b2b_status;
@@ -85,8 +85,12 @@ typedef enum b2b_epilogue { B2B_EPI_NONE = 0, B2B_EPI_RELU = 1, B2B_EPI_HARDSWIS
  *  "Shared-memory-resident fusion").
  *   A  [M][K0]  row-major      W0 [K0][N0] row-major     b0 [N0] or NULL
  *   W1 [N0][N1] row-major      b1 [N1] or NULL           D  [M][N1] row-major (output)
- * Limits: M >= 0; K0 >= 8; 8 <= N0 <= 256; 8 <= N1 <= 256; K0, N0, N1 multiples of 8.
- * The GEMM0 result tile (128 rows x N0) is rounded to dt and kept in shared memory. */
+ * Limits: M >= 0; K0 >= 8; 8 <= N0 <= 512; 8 <= N1 <= 256, and N1 <= 128 when N0 > 256;
+ * K0, N0, N1 multiples of 8.  The GEMM0 result tile (128 rows x N0) is rounded to dt and
+ * kept on chip: in shared memory, or in TMEM over the GEMM0 columns already read (wide
+ * N0).  For 256 < N0 <= 512 GEMM0 runs as two MMAs per K step over the two halves of the
+ * 512 TMEM columns, one tile in flight per CTA (the Blackwell form of wider
+ * threadblock-resident chains: the CTA still owns all N0 columns of its rows). */
 b2b_status b2b_gemm(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
                     const void* A, const void* W0, const void* b0, b2b_epilogue e0,
                     const void* W1, const void* b1, b2b_epilogue e1,

@@ -62,7 +62,7 @@ def gemm(L, dt=F16, M=256, K0=64, N0=64, N1=64, A=FAKE, W0=FAKE, b0=None, e0=1, 
     (dict(dt=2), UNSUP), (dict(e0=3), UNSUP), (dict(e1=-1), UNSUP),
     (dict(M=-1), SHAPE), (dict(K0=0), SHAPE), (dict(N1=-8), SHAPE),
     (dict(K0=12), ALIGN), (dict(N0=4), ALIGN), (dict(N1=30), ALIGN),
-    (dict(N0=264), UNSUP), (dict(N1=512), UNSUP),
+    (dict(N0=520), UNSUP), (dict(N0=264, N1=136), UNSUP), (dict(N1=512), UNSUP),
     (dict(A=None), NULL), (dict(W1=None), NULL), (dict(D=None), NULL),
     (dict(A=MIS), ALIGN), (dict(D=MIS), ALIGN), (dict(b0=FAKE + 1), ALIGN),
     (dict(M=0, A=None, D=None), OK),

@@ -48,6 +48,11 @@ GEMM_SHAPES = [
     ("f16", 300, 128, 160, 128),
     ("bf16", 257, 72, 200, 120),
     ("f16", 640, 128, 144, 96),
+    # 256 < N0 <= 512: GEMM0 as two MMAs over D0's halves, one tile in flight
+    ("bf16", 300, 128, 384, 64),
+    ("f16", 257, 72, 264, 24),
+    ("bf16", 1000, 256, 512, 128),
+    ("bf16", 129, 64, 320, 96),
 ]
 
 
@@ -146,6 +151,13 @@ def test_gemm_bias_act(shape, integer):
     ref = oracle.gemm_bias_act(dt, wl.to_bits(t["A"]), wl.to_bits(t["W0"]), wl.to_bits(t["b0"]),
                                w.act0)
     compare(dt, wl.to_bits(out.cpu()), ref, integer, "gemm_bias_act")
+
+
+def test_b2b_gemm_wide_n0_sampled_rows():
+    # N0 = 512 over 40000 rows (313 tiles): every CTA runs two or three tiles one at a time
+    w = wl.GemmChain("wide512", "bf16", 40000, 256, 512, 128, "hardswish", "relu",
+                     a_dist="normal")
+    run_b2b_gemm(w, seed=17, rows=np.r_[0:512, 20000:20128, 39744:40000])
 
 
 # ------------------------------------------------------------------------------------

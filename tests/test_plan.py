@@ -23,7 +23,7 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes",
           "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2", "d1_col3", "cand", "ncand",
           "grid_choice", "pf_choice", "ring_extend", "off_w2", "off_p1_0", "off_p1_1", "d2_col0",
-          "d2_col1"]
+          "d2_col1", "p_split"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4, "b2b_gemm3": 5}
@@ -31,8 +31,8 @@ KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nh
 
 def plan(kind, dims):
     arr = (ctypes.c_int64 * len(dims))(*dims)
-    out = (ctypes.c_uint32 * 57)()
-    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 57)
+    out = (ctypes.c_uint32 * 58)()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 58)
     return st, dict(zip(FIELDS, list(out)))
 
 
@@ -79,7 +79,15 @@ def check(kind, dims, row_major_w):
     if mode == 2:
         assert groups == 2                       # the pool epilogue needs whole rows per warp
     p_tmem = p["p_tmem"] == 1
-    assert not p_tmem or (mode == 0 and dual and groups == 2 and not p["alias"])
+    wide = p["p_split"] > 0
+    assert not p_tmem or (mode == 0 and not p["alias"] and (wide or (dual and groups == 2)))
+    if wide:
+        # 256 < N0 <= 512: one tile in flight, both warpgroups, P's halves packed in place at
+        # 0 and 256, D1 between them
+        assert p_tmem and not dual and groups == 1 and N0p > 256 and N1p <= 128
+        assert p["p_split"] == 256 and p["tmem_cols"] == 512 and p["d0_col0"] == 0
+        assert p["d1_col0"] == 128 and p["w1_group"] == 0 and not p["resident"]
+        assert p["stage_bytes"] >= 16384 + N0p // 64 * 8192
     if p["w1_group"]:
         # W1 packed w1_per_stage chunks per ring stage; all its stages in the ring at once
         assert p_tmem and not p["resident"]
@@ -129,6 +137,8 @@ def check(kind, dims, row_major_w):
         assert oa + sa <= ob or ob + sb <= oa, (a, b)
     # TMEM: every accumulator buffer in range, 32-column aligned, distinct buffers disjoint
     assert p["tmem_cols"] in (32, 64, 128, 256, 512)
+    if wide:
+        return p
     if p_tmem:
         # buffer b: D0 [d0, d0 + N0p); P (packed) [d0, d0 + N0p/2); D1 [d1, d1 + N1p) after P
         spans = []
@@ -234,7 +244,7 @@ def test_workload_tile_counts():
 
 def test_plan_rejects_like_the_entry_points():
     assert plan("b2b_gemm", (10, 12, 64, 64))[0] == 3        # K0 not a multiple of 8
-    assert plan("b2b_gemm", (10, 64, 264, 64))[0] == 4       # N0 > 256
+    assert plan("b2b_gemm", (10, 64, 520, 64))[0] == 4       # N0 > 512
     assert plan("conv_relu_maxpool", (1, 1, 8, 8, 8))[0] == 2
 
 
@@ -305,3 +315,18 @@ def test_gemm3_limits():
     assert plan("b2b_gemm3", (1000, 64, 128, 128, 64))[0] == 4   # 2 x (128 + 128 + 64) > 512
     assert plan("b2b_gemm3", (1000, 64, 64, 64, 12))[0] == 3     # N2 not a multiple of 8
     assert plan("b2b_gemm3", (1000, 8192, 128, 64, 64))[0] == 4  # W0 does not fit
+
+
+@pytest.mark.parametrize("dims", [(32768, 256, 512, 128), (300, 128, 384, 64), (257, 72, 264, 24),
+                                  (1, 64, 512, 128), (1000, 512, 320, 96)])
+def test_wide_chains_split_gemm0(dims):
+    # 256 < N0 <= 512 (N1 <= 128): GEMM0 as two MMAs over D0's halves, P packed in place in
+    # each half, one tile in flight, both warpgroups on every tile
+    p = check("b2b_gemm", dims, True)
+    assert p["p_split"] == 256 and p["groups"] == 1 and p["nbuf"] == 1
+
+
+def test_wide_chain_limits():
+    assert plan("b2b_gemm", (1000, 64, 512, 136))[0] == 4     # N1 > 128 beside a wide N0
+    assert plan("b2b_gemm", (1000, 64, 520, 64))[0] == 4      # N0 > 512
+    assert plan("gemm_bias_act", (1000, 64, 264))[0] == 4     # single operators keep N <= 256
