@@ -225,7 +225,7 @@ __device__ __forceinline__ void prefetch_a_tile(const ChainParams& p, int32_t t)
   bulk_prefetch_l2(p.pf_a + off, static_cast<uint32_t>(n));
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool WIDE>
 __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
                               const CUtensorMap* tmW0, const CUtensorMap* tmW1, uint32_t base,
                               uint32_t bars, volatile uint32_t* abort_flag) {
@@ -323,7 +323,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
   };
 
   const int ntiles = local_tiles(p);
-  if (MODE == MODE_CHAIN && p.p_tmem && p.p_split == 0u) {
+  if (MODE == MODE_CHAIN && !WIDE && p.p_tmem) {
     // Pairs: G0(0), G0(1), then G1(k), G1(k+1), G0(k+2), G0(k+3) -- as the MMA issuer.
     for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = load_g0(it);
     for (int k = 0; ok && k < ntiles; k += 2) {
@@ -389,9 +389,11 @@ __device__ __forceinline__ void issue_chunk(uint32_t lead, uint32_t d, uint64_t 
 // TMEM column (from its buffer's start) of GEMM1's A operand, K chunk kc1, when P is kept
 // in TMEM: packed pairs, 32 columns per 64-wide chunk; for wide chains the chunks from
 // p_split on sit in P's upper half at p_hi.
+template <bool WIDE>
 __device__ __forceinline__ uint32_t p_col_of(const ChainParams& p, int kc1) {
   const uint32_t k = static_cast<uint32_t>(kc1) * 64u;
-  return (p.p_split == 0u || k < p.p_split) ? (k >> 1) : p.p_hi + ((k - p.p_split) >> 1);
+  if constexpr (!WIDE) return k >> 1;
+  return k < p.p_split ? (k >> 1) : p.p_hi + ((k - p.p_split) >> 1);
 }
 
 // GEMM1 chunk with A (= P) in TMEM: 8 packed columns per 16-wide K step.
@@ -405,7 +407,7 @@ __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32
                (first && ks == 0) ? 0u : 1u);
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE>
 __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
                          volatile uint32_t* abort_flag) {
   const uint32_t idesc0 = idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p);
@@ -445,12 +447,12 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const int last_nks1 = rem1 >= 64 ? 4 : (rem1 >> 4);
   // Wide chains: GEMM0 as two MMAs of N = 256 and N0p - 256; the upper half's B starts
   // four 64-wide blocks (32 KiB, MN-major) into the W0 chunk, its bias four blocks in.
-  const bool wide = p.p_split != 0u;
-  const uint32_t idesc0_lo = wide ? idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, 256) : 0u;
+  // (A separate instantiation, WIDE, so that no other launch pays for the split.)
+  const uint32_t idesc0_lo = WIDE ? idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, 256) : 0u;
   const uint32_t idesc0_hi =
-      wide ? idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p - 256) : 0u;
-  const uint32_t idesc_b0_lo = wide ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, 256) : 0u;
-  const uint32_t idesc_b0_hi = wide ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N0p - 256) : 0u;
+      WIDE ? idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p - 256) : 0u;
+  const uint32_t idesc_b0_lo = WIDE ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, 256) : 0u;
+  const uint32_t idesc_b0_hi = WIDE ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N0p - 256) : 0u;
   const uint64_t w0_hi_step = (4u * 8192u) >> 4;
   // Three-operator chain: GEMM2 reads P1 (K-major, as P) and the resident W2 (MN-major).
   // Other modes never read these (zero, so that they cost nothing).
@@ -512,7 +514,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         const uint64_t bdesc = p.resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
                                           : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
         if (++cb == p.kc_per_tap) cb = 0;
-        if (p.p_split != 0u) {   // wide: D0 columns [0, 256) and [256, N0p)
+        if constexpr (WIDE) {   // D0 columns [0, 256) and [256, N0p)
           issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0_lo, nks, kc == 0);
           issue_chunk<W0MN>(lead, d0 + 256u, adesc, bdesc + w0_hi_step, idesc0_hi, nks, kc == 0);
         } else {
@@ -530,7 +532,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         return false;
       bias_ready = true;
     }
-    if (p.p_split != 0u) {
+    if constexpr (WIDE) {
       mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0_lo, 1u);
       mma_f16_ss(lead, d0 + 256u, ones_desc, bias0_desc + ((4u * kBiasBlockBytes) >> 4),
                  idesc_b0_hi, 1u);
@@ -564,7 +566,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       }
       const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
       if (p.p_tmem) {
-        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + p_col_of(p, kc1), bdesc, idesc1,
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + p_col_of<WIDE>(p, kc1), bdesc, idesc1,
                              nks1, kc1 == 0);
       } else {
         // P buffer b, chunk kc1 (P buffers are whole 1 KiB multiples apart)
@@ -654,7 +656,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   };
 
   if (ok) {
-    if (MODE == MODE_CHAIN && p.p_tmem && p.p_split == 0u) {
+    if (MODE == MODE_CHAIN && !WIDE && p.p_tmem) {
       // Pairs of tiles: while the epilogue of one tile drains, the other tile's MMAs run.
       for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = issue_g0(it);
       for (int k = 0; ok && k < ntiles; k += 2) {
@@ -905,7 +907,7 @@ __device__ __forceinline__ bool warp_wait(bool alive, uint32_t bar, uint32_t par
 // Epilogue warps.  With epi_groups == 2 warpgroup g (warps 2+4g .. 5+4g) takes the
 // CTA's tiles i with i & 1 == g and owns buffer g; with epi_groups == 1 all eight warps
 // take every tile and warpgroup g drains the 32-column blocks 2k + g.
-template <int MODE, bool A4D, bool BF16>
+template <int MODE, bool A4D, bool BF16, bool WIDE>
 __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, uint32_t base,
                               uint32_t bars, uint32_t tmem_base,
                               volatile uint32_t* abort_flag) {
@@ -940,7 +942,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       named_bar_sync(bar_id, group_threads);
     }
     if (alive) {
-      if (p.p_tmem && p.p_split != 0u) {
+      if constexpr (WIDE) {
         // wide: warpgroup wg packs D0 columns [wg * p_split, ...) in place
         const int c0 = wg * static_cast<int>(p.p_split);
         const int n = min(static_cast<int>(p.p_split), p.N0p - c0);
@@ -1167,7 +1169,7 @@ __device__ __forceinline__ void fill_w2(const ChainParams& p, uint8_t* dst, int 
 // ------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW0,
                  const __grid_constant__ CUtensorMap tmW1,
@@ -1242,12 +1244,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     __syncwarp();
     grid_dependency_wait();
-    producer_role<MODE, A4D, W0MN, W1MN>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
+    producer_role<MODE, A4D, W0MN, W1MN, WIDE>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
     grid_dependency_wait();   // so that no bounded wait below runs while it is pending
     ktrace(EV_DEP_READY, 0, 0);
-    mma_role<MODE, A4D, W0MN, W1MN, BF16>(p, base, bars, tmem_base, abort_flag);
+    mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE>(p, base, bars, tmem_base, abort_flag);
     __syncwarp();
   } else {
     // The bias operands, off the producer's critical path; the MMA issuer waits for them
@@ -1261,7 +1263,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8u * BAR_BIAS_READY);
-    epilogue_role<MODE, A4D, BF16>(p, &tmOut, base, bars, tmem_base, abort_flag);
+    epilogue_role<MODE, A4D, BF16, WIDE>(p, &tmOut, base, bars, tmem_base, abort_flag);
   }
 
   tc_fence_before_sync();

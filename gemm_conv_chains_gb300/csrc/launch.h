@@ -21,6 +21,7 @@ enum Variant : int {
   V_CONV_SINGLE,
   V_CONV_POOL,
   V_GEMM_CHAIN3,
+  V_GEMM_CHAIN_WIDE,
   V_COUNT
 };
 
