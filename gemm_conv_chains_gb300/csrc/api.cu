@@ -363,6 +363,10 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
       p.w1_per_stage = per;
     }
   }
+  // Wide chains (one tile in flight): W1 packed the same way for every tile, so that its
+  // GEMM1 waits for two ring fills instead of one per chunk.
+  if (mode == MODE_CHAIN && !k.resident && p.p_split != 0u)
+    p.w1_per_stage = std::max(1u, p.stage_bytes / p.w1_chunk_bytes);
   Regions r;
   r.cand = pick;
   r.ncand = nfeas;

@@ -288,24 +288,10 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     }
     return true;
   };
-  // Streamed W1 chunks for GEMM1 of the it-th tile.
+  // Streamed W1 for GEMM1 of the it-th tile (or, with w1_group, of the pair it, it + 1):
+  // w1_per_stage chunks per ring stage.
   auto load_g1 = [&](int it) -> bool {
     if (MODE != MODE_CHAIN || p.resident) return true;
-    const int32_t t = blockIdx.x + it * gridDim.x;
-    for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
-      if (!acquire(t)) return false;
-      const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
-      mbar_arrive_expect_tx_if(lead, fb, p.w1_chunk_bytes);
-      load_w1_chunk<W1MN>(lead, p, tmW1, base + p.off_ring + stage * p.stage_bytes, kc1, fb,
-                          pol_keep);
-      trace(EV_PROD_W1_ISSUED, kc1, it);
-      advance();
-    }
-    return true;
-  };
-
-  // W1 once for the pair of tiles it, it + 1: w1_per_stage chunks per ring stage.
-  auto load_w1_group = [&](int it) -> bool {
     const int32_t t = blockIdx.x + it * gridDim.x;
     for (int kc1 = 0; kc1 < p.kchunks1;) {
       if (!acquire(t)) return false;
@@ -328,7 +314,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = load_g0(it);
     for (int k = 0; ok && k < ntiles; k += 2) {
       if (p.w1_group) {
-        ok = load_w1_group(k);
+        ok = load_g1(k);
       } else {
         ok = load_g1(k);
         if (ok && k + 1 < ntiles) ok = load_g1(k + 1);
@@ -553,16 +539,21 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     trace(EV_MMA_P_READY, b, j);
     tc_fence_after_sync();
     const uint32_t d1 = tmem_base + p.d1_col[b];
+    const int per = static_cast<int>(p.w1_per_stage);   // streamed W1 chunks per ring stage
+    int slot = 0;
     for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
       uint64_t bdesc;
       if (p.resident) {
         bdesc = res_w1 + static_cast<uint64_t>(kc1) * w1_step;
       } else {
-        if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL,
-                            t))
-          return false;
-        trace(EV_MMA_W1_FULL, kc1, j);
-        bdesc = ring_w1 + static_cast<uint64_t>(stage) * stage_step;
+        if (slot == 0) {
+          if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag,
+                              SITE_MMA_FULL, t))
+            return false;
+          trace(EV_MMA_W1_FULL, kc1, j);
+        }
+        bdesc = ring_w1 + static_cast<uint64_t>(stage) * stage_step +
+                static_cast<uint64_t>(slot) * w1_step;
       }
       const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
       if (p.p_tmem) {
@@ -574,7 +565,8 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
                                static_cast<uint64_t>(kc1) * (kPChunkBytes >> 4);
         issue_chunk<W1MN>(lead, d1, adesc, bdesc, idesc1, nks1, kc1 == 0);
       }
-      if (!p.resident) {
+      if (!p.resident && (++slot == per || kc1 == p.kchunks1 - 1)) {
+        slot = 0;
         mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));
         if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
       }

@@ -88,6 +88,10 @@ def check(kind, dims, row_major_w):
         assert p["p_split"] == 256 and p["tmem_cols"] == 512 and p["d0_col0"] == 0
         assert p["d1_col0"] == 128 and p["w1_group"] == 0 and not p["resident"]
         assert p["stage_bytes"] >= 16384 + N0p // 64 * 8192
+        # each tile's W1 packed as many chunks per ring stage as fit
+        assert p["w1_per_stage"] == p["stage_bytes"] // w1_chunk
+    elif not p["w1_group"]:
+        assert p["w1_per_stage"] == 1
     if p["w1_group"]:
         # W1 packed w1_per_stage chunks per ring stage; all its stages in the ring at once
         assert p_tmem and not p["resident"]
