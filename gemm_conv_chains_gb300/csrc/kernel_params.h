@@ -66,6 +66,8 @@ enum TraceEvent : uint32_t {
   EV_DEP_READY = 20,       // the MMA warp's wait for the previous grid returned
   EV_EPI_P1_DONE = 21,     // three-operator chain: epilogue group published P1
   EV_MMA_G2_DONE = 22,     // three-operator chain: GEMM2 of a tile issued and committed
+  EV_PROD_START = 23,      // producer past its wait for the previous grid
+  EV_MMA_SETUP = 24,       // MMA issuer's descriptors ready, before its first wait
 };
 
 constexpr int kBlockM = 128;          // rows of one tile = TMEM lanes = tcgen05 M

@@ -441,7 +441,7 @@ TRACE_EVENTS = {1: "prod_acquire", 2: "prod_issued", 3: "mma_full", 4: "mma_g0_d
                 13: "mma_wait", 14: "mma_issued",
                 15: "prod_w1_issued", 16: "mma_w1_full",
                 17: "kernel_entry", 18: "epi_drained", 19: "setup_done", 20: "dep_ready",
-                21: "epi_p1_done", 22: "mma_g2_done"}
+                21: "epi_p1_done", 22: "mma_g2_done", 23: "prod_start", 24: "mma_setup"}
 
 
 def set_trace(buf, cta: int = 0) -> None:

@@ -46,6 +46,12 @@ def test_trace_of_a_chain_is_complete_and_causal():
         assert names.count(name) == 1, name
     assert all(when[("kernel_entry", 0)] <= e[0] for e in ev)
     assert when[("setup_done", 0)] <= when[("dep_ready", 0)] <= when[("mma_g0_done", 0)]
+    # the producer starts after its own dependency wait and before its first load; the MMA
+    # issuer sets up before its wait for the previous grid
+    for name in ("prod_start", "mma_setup"):
+        assert names.count(name) == 1, name
+    assert when[("prod_start", 0)] <= when[("prod_acquire", 0)]
+    assert when[("setup_done", 0)] <= when[("mma_setup", 0)] <= when[("dep_ready", 0)]
 
 
 def test_trace_off_records_nothing():
