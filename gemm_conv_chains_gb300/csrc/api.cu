@@ -198,12 +198,17 @@ uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = fals
   p.p_split = 0;
   p.p_hi = 0;
   if (mode == MODE_CHAIN && p_tmem && p.N0p > 256) {
-    // Wide: one buffer of 512 columns.  D0 = [0, N0p); P's halves pack in place into
-    // [0, 128) and [256, 256 + (N0p - 256) / 2); D1 = [128, 128 + N1p) between them.
+    // Wide: all 512 columns.  GEMM0 runs over the halves of N0 into [0, 256) and
+    // [256, 256 + N0p - 256); each half's P packs in place into its first 128 columns.  D1
+    // sits in the upper columns of the half computed first: [128, 128 + N1p) on even tiles
+    // (lower half first), [384, 384 + N1p) on odd ones (upper half first), so that a
+    // tile's first GEMM0 pass never touches the previous tile's D1.
     p.p_split = 256u;
     p.p_hi = 256u;
     p.d0_col[0] = 0;
+    p.d0_col[1] = 256u;
     p.d1_col[0] = 128u;
+    p.d1_col[1] = 384u;
     return 512u;
   }
   if (mode == MODE_CHAIN3) {
@@ -252,7 +257,10 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   const uint32_t budget = kSmemLimit - 1024u;   // 1 KiB slack to align the base to 1024
   const uint32_t n0blk = static_cast<uint32_t>((p.N0p + 63) / 64);
   const uint32_t n1blk = static_cast<uint32_t>((p.N1p + 63) / 64);
-  p.w0_chunk_bytes = w0mn ? n0blk * 8192u : static_cast<uint32_t>(p.N0p) * 128u;
+  // (Wide chains stream W0 by halves of N0: four 64-wide blocks per chunk.)
+  const bool wide = mode == MODE_CHAIN && p.N0p > 256;
+  p.w0_chunk_bytes = w0mn ? std::min(n0blk, wide ? 4u : n0blk) * 8192u
+                          : static_cast<uint32_t>(p.N0p) * 128u;
   p.w1_chunk_bytes = mode == MODE_CHAIN ? (w1mn ? n1blk * 8192u : static_cast<uint32_t>(p.N1p) * 128u) : 0u;
   const uint32_t p_bytes = mode == MODE_CHAIN ? n0blk * kPChunkBytes : 0u;
   const uint32_t out_bytes = mode == MODE_CHAIN    ? n1blk * kPChunkBytes
@@ -671,13 +679,17 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   // box then covers every 64-wide column block of `box_rows` rows, laid out block after
   // block exactly as the kernel's per-block boxes land.  Returns false (and the caller
   // keeps the per-block 2-D map) if N is ragged or the driver refuses the view.
-  auto map3 = [&](CUtensorMap* m, const void* ptr, uint64_t rows, int32_t N, uint32_t box_rows) {
+  // A box of `box_blocks` blocks (all of them by default).
+  auto map3 = [&](CUtensorMap* m, const void* ptr, uint64_t rows, int32_t N, uint32_t box_rows,
+                  uint32_t box_blocks = 0) {
     if (N % 64 != 0) return false;
-    return make_map(m, ptr, p.is_bf16, 3, {64, rows, static_cast<uint64_t>(N / 64)},
-                    {N * e, 128}, {64, box_rows, static_cast<uint32_t>(N / 64)});
+    const uint32_t nb = static_cast<uint32_t>(N / 64);
+    return make_map(m, ptr, p.is_bf16, 3, {64, rows, nb}, {N * e, 128},
+                    {64, box_rows, box_blocks ? std::min(box_blocks, nb) : nb});
   };
   if (w_mn) {
-    p.w0_box3 = map3(&tw0, W0, static_cast<uint64_t>(K0), N0, 64) ? 1 : 0;
+    // Wide chains load W0 by halves of N0: boxes of four blocks.
+    p.w0_box3 = map3(&tw0, W0, static_cast<uint64_t>(K0), N0, 64, p.p_split ? 4u : 0u) ? 1 : 0;
     if (!p.w0_box3)
       ok = ok && make_map(&tw0, W0, p.is_bf16, 2,
                           {static_cast<uint64_t>(N0), static_cast<uint64_t>(K0)}, {N0 * e}, {64, 64});

@@ -198,6 +198,25 @@ __device__ __forceinline__ void load_w0_chunk(uint32_t lead, const ChainParams& 
   }
 }
 
+// Wide chains: the K chunk's 64-wide N blocks [4h, 4h + 4) of W0 (half h of N0): one box
+// of four blocks in the [N0/64][K0][64] view (blocks past N0 zero-filled), else one 2-D box
+// per block.  Returns the bytes the loads deliver.
+__device__ __forceinline__ uint32_t w0_half_bytes(const ChainParams& p, int h) {
+  if (h == 0 || p.w0_box3) return p.w0_chunk_bytes;
+  return static_cast<uint32_t>(((p.N0p + 63) >> 6) - 4) * 8192u;
+}
+__device__ __forceinline__ void load_w0_half(uint32_t lead, const ChainParams& p,
+                                             const CUtensorMap* tmW0, uint32_t dst, int kc,
+                                             int h, uint32_t bar, uint64_t pol) {
+  if (p.w0_box3) {
+    tma_load_3d(lead, dst, tmW0, bar, 0, kc * kChunkK, 4 * h, pol);
+    return;
+  }
+  const int nblk = min((p.N0p + 63) >> 6, 4 * h + 4);
+  for (int nb = 4 * h; nb < nblk; ++nb)
+    tma_load_2d(lead, dst + (nb - 4 * h) * 8192u, tmW0, bar, nb * 64, kc * kChunkK, pol);
+}
+
 template <bool W1MN>
 __device__ __forceinline__ void load_w1_chunk(uint32_t lead, const ChainParams& p,
                                               const CUtensorMap* tmW1, uint32_t dst, int kc1,
@@ -310,8 +329,58 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     return true;
   };
 
+  // Wide chains, tile it, half h of N0: GEMM0's A chunks with that half's W0 chunks, and
+  // W1's rows of that half (w1_per_stage chunks per ring stage).
+  auto load_g0_half = [&](int it, int h) -> bool {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    const TileCoord tc = tile_coord<A4D>(p, t);
+    const uint32_t wbytes = w0_half_bytes(p, h);
+    KPos k;
+    for (int kc = 0; kc < p.kchunks0; ++kc, k.next(p)) {
+      if (!acquire(t)) return false;
+      trace(EV_PROD_ACQUIRE, kc, it);
+      const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
+      const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
+      mbar_arrive_expect_tx_if(lead, fb, kABytes + wbytes);
+      load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, k, fb, pol_stream);
+      load_w0_half(lead, p, tmW0, sbase + kABytes, kc, h, fb, pol_keep);
+      if (kc == 0 && h == (it & 1) && lead)
+        prefetch_a_tile(p, t + 2 * static_cast<int32_t>(gridDim.x));
+      trace(EV_PROD_ISSUED, kc, it);
+      advance();
+    }
+    return true;
+  };
+  auto load_w1_half = [&](int it, int h) -> bool {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    const int first = 4 * h, end = h == 0 ? min(4, p.kchunks1) : p.kchunks1;
+    for (int kc1 = first; kc1 < end;) {
+      if (!acquire(t)) return false;
+      const int n = min(static_cast<int>(p.w1_per_stage), end - kc1);
+      const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
+      const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
+      mbar_arrive_expect_tx_if(lead, fb, static_cast<uint32_t>(n) * p.w1_chunk_bytes);
+      for (int j = 0; j < n; ++j)
+        load_w1_chunk<W1MN>(lead, p, tmW1, sbase + j * p.w1_chunk_bytes, kc1 + j, fb, pol_keep);
+      trace(EV_PROD_W1_ISSUED, kc1, it);
+      advance();
+      kc1 += n;
+    }
+    return true;
+  };
+
   const int ntiles = local_tiles(p);
-  if (MODE == MODE_CHAIN && !WIDE && p.p_tmem) {
+  if constexpr (MODE == MODE_CHAIN && WIDE) {
+    // As the MMA issuer consumes: per tile, GEMM0 over the first half of N0 (the lower on
+    // even tiles, the upper on odd ones), then over the other half, then W1 in that order.
+    for (int it = 0; ok && it < ntiles; ++it) {
+      const int f = it & 1;
+      ok = load_g0_half(it, f);
+      if (ok) ok = load_g0_half(it, f ^ 1);
+      if (ok) ok = load_w1_half(it, f);
+      if (ok) ok = load_w1_half(it, f ^ 1);
+    }
+  } else if (MODE == MODE_CHAIN && p.p_tmem) {
     // Pairs: G0(0), G0(1), then G1(k), G1(k+1), G0(k+2), G0(k+3) -- as the MMA issuer.
     for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = load_g0(it);
     for (int k = 0; ok && k < ntiles; k += 2) {
@@ -374,16 +443,6 @@ __device__ __forceinline__ void issue_chunk(uint32_t lead, uint32_t d, uint64_t 
   }
 }
 
-// TMEM column (from its buffer's start) of GEMM1's A operand, K chunk kc1, when P is kept
-// in TMEM: packed pairs, 32 columns per 64-wide chunk; for wide chains the chunks from
-// p_split on sit in P's upper half at p_hi.
-template <bool WIDE>
-__device__ __forceinline__ uint32_t p_col_of(const ChainParams& p, int kc1) {
-  const uint32_t k = static_cast<uint32_t>(kc1) * 64u;
-  if constexpr (!WIDE) return k >> 1;
-  return k < p.p_split ? (k >> 1) : p.p_hi + ((k - p.p_split) >> 1);
-}
-
 // GEMM1 chunk with A (= P) in TMEM: 8 packed columns per 16-wide K step.
 template <bool BMN>
 __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32_t a_tmem,
@@ -433,15 +492,14 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   const int last_nks = last_rem >= 64 ? 4 : (last_rem + 15) >> 4;
   const int rem1 = p.N0p - (p.kchunks1 - 1) * kChunkK;
   const int last_nks1 = rem1 >= 64 ? 4 : (rem1 >> 4);
-  // Wide chains: GEMM0 as two MMAs of N = 256 and N0p - 256; the upper half's B starts
-  // four 64-wide blocks (32 KiB, MN-major) into the W0 chunk, its bias four blocks in.
-  // (A separate instantiation, WIDE, so that no other launch pays for the split.)
+  // Wide chains: GEMM0 in two passes of N = 256 and N0p - 256 (the halves of N0), each
+  // with its bias four 64-wide blocks apart.  (A separate instantiation, WIDE, so that no
+  // other launch pays for them.)
   const uint32_t idesc0_lo = WIDE ? idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, 256) : 0u;
   const uint32_t idesc0_hi =
       WIDE ? idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p - 256) : 0u;
   const uint32_t idesc_b0_lo = WIDE ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, 256) : 0u;
   const uint32_t idesc_b0_hi = WIDE ? idesc_f16_f32(BF16 ? 1u : 0u, 1u, kBlockM, p.N0p - 256) : 0u;
-  const uint64_t w0_hi_step = (4u * 8192u) >> 4;
   // Three-operator chain: GEMM2 reads P1 (K-major, as P) and the resident W2 (MN-major).
   // Other modes never read these (zero, so that they cost nothing).
   constexpr bool kThree = MODE == MODE_CHAIN3;
@@ -507,12 +565,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         const uint64_t bdesc = p.resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
                                           : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
         if (++cb == p.kc_per_tap) cb = 0;
-        if constexpr (WIDE) {   // D0 columns [0, 256) and [256, N0p)
-          issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0_lo, nks, kc == 0);
-          issue_chunk<W0MN>(lead, d0 + 256u, adesc, bdesc + w0_hi_step, idesc0_hi, nks, kc == 0);
-        } else {
-          issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
-        }
+        issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
       }
       trace(EV_MMA_ISSUED, kc, it);
       mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));   // frees the ring slot when read
@@ -525,13 +578,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         return false;
       bias_ready = true;
     }
-    if constexpr (WIDE) {
-      mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0_lo, 1u);
-      mma_f16_ss(lead, d0 + 256u, ones_desc, bias0_desc + ((4u * kBiasBlockBytes) >> 4),
-                 idesc_b0_hi, 1u);
-    } else {
-      mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0, 1u);   // D0 += bias
-    }
+    mma_f16_ss(lead, d0, ones_desc, bias0_desc, idesc_b0, 1u);   // D0 += bias
     mma_commit(lead, bars + 8u * (BAR_ACC_FULL0 + b));
     trace(EV_MMA_G0_DONE, b, it);
     return true;
@@ -564,7 +611,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       }
       const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
       if (p.p_tmem) {
-        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + p_col_of<WIDE>(p, kc1), bdesc, idesc1,
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * static_cast<uint32_t>(kc1), bdesc, idesc1,
                              nks1, kc1 == 0);
       } else {
         // P buffer b, chunk kc1 (P buffers are whole 1 KiB multiples apart)
@@ -654,8 +701,102 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     return true;
   };
 
+  // Wide chains, GEMM0 of tile it over half h of N0 into TMEM columns [256h, 256h + 256);
+  // commits ACC_FULL[h].  The tile's second pass overwrites the previous tile's D1 (which
+  // sits in the other half), so it waits for that tile's epilogue to have drained it.
+  auto issue_g0_half = [&](int it, int h, bool second) -> bool {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    if (second && it > 0) {
+      if (!warp_mbar_wait(bars + 8u * BAR_ACC_EMPTY0, static_cast<uint32_t>(it - 1) & 1u, p,
+                          abort_flag, SITE_MMA_ACC_EMPTY, t))
+        return false;
+      trace(EV_MMA_ACC_FREE, h, it);
+      tc_fence_after_sync();
+    }
+    const uint32_t d0 = tmem_base + 256u * static_cast<uint32_t>(h);
+    const uint32_t idesc = h ? idesc0_hi : idesc0_lo;
+    for (int kc = 0; kc < p.kchunks0; ++kc) {
+      trace(EV_MMA_WAIT, kc, it);
+      if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL, t))
+        return false;
+      trace(EV_MMA_FULL, kc, it);
+      const uint64_t adesc = ring_a + static_cast<uint64_t>(stage) * stage_step;
+      const uint64_t bdesc = ring_w0 + static_cast<uint64_t>(stage) * stage_step;
+      issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc, kc == p.kchunks0 - 1 ? last_nks : 4,
+                        kc == 0);
+      trace(EV_MMA_ISSUED, kc, it);
+      mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));
+      if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+    }
+    if (!bias_ready) {
+      if (!warp_mbar_wait(bars + 8u * BAR_BIAS_READY, 0u, p, abort_flag, SITE_MMA_WEIGHTS, t))
+        return false;
+      bias_ready = true;
+    }
+    mma_f16_ss(lead, d0, ones_desc,
+               bias0_desc + static_cast<uint64_t>(h) * ((4u * kBiasBlockBytes) >> 4),
+               h ? idesc_b0_hi : idesc_b0_lo, 1u);
+    mma_commit(lead, bars + 8u * (BAR_ACC_FULL0 + h));
+    trace(EV_MMA_G0_DONE, h, it);
+    return true;
+  };
+
+  // Wide chains, GEMM1 of tile it: D1 (at d1_col[it & 1], the first half's upper columns)
+  // = P_f . W1[f] + P_s . W1[s] over the first half f = it & 1, then the other one s, each
+  // as soon as its P (packed in place at 256h) is published; commits D1_FULL[0].
+  auto issue_g1_wide = [&](int it) -> bool {
+    const int32_t t = blockIdx.x + it * gridDim.x;
+    const int f = it & 1;
+    const uint32_t d1 = tmem_base + p.d1_col[f];
+    const int per = static_cast<int>(p.w1_per_stage);
+    bool first = true;
+    for (int pass = 0; pass < 2; ++pass) {
+      const int h = pass == 0 ? f : f ^ 1;
+      if (!warp_mbar_wait(bars + 8u * (BAR_P_FULL0 + h), static_cast<uint32_t>(it) & 1u, p,
+                          abort_flag, SITE_MMA_P_FULL, t))
+        return false;
+      trace(EV_MMA_P_READY, h, it);
+      tc_fence_after_sync();
+      const int kbeg = 4 * h, kend = h == 0 ? min(4, p.kchunks1) : p.kchunks1;
+      int slot = 0;
+      for (int kc1 = kbeg; kc1 < kend; ++kc1) {
+        if (slot == 0) {
+          if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag,
+                              SITE_MMA_FULL, t))
+            return false;
+          trace(EV_MMA_W1_FULL, kc1, it);
+        }
+        const uint64_t bdesc = ring_w1 + static_cast<uint64_t>(stage) * stage_step +
+                               static_cast<uint64_t>(slot) * w1_step;
+        issue_chunk_ts<W1MN>(lead, d1,
+                             tmem_base + 256u * static_cast<uint32_t>(h) +
+                                 32u * static_cast<uint32_t>(kc1 - kbeg),
+                             bdesc, idesc1, kc1 == p.kchunks1 - 1 ? last_nks1 : 4, first);
+        first = false;
+        if (++slot == per || kc1 == kend - 1) {
+          slot = 0;
+          mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));
+          if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+    mma_f16_ss(lead, d1, ones_desc, bias1_desc, idesc_b1, 1u);   // D1 += bias
+    mma_commit(lead, bars + 8u * BAR_D1_FULL0);
+    trace(EV_MMA_G1_DONE, 0, it);
+    return true;
+  };
+
   if (ok) {
-    if (MODE == MODE_CHAIN && !WIDE && p.p_tmem) {
+    if constexpr (MODE == MODE_CHAIN && WIDE) {
+      // Per tile: GEMM0 over the first half, over the second, then GEMM1.  The next tile's
+      // first half is the other one, so its GEMM0 runs while this tile's D1 drains.
+      for (int it = 0; ok && it < ntiles; ++it) {
+        const int f = it & 1;
+        ok = issue_g0_half(it, f, false);
+        if (ok) ok = issue_g0_half(it, f ^ 1, true);
+        if (ok) ok = issue_g1_wide(it);
+      }
+    } else if (MODE == MODE_CHAIN && p.p_tmem) {
       // Pairs of tiles: while the epilogue of one tile drains, the other tile's MMAs run.
       for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = issue_g0(it);
       for (int k = 0; ok && k < ntiles; k += 2) {
@@ -941,13 +1082,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       named_bar_sync(bar_id, group_threads);
     }
     if (alive) {
-      if constexpr (WIDE) {
-        // wide: warpgroup wg packs D0 columns [wg * p_split, ...) in place
-        const int c0 = wg * static_cast<int>(p.p_split);
-        const int n = min(static_cast<int>(p.p_split), p.N0p - c0);
-        if (n > 0)
-          drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b] + c0, n, p.d0_col[b] + c0);
-      } else if (p.p_tmem)
+      if (p.p_tmem)
         drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b], p.N0p, p.d0_col[b]);
       else
         drain_to_smem<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, p_tile,
@@ -1035,7 +1170,50 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
   };
 
   const int ntiles = local_tiles(p);
-  if (MODE == MODE_CHAIN3) {
+  if constexpr (MODE == MODE_CHAIN && WIDE) {
+    // Wide chains (one group of both warpgroups): warpgroup wg packs half wg of D0 into P
+    // in place and publishes it on P_FULL[wg] (four warps); then both drain D1, 32 of every
+    // 64 columns each, and free the tile's TMEM on ACC_EMPTY[0] (eight warps).  Every
+    // barrier completes once per tile, so tile it waits on parity it & 1.
+    for (int it = 0; it < ntiles; ++it) {
+      const int32_t t = blockIdx.x + it * gridDim.x;
+      const uint32_t u = static_cast<uint32_t>(it) & 1u;
+      alive = warp_wait(alive, bars + 8u * (BAR_ACC_FULL0 + wg), u, p, abort_flag,
+                        SITE_EPI_ACC_FULL, t);
+      if (elected) trace(EV_EPI_ACC_READY, wg, it);
+      tc_fence_after_sync();
+      const int c0 = 256 * wg, n = min(256, p.N0p - c0);
+      if (alive && n > 0)
+        drain_to_tmem<BF16>(p.act0, tm_lane, static_cast<uint32_t>(c0), n,
+                            static_cast<uint32_t>(c0));
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8u * (BAR_P_FULL0 + wg));
+      if (elected) trace(EV_EPI_P_DONE, wg, it);
+
+      const TileCoord tc = tile_coord<A4D>(p, t);
+      alive = warp_wait(alive, bars + 8u * BAR_D1_FULL0, u, p, abort_flag, SITE_EPI_D1_FULL, t);
+      if (elected) trace(EV_EPI_D1_READY, 0, it);
+      tc_fence_after_sync();
+      if (elected) bulk_wait_read_all();   // the staging is free again
+      named_bar_sync(bar_id, group_threads);
+      if (elected) trace(EV_EPI_STAGING, 0, it);
+      if (alive)
+        drain_to_smem<BF16>(p.act1, tm_lane, p.d1_col[it & 1], c_first, c_step, p.N1p, out_tile,
+                            row, kPChunkBytes);
+      if (elected) trace(EV_EPI_DRAINED, 0, it);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8u * BAR_ACC_EMPTY0);
+      fence_proxy_async_smem();
+      named_bar_sync(bar_id, group_threads);
+      if (elected && !*abort_flag) {
+        store_tile<A4D>(p, tmOut, out_tile, (p.N1p + 63) >> 6, tc);
+        bulk_commit_group();
+        trace(EV_EPI_STORED, 0, it);
+      }
+    }
+  } else if (MODE == MODE_CHAIN3) {
     for (int it = g; it < ntiles; it += groups) {
       epi0(it);
       epi1_p1(it);
@@ -1203,7 +1381,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (uint32_t a = 0; a < kMaxBufs; ++a) {
       mbar_init(bars + 8u * (BAR_ACC_FULL0 + a), 1);
       mbar_init(bars + 8u * (BAR_ACC_EMPTY0 + a), warps_per_group);
-      mbar_init(bars + 8u * (BAR_P_FULL0 + a), warps_per_group);
+      mbar_init(bars + 8u * (BAR_P_FULL0 + a), WIDE ? 4u : warps_per_group);
       mbar_init(bars + 8u * (BAR_D1_FULL0 + a), 1);
       if (MODE == MODE_CHAIN3) {
         mbar_init(bars + 8u * (BAR_P1_FULL0 + a), warps_per_group);

@@ -141,7 +141,7 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
     in shared memory but cross the L2 -> SM crossbar all the same (ncu's
     l1tex__m_xbar2l1tex_read_bytes of the 3x3 conv chains on 56 x 56 and 64 x 64 images
     and of conv + pool equals the whole-box sum to the byte).  A: per tile, one box per
-    K chunk (2-D), or per column tap and channel block (halo boxes of (8 + R - 1) x 16
+    K chunk (2-D; twice in wide chains, once per half of N0), or per column tap and channel block (halo boxes of (8 + R - 1) x 16
     pixels), or per tap and channel block (8 x 16 pixels).  Weights: once per CTA when
     resident; when streamed, W0 once per tile and W1 once per tile, or once per pair of
     tiles when the plan groups W1 (P in TMEM).  Biases: once per CTA (plain loads by the
@@ -155,8 +155,15 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
     R = getattr(w, "R", 3 if isinstance(w, wl.ConvPool) else 1)
     a_tile = (plan["kchunks0"] // R * plan["a_stage_bytes"] if plan["halo"]
               else plan["kchunks0"] * A_BOX)
-    out["A"] = tiles * a_tile
     w0 = plan["kchunks0"] * plan["w0_chunk"]
+    if plan["p_split"]:
+        # wide chains: GEMM0 in two passes over the halves of N0, each reading the A chunks
+        # again with that half's W0 blocks (one box of four blocks, or one per block)
+        a_tile *= 2
+        n0blk = -(-plan["N0p"] // 64)
+        hi = plan["w0_chunk"] if w.N0 % 64 == 0 else (n0blk - 4) * 8192
+        w0 = plan["kchunks0"] * (plan["w0_chunk"] + hi)
+    out["A"] = tiles * a_tile
     w1 = plan["kchunks1"] * plan["w1_chunk"]
     if isinstance(w, wl.GemmChain3):
         # W0, W1 by TMA boxes and W2 by the epilogue warps' loads (its bytes, unpadded),

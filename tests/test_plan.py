@@ -51,7 +51,8 @@ def check(kind, dims, row_major_w):
     N0p, N1p = p["N0p"], p["N1p"]
     n0blk, n1blk = -(-N0p // 64), -(-N1p // 64)
     # what the kernel touches
-    w0_chunk = n0blk * 8192 if row_major_w else N0p * 128
+    # (wide chains, 256 < N0: one half of N0, four 64-wide blocks, per chunk)
+    w0_chunk = min(n0blk, 4 if mode == 0 and N0p > 256 else n0blk) * 8192 if row_major_w else N0p * 128
     w1_chunk = (n1blk * 8192 if row_major_w else N1p * 128) if mode == 0 else 0
     p_need = n0blk * 16384 if mode == 0 else 0
     out_need = {0: n1blk * 16384, 1: n0blk * 16384, 2: n0blk * 4096}[mode]
@@ -87,7 +88,10 @@ def check(kind, dims, row_major_w):
         assert p_tmem and not dual and groups == 1 and N0p > 256 and N1p <= 128
         assert p["p_split"] == 256 and p["tmem_cols"] == 512 and p["d0_col0"] == 0
         assert p["d1_col0"] == 128 and p["w1_group"] == 0 and not p["resident"]
-        assert p["stage_bytes"] >= 16384 + N0p // 64 * 8192
+        # GEMM0 by halves of N0: a ring stage holds an A chunk and four 64-wide W0 blocks;
+        # D1 in the upper columns of the half computed first (the lower on even tiles)
+        assert p["w0_chunk"] == 4 * 8192 and p["stage_bytes"] == 16384 + 4 * 8192
+        assert p["d0_col1"] == 256 and p["d1_col1"] == 384
         # each tile's W1 packed as many chunks per ring stage as fit
         assert p["w1_per_stage"] == p["stage_bytes"] // w1_chunk
     elif not p["w1_group"]:
@@ -324,8 +328,8 @@ def test_gemm3_limits():
 @pytest.mark.parametrize("dims", [(32768, 256, 512, 128), (300, 128, 384, 64), (257, 72, 264, 24),
                                   (1, 64, 512, 128), (1000, 512, 320, 96)])
 def test_wide_chains_split_gemm0(dims):
-    # 256 < N0 <= 512 (N1 <= 128): GEMM0 as two MMAs over D0's halves, P packed in place in
-    # each half, one tile in flight, both warpgroups on every tile
+    # 256 < N0 <= 512 (N1 <= 128): GEMM0 in two passes over the halves of N0, P packed in
+    # place in each half, both warpgroups on every tile
     p = check("b2b_gemm", dims, True)
     assert p["p_split"] == 256 and p["groups"] == 1 and p["nbuf"] == 1
 
