@@ -723,7 +723,9 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   p.pf_w1 = static_cast<const uint8_t*>(W1);
   p.pf_w1_bytes = mode == MODE_CHAIN ? static_cast<uint32_t>(static_cast<uint64_t>(N0) * N1 * e) : 0u;
   Variant v;
-  if (mode == MODE_CHAIN) v = w_mn ? (p.p_split ? V_GEMM_CHAIN_WIDE : V_GEMM_CHAIN) : V_CONV1X1_CHAIN;
+  if (mode == MODE_CHAIN)
+    v = !w_mn ? V_CONV1X1_CHAIN
+              : (p.p_split ? V_GEMM_CHAIN_WIDE : (p.p_tmem ? V_GEMM_CHAIN_PAIR : V_GEMM_CHAIN));
   else v = w_mn ? V_GEMM_SINGLE : V_CONV1X1_SINGLE;
   return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
 }

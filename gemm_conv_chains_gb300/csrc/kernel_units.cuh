@@ -8,16 +8,18 @@
 
 namespace b2b {
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
+          bool PAIR = false>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE>);
+  return reinterpret_cast<const void*>(&chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR>);
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
+          bool PAIR = false>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1,
                        const CUtensorMap& out, const ChainParams& p, int grid, size_t smem,
                        cudaStream_t stream) {
-  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE>, a, w0, w1, out, p, grid,
+  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR>, a, w0, w1, out, p, grid,
                       smem, stream);
 }
 
@@ -31,6 +33,7 @@ const void* variant_func_a2d(Variant v) {
     case V_CONV1X1_SINGLE: return kernel_ptr<MODE_SINGLE, false, false, false, BF16>();
     case V_GEMM_CHAIN3: return kernel_ptr<MODE_CHAIN3, false, true, true, BF16>();
     case V_GEMM_CHAIN_WIDE: return kernel_ptr<MODE_CHAIN, false, true, true, BF16, true>();
+    case V_GEMM_CHAIN_PAIR: return kernel_ptr<MODE_CHAIN, false, true, true, BF16, false, true>();
     default: return nullptr;
   }
 }
@@ -53,6 +56,9 @@ cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMa
     case V_GEMM_CHAIN_WIDE:
       return launch_one<MODE_CHAIN, false, true, true, BF16, true>(a, w0, w1, out, p, grid, smem,
                                                                    s);
+    case V_GEMM_CHAIN_PAIR:
+      return launch_one<MODE_CHAIN, false, true, true, BF16, false, true>(a, w0, w1, out, p, grid,
+                                                                         smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
