@@ -725,7 +725,8 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   Variant v;
   if (mode == MODE_CHAIN)
     v = !w_mn ? V_CONV1X1_CHAIN
-              : (p.p_split ? V_GEMM_CHAIN_WIDE : (p.p_tmem ? V_GEMM_CHAIN_PAIR : V_GEMM_CHAIN));
+              : (p.p_split ? V_GEMM_CHAIN_WIDE
+                           : (p.p_tmem && !p.resident ? V_GEMM_CHAIN_PAIR : V_GEMM_CHAIN));
   else v = w_mn ? V_GEMM_SINGLE : V_CONV1X1_SINGLE;
   return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
 }

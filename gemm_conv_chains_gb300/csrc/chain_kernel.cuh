@@ -248,6 +248,8 @@ template <int MODE, bool A4D, bool W0MN, bool W1MN, bool WIDE, bool PAIR>
 __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
                               const CUtensorMap* tmW0, const CUtensorMap* tmW1, uint32_t base,
                               uint32_t bars, volatile uint32_t* abort_flag) {
+  // Tile-pair instantiations are launched with streamed weights only.
+  const bool resident = !PAIR && p.resident != 0;
   const uint32_t lead = elect_one();
   const uint64_t pol_stream = l2_policy_evict_first();
   const uint64_t pol_keep = l2_policy_evict_last();
@@ -258,7 +260,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
   bool w_issued = false;
   bool ok = true;
 
-  if (p.resident) {
+  if (resident) {
     const uint32_t wbar = bars + 8u * BAR_WFULL;
     uint32_t total = p.kchunks0 * p.w0_chunk_bytes;
     if (MODE == MODE_CHAIN || MODE == MODE_CHAIN3) total += p.kchunks1 * p.w1_chunk_bytes;
@@ -295,9 +297,9 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
       trace(EV_PROD_ACQUIRE, kc, it);
       const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
-      mbar_arrive_expect_tx_if(lead, fb, p.a_stage_bytes + (p.resident ? 0u : p.w0_chunk_bytes));
+      mbar_arrive_expect_tx_if(lead, fb, p.a_stage_bytes + (resident ? 0u : p.w0_chunk_bytes));
       load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, k, fb, pol_stream);
-      if (!p.resident)
+      if (!resident)
         load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, k, fb, pol_keep);
       if (A4D && p.halo) k.next_halo(p); else k.next(p);
       // Tile it + 2's A into L2 behind this tile's first chunk (tile 0, and tile 1 when
@@ -312,7 +314,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
   // Streamed W1 for GEMM1 of the it-th tile (or, with w1_group, of the pair it, it + 1):
   // w1_per_stage chunks per ring stage.
   auto load_g1 = [&](int it) -> bool {
-    if (MODE != MODE_CHAIN || p.resident) return true;
+    if (MODE != MODE_CHAIN || resident) return true;
     const int32_t t = blockIdx.x + it * gridDim.x;
     for (int kc1 = 0; kc1 < p.kchunks1;) {
       if (!acquire(t)) return false;
@@ -457,12 +459,13 @@ __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE, bool PAIR>
 __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
                          volatile uint32_t* abort_flag) {
+  const bool resident = !PAIR && p.resident != 0;   // (as in the producer)
   const uint32_t idesc0 = idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p);
   const uint32_t idesc1 = idesc_f16_f32(BF16 ? 1u : 0u, W1MN ? 1u : 0u, kBlockM, p.N1p);
   bool ok = true;
   const uint32_t lead = elect_one();
   Tracer trace(p, 1, lead, 3);   // slots 0..2: the kernel's entry, setup and dependency events
-  if (p.resident)
+  if (resident)
     ok = warp_mbar_wait(bars + 8u * BAR_WFULL, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
   bool bias_ready = false;   // the epilogue warps write the bias operands at the start
 
@@ -562,7 +565,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         }
         if (++cb == p.kc_per_tap) { cb = 0; ++s_tap; }
       } else {
-        const uint64_t bdesc = p.resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
+        const uint64_t bdesc = resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
                                           : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
         if (++cb == p.kc_per_tap) cb = 0;
         issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
@@ -597,7 +600,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     int slot = 0;
     for (int kc1 = 0; kc1 < p.kchunks1; ++kc1) {
       uint64_t bdesc;
-      if (p.resident) {
+      if (resident) {
         bdesc = res_w1 + static_cast<uint64_t>(kc1) * w1_step;
       } else {
         if (slot == 0) {
@@ -619,7 +622,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
                                static_cast<uint64_t>(kc1) * (kPChunkBytes >> 4);
         issue_chunk<W1MN>(lead, d1, adesc, bdesc, idesc1, nks1, kc1 == 0);
       }
-      if (!p.resident && (++slot == per || kc1 == p.kchunks1 - 1)) {
+      if (!resident && (++slot == per || kc1 == p.kchunks1 - 1)) {
         slot = 0;
         mma_commit(lead, bars + 8u * (BAR_EMPTY0 + stage));
         if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
@@ -1056,7 +1059,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
   const int q = warp & 3;                     // TMEM lane quadrant this warp may access
   const int row = q * 32 + lane;
   const uint32_t tm_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-  const int groups = p.epi_groups;
+  const int groups = PAIR ? 2 : p.epi_groups;   // tile pairs: alternate tiles
   const int g = groups == 2 ? wg : 0;         // which tiles
   const int c_first = groups == 2 ? 0 : 32 * wg;   // which columns
   const int c_step = groups == 2 ? 32 : 64;
@@ -1077,7 +1080,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
                       SITE_EPI_ACC_FULL, t);
     if (elected) trace(EV_EPI_ACC_READY, g, it);
     tc_fence_after_sync();
-    if (p.out_alias_p) {   // P[b] doubles as this group's previous output staging
+    if (!PAIR && p.out_alias_p) {   // P[b] doubles as this group's previous output staging
       if (elected) bulk_wait_read_all();
       named_bar_sync(bar_id, group_threads);
     }
@@ -1104,7 +1107,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
                       SITE_EPI_D1_FULL, t);
     if (elected) trace(EV_EPI_D1_READY, g, it);
     tc_fence_after_sync();
-    if (!p.out_alias_p) {
+    if (PAIR || !p.out_alias_p) {
       if (elected) bulk_wait_read_all();
       named_bar_sync(bar_id, group_threads);
     }

@@ -22,7 +22,7 @@ enum Variant : int {
   V_CONV_POOL,
   V_GEMM_CHAIN3,
   V_GEMM_CHAIN_WIDE,
-  V_GEMM_CHAIN_PAIR,   // P in TMEM, tiles in pairs (the loops of the other plans left out)
+  V_GEMM_CHAIN_PAIR,   // P in TMEM, tiles in pairs, streamed weights (other loops left out)
   V_COUNT
 };
 
