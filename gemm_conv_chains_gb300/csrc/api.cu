@@ -37,7 +37,7 @@ struct DeviceState {
   int num_sms = 0;
   uint32_t* err = nullptr;                    // device address of g_error_word
   cudaError_t init_error = cudaSuccess;
-  std::atomic<uint32_t> attr_done{0};         // bit 2v + bf16: smem attribute set
+  std::atomic<uint64_t> attr_done{0};   // bit 2 (v + V_COUNT traced) + bf16: smem attribute set
 };
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
@@ -516,9 +516,11 @@ void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const v
 b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtensorMap& w0,
                   const CUtensorMap& w1, const CUtensorMap& out, ChainParams& p, size_t smem,
                   int grid, void* stream) {
-  const uint32_t bit = 1u << (2u * static_cast<uint32_t>(v) + (p.is_bf16 ? 1u : 0u));
+  const bool traced = p.trace != nullptr;
+  const uint64_t bit = 1ull << (2u * (static_cast<uint32_t>(v) + (traced ? V_COUNT : 0u)) +
+                                (p.is_bf16 ? 1u : 0u));
   if ((d->attr_done.load() & bit) == 0u) {
-    if (cudaFuncSetAttribute(variant_func(v, p.is_bf16 != 0),
+    if (cudaFuncSetAttribute(variant_func(v, p.is_bf16 != 0, traced),
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemLimit)) != cudaSuccess) {
       cudaGetLastError();

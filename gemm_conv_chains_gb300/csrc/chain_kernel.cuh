@@ -51,7 +51,20 @@
 #include "kernel_params.h"
 #include "ptx.cuh"
 
+// Every kernel unit is compiled twice: without the event trace (B2B_TRACE 0, the kernels
+// every launch uses) and with it (B2B_TRACE 1, launched only while a trace buffer is set).
+// The two builds live in the namespaces b2b::plain and b2b::traced.
+#ifndef B2B_TRACE
+#define B2B_TRACE 0
+#endif
+#if B2B_TRACE
+#define B2B_KNS traced
+#else
+#define B2B_KNS plain
+#endif
+
 namespace b2b {
+namespace B2B_KNS {
 
 // Barrier slots (8 bytes each) at p.off_bar.
 enum : uint32_t {
@@ -96,6 +109,9 @@ __device__ __forceinline__ TileCoord tile_coord(const ChainParams& p, int32_t t)
 // own region with plain stores, so tracing costs a few instructions per event.  An event
 // is two words: %globaltimer (ns; one clock for all warps and SMs), and
 // code | group << 8 | tile index << 16 | 1 << 63.
+// Without B2B_TRACE the tracer is empty: even a disabled trace (a pointer test per event)
+// cost the FFN chain 5 % and the 1x1 conv chain 8 % per launch.
+#if B2B_TRACE
 struct Tracer {
   unsigned long long* base = nullptr;
   uint32_t n = 0, cap = 0;
@@ -115,6 +131,12 @@ struct Tracer {
     ++n;
   }
 };
+#else
+struct Tracer {
+  __device__ __forceinline__ Tracer(const ChainParams&, uint32_t, uint32_t, uint32_t = 0) {}
+  __device__ __forceinline__ void operator()(uint32_t, uint32_t, int) {}
+};
+#endif
 
 // Number of tiles this CTA processes (tiles blockIdx.x, blockIdx.x + gridDim.x, ...).
 __device__ __forceinline__ int local_tiles(const ChainParams& p) {
@@ -1460,4 +1482,5 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   }
 }
 
+}  // namespace B2B_KNS
 }  // namespace b2b

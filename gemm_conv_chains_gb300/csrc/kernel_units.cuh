@@ -7,6 +7,7 @@
 #include "launch.h"
 
 namespace b2b {
+namespace B2B_KNS {
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
           bool PAIR = false>
@@ -89,4 +90,5 @@ cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMa
   }
 }
 
+}  // namespace B2B_KNS
 }  // namespace b2b

@@ -8,36 +8,57 @@
 
 namespace b2b {
 
-template <bool BF16>
-const void* variant_func_a2d(Variant v);
-template <bool BF16>
-const void* variant_func_a4d(Variant v);
-template <bool BF16>
-cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
-                               const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
-                               int grid, size_t smem, cudaStream_t s);
-template <bool BF16>
-cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
-                               const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
-                               int grid, size_t smem, cudaStream_t s);
+// The kernel units, each compiled without (b2b::plain) and with (b2b::traced) the trace.
+#define B2B_UNIT_DECLS                                                                       \
+  template <bool BF16>                                                                       \
+  const void* variant_func_a2d(Variant v);                                                   \
+  template <bool BF16>                                                                       \
+  const void* variant_func_a4d(Variant v);                                                   \
+  template <bool BF16>                                                                       \
+  cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,     \
+                                 const CUtensorMap& w1, const CUtensorMap& out,              \
+                                 const ChainParams& p, int grid, size_t smem, cudaStream_t s); \
+  template <bool BF16>                                                                       \
+  cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,     \
+                                 const CUtensorMap& w1, const CUtensorMap& out,              \
+                                 const ChainParams& p, int grid, size_t smem, cudaStream_t s);
+namespace plain {
+B2B_UNIT_DECLS
+}
+namespace traced {
+B2B_UNIT_DECLS
+}
+#undef B2B_UNIT_DECLS
 
 static bool is_a4d(Variant v) {
   return v == V_CONV_CHAIN || v == V_CONV_SINGLE || v == V_CONV_POOL;
 }
 
-const void* variant_func(Variant v, bool bf16) {
-  if (is_a4d(v)) return bf16 ? variant_func_a4d<true>(v) : variant_func_a4d<false>(v);
-  return bf16 ? variant_func_a2d<true>(v) : variant_func_a2d<false>(v);
+const void* variant_func(Variant v, bool bf16, bool trace) {
+  if (trace) {
+    if (is_a4d(v)) return bf16 ? traced::variant_func_a4d<true>(v) : traced::variant_func_a4d<false>(v);
+    return bf16 ? traced::variant_func_a2d<true>(v) : traced::variant_func_a2d<false>(v);
+  }
+  if (is_a4d(v)) return bf16 ? plain::variant_func_a4d<true>(v) : plain::variant_func_a4d<false>(v);
+  return bf16 ? plain::variant_func_a2d<true>(v) : plain::variant_func_a2d<false>(v);
 }
 
 cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
                            const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
                            int grid, size_t smem, cudaStream_t stream) {
+  const bool bf16 = p.is_bf16 != 0;
+  if (p.trace != nullptr) {
+    if (is_a4d(v))
+      return bf16 ? traced::launch_variant_a4d<true>(v, a, w0, w1, out, p, grid, smem, stream)
+                  : traced::launch_variant_a4d<false>(v, a, w0, w1, out, p, grid, smem, stream);
+    return bf16 ? traced::launch_variant_a2d<true>(v, a, w0, w1, out, p, grid, smem, stream)
+                : traced::launch_variant_a2d<false>(v, a, w0, w1, out, p, grid, smem, stream);
+  }
   if (is_a4d(v))
-    return p.is_bf16 ? launch_variant_a4d<true>(v, a, w0, w1, out, p, grid, smem, stream)
-                     : launch_variant_a4d<false>(v, a, w0, w1, out, p, grid, smem, stream);
-  return p.is_bf16 ? launch_variant_a2d<true>(v, a, w0, w1, out, p, grid, smem, stream)
-                   : launch_variant_a2d<false>(v, a, w0, w1, out, p, grid, smem, stream);
+    return bf16 ? plain::launch_variant_a4d<true>(v, a, w0, w1, out, p, grid, smem, stream)
+                : plain::launch_variant_a4d<false>(v, a, w0, w1, out, p, grid, smem, stream);
+  return bf16 ? plain::launch_variant_a2d<true>(v, a, w0, w1, out, p, grid, smem, stream)
+              : plain::launch_variant_a2d<false>(v, a, w0, w1, out, p, grid, smem, stream);
 }
 
 // ------------------------------------------------------------------------------------

@@ -48,10 +48,11 @@ inline cudaError_t launch_chain(ChainKernelFn fn, const CUtensorMap& a, const CU
   return cudaLaunchKernelEx(&cfg, fn, a, w0, w1, out, p);
 }
 
-// Kernel function pointer of a variant and operand dtype (for cudaFuncSetAttribute).
-const void* variant_func(Variant v, bool bf16);
+// Kernel function pointer of a variant, operand dtype and build (with or without the event
+// trace), for cudaFuncSetAttribute.
+const void* variant_func(Variant v, bool bf16, bool trace);
 
-// Launches the variant's kernel for p.is_bf16.
+// Launches the variant's kernel for p.is_bf16, the traced build when p.trace is set.
 cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w0,
                            const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
                            int grid, size_t smem, cudaStream_t stream);

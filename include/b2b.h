@@ -221,7 +221,9 @@ void b2b_set_wait_limit_ns(uint64_t ns);
  * MMA issuer, epilogue group 0, epilogue group 1); each role appends its events to its
  * region: word 2i = time, word 2i+1 = event code | group << 8 | tile index << 16 |
  * 1 << 63 (codes: TraceEvent in kernel_params.h); unused words stay 0.  buf = NULL turns
- * tracing off.  buf must be 8-byte aligned and stay valid while traced launches run. */
+ * tracing off.  buf must be 8-byte aligned and stay valid while traced launches run.
+ * Traced launches run a separate build of the kernels with the recording compiled in;
+ * untraced launches carry none of it, so timings taken under a trace run a little slow. */
 b2b_status b2b_set_trace(void* buf, uint32_t capacity, uint32_t cta);
 
 /* Reads and clears the current device's error word.  Synchronises the current device.
