@@ -726,9 +726,10 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   p.pf_w1_bytes = mode == MODE_CHAIN ? static_cast<uint32_t>(static_cast<uint64_t>(N0) * N1 * e) : 0u;
   Variant v;
   if (mode == MODE_CHAIN)
-    v = !w_mn ? V_CONV1X1_CHAIN
-              : (p.p_split ? V_GEMM_CHAIN_WIDE
-                           : (p.p_tmem && !p.resident ? V_GEMM_CHAIN_PAIR : V_GEMM_CHAIN));
+    v = !w_mn ? (p.p_tmem ? V_CONV1X1_CHAIN : V_CONV1X1_CHAIN_NP)
+              : (p.p_split  ? V_GEMM_CHAIN_WIDE
+                 : !p.p_tmem ? V_GEMM_CHAIN_NP
+                             : (!p.resident ? V_GEMM_CHAIN_PAIR : V_GEMM_CHAIN));
   else v = w_mn ? V_GEMM_SINGLE : V_CONV1X1_SINGLE;
   return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
 }
@@ -850,7 +851,9 @@ b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t
   p.pf_w0_bytes = static_cast<uint32_t>(static_cast<uint64_t>(C0) * R * S * C * e);
   p.pf_w1 = static_cast<const uint8_t*>(W1);
   p.pf_w1_bytes = mode == MODE_CHAIN ? static_cast<uint32_t>(static_cast<uint64_t>(C1) * C0 * e) : 0u;
-  const Variant v = mode == MODE_CHAIN ? V_CONV_CHAIN : mode == MODE_SINGLE ? V_CONV_SINGLE : V_CONV_POOL;
+  const Variant v = mode == MODE_CHAIN    ? (p.p_tmem ? V_CONV_CHAIN : V_CONV_CHAIN_NP)
+                    : mode == MODE_SINGLE ? V_CONV_SINGLE
+                                          : V_CONV_POOL;
   return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
 }
 

@@ -266,7 +266,7 @@ __device__ __forceinline__ void prefetch_a_tile(const ChainParams& p, int32_t t)
   bulk_prefetch_l2(p.pf_a + off, static_cast<uint32_t>(n));
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool WIDE, bool PAIR>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool WIDE, bool PAIR, bool NOPAIR>
 __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
                               const CUtensorMap* tmW0, const CUtensorMap* tmW1, uint32_t base,
                               uint32_t bars, volatile uint32_t* abort_flag) {
@@ -404,7 +404,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
       if (ok) ok = load_w1_half(it, f);
       if (ok) ok = load_w1_half(it, f ^ 1);
     }
-  } else if (MODE == MODE_CHAIN && (PAIR || p.p_tmem)) {
+  } else if (MODE == MODE_CHAIN && (PAIR || (!NOPAIR && p.p_tmem))) {
     // Pairs: G0(0), G0(1), then G1(k), G1(k+1), G0(k+2), G0(k+3) -- as the MMA issuer.
     for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = load_g0(it);
     for (int k = 0; ok && k < ntiles; k += 2) {
@@ -478,7 +478,7 @@ __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32
                (first && ks == 0) ? 0u : 1u);
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE, bool PAIR>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE, bool PAIR, bool NOPAIR>
 __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
                          volatile uint32_t* abort_flag) {
   const bool resident = !PAIR && p.resident != 0;   // (as in the producer)
@@ -554,7 +554,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   auto issue_g0 = [&](int it) -> bool {
     const int32_t t = blockIdx.x + it * gridDim.x;
     const uint32_t b = buf_of(p, it);
-    if ((MODE != MODE_CHAIN && MODE != MODE_CHAIN3) || PAIR || p.p_tmem) {
+    if ((MODE != MODE_CHAIN && MODE != MODE_CHAIN3) || PAIR || (!NOPAIR && p.p_tmem)) {
       // The epilogue must have drained the buffer's previous tile (with P in TMEM: its
       // GEMM1 accumulator, the last thing read from the buffer).
       if (!warp_mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), use_of(p, it) ^ 1u, p, abort_flag,
@@ -635,7 +635,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
                 static_cast<uint64_t>(slot) * w1_step;
       }
       const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
-      if (PAIR || p.p_tmem) {
+      if (PAIR || (!NOPAIR && p.p_tmem)) {
         issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * static_cast<uint32_t>(kc1), bdesc, idesc1,
                              nks1, kc1 == 0);
       } else {
@@ -821,7 +821,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         if (ok) ok = issue_g0_half(it, f ^ 1, true);
         if (ok) ok = issue_g1_wide(it);
       }
-    } else if (MODE == MODE_CHAIN && (PAIR || p.p_tmem)) {
+    } else if (MODE == MODE_CHAIN && (PAIR || (!NOPAIR && p.p_tmem))) {
       // Pairs of tiles: while the epilogue of one tile drains, the other tile's MMAs run.
       for (int it = 0; ok && it < 2 && it < ntiles; ++it) ok = issue_g0(it);
       for (int k = 0; ok && k < ntiles; k += 2) {
@@ -1072,7 +1072,7 @@ __device__ __forceinline__ bool warp_wait(bool alive, uint32_t bar, uint32_t par
 // Epilogue warps.  With epi_groups == 2 warpgroup g (warps 2+4g .. 5+4g) takes the
 // CTA's tiles i with i & 1 == g and owns buffer g; with epi_groups == 1 all eight warps
 // take every tile and warpgroup g drains the 32-column blocks 2k + g.
-template <int MODE, bool A4D, bool BF16, bool WIDE, bool PAIR>
+template <int MODE, bool A4D, bool BF16, bool WIDE, bool PAIR, bool NOPAIR>
 __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, uint32_t base,
                               uint32_t bars, uint32_t tmem_base,
                               volatile uint32_t* abort_flag) {
@@ -1107,7 +1107,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       named_bar_sync(bar_id, group_threads);
     }
     if (alive) {
-      if (PAIR || p.p_tmem)
+      if (PAIR || (!NOPAIR && p.p_tmem))
         drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b], p.N0p, p.d0_col[b]);
       else
         drain_to_smem<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, p_tile,
@@ -1139,7 +1139,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
                           row, kPChunkBytes);
     if (elected) trace(EV_EPI_DRAINED, g, it);
     tc_fence_before_sync();
-    if (PAIR || p.p_tmem) {   // the buffer (D0 -> P + D1) may take tile i + 2
+    if (PAIR || (!NOPAIR && p.p_tmem)) {   // the buffer (D0 -> P + D1) may take tile i + 2
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + b));
     }
@@ -1372,7 +1372,7 @@ __device__ __forceinline__ void fill_w2(const ChainParams& p, uint8_t* dst, int 
 // the kernel
 // ------------------------------------------------------------------------------------
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false>
+          bool PAIR = false, bool NOPAIR = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW0,
                  const __grid_constant__ CUtensorMap tmW1,
@@ -1454,10 +1454,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
     }
     __syncwarp();
-    producer_role<MODE, A4D, W0MN, W1MN, WIDE, PAIR>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
+    producer_role<MODE, A4D, W0MN, W1MN, WIDE, PAIR, NOPAIR>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR>(p, base, bars, tmem_base, abort_flag);
+    mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR>(p, base, bars, tmem_base, abort_flag);
     __syncwarp();
   } else {
     // The bias operands, off the producer's critical path; the MMA issuer waits for them
@@ -1471,7 +1471,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8u * BAR_BIAS_READY);
-    epilogue_role<MODE, A4D, BF16, WIDE, PAIR>(p, &tmOut, base, bars, tmem_base, abort_flag);
+    epilogue_role<MODE, A4D, BF16, WIDE, PAIR, NOPAIR>(p, &tmOut, base, bars, tmem_base, abort_flag);
   }
 
   tc_fence_before_sync();

@@ -10,17 +10,18 @@ namespace b2b {
 namespace B2B_KNS {
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false>
+          bool PAIR = false, bool NOPAIR = false>
 const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR>);
+  return reinterpret_cast<const void*>(
+      &chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR>);
 }
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false>
+          bool PAIR = false, bool NOPAIR = false>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1,
                        const CUtensorMap& out, const ChainParams& p, int grid, size_t smem,
                        cudaStream_t stream) {
-  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR>, a, w0, w1, out, p, grid,
+  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR>, a, w0, w1, out, p, grid,
                       smem, stream);
 }
 
@@ -35,6 +36,10 @@ const void* variant_func_a2d(Variant v) {
     case V_GEMM_CHAIN3: return kernel_ptr<MODE_CHAIN3, false, true, true, BF16>();
     case V_GEMM_CHAIN_WIDE: return kernel_ptr<MODE_CHAIN, false, true, true, BF16, true>();
     case V_GEMM_CHAIN_PAIR: return kernel_ptr<MODE_CHAIN, false, true, true, BF16, false, true>();
+    case V_GEMM_CHAIN_NP:
+      return kernel_ptr<MODE_CHAIN, false, true, true, BF16, false, false, true>();
+    case V_CONV1X1_CHAIN_NP:
+      return kernel_ptr<MODE_CHAIN, false, false, false, BF16, false, false, true>();
     default: return nullptr;
   }
 }
@@ -60,6 +65,12 @@ cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMa
     case V_GEMM_CHAIN_PAIR:
       return launch_one<MODE_CHAIN, false, true, true, BF16, false, true>(a, w0, w1, out, p, grid,
                                                                          smem, s);
+    case V_GEMM_CHAIN_NP:
+      return launch_one<MODE_CHAIN, false, true, true, BF16, false, false, true>(
+          a, w0, w1, out, p, grid, smem, s);
+    case V_CONV1X1_CHAIN_NP:
+      return launch_one<MODE_CHAIN, false, false, false, BF16, false, false, true>(
+          a, w0, w1, out, p, grid, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -69,6 +80,8 @@ template <bool BF16>
 const void* variant_func_a4d(Variant v) {
   switch (v) {
     case V_CONV_CHAIN: return kernel_ptr<MODE_CHAIN, true, false, false, BF16>();
+    case V_CONV_CHAIN_NP:
+      return kernel_ptr<MODE_CHAIN, true, false, false, BF16, false, false, true>();
     case V_CONV_SINGLE: return kernel_ptr<MODE_SINGLE, true, false, false, BF16>();
     case V_CONV_POOL: return kernel_ptr<MODE_POOL, true, false, false, BF16>();
     default: return nullptr;
@@ -82,6 +95,9 @@ cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMa
   switch (v) {
     case V_CONV_CHAIN:
       return launch_one<MODE_CHAIN, true, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    case V_CONV_CHAIN_NP:
+      return launch_one<MODE_CHAIN, true, false, false, BF16, false, false, true>(
+          a, w0, w1, out, p, grid, smem, s);
     case V_CONV_SINGLE:
       return launch_one<MODE_SINGLE, true, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
     case V_CONV_POOL:

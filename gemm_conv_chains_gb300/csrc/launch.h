@@ -23,6 +23,9 @@ enum Variant : int {
   V_GEMM_CHAIN3,
   V_GEMM_CHAIN_WIDE,
   V_GEMM_CHAIN_PAIR,   // P in TMEM, tiles in pairs, streamed weights (other loops left out)
+  V_GEMM_CHAIN_NP,     // the chain variants above with P in shared memory (the P-in-TMEM
+  V_CONV1X1_CHAIN_NP,  //   loops left out)
+  V_CONV_CHAIN_NP,
   V_COUNT
 };
 

@@ -34,11 +34,14 @@ def test_trace_of_a_chain_is_complete_and_causal():
     for name in ("mma_g0_done", "mma_p_ready", "mma_g1_done", "epi_acc_ready", "epi_p_done",
                  "epi_d1_ready", "epi_stored"):
         assert names.count(name) == ntiles, (name, names.count(name), ntiles)
-    when = {(e[1], e[3]): e[0] for e in ev}
+    when = {(e[1], e[3]): e[0] for e in ev}   # the last event of each kind per tile
     for it in range(ntiles):
-        assert when[("mma_g0_done", it)] <= when[("epi_acc_ready", it)]
+        # An MMA issuer's stamp taken after it commits may come after the epilogue has seen
+        # the MMAs complete, so each epilogue step is ordered after a stamp taken before the
+        # MMAs it waits for were issued: the last GEMM0 chunk's arrival, P's publication.
+        assert when[("mma_full", it)] <= when[("epi_acc_ready", it)]
         assert when[("mma_p_ready", it)] <= when[("mma_g1_done", it)]
-        assert when[("mma_g1_done", it)] <= when[("epi_d1_ready", it)]
+        assert when[("mma_p_ready", it)] <= when[("epi_d1_ready", it)]
         assert when[("epi_d1_ready", it)] <= when[("epi_stored", it)]
     # the CTA's entry event comes first, then the end of its setup, then the end of the
     # wait for the previous grid; the first MMA follows both
