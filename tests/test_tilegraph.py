@@ -49,6 +49,24 @@ def test_ffn_l2_traffic_by_hand():
     assert t["total"] == 16_777_216 + 33_554_432 + 9_961_472 + 116_736   # 60.41 MB
 
 
+def test_wide_chain_l2_traffic_by_hand():
+    # N0 = 512: GEMM0 in two passes over the halves of N0, so every tile's A crosses twice;
+    # W0 and W1 streamed per tile (one tile at a time), biases once per CTA.
+    t = tg.l2_to_smem_traffic(wl.GEMM_WIDE)
+    assert t["A"] == 2 * 32768 * 256 * 2
+    assert t["W0"] == 256 * 256 * 512 * 2
+    assert t["W1"] == 256 * 512 * 128 * 2
+    assert t["bias"] == 152 * (512 + 128) * 2
+    assert t["A_in_bounds"] * 2 == t["A"]
+    assert t["total"] == 33_554_432 + 67_108_864 + 33_554_432 + 194_560   # 134.41 MB
+    # a ragged upper half (N0 = 320) still moves a whole four-block box per K chunk
+    w = wl.GemmChain("w320", "bf16", 1280, 128, 320, 64, "relu", "relu")
+    assert tg.l2_to_smem_traffic(w)["W0"] == 10 * 2 * (2 * 4 * 64 * 64 * 2)
+    # and with N0 not a multiple of 64 one box per block: 5 blocks per K chunk
+    w = wl.GemmChain("w296", "bf16", 1280, 128, 296, 64, "relu", "relu")
+    assert tg.l2_to_smem_traffic(w)["W0"] == 10 * 2 * (5 * 64 * 64 * 2)
+
+
 def test_conv_boxes_are_moved_whole():
     # conv3x3 -> 1x1 on 56 x 56 images: 32 x 7 x 4 tiles of 8 x 16 pixels (the fourth tile
     # column is half outside the image), 3 halo boxes of 10 x 16 pixels x 64 channels each;
