@@ -446,7 +446,9 @@ TRACE_EVENTS = {1: "prod_acquire", 2: "prod_issued", 3: "mma_full", 4: "mma_g0_d
 
 def set_trace(buf, cta: int = 0) -> None:
     """Records the per-step timeline of CTA `cta` of later launches into `buf` (a zeroed,
-    contiguous CUDA int64 tensor of 2 * capacity words); None turns it off."""
+    contiguous CUDA int64 tensor of 2 * capacity words); None turns it off.  Traced launches
+    run a separate build of the kernels with the recording compiled in, a little slower
+    than the plain build every other launch uses."""
     if buf is None:
         _raise(lib().b2b_set_trace(None, 0, 0), "b2b_set_trace")
         return
