@@ -334,6 +334,20 @@ def test_wide_chains_split_gemm0(dims):
     assert p["p_split"] == 256 and p["groups"] == 1 and p["nbuf"] == 1
 
 
+def test_wide_chain_plan_sweep():
+    # every width 256 < N0 <= 512 (multiples of 8) beside N1 up to 128: the two-pass plan,
+    # its W0 half chunks within a ring stage, W1 packed, D1 inside TMEM on both parities
+    for n0 in range(264, 513, 8):
+        for n1 in (8, 64, 120, 128):
+            for k0 in (8, 256, 1000):
+                p = check("b2b_gemm", (4096, k0, n0, n1), True)
+                assert p["p_split"] == 256 and p["tmem_cols"] == 512
+                assert p["d1_col1"] + p["N1p"] <= 512 and p["d1_col0"] + p["N1p"] <= 256
+                # the upper half's packed P (at 256) ends before D1 of odd tiles (at 384)
+                assert 256 + (p["N0p"] - 256) // 2 <= p["d1_col1"]
+                assert p["w1_per_stage"] * p["w1_chunk"] <= p["stage_bytes"]
+
+
 def test_wide_chain_limits():
     assert plan("b2b_gemm", (1000, 64, 512, 136))[0] == 4     # N1 > 128 beside a wide N0
     assert plan("b2b_gemm", (1000, 64, 520, 64))[0] == 4      # N0 > 512
