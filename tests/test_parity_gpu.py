@@ -48,7 +48,7 @@ GEMM_SHAPES = [
     ("f16", 300, 128, 160, 128),
     ("bf16", 257, 72, 200, 120),
     ("f16", 640, 128, 144, 96),
-    # 256 < N0 <= 512: GEMM0 as two MMAs over D0's halves, one tile in flight
+    # 256 < N0 <= 512: GEMM0 in two passes over the halves of N0 (one tile per CTA here)
     ("bf16", 300, 128, 384, 64),
     ("f16", 257, 72, 264, 24),
     ("bf16", 1000, 256, 512, 128),
@@ -153,10 +153,15 @@ def test_gemm_bias_act(shape, integer):
     compare(dt, wl.to_bits(out.cpu()), ref, integer, "gemm_bias_act")
 
 
-def test_b2b_gemm_wide_n0_sampled_rows():
-    # N0 = 512 over 40000 rows (313 tiles): every CTA runs two or three tiles one at a time
-    w = wl.GemmChain("wide512", "bf16", 40000, 256, 512, 128, "hardswish", "relu",
-                     a_dist="normal")
+@pytest.mark.parametrize("dt,K0,N0,N1", [("bf16", 256, 512, 128), ("f16", 72, 264, 24),
+                                         ("bf16", 128, 384, 64)])
+def test_b2b_gemm_wide_n0_sampled_rows(dt, K0, N0, N1):
+    # 256 < N0 <= 512 over 40000 rows (313 tiles): every CTA runs two or three tiles, which
+    # alternate the half of N0 computed first; the rows sampled cover first tiles (lower
+    # half first), CTA 4's second tile (upper half first) and third tiles.  N0 = 264 loads
+    # W0 one 64-wide block at a time with a one-block upper half; 384 a four-block box
+    # whose upper half is half out of bounds.
+    w = wl.GemmChain(f"wide{N0}", dt, 40000, K0, N0, N1, "hardswish", "relu", a_dist="normal")
     run_b2b_gemm(w, seed=17, rows=np.r_[0:512, 20000:20128, 39744:40000])
 
 
