@@ -299,6 +299,65 @@ def read_ncu_raw_csv(path: str) -> Dict[str, float]:
     return out
 
 
+# Per-SM TMA ingress from L2 measured on the GB300 for one SM loading alone (~89 B/clk);
+# with every SM loading inside the FFN chain it was ~55 B/clk (48 KiB stages ~0.42 us
+# apart), so the L2 bound below is optimistic.
+L2_TO_SM_BYTES_PER_CLK = 89.0
+
+
+def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
+                  tensor_tflops: float = 1951.4, sm_mhz: float = 2070.0,
+                  num_sms: int = 152) -> Dict[str, float]:
+    """Lower bounds, in microseconds, on one fused launch from each resource it streams
+    through.  HBM: the algorithmic bytes (inputs, weights, biases, output) over the copy
+    bandwidth.  L2 -> SM: the busiest CTA's bytes (its tiles' A and streamed weights, W1
+    once per pair of tiles when grouped, its resident weights and biases) over one SM's
+    TMA ingress.  Tensor: the busiest CTA's share of the MMA FLOPs over one SM's share of
+    the peak.  `floor` is the largest; `bound` names it."""
+    plan = plan or plan_of(w)
+    per_cta = tiles_per_cta(plan["tiles"], num_sms)
+    ctas, tiles, n = len(per_cta), plan["tiles"], max(per_cta)
+    t = l2_to_smem_traffic(w, plan, num_sms)
+    cta_bytes = t["A"] / tiles * n + t.get("bias", 0) / ctas + t.get("W2", 0) / ctas
+    for k in ("W0", "W1"):
+        if k not in t:
+            continue
+        if plan["resident"] or isinstance(w, wl.GemmChain3):
+            cta_bytes += t[k] / ctas
+        elif k == "W1" and plan["w1_group"]:
+            loads = sum(-(-m // 2) for m in per_cta)
+            cta_bytes += t[k] / loads * -(-n // 2)
+        else:
+            cta_bytes += t[k] / tiles * n
+    out = {
+        "hbm_us": w.floor_bytes / (hbm_gbs * 1e3),
+        "l2_us": cta_bytes / (L2_TO_SM_BYTES_PER_CLK * sm_mhz),
+        "tensor_us": w.flops / tiles * n / (tensor_tflops * 1e6 / num_sms),
+    }
+    out["bound"] = max(out, key=out.get)[:-3]
+    out["floor_us"] = max(out["hbm_us"], out["l2_us"], out["tensor_us"])
+    return out
+
+
+def bounds_report(measured_us: Optional[Dict[str, float]] = None) -> str:
+    """Markdown table of launch_bounds for every workload, beside measured microseconds per
+    launch where given (name -> us)."""
+    measured_us = measured_us or {}
+    lines = ["| workload | tiles per CTA (max) | HBM us | L2 -> SM us | tensor us | floor | "
+             "measured us | floor / measured |", "|---|---|---|---|---|---|---|---|"]
+    for name, w in wl.WORKLOADS.items():
+        plan = plan_of(w)
+        b = launch_bounds(w, plan)
+        m = measured_us.get(name)
+        got = "" if m is None else f"{m:.2f}"
+        frac = "" if m is None else f"{b['floor_us'] / m:.2f}"
+        lines.append(
+            f"| {name} | {max(tiles_per_cta(plan['tiles'], 152))} | {b['hbm_us']:.2f} "
+            f"| {b['l2_us']:.2f} | {b['tensor_us']:.2f} | {b['floor_us']:.2f} ({b['bound']}) "
+            f"| {got} | {frac} |")
+    return "\n".join(lines)
+
+
 def report(ncu: Optional[Dict[str, str]] = None) -> str:
     """Markdown table of the model for every workload, beside the counters of one
     captured launch per workload where an export is given (name -> csv path)."""
@@ -328,7 +387,13 @@ def main(argv: Optional[Sequence[str]] = None) -> None:
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--ncu", nargs="*", default=[], metavar="WORKLOAD=CSV",
                     help="raw-page csv export of one captured chain launch per workload")
+    ap.add_argument("--bounds", nargs="*", default=None, metavar="WORKLOAD=US",
+                    help="print the per-resource launch bounds instead, beside measured "
+                         "microseconds per launch")
     args = ap.parse_args(argv)
+    if args.bounds is not None:
+        print(bounds_report({k: float(v) for k, v in (a.split("=", 1) for a in args.bounds)}))
+        return
     print(report(dict(a.split("=", 1) for a in args.ncu)))
 
 

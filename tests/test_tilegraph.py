@@ -67,6 +67,22 @@ def test_wide_chain_l2_traffic_by_hand():
     assert tg.l2_to_smem_traffic(w)["W0"] == 10 * 2 * (5 * 64 * 64 * 2)
 
 
+def test_ffn_launch_bounds_by_hand():
+    # 104 CTAs run two tiles: per busiest SM, A 2 x 64 KiB + W0 2 x 128 KiB + W1 64 KiB
+    # (once per pair) + biases 768 B from L2; 2/256 of the MMA FLOPs on 1/152 of the peak
+    b = tg.launch_bounds(wl.GEMM_FFN, hbm_gbs=6791.4, tensor_tflops=1951.4, sm_mhz=2070.0)
+    assert abs(b["hbm_us"] - 25_363_200 / 6791.4e3) < 1e-9
+    cta = 2 * 65536 + 2 * 131072 + 65536 + 768
+    assert abs(b["l2_us"] - cta / (tg.L2_TO_SM_BYTES_PER_CLK * 2070.0)) < 1e-9
+    flops = 2 * 32768 * (256 * 256 + 256 * 128)
+    assert abs(b["tensor_us"] - flops * 2 / 256 / (1951.4e6 / 152)) < 1e-9
+    assert b["bound"] == "tensor" and b["floor_us"] == b["tensor_us"]
+    # a resident-weight chain charges its weights once per CTA
+    b1 = tg.launch_bounds(wl.CONV1X1)
+    assert b1["bound"] == "hbm"
+    assert "| gemm_ffn | 2 |" in tg.bounds_report({"gemm_ffn": 9.3})
+
+
 def test_conv_boxes_are_moved_whole():
     # conv3x3 -> 1x1 on 56 x 56 images: 32 x 7 x 4 tiles of 8 x 16 pixels (the fourth tile
     # column is half outside the image), 3 halo boxes of 10 x 16 pixels x 64 channels each;
