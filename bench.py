@@ -64,10 +64,15 @@ def load_peaks():
 
 
 def kernel_source_sha():
+    """Hash of the kernel and launch-planner sources, comments and blank lines left out, so
+    that a comment edit keeps the counters taken on the same code valid."""
     h = hashlib.sha256()
     for name in ("chain_kernel.cuh", "ptx.cuh", "kernel_params.h", "kernel_units.cuh", "api.cu"):
-        with open(os.path.join(ROOT, "gemm_conv_chains_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "gemm_conv_chains_gb300", "csrc", name)) as f:
+            for line in f.read().splitlines():
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -38,7 +38,13 @@
 // tiles, so GEMM0 of tile i+2 and GEMM1 of tile i+1 run while the epilogue of tile i
 // drains.  The MMA issue order is G0(0), G0(1), then G1(j), G0(j+2) for j = 0, 1, ...
 // Otherwise (one buffer) it is G0(0), then G1(j), G0(j+1), and both warpgroups split the
-// columns of every tile.
+// columns of every tile.  With P kept in TMEM (N0 > 128) tiles run in pairs: G0(k),
+// G0(k+1), G1(k), G1(k+1), each tile's P packed in place over its GEMM0 columns.  Wide
+// chains (256 < N0 <= 512, the WIDE instantiation) run GEMM0 in two passes over the
+// halves of N0, each warpgroup packing one half's P while the other pass or GEMM1 runs;
+// D1 sits in the half computed first, which alternates from tile to tile.  The schedules
+// are separate instantiations (WIDE, PAIR, NOPAIR) so that each kernel carries only its
+// own loops, and every unit is compiled once without the event trace and once with it.
 //
 // Every wait is bounded (see ptx.cuh); on a timeout all roles leave their loops, the MMA
 // issuer drains its MMAs, the producer drains its copies, and TMEM is freed.

@@ -149,12 +149,12 @@ struct ChainParams {
                                 //    pair of tiles, w1_per_stage chunks per ring stage,
                                 //    and both tiles' GEMM1 read it from the same stages
   uint32_t w1_per_stage;        // W1 chunks per ring stage when w1_group
-  uint32_t p_hi;                // (wide) TMEM column of P's upper half from the buffer start
-  uint32_t p_split;             // wide chains (256 < N0p <= 512, P in TMEM, one tile in
-                                //    flight): GEMM0 runs as two MMAs per K step, D0's
-                                //    columns [0, 256) and [256, N0p); each warpgroup packs
-                                //    one half in place, P's K chunks from p_split on sit at
-                                //    p_hi.  0 otherwise.
+  uint32_t p_hi;                // (wide) TMEM column of the upper half's D0 and P
+  uint32_t p_split;             // wide chains (256 < N0p <= 512, P in TMEM): 256, the
+                                //    width of GEMM0's lower pass; GEMM0 runs in two passes
+                                //    over the halves of N0 into TMEM columns [0, 256) and
+                                //    [256, N0p), each half's P packed in place by one
+                                //    warpgroup.  0 otherwise.
   int32_t epi_groups;           // 2: the epilogue warpgroups take alternate tiles;
                                 // 1: both warpgroups split the columns of every tile
   uint32_t tmem_cols;
