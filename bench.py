@@ -518,6 +518,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": w.floor_bytes,
+                     "kernel_source_sha": kernel_source_sha(),
                      "peak_source": peaks["source"],
                      "tensor": {"achieved_tflops": round(tflops, 1), "peak": peaks["bf16_tflops"],
                                 "frac": round(tflops / peaks["bf16_tflops"], 4)}},
