@@ -2,16 +2,21 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Headline workload: the FFN-like b2b GEMM, bf16, A[32768,256] . W0[256,256] (+b0,
-Hardswish) . W1[256,128] (+b1, Hardswish).  One step = one fused launch over one batch.
-Prints ONE JSON line (rank 0).
+Headline workload: the FFN-like b2b GEMM, bf16, A[262144,256] . W0[256,256] (+b0,
+Hardswish) . W1[256,128] (+b1, Hardswish) -- the largest point of that chain's M sweep
+(4096 .. 262144 rows), the largest single-GPU configuration of the chain.  One step = one
+fused launch over one batch.  Prints ONE JSON line (rank 0).
 
   value        whole-job TFLOP/s (MMA FLOPs 2*M*(K0*N0 + N0*N1) per step), inputs resident
                in HBM; the K timed steps rotate through input/output sets whose total size
                exceeds twice the L2, so every step streams its A from HBM.
-  roofline     the fused kernel's algorithmic bytes (A + W0 + b0 + W1 + b1 + out) per
-               launch over its average launch time, against the measured HBM copy rate.
+  roofline     the fused kernel against the resource that bounds it: the slower of its
+               FLOPs at the measured tensor peak and its algorithmic bytes (A + W0 + b0 +
+               W1 + b1 + out) at the measured HBM copy rate.  HBM-bound: achieved GB/s of
+               algorithmic bytes over the average launch time; tensor-bound: TFLOP/s.
   pct_of_roofline  100 * max(FLOPs / tensor peak, bytes / HBM peak) / measured time.
+  sweep        the FFN-like chain over its M sweep: per M, microseconds per launch,
+               TFLOP/s, percent of roofline and the unfused path's microseconds.
   unfused      the same chain as two launches (GEMM0 + epilogue -> HBM -> GEMM1), its
                time and algorithmic bytes (the intermediate written and read back).
   e2e          the same metric through the public API from pinned host buffers: every step
@@ -47,7 +52,7 @@ from gemm_conv_chains_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "fused-chain TFLOPS and % of roofline; HBM bytes vs unfused 2-kernel path"
 UNIT = "TFLOP/s"
-HEADLINE = wl.GEMM_FFN
+HEADLINE = wl.GEMM_FFN_LARGE
 
 
 def load_peaks():
@@ -277,6 +282,33 @@ def pool_runner(w: wl.ConvPool, dev):
     return fused, unfused, n, set_bytes
 
 
+def roofline_of(w, t_step, peaks):
+    """The bound of workload `w` (the slower of FLOPs at the tensor peak and algorithmic
+    bytes at the HBM peak) and what one step of `t_step` seconds achieves against it."""
+    t_flop = w.flops / (peaks["bf16_tflops"] * 1e12)
+    t_byte = w.floor_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_flop > t_byte:
+        achieved = w.flops / t_step / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4)}
+    achieved = w.floor_bytes / t_step / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+
+
+def shape_config(w):
+    """The shape keys of a workload, for the printed config."""
+    if isinstance(w, wl.GemmChain):
+        return {"M": w.M, "K0": w.K0, "N0": w.N0, "N1": w.N1, "act0": w.act0, "act1": w.act1}
+    if isinstance(w, wl.GemmChain3):
+        return {"M": w.M, "K0": w.K0, "N0": w.N0, "N1": w.N1, "N2": w.N2,
+                "acts": [w.act0, w.act1, w.act2]}
+    if isinstance(w, wl.ConvChain):
+        return {"N": w.N, "H": w.H, "W": w.W, "C": w.C, "C0": w.C0, "R": w.R, "S": w.S,
+                "pad": w.pad, "stride": w.stride, "C1": w.C1, "act0": w.act0, "act1": w.act1}
+    return {"N": w.N, "H": w.H, "W": w.W, "Cin": w.Cin, "Cout": w.Cout}
+
+
 def runner_for(w, dev):
     if isinstance(w, wl.GemmChain):
         return gemm_runner(w, dev)
@@ -451,12 +483,19 @@ def whole_job_value(flops_per_step, steps, sec, world):
     return world * flops_per_step * steps / sec / 1e12
 
 
+def workload_config(w, world):
+    par = f"replicas{world}" if world > 1 else "single-gpu"
+    if w is HEADLINE:
+        desc = (f"{w.name}: b2b GEMM {w.dtype} A[{w.M},{w.K0}] W0[{w.K0},{w.N0}] "
+                f"W1[{w.N0},{w.N1}], bias+{w.act0}/bias+{w.act1} (FFN-like chain, the largest "
+                f"point of its M sweep)")
+    else:
+        desc = w.name
+    return {"workload": desc, **shape_config(w), "dtype": w.dtype, "parallelism": par}
+
+
 def headline_config(world):
-    w = HEADLINE
-    return {"workload": f"{w.name}: b2b GEMM bf16 A[{w.M},{w.K0}] W0[{w.K0},{w.N0}] "
-                        f"W1[{w.N0},{w.N1}], bias+{w.act0}/bias+{w.act1}",
-            "M": w.M, "K0": w.K0, "N0": w.N0, "N1": w.N1, "dtype": w.dtype,
-            "parallelism": f"replicas{world}" if world > 1 else "single-gpu"}
+    return workload_config(HEADLINE, world)
 
 
 def run_ours(args):
@@ -504,22 +543,22 @@ def run_ours(args):
     t_roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.floor_bytes / (peaks["hbm_gbs"] * 1e9))
     t_unf = sec_unfused / unfused_steps if sec_unfused else None
     traffic = load_traffic(w.name)
+    roof = roofline_of(w, t_step, peaks)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; A ~ N(0,1), W ~ N(0, 1/K), b ~ U[-0.1, 0.1])",
-        "config": {**(headline_config(world) if w is HEADLINE else
-                      {"workload": w.name, "dtype": w.dtype,
-                       "parallelism": f"replicas{world}" if world > 1 else "single-gpu"}),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded; A ~ N(0,1) or U[-1,1], W ~ N(0, 1/K), b ~ U[-0.1, 0.1])",
+        "config": {**workload_config(w, world),
                    "l2": f"{nsets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB "
                          f"(> 2x L2) replayed in CUDA graphs"},
         "pct_of_roofline": round(100.0 * t_roof / t_step, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": w.floor_bytes,
+        "roofline": {**roof, "traffic": traffic, "algorithmic_bytes_per_launch": w.floor_bytes,
+                     "flops_per_launch": w.flops,
                      "kernel_source_sha": kernel_source_sha(),
                      "peak_source": peaks["source"],
+                     "hbm": {"achieved_gbs": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"],
+                             "frac": round(achieved_gbs / peaks["hbm_gbs"], 4)},
                      "tensor": {"achieved_tflops": round(tflops, 1), "peak": peaks["bf16_tflops"],
                                 "frac": round(tflops / peaks["bf16_tflops"], 4)}},
         "unfused": ({"ms_per_step": round(t_unf * 1e3, 6),
@@ -535,6 +574,7 @@ def run_ours(args):
         if not args.skip_cpu and isinstance(w, wl.GemmChain):
             line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
         if not args.headline_only:
+            line["sweep"] = ffn_sweep(dev, peaks, args.warmup)
             line["workloads"] = other_workloads(dev, peaks, max(args.steps // 8, 64), args.warmup)
         line["clocks"] = clocks.summary()
         print(json.dumps(line), flush=True)
@@ -553,8 +593,8 @@ def other_workloads(dev, peaks, steps, warmup):
         out[w.name] = {"us_per_step": round(s_f * 1e6, 3), "tflops": round(w.flops / s_f / 1e12, 1),
                        "pct_of_roofline": round(100 * t_roof / s_f, 1),
                        "hbm_gbs_algorithmic": round(w.floor_bytes / s_f / 1e9, 1),
-                       "bound": "tensor" if w.flops / (peaks["bf16_tflops"] * 1e12) >
-                                w.floor_bytes / (peaks["hbm_gbs"] * 1e9) else "hbm",
+                       "bound": roofline_of(w, s_f, peaks)["bound"], "dtype": w.dtype,
+                       "config": shape_config(w),
                        "unfused_us_per_step": round(s_u * 1e6, 3) if s_u else None,
                        "fused_speedup": round(s_u / s_f, 3) if s_u else None,
                        "floor_bytes": w.floor_bytes, "unfused_bytes": w.unfused_bytes}
@@ -564,6 +604,27 @@ def other_workloads(dev, peaks, steps, warmup):
     st, info = ops.get_device_error()
     if st != 0:
         raise RuntimeError(f"device error word: {st} {info}")
+    return out
+
+
+def ffn_sweep(dev, peaks, warmup):
+    """The FFN-like chain over its M sweep, fused and unfused, each point timed over about
+    the same span of device time (inputs rotating through sets larger than twice L2)."""
+    out = {}
+    for M in wl.FFN_SWEEP_M:
+        w = wl.GEMM_FFN.with_m(M)
+        fused, unfused, nsets, _ = runner_for(w, dev)
+        steps = max(32, min(1024, (1 << 22) // M))
+        s_f = time_steps(fused, steps, warmup, nsets, dev) / steps
+        s_u = time_steps(unfused, steps, warmup, nsets, dev) / steps
+        t_roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.floor_bytes / (peaks["hbm_gbs"] * 1e9))
+        out[str(M)] = {"us_per_step": round(s_f * 1e6, 3), "tflops": round(w.flops / s_f / 1e12, 1),
+                       "pct_of_roofline": round(100 * t_roof / s_f, 1),
+                       "roofline": roofline_of(w, s_f, peaks), "steps": steps,
+                       "unfused_us_per_step": round(s_u * 1e6, 3),
+                       "fused_speedup": round(s_u / s_f, 3)}
+        del fused, unfused
+        torch.cuda.empty_cache()
     return out
 
 
@@ -590,7 +651,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": headline_config(world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
@@ -609,8 +670,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", choices=sorted(wl.WORKLOADS), default=HEADLINE.name,
-                    help="workload of the timed line (default: the FFN-like chain); the "
-                         "others are for profiling single kernels")
+                    help="workload of the timed line (default: the FFN-like chain at its "
+                         "largest M); the others are for profiling single kernels")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -1446,8 +1446,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   ktrace(EV_SETUP_DONE, 0, 0);
 
-  // Global memory is touched only after the previous kernel of the stream has completed
-  // (inputs may be its outputs, outputs its inputs); the setup above overlaps its tail.
+  // Loads and stores of global memory wait for the previous kernel of the stream to
+  // complete (inputs may be its outputs, outputs its inputs): every role executes
+  // griddepcontrol.wait before its first one.  The L2 prefetches just below are issued
+  // BEFORE that wait.  They are hints that move no data into the CTA and write nothing:
+  // a line the previous kernel is still writing is kept coherent in L2 (the point where
+  // its stores land), so a prefetch at worst warms a line that is rewritten later, and
+  // the TMA loads issued after the wait read the final data.
   if (warp == 0) {
     // The first tile's A (and, if the plan asks, the second's) and (from one CTA) the
     // weights into L2 while the previous kernel finishes.

@@ -132,9 +132,27 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _common_device(**tensors) -> torch.device:
+    """The one device every given tensor (None skipped) lives on.  The library launches on
+    the current device and encodes its tensor maps over the pointers it is given, so an
+    operand on another device must be refused before anything is launched."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other operands on {dev}: "
+                             "all operands and the output must be on one device")
+    if dev is None:
+        raise ValueError("no tensor operand given")
+    return dev
+
+
+def _stream(stream, device=None) -> ctypes.c_void_p:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     if isinstance(stream, torch.cuda.Stream):
         return ctypes.c_void_p(stream.cuda_stream)
     return ctypes.c_void_p(int(stream))
@@ -164,8 +182,11 @@ def b2b_gemm(A, W0, b0, W1, b1, epi0="relu", epi1="relu", out=None, stream=None)
     if out is None:
         out = torch.empty((M, N1), dtype=dt, device=A.device)
     _check_tensor(out, "out", dt, (M, N1))
-    _raise(lib().b2b_gemm(_dtype_code(A), M, K0, N0, N1, _ptr(A), _ptr(W0), _ptr(b0), _epi(epi0),
-                          _ptr(W1), _ptr(b1), _epi(epi1), _ptr(out), _stream(stream)), "b2b_gemm")
+    dev = _common_device(A=A, W0=W0, b0=b0, W1=W1, b1=b1, out=out)
+    with torch.cuda.device(dev):
+        _raise(lib().b2b_gemm(_dtype_code(A), M, K0, N0, N1, _ptr(A), _ptr(W0), _ptr(b0),
+                              _epi(epi0), _ptr(W1), _ptr(b1), _epi(epi1), _ptr(out),
+                              _stream(stream, dev)), "b2b_gemm")
     return out
 
 
@@ -190,9 +211,11 @@ def b2b_gemm3(A, W0, b0, W1, b1, W2, b2, epi0="relu", epi1="relu", epi2="relu", 
     if out is None:
         out = torch.empty((M, N2), dtype=dt, device=A.device)
     _check_tensor(out, "out", dt, (M, N2))
-    _raise(lib().b2b_gemm3(_dtype_code(A), M, K0, N0, N1, N2, _ptr(A), _ptr(W0), _ptr(b0),
-                           _epi(epi0), _ptr(W1), _ptr(b1), _epi(epi1), _ptr(W2), _ptr(b2),
-                           _epi(epi2), _ptr(out), _stream(stream)), "b2b_gemm3")
+    dev = _common_device(A=A, W0=W0, b0=b0, W1=W1, b1=b1, W2=W2, b2=b2, out=out)
+    with torch.cuda.device(dev):
+        _raise(lib().b2b_gemm3(_dtype_code(A), M, K0, N0, N1, N2, _ptr(A), _ptr(W0), _ptr(b0),
+                               _epi(epi0), _ptr(W1), _ptr(b1), _epi(epi1), _ptr(W2), _ptr(b2),
+                               _epi(epi2), _ptr(out), _stream(stream, dev)), "b2b_gemm3")
     return out
 
 
@@ -225,15 +248,18 @@ def _b2b_conv(x, W0, b0, W1, b1, pad, stride, epi0, epi1, out, stream):
     if out is None:
         out = torch.empty((N, Ho, Wo, C1), dtype=dt, device=x.device)
     _check_tensor(out, "out", dt, (N, Ho, Wo, C1))
-    if stride == 1:
-        _raise(lib().b2b_conv_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(W0), C0, R, S, pad,
-                                   _ptr(b0), _epi(epi0), _ptr(W1), C1, _ptr(b1), _epi(epi1),
-                                   _ptr(out), _stream(stream)), "b2b_conv_nhwc")
-    else:
-        _raise(lib().b2b_conv_nhwc_strided(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(W0), C0, R, S,
-                                           pad, stride, _ptr(b0), _epi(epi0), _ptr(W1), C1,
-                                           _ptr(b1), _epi(epi1), _ptr(out), _stream(stream)),
-               "b2b_conv_nhwc_strided")
+    dev = _common_device(x=x, W0=W0, b0=b0, W1=W1, b1=b1, out=out)
+    with torch.cuda.device(dev):
+        if stride == 1:
+            _raise(lib().b2b_conv_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(W0), C0, R, S,
+                                       pad, _ptr(b0), _epi(epi0), _ptr(W1), C1, _ptr(b1),
+                                       _epi(epi1), _ptr(out), _stream(stream, dev)),
+                   "b2b_conv_nhwc")
+        else:
+            _raise(lib().b2b_conv_nhwc_strided(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(W0), C0,
+                                               R, S, pad, stride, _ptr(b0), _epi(epi0), _ptr(W1),
+                                               C1, _ptr(b1), _epi(epi1), _ptr(out),
+                                               _stream(stream, dev)), "b2b_conv_nhwc_strided")
     return out
 
 
@@ -250,8 +276,10 @@ def conv_relu_maxpool(x, Wt, b, out=None, stream=None):
     if out is None:
         out = torch.empty((N, H // 2, W // 2, Cout), dtype=dt, device=x.device)
     _check_tensor(out, "out", dt, (N, H // 2, W // 2, Cout))
-    _raise(lib().conv_relu_maxpool(_dtype_code(x), N, H, W, Cin, _ptr(x), _ptr(Wt), _ptr(b), Cout,
-                                   _ptr(out), _stream(stream)), "conv_relu_maxpool")
+    dev = _common_device(x=x, Wt=Wt, b=b, out=out)
+    with torch.cuda.device(dev):
+        _raise(lib().conv_relu_maxpool(_dtype_code(x), N, H, W, Cin, _ptr(x), _ptr(Wt), _ptr(b),
+                                       Cout, _ptr(out), _stream(stream, dev)), "conv_relu_maxpool")
     return out
 
 
@@ -271,8 +299,10 @@ def gemm_bias_act(A, W, b, epi="relu", out=None, stream=None):
     if out is None:
         out = torch.empty((M, N), dtype=dt, device=A.device)
     _check_tensor(out, "out", dt, (M, N))
-    _raise(lib().gemm_bias_act(_dtype_code(A), M, K, N, _ptr(A), _ptr(W), _ptr(b), _epi(epi),
-                               _ptr(out), _stream(stream)), "gemm_bias_act")
+    dev = _common_device(A=A, W=W, b=b, out=out)
+    with torch.cuda.device(dev):
+        _raise(lib().gemm_bias_act(_dtype_code(A), M, K, N, _ptr(A), _ptr(W), _ptr(b), _epi(epi),
+                                   _ptr(out), _stream(stream, dev)), "gemm_bias_act")
     return out
 
 
@@ -298,14 +328,17 @@ def _conv_single(x, Wt, b, pad, stride, epi, out, stream):
     if out is None:
         out = torch.empty((N, Ho, Wo, Co), dtype=dt, device=x.device)
     _check_tensor(out, "out", dt, (N, Ho, Wo, Co))
-    if stride == 1:
-        _raise(lib().conv_bias_act_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(Wt), Co, R, S,
-                                        pad, _ptr(b), _epi(epi), _ptr(out), _stream(stream)),
-               "conv_bias_act_nhwc")
-    else:
-        _raise(lib().conv_bias_act_nhwc_strided(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(Wt), Co,
-                                                R, S, pad, stride, _ptr(b), _epi(epi), _ptr(out),
-                                                _stream(stream)), "conv_bias_act_nhwc_strided")
+    dev = _common_device(x=x, Wt=Wt, b=b, out=out)
+    with torch.cuda.device(dev):
+        if stride == 1:
+            _raise(lib().conv_bias_act_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(Wt), Co, R,
+                                            S, pad, _ptr(b), _epi(epi), _ptr(out),
+                                            _stream(stream, dev)), "conv_bias_act_nhwc")
+        else:
+            _raise(lib().conv_bias_act_nhwc_strided(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(Wt),
+                                                    Co, R, S, pad, stride, _ptr(b), _epi(epi),
+                                                    _ptr(out), _stream(stream, dev)),
+                   "conv_bias_act_nhwc_strided")
     return out
 
 
@@ -327,10 +360,13 @@ def fold_batchnorm(W, b, gamma, beta, mean, var, eps=1e-5, out_inner=False, W_ou
     b_out = torch.empty((Co,), dtype=dt, device=W.device) if b_out is None else b_out
     _check_tensor(W_out, "W_out", dt, tuple(W.shape))
     _check_tensor(b_out, "b_out", dt, (Co,))
-    _raise(lib().b2b_fold_batchnorm(_dtype_code(W), Co, K, 1 if out_inner else 0, _ptr(W), _ptr(b),
-                                    _ptr(gamma), _ptr(beta), _ptr(mean), _ptr(var), float(eps),
-                                    _ptr(W_out), _ptr(b_out), _stream(stream)),
-           "b2b_fold_batchnorm")
+    dev = _common_device(W=W, b=b, gamma=gamma, beta=beta, mean=mean, var=var, W_out=W_out,
+                         b_out=b_out)
+    with torch.cuda.device(dev):
+        _raise(lib().b2b_fold_batchnorm(_dtype_code(W), Co, K, 1 if out_inner else 0, _ptr(W),
+                                        _ptr(b), _ptr(gamma), _ptr(beta), _ptr(mean), _ptr(var),
+                                        float(eps), _ptr(W_out), _ptr(b_out),
+                                        _stream(stream, dev)), "b2b_fold_batchnorm")
     return W_out, b_out
 
 
@@ -342,8 +378,10 @@ def maxpool2x2_nhwc(x, out=None, stream=None):
     if out is None:
         out = torch.empty((N, H // 2, W // 2, C), dtype=dt, device=x.device)
     _check_tensor(out, "out", dt, (N, H // 2, W // 2, C))
-    _raise(lib().maxpool2x2_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(out), _stream(stream)),
-           "maxpool2x2_nhwc")
+    dev = _common_device(x=x, out=out)
+    with torch.cuda.device(dev):
+        _raise(lib().maxpool2x2_nhwc(_dtype_code(x), N, H, W, C, _ptr(x), _ptr(out),
+                                     _stream(stream, dev)), "maxpool2x2_nhwc")
     return out
 
 

@@ -11,7 +11,8 @@ The five workloads stand in for the BERT / ResNet-50 operators that the BOLT not
 
   gemm_small  fp16 b2b GEMM A[1024,64] . W0[64,64] (+b0, ReLU) . W1[64,64] (+b1, ReLU)
   gemm_ffn    bf16 b2b GEMM A[32768,256] . W0[256,256] (+b0, Hardswish) . W1[256,128]
-              (+b1, Hardswish); the same shape is swept over M = 4096 .. 262144
+              (+b1, Hardswish); the same shape is swept over M = 4096 .. 262144, and
+              gemm_ffn_m262144 is its largest point
   conv1x1     fp16 two chained 1x1 convs on x[64,56,56,64], 64->64->64, ReLU/ReLU
   conv3x3_1x1 fp16 conv3x3 (pad 1) 64->64 + Hardswish, then conv1x1 64->128 + bias,
               on x[32,56,56,64]
@@ -188,9 +189,12 @@ GEMM_WIDE = GemmChain("gemm_wide", "bf16", 32768, 256, 512, 128, "hardswish", "h
 # A three-operator MLP head: 128 -> 128 -> 64 -> 64 over 32768 rows, bf16.
 MLP3 = GemmChain3("mlp3", "bf16", 32768, 128, 128, 64, 64, "hardswish", "hardswish", "none")
 
-WORKLOADS = {w.name: w for w in (GEMM_SMALL, GEMM_FFN, CONV1X1, CONV3X3_1X1, CONV_POOL,
-                                 CONV3X3S2_1X1, MLP3, GEMM_WIDE)}
 FFN_SWEEP_M = [4096, 8192, 16384, 32768, 65536, 131072, 262144]
+# The largest point of the FFN-like chain's M sweep: 2048 tiles, 13 or 14 per SM.
+GEMM_FFN_LARGE = GEMM_FFN.with_m(FFN_SWEEP_M[-1])
+
+WORKLOADS = {w.name: w for w in (GEMM_SMALL, GEMM_FFN, GEMM_FFN_LARGE, CONV1X1, CONV3X3_1X1,
+                                 CONV_POOL, CONV3X3S2_1X1, MLP3, GEMM_WIDE)}
 
 
 # ------------------------------------------------------------------------------------

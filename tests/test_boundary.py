@@ -181,3 +181,17 @@ def test_pad_channels_zero_fills():
     assert torch.equal(p[..., :5], t)
     assert torch.count_nonzero(p[..., 5:]) == 0
     assert ops.pad_channels(p, dim=2).shape == (2, 3, 8)
+
+
+def test_operands_on_different_devices_are_refused_before_any_launch():
+    # The library launches on the current device over the pointers it is given; the binding
+    # must refuse operands spread over two devices.  CPU and meta tensors stand in for two
+    # devices here (no GPU, and nothing is launched).
+    from gemm_conv_chains_gb300 import ops
+    a = torch.zeros(4)
+    b = torch.zeros(4, device="meta")
+    assert ops._common_device(A=a, W0=a, b0=None, out=a) == a.device
+    with pytest.raises(ValueError, match="one device"):
+        ops._common_device(A=a, W0=a, b0=None, out=b)
+    with pytest.raises(ValueError):
+        ops._common_device(A=None)

@@ -1,5 +1,6 @@
 """Launch choices on the GPU: every layout x grid x prefetch choice of a problem computes
-bit-identical results, and the profiler keeps a choice no slower than the default.
+bit-identical results, the default choice matches the CPU oracle at each problem's own
+shape (so every choice does), and the profiler keeps a choice no slower than the default.
 
 The choices change where tiles run and what sits where on chip, not the products or the
 roundings, so any difference is a layout or scheduling bug.  One thing may change: an
@@ -7,11 +8,15 @@ R x S conv with resident filters (halo loads) sums its taps column tap by column
 with streamed filters tap by tap, a different fp32 summation order; its cases use
 integer-valued inputs, whose sums are exact in any order.
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from gemm_conv_chains_gb300 import ops
 from gemm_conv_chains_gb300 import workloads as wl
+
+from gpu_util import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -29,31 +34,72 @@ def _gpu():
     ops.autotune_reset()
 
 
+def _rows(M):
+    """Rows the oracle checks: the first and last tiles and an even sample (all if small)."""
+    if M <= 4096:
+        return np.arange(M)
+    return np.unique(np.r_[0:128, M - 128:M, np.linspace(0, M - 1, 768).astype(int)])
+
+
 def _gemm(w, seed=5):
-    t = {k: (v.cuda() if v is not None else None) for k, v in wl.gemm_inputs(w, seed=seed).items()}
+    cpu = wl.gemm_inputs(w, seed=seed)
+    t = {k: (v.cuda() if v is not None else None) for k, v in cpu.items()}
     dims = (w.M, w.K0, w.N0, w.N1)
+    rows = _rows(w.M)
+
+    def check(out):
+        b = {k: wl.to_bits(v) for k, v in cpu.items()}
+        ref = oracle.b2b_gemm(w.dtype, b["A"][rows], b["W0"], b["b0"], b["W1"], b["b1"], w.act0,
+                              w.act1)
+        compare(w.dtype, wl.to_bits(out.cpu())[rows], ref, False, w.name)
+
     return "b2b_gemm", dims, lambda: ops.b2b_gemm(t["A"], t["W0"], t["b0"], t["W1"], t["b1"],
-                                                  w.act0, w.act1)
+                                                  w.act0, w.act1), check
 
 
 def _gemm3(w, seed=8):
-    t = {k: v.cuda() for k, v in wl.gemm3_inputs(w, seed=seed).items()}
+    cpu = wl.gemm3_inputs(w, seed=seed)
+    t = {k: v.cuda() for k, v in cpu.items()}
     dims = (w.M, w.K0, w.N0, w.N1, w.N2)
+    rows = _rows(w.M)
+
+    def check(out):
+        b = {k: wl.to_bits(v) for k, v in cpu.items()}
+        ref = oracle.b2b_gemm3(w.dtype, b["A"][rows], b["W0"], b["b0"], b["W1"], b["b1"], b["W2"],
+                               b["b2"], w.act0, w.act1, w.act2)
+        compare(w.dtype, wl.to_bits(out.cpu())[rows], ref, False, w.name)
+
     return "b2b_gemm3", dims, lambda: ops.b2b_gemm3(
-        *(t[k] for k in ("A", "W0", "b0", "W1", "b1", "W2", "b2")), w.act0, w.act1, w.act2)
+        *(t[k] for k in ("A", "W0", "b0", "W1", "b1", "W2", "b2")), w.act0, w.act1, w.act2), check
 
 
 def _conv(w, seed=6):
-    t = {k: v.cuda() for k, v in wl.conv_inputs(w, seed=seed, integer=w.R > 1).items()}
+    integer = w.R > 1
+    cpu = wl.conv_inputs(w, seed=seed, integer=integer)
+    t = {k: v.cuda() for k, v in cpu.items()}
     dims = (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1)
+
+    def check(out):
+        b = {k: wl.to_bits(v) for k, v in cpu.items()}
+        ref = oracle.b2b_conv_nhwc(w.dtype, b["x"], b["W0"], b["b0"], b["W1"], b["b1"], w.pad,
+                                   w.act0, w.act1)
+        compare(w.dtype, wl.to_bits(out.cpu()), ref, integer, w.name)
+
     return "b2b_conv_nhwc", dims, lambda: ops.b2b_conv_nhwc(
-        t["x"], t["W0"], t["b0"], t["W1"], t["b1"], pad=w.pad, epi0=w.act0, epi1=w.act1)
+        t["x"], t["W0"], t["b0"], t["W1"], t["b1"], pad=w.pad, epi0=w.act0, epi1=w.act1), check
 
 
 def _pool(w, seed=7):
-    t = {k: v.cuda() for k, v in wl.pool_inputs(w, seed=seed, integer=True).items()}
+    cpu = wl.pool_inputs(w, seed=seed, integer=True)
+    t = {k: v.cuda() for k, v in cpu.items()}
     dims = (w.N, w.H, w.W, w.Cin, w.Cout)
-    return "conv_relu_maxpool", dims, lambda: ops.conv_relu_maxpool(t["x"], t["Wt"], t["b"])
+
+    def check(out):
+        ref = oracle.conv_relu_maxpool(w.dtype, wl.to_bits(cpu["x"]), wl.to_bits(cpu["Wt"]),
+                                       wl.to_bits(cpu["b"]))
+        compare(w.dtype, wl.to_bits(out.cpu()), ref, True, w.name)
+
+    return "conv_relu_maxpool", dims, lambda: ops.conv_relu_maxpool(t["x"], t["Wt"], t["b"]), check
 
 
 PROBLEMS = {
@@ -76,8 +122,10 @@ PROBLEMS = {
 
 @pytest.mark.parametrize("name", sorted(PROBLEMS))
 def test_every_choice_is_bit_identical(name):
-    kind, dims, call = PROBLEMS[name]()
+    kind, dims, call, check = PROBLEMS[name]()
     ref = call().clone()
+    torch.cuda.synchronize()
+    check(ref)                        # the default matches the oracle, so every choice must
     n = ops.debug_plan(kind, dims)["ncand"]
     for cand in range(n):
         for grid in (0, 1, 2):
@@ -92,7 +140,7 @@ def test_every_choice_is_bit_identical(name):
 
 
 def test_profiler_keeps_the_fastest_choice():
-    kind, dims, call = PROBLEMS["ffn"]()
+    kind, dims, call, _ = PROBLEMS["ffn"]()
     ref = call().clone()
     ops.set_autotune(True)
     out = call()                      # times every choice, then runs the fastest
@@ -117,7 +165,7 @@ def test_profiler_keeps_the_fastest_choice():
 
 
 def test_profiler_does_not_time_inside_graph_capture():
-    kind, dims, call = PROBLEMS["small"]()
+    kind, dims, call, _ = PROBLEMS["small"]()
     ref = call().clone()
     ops.set_autotune(True)
     stream = torch.cuda.Stream()

@@ -215,6 +215,35 @@ def test_b2b_equals_two_stages(oracle_mod):
     assert np.array_equal(y, y2)
 
 
+def test_b2b_past_the_first_row_block(oracle_mod):
+    # The oracle forms the intermediate 4096 rows at a time.  M = 4096 + 300 reaches a
+    # second, partial block, checked three independent ways: numpy's int64 matmul with
+    # numpy's own fp16 rounding (integer data: h = relu(A W0 + b0) <= 98 is exact in fp16,
+    # y = relu(h W1 + b1) <= 7842 is rounded once, by numpy); the rows of the second block
+    # run on their own (rows are independent, so a slip in the block offset shows); and two
+    # separate stages.  Distinct K0, N0, N1 catch a transposed operand.
+    rng = np.random.default_rng(11)
+    M, K0, N0, N1 = 4096 + 300, 24, 40, 16
+    A = rng.integers(-2, 3, (M, K0))
+    W0 = rng.integers(-2, 3, (K0, N0))
+    b0 = rng.integers(-2, 3, (N0,))
+    W1 = rng.integers(-2, 3, (N0, N1))
+    b1 = rng.integers(-2, 3, (N1,))
+    h = np.maximum(A @ W0 + b0, 0)
+    assert np.abs(h).max() <= 2048                        # exact in fp16
+    ref = np.maximum(h @ W1 + b1, 0).astype(np.float64).astype(np.float16).view(np.uint16)
+    y = oracle_mod.b2b_gemm("f16", f16_bits(A), f16_bits(W0), f16_bits(b0), f16_bits(W1),
+                            f16_bits(b1), "relu", "relu")
+    assert y.shape == (M, N1)
+    assert np.array_equal(y, ref)
+    tail = oracle_mod.b2b_gemm("f16", f16_bits(A[4096:]), f16_bits(W0), f16_bits(b0),
+                               f16_bits(W1), f16_bits(b1), "relu", "relu")
+    assert np.array_equal(y[4096:], tail)
+    h16 = oracle_mod.gemm_bias_act("f16", f16_bits(A), f16_bits(W0), f16_bits(b0), "relu")
+    y2 = oracle_mod.gemm_bias_act("f16", h16, f16_bits(W1), f16_bits(b1), "relu")
+    assert np.array_equal(y, y2)
+
+
 # ------------------------------------------------------------------------------------
 # convolution
 # ------------------------------------------------------------------------------------

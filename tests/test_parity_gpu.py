@@ -90,6 +90,21 @@ def test_b2b_gemm_ffn_workload_sampled_rows():
     run_b2b_gemm(w, seed=0, rows=rows)
 
 
+@pytest.mark.parametrize("M", wl.FFN_SWEEP_M)
+def test_b2b_gemm_ffn_sweep_sampled_rows(M):
+    # The FFN-like chain over the M sweep 4096 .. 262144 (32 .. 2048 tiles; at 262144 every
+    # CTA runs 13 or 14 tiles), in the benchmark's launch configuration.  The oracle checks
+    # every tile of CTA 0 (tiles 0, G, 2G, ... for a grid of G CTAs), the last tile and a
+    # random sample of rows.
+    w = wl.GEMM_FFN.with_m(M)
+    tiles = (M + 127) // 128
+    grid = min(tiles, ops.num_sms())
+    rng = np.random.default_rng(M)
+    cta0 = np.concatenate([np.arange(128 * t, min(128 * t + 128, M)) for t in range(0, tiles, grid)])
+    rows = np.unique(np.concatenate([cta0, np.arange(M - 128, M), rng.choice(M, 512, replace=False)]))
+    run_b2b_gemm(w, seed=M + 7, rows=rows)
+
+
 @pytest.mark.parametrize("integer", [True, False])
 def test_b2b_gemm_narrow_four_buffers_sampled_rows(integer):
     # 64 -> 64 -> 64 keeps four tiles in flight (each epilogue group one tile ahead); with
