@@ -38,6 +38,10 @@ struct DeviceState {
   uint32_t* err = nullptr;                    // device address of g_error_word
   cudaError_t init_error = cudaSuccess;
   std::atomic<uint64_t> attr_done{0};   // bit 2 (v + V_COUNT traced) + bf16: smem attribute set
+  // CTA-pair kernel: resident clusters of two (per bf16 + 2 * traced), for the dynamic
+  // shared memory size they were computed for; 0 = not yet known
+  std::atomic<int> cta2_clusters[4] = {0, 0, 0, 0};
+  std::atomic<size_t> cta2_smem[4] = {0, 0, 0, 0};
 };
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
@@ -277,7 +281,10 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   // memory; else two tiles in flight with P in TMEM (wide N0, where two P tiles and two
   // accumulator pairs do not fit); else one tile at a time.
   // dual: chain accumulator / P buffers (1, 2 or 4); single/pool always have two.
-  struct Cand { int dual, groups, resident, alias, p_tmem; };
+  // w0res: P in TMEM with W0 alone resident (row-major weights, at most kMaxW0Chunks K
+  // chunks): the ring carries A and W1 chunks and the output goes from registers straight
+  // to global memory, so the plan has no output staging.
+  struct Cand { int dual, groups, resident, alias, p_tmem, w0res = 0; };
   Cand cands[16];
   int ncand = 0;
   if (mode == MODE_CHAIN) {
@@ -296,8 +303,11 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
       if (tmem_dual_ok)
         for (int resident = 1; resident >= 0; --resident)
           for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {2, 2, resident, alias, 0};
-      if (tmem_p_ok)
-        for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {2, 2, resident, 0, 1};
+      if (tmem_p_ok) {
+        cands[ncand++] = {2, 2, 1, 0, 1};
+        cands[ncand++] = {2, 2, 0, 0, 1};
+        if (w0mn && w1mn && p.kchunks0 <= kMaxW0Chunks) cands[ncand++] = {2, 2, 0, 0, 1, 1};
+      }
       for (int resident = 1; resident >= 0; --resident)
         for (int alias = 0; alias <= 1; ++alias) cands[ncand++] = {1, 1, resident, alias, 0};
     }
@@ -321,12 +331,15 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
                                    : kABytes;
       const uint32_t stage_bytes =
           k.resident ? a_bytes
+          : k.w0res  ? round_up(std::max(kABytes, p.w1_chunk_bytes), 1024u)
                      : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
       const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? static_cast<uint32_t>(k.dual) : 0u;
-      const uint32_t obufs = k.groups == 2 ? 2u : 1u;
+      const uint32_t obufs = k.w0res ? 0u : (k.groups == 2 ? 2u : 1u);
       const uint32_t shared = k.alias ? pbufs * std::max(p_bytes, out_bytes)
                                       : pbufs * p_bytes + obufs * out_bytes;
-      const uint32_t fixed = (k.resident ? w_res : 0u) + shared + bias_bytes + bar_bytes;
+      const uint32_t w0_res_bytes = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
+      const uint32_t fixed =
+          (k.resident ? w_res : k.w0res ? w0_res_bytes : 0u) + shared + bias_bytes + bar_bytes;
       if (fixed >= budget) continue;
       const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / stage_bytes);
       if (stages < 2u) continue;
@@ -351,6 +364,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.nbuf_log2 = mode != MODE_CHAIN ? 1 : (k.dual == 4 ? 2 : (k.dual == 2 ? 1 : 0));
   p.epi_groups = k.groups;
   p.resident = k.resident;
+  p.w0_res = k.w0res;
   p.out_alias_p = k.alias;
   p.p_tmem = k.p_tmem;
   p.num_stages = chosen_stages;
@@ -379,13 +393,13 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   r.cand = pick;
   r.ncand = nfeas;
   r.ring = p.num_stages * p.stage_bytes;
-  r.w_res = p.resident ? w_res : 0u;
+  r.w_res = p.resident ? w_res : (k.w0res ? static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes : 0u);
   const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? static_cast<uint32_t>(k.dual) : 0u;
   r.p_each = pbufs ? (p.out_alias_p ? std::max(p_bytes, out_bytes) : p_bytes) : 0u;
-  r.out_each = p.out_alias_p ? 0u : out_bytes;
+  r.out_each = (p.out_alias_p || k.w0res) ? 0u : out_bytes;
   r.bias = bias_bytes;
   r.bar = bar_bytes;
-  const uint32_t obufs = k.groups == 2 ? 2u : 1u;
+  const uint32_t obufs = k.w0res ? 0u : (k.groups == 2 ? 2u : 1u);
   uint32_t off = 0;
   p.off_ring = off;
   off += r.ring;
@@ -396,6 +410,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   off += pbufs * r.p_each;
   for (uint32_t b = 0; b < 2; ++b) {
     if (p.out_alias_p) p.off_out[b] = p.off_p[b];
+    else if (obufs == 0u) p.off_out[b] = 0u;   // no staging (never read)
     else p.off_out[b] = off + (b < obufs ? b : 0u) * r.out_each;
   }
   if (!p.out_alias_p) off += obufs * r.out_each;
@@ -410,7 +425,7 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   // GEMM0 chunk).  The extra stages are counted here and taken at launch when the grid
   // gives no CTA a third tile, provided that W1's stages of the pair miss them.
   r.extend = 0;
-  if (mode == MODE_CHAIN && k.p_tmem && !k.resident && p.w1_group &&
+  if (mode == MODE_CHAIN && k.p_tmem && !k.resident && !k.w0res && p.w1_group &&
       p.off_out[0] == p.off_ring + r.ring) {
     const uint32_t span = r.ring + obufs * r.out_each;
     const uint32_t total = std::min<uint32_t>(kMaxStages, span / p.stage_bytes);
@@ -497,6 +512,77 @@ bool plan_smem_chain3(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   return *smem_bytes <= kSmemLimit;
 }
 
+// Row tiles (128 rows) from which a chain that fits the CTA-pair kernel runs over CTA
+// pairs by default.
+constexpr int32_t kCta2MinTiles = 512;
+
+// The CTA-pair plan of a b2b GEMM chain with row-major weights (chain_cta2_kernel.cuh): per
+// CTA a ring of 16 KiB A chunks, its halves of W0 and W1 resident (N0 / 2 and N1 / 2
+// columns), the bias operands of its halves and the barriers (no output staging: the
+// epilogue stores the output from registers); in TMEM the tile-pair layout with P kept over GEMM0's
+// columns.  p.num_tiles becomes the number of 256-row tiles.
+// False when the chain is outside the kernel's limits (N0 or N1 not a multiple of 128,
+// more than kMaxW0Chunks K chunks, the TMEM layout over 512 columns, fewer than three ring
+// stages beside the weights).
+bool plan_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
+  if (p.N0p % 128 != 0 || p.N1p % 128 != 0 || p.N0p > 256 || p.N1p > 256) return false;
+  if (p.kchunks0 > kMaxW0Chunks || p.kchunks0 < 1) return false;
+  const uint32_t budget = kSmemLimit - 1024u;
+  const uint32_t nb0 = static_cast<uint32_t>(p.N0p / 128), nb1 = static_cast<uint32_t>(p.N1p / 128);
+  p.w0_chunk_bytes = nb0 * 8192u;
+  p.w1_chunk_bytes = nb1 * 8192u;
+  const uint32_t w0b = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
+  const uint32_t w1b = static_cast<uint32_t>(p.kchunks1) * p.w1_chunk_bytes;
+  const uint32_t bias_bytes = kOnesBytes + kBiasBlockBytes * (nb0 + nb1);
+  const uint32_t bar_bytes = 1024u;
+  const uint32_t fixed = w0b + w1b + bias_bytes + bar_bytes;
+  if (fixed >= budget) return false;
+  const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / kABytes);
+  if (stages < 3u) return false;
+  p.tmem_cols = tmem_layout(p, MODE_CHAIN, 2u, true);
+  if (p.tmem_cols > 512u) return false;
+  p.cta_pair = 1;
+  p.num_tiles = ceil_div(p.M, 2 * kBlockM);
+  p.acc_dual = 1;
+  p.nbuf_log2 = 1;
+  p.epi_groups = 2;
+  p.resident = 1;
+  p.w0_res = 0;
+  p.out_alias_p = 0;
+  p.p_tmem = 1;
+  p.halo = 0;
+  p.num_stages = stages;
+  p.stage_bytes = kABytes;
+  p.a_stage_bytes = kABytes;
+  p.kstages0 = p.kchunks0;
+  p.w1_group = 0;
+  p.w1_per_stage = 1;
+  uint32_t off = 0;
+  p.off_ring = off;
+  off += stages * kABytes;
+  p.off_w0 = off;
+  p.off_w1 = off + w0b;
+  off += w0b + w1b;
+  for (uint32_t b = 0; b < kMaxBufs; ++b) p.off_p[b] = 0;
+  p.off_out[0] = p.off_out[1] = 0;   // no staging: the output leaves from registers
+  p.off_bias = off;
+  off += bias_bytes;
+  p.off_bar = off;
+  off += bar_bytes;
+  if (regions) {
+    Regions r;
+    r.ring = stages * kABytes;
+    r.w_res = w0b + w1b;
+    r.p_each = 0;
+    r.out_each = 0;
+    r.bias = bias_bytes;
+    r.bar = bar_bytes;
+    *regions = r;
+  }
+  *smem_bytes = off + 1024u;
+  return *smem_bytes <= kSmemLimit;
+}
+
 void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const void* b1,
                  DeviceState* d, uint32_t kid) {
   p.is_bf16 = dt == B2B_BF16 ? 1 : 0;
@@ -513,14 +599,12 @@ void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const v
   p.trace_cta = g_trace_cta;
 }
 
-b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtensorMap& w0,
-                  const CUtensorMap& w1, const CUtensorMap& out, ChainParams& p, size_t smem,
-                  int grid, void* stream) {
-  const bool traced = p.trace != nullptr;
+// Lets the kernel of variant v (the launch's dtype and build) use the full shared memory.
+b2b_status ensure_smem_attribute(Variant v, DeviceState* d, bool bf16, bool traced) {
   const uint64_t bit = 1ull << (2u * (static_cast<uint32_t>(v) + (traced ? V_COUNT : 0u)) +
-                                (p.is_bf16 ? 1u : 0u));
+                                (bf16 ? 1u : 0u));
   if ((d->attr_done.load() & bit) == 0u) {
-    if (cudaFuncSetAttribute(variant_func(v, p.is_bf16 != 0, traced),
+    if (cudaFuncSetAttribute(variant_func(v, bf16, traced),
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemLimit)) != cudaSuccess) {
       cudaGetLastError();
@@ -528,6 +612,15 @@ b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtenso
     }
     d->attr_done.fetch_or(bit);
   }
+  return B2B_OK;
+}
+
+b2b_status launch(Variant v, DeviceState* d, const CUtensorMap& a, const CUtensorMap& w0,
+                  const CUtensorMap& w1, const CUtensorMap& out, ChainParams& p, size_t smem,
+                  int grid, void* stream) {
+  const bool traced = p.trace != nullptr;
+  if (b2b_status st = ensure_smem_attribute(v, d, p.is_bf16 != 0, traced); st != B2B_OK)
+    return st;
   const cudaError_t e =
       launch_variant(v, a, w0, w1, out, p, grid, smem, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
@@ -555,6 +648,35 @@ bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int
   p.kchunks1 = mode == MODE_CHAIN ? ceil_div(p.N0p, kChunkK) : 0;
   p.num_tiles = ceil_div(M, kBlockM);
   p.stride = 1;
+  // A chain with row-major weights may also run over CTA pairs: that plan is one more
+  // feasible layout, after the single-CTA ones, and the default from kCta2MinTiles
+  // 128-row tiles on (measured on the FFN-like chain: 16.7 against 17.8 us at 512 tiles,
+  // 44.6 against 53.0 us at 2048, but 9.8 against 9.3 us at 256 tiles, where the pairs'
+  // longer start -- both weight halves before the first MMA -- is not yet amortised).
+  if (mode == MODE_CHAIN && w_mn) {
+    ChainParams q = p;
+    size_t qs = 0;
+    Regions qr;
+    const bool single_ok = plan_smem(q, mode, true, true, &qs, &qr, -1);
+    const int nsingle = single_ok ? qr.ncand : 0;
+    ChainParams c = p;
+    size_t cs = 0;
+    Regions cr;
+    const bool pair_ok = plan_cta2(c, &cs, &cr);
+    if (pair_ok && (forced == nsingle || (forced < 0 && p.num_tiles >= kCta2MinTiles))) {
+      p = c;
+      *smem = cs;
+      if (regions) {
+        *regions = cr;
+        regions->cand = nsingle;
+        regions->ncand = nsingle + 1;
+      }
+      return true;
+    }
+    const bool ok = plan_smem(p, mode, w_mn, w_mn, smem, regions, forced);
+    if (ok && pair_ok && regions) regions->ncand += 1;
+    return ok;
+  }
   return plan_smem(p, mode, w_mn, w_mn, smem, regions, forced);
 }
 
@@ -656,6 +778,52 @@ int32_t pf_second_for(int32_t tiles, int grid, int32_t pf2) {
 // ------------------------------------------------------------------------------------
 // GEMM-shaped entry points (2-D A operand)
 // ------------------------------------------------------------------------------------
+// The b2b GEMM chain over CTA pairs (plan_cta2): clusters of two CTAs, at most as many as
+// can be resident at once; grid choices as for single CTAs, counted in pairs.
+b2b_status run_cta2(const Choice& ch, Info* info, const Regions& r, ChainParams& p, size_t smem,
+                    DeviceState* d, int dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
+                    const void* A, const void* W0, const void* b0, int e0, const void* W1,
+                    const void* b1, int e1, void* D, void* stream) {
+  fill_common(p, dt, e0, e1, b0, b1, d, KID_GEMM_CHAIN_CTA2);
+  const bool traced = p.trace != nullptr;
+  if (b2b_status st = ensure_smem_attribute(V_GEMM_CHAIN_CTA2, d, p.is_bf16 != 0, traced);
+      st != B2B_OK)
+    return st;
+  const int ci = (p.is_bf16 ? 1 : 0) + (traced ? 2 : 0);
+  int clusters = d->cta2_clusters[ci].load();
+  if (clusters <= 0 || d->cta2_smem[ci].load() != smem) {
+    if (cta2_max_clusters(p.is_bf16 != 0, traced, smem, &clusters) != cudaSuccess || clusters < 1) {
+      cudaGetLastError();
+      return B2B_ERR_CUDA;
+    }
+    d->cta2_clusters[ci].store(clusters);
+    d->cta2_smem[ci].store(smem);
+  }
+  const int pairs = grid_for(p.num_tiles, clusters, ch.grid);
+  p.pf_second = 0;
+  if (info) *info = info_for(r.ncand, p.num_tiles, clusters, true);
+  const uint64_t e = 2;
+  CUtensorMap ta, tw0, tw1;
+  bool ok = make_map(&ta, A, p.is_bf16, 2, {static_cast<uint64_t>(K0), static_cast<uint64_t>(M)},
+                     {K0 * e}, {kChunkK, kBlockM});
+  // [N/64][rows][64] views of the row-major weights; each CTA loads its half of the
+  // 64-wide blocks of every K chunk in one box
+  ok = ok && make_map(&tw0, W0, p.is_bf16, 3,
+                      {64, static_cast<uint64_t>(K0), static_cast<uint64_t>(N0 / 64)}, {N0 * e, 128},
+                      {64, 64, static_cast<uint32_t>(p.N0p / 128)});
+  ok = ok && make_map(&tw1, W1, p.is_bf16, 3,
+                      {64, static_cast<uint64_t>(N0), static_cast<uint64_t>(N1 / 64)}, {N1 * e, 128},
+                      {64, 64, static_cast<uint32_t>(p.N1p / 128)});
+  if (!ok) return B2B_ERR_CUDA;
+  p.pf_a = static_cast<const uint8_t*>(A);
+  p.pf_a_bytes = static_cast<uint64_t>(M) * K0 * e;
+  p.pf_a_tile_bytes = static_cast<uint32_t>(kBlockM * K0 * e);
+  p.out_ptr = static_cast<uint8_t*>(D);
+  p.out_ld = N1;
+  // (no output map: the output leaves from registers)
+  return launch(V_GEMM_CHAIN_CTA2, d, ta, tw0, tw1, ta, p, smem, 2 * pairs, stream);
+}
+
 b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int dt, int64_t M,
                          int32_t K0, int32_t N0, int32_t N1, const void* A, const void* W0,
                          const void* b0, int e0, const void* W1, const void* b1, int e1, void* D,
@@ -667,6 +835,9 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   b2b_status st = B2B_OK;
   DeviceState* d = device_state(&st);
   if (d == nullptr) return st;
+  if (p.cta_pair)
+    return run_cta2(ch, info, r, p, smem, d, dt, M, K0, N0, N1, A, W0, b0, e0, W1, b1, e1, D,
+                    stream);
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = pf_second_for(p.num_tiles, grid, ch.pf2);
@@ -724,11 +895,14 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   p.pf_w0_bytes = static_cast<uint32_t>(static_cast<uint64_t>(K0) * N0 * e);
   p.pf_w1 = static_cast<const uint8_t*>(W1);
   p.pf_w1_bytes = mode == MODE_CHAIN ? static_cast<uint32_t>(static_cast<uint64_t>(N0) * N1 * e) : 0u;
+  p.out_ptr = static_cast<uint8_t*>(D);
+  p.out_ld = Nout;
   Variant v;
   if (mode == MODE_CHAIN)
     v = !w_mn ? (p.p_tmem ? V_CONV1X1_CHAIN : V_CONV1X1_CHAIN_NP)
               : (p.p_split  ? V_GEMM_CHAIN_WIDE
                  : !p.p_tmem ? V_GEMM_CHAIN_NP
+                 : p.w0_res  ? V_GEMM_CHAIN_PAIR_W0
                              : (!p.resident ? V_GEMM_CHAIN_PAIR : V_GEMM_CHAIN));
   else v = w_mn ? V_GEMM_SINGLE : V_CONV1X1_SINGLE;
   return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
@@ -1360,7 +1534,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   b2b_status st = check_plan_args(kind, dims, ndims);
   if (st != B2B_OK) return st;
   if (out == nullptr) return B2B_ERR_NULL;
-  if (out_len < 58) return B2B_ERR_SHAPE;
+  if (out_len < 60) return B2B_ERR_SHAPE;
   Choice c;
   find_choice(plan_key(kind, dims, ndims), &c);
   ChainParams p;
@@ -1368,7 +1542,7 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
   if ((st = plan_for_kind(kind, dims, ndims, c.cand, p, r, smem, mode)) != B2B_OK) return st;
-  const uint32_t v[58] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[60] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -1384,7 +1558,8 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
                           p.d1_col[2], p.d1_col[3], static_cast<uint32_t>(r.cand),
                           static_cast<uint32_t>(r.ncand), static_cast<uint32_t>(c.grid),
                           static_cast<uint32_t>(c.pf2), r.extend, p.off_w2, p.off_p1[0],
-                          p.off_p1[1], p.d2_col[0], p.d2_col[1], p.p_split};
+                          p.off_p1[1], p.d2_col[0], p.d2_col[1], p.p_split,
+                          static_cast<uint32_t>(p.w0_res), static_cast<uint32_t>(p.cta_pair)};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

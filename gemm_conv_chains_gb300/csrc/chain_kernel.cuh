@@ -85,9 +85,11 @@ enum : uint32_t {
   BAR_D2_FULL0 = BAR_P1_FULL0 + kMaxBufs,   // three-operator chain: GEMM2 accumulator ready
   BAR_MMA_DONE = BAR_D2_FULL0 + kMaxBufs,
   BAR_BIAS_READY = BAR_MMA_DONE + 1,
-  BAR_COUNT = BAR_BIAS_READY + 1,
+  BAR_W0C0 = BAR_BIAS_READY + 1,            // resident W0 beside streamed W1: one per K chunk
+  BAR_COUNT = BAR_W0C0 + kMaxW0Chunks,
 };
 constexpr uint32_t kBarRegionBytes = 512;   // barriers, then TMEM slot and abort flag
+static_assert(8u * BAR_COUNT + 8u <= kBarRegionBytes, "barrier region too small");
 
 struct TileCoord {
   int32_t m0;              // 2-D: first row
@@ -272,12 +274,14 @@ __device__ __forceinline__ void prefetch_a_tile(const ChainParams& p, int32_t t)
   bulk_prefetch_l2(p.pf_a + off, static_cast<uint32_t>(n));
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool WIDE, bool PAIR, bool NOPAIR>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool WIDE, bool PAIR, bool NOPAIR, bool W0RES>
 __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
                               const CUtensorMap* tmW0, const CUtensorMap* tmW1, uint32_t base,
                               uint32_t bars, volatile uint32_t* abort_flag) {
-  // Tile-pair instantiations are launched with streamed weights only.
+  // Tile-pair instantiations are launched with streamed weights only, or (W0RES) with W0
+  // alone resident: then the ring carries A chunks and W1 chunks.
   const bool resident = !PAIR && p.resident != 0;
+  const bool stream_w0 = !resident && !W0RES;
   const uint32_t lead = elect_one();
   const uint64_t pol_stream = l2_policy_evict_first();
   const uint64_t pol_keep = l2_policy_evict_last();
@@ -286,6 +290,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
   trace(EV_PROD_START, 0, 0);
   uint32_t issued = 0, issued_parity = 0;   // per-stage: a fill in flight, and its parity
   bool w_issued = false;
+  uint32_t w0_issued = 0;                   // W0RES: resident W0 chunks requested
   bool ok = true;
 
   if (resident) {
@@ -321,13 +326,22 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     const TileCoord tc = tile_coord<A4D>(p, t);
     KPos k;
     for (int kc = 0; kc < p.kstages0; ++kc) {
+      if (W0RES && it == 0) {
+        // The resident W0, chunk by chunk beside the CTA's first tile, so that its first
+        // MMAs wait for one chunk, not for the whole matrix.
+        const uint32_t wb = bars + 8u * (BAR_W0C0 + kc);
+        mbar_arrive_expect_tx_if(lead, wb, p.w0_chunk_bytes);
+        load_w0_chunk<A4D, W0MN>(lead, p, tmW0, base + p.off_w0 + kc * p.w0_chunk_bytes, k, wb,
+                                 pol_keep);
+        w0_issued |= 1u << kc;
+      }
       if (!acquire(t)) return false;
       trace(EV_PROD_ACQUIRE, kc, it);
       const uint32_t fb = bars + 8u * (BAR_FULL0 + stage);
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
-      mbar_arrive_expect_tx_if(lead, fb, p.a_stage_bytes + (resident ? 0u : p.w0_chunk_bytes));
+      mbar_arrive_expect_tx_if(lead, fb, p.a_stage_bytes + (stream_w0 ? p.w0_chunk_bytes : 0u));
       load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, k, fb, pol_stream);
-      if (!resident)
+      if (stream_w0)
         load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, k, fb, pol_keep);
       if (A4D && p.halo) k.next_halo(p); else k.next(p);
       // Tile it + 2's A into L2 behind this tile's first chunk (tile 0, and tile 1 when
@@ -445,6 +459,10 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     if (w_issued)
       (void)mbar_wait(bars + 8u * BAR_WFULL, 0u, drain_ns, nullptr, p.err, p.kernel_id,
                       SITE_PRODUCER_DRAIN, 0);
+    for (uint32_t c = 0; c < static_cast<uint32_t>(kMaxW0Chunks); ++c)
+      if (w0_issued & (1u << c))
+        (void)mbar_wait(bars + 8u * (BAR_W0C0 + c), 0u, drain_ns, nullptr, p.err, p.kernel_id,
+                        SITE_PRODUCER_DRAIN, 0);
   }
 }
 
@@ -484,7 +502,8 @@ __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32
                (first && ks == 0) ? 0u : 1u);
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE, bool PAIR, bool NOPAIR>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE, bool PAIR, bool NOPAIR,
+          bool W0RES>
 __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
                          volatile uint32_t* abort_flag) {
   const bool resident = !PAIR && p.resident != 0;   // (as in the producer)
@@ -593,8 +612,14 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         }
         if (++cb == p.kc_per_tap) { cb = 0; ++s_tap; }
       } else {
-        const uint64_t bdesc = resident ? res_w0 + static_cast<uint64_t>(kc) * w0_step
-                                          : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
+        if (W0RES && it == 0) {
+          // the resident W0's chunk kc has landed (once per CTA; TMA data, no tcgen05 order)
+          if (!warp_mbar_wait(bars + 8u * (BAR_W0C0 + kc), 0u, p, abort_flag, SITE_MMA_WEIGHTS, t))
+            return false;
+        }
+        const uint64_t bdesc = (resident || W0RES)
+                                   ? res_w0 + static_cast<uint64_t>(kc) * w0_step
+                                   : ring_w0 + static_cast<uint64_t>(stage) * stage_step;
         if (++cb == p.kc_per_tap) cb = 0;
         issue_chunk<W0MN>(lead, d0, adesc, bdesc, idesc0, nks, kc == 0);
       }
@@ -1001,6 +1026,224 @@ __device__ __forceinline__ void drain_to_tmem(int act, uint32_t tm_lane, uint32_
     drain_to_tmem_act<BF16, 0>(tm_lane, col0, ncols, p_col0);
 }
 
+// 16 converted columns (8 packed pairs) to global memory at `dst`, 16 bytes at a time;
+// `n` = the columns left in the row (units at or past the row's end are not stored).
+__device__ __forceinline__ void st_global_cols16(uint8_t* dst, const uint32_t (&v)[8], int n) {
+  if (n >= 8)
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3])
+                 : "memory");
+  if (n >= 16)
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16), "r"(v[4]),
+                 "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// Accumulator columns [col0, col0 + ncols) of this thread's row -> act -> dtype -> the
+// row in global memory (`dst` = its first element), with no staging tile.  Columns at or
+// past `nvalid` (the output's width, a multiple of 8) and a row outside the output
+// (`row_ok` false: the last tile's rows past M) are not stored.  The TMEM loads are
+// warp-collective, so every lane runs the loop.
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain_to_global_act(uint32_t tm_lane, uint32_t col0, int ncols,
+                                                    uint8_t* dst, int nvalid, bool row_ok) {
+  for (int c = 0; c < ncols; c += 32) {
+    const bool two = c + 16 < ncols;
+    uint32_t a[16], b[16], v[8];
+    tmem_ld32(tm_lane + col0 + c, two, a, b);
+    tmem_wait_ld(a, b);
+    if (row_ok) {
+      convert16<BF16, ACT>(a, v);
+      st_global_cols16(dst + 2 * c, v, nvalid - c);
+      if (two) {
+        convert16<BF16, ACT>(b, v);
+        st_global_cols16(dst + 2 * (c + 16), v, nvalid - c - 16);
+      }
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void drain_to_global(int act, uint32_t tm_lane, uint32_t col0,
+                                                int ncols, uint8_t* dst, int nvalid, bool row_ok) {
+  if (act == 2)
+    drain_to_global_act<BF16, 2>(tm_lane, col0, ncols, dst, nvalid, row_ok);
+  else if (act == 1)
+    drain_to_global_act<BF16, 1>(tm_lane, col0, ncols, dst, nvalid, row_ok);
+  else
+    drain_to_global_act<BF16, 0>(tm_lane, col0, ncols, dst, nvalid, row_ok);
+}
+
+// ------------------------------------------------------------------------------------
+// wide drains: 64 accumulator columns per TMEM load and wait
+// ------------------------------------------------------------------------------------
+// Waits for this thread's outstanding TMEM loads and ties all 64 loaded registers to the
+// wait, so that none of their uses is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld64(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+  asm volatile(""
+               : "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]),
+                 "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]),
+                 "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]),
+                 "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]),
+                 "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]),
+                 "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
+}
+
+// As drain_to_tmem_act (GEMM0's accumulator -> act -> packed pairs written back over the
+// columns already read), 64 columns per load (ncols a multiple of 64) and 32 packed
+// columns per store: step c writes columns below p_col0 + c / 2 + 32 <= col0 + c + 64,
+// the next step's first column, when p_col0 = col0.
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain64_to_tmem_act(uint32_t tm_lane, uint32_t col0, int ncols,
+                                                    uint32_t p_col0) {
+  for (int c = 0; c < ncols; c += 64) {
+    uint32_t r[64], v[32];
+    tmem_ld64x(tm_lane + col0 + c, r);
+    tmem_wait_ld64(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      v[j] = pack2<BF16, ACT == 1>(act_fn<ACT>(__uint_as_float(r[2 * j])),
+                                   act_fn<ACT>(__uint_as_float(r[2 * j + 1])));
+    tmem_st32(tm_lane + p_col0 + (c >> 1), v);
+  }
+  tmem_wait_st();
+}
+
+template <bool BF16>
+__device__ __forceinline__ void drain64_to_tmem(int act, uint32_t tm_lane, uint32_t col0,
+                                                int ncols, uint32_t p_col0) {
+  if (act == 2)
+    drain64_to_tmem_act<BF16, 2>(tm_lane, col0, ncols, p_col0);
+  else if (act == 1)
+    drain64_to_tmem_act<BF16, 1>(tm_lane, col0, ncols, p_col0);
+  else
+    drain64_to_tmem_act<BF16, 0>(tm_lane, col0, ncols, p_col0);
+}
+
+// 64 accumulator columns of this thread's row (TMEM address taddr) -> act -> dtype -> row
+// `row` of a 128 x 64 staging tile in the 128B-swizzled layout a TMA store reads.
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain64_to_staging_act(uint32_t taddr, uint32_t staging, int row) {
+  uint32_t r[64];
+  tmem_ld64x(taddr, r);
+  tmem_wait_ld64(r);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      v[k] = pack2<BF16, ACT == 1>(act_fn<ACT>(__uint_as_float(r[16 * j + 2 * k])),
+                                   act_fn<ACT>(__uint_as_float(r[16 * j + 2 * k + 1])));
+    st_row16_sw128(staging, row, 16 * j, kPChunkBytes, v);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void drain64_to_staging(int act, uint32_t taddr, uint32_t staging,
+                                                   int row) {
+  if (act == 2)
+    drain64_to_staging_act<BF16, 2>(taddr, staging, row);
+  else if (act == 1)
+    drain64_to_staging_act<BF16, 1>(taddr, staging, row);
+  else
+    drain64_to_staging_act<BF16, 0>(taddr, staging, row);
+}
+
+// Exchanges 16-byte units inside each quad of lanes (lanes 4q .. 4q + 3): on entry lane
+// 4q + i holds units 0..3 (x[u][0..3]) of row 4q + i of the warp's rows; on return it holds
+// unit i of rows 4q + 0 .. 4q + 3 (x[j] = unit i of row 4q + j), so that the quad's four
+// lanes together hold one row's 64 contiguous bytes per j.  Two rounds of lane-xor
+// exchanges, one per bit of the lane index within the quad: in the round for bit b, a lane
+// swaps with lane ^ (1 << b) every unit u whose bit b differs from its own lane bit.
+__device__ __forceinline__ void quad_transpose_units(uint32_t (&x)[4][4], int lane) {
+  const bool i0 = (lane & 1) != 0, i1 = (lane & 2) != 0;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {          // bit 0: units 2m and 2m + 1
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t send = i0 ? x[2 * m][k] : x[2 * m + 1][k];
+      const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 1);
+      if (i0) x[2 * m][k] = got; else x[2 * m + 1][k] = got;
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {          // bit 1: units m and m + 2
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t send = i1 ? x[m][k] : x[m + 2][k];
+      const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 2);
+      if (i1) x[m][k] = got; else x[m + 2][k] = got;
+    }
+  }
+}
+
+// GEMM1's accumulator columns [col0, col0 + ncols) of the warp's 32 rows -> act -> dtype ->
+// global memory, 64 columns per wait (ncols a multiple of 64) and coalesced: after
+// quad_transpose_units each store instruction of the warp writes eight rows' 64
+// contiguous bytes.  `out_row0` is the warp's first row in the output (`rows` valid rows
+// in all, `ld` elements per row), `nvalid` the output's width (a multiple of 8); rows and
+// 16-byte units outside the output are not stored.  Every lane runs the loop
+// (warp-collective loads and shuffles).
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain64_to_global_act(uint32_t tm_lane, uint32_t col0, int ncols,
+                                                      uint8_t* out, int64_t out_row0,
+                                                      int64_t rows, int ld, int nvalid,
+                                                      int lane) {
+  const int quad = lane >> 2, unit = lane & 3;
+  for (int c = 0; c < ncols; c += 64) {
+    uint32_t r[64];
+    tmem_ld64x(tm_lane + col0 + c, r);
+    tmem_wait_ld64(r);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {        // 32 columns: units of 8 columns, 4 per row
+      uint32_t x[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int o = 32 * h + 8 * u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          x[u][k] = pack2<BF16, ACT == 1>(act_fn<ACT>(__uint_as_float(r[o + 2 * k])),
+                                           act_fn<ACT>(__uint_as_float(r[o + 2 * k + 1])));
+      }
+      quad_transpose_units(x, lane);
+      const int col = c + 32 * h + 8 * unit;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t row = out_row0 + 4 * quad + j;
+        if (row < rows && col < nvalid)
+          asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(
+                           out + (static_cast<size_t>(row) * static_cast<size_t>(ld) +
+                                  static_cast<size_t>(col)) * 2u),
+                       "r"(x[j][0]), "r"(x[j][1]), "r"(x[j][2]), "r"(x[j][3])
+                       : "memory");
+      }
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void drain64_to_global(int act, uint32_t tm_lane, uint32_t col0,
+                                                  int ncols, uint8_t* out, int64_t out_row0,
+                                                  int64_t rows, int ld, int nvalid, int lane) {
+  if (act == 2)
+    drain64_to_global_act<BF16, 2>(tm_lane, col0, ncols, out, out_row0, rows, ld, nvalid, lane);
+  else if (act == 1)
+    drain64_to_global_act<BF16, 1>(tm_lane, col0, ncols, out, out_row0, rows, ld, nvalid, lane);
+  else
+    drain64_to_global_act<BF16, 0>(tm_lane, col0, ncols, out, out_row0, rows, ld, nvalid, lane);
+}
+
 // Elementwise max of two packed fp16/bf16 pairs.
 template <bool BF16>
 __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
@@ -1078,7 +1321,7 @@ __device__ __forceinline__ bool warp_wait(bool alive, uint32_t bar, uint32_t par
 // Epilogue warps.  With epi_groups == 2 warpgroup g (warps 2+4g .. 5+4g) takes the
 // CTA's tiles i with i & 1 == g and owns buffer g; with epi_groups == 1 all eight warps
 // take every tile and warpgroup g drains the 32-column blocks 2k + g.
-template <int MODE, bool A4D, bool BF16, bool WIDE, bool PAIR, bool NOPAIR>
+template <int MODE, bool A4D, bool BF16, bool WIDE, bool PAIR, bool NOPAIR, bool W0RES>
 __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, uint32_t base,
                               uint32_t bars, uint32_t tmem_base,
                               volatile uint32_t* abort_flag) {
@@ -1135,6 +1378,22 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
                       SITE_EPI_D1_FULL, t);
     if (elected) trace(EV_EPI_D1_READY, g, it);
     tc_fence_after_sync();
+    if constexpr (W0RES) {
+      // Straight from registers to the output rows (no staging tile, no TMA store); then
+      // the buffer (D0 -> P + D1) may take tile i + 2.
+      const int32_t m = tc.m0 + row;
+      if (alive)   // warp-uniform: the drain's TMEM loads are warp-collective
+        drain_to_global<BF16>(p.act1, tm_lane, p.d1_col[b], p.N1p,
+                              p.out_ptr + static_cast<size_t>(m < p.M ? m : 0) *
+                                              static_cast<size_t>(p.out_ld) * 2u,
+                              p.N1, m < p.M);
+      if (elected) trace(EV_EPI_DRAINED, g, it);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + b));
+      if (elected) trace(EV_EPI_STORED, g, it);
+      return;
+    }
     if (PAIR || !p.out_alias_p) {
       if (elected) bulk_wait_read_all();
       named_bar_sync(bar_id, group_threads);
@@ -1378,7 +1637,7 @@ __device__ __forceinline__ void fill_w2(const ChainParams& p, uint8_t* dst, int 
 // the kernel
 // ------------------------------------------------------------------------------------
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false, bool NOPAIR = false>
+          bool PAIR = false, bool NOPAIR = false, bool W0RES = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW0,
                  const __grid_constant__ CUtensorMap tmW1,
@@ -1422,6 +1681,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     mbar_init(bars + 8u * BAR_MMA_DONE, 1);
     mbar_init(bars + 8u * BAR_BIAS_READY, kNumEpiWarps);
+    if (W0RES)
+      for (uint32_t c = 0; c < static_cast<uint32_t>(kMaxW0Chunks); ++c)
+        mbar_init(bars + 8u * (BAR_W0C0 + c), 1);
     *abort_flag = 0u;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -1465,10 +1727,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
     }
     __syncwarp();
-    producer_role<MODE, A4D, W0MN, W1MN, WIDE, PAIR, NOPAIR>(p, &tmA, &tmW0, &tmW1, base, bars, abort_flag);
+    producer_role<MODE, A4D, W0MN, W1MN, WIDE, PAIR, NOPAIR, W0RES>(p, &tmA, &tmW0, &tmW1, base,
+                                                                   bars, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR>(p, base, bars, tmem_base, abort_flag);
+    mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>(p, base, bars, tmem_base,
+                                                                    abort_flag);
     __syncwarp();
   } else {
     // The bias operands, off the producer's critical path; the MMA issuer waits for them
@@ -1482,7 +1746,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8u * BAR_BIAS_READY);
-    epilogue_role<MODE, A4D, BF16, WIDE, PAIR, NOPAIR>(p, &tmOut, base, bars, tmem_base, abort_flag);
+    epilogue_role<MODE, A4D, BF16, WIDE, PAIR, NOPAIR, W0RES>(p, &tmOut, base, bars, tmem_base,
+                                                              abort_flag);
   }
 
   tc_fence_before_sync();

@@ -23,6 +23,7 @@ enum KernelId : uint32_t {
   KID_CONV_SINGLE = 6,
   KID_CONV_POOL = 7,
   KID_GEMM_CHAIN3 = 8,
+  KID_GEMM_CHAIN_CTA2 = 9,   // b2b GEMM chain over CTA pairs (cta_group::2)
   KID_PROBE = 15,
 };
 
@@ -77,6 +78,7 @@ constexpr int kNumEpiThreads = 32 * kNumEpiWarps;
 constexpr int kNumThreads = 64 + kNumEpiThreads;   // warp 0 TMA, warp 1 MMA + TMEM, 2..9 epilogue
 constexpr int kMaxStages = 8;
 constexpr int kMaxBufs = 4;          // accumulator / P buffers per CTA
+constexpr int kMaxW0Chunks = 8;      // K chunks of a W0 kept resident beside streamed W1
 // Bias operands in shared memory (at off_bias): a 1 KiB ONES tile, then per GEMM one
 // 2 KiB BIAS block per 64-wide N block.
 constexpr uint32_t kOnesBytes = 1024;
@@ -145,6 +147,17 @@ struct ChainParams {
                                 //    [N/64][K][64], so one 3-D box loads a whole K chunk
   int32_t out_box3;             // 1: the 2-D output (N a multiple of 64) is mapped the same
                                 //    way and a tile is stored by one 3-D box
+  int32_t w0_res;               // 1 (P in TMEM, tile pairs): W0 alone is resident, loaded
+                                //    once per CTA with one barrier per K chunk; A and W1
+                                //    stream through the ring, and epilogue 1 stores the
+                                //    output tile from registers straight to global memory
+                                //    (no staging tile: W0 takes its shared memory)
+  int32_t cta_pair;             // 1: the chain runs over CTA pairs (chain_cta2_kernel.cuh,
+                                //    clusters of two CTAs, tcgen05 .cta_group::2); num_tiles
+                                //    then counts 256-row tiles, and each CTA holds half of
+                                //    W0 and of W1 (w0/w1_chunk_bytes are the halves' chunks)
+  uint8_t* out_ptr;             // w0_res, cta_pair: the output D [M][out_ld] row-major
+  int32_t out_ld;               // w0_res, cta_pair: elements per output row
   int32_t w1_group;             // 1 (P in TMEM, streamed weights): W1 is loaded once per
                                 //    pair of tiles, w1_per_stage chunks per ring stage,
                                 //    and both tiles' GEMM1 read it from the same stages

@@ -10,19 +10,19 @@ namespace b2b {
 namespace B2B_KNS {
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false, bool NOPAIR = false>
+          bool PAIR = false, bool NOPAIR = false, bool W0RES = false>
 const void* kernel_ptr() {
   return reinterpret_cast<const void*>(
-      &chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR>);
+      &chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>);
 }
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false, bool NOPAIR = false>
+          bool PAIR = false, bool NOPAIR = false, bool W0RES = false>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1,
                        const CUtensorMap& out, const ChainParams& p, int grid, size_t smem,
                        cudaStream_t stream) {
-  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR>, a, w0, w1, out, p, grid,
-                      smem, stream);
+  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>, a, w0,
+                      w1, out, p, grid, smem, stream);
 }
 
 // 2-D A operand: GEMM chains (row-major weights) and 1x1 convs (K-major filters).
@@ -36,6 +36,8 @@ const void* variant_func_a2d(Variant v) {
     case V_GEMM_CHAIN3: return kernel_ptr<MODE_CHAIN3, false, true, true, BF16>();
     case V_GEMM_CHAIN_WIDE: return kernel_ptr<MODE_CHAIN, false, true, true, BF16, true>();
     case V_GEMM_CHAIN_PAIR: return kernel_ptr<MODE_CHAIN, false, true, true, BF16, false, true>();
+    case V_GEMM_CHAIN_PAIR_W0:
+      return kernel_ptr<MODE_CHAIN, false, true, true, BF16, false, true, false, true>();
     case V_GEMM_CHAIN_NP:
       return kernel_ptr<MODE_CHAIN, false, true, true, BF16, false, false, true>();
     case V_CONV1X1_CHAIN_NP:
@@ -65,6 +67,9 @@ cudaError_t launch_variant_a2d(Variant v, const CUtensorMap& a, const CUtensorMa
     case V_GEMM_CHAIN_PAIR:
       return launch_one<MODE_CHAIN, false, true, true, BF16, false, true>(a, w0, w1, out, p, grid,
                                                                          smem, s);
+    case V_GEMM_CHAIN_PAIR_W0:
+      return launch_one<MODE_CHAIN, false, true, true, BF16, false, true, false, true>(
+          a, w0, w1, out, p, grid, smem, s);
     case V_GEMM_CHAIN_NP:
       return launch_one<MODE_CHAIN, false, true, true, BF16, false, false, true>(
           a, w0, w1, out, p, grid, smem, s);

@@ -21,7 +21,15 @@ namespace b2b {
   template <bool BF16>                                                                       \
   cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMap& w0,     \
                                  const CUtensorMap& w1, const CUtensorMap& out,              \
-                                 const ChainParams& p, int grid, size_t smem, cudaStream_t s);
+                                 const ChainParams& p, int grid, size_t smem, cudaStream_t s); \
+  template <bool BF16>                                                                       \
+  const void* cta2_func();                                                                   \
+  template <bool BF16>                                                                       \
+  cudaError_t cta2_launch(const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1, \
+                          const CUtensorMap& out, const ChainParams& p, int grid, size_t smem, \
+                          cudaStream_t s);                                                   \
+  template <bool BF16>                                                                       \
+  cudaError_t cta2_clusters(size_t smem, int* clusters);
 namespace plain {
 B2B_UNIT_DECLS
 }
@@ -35,6 +43,10 @@ static bool is_a4d(Variant v) {
 }
 
 const void* variant_func(Variant v, bool bf16, bool trace) {
+  if (v == V_GEMM_CHAIN_CTA2) {
+    if (trace) return bf16 ? traced::cta2_func<true>() : traced::cta2_func<false>();
+    return bf16 ? plain::cta2_func<true>() : plain::cta2_func<false>();
+  }
   if (trace) {
     if (is_a4d(v)) return bf16 ? traced::variant_func_a4d<true>(v) : traced::variant_func_a4d<false>(v);
     return bf16 ? traced::variant_func_a2d<true>(v) : traced::variant_func_a2d<false>(v);
@@ -47,6 +59,13 @@ cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w
                            const CUtensorMap& w1, const CUtensorMap& out, const ChainParams& p,
                            int grid, size_t smem, cudaStream_t stream) {
   const bool bf16 = p.is_bf16 != 0;
+  if (v == V_GEMM_CHAIN_CTA2) {
+    if (p.trace != nullptr)
+      return bf16 ? traced::cta2_launch<true>(a, w0, w1, out, p, grid, smem, stream)
+                  : traced::cta2_launch<false>(a, w0, w1, out, p, grid, smem, stream);
+    return bf16 ? plain::cta2_launch<true>(a, w0, w1, out, p, grid, smem, stream)
+                : plain::cta2_launch<false>(a, w0, w1, out, p, grid, smem, stream);
+  }
   if (p.trace != nullptr) {
     if (is_a4d(v))
       return bf16 ? traced::launch_variant_a4d<true>(v, a, w0, w1, out, p, grid, smem, stream)
@@ -59,6 +78,13 @@ cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w
                 : plain::launch_variant_a4d<false>(v, a, w0, w1, out, p, grid, smem, stream);
   return bf16 ? plain::launch_variant_a2d<true>(v, a, w0, w1, out, p, grid, smem, stream)
               : plain::launch_variant_a2d<false>(v, a, w0, w1, out, p, grid, smem, stream);
+}
+
+cudaError_t cta2_max_clusters(bool bf16, bool trace, size_t smem, int* clusters) {
+  if (trace)
+    return bf16 ? traced::cta2_clusters<true>(smem, clusters)
+                : traced::cta2_clusters<false>(smem, clusters);
+  return bf16 ? plain::cta2_clusters<true>(smem, clusters) : plain::cta2_clusters<false>(smem, clusters);
 }
 
 // ------------------------------------------------------------------------------------

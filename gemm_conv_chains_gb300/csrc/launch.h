@@ -26,6 +26,9 @@ enum Variant : int {
   V_GEMM_CHAIN_NP,     // the chain variants above with P in shared memory (the P-in-TMEM
   V_CONV1X1_CHAIN_NP,  //   loops left out)
   V_CONV_CHAIN_NP,
+  V_GEMM_CHAIN_PAIR_W0,   // tile pairs, P in TMEM, W0 resident, A and W1 streamed, output
+                          //   stored from registers
+  V_GEMM_CHAIN_CTA2,      // the chain over CTA pairs (chain_cta2_kernel.cuh)
   V_COUNT
 };
 
@@ -50,6 +53,34 @@ inline cudaError_t launch_chain(ChainKernelFn fn, const CUtensorMap& a, const CU
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fn, a, w0, w1, out, p);
 }
+
+// Launches a CTA-pair kernel (V_GEMM_CHAIN_CTA2) in clusters of two CTAs (`grid` even),
+// with programmatic stream serialisation as launch_chain.
+inline cudaError_t launch_chain_cta2(ChainKernelFn fn, const CUtensorMap& a, const CUtensorMap& w0,
+                                     const CUtensorMap& w1, const CUtensorMap& out,
+                                     const ChainParams& p, int grid, size_t smem,
+                                     cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(kNumThreads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, fn, a, w0, w1, out, p);
+}
+
+// How many clusters of two CTAs of the CTA-pair kernel (dtype, build) can be resident at
+// once with `smem` bytes of dynamic shared memory each (its function attributes set), or
+// an error.
+cudaError_t cta2_max_clusters(bool bf16, bool trace, size_t smem, int* clusters);
 
 // Kernel function pointer of a variant, operand dtype and build (with or without the event
 // trace), for cudaFuncSetAttribute.

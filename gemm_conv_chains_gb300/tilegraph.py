@@ -148,6 +148,8 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
     epilogue warps).  `A_in_bounds` (not in the total) is the part of A inside the
     tensor; A / A_in_bounds is the waste of ragged and halo tiles."""
     plan = plan or plan_of(w)
+    if plan.get("cta_pair"):
+        return _cta_pair_traffic(w, plan, num_sms)
     per_cta = tiles_per_cta(plan["tiles"], num_sms)
     ctas = len(per_cta)
     tiles = plan["tiles"]
@@ -178,6 +180,11 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
         out["W0"] = ctas * w0
         if w1:
             out["W1"] = ctas * w1
+    elif plan.get("w0_res"):
+        # W0 alone resident, W1 streamed (once per pair of tiles when grouped)
+        out["W0"] = ctas * w0
+        loads_w1 = sum(-(-n // 2) for n in per_cta) if plan["w1_group"] else tiles
+        out["W1"] = loads_w1 * w1
     else:
         out["W0"] = tiles * w0
         if w1:
@@ -196,6 +203,22 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
         useful = _conv_tile_input_bytes(w.N, w.H, w.W, w.Cin, 3, 3, 1, bool(plan["halo"]))
     out["total"] = sum(out.values())
     out["A_in_bounds"] = useful
+    return out
+
+
+def _cta_pair_traffic(w, plan: dict, num_sms: int) -> Dict[str, int]:
+    """l2_to_smem_traffic of a plan over CTA pairs (b2b GEMM chains): 256-row tiles on up to
+    num_sms / 2 pairs; each CTA loads its 128 rows of every A chunk, its halves of W0 and W1
+    once, and its halves of the biases."""
+    pairs = len(tiles_per_cta(plan["tiles"], num_sms // 2))
+    ctas = 2 * pairs
+    out: Dict[str, int] = {}
+    out["A"] = plan["tiles"] * 2 * plan["kchunks0"] * A_BOX
+    out["W0"] = ctas * plan["kchunks0"] * plan["w0_chunk"]
+    out["W1"] = ctas * plan["kchunks1"] * plan["w1_chunk"]
+    out["bias"] = ctas * (plan["N0p"] // 2 + plan["N1p"] // 2) * ELEM
+    out["total"] = sum(out.values())
+    out["A_in_bounds"] = w.M * w.K0 * ELEM
     return out
 
 
@@ -243,7 +266,10 @@ def chain_buffers(plan: dict) -> List[Buffer]:
     whole = (0, 5)
     bufs = [Buffer("ring", plan["ring"], whole), Buffer("bias", plan["bias"], whole),
             Buffer("bar", plan["bar"], whole)]
-    if plan["resident"]:
+    if plan.get("cta_pair"):
+        # CTA pairs: the halves of both weights resident, P in TMEM, no output staging
+        return bufs + [Buffer("weights", plan["w_res"], whole)]
+    if plan["resident"] or plan.get("w0_res"):
         bufs.append(Buffer("weights", plan["w_res"], whole))
     if plan["mode"] == 3:
         # three-operator chain: two tiles in flight hold P0, P1 and the staging of both
@@ -258,7 +284,8 @@ def chain_buffers(plan: dict) -> List[Buffer]:
     out_cols = plan["N1p"] if chain else plan["N0p"]
     per_chunk = 32 * 128 if plan["mode"] == 2 else 128 * 128   # pooled: 4 x 8 pixels per tile
     out_bytes = (out_cols + 63) // 64 * per_chunk
-    obufs = 2 if plan["groups"] == 2 else 1
+    # (W0 resident beside streamed W1: the output leaves from registers, no staging)
+    obufs = 0 if plan.get("w0_res") else (2 if plan["groups"] == 2 else 1)
     paired = bool(plan["alias"]) and pbufs == obufs
     for i in range(pbufs):
         bufs.append(Buffer(f"P{i}", p_bytes, (2, 3) if paired else whole))
@@ -315,6 +342,20 @@ def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
     TMA ingress.  Tensor: the busiest CTA's share of the MMA FLOPs over one SM's share of
     the peak.  `floor` is the largest; `bound` names it."""
     plan = plan or plan_of(w)
+    if plan.get("cta_pair"):
+        # pairs of SMs share each 256-row tile; per SM: 128 rows of each of its pair's tiles,
+        # its weight halves, half of each tile's MMA FLOPs
+        per_pair = tiles_per_cta(plan["tiles"], num_sms // 2)
+        n = max(per_pair)
+        t = l2_to_smem_traffic(w, plan, num_sms)
+        ctas = 2 * len(per_pair)
+        cta_bytes = (t["A"] / (2 * plan["tiles"]) * n + (t["W0"] + t["W1"] + t["bias"]) / ctas)
+        out = {"hbm_us": w.floor_bytes / (hbm_gbs * 1e3),
+               "l2_us": cta_bytes / (L2_TO_SM_BYTES_PER_CLK * sm_mhz),
+               "tensor_us": w.flops / (2 * plan["tiles"]) * n / (tensor_tflops * 1e6 / num_sms)}
+        out["bound"] = max(out, key=out.get)[:-3]
+        out["floor_us"] = max(out["hbm_us"], out["l2_us"], out["tensor_us"])
+        return out
     per_cta = tiles_per_cta(plan["tiles"], num_sms)
     ctas, tiles, n = len(per_cta), plan["tiles"], max(per_cta)
     t = l2_to_smem_traffic(w, plan, num_sms)
@@ -322,7 +363,7 @@ def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
     for k in ("W0", "W1"):
         if k not in t:
             continue
-        if plan["resident"] or isinstance(w, wl.GemmChain3):
+        if plan["resident"] or isinstance(w, wl.GemmChain3) or (k == "W0" and plan.get("w0_res")):
             cta_bytes += t[k] / ctas
         elif k == "W1" and plan["w1_group"]:
             loads = sum(-(-m // 2) for m in per_cta)
@@ -368,7 +409,8 @@ def report(ncu: Optional[Dict[str, str]] = None) -> str:
     for name, w in wl.WORKLOADS.items():
         plan = plan_of(w)
         t = l2_to_smem_traffic(w, plan)
-        desc = ("resident" if plan["resident"] else "streamed") + \
+        desc = ("CTA pairs, " if plan.get("cta_pair") else "") + \
+            ("W0 resident" if plan.get("w0_res") else "resident" if plan["resident"] else "streamed") + \
             (", P in TMEM" if plan["p_tmem"] else f", {plan['nbuf']} P buffers") * (plan["mode"] == 0) + \
             (", halo" if plan["halo"] else "") + (", alias" if plan["alias"] else "")
         got = read_ncu_raw_csv(ncu[name]).get(NCU_L2_TO_SM) if name in ncu else None

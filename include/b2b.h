@@ -245,7 +245,7 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad[, stride]}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
  *   kind 5 b2b_gemm3           dims = {M, K0, N0, N1, N2}
- * out (out_len >= 57) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ * out (out_len >= 60) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
  * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
  * P offsets [2], bytes per P buffer, staging offsets [2], bytes per staging buffer,
@@ -264,7 +264,12 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * a launch adds over the output staging when no CTA gets more than two tiles (P in TMEM,
  * streamed weights; the staging is first written after the pair's last GEMM0), then, for
  * the three-operator chain, the resident W2 offset, P1 offsets [2] and GEMM2 accumulator
- * columns [2] (0 otherwise).  A choice pinned or measured for these sizes is reflected.
+ * columns [2] (0 otherwise), the TMEM column split of a wide chain's two GEMM0 passes (256,
+ * else 0), and 1 if W0 alone stays resident while A and W1 stream through the ring (P in
+ * TMEM, tile pairs; the output is then stored from registers, with no staging tile), and
+ * 1 if the chain runs over CTA pairs (clusters of two CTAs sharing each MMA of 256 rows,
+ * each holding half of W0 and W1; tiles then count 256 rows).  A choice pinned or
+ * measured for these sizes is reflected.
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,

@@ -119,19 +119,31 @@ def test_b2b_gemm_narrow_four_buffers_sampled_rows(integer):
     run_b2b_gemm(w, seed=13, integer=integer, rows=rows)
 
 
+@pytest.mark.parametrize("streamed", [False, True])
 @pytest.mark.parametrize("integer", [True, False])
-def test_b2b_gemm_wide_streamed_pairs_sampled_rows(integer):
-    # K0 = 256 streams the weights, so GEMM0 of each tile pair runs interleaved (one W0
-    # chunk per stage for both tiles); 3 x SMs + 1 tiles give CTA 0 two pairs, the second
-    # with one ragged tile.
+def test_b2b_gemm_wide_streamed_pairs_sampled_rows(integer, streamed):
+    # K0 = 256: by default both weights stream (W0 with every tile's A chunks); with
+    # `streamed` False the next layout is pinned, which keeps W0 (128 KiB) resident and
+    # streams A and W1 through the ring, the output leaving from registers.  3 x SMs + 1
+    # tiles give CTA 0 two tile pairs, the second with one ragged tile.
     nsm = ops.num_sms()
     M = 128 * nsm * 3 + 77
-    acts = ("relu", "none") if integer else ("hardswish", "hardswish")   # exact: no fractions
-    w = wl.GemmChain("spairs", "bf16", M, 256, 256, 128, *acts)
-    rng = np.random.default_rng(6)
-    cta0 = np.concatenate([np.arange(128 * t, min(128 * t + 128, M)) for t in range(0, 3 * nsm + 1, nsm)])
-    rows = np.unique(np.concatenate([cta0, rng.choice(M, 512, replace=False)]))
-    run_b2b_gemm(w, seed=12, integer=integer, rows=rows)
+    dims = (M, 256, 256, 128)
+    plan = ops.debug_plan("b2b_gemm", dims)
+    assert plan["w0_res"] == 0 and plan["cta_pair"] == 0
+    if not streamed:
+        ops.set_choice("b2b_gemm", dims, cand=plan["cand"] + 1)
+        assert ops.debug_plan("b2b_gemm", dims)["w0_res"] == 1
+    try:
+        acts = ("relu", "none") if integer else ("hardswish", "hardswish")   # exact: no fractions
+        w = wl.GemmChain("spairs", "bf16", M, 256, 256, 128, *acts)
+        rng = np.random.default_rng(6)
+        cta0 = np.concatenate([np.arange(128 * t, min(128 * t + 128, M))
+                               for t in range(0, 3 * nsm + 1, nsm)])
+        rows = np.unique(np.concatenate([cta0, rng.choice(M, 512, replace=False)]))
+        run_b2b_gemm(w, seed=12, integer=integer, rows=rows)
+    finally:
+        ops.autotune_reset()
 
 
 @pytest.mark.parametrize("integer", [True, False])
@@ -471,3 +483,58 @@ def test_timeout_path_reports_and_context_survives():
     assert st == 6 and info[0] == 6 and info[1] == 15, (st, info)
     assert ops.get_device_error()[0] == 0    # read-and-clear
     run_b2b_gemm(wl.GemmChain("after", "f16", 200, 64, 64, 64, "relu", "none"), integer=True)
+
+
+# ------------------------------------------------------------------------------------
+# the chain over CTA pairs (clusters of two CTAs sharing each 256-row MMA)
+# ------------------------------------------------------------------------------------
+def _pin_cta_pair(dims):
+    n = ops.debug_plan("b2b_gemm", dims)["ncand"]
+    ops.set_choice("b2b_gemm", dims, cand=n - 1)
+    assert ops.debug_plan("b2b_gemm", dims)["cta_pair"] == 1
+
+
+CTA_PAIR_SHAPES = [
+    # dtype, M, K0, N0, N1
+    ("bf16", 513, 256, 256, 128),     # three 256-row tiles, the last one's second CTA idle
+    ("f16", 300, 64, 128, 128),
+    ("bf16", 129, 8, 128, 128),       # one tile, ragged inside the first CTA
+    ("f16", 1000, 448, 256, 128),     # seven K chunks of W0 (four ring stages)
+    ("bf16", 700, 200, 128, 128),     # a partial last K chunk
+]
+
+
+@pytest.mark.parametrize("shape", CTA_PAIR_SHAPES, ids=lambda s: "-".join(map(str, s)))
+@pytest.mark.parametrize("integer", [True, False])
+def test_b2b_gemm_cta_pair(shape, integer):
+    dt, M, K0, N0, N1 = shape
+    _pin_cta_pair((M, K0, N0, N1))
+    try:
+        acts = ("relu", "none") if integer else ("hardswish", "relu")
+        w = wl.GemmChain("cta2", dt, M, K0, N0, N1, *acts, a_dist="normal")
+        run_b2b_gemm(w, seed=M + K0, integer=integer)
+    finally:
+        ops.autotune_reset()
+
+
+@pytest.mark.parametrize("integer", [True, False])
+def test_b2b_gemm_cta_pair_many_tiles_sampled_rows(integer):
+    # 5 x SMs + 1 tiles of 128 rows: each pair runs five or six 256-row tiles (both TMEM
+    # buffers reused), the last one ragged; rows of every tile of the first pair
+    nsm = ops.num_sms()
+    M = 128 * nsm * 5 + 77
+    dims = (M, 256, 256, 128)
+    _pin_cta_pair(dims)
+    try:
+        acts = ("relu", "none") if integer else ("hardswish", "hardswish")
+        w = wl.GemmChain("cta2many", "bf16", M, 256, 256, 128, *acts, a_dist="normal")
+        pairs = ops.debug_plan("b2b_gemm", dims)["tiles"]
+        rng = np.random.default_rng(9)
+        npairs_max = nsm // 2
+        first = np.concatenate([np.arange(256 * t, min(256 * t + 256, M))
+                                for t in range(0, pairs, npairs_max)])
+        rows = np.unique(np.concatenate([first, np.arange(M - 256, M),
+                                         rng.choice(M, 512, replace=False)]))
+        run_b2b_gemm(w, seed=21, integer=integer, rows=rows)
+    finally:
+        ops.autotune_reset()

@@ -23,7 +23,7 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes",
           "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2", "d1_col3", "cand", "ncand",
           "grid_choice", "pf_choice", "ring_extend", "off_w2", "off_p1_0", "off_p1_1", "d2_col0",
-          "d2_col1", "p_split"]
+          "d2_col1", "p_split", "w0_res", "cta_pair"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4, "b2b_gemm3": 5}
@@ -31,8 +31,8 @@ KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nh
 
 def plan(kind, dims):
     arr = (ctypes.c_int64 * len(dims))(*dims)
-    out = (ctypes.c_uint32 * 58)()
-    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, 58)
+    out = (ctypes.c_uint32 * len(FIELDS))()
+    st = ops.lib().b2b_debug_plan(KIND[kind], arr, len(dims), out, len(FIELDS))
     return st, dict(zip(FIELDS, list(out)))
 
 
@@ -47,6 +47,8 @@ def check(kind, dims, row_major_w):
     if kind in ("b2b_conv_nhwc", "conv_bias_act_nhwc") and dims[5] == 1 and dims[6] == 1 and dims[7] == 0:
         R = 1   # a 1x1 pad-0 conv runs as a GEMM
     assert st == 0, (kind, dims, st)
+    if p["cta_pair"]:
+        return check_cta2(kind, dims, p)
     mode = p["mode"]
     N0p, N1p = p["N0p"], p["N1p"]
     n0blk, n1blk = -(-N0p // 64), -(-N1p // 64)
@@ -60,7 +62,8 @@ def check(kind, dims, row_major_w):
     assert p["smem"] <= SMEM_LIMIT
     assert 2 <= p["stages"] <= 8
     assert p["ring"] == p["stages"] * p["stage_bytes"]
-    assert p["stage_bytes"] >= p["a_stage_bytes"] + (0 if p["resident"] else w0_chunk)
+    w0_res = p["w0_res"] == 1
+    assert p["stage_bytes"] >= p["a_stage_bytes"] + (0 if p["resident"] or w0_res else w0_chunk)
     if p["halo"]:
         # one box of (8 + R - 1) x 16 pixels x 64 channels per column tap feeds all row taps
         assert p["resident"] and p["a_stage_bytes"] == (8 + R - 1) * 16 * 128
@@ -71,9 +74,17 @@ def check(kind, dims, row_major_w):
     regions = [("ring", p["off_ring"], p["ring"]), ("bias", p["off_bias"], p["bias"]),
                ("bar", p["off_bar"], p["bar"])]
     if p["resident"]:
+        assert not w0_res
         assert p["w_res"] >= p["kchunks0"] * w0_chunk + p["kchunks1"] * w1_chunk
         assert p["off_w1"] == p["off_w0"] + p["kchunks0"] * w0_chunk
         regions.append(("w", p["off_w0"], p["w_res"]))
+    if w0_res:
+        # W0 alone resident (one barrier per K chunk, at most 8), A and W1 through the ring,
+        # tile pairs with P in TMEM, and no output staging (stores from registers)
+        assert mode == 0 and row_major_w and p["p_tmem"] and p["dual"] and p["groups"] == 2
+        assert p["kchunks0"] <= 8 and p["w_res"] >= p["kchunks0"] * w0_chunk
+        assert p["stage_bytes"] >= max(128 * 128, w1_chunk) and not p["ring_extend"]
+        regions.append(("w0", p["off_w0"], p["w_res"]))
     dual = p["dual"] == 1
     groups = p["groups"]
     assert groups in (1, 2) and (groups == 1 or dual)
@@ -118,6 +129,8 @@ def check(kind, dims, row_major_w):
         # staging b (used by epilogue group b, which handles the tiles using P[b])
         for b in range(obufs):
             assert p[f"off_out{b}"] == p[f"off_p{b if dual else 0}"]
+    elif w0_res:
+        assert p["out"] == 0
     else:
         assert p["out"] >= out_need
         for b in range(obufs):
@@ -170,6 +183,69 @@ def check(kind, dims, row_major_w):
     return p
 
 
+def check_cta2(kind, dims, p):
+    """A plan over CTA pairs (clusters of two CTAs sharing each 256-row MMA): per CTA a ring
+    of 16 KiB A chunks (128 rows x 64 K), its half of W0 and of W1 resident (64-wide blocks
+    of 64 K-rows x 128 B), the ONES tile and a 2 KiB bias block per 64 columns of its halves,
+    the barriers; P kept in TMEM over GEMM0's columns, two 256-row tiles in flight."""
+    assert kind == "b2b_gemm" and p["mode"] == 0
+    M, K0, N0, N1 = dims[:4]
+    N0p, N1p = p["N0p"], p["N1p"]
+    assert N0p % 128 == 0 and N1p % 128 == 0 and N0p <= 256 and N1p <= 256
+    nb0, nb1 = N0p // 128, N1p // 128
+    k0, k1 = -(-K0 // 64), -(-N0p // 64)
+    assert p["kchunks0"] == k0 <= 8 and p["kchunks1"] == k1
+    assert p["tiles"] == -(-M // 256)
+    assert p["w0_chunk"] == nb0 * 8192 and p["w1_chunk"] == nb1 * 8192
+    assert p["stage_bytes"] == p["a_stage_bytes"] == 128 * 128 and 3 <= p["stages"] <= 8
+    assert p["ring"] == p["stages"] * p["stage_bytes"]
+    assert p["resident"] and p["p_tmem"] and p["dual"] and p["groups"] == 2 and p["nbuf"] == 2
+    assert not p["w0_res"] and not p["halo"] and p["p"] == 0
+    assert p["out"] == 0                         # the output leaves from registers
+    assert p["off_w1"] == p["off_w0"] + k0 * p["w0_chunk"]
+    assert p["w_res"] == k0 * p["w0_chunk"] + k1 * p["w1_chunk"]
+    assert p["bias"] >= 1024 + 2048 * (nb0 + nb1)
+    assert p["bar"] >= 8 * 35 + 8                # 35 barriers, then the TMEM slot and flag
+    assert p["smem"] <= SMEM_LIMIT
+    usable = p["smem"] - 1024
+    regions = [("ring", p["off_ring"], p["ring"]), ("w", p["off_w0"], p["w_res"]),
+               ("bias", p["off_bias"], p["bias"]), ("bar", p["off_bar"], p["bar"])]
+    for name, off, size in regions:
+        assert off % 1024 == 0 and off + size <= usable, (name, off, size, usable)
+    for (a, oa, sa), (b, ob, sb) in itertools.combinations(regions, 2):
+        assert oa + sa <= ob or ob + sb <= oa, (a, b)
+    spans = []
+    for b in range(2):
+        d0, d1 = p[f"d0_col{b}"], p[f"d1_col{b}"]
+        assert d0 % 32 == 0 and d1 % 32 == 0 and d1 >= d0 + N0p // 2
+        spans.append((d0, max(d0 + N0p, d1 + N1p)))
+        assert spans[-1][1] <= p["tmem_cols"] <= 512
+    assert spans[0][1] <= spans[1][0] or spans[1][1] <= spans[0][0]
+    return p
+
+
+def test_ffn_offers_a_cta_pair_plan():
+    # the FFN-like chain also runs over CTA pairs: each SM keeps half of W0 (64 KiB) and of
+    # W1 (32 KiB) resident beside a seven-stage ring of A chunks
+    dims = (32768, 256, 256, 128)
+    n = ops.debug_plan("b2b_gemm", dims)["ncand"]
+    ops.set_choice("b2b_gemm", dims, cand=n - 1)
+    try:
+        p = check("b2b_gemm", dims, True)
+    finally:
+        ops.autotune_reset()
+    assert p["cta_pair"] == 1 and p["stages"] == 7 and p["w_res"] == 96 * 1024
+    assert p["tiles"] == 128
+    # chains the pair kernel does not take offer no such plan
+    for d in ((1000, 64, 64, 64), (1000, 64, 192, 128), (1000, 576, 256, 128)):
+        m = ops.debug_plan("b2b_gemm", d)["ncand"]
+        ops.set_choice("b2b_gemm", d, cand=m - 1)
+        try:
+            assert ops.debug_plan("b2b_gemm", d)["cta_pair"] == 0
+        finally:
+            ops.autotune_reset()
+
+
 GEMM = [(1, 64, 64, 64), (640, 128, 128, 256), (200, 320, 96, 200), (384, 64, 256, 256),
         (32768, 256, 256, 128), (1024, 64, 64, 64), (129, 8, 8, 8), (257, 72, 40, 24),
         (100, 2048, 256, 256), (100, 8, 256, 8)]
@@ -188,16 +264,39 @@ def test_b2b_gemm_plan_sweep():
 
 
 def test_ffn_plan_keeps_p_in_tmem():
-    p = check("b2b_gemm", (32768, 256, 256, 128), True)
+    dims = (32768, 256, 256, 128)
+    p = check("b2b_gemm", dims, True)
     assert p["resident"] == 0      # 192 KiB of weights cannot stay beside the ring
     # 2 x (256 + 128) accumulator columns exceed 512, but D0 -> P + D1 in one 256-column
     # buffer per tile gives two tiles in flight with P in TMEM
     assert p["p_tmem"] == 1 and p["dual"] == 1
-    # W1 (4 chunks of 16 KiB) fits in two 48 KiB stages, loaded once per pair of tiles
+    # both weights stream: three 48 KiB stages (an A chunk and a W0 chunk each), W1 three
+    # chunks to a stage, and a fourth stage over the two 32 KiB output staging buffers when
+    # no CTA has a third tile (W1's stages of the pair, fills 8 and 9, land on stages 0, 1)
+    assert p["w0_res"] == 0 and p["cta_pair"] == 0
     assert p["w1_group"] == 1 and p["w1_per_stage"] == 3
-    # three 48 KiB stages, and a fourth over the two 32 KiB output staging buffers when no
-    # CTA has a third tile (W1's stages of the pair, fills 8 and 9, land on stages 0 and 1)
     assert p["stages"] == 3 and p["ring_extend"] == 1
+    # the next layout keeps W0 (128 KiB) alone resident: five 16 KiB stages carry A and W1
+    # chunks, W1 (4 chunks of 16 KiB) once per pair of tiles, no output staging
+    ops.set_choice("b2b_gemm", dims, cand=p["cand"] + 1)
+    try:
+        q = check("b2b_gemm", dims, True)
+    finally:
+        ops.autotune_reset()
+    assert q["w0_res"] == 1 and q["w_res"] == 4 * 32768 and q["out"] == 0
+    assert q["stages"] == 5 and q["stage_bytes"] == 16384
+    assert q["w1_group"] == 1 and q["w1_per_stage"] == 1
+
+
+def test_large_chains_default_to_cta_pairs():
+    # from 512 row tiles on, a chain the CTA-pair kernel takes runs over CTA pairs by
+    # default (tiles then count 256 rows); below, over single CTAs
+    for M, pair in ((511 * 128, False), (511 * 128 + 1, True), (262144, True), (32768, False)):
+        p = check("b2b_gemm", (M, 256, 256, 128), True)
+        assert p["cta_pair"] == int(pair), M
+        assert p["tiles"] == -(-M // (256 if pair else 128))
+        assert p["cand"] == p["ncand"] - 1 if pair else p["cand"] < p["ncand"] - 1
+    assert check("b2b_gemm", (262144, 64, 64, 64), True)["cta_pair"] == 0   # N0 not % 128
 
 
 def test_small_chains_keep_four_tiles_in_flight():

@@ -7,6 +7,7 @@ allocation lets buffers with disjoint lifetimes share an offset.
 """
 import pytest
 
+from gemm_conv_chains_gb300 import ops
 from gemm_conv_chains_gb300 import tilegraph as tg
 from gemm_conv_chains_gb300 import workloads as wl
 
@@ -47,6 +48,9 @@ def test_ffn_l2_traffic_by_hand():
     assert t["W1"] == 152 * 256 * 128 * 2
     assert t["bias"] == 152 * (256 + 128) * 2
     assert t["total"] == 16_777_216 + 33_554_432 + 9_961_472 + 116_736   # 60.41 MB
+    # with W0 resident (the next layout), W0 crosses once per CTA
+    plan = dict(ops.debug_plan("b2b_gemm", (32768, 256, 256, 128)), w0_res=1)
+    assert tg.l2_to_smem_traffic(wl.GEMM_FFN, plan)["W0"] == 152 * 256 * 256 * 2
 
 
 def test_wide_chain_l2_traffic_by_hand():
