@@ -31,6 +31,7 @@ on a per-step sample of the same workload sized so the whole run takes about a m
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -72,7 +73,8 @@ def kernel_source_sha():
     """Hash of the kernel and launch-planner sources, comments and blank lines left out, so
     that a comment edit keeps the counters taken on the same code valid."""
     h = hashlib.sha256()
-    for name in ("chain_kernel.cuh", "ptx.cuh", "kernel_params.h", "kernel_units.cuh", "api.cu"):
+    for name in ("chain_kernel.cuh", "chain_cta2_kernel.cuh", "ptx.cuh", "kernel_params.h",
+                 "kernel_units.cuh", "kernels_cta2_units.cuh", "api.cu"):
         with open(os.path.join(ROOT, "gemm_conv_chains_gb300", "csrc", name)) as f:
             for line in f.read().splitlines():
                 code = line.split("//", 1)[0].rstrip()
@@ -512,6 +514,14 @@ def run_ours(args):
     ops.get_device_error()
     peaks = load_peaks()
     w = wl.WORKLOADS[args.workload]
+    if args.rows is not None:
+        if not isinstance(w, wl.GemmChain):
+            raise SystemExit("--rows applies to the GEMM-chain workloads only")
+        w = w.with_m(args.rows)
+    if args.batch is not None:
+        if not isinstance(w, (wl.ConvChain, wl.ConvPool)):
+            raise SystemExit("--batch applies to the conv workloads only")
+        w = dataclasses.replace(w, N=args.batch, name=f"{w.name}_n{args.batch}")
     fused, unfused, nsets, set_bytes = runner_for(w, dev)
     clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES")
                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
@@ -672,6 +682,12 @@ def main():
     ap.add_argument("--workload", choices=sorted(wl.WORKLOADS), default=HEADLINE.name,
                     help="workload of the timed line (default: the FFN-like chain at its "
                          "largest M); the others are for profiling single kernels")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="for profiling: run a GEMM-chain workload over this many rows "
+                         "instead of its own M")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="for profiling: run a conv workload over this many images instead "
+                         "of its own N")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -6,7 +6,8 @@ import shutil
 
 import bench
 
-SRC = ("chain_kernel.cuh", "ptx.cuh", "kernel_params.h", "kernel_units.cuh", "api.cu")
+SRC = ("chain_kernel.cuh", "chain_cta2_kernel.cuh", "ptx.cuh", "kernel_params.h", "kernel_units.cuh",
+       "kernels_cta2_units.cuh", "api.cu")
 
 
 def _copy_tree(tmp_path):
