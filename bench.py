@@ -500,6 +500,29 @@ def headline_config(world):
     return workload_config(HEADLINE, world)
 
 
+def print_trace(fused, cta: int, dev) -> None:
+    """Prints the event timeline of CTA `cta` over one fused launch of the traced build of
+    the kernel (after two launches of it that warm its code and data in the caches), one
+    event per line: microseconds since the CTA's first event, event, epilogue group or
+    buffer, tile."""
+    from gemm_conv_chains_gb300 import ops
+    fused(0)
+    torch.cuda.synchronize(dev)
+    try:
+        for i in range(3):
+            buf = torch.zeros(2 * (1 << 15), dtype=torch.int64, device=dev)
+            ops.set_trace(buf, cta=cta)
+            fused(0)
+            torch.cuda.synchronize(dev)
+    finally:
+        ops.set_trace(None)
+    for t, e, g, it in ops.read_trace(buf):
+        print(f"{t / 1e3:9.3f} {e:18s} g{g} t{it}")
+    st, _ = ops.get_device_error()
+    if st != 0:
+        raise SystemExit(f"device error {st}")
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     dev = torch.device("cuda", local)
@@ -523,6 +546,9 @@ def run_ours(args):
             raise SystemExit("--batch applies to the conv workloads only")
         w = dataclasses.replace(w, N=args.batch, name=f"{w.name}_n{args.batch}")
     fused, unfused, nsets, set_bytes = runner_for(w, dev)
+    if args.trace is not None:
+        print_trace(fused, args.trace, dev)
+        return
     clocks = ClockSampler(torch.cuda.current_device() if not os.environ.get("CUDA_VISIBLE_DEVICES")
                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     clocks.start()
@@ -688,6 +714,9 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="for profiling: run a conv workload over this many images instead "
                          "of its own N")
+    ap.add_argument("--trace", type=int, default=None, metavar="CTA",
+                    help="for profiling: print the event timeline of this CTA over one launch "
+                         "of the workload instead of timing it")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

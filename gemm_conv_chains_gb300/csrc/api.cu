@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <initializer_list>
@@ -19,6 +20,9 @@
 #include "b2b.h"
 #include "ptx.cuh"
 #include "launch.h"
+
+// The tile-graph model's ranking of a problem's layouts (defined with the plan functions).
+static b2b_status model_top(const std::vector<int64_t>& key, std::vector<int32_t>* top);
 
 namespace b2b {
 namespace {
@@ -253,9 +257,10 @@ uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = fals
 // Shared-memory plan: ring of A (and, when streamed, weight) chunks; resident weights;
 // P tiles; output staging; bias operands; barriers.  The candidates that leave at least two
 // ring stages are feasible, in order of preference -- more tiles in flight, resident
-// weights, separate staging.  By default the first feasible one with three or more stages
-// is taken (else the first feasible one); `forced` >= 0 takes that feasible candidate
-// instead.  Fills p's layout fields.
+// weights, separate staging.  `forced` >= 0 takes that feasible candidate (launches always
+// name one: the tile-graph model's pick, a pinned or a measured choice); without it the
+// first feasible one with three or more stages is taken (else the first feasible one),
+// which only validation uses.  Fills p's layout fields.
 bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_bytes,
                Regions* regions, int forced = -1) {
   const uint32_t budget = kSmemLimit - 1024u;   // 1 KiB slack to align the base to 1024
@@ -512,10 +517,6 @@ bool plan_smem_chain3(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   return *smem_bytes <= kSmemLimit;
 }
 
-// Row tiles (128 rows) from which a chain that fits the CTA-pair kernel runs over CTA
-// pairs by default.
-constexpr int32_t kCta2MinTiles = 512;
-
 // The CTA-pair plan of a b2b GEMM chain with row-major weights (chain_cta2_kernel.cuh): per
 // CTA a ring of 16 KiB A chunks, its halves of W0 and W1 resident (N0 / 2 and N1 / 2
 // columns), the bias operands of its halves and the barriers (no output staging: the
@@ -649,10 +650,11 @@ bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int
   p.num_tiles = ceil_div(M, kBlockM);
   p.stride = 1;
   // A chain with row-major weights may also run over CTA pairs: that plan is one more
-  // feasible layout, after the single-CTA ones, and the default from kCta2MinTiles
-  // 128-row tiles on (measured on the FFN-like chain: 16.7 against 17.8 us at 512 tiles,
-  // 44.6 against 53.0 us at 2048, but 9.8 against 9.3 us at 256 tiles, where the pairs'
-  // longer start -- both weight halves before the first MMA -- is not yet amortised).
+  // feasible layout, after the single-CTA ones (last in the order of preference; the
+  // tile-graph model takes it where its bounds are lower and every pair runs three or
+  // more tiles -- measured on the FFN-like chain: 12.0 against 13.1 us at 40000 rows,
+  // 44.6 against 53.0 us at 262144, but 9.8 against 9.3 us at 32768, two tiles per pair,
+  // where the pairs' longer start is not amortised).
   if (mode == MODE_CHAIN && w_mn) {
     ChainParams q = p;
     size_t qs = 0;
@@ -663,7 +665,7 @@ bool gemm_params(ChainParams& p, int mode, bool w_mn, int64_t M, int32_t K0, int
     size_t cs = 0;
     Regions cr;
     const bool pair_ok = plan_cta2(c, &cs, &cr);
-    if (pair_ok && (forced == nsingle || (forced < 0 && p.num_tiles >= kCta2MinTiles))) {
+    if (pair_ok && forced == nsingle) {
       p = c;
       *smem = cs;
       if (regions) {
@@ -745,6 +747,7 @@ struct Choice {
 // What one launch looked like, for the profiler's enumeration.
 constexpr int kGridModes = 3;
 struct Info {
+  int32_t cand = 0;   // the layout the launch took (the planner's default when not forced)
   int32_t ncand = 0, tiles = 0, can_prefetch = 0;
   int32_t grid[kGridModes] = {0, 0, 0};   // the grid of each mode
 };
@@ -757,9 +760,10 @@ int grid_for(int32_t tiles, int sms, int32_t mode) {
   return std::max(1, (tiles + per - 1) / per);
 }
 
-Info info_for(int32_t ncand, int32_t tiles, int sms, bool can_prefetch) {
+Info info_for(const Regions& r, int32_t tiles, int sms, bool can_prefetch) {
   Info i;
-  i.ncand = ncand;
+  i.cand = r.cand;
+  i.ncand = r.ncand;
   i.tiles = tiles;
   i.can_prefetch = can_prefetch ? 1 : 0;
   for (int m = 0; m < kGridModes; ++m) i.grid[m] = grid_for(tiles, sms, m);
@@ -801,7 +805,7 @@ b2b_status run_cta2(const Choice& ch, Info* info, const Regions& r, ChainParams&
   }
   const int pairs = grid_for(p.num_tiles, clusters, ch.grid);
   p.pf_second = 0;
-  if (info) *info = info_for(r.ncand, p.num_tiles, clusters, true);
+  if (info) *info = info_for(r, p.num_tiles, clusters, true);
   const uint64_t e = 2;
   CUtensorMap ta, tw0, tw1;
   bool ok = make_map(&ta, A, p.is_bf16, 2, {static_cast<uint64_t>(K0), static_cast<uint64_t>(M)},
@@ -842,7 +846,7 @@ b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int 
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = pf_second_for(p.num_tiles, grid, ch.pf2);
   if (r.extend > 0 && (p.num_tiles + grid - 1) / grid <= 2) p.num_stages += r.extend;
-  if (info) *info = info_for(r.ncand, p.num_tiles, d->num_sms, true);
+  if (info) *info = info_for(r, p.num_tiles, d->num_sms, true);
 
   CUtensorMap ta, tw0, tw1, to;
   const uint64_t e = 2;
@@ -926,7 +930,7 @@ b2b_status run_gemm3_with(const Choice& ch, Info* info, int dt, int64_t M, int32
   p.w2 = static_cast<const uint16_t*>(W2);
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = pf_second_for(p.num_tiles, grid, ch.pf2);
-  if (info) *info = info_for(r.ncand, p.num_tiles, d->num_sms, true);
+  if (info) *info = info_for(r, p.num_tiles, d->num_sms, true);
 
   CUtensorMap ta, tw0, tw1, to;
   const uint64_t e = 2;
@@ -981,7 +985,7 @@ b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = 0;   // the implicit-GEMM A has no per-tile contiguous range to prefetch
   if (r.extend > 0 && (p.num_tiles + grid - 1) / grid <= 2) p.num_stages += r.extend;
-  if (info) *info = info_for(r.ncand, p.num_tiles, d->num_sms, false);
+  if (info) *info = info_for(r, p.num_tiles, d->num_sms, false);
   const int32_t Ho = p.Ho, Wo = p.Wo;
 
   const uint64_t e = 2;
@@ -1035,17 +1039,40 @@ b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t
 // light-weight profiler (BOLT notes, "Light-weight performance profiler": a search over
 // launch parameters by timing): per problem, time every launch choice once, keep the fastest
 // ------------------------------------------------------------------------------------
-// Problems are keyed by the entry point and its sizes, as b2b_debug_plan takes them.
+// Problems are keyed by the entry point, its sizes (as b2b_debug_plan takes them) and,
+// last, its variant: the dtype and epilogue kinds, which select different kernel
+// instantiations (kAnyVariant: a choice pinned or ranked for every variant of the sizes).
 using TuneKey = std::vector<int64_t>;
+constexpr int64_t kAnyVariant = -1;
+
+int64_t variant_of(int dt, int e0 = 0, int e1 = 0, int e2 = 0) {
+  return static_cast<int64_t>(dt) | (static_cast<int64_t>(e0) << 4) |
+         (static_cast<int64_t>(e1) << 8) | (static_cast<int64_t>(e2) << 12);
+}
+
+TuneKey any_variant(TuneKey k) {
+  k.back() = kAnyVariant;
+  return k;
+}
+
+// One timed launch choice: the layout, grid mode and the CTAs it gave, the second-tile
+// prefetch (-1: the default rule) and the fastest round's time per launch.
+struct TimedChoice {
+  int32_t cand, grid, ctas, pf2, ns;
+};
 
 struct Tuned {
   Choice c;
-  int32_t source = 0;   // 1 pinned by b2b_set_choice, 2 measured
+  int32_t source = 0;   // 1 pinned by b2b_set_choice, 2 measured, 3 ranked by b2b_set_candidates
   uint32_t best_ns = 0, default_ns = 0, timed = 0;
+  uint64_t seq = 0;                  // order of recording (the most recent wins a wildcard query)
+  std::vector<int32_t> cands;        // source 3: the layouts to time, the first the default
+  std::vector<TimedChoice> record;   // source 2: every choice timed, the default first
 };
 
 std::mutex g_tune_mu;
 std::map<TuneKey, Tuned> g_tuned;
+uint64_t g_tune_seq = 0;
 std::atomic<int> g_autotune{0};
 // Per choice: kTuneWarm untimed launches, then kTuneRounds rounds of kTuneReps launches;
 // a choice's time is its fastest round.  Another choice replaces the default only when
@@ -1053,22 +1080,51 @@ std::atomic<int> g_autotune{0};
 constexpr int kTuneWarm = 2, kTuneReps = 10, kTuneRounds = 3;
 constexpr float kTuneMargin = 0.02f;
 
+// The entry recorded for a call's key: its own variant's, else one for every variant.
+bool find_tuned(const TuneKey& key, Tuned* t) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  auto it = g_tuned.find(key);
+  if (it == g_tuned.end() && key.back() != kAnyVariant) it = g_tuned.find(any_variant(key));
+  if (it == g_tuned.end()) return false;
+  *t = it->second;
+  return true;
+}
+
+// A query for a variant: its own entry, else the one for every variant of its sizes (what
+// its calls take).  A query by sizes alone (kAnyVariant): the most recently recorded entry
+// of those sizes, for every variant or for one.  Caller holds g_tune_mu.
+const Tuned* find_for_query(const TuneKey& key) {
+  if (key.back() != kAnyVariant) {
+    auto it = g_tuned.find(key);
+    if (it == g_tuned.end()) it = g_tuned.find(any_variant(key));
+    return it == g_tuned.end() ? nullptr : &it->second;
+  }
+  const Tuned* best = nullptr;
+  for (auto j = g_tuned.lower_bound(key); j != g_tuned.end(); ++j) {
+    if (!std::equal(key.begin(), key.end() - 1, j->first.begin(), j->first.end() - 1)) break;
+    if (best == nullptr || j->second.seq > best->seq) best = &j->second;
+  }
+  return best;
+}
+
 bool find_choice(const TuneKey& key, Choice* c) {
   std::lock_guard<std::mutex> lk(g_tune_mu);
-  const auto it = g_tuned.find(key);
-  if (it == g_tuned.end()) return false;
-  *c = it->second.c;
+  const Tuned* t = find_for_query(key);
+  if (t == nullptr) return false;
+  *c = t->c;
   return true;
 }
 
 // Times `go(choice)` for the default and for every layout x grid x prefetch choice that
 // differs from it in effect, on the caller's stream (which it synchronises), records the
-// fastest and launches it for the caller.
+// fastest (and every time) under `key` and launches it for the caller.  `cands`, if not
+// empty, restricts the layouts to those (a model's ranking) and makes the first the default.
 template <class Go>
-b2b_status tune(const TuneKey& key, void* stream, Go&& go) {
+b2b_status tune(const TuneKey& key, void* stream, Go&& go, const std::vector<int32_t>& cands) {
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Choice def = cands.empty() ? Choice{} : Choice{cands[0], -1, -1};
   Info info;
-  b2b_status st = go(Choice{}, &info);
+  b2b_status st = go(def, &info);
   if (st != B2B_OK) return st;
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;
   if (cudaEventCreate(&ev0) != cudaSuccess || cudaEventCreate(&ev1) != cudaSuccess) {
@@ -1092,15 +1148,19 @@ b2b_status tune(const TuneKey& key, void* stream, Go&& go) {
     }
     return B2B_OK;
   };
+  std::vector<int32_t> layouts = cands;
+  if (layouts.empty())
+    for (int32_t c = 0; c < info.ncand; ++c) layouts.push_back(c);
   float def_us = 0.f, best_us = 0.f;
-  Choice best;
-  uint32_t timed = 0;
-  st = time_of(Choice{}, &def_us);
+  Choice best = def;
+  std::vector<TimedChoice> record;
+  st = time_of(def, &def_us);
   if (st == B2B_OK) {
     best_us = def_us;
-    timed = 1;
-    for (int32_t cand = 0; cand < info.ncand && st == B2B_OK; ++cand)
+    record.push_back({info.cand, 0, info.grid[0], -1, static_cast<int32_t>(def_us * 1000.f)});
+    for (size_t li = 0; li < layouts.size() && st == B2B_OK; ++li)
       for (int32_t grid = 0; grid < kGridModes && st == B2B_OK; ++grid) {
+        const int32_t cand = layouts[li];
         bool same = false;   // a grid mode that gives an earlier mode's grid is skipped
         for (int m = 0; m < grid; ++m) same = same || info.grid[m] == info.grid[grid];
         if (same) continue;
@@ -1111,7 +1171,7 @@ b2b_status tune(const TuneKey& key, void* stream, Go&& go) {
           float us = 0.f;
           st = time_of(c, &us);
           if (st == B2B_OK) {
-            ++timed;
+            record.push_back({cand, grid, info.grid[grid], c.pf2, static_cast<int32_t>(us * 1000.f)});
             if (us < best_us && us < def_us * (1.f - kTuneMargin)) {
               best = c;
               best_us = us;
@@ -1127,29 +1187,49 @@ b2b_status tune(const TuneKey& key, void* stream, Go&& go) {
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
     Tuned& t = g_tuned[key];
+    t = Tuned{};
     t.c = best;
     t.source = 2;
     t.best_ns = static_cast<uint32_t>(best_us * 1000.f);
     t.default_ns = static_cast<uint32_t>(def_us * 1000.f);
-    t.timed = timed;
+    t.timed = static_cast<uint32_t>(record.size());
+    t.seq = ++g_tune_seq;
+    t.cands = cands;
+    t.record = std::move(record);
   }
   return go(best, nullptr);
 }
 
 // The launch choice of a problem: pinned or measured before, else (with the profiler on,
-// outside stream capture) measured now, else the planner's default.
+// outside stream capture) measured now over the top layouts of a ranking -- the caller's
+// (b2b_set_candidates) or the tile-graph model's -- else that ranking's first layout.
 template <class Go>
 b2b_status dispatch(const TuneKey& key, void* stream, Go&& go) {
-  Choice c;
-  if (find_choice(key, &c)) return go(c, nullptr);
-  if (g_autotune.load() == 0) return go(Choice{}, nullptr);
+  Tuned t;
+  const bool have = find_tuned(key, &t);
+  if (have && t.source != 3) {
+    if (t.c.cand < 0) {   // a pinned grid or prefetch alone: the model's layout
+      std::vector<int32_t> top;
+      if (b2b_status st = model_top(key, &top); st != B2B_OK) return st;
+      t.c.cand = top[0];
+    }
+    return go(t.c, nullptr);
+  }
+  std::vector<int32_t> cands;
+  if (have) {
+    cands = t.cands;
+  } else if (b2b_status st = model_top(key, &cands); st != B2B_OK) {
+    return st;
+  }
+  const Choice c{cands[0], -1, -1};
+  if (g_autotune.load() == 0) return go(c, nullptr);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
     cudaGetLastError();
     return B2B_ERR_CUDA;
   }
-  if (cs != cudaStreamCaptureStatusNone) return go(Choice{}, nullptr);
-  return tune(key, stream, go);
+  if (cs != cudaStreamCaptureStatusNone) return go(c, nullptr);
+  return tune(key, stream, go, cands);
 }
 
 b2b_status run_gemm(const TuneKey& key, int mode, bool w_mn, int dt, int64_t M, int32_t K0,
@@ -1212,7 +1292,7 @@ b2b_status b2b_gemm(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1,
   if (!A || !W0 || !W1 || !D) return B2B_ERR_NULL;
   if (!aligned16(A) || !aligned16(W0) || !aligned16(W1) || !aligned16(D)) return B2B_ERR_ALIGN;
   if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1))) return B2B_ERR_ALIGN;
-  return run_gemm({0, M, K0, N0, N1}, MODE_CHAIN, true, dt, M, K0, N0, N1, A, W0, b0, e0, W1, b1,
+  return run_gemm({0, M, K0, N0, N1, variant_of(dt, e0, e1)}, MODE_CHAIN, true, dt, M, K0, N0, N1, A, W0, b0, e0, W1, b1,
                   e1, D, stream, KID_GEMM_CHAIN);
 }
 
@@ -1235,7 +1315,7 @@ b2b_status b2b_gemm3(b2b_dtype dt, int64_t M, int32_t K0, int32_t N0, int32_t N1
     return B2B_ERR_ALIGN;
   if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1)) || (b2 && !aligned2(b2)))
     return B2B_ERR_ALIGN;
-  return run_gemm3({5, M, K0, N0, N1, N2}, dt, M, K0, N0, N1, N2, A, W0, b0, e0, W1, b1, e1, W2,
+  return run_gemm3({5, M, K0, N0, N1, N2, variant_of(dt, e0, e1, e2)}, dt, M, K0, N0, N1, N2, A, W0, b0, e0, W1, b1, e1, W2,
                    b2, e2, D, stream);
 }
 
@@ -1251,7 +1331,7 @@ b2b_status gemm_bias_act(b2b_dtype dt, int64_t M, int32_t K, int32_t N, const vo
   if (!A || !W || !D) return B2B_ERR_NULL;
   if (!aligned16(A) || !aligned16(W) || !aligned16(D)) return B2B_ERR_ALIGN;
   if (b && !aligned2(b)) return B2B_ERR_ALIGN;
-  return run_gemm({1, M, K, N}, MODE_SINGLE, true, dt, M, K, N, 0, A, W, b, e, nullptr, nullptr, 0,
+  return run_gemm({1, M, K, N, variant_of(dt, e)}, MODE_SINGLE, true, dt, M, K, N, 0, A, W, b, e, nullptr, nullptr, 0,
                   D, stream, KID_GEMM_SINGLE);
 }
 
@@ -1284,7 +1364,7 @@ b2b_status b2b_conv_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_t W, 
   if (!x || !W0 || !W1 || !y) return B2B_ERR_NULL;
   if (!aligned16(x) || !aligned16(W0) || !aligned16(W1) || !aligned16(y)) return B2B_ERR_ALIGN;
   if ((b0 && !aligned2(b0)) || (b1 && !aligned2(b1))) return B2B_ERR_ALIGN;
-  const TuneKey key{2, N, H, W, C, C0, R, S, pad, C1, stride};
+  const TuneKey key{2, N, H, W, C, C0, R, S, pad, C1, stride, variant_of(dt, e0, e1)};
   if (R == 1 && S == 1 && pad == 0 && stride == 1) {
     // A 1x1 conv is a GEMM over the N*H*W pixel rows (interview notes, "Conv
     // optimisation", item 5): run the GEMM-shaped kernel with K-major filters.
@@ -1316,7 +1396,7 @@ b2b_status conv_bias_act_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_
   if (!x || !Wt || !y) return B2B_ERR_NULL;
   if (!aligned16(x) || !aligned16(Wt) || !aligned16(y)) return B2B_ERR_ALIGN;
   if (b && !aligned2(b)) return B2B_ERR_ALIGN;
-  const TuneKey key{3, N, H, W, C, Co, R, S, pad, stride};
+  const TuneKey key{3, N, H, W, C, Co, R, S, pad, stride, variant_of(dt, e)};
   if (R == 1 && S == 1 && pad == 0 && stride == 1) {
     const int64_t M = static_cast<int64_t>(N) * H * W;
     if (M > static_cast<int64_t>(INT32_MAX) - kBlockM) return B2B_ERR_UNSUPPORTED;
@@ -1345,7 +1425,7 @@ b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int3
   if (!x || !Wt || !y) return B2B_ERR_NULL;
   if (!aligned16(x) || !aligned16(Wt) || !aligned16(y)) return B2B_ERR_ALIGN;
   if (b && !aligned2(b)) return B2B_ERR_ALIGN;
-  return run_conv({4, N, H, W, Cin, Cout}, MODE_POOL, dt, N, H, W, Cin, x, Wt, Cout, 3, 3, 1, 1, b,
+  return run_conv({4, N, H, W, Cin, Cout, variant_of(dt)}, MODE_POOL, dt, N, H, W, Cin, x, Wt, Cout, 3, 3, 1, 1, b,
                   B2B_EPI_RELU, nullptr, 0, nullptr, 0, y, stream, KID_CONV_POOL);
 }
 
@@ -1444,30 +1524,57 @@ b2b_status b2b_get_device_error(uint32_t info[4]) {
   return w[0] == ERR_CODE_TIMEOUT ? B2B_ERR_TIMEOUT : B2B_ERR_CUDA;
 }
 
-// Sizes an entry point takes, per kind (b2b_debug_plan's numbering).
+// Sizes an entry point takes, per kind (b2b_debug_plan's numbering), and its epilogue kinds.
 static const int32_t kPlanDims[6] = {4, 3, 9, 8, 5, 5};
+static const int32_t kPlanActs[6] = {2, 1, 2, 1, 0, 3};
+
+static bool plan_is_conv(int32_t kind) { return kind == 2 || kind == 3; }
+
+// Where the optional variant (dtype, then each epilogue kind) starts in dims: after the
+// sizes and, for the convs, the stride (which must then be given).
+static int32_t plan_variant_at(int32_t kind) { return kPlanDims[kind] + (plan_is_conv(kind) ? 1 : 0); }
 
 // The convs (kinds 2 and 3) take an optional stride after their sizes (default 1).
 static int64_t plan_stride(int32_t kind, const int64_t* dims, int32_t ndims) {
-  return ((kind == 2 || kind == 3) && ndims > kPlanDims[kind]) ? dims[kPlanDims[kind]] : 1;
+  return (plan_is_conv(kind) && ndims > kPlanDims[kind]) ? dims[kPlanDims[kind]] : 1;
 }
+
+static bool plan_has_variant(int32_t kind, int32_t ndims) { return ndims > plan_variant_at(kind); }
 
 static b2b_status check_plan_args(int32_t kind, const int64_t* dims, int32_t ndims) {
   if (kind < 0 || kind > 5) return B2B_ERR_UNSUPPORTED;
   if (dims == nullptr) return B2B_ERR_NULL;
-  if (ndims < kPlanDims[kind]) return B2B_ERR_SHAPE;
-  for (int i = 0; i < kPlanDims[kind]; ++i)
+  const int32_t base = kPlanDims[kind], at = plan_variant_at(kind);
+  if (ndims < base) return B2B_ERR_SHAPE;
+  if (ndims > at && ndims != at + 1 + kPlanActs[kind]) return B2B_ERR_SHAPE;
+  for (int i = 0; i < base; ++i)
     if (dims[i] < 0 || dims[i] > INT32_MAX) return B2B_ERR_SHAPE;
   const int64_t st = plan_stride(kind, dims, ndims);
   if (st < 1 || st > INT32_MAX) return B2B_ERR_SHAPE;
+  if (plan_has_variant(kind, ndims)) {
+    if (dims[at] < 0 || dims[at] > 1 || !valid_dtype(static_cast<int>(dims[at])))
+      return B2B_ERR_SHAPE;
+    for (int a = 0; a < kPlanActs[kind]; ++a)
+      if (dims[at + 1 + a] < 0 || dims[at + 1 + a] > 2) return B2B_ERR_SHAPE;
+  }
   return B2B_OK;
 }
 
-// The key the entry point files its launch choice under (the convs' with their stride).
+// The key the entry point files its launch choice under (the convs' with their stride),
+// for the variant dims names, else for every variant.
 static TuneKey plan_key(int32_t kind, const int64_t* dims, int32_t ndims) {
   TuneKey k{kind};
   k.insert(k.end(), dims, dims + kPlanDims[kind]);
-  if (kind == 2 || kind == 3) k.push_back(plan_stride(kind, dims, ndims));
+  if (plan_is_conv(kind)) k.push_back(plan_stride(kind, dims, ndims));
+  if (!plan_has_variant(kind, ndims)) {
+    k.push_back(kAnyVariant);
+    return k;
+  }
+  const int32_t at = plan_variant_at(kind);
+  int e[3] = {0, 0, 0};
+  // conv_relu_maxpool's epilogue is fixed (ReLU), as its entry point files it
+  for (int a = 0; a < kPlanActs[kind]; ++a) e[a] = static_cast<int>(dims[at + 1 + a]);
+  k.push_back(variant_of(static_cast<int>(dims[at]), e[0], e[1], e[2]));
   return k;
 }
 
@@ -1529,19 +1636,281 @@ static b2b_status plan_for_kind(int32_t kind, const int64_t* dims, int32_t ndims
   return ok ? B2B_OK : B2B_ERR_UNSUPPORTED;
 }
 
-b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,
-                          int32_t out_len) {
-  b2b_status st = check_plan_args(kind, dims, ndims);
-  if (st != B2B_OK) return st;
-  if (out == nullptr) return B2B_ERR_NULL;
-  if (out_len < 60) return B2B_ERR_SHAPE;
-  Choice c;
-  find_choice(plan_key(kind, dims, ndims), &c);
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------
+// tile-graph cost model (Welder notes, "Scheduling policy": enumerate candidate tile
+// graphs, keep those within the memory footprint -- here, the planner's feasible layouts --
+// order them by their traffic, and profile only the best few)
+// ------------------------------------------------------------------------------------
+// Per layout, lower bounds in microseconds on one launch from each resource it streams
+// through: HBM (the problem's irreducible bytes over the copy rate), L2 -> SM (the busiest
+// CTA's TMA and bias bytes over one SM's ingress) and the tensor pipe (the busiest CTA's
+// share of the FLOPs over one SM's share of the peak).  Rates measured on the GB300 (copy
+// bandwidth, cuBLAS bf16, one SM's TMA ingress from L2 at 2070 MHz); the model assumes its
+// 152 SMs.  The same model, written for reading, is gemm_conv_chains_gb300/tilegraph.py
+// (`launch_bounds`, `rank`); tests hold the two to the same choices.
+namespace {
+constexpr double kModelHbmGBs = 6791.4, kModelTensorTF = 1951.4, kModelSmMHz = 2070.0;
+constexpr double kModelL2BytesPerClk = 89.0, kModelTol = 0.02;
+constexpr int32_t kModelSms = 152, kModelSteadyTiles = 3, kModelTopK = 3;
+constexpr double kModelABox = 128.0 * 64.0 * 2.0;   // one 128-row x 64-element A box
+
+struct ModelEval {
+  double d[3];        // the three bounds, largest first
+  int32_t n;          // tiles of the busiest CTA (or CTA pair)
+  bool shallow;       // fewer than three ring stages
+};
+
+// The problem's FLOPs, irreducible bytes, bias bytes per CTA, filter rows R and W2 bytes.
+struct ModelProblem {
+  double flops, floor_bytes, bias_cta, w2 = 0.0;
+  int64_t R = 1;
+  int32_t N0 = 0;
+  bool three = false;
+};
+
+ModelProblem model_problem(int32_t kind, const int64_t* d, int32_t ndims) {
+  ModelProblem m;
+  const double e = 2.0;
+  switch (kind) {
+    case 0: {   // M, K0, N0, N1
+      const double M = d[0], K0 = d[1], N0 = d[2], N1 = d[3];
+      m.flops = 2.0 * M * (K0 * N0 + N0 * N1);
+      m.floor_bytes = e * (M * K0 + K0 * N0 + N0 * N1 + M * N1) + (N0 + N1) * e;
+      m.bias_cta = (N0 + N1) * e;
+      m.N0 = static_cast<int32_t>(d[2]);
+      break;
+    }
+    case 1: {   // M, K, N
+      const double M = d[0], K = d[1], N = d[2];
+      m.flops = 2.0 * M * (K * N);
+      m.floor_bytes = e * (M * K + K * N + N + M * N);
+      m.bias_cta = N * e;
+      m.N0 = static_cast<int32_t>(d[2]);
+      break;
+    }
+    case 2:
+    case 3: {   // N, H, W, C, C0, R, S, pad[, C1][, stride]
+      const int64_t st = plan_stride(kind, d, ndims);
+      const int64_t Ho = std::max<int64_t>(0, (d[1] + 2 * d[7] - d[5]) / st + 1);
+      const int64_t Wo = std::max<int64_t>(0, (d[2] + 2 * d[7] - d[6]) / st + 1);
+      const double M = static_cast<double>(d[0] * Ho * Wo);
+      const double C = d[3], C0 = d[4], RS = static_cast<double>(d[5] * d[6]);
+      const double C1 = kind == 2 ? static_cast<double>(d[8]) : 0.0;
+      const double x = static_cast<double>(d[0] * d[1] * d[2]) * C;
+      m.flops = 2.0 * M * (RS * C * C0 + C0 * C1);
+      m.floor_bytes = kind == 2 ? e * (x + C0 * RS * C + C0 + C1 * C0 + C1 + M * C1)
+                                : e * (x + C0 * RS * C + C0 + M * C0);
+      m.bias_cta = (C0 + C1) * e;
+      m.R = d[5];
+      m.N0 = static_cast<int32_t>(d[4]);
+      break;
+    }
+    case 4: {   // N, H, W, Cin, Cout
+      const double N = d[0], H = d[1], W = d[2], Cin = d[3], Cout = d[4];
+      m.flops = 2.0 * N * H * W * 9.0 * Cin * Cout;
+      m.floor_bytes = e * (N * H * W * Cin + Cout * 9.0 * Cin + Cout +
+                           N * static_cast<double>(d[1] / 2) * static_cast<double>(d[2] / 2) * Cout);
+      m.bias_cta = Cout * e;
+      m.R = 3;
+      m.N0 = static_cast<int32_t>(d[4]);
+      break;
+    }
+    default: {  // 5: M, K0, N0, N1, N2
+      const double M = d[0], K0 = d[1], N0 = d[2], N1 = d[3], N2 = d[4];
+      m.flops = 2.0 * M * (K0 * N0 + N0 * N1 + N1 * N2);
+      m.floor_bytes = e * (M * K0 + K0 * N0 + N0 * N1 + N1 * N2 + N0 + N1 + N2 + M * N2);
+      m.bias_cta = (N0 + N1 + N2) * e;
+      m.w2 = N1 * N2 * e;
+      m.three = true;
+      m.N0 = static_cast<int32_t>(d[2]);
+      break;
+    }
+  }
+  return m;
+}
+
+bool model_eval(int32_t kind, const int64_t* dims, int32_t ndims, int cand, ModelEval* out) {
   ChainParams p;
   Regions r;
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
-  if ((st = plan_for_kind(kind, dims, ndims, c.cand, p, r, smem, mode)) != B2B_OK) return st;
+  if (plan_for_kind(kind, dims, ndims, cand, p, r, smem, mode) != B2B_OK) return false;
+  out->shallow = p.num_stages < 3u;
+  if (p.num_tiles <= 0) {   // no work: nothing to order by
+    out->d[0] = out->d[1] = out->d[2] = 0.0;
+    out->n = 0;
+    return true;
+  }
+  const ModelProblem m = model_problem(kind, dims, ndims);
+  const double tiles = static_cast<double>(p.num_tiles);
+  const double hbm = m.floor_bytes / (kModelHbmGBs * 1e3);
+  double cta_bytes = 0.0, tensor = 0.0;
+  int64_t n = 0;
+  if (p.cta_pair) {
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(p.num_tiles, kModelSms / 2));
+    n = (p.num_tiles + grid - 1) / grid;
+    const double ctas = 2.0 * static_cast<double>(grid);
+    const double A = tiles * 2.0 * p.kchunks0 * kModelABox;
+    const double W0 = ctas * p.kchunks0 * p.w0_chunk_bytes;
+    const double W1 = ctas * p.kchunks1 * p.w1_chunk_bytes;
+    const double bias = ctas * (p.N0p / 2 + p.N1p / 2) * 2.0;
+    cta_bytes = A / (2.0 * tiles) * static_cast<double>(n) + (W0 + W1 + bias) / ctas;
+    tensor = m.flops / (2.0 * tiles) * static_cast<double>(n) / (kModelTensorTF * 1e6 / kModelSms);
+  } else {
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(p.num_tiles, kModelSms));
+    const int64_t q = p.num_tiles / grid, rem = p.num_tiles % grid;
+    n = q + (rem > 0 ? 1 : 0);
+    const double ctas = static_cast<double>(grid);
+    // W1 loads when grouped: once per pair of each CTA's tiles
+    const double loads = static_cast<double>(rem * ((q + 2) / 2) + (grid - rem) * ((q + 1) / 2));
+    double a_tile = p.halo ? static_cast<double>(p.kchunks0 / m.R) * p.a_stage_bytes
+                           : p.kchunks0 * kModelABox;
+    double w0 = static_cast<double>(p.kchunks0) * p.w0_chunk_bytes;
+    if (p.p_split) {
+      a_tile *= 2.0;
+      const int32_t n0blk = (p.N0p + 63) / 64;
+      const double hi = m.N0 % 64 == 0 ? static_cast<double>(p.w0_chunk_bytes) : (n0blk - 4) * 8192.0;
+      w0 = p.kchunks0 * (p.w0_chunk_bytes + hi);
+    }
+    const double A = tiles * a_tile;
+    const double w1 = static_cast<double>(p.kchunks1) * p.w1_chunk_bytes;
+    const double bias = ctas * m.bias_cta;
+    const double W2 = m.three ? ctas * m.w2 : 0.0;
+    const double nn = static_cast<double>(n);
+    cta_bytes = A / tiles * nn + bias / ctas + W2 / ctas;
+    // W0: once per CTA when resident (alone or with W1), else once per tile
+    const double W0 = (p.resident || m.three || p.w0_res) ? ctas * w0 : tiles * w0;
+    cta_bytes += (p.resident || m.three || p.w0_res) ? W0 / ctas : W0 / tiles * nn;
+    if (w1 != 0.0 || p.w0_res || m.three) {
+      if (p.resident || m.three) {
+        cta_bytes += (ctas * w1) / ctas;
+      } else if (p.w1_group) {
+        cta_bytes += (loads * w1) / loads * static_cast<double>((n + 1) / 2);
+      } else {
+        cta_bytes += (tiles * w1) / tiles * nn;
+      }
+    }
+    tensor = m.flops / tiles * nn / (kModelTensorTF * 1e6 / kModelSms);
+  }
+  const double l2 = cta_bytes / (kModelL2BytesPerClk * kModelSmMHz);
+  double d[3] = {hbm, l2, tensor};
+  std::sort(d, d + 3, [](double a, double b) { return a > b; });
+  std::memcpy(out->d, d, sizeof(d));
+  out->n = static_cast<int32_t>(n);
+  return true;
+}
+
+// Whether the model orders x and y by their bounds (both in the steady state, and some
+// bound differs by more than the tolerance); *sign < 0 if x is better.
+bool model_orders(const ModelEval& x, const ModelEval& y, int* sign) {
+  if (std::min(x.n, y.n) < kModelSteadyTiles) return false;
+  for (int j = 0; j < 3; ++j) {
+    const double a = x.d[j], b = y.d[j];
+    if (std::fabs(a - b) > kModelTol * std::max(a, b)) {
+      *sign = a < b ? -1 : 1;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Steady state (both plans give their busiest CTA kModelSteadyTiles or more tiles): the
+// bounds describe the launch, so the lower demand wins, resource by resource from the
+// binding one.  Otherwise, or on a tie, the planner's order of preference stands (more
+// tiles in flight, resident weights, separate staging; rings of three or more stages
+// first): below the steady state a launch is mostly pipeline fill and drain, which the
+// bounds do not see.
+int model_compare(const ModelEval& x, int xi, const ModelEval& y, int yi) {
+  int sign = 0;
+  if (model_orders(x, y, &sign)) return sign;
+  if (x.shallow != y.shallow) return x.shallow ? 1 : -1;
+  return (xi > yi) - (xi < yi);
+}
+
+// Every feasible layout of a problem, best first.
+b2b_status model_ranking(int32_t kind, const int64_t* dims, int32_t ndims,
+                         std::vector<int32_t>* ranked) {
+  ChainParams p;
+  Regions r;
+  size_t smem = 0;
+  int32_t mode = MODE_CHAIN;
+  if (b2b_status st = plan_for_kind(kind, dims, ndims, 0, p, r, smem, mode); st != B2B_OK)
+    return st;
+  std::vector<int32_t> left;
+  std::vector<ModelEval> ev;
+  for (int32_t c = 0; c < r.ncand; ++c) {
+    ModelEval e;
+    if (!model_eval(kind, dims, ndims, c, &e)) return B2B_ERR_UNSUPPORTED;
+    left.push_back(c);
+    ev.push_back(e);
+  }
+  ranked->clear();
+  while (!left.empty()) {
+    size_t best = 0;
+    for (size_t i = 1; i < left.size(); ++i)
+      if (model_compare(ev[i], left[i], ev[best], left[best]) < 0) best = i;
+    ranked->push_back(left[best]);
+    left.erase(left.begin() + static_cast<std::ptrdiff_t>(best));
+    ev.erase(ev.begin() + static_cast<std::ptrdiff_t>(best));
+  }
+  return B2B_OK;
+}
+
+std::mutex g_model_mu;
+std::map<std::vector<int64_t>, std::vector<int32_t>> g_model_top;   // by sizes
+}  // namespace
+
+// The top layouts of the model's ranking for a call's key (kind, sizes, variant): the best
+// kModelTopK, then every later one the bounds do not order against the last of them (the
+// model cannot tell those apart, so the profiler should).  Ranks by repeated selection of
+// the best remaining layout, in the planner's order.
+static b2b_status model_top(const std::vector<int64_t>& key, std::vector<int32_t>* top) {
+  std::vector<int64_t> sizes(key.begin(), key.end() - 1);
+  {
+    std::lock_guard<std::mutex> lk(g_model_mu);
+    const auto it = g_model_top.find(sizes);
+    if (it != g_model_top.end()) {
+      *top = it->second;
+      return B2B_OK;
+    }
+  }
+  const int32_t kind = static_cast<int32_t>(sizes[0]);
+  const int64_t* dims = sizes.data() + 1;
+  const int32_t ndims = static_cast<int32_t>(sizes.size()) - 1;
+  std::vector<int32_t> ranked;
+  if (b2b_status st = model_ranking(kind, dims, ndims, &ranked); st != B2B_OK) return st;
+  std::vector<ModelEval> ev(ranked.size());
+  for (size_t i = 0; i < ranked.size(); ++i) model_eval(kind, dims, ndims, ranked[i], &ev[i]);
+  std::vector<int32_t> out;
+  for (size_t i = 0; i < ranked.size(); ++i) {
+    int sign = 0;
+    if (static_cast<int>(i) >= kModelTopK &&
+        model_orders(ev[kModelTopK - 1], ev[i], &sign))
+      break;
+    out.push_back(ranked[i]);
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_model_mu);
+    g_model_top[sizes] = out;
+  }
+  *top = std::move(out);
+  return B2B_OK;
+}
+
+extern "C" {
+
+static b2b_status debug_plan_with(int32_t kind, const int64_t* dims, int32_t ndims, int forced,
+                                  const Choice& c, uint32_t* out, int32_t out_len) {
+  if (out == nullptr) return B2B_ERR_NULL;
+  if (out_len < 60) return B2B_ERR_SHAPE;
+  ChainParams p;
+  Regions r;
+  size_t smem = 0;
+  int32_t mode = MODE_CHAIN;
+  if (b2b_status st = plan_for_kind(kind, dims, ndims, forced, p, r, smem, mode); st != B2B_OK)
+    return st;
   const uint32_t v[60] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
@@ -1564,6 +1933,28 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
   return B2B_OK;
 }
 
+b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,
+                          int32_t out_len) {
+  b2b_status st = check_plan_args(kind, dims, ndims);
+  if (st != B2B_OK) return st;
+  const TuneKey key = plan_key(kind, dims, ndims);
+  Choice c;
+  if (!find_choice(key, &c) || c.cand < 0) {
+    std::vector<int32_t> top;
+    if ((st = model_top(key, &top)) != B2B_OK) return st;
+    c.cand = top[0];
+  }
+  return debug_plan_with(kind, dims, ndims, c.cand, c, out, out_len);
+}
+
+b2b_status b2b_debug_plan_candidate(int32_t kind, const int64_t* dims, int32_t ndims,
+                                    int32_t cand, uint32_t* out, int32_t out_len) {
+  b2b_status st = check_plan_args(kind, dims, ndims);
+  if (st != B2B_OK) return st;
+  if (cand < 0) return B2B_ERR_SHAPE;
+  return debug_plan_with(kind, dims, ndims, cand, Choice{cand, -1, -1}, out, out_len);
+}
+
 b2b_status b2b_set_choice(int32_t kind, const int64_t* dims, int32_t ndims, int32_t cand,
                           int32_t grid, int32_t prefetch_second) {
   b2b_status st = check_plan_args(kind, dims, ndims);
@@ -1580,6 +1971,7 @@ b2b_status b2b_set_choice(int32_t kind, const int64_t* dims, int32_t ndims, int3
   t = Tuned{};
   t.c = Choice{cand, grid, prefetch_second};
   t.source = 1;
+  t.seq = ++g_tune_seq;
   return B2B_OK;
 }
 
@@ -1592,12 +1984,57 @@ b2b_status b2b_get_choice(int32_t kind, const int64_t* dims, int32_t ndims, int3
   Tuned t;
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
-    const auto it = g_tuned.find(plan_key(kind, dims, ndims));
-    if (it != g_tuned.end()) t = it->second;
+    if (const Tuned* f = find_for_query(plan_key(kind, dims, ndims))) t = *f;
   }
   const int32_t v[7] = {t.source, t.c.cand, t.c.grid, t.c.pf2, static_cast<int32_t>(t.best_ns),
                         static_cast<int32_t>(t.default_ns), static_cast<int32_t>(t.timed)};
   std::memcpy(out, v, sizeof(v));
+  return B2B_OK;
+}
+
+b2b_status b2b_set_candidates(int32_t kind, const int64_t* dims, int32_t ndims,
+                              const int32_t* cands, int32_t n) {
+  b2b_status st = check_plan_args(kind, dims, ndims);
+  if (st != B2B_OK) return st;
+  if (cands == nullptr) return B2B_ERR_NULL;
+  if (n < 1 || n > 64) return B2B_ERR_SHAPE;
+  std::vector<int32_t> list;
+  for (int32_t i = 0; i < n; ++i) {
+    if (cands[i] < 0) return B2B_ERR_SHAPE;
+    for (int32_t c : list)
+      if (c == cands[i]) return B2B_ERR_SHAPE;
+    ChainParams p;
+    Regions r;
+    size_t smem = 0;
+    int32_t mode = MODE_CHAIN;
+    if ((st = plan_for_kind(kind, dims, ndims, cands[i], p, r, smem, mode)) != B2B_OK) return st;
+    list.push_back(cands[i]);
+  }
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  Tuned& t = g_tuned[plan_key(kind, dims, ndims)];
+  t = Tuned{};
+  t.c = Choice{list[0], -1, -1};
+  t.source = 3;
+  t.seq = ++g_tune_seq;
+  t.cands = std::move(list);
+  return B2B_OK;
+}
+
+b2b_status b2b_get_tune_record(int32_t kind, const int64_t* dims, int32_t ndims, int32_t* out,
+                               int32_t max_rows, int32_t* rows) {
+  b2b_status st = check_plan_args(kind, dims, ndims);
+  if (st != B2B_OK) return st;
+  if (rows == nullptr || (out == nullptr && max_rows > 0)) return B2B_ERR_NULL;
+  if (max_rows < 0) return B2B_ERR_SHAPE;
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  const Tuned* t = find_for_query(plan_key(kind, dims, ndims));
+  const int32_t total = t ? static_cast<int32_t>(t->record.size()) : 0;
+  *rows = total;
+  for (int32_t i = 0; i < total && i < max_rows; ++i) {
+    const TimedChoice& c = t->record[static_cast<size_t>(i)];
+    const int32_t v[5] = {c.cand, c.grid, c.ctas, c.pf2, c.ns};
+    std::memcpy(out + 5 * i, v, sizeof(v));
+  }
   return B2B_OK;
 }
 

@@ -90,6 +90,16 @@ def lib() -> ctypes.CDLL:
         L.b2b_set_choice.restype = ci
         L.b2b_get_choice.argtypes = [i32, p64, i32, ctypes.POINTER(i32), i32]
         L.b2b_get_choice.restype = ci
+        L.b2b_debug_plan.argtypes = [i32, p64, i32, ctypes.POINTER(ctypes.c_uint32), i32]
+        L.b2b_debug_plan.restype = ci
+        L.b2b_debug_plan_candidate.argtypes = [i32, p64, i32, i32, ctypes.POINTER(ctypes.c_uint32),
+                                               i32]
+        L.b2b_debug_plan_candidate.restype = ci
+        L.b2b_set_candidates.argtypes = [i32, p64, i32, ctypes.POINTER(i32), i32]
+        L.b2b_set_candidates.restype = ci
+        L.b2b_get_tune_record.argtypes = [i32, p64, i32, ctypes.POINTER(i32), i32,
+                                          ctypes.POINTER(i32)]
+        L.b2b_get_tune_record.restype = ci
         _lib = L
         return L
 
@@ -403,13 +413,33 @@ PLAN_KINDS = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_
               "conv_relu_maxpool": 4, "b2b_gemm3": 5}
 
 
-def debug_plan(kind: str, dims) -> dict:
+def _dims(dims):
+    return (ctypes.c_int64 * len(dims))(*[int(d) for d in dims])
+
+
+def variant(dtype, *acts) -> list:
+    """The trailing dims that name a call's variant for the plan and choice functions:
+    the dtype code (torch.float16 / torch.bfloat16 or "f16" / "bf16"), then each epilogue
+    kind.  Append it to the sizes (for the convs, after the stride)."""
+    codes = {torch.float16: 0, torch.bfloat16: 1, "f16": 0, "bf16": 1}
+    if dtype not in codes:
+        raise TypeError(f"expected float16 or bfloat16, got {dtype!r}")
+    return [codes[dtype]] + [_epi(a) for a in acts]
+
+
+def debug_plan(kind: str, dims, cand: Optional[int] = None) -> dict:
     """The launch plan the entry point `kind` would use for `dims` (b2b_debug_plan; no CUDA
-    call).  Raises B2BError with the entry point's status if it would not launch."""
-    arr = (ctypes.c_int64 * len(dims))(*[int(d) for d in dims])
+    call), or, with `cand`, the plan of that feasible layout candidate whatever is pinned
+    (b2b_debug_plan_candidate).  Raises B2BError with the entry point's status if it would
+    not launch."""
+    arr = _dims(dims)
     out = (ctypes.c_uint32 * len(PLAN_FIELDS))()
-    _raise(lib().b2b_debug_plan(PLAN_KINDS[kind], arr, len(dims), out, len(PLAN_FIELDS)),
-           "b2b_debug_plan")
+    if cand is None:
+        _raise(lib().b2b_debug_plan(PLAN_KINDS[kind], arr, len(dims), out, len(PLAN_FIELDS)),
+               "b2b_debug_plan")
+    else:
+        _raise(lib().b2b_debug_plan_candidate(PLAN_KINDS[kind], arr, len(dims), int(cand), out,
+                                              len(PLAN_FIELDS)), "b2b_debug_plan_candidate")
     plan = dict(zip(PLAN_FIELDS, [int(v) for v in out]))
     for k in _SIGNED_PLAN_FIELDS:
         plan[k] = ctypes.c_int32(plan[k]).value
@@ -435,6 +465,29 @@ def set_choice(kind: str, dims, cand: int = -1, grid: int = -1, prefetch_second:
     arr = (ctypes.c_int64 * len(dims))(*[int(d) for d in dims])
     _raise(lib().b2b_set_choice(PLAN_KINDS[kind], arr, len(dims), int(cand), int(grid),
                                 int(prefetch_second)), "b2b_set_choice")
+
+
+def set_candidates(kind: str, dims, cands) -> None:
+    """Hands the profiler a ranked list of layouts for `dims` (b2b_set_candidates): the
+    first becomes the default, and the profiler times only these."""
+    c = [int(x) for x in cands]
+    arr = (ctypes.c_int32 * len(c))(*c)
+    _raise(lib().b2b_set_candidates(PLAN_KINDS[kind], _dims(dims), len(dims), arr, len(c)),
+           "b2b_set_candidates")
+
+
+def tune_record(kind: str, dims) -> list:
+    """Every launch choice the profiler timed for `dims`, the default first
+    (b2b_get_tune_record): dicts of cand, grid (mode), ctas, prefetch_second, ns."""
+    L, arr, n = lib(), _dims(dims), ctypes.c_int32(0)
+    _raise(L.b2b_get_tune_record(PLAN_KINDS[kind], arr, len(dims), None, 0, ctypes.byref(n)),
+           "b2b_get_tune_record")
+    rows = n.value
+    out = (ctypes.c_int32 * max(1, 5 * rows))()
+    _raise(L.b2b_get_tune_record(PLAN_KINDS[kind], arr, len(dims), out, rows, ctypes.byref(n)),
+           "b2b_get_tune_record")
+    keys = ("cand", "grid", "ctas", "prefetch_second", "ns")
+    return [dict(zip(keys, [int(v) for v in out[5 * i:5 * i + 5]])) for i in range(min(rows, n.value))]
 
 
 def get_choice(kind: str, dims) -> dict:

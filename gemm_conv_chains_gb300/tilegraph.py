@@ -12,6 +12,12 @@ loads move from L2 into the SMs for a given launch plan (`ops.debug_plan`; whole
 out-of-bounds fill included), and
 `smem_footprint` a best-fit allocation of buffers by lifetime.  Predictions are compared
 with the ncu counters of the same launches in the profile summaries.
+
+Welder notes, "Scheduling policy": the model also chooses.  `rank` enumerates the layouts
+the planner finds feasible for a problem (`ops.debug_plan(..., cand=i)`), drops those over
+the shared-memory / TMEM footprint, and orders the rest by their launch bounds; `choose`
+hands the top k to the light-weight profiler (`ops.set_candidates`), which times only those
+and keeps the fastest.
 """
 from __future__ import annotations
 
@@ -83,14 +89,7 @@ def dram_traffic(w, fused: bool = True) -> int:
 def plan_of(w) -> dict:
     """The C planner's launch plan for a workload."""
     from . import ops
-    if isinstance(w, wl.GemmChain):
-        return ops.debug_plan("b2b_gemm", (w.M, w.K0, w.N0, w.N1))
-    if isinstance(w, wl.GemmChain3):
-        return ops.debug_plan("b2b_gemm3", (w.M, w.K0, w.N0, w.N1, w.N2))
-    if isinstance(w, wl.ConvChain):
-        return ops.debug_plan("b2b_conv_nhwc", (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1,
-                                                w.stride))
-    return ops.debug_plan("conv_relu_maxpool", (w.N, w.H, w.W, w.Cin, w.Cout))
+    return ops.debug_plan(*problem_of(w))
 
 
 def tiles_per_cta(num_tiles: int, num_sms: int) -> List[int]:
@@ -378,6 +377,186 @@ def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
     out["bound"] = max(out, key=out.get)[:-3]
     out["floor_us"] = max(out["hbm_us"], out["l2_us"], out["tensor_us"])
     return out
+
+
+# ------------------------------------------------------------------------------------
+# choosing: enumerate, check the footprint, rank, hand the top candidates to the profiler
+# ------------------------------------------------------------------------------------
+SMEM_LIMIT = 227 * 1024     # dynamic shared memory per CTA
+TMEM_COLS = 512             # TMEM columns per SM
+RANK_TOL = 0.02             # bounds closer than this (relative) count as equal
+STEADY_TILES = 3            # tiles per CTA (or pair) from which the bounds rank layouts
+
+
+@dataclasses.dataclass(frozen=True)
+class GemmSingle(wl.GemmChain):
+    """One GEMM + bias + activation (gemm_bias_act) in the chain's terms: N1 = 0, and the
+    output is the M x N0 product."""
+
+    @property
+    def floor_bytes(self) -> int:
+        return 2 * (self.M * self.K0 + self.K0 * self.N0 + self.N0 + self.M * self.N0)
+
+
+@dataclasses.dataclass(frozen=True)
+class ConvSingle(wl.ConvChain):
+    """One conv + bias + activation (conv_bias_act_nhwc) in the chain's terms: C1 = 0, and
+    the output is the M x C0 conv."""
+
+    @property
+    def floor_bytes(self) -> int:
+        return 2 * (self.N * self.H * self.W * self.C + self.C0 * self.R * self.S * self.C
+                    + self.C0 + self.M * self.C0)
+
+
+def problem_of(w) -> Tuple[str, Tuple[int, ...]]:
+    """The entry point and sizes (as the plan functions take them) of a workload."""
+    if isinstance(w, GemmSingle):
+        return "gemm_bias_act", (w.M, w.K0, w.N0)
+    if isinstance(w, ConvSingle):
+        return "conv_bias_act_nhwc", (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.stride)
+    if isinstance(w, wl.GemmChain):
+        return "b2b_gemm", (w.M, w.K0, w.N0, w.N1)
+    if isinstance(w, wl.GemmChain3):
+        return "b2b_gemm3", (w.M, w.K0, w.N0, w.N1, w.N2)
+    if isinstance(w, wl.ConvChain):
+        return "b2b_conv_nhwc", (w.N, w.H, w.W, w.C, w.C0, w.R, w.S, w.pad, w.C1, w.stride)
+    return "conv_relu_maxpool", (w.N, w.H, w.W, w.Cin, w.Cout)
+
+
+def workload_of(kind: str, dims) -> object:
+    """The model's view of a problem given as an entry point and its sizes (the inverse of
+    problem_of; dtype and epilogues do not enter the model)."""
+    d = [int(x) for x in dims]
+    if kind == "b2b_gemm":
+        return wl.GemmChain("problem", "bf16", *d[:4], "none", "none")
+    if kind == "gemm_bias_act":
+        return GemmSingle("problem", "bf16", d[0], d[1], d[2], 0, "none", "none")
+    if kind == "b2b_gemm3":
+        return wl.GemmChain3("problem", "bf16", *d[:5], "none", "none", "none")
+    if kind == "b2b_conv_nhwc":
+        return wl.ConvChain("problem", "bf16", *d[:9], "none", "none",
+                            stride=d[9] if len(d) > 9 else 1)
+    if kind == "conv_bias_act_nhwc":
+        return ConvSingle("problem", "bf16", *d[:8], 0, "none", "none",
+                          stride=d[8] if len(d) > 8 else 1)
+    if kind == "conv_relu_maxpool":
+        return wl.ConvPool("problem", "bf16", *d[:5])
+    raise ValueError(kind)
+
+
+def fits(plan: dict) -> bool:
+    """The footprint check of a candidate: its buffers' best-fit extent (plus the 1 KiB
+    the kernel adds to align its base) within the shared memory of a CTA, and its
+    accumulators within the SM's TMEM."""
+    return smem_footprint(plan) + 1024 <= SMEM_LIMIT and plan["tmem_cols"] <= TMEM_COLS
+
+
+@dataclasses.dataclass
+class Candidate:
+    cand: int                    # layout index, as b2b_debug_plan_candidate numbers it
+    plan: dict
+    bounds: Dict[str, float]     # launch_bounds of the plan
+    tiles_per_unit: int          # tiles of the busiest CTA (or CTA pair)
+
+    @property
+    def demand(self) -> List[float]:
+        """The three per-resource bounds, largest first."""
+        return sorted((self.bounds["hbm_us"], self.bounds["l2_us"], self.bounds["tensor_us"]),
+                      reverse=True)
+
+    @property
+    def shallow(self) -> bool:
+        """Fewer than three ring stages: a load cannot be in flight beside the two stages
+        the MMAs and the producer hold."""
+        return self.plan["stages"] < 3
+
+
+def orders(x: Candidate, y: Candidate) -> int:
+    """-1 or 1 if the bounds order x before or after y, 0 if they do not: below the steady
+    state (some CTA of either plan with fewer than STEADY_TILES tiles) the launch is mostly
+    pipeline fill and drain, which the bounds do not see; in it, the lower demand wins,
+    resource by resource from the binding one, bounds within RANK_TOL tying."""
+    if min(x.tiles_per_unit, y.tiles_per_unit) < STEADY_TILES:
+        return 0
+    for a, b in zip(x.demand, y.demand):
+        if abs(a - b) > RANK_TOL * max(a, b):
+            return -1 if a < b else 1
+    return 0
+
+
+def compare(x: Candidate, y: Candidate) -> int:
+    """The model's order: the bounds where they decide, else the planner's order of
+    preference (more tiles in flight, resident weights, separate staging; rings of three
+    or more stages before shallower ones)."""
+    o = orders(x, y)
+    if o:
+        return o
+    if x.shallow != y.shallow:
+        return 1 if x.shallow else -1
+    return (x.cand > y.cand) - (x.cand < y.cand)
+
+
+def candidates(w, num_sms: int = 152) -> List[Candidate]:
+    """Every layout the planner finds feasible for the workload, with its plan, bounds and
+    tiles per CTA, in the planner's order; candidates over the footprint are dropped."""
+    from . import ops
+    kind, dims = problem_of(w)
+    n = ops.debug_plan(kind, dims, cand=0)["ncand"]
+    out = []
+    for c in range(n):
+        plan = ops.debug_plan(kind, dims, cand=c)
+        if not fits(plan):
+            continue
+        units = num_sms // 2 if plan.get("cta_pair") else num_sms
+        if plan["tiles"] == 0:
+            b = {"hbm_us": 0.0, "l2_us": 0.0, "tensor_us": 0.0, "floor_us": 0.0, "bound": "hbm"}
+            out.append(Candidate(c, plan, b, 0))
+            continue
+        out.append(Candidate(c, plan, launch_bounds(w, plan, num_sms=num_sms),
+                             max(tiles_per_cta(plan["tiles"], units))))
+    return out
+
+
+def rank(w, num_sms: int = 152) -> List[Candidate]:
+    """The feasible layouts of a workload, best first (Welder notes, "Scheduling policy":
+    candidates that pass the memory-footprint check are ordered by the cost model).  The
+    order is built by repeatedly taking the best remaining candidate, scanning in the
+    planner's order (`compare` may tie two candidates that a third separates)."""
+    left = candidates(w, num_sms)
+    out = []
+    while left:
+        best = 0
+        for i in range(1, len(left)):
+            if compare(left[i], left[best]) < 0:
+                best = i
+        out.append(left.pop(best))
+    return out
+
+
+def top(w, k: int = 3, num_sms: int = 152) -> List[Candidate]:
+    """The model's best k layouts, and every later one the bounds do not order against the
+    k-th (the model cannot tell those apart, so the profiler should)."""
+    r = rank(w, num_sms)
+    out = r[:k]
+    for c in r[k:]:
+        if orders(r[k - 1], c) != 0:
+            break
+        out.append(c)
+    return out
+
+
+def choose(w, k: int = 3, variant: Optional[Sequence[int]] = None) -> List[int]:
+    """Hands the model's top layouts to the profiler (b2b_set_candidates): the first
+    becomes the default of calls with these sizes (of one variant, if given:
+    ops.variant(...)), and the profiler, when on, times only these.  The library ranks the
+    same way by itself; this makes the choice explicit, or narrower with a smaller k.
+    Returns the layout indices handed over."""
+    from . import ops
+    kind, dims = problem_of(w)
+    cands = [c.cand for c in top(w, k)]
+    ops.set_candidates(kind, list(dims) + list(variant or ()), cands)
+    return cands
 
 
 def bounds_report(measured_us: Optional[Dict[str, float]] = None) -> str:

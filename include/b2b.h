@@ -245,6 +245,12 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  *   kind 3 conv_bias_act_nhwc  dims = {N, H, W, C, Co, R, S, pad[, stride]}
  *   kind 4 conv_relu_maxpool   dims = {N, H, W, Cin, Cout}
  *   kind 5 b2b_gemm3           dims = {M, K0, N0, N1, N2}
+ * The sizes may be followed (for the convs, after the stride, which must then be given) by
+ * the call's variant: its dtype (b2b_dtype), then each of its epilogue kinds (b2b_epilogue:
+ * e0, e1 for kinds 0 and 2, e for 1 and 3, e0, e1, e2 for 5, none for 4).  Launch choices are
+ * filed per variant, since each dtype and epilogue pair runs its own kernel instantiation;
+ * sizes alone address every variant (see b2b_set_choice).  Any other count of dims, or a
+ * variant value out of range, returns B2B_ERR_SHAPE.
  * out (out_len >= 60) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
  * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
@@ -268,12 +274,22 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * else 0), and 1 if W0 alone stays resident while A and W1 stream through the ring (P in
  * TMEM, tile pairs; the output is then stored from registers, with no staging tile), and
  * 1 if the chain runs over CTA pairs (clusters of two CTAs sharing each MMA of 256 rows,
- * each holding half of W0 and W1; tiles then count 256 rows).  A choice pinned or
- * measured for these sizes is reflected.
+ * each holding half of W0 and W1; tiles then count 256 rows).  A choice pinned,
+ * measured or ranked for these sizes is reflected; without one, the layout is the
+ * tile-graph model's pick, as the entry point takes it (see b2b_set_autotune).
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
  * launch). */
 b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint32_t* out,
                           int32_t out_len);
+
+/* As b2b_debug_plan, with the layout forced to feasible candidate `cand` (0 = the
+ * planner's most preferred) whatever is pinned or measured: the plan each candidate
+ * would make, for a host-side model to rank (Welder notes, "Scheduling policy": candidate
+ * tile graphs are enumerated, checked against the memory footprint and ranked by their
+ * traffic before any is profiled).  B2B_ERR_UNSUPPORTED if cand is not feasible,
+ * B2B_ERR_SHAPE if it is negative. */
+b2b_status b2b_debug_plan_candidate(int32_t kind, const int64_t* dims, int32_t ndims,
+                                    int32_t cand, uint32_t* out, int32_t out_len);
 
 /* Launch choices and the light-weight profiler (BOLT notes, "Light-weight performance
  * profiler" under "Automating templated code generation": a profiler picks among
@@ -282,7 +298,20 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
  * roundings: results are bit-identical, except that an R x S conv (R > 1) sums its taps
  * in another fp32 order when its filters are resident (halo loads) than when they are
  * streamed).
- * A problem is an entry point (kind, as for b2b_debug_plan) and its sizes (dims).  Its
+ * The default layout of a problem is the pick of a tile-graph cost model (Welder notes,
+ * "Scheduling policy": candidates are ordered by their traffic before any is profiled):
+ * for each feasible layout it bounds the launch from below by HBM (the problem's
+ * irreducible bytes), L2 -> SM (the busiest CTA's loads) and the tensor pipe (the busiest
+ * CTA's MMAs).  Where every CTA of the compared plans runs three or more tiles, the plan
+ * with the lower bounds wins, resource by resource from the binding one (within 2 % they
+ * tie); otherwise, or on a tie, the planner's order of preference decides (more tiles in
+ * flight, resident weights, separate staging, rings of three or more stages first).  The
+ * profiler times the model's best three layouts and every later one the bounds do not
+ * order against the third.
+ * A problem is an entry point (kind, as for b2b_debug_plan), its sizes and its variant
+ * (dtype and epilogue kinds; dims as for b2b_debug_plan).  A call looks up its own
+ * variant's choice first, then one recorded for the sizes alone; the profiler files what
+ * it measures under the call's variant.  Its
  * launch may vary: the shared-memory / TMEM layout (cand: an index into the feasible
  * layouts, 0 = most preferred), the grid (0: one CTA per SM, or per tile when there are
  * fewer tiles; 1: the fewest CTAs that give no CTA more tiles than grid 0 does; 2: one
@@ -291,7 +320,8 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
  * (prefetch_second 0/1; 2-D A operands only).  -1 leaves a field to the default.
  *
  * b2b_set_autotune(1): from then on, the first call of an entry point for a problem with
- * no pinned or measured choice times the default and every choice (2 warm-up launches,
+ * no pinned or measured choice times the default and every choice over the ranked
+ * layouts (2 warm-up launches,
  * then the fastest of 3 rounds of 10, CUDA events on the caller's stream, which it
  * synchronises; the outputs are overwritten with the same values each time; the inputs
  * are the caller's, so a problem smaller than L2 is timed with its inputs in L2), keeps
@@ -303,17 +333,43 @@ b2b_status b2b_debug_plan(int32_t kind, const int64_t* dims, int32_t ndims, uint
 void b2b_set_autotune(int32_t on);
 void b2b_autotune_reset(void);
 
-/* Pins a launch choice for a problem (no CUDA call).  B2B_ERR_UNSUPPORTED if cand is not
+/* Pins a launch choice for a problem (no CUDA call); dims without a variant pin it for
+ * every dtype and epilogue of those sizes.  B2B_ERR_UNSUPPORTED if cand is not
  * a feasible layout for these sizes, B2B_ERR_SHAPE for a field out of range, otherwise the
  * status b2b_debug_plan would return. */
 b2b_status b2b_set_choice(int32_t kind, const int64_t* dims, int32_t ndims, int32_t cand,
                           int32_t grid, int32_t prefetch_second);
 
 /* The choice recorded for a problem (no CUDA call): out (out_len >= 7) = {source (0 none,
- * 1 pinned, 2 measured), cand, grid, prefetch_second, fastest time in ns, default's time
- * in ns, choices timed} (times 0 unless measured). */
+ * 1 pinned, 2 measured, 3 ranked by b2b_set_candidates and not yet measured), cand, grid,
+ * prefetch_second, fastest time in ns, default's time in ns, choices timed} (times 0
+ * unless measured).  dims with a variant read that variant's entry, else the one pinned for
+ * its sizes alone (the choice its calls take); dims without one read the most recently
+ * recorded entry of those sizes, for every variant or for one. */
 b2b_status b2b_get_choice(int32_t kind, const int64_t* dims, int32_t ndims, int32_t* out,
                           int32_t out_len);
+
+/* Hands the profiler a model's ranking of layouts for a problem (no CUDA call; Welder
+ * notes, "Scheduling policy": the cost model keeps the top candidates and hardware
+ * profiling picks among them).  cands (n in [1, 64], distinct feasible layout indices as
+ * b2b_debug_plan_candidate numbers them) replaces any pinned or measured choice of the
+ * problem: calls launch cands[0] with the default grid and prefetch, and with the profiler
+ * on, the first call times only these layouts (each with every grid and prefetch choice),
+ * cands[0] standing as the default that another must beat by the profiler's margin.
+ * B2B_ERR_SHAPE (n out of range, a negative or repeated index), B2B_ERR_NULL,
+ * B2B_ERR_UNSUPPORTED (an infeasible index), otherwise the status of b2b_debug_plan. */
+b2b_status b2b_set_candidates(int32_t kind, const int64_t* dims, int32_t ndims,
+                              const int32_t* cands, int32_t n);
+
+/* Why the profiler chose what it chose (no CUDA call): every launch choice it timed for a
+ * problem, the default first, as rows of five int32 in out (room for max_rows rows):
+ * {layout index, grid mode, CTAs launched (clusters for CTA pairs), prefetch_second (-1:
+ * the default rule), fastest round's time per launch in ns}.  *rows receives the number of
+ * rows recorded (0 unless measured), which may exceed max_rows.  dims as for
+ * b2b_get_choice.  B2B_ERR_NULL (rows NULL, or out NULL with max_rows > 0),
+ * B2B_ERR_SHAPE (max_rows < 0). */
+b2b_status b2b_get_tune_record(int32_t kind, const int64_t* dims, int32_t ndims, int32_t* out,
+                               int32_t max_rows, int32_t* rows);
 
 #ifdef __cplusplus
 }

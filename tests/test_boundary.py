@@ -36,7 +36,8 @@ def test_header_declares_the_entry_points():
     for n in ("b2b_gemm", "b2b_conv_nhwc", "conv_relu_maxpool", "gemm_bias_act",
               "conv_bias_act_nhwc", "maxpool2x2_nhwc", "b2b_status_str", "b2b_get_device_error",
               "b2b_conv_nhwc_strided", "conv_bias_act_nhwc_strided", "b2b_set_autotune",
-              "b2b_set_choice", "b2b_get_choice", "b2b_fold_batchnorm", "b2b_gemm3"):
+              "b2b_set_choice", "b2b_get_choice", "b2b_fold_batchnorm", "b2b_gemm3",
+              "b2b_debug_plan_candidate", "b2b_set_candidates", "b2b_get_tune_record"):
         assert n in names
 
 

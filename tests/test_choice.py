@@ -7,6 +7,7 @@ reflected by b2b_debug_plan, and infeasible or out-of-range choices must be refu
 import pytest
 
 from gemm_conv_chains_gb300 import ops
+from gemm_conv_chains_gb300 import tilegraph as tg
 from test_plan import check
 
 PROBLEMS = [
@@ -46,9 +47,8 @@ def test_every_feasible_layout_is_a_valid_plan(kind, dims):
         p = check(kind, dims, _row_major(kind, dims))
         assert p["cand"] == cand and p["ncand"] == n
         stages.append(p["stages"])
-    # the default is the first feasible layout with three or more ring stages, else the first
-    first3 = next((i for i, s in enumerate(stages) if s >= 3), 0)
-    assert default["cand"] == first3
+    # the default is the tile-graph model's pick
+    assert default["cand"] == tg.rank(tg.workload_of(kind, dims))[0].cand
     assert all(s >= 2 for s in stages)
 
 
@@ -84,3 +84,79 @@ def test_pinned_choice_is_recorded_and_reset():
 def test_autotune_switch_needs_no_device():
     ops.set_autotune(True)
     ops.set_autotune(False)
+
+
+def test_plan_of_a_forced_candidate_ignores_the_pinned_choice():
+    kind, dims = "b2b_gemm", (32768, 256, 256, 128)
+    n = ops.debug_plan(kind, dims)["ncand"]
+    ops.set_choice(kind, dims, cand=n - 1)
+    for cand in range(n):
+        p = ops.debug_plan(kind, dims, cand=cand)
+        assert p["cand"] == cand and p["grid_choice"] == -1
+    with pytest.raises(ops.B2BError) as e:
+        ops.debug_plan(kind, dims, cand=n)
+    assert e.value.status == 4
+    with pytest.raises(ops.B2BError) as e:
+        ops.debug_plan(kind, dims, cand=-1)
+    assert e.value.status == 2
+
+
+def test_choices_are_filed_per_dtype_and_epilogue():
+    """A choice pinned for one dtype / epilogue pair applies to that variant only; sizes
+    alone pin it for every variant, and a variant's own entry takes precedence."""
+    kind, dims = "b2b_gemm", (4096, 128, 128, 64)
+    bf16_hs = list(dims) + ops.variant("bf16", "hardswish", "hardswish")
+    f16_relu = list(dims) + ops.variant("f16", "relu", "relu")
+    default = ops.debug_plan(kind, dims)["cand"]
+    assert default != 1
+    ops.set_choice(kind, bf16_hs, cand=1)
+    assert ops.get_choice(kind, bf16_hs)["cand"] == 1
+    assert ops.get_choice(kind, f16_relu)["source"] == 0
+    assert ops.debug_plan(kind, bf16_hs)["cand"] == 1
+    assert ops.debug_plan(kind, f16_relu)["cand"] == default
+    # a query by sizes alone reads the most recent entry of any variant
+    assert ops.get_choice(kind, dims)["cand"] == 1
+    ops.set_choice(kind, f16_relu, cand=2)
+    assert ops.get_choice(kind, dims)["cand"] == 2
+    # sizes alone: a wildcard entry, which variants without their own entry fall back to
+    ops.set_choice(kind, dims, cand=3)
+    assert ops.get_choice(kind, dims)["cand"] == 3
+    assert ops.get_choice(kind, bf16_hs)["cand"] == 1
+    other = list(dims) + ops.variant("bf16", "relu", "none")
+    # a variant with no entry of its own takes the wildcard's
+    assert ops.get_choice(kind, other)["cand"] == ops.debug_plan(kind, other)["cand"] == 3
+
+
+@pytest.mark.parametrize("kind,dims,nv", [
+    ("b2b_gemm", (1024, 64, 64, 64), 3), ("gemm_bias_act", (513, 256, 256), 2),
+    ("b2b_conv_nhwc", (2, 9, 9, 64, 64, 3, 3, 1, 64, 1), 3),
+    ("conv_bias_act_nhwc", (2, 9, 9, 64, 64, 3, 3, 1, 1), 2),
+    ("conv_relu_maxpool", (1, 7, 9, 16, 8), 1), ("b2b_gemm3", (1024, 64, 64, 64, 64), 4)])
+def test_variant_dims_are_checked(kind, dims, nv):
+    good = list(dims) + [1] + [2] * (nv - 1)
+    ops.set_choice(kind, good, cand=0)
+    assert ops.get_choice(kind, good)["source"] == 1
+    for bad in (good[:-1] if nv > 1 else None, good + [0], good[:len(dims)] + [2] + good[len(dims) + 1:],
+                good[:len(dims) + 1] + [3] * (nv - 1) if nv > 1 else None):
+        if bad is None:
+            continue
+        with pytest.raises(ops.B2BError) as e:
+            ops.debug_plan(kind, bad)
+        assert e.value.status == 2, bad
+
+
+def test_model_ranking_sets_the_default_and_is_recorded():
+    kind, dims = "b2b_gemm", (32768, 256, 256, 128)
+    n = ops.debug_plan(kind, dims)["ncand"]
+    ops.set_candidates(kind, dims, [n - 1, 0])
+    c = ops.get_choice(kind, dims)
+    assert (c["source"], c["cand"], c["grid"]) == (3, n - 1, -1)
+    assert ops.debug_plan(kind, dims)["cand"] == n - 1
+    assert ops.tune_record(kind, dims) == []              # nothing measured yet
+    for bad, status in (([], 2), ([0, 0], 2), ([-1], 2), ([n], 4)):
+        with pytest.raises(ops.B2BError) as e:
+            ops.set_candidates(kind, dims, bad)
+        assert e.value.status == status
+    # pinning replaces the ranking
+    ops.set_choice(kind, dims, cand=0)
+    assert ops.get_choice(kind, dims)["source"] == 1

@@ -122,18 +122,19 @@ def test_b2b_gemm_narrow_four_buffers_sampled_rows(integer):
 @pytest.mark.parametrize("streamed", [False, True])
 @pytest.mark.parametrize("integer", [True, False])
 def test_b2b_gemm_wide_streamed_pairs_sampled_rows(integer, streamed):
-    # K0 = 256: by default both weights stream (W0 with every tile's A chunks); with
-    # `streamed` False the next layout is pinned, which keeps W0 (128 KiB) resident and
-    # streams A and W1 through the ring, the output leaving from registers.  3 x SMs + 1
-    # tiles give CTA 0 two tile pairs, the second with one ragged tile.
+    # K0 = 256, single CTAs with P in TMEM: with `streamed` both weights stream (W0 with
+    # every tile's A chunks); else W0 (128 KiB) stays resident and A and W1 stream through
+    # the ring, the output leaving from registers.  Both layouts are pinned (the model
+    # takes CTA pairs at this size).  3 x SMs + 1 tiles give CTA 0 two tile pairs, the
+    # second with one ragged tile.
     nsm = ops.num_sms()
     M = 128 * nsm * 3 + 77
     dims = (M, 256, 256, 128)
-    plan = ops.debug_plan("b2b_gemm", dims)
-    assert plan["w0_res"] == 0 and plan["cta_pair"] == 0
-    if not streamed:
-        ops.set_choice("b2b_gemm", dims, cand=plan["cand"] + 1)
-        assert ops.debug_plan("b2b_gemm", dims)["w0_res"] == 1
+    n = ops.debug_plan("b2b_gemm", dims, cand=0)["ncand"]
+    want = dict(p_tmem=1, resident=0, cta_pair=0, w0_res=0 if streamed else 1)
+    cand = next(c for c in range(n)
+                if all(ops.debug_plan("b2b_gemm", dims, cand=c)[k] == v for k, v in want.items()))
+    ops.set_choice("b2b_gemm", dims, cand=cand)
     try:
         acts = ("relu", "none") if integer else ("hardswish", "hardswish")   # exact: no fractions
         w = wl.GemmChain("spairs", "bf16", M, 256, 256, 128, *acts)
@@ -148,17 +149,26 @@ def test_b2b_gemm_wide_streamed_pairs_sampled_rows(integer, streamed):
 
 @pytest.mark.parametrize("integer", [True, False])
 def test_b2b_gemm_wide_many_pairs_sampled_rows(integer):
-    # N0 = 256 keeps P in TMEM and processes tiles in pairs; with 5 x SMs + 1 tiles, CTA 0
-    # runs three pairs (W1 reloaded into the output staging between them, the last pair
-    # with one ragged tile).  Rows of every tile of CTA 0 plus a random sample.
+    # N0 = 256 keeps P in TMEM and processes tiles in pairs on single CTAs (pinned: the
+    # model takes CTA pairs at this size); with 5 x SMs + 1 tiles, CTA 0 runs three pairs,
+    # the last with one ragged tile.  Rows of every tile of CTA 0 plus a random sample.
     nsm = ops.num_sms()
     M = 128 * nsm * 5 + 77
-    acts = ("relu", "none") if integer else ("hardswish", "relu")   # exact: no fractions
-    w = wl.GemmChain("pairs", "bf16", M, 64, 256, 128, *acts)
-    rng = np.random.default_rng(5)
-    cta0 = np.concatenate([np.arange(128 * t, min(128 * t + 128, M)) for t in range(0, 5 * nsm + 1, nsm)])
-    rows = np.unique(np.concatenate([cta0, rng.choice(M, 512, replace=False)]))
-    run_b2b_gemm(w, seed=11, integer=integer, rows=rows)
+    dims = (M, 64, 256, 128)
+    n = ops.debug_plan("b2b_gemm", dims, cand=0)["ncand"]
+    cand = next(c for c in range(n) if ops.debug_plan("b2b_gemm", dims, cand=c)["p_tmem"] == 1
+                and ops.debug_plan("b2b_gemm", dims, cand=c)["cta_pair"] == 0)
+    ops.set_choice("b2b_gemm", dims, cand=cand)
+    try:
+        acts = ("relu", "none") if integer else ("hardswish", "relu")   # exact: no fractions
+        w = wl.GemmChain("pairs", "bf16", M, 64, 256, 128, *acts)
+        rng = np.random.default_rng(5)
+        cta0 = np.concatenate([np.arange(128 * t, min(128 * t + 128, M))
+                               for t in range(0, 5 * nsm + 1, nsm)])
+        rows = np.unique(np.concatenate([cta0, rng.choice(M, 512, replace=False)]))
+        run_b2b_gemm(w, seed=11, integer=integer, rows=rows)
+    finally:
+        ops.autotune_reset()
 
 
 # ------------------------------------------------------------------------------------

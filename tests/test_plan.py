@@ -289,9 +289,10 @@ def test_ffn_plan_keeps_p_in_tmem():
 
 
 def test_large_chains_default_to_cta_pairs():
-    # from 512 row tiles on, a chain the CTA-pair kernel takes runs over CTA pairs by
-    # default (tiles then count 256 rows); below, over single CTAs
-    for M, pair in ((511 * 128, False), (511 * 128 + 1, True), (262144, True), (32768, False)):
+    # the tile-graph model takes CTA pairs (lower L2 -> SM bounds) once every CTA and every
+    # pair runs three or more tiles -- past 152 x 256 rows on the 152 SMs (tiles then count
+    # 256 rows); below, the planner's preference keeps single CTAs
+    for M, pair in ((152 * 256, False), (152 * 256 + 1, True), (262144, True), (32768, False)):
         p = check("b2b_gemm", (M, 256, 256, 128), True)
         assert p["cta_pair"] == int(pair), M
         assert p["tiles"] == -(-M // (256 if pair else 128))

@@ -162,3 +162,97 @@ def test_read_ncu_raw_csv(tmp_path):
     assert d["launch__grid_size"] == 152 and "Kernel Name" not in d
     table = tg.report({"gemm_ffn": str(p)})
     assert "| gemm_ffn |" in table and "60.410 | 1.000 | 60.410 | 1.000" in table
+
+
+# ------------------------------------------------------------------------------------
+# choosing: the model ranks the planner's layouts and its pick is the library's default
+# ------------------------------------------------------------------------------------
+MODEL_PROBLEMS = [
+    ("b2b_gemm", (32768, 256, 256, 128)), ("b2b_gemm", (262144, 256, 256, 128)),
+    ("b2b_gemm", (40000, 256, 256, 128)), ("b2b_gemm", (40000, 64, 256, 128)),
+    ("b2b_gemm", (200000, 256, 256, 64)), ("b2b_gemm", (1024, 64, 64, 64)),
+    ("b2b_gemm", (640, 128, 128, 256)), ("b2b_gemm", (300, 128, 256, 64)),
+    ("b2b_gemm", (257, 72, 40, 24)), ("b2b_gemm", (32768, 256, 512, 128)),
+    ("gemm_bias_act", (513, 256, 256)), ("gemm_bias_act", (300000, 64, 64)),
+    ("b2b_conv_nhwc", (64, 56, 56, 64, 64, 1, 1, 0, 64)),
+    ("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128)),
+    ("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128, 2)),
+    ("b2b_conv_nhwc", (1, 10, 12, 32, 32, 5, 5, 2, 16)),
+    ("conv_bias_act_nhwc", (2, 9, 9, 64, 64, 3, 3, 1)),
+    ("conv_bias_act_nhwc", (64, 28, 28, 128, 64, 3, 3, 1, 2)),
+    ("conv_relu_maxpool", (32, 112, 112, 64, 64)), ("conv_relu_maxpool", (1, 7, 9, 16, 8)),
+    ("b2b_gemm3", (40000, 128, 128, 64, 64)), ("b2b_gemm3", (262144, 64, 64, 64, 64)),
+]
+
+
+@pytest.fixture
+def _no_choices():
+    ops.autotune_reset()
+    yield
+    ops.autotune_reset()
+
+
+def test_pair_and_streamed_bounds_by_hand():
+    # FFN at 262144 rows.  CTA pairs: 1024 tiles of 256 rows on 76 pairs, the busiest with
+    # 14; per SM its 128 rows of each tile's A (64 KiB per tile), its halves of W0 (64 KiB)
+    # and W1 (32 KiB) once, its bias halves (128 + 64 elements).  Single CTAs, W0 streamed:
+    # 2048 tiles on 152 CTAs, the busiest with 14: A and W0 (128 KiB) per tile, W1 (64 KiB)
+    # once per pair of tiles, both biases.  One SM moves 89 B/clk at 2070 MHz.
+    w = wl.GEMM_FFN_LARGE
+    rate = 89.0 * 2070.0                       # bytes per microsecond
+    by_cand = {c.cand: c for c in tg.candidates(w)}
+    pair = by_cand[4]
+    assert pair.plan["cta_pair"] == 1 and pair.tiles_per_unit == 14
+    assert pair.bounds["l2_us"] == pytest.approx((14 * 65536 + 65536 + 32768 + 384) / rate)
+    streamed = by_cand[0]
+    assert streamed.plan["resident"] == 0 and streamed.plan["w0_res"] == 0
+    assert streamed.tiles_per_unit == 14
+    assert streamed.bounds["l2_us"] == pytest.approx(
+        (14 * 65536 + 14 * 131072 + 7 * 65536 + 768) / rate)
+    # HBM: 768 B per row (A in, output out) and the weights and biases once
+    assert pair.bounds["hbm_us"] == pytest.approx((262144 * 768 + 197376) / 6791.4e3)
+
+
+@pytest.mark.parametrize("kind,dims", MODEL_PROBLEMS, ids=lambda x: str(x))
+def test_model_pick_is_the_library_default(kind, dims, _no_choices):
+    """The library ranks layouts with its own copy of the model (C); both must pick the
+    same layout, and every layout the planner offers must pass the model's footprint
+    check."""
+    w = tg.workload_of(kind, dims)
+    ranked = tg.rank(w)
+    n = ops.debug_plan(kind, dims, cand=0)["ncand"]
+    assert sorted(c.cand for c in ranked) == list(range(n))       # none over the footprint
+    assert ops.debug_plan(kind, dims)["cand"] == ranked[0].cand
+
+
+def test_every_workload_defaults_to_the_model_pick(_no_choices):
+    for name, w in wl.WORKLOADS.items():
+        assert tg.plan_of(w)["cand"] == tg.rank(w)[0].cand, name
+
+
+def test_pairs_only_in_the_steady_state(_no_choices):
+    # two tiles per CTA (32768 rows): the bounds do not decide, the planner's preference
+    # (single CTAs, P in TMEM, streamed weights) does; three or more (past 152 x 256 rows):
+    # the pairs' lower L2 -> SM bound wins
+    assert tg.rank(wl.GEMM_FFN)[0].plan["cta_pair"] == 0
+    assert tg.rank(wl.GEMM_FFN.with_m(152 * 256 + 1))[0].plan["cta_pair"] == 1
+    assert tg.rank(wl.GEMM_FFN_LARGE)[0].plan["cta_pair"] == 1
+
+
+def test_top_extends_over_what_the_model_cannot_order(_no_choices):
+    # one tile per CTA: no layout is ordered by the bounds, so the profiler gets them all
+    small = tg.top(wl.GEMM_SMALL)
+    assert [c.cand for c in small] == [c.cand for c in tg.rank(wl.GEMM_SMALL)]
+    # steady state with distinct bounds: exactly the best three
+    large = tg.top(wl.GEMM_FFN_LARGE)
+    assert len(large) == 3 and large[0].plan["cta_pair"] == 1
+
+
+def test_choose_hands_the_top_to_the_profiler(_no_choices):
+    w = wl.GEMM_FFN_LARGE
+    kind, dims = tg.problem_of(w)
+    got = tg.choose(w, k=2)
+    assert got == [c.cand for c in tg.rank(w)[:2]]
+    c = ops.get_choice(kind, dims)
+    assert (c["source"], c["cand"]) == (3, got[0])
+    assert ops.debug_plan(kind, dims)["cand"] == got[0]
