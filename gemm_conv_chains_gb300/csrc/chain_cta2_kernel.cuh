@@ -371,13 +371,18 @@ __device__ void cta2_epilogue(const ChainParams& p, uint32_t bars, uint32_t tmem
                          SITE_EPI_D1_FULL, it);
     if (elected) trace(EV_EPI_D1_READY, g, it);
     tc_fence_after_sync();
-    if (alive)   // warp-uniform: the drain's TMEM loads and shuffles are warp-collective
-      drain64_to_global<BF16>(p.act1, tm_lane, p.d1_col[b], p.N1p, p.out_ptr, m0 + q * 32, p.M,
-                              p.out_ld, p.N1, lane);
-    // every TMEM load of the tile is done: the buffer (D0 -> P + D1) may take tile it + 2
-    tc_fence_before_sync();
-    __syncwarp();
-    if (lane == 0) report(PB_ACC_EMPTY0 + b);
+    // The buffer (D0 -> P + D1) may take tile it + 2 as soon as the last TMEM load of the
+    // tile has completed: the drain reports to the leader's ACC_EMPTY then, before it
+    // converts and stores those columns from registers.
+    if (alive) {   // warp-uniform: the drain's TMEM loads and shuffles are warp-collective
+      drain64_release_to_global<BF16>(p.act1, tm_lane, p.d1_col[b], p.N1p, p.out_ptr,
+                                      m0 + q * 32, p.M, p.out_ld, p.N1, lane,
+                                      leader_bar(PB_ACC_EMPTY0 + b));
+    } else {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) report(PB_ACC_EMPTY0 + b);
+    }
     if (elected) trace(EV_EPI_DRAINED, g, it);
     if (elected) trace(EV_EPI_STORED, g, it);
   }

@@ -1199,37 +1199,139 @@ template <bool BF16, int ACT>
 __device__ __noinline__ void drain64_to_global_act(uint32_t tm_lane, uint32_t col0, int ncols,
                                                       uint8_t* out, int64_t out_row0,
                                                       int64_t rows, int ld, int nvalid,
-                                                      int lane) {
+                                                      int lane);
+
+// Ties 64 more registers, loaded by tcgen05.ld before a tmem_wait_ld64 that has returned,
+// to that wait (so that none of their uses is scheduled before it).
+__device__ __forceinline__ void tmem_tie64(uint32_t (&r)[64]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+  asm volatile(""
+               : "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]),
+                 "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]),
+                 "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]),
+                 "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]),
+                 "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]),
+                 "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
+}
+
+// 64 loaded accumulator columns (registers r) -> act -> dtype: 32 packed pairs.
+template <bool BF16, int ACT>
+__device__ __forceinline__ void pack64(const uint32_t (&r)[64], uint32_t (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    v[j] = pack2<BF16, ACT == 1>(act_fn<ACT>(__uint_as_float(r[2 * j])),
+                                 act_fn<ACT>(__uint_as_float(r[2 * j + 1])));
+}
+
+// 64 packed output columns of this lane's row (v; output columns from col_base) -> global
+// memory: after quad_transpose_units each store instruction of the warp writes eight rows'
+// 64 contiguous bytes.
+__device__ __forceinline__ void store_packed64(const uint32_t (&v)[32], int col_base, uint8_t* out,
+                                               int64_t out_row0, int64_t rows, int ld,
+                                               int nvalid, int lane) {
   const int quad = lane >> 2, unit = lane & 3;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {        // 32 columns: units of 8 columns, 4 per row
+    uint32_t x[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[u][k] = v[16 * h + 4 * u + k];
+    quad_transpose_units(x, lane);
+    const int col = col_base + 32 * h + 8 * unit;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t row = out_row0 + 4 * quad + j;
+      if (row < rows && col < nvalid)
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(
+                         out + (static_cast<size_t>(row) * static_cast<size_t>(ld) +
+                                static_cast<size_t>(col)) * 2u),
+                     "r"(x[j][0]), "r"(x[j][1]), "r"(x[j][2]), "r"(x[j][3])
+                     : "memory");
+    }
+  }
+}
+
+template <bool BF16, int ACT>
+__device__ __forceinline__ void store64_to_global(const uint32_t (&r)[64], int col_base,
+                                                  uint8_t* out, int64_t out_row0, int64_t rows,
+                                                  int ld, int nvalid, int lane) {
+  uint32_t v[32];
+  pack64<BF16, ACT>(r, v);
+  store_packed64(v, col_base, out, out_row0, rows, ld, nvalid, lane);
+}
+
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain64_to_global_act(uint32_t tm_lane, uint32_t col0, int ncols,
+                                                      uint8_t* out, int64_t out_row0,
+                                                      int64_t rows, int ld, int nvalid,
+                                                      int lane) {
   for (int c = 0; c < ncols; c += 64) {
     uint32_t r[64];
     tmem_ld64x(tm_lane + col0 + c, r);
     tmem_wait_ld64(r);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {        // 32 columns: units of 8 columns, 4 per row
-      uint32_t x[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int o = 32 * h + 8 * u;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          x[u][k] = pack2<BF16, ACT == 1>(act_fn<ACT>(__uint_as_float(r[o + 2 * k])),
-                                           act_fn<ACT>(__uint_as_float(r[o + 2 * k + 1])));
-      }
-      quad_transpose_units(x, lane);
-      const int col = c + 32 * h + 8 * unit;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t row = out_row0 + 4 * quad + j;
-        if (row < rows && col < nvalid)
-          asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(
-                           out + (static_cast<size_t>(row) * static_cast<size_t>(ld) +
-                                  static_cast<size_t>(col)) * 2u),
-                       "r"(x[j][0]), "r"(x[j][1]), "r"(x[j][2]), "r"(x[j][3])
-                       : "memory");
-      }
-    }
+    store64_to_global<BF16, ACT>(r, c, out, out_row0, rows, ld, nvalid, lane);
   }
+}
+
+// As drain64_to_global_act, releasing the accumulator early: the last 128 columns (ncols a
+// multiple of 64, at least 128) are loaded from TMEM together, and once that load has
+// completed -- before any of them is converted or stored -- the warp's lane 0 arrives on
+// `release` (a barrier address in the cluster's shared window; the caller's barrier
+// counts one arrive per warp) after `tcgen05.fence::before_thread_sync`.  The MMA issuer
+// may then overwrite the columns while this warp finishes its stores from registers.
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain64_release_to_global_act(uint32_t tm_lane, uint32_t col0,
+                                                           int ncols, uint8_t* out,
+                                                           int64_t out_row0, int64_t rows, int ld,
+                                                           int nvalid, int lane,
+                                                           uint32_t release) {
+  const int head = ncols - 128;   // columns drained before the last 128
+  for (int c = 0; c < head; c += 64) {
+    uint32_t r[64];
+    tmem_ld64x(tm_lane + col0 + c, r);
+    tmem_wait_ld64(r);
+    store64_to_global<BF16, ACT>(r, c, out, out_row0, rows, ld, nvalid, lane);
+  }
+  uint32_t r0[64], r1[64];
+  tmem_ld64x(tm_lane + col0 + head, r0);
+  tmem_ld64x(tm_lane + col0 + head + 64, r1);
+  tmem_wait_ld64(r0);
+  tmem_tie64(r1);
+  tc_fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_remote(release);
+  uint32_t v0[32], v1[32];
+  pack64<BF16, ACT>(r0, v0);
+  pack64<BF16, ACT>(r1, v1);
+  store_packed64(v0, head, out, out_row0, rows, ld, nvalid, lane);
+  store_packed64(v1, head + 64, out, out_row0, rows, ld, nvalid, lane);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void drain64_release_to_global(int act, uint32_t tm_lane,
+                                                          uint32_t col0, int ncols, uint8_t* out,
+                                                          int64_t out_row0, int64_t rows, int ld,
+                                                          int nvalid, int lane, uint32_t release) {
+  if (act == 2)
+    drain64_release_to_global_act<BF16, 2>(tm_lane, col0, ncols, out, out_row0, rows, ld, nvalid,
+                                           lane, release);
+  else if (act == 1)
+    drain64_release_to_global_act<BF16, 1>(tm_lane, col0, ncols, out, out_row0, rows, ld, nvalid,
+                                           lane, release);
+  else
+    drain64_release_to_global_act<BF16, 0>(tm_lane, col0, ncols, out, out_row0, rows, ld, nvalid,
+                                           lane, release);
 }
 
 template <bool BF16>
