@@ -525,6 +525,8 @@ bool plan_smem_chain3(ChainParams& p, size_t* smem_bytes, Regions* regions) {
 // False when the chain is outside the kernel's limits (N0 or N1 not a multiple of 128,
 // more than kMaxW0Chunks K chunks, the TMEM layout over 512 columns, fewer than three ring
 // stages beside the weights).
+constexpr uint32_t kCta2StagingBytes = 8u * 4096u;   // 32 rows x 64 columns per epilogue warp
+
 bool plan_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   if (p.N0p % 128 != 0 || p.N1p % 128 != 0 || p.N0p > 256 || p.N1p > 256) return false;
   if (p.kchunks0 > kMaxW0Chunks || p.kchunks0 < 1) return false;
@@ -538,7 +540,13 @@ bool plan_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   const uint32_t bar_bytes = 1024u;
   const uint32_t fixed = w0b + w1b + bias_bytes + bar_bytes;
   if (fixed >= budget) return false;
-  const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / kABytes);
+  // The output leaves through a 4 KiB staging slot per epilogue warp and TMA stores when
+  // the ring keeps five stages beside it (measured on the FFN-like chain: five stages run
+  // as fast as seven, four do not); else from registers.
+  const bool stage_out = fixed + kCta2StagingBytes < budget &&
+                         (budget - fixed - kCta2StagingBytes) / kABytes >= 5u;
+  const uint32_t staging = stage_out ? kCta2StagingBytes : 0u;
+  const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed - staging) / kABytes);
   if (stages < 3u) return false;
   p.tmem_cols = tmem_layout(p, MODE_CHAIN, 2u, true);
   if (p.tmem_cols > 512u) return false;
@@ -565,7 +573,12 @@ bool plan_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   p.off_w1 = off + w0b;
   off += w0b + w1b;
   for (uint32_t b = 0; b < kMaxBufs; ++b) p.off_p[b] = 0;
-  p.off_out[0] = p.off_out[1] = 0;   // no staging: the output leaves from registers
+  p.off_out[0] = p.off_out[1] = 0;
+  p.out_stage = stage_out ? 1 : 0;
+  if (stage_out) {
+    p.off_out[0] = off;
+    off += staging;
+  }
   p.off_bias = off;
   off += bias_bytes;
   p.off_bar = off;
@@ -575,7 +588,7 @@ bool plan_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
     r.ring = stages * kABytes;
     r.w_res = w0b + w1b;
     r.p_each = 0;
-    r.out_each = 0;
+    r.out_each = staging;
     r.bias = bias_bytes;
     r.bar = bar_bytes;
     *regions = r;
@@ -824,8 +837,13 @@ b2b_status run_cta2(const Choice& ch, Info* info, const Regions& r, ChainParams&
   p.pf_a_tile_bytes = static_cast<uint32_t>(kBlockM * K0 * e);
   p.out_ptr = static_cast<uint8_t*>(D);
   p.out_ld = N1;
-  // (no output map: the output leaves from registers)
-  return launch(V_GEMM_CHAIN_CTA2, d, ta, tw0, tw1, ta, p, smem, 2 * pairs, stream);
+  // The output map stores one warp's 32 rows x 64 columns per box (staged output only).
+  CUtensorMap to = ta;
+  if (p.out_stage &&
+      !make_map(&to, D, p.is_bf16, 2, {static_cast<uint64_t>(N1), static_cast<uint64_t>(M)},
+                {N1 * e}, {64, 32}))
+    return B2B_ERR_CUDA;
+  return launch(V_GEMM_CHAIN_CTA2, d, ta, tw0, tw1, to, p, smem, 2 * pairs, stream);
 }
 
 b2b_status run_gemm_with(const Choice& ch, Info* info, int mode, bool w_mn, int dt, int64_t M,

@@ -335,8 +335,9 @@ __device__ __forceinline__ void fill_bias_half(const ChainParams& p, uint8_t* re
 // epilogue (both CTAs; warpgroup g takes the pair's tiles i with i & 1 == g)
 // ------------------------------------------------------------------------------------
 template <bool BF16>
-__device__ void cta2_epilogue(const ChainParams& p, uint32_t bars, uint32_t tmem_base,
-                              uint32_t rank, volatile uint32_t* abort_flag) {
+__device__ void cta2_epilogue(const ChainParams& p, const CUtensorMap* tmOut, uint32_t base,
+                              uint32_t bars, uint32_t tmem_base, uint32_t rank,
+                              volatile uint32_t* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = (warp - 2) >> 2;   // warpgroup = the tiles it takes
   const int q = warp & 3;          // TMEM lane quadrant this warp may access
@@ -350,6 +351,8 @@ __device__ void cta2_epilogue(const ChainParams& p, uint32_t bars, uint32_t tmem
   // and which cost ~0.6 us per arrive.
   auto report = [&](uint32_t slot) { mbar_arrive_remote(leader_bar(slot)); };
   Tracer trace(p, 2u + static_cast<uint32_t>(g), elected ? 1u : 0u);
+  // this warp's output staging slot (p.out_stage)
+  const uint32_t slot = base + p.off_out[0] + static_cast<uint32_t>(warp - 2) * 4096u;
   bool alive = true;
   const int ntiles = cta2_tiles(p);
   for (int it = g; it < ntiles; it += 2) {
@@ -374,7 +377,10 @@ __device__ void cta2_epilogue(const ChainParams& p, uint32_t bars, uint32_t tmem
     // The buffer (D0 -> P + D1) may take tile it + 2 as soon as the last TMEM load of the
     // tile has completed: the drain reports to the leader's ACC_EMPTY then, before it
     // converts and stores those columns from registers.
-    if (alive) {   // warp-uniform: the drain's TMEM loads and shuffles are warp-collective
+    if (alive && p.out_stage) {   // warp-uniform: TMEM loads and the slot are the warp's
+      drain64_release_to_staging<BF16>(p.act1, tm_lane, p.d1_col[b], p.N1p, slot, tmOut,
+                                       m0 + q * 32, p.M, lane, leader_bar(PB_ACC_EMPTY0 + b));
+    } else if (alive) {   // warp-uniform: the drain's TMEM loads and shuffles are warp-collective
       drain64_release_to_global<BF16>(p.act1, tm_lane, p.d1_col[b], p.N1p, p.out_ptr,
                                       m0 + q * 32, p.M, p.out_ld, p.N1, lane,
                                       leader_bar(PB_ACC_EMPTY0 + b));
@@ -386,6 +392,8 @@ __device__ void cta2_epilogue(const ChainParams& p, uint32_t bars, uint32_t tmem
     if (elected) trace(EV_EPI_DRAINED, g, it);
     if (elected) trace(EV_EPI_STORED, g, it);
   }
+  // the TMA engine has read every staged box before the CTA can leave
+  if (p.out_stage && lane == 0) bulk_wait_read_all();
 }
 
 // ------------------------------------------------------------------------------------
@@ -472,7 +480,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(mapa_shared(bars + 8u * PB_BIAS_READY, 0u));
-    cta2_epilogue<BF16>(p, bars, tmem_base, rank, abort_flag);
+    cta2_epilogue<BF16>(p, &tmOut, base, bars, tmem_base, rank, abort_flag);
   }
 
   // Neither CTA leaves while the other may still read its shared memory (the leader's

@@ -1318,6 +1318,79 @@ __device__ __noinline__ void drain64_release_to_global_act(uint32_t tm_lane, uin
   store_packed64(v1, head + 64, out, out_row0, rows, ld, nvalid, lane);
 }
 
+// 64 packed output columns of this lane's row (v) -> the warp's staging slot (32 rows x
+// 128 B, 128B-swizzled: the output map's box of 64 columns x 32 rows) -> one TMA store at
+// output column `col`, rows row0 .. row0 + 31 (TMA clips rows past the output; a box whose
+// rows all lie past it is not issued).  Lane 0 first waits until its previous store has
+// read the slot.
+__device__ __forceinline__ void stage_store64(const uint32_t (&v)[32], uint32_t slot,
+                                              const CUtensorMap* map, int col, int32_t row0,
+                                              int64_t rows, int lane) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+  const uint32_t rb = slot + static_cast<uint32_t>(lane) * 128u;
+  const uint32_t x = static_cast<uint32_t>(lane) & 7u;
+#pragma unroll
+  for (uint32_t j = 0; j < 8; ++j)
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + ((j ^ x) << 4)),
+                 "r"(v[4 * j]), "r"(v[4 * j + 1]), "r"(v[4 * j + 2]), "r"(v[4 * j + 3])
+                 : "memory");
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && row0 < rows) {
+    tma_store_2d(map, slot, col, row0);
+    bulk_commit_group();
+  }
+}
+
+// As drain64_release_to_global_act, the output leaving through the warp's staging slot
+// and TMA stores (stage_store64) instead of stores from registers.
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain64_release_to_staging_act(uint32_t tm_lane, uint32_t col0,
+                                                            int ncols, uint32_t slot,
+                                                            const CUtensorMap* map, int32_t row0,
+                                                            int64_t rows, int lane,
+                                                            uint32_t release) {
+  const int head = ncols - 128;   // columns drained before the last 128
+  for (int c = 0; c < head; c += 64) {
+    uint32_t r[64], v[32];
+    tmem_ld64x(tm_lane + col0 + c, r);
+    tmem_wait_ld64(r);
+    pack64<BF16, ACT>(r, v);
+    stage_store64(v, slot, map, c, row0, rows, lane);
+  }
+  uint32_t r0[64], r1[64];
+  tmem_ld64x(tm_lane + col0 + head, r0);
+  tmem_ld64x(tm_lane + col0 + head + 64, r1);
+  tmem_wait_ld64(r0);
+  tmem_tie64(r1);
+  tc_fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_remote(release);
+  uint32_t v0[32], v1[32];
+  pack64<BF16, ACT>(r0, v0);
+  pack64<BF16, ACT>(r1, v1);
+  stage_store64(v0, slot, map, head, row0, rows, lane);
+  stage_store64(v1, slot, map, head + 64, row0, rows, lane);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void drain64_release_to_staging(int act, uint32_t tm_lane,
+                                                           uint32_t col0, int ncols,
+                                                           uint32_t slot, const CUtensorMap* map,
+                                                           int32_t row0, int64_t rows, int lane,
+                                                           uint32_t release) {
+  if (act == 2)
+    drain64_release_to_staging_act<BF16, 2>(tm_lane, col0, ncols, slot, map, row0, rows, lane,
+                                            release);
+  else if (act == 1)
+    drain64_release_to_staging_act<BF16, 1>(tm_lane, col0, ncols, slot, map, row0, rows, lane,
+                                            release);
+  else
+    drain64_release_to_staging_act<BF16, 0>(tm_lane, col0, ncols, slot, map, row0, rows, lane,
+                                            release);
+}
+
 template <bool BF16>
 __device__ __forceinline__ void drain64_release_to_global(int act, uint32_t tm_lane,
                                                           uint32_t col0, int ncols, uint8_t* out,

@@ -158,6 +158,10 @@ struct ChainParams {
                                 //    W0 and of W1 (w0/w1_chunk_bytes are the halves' chunks)
   uint8_t* out_ptr;             // w0_res, cta_pair: the output D [M][out_ld] row-major
   int32_t out_ld;               // w0_res, cta_pair: elements per output row
+  int32_t out_stage;            // cta_pair: 1 if each epilogue warp stages its 32 rows' output
+                                //    64 columns at a time (4 KiB per warp from off_out[0],
+                                //    128B-swizzled) and stores them with TMA; 0: stored
+                                //    from registers
   int32_t w1_group;             // 1 (P in TMEM, streamed weights): W1 is loaded once per
                                 //    pair of tiles, w1_per_stage chunks per ring stage,
                                 //    and both tiles' GEMM1 read it from the same stages

@@ -266,8 +266,10 @@ def chain_buffers(plan: dict) -> List[Buffer]:
     bufs = [Buffer("ring", plan["ring"], whole), Buffer("bias", plan["bias"], whole),
             Buffer("bar", plan["bar"], whole)]
     if plan.get("cta_pair"):
-        # CTA pairs: the halves of both weights resident, P in TMEM, no output staging
-        return bufs + [Buffer("weights", plan["w_res"], whole)]
+        # CTA pairs: the halves of both weights resident, P in TMEM, and (when the ring keeps
+        # five stages beside it) a 4 KiB output staging slot per epilogue warp
+        extra = [Buffer("out", plan["out"], whole)] if plan["out"] else []
+        return bufs + [Buffer("weights", plan["w_res"], whole)] + extra
     if plan["resident"] or plan.get("w0_res"):
         bufs.append(Buffer("weights", plan["w_res"], whole))
     if plan["mode"] == 3:

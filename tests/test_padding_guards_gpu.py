@@ -153,6 +153,10 @@ GUARD_GEMMS = [
 
 @pytest.mark.parametrize("shape", GUARD_GEMMS, ids=lambda s: "-".join(map(str, s)))
 def test_b2b_gemm_guards(shape):
+    _gemm_guarded(shape)
+
+
+def _gemm_guarded(shape):
     dt, M, K0, N0, N1 = shape
     w = wl.GemmChain("guard", dt, M, K0, N0, N1, "hardswish", "relu", a_dist="normal")
     t = wl.gemm_inputs(w, seed=31)
@@ -166,6 +170,23 @@ def test_b2b_gemm_guards(shape):
     b = {k: wl.to_bits(v) for k, v in t.items()}
     ref = oracle.b2b_gemm(dt, b["A"][rows], b["W0"], b["b0"], b["W1"], b["b1"], w.act0, w.act1)
     compare(dt, wl.to_bits(out.cpu())[rows], ref, False, "b2b_gemm guarded")
+
+
+@pytest.mark.parametrize("shape", [
+    # dtype, M, K0, N0, N1 over CTA pairs: output staged per warp and stored with TMA (the
+    # last tile's second CTA past M), and, with seven K chunks of W0, stored from registers
+    ("bf16", 40000, 256, 256, 128), ("f16", 1000, 448, 256, 128), ("bf16", 700, 200, 128, 128)],
+    ids=lambda s: "-".join(map(str, s)))
+def test_b2b_gemm_cta_pair_guards(shape):
+    dt, M, K0, N0, N1 = shape
+    dims = (M, K0, N0, N1)
+    n = ops.debug_plan("b2b_gemm", dims, cand=0)["ncand"]
+    ops.set_choice("b2b_gemm", dims, cand=n - 1)
+    try:
+        assert ops.debug_plan("b2b_gemm", dims)["cta_pair"] == 1
+        _gemm_guarded(shape)
+    finally:
+        ops.autotune_reset()
 
 
 @pytest.mark.parametrize("shape", [("f16", 2, 9, 9, 64, 64, 3, 3, 1, 128),
