@@ -394,6 +394,14 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   // GEMM1 waits for two ring fills instead of one per chunk.
   if (mode == MODE_CHAIN && !k.resident && p.p_split != 0u)
     p.w1_per_stage = std::max(1u, p.stage_bytes / p.w1_chunk_bytes);
+  // The conv + pool kernel with N <= 64: two MMA issuers over two sub-rings, each holding
+  // all the ring stages of one tile (measured, N = 64, three stages per tile in a
+  // seven-stage ring: 39.4 -> 35.6 us).  With longer MMAs one issuer keeps the tensor core
+  // busy, and sub-rings shallower than a tile starve both issuers; on the single GEMMs of
+  // the unfused operators (also tried: N = 64 and N = 128-256) two issuers ran 2-10 %
+  // slower, so they keep one.
+  p.two_issuers = mode == MODE_POOL && p.N0p <= 64 &&
+                  p.num_stages / 2u >= static_cast<uint32_t>(p.kstages0) ? 1 : 0;
   Regions r;
   r.cand = pick;
   r.ncand = nfeas;
@@ -1922,14 +1930,14 @@ extern "C" {
 static b2b_status debug_plan_with(int32_t kind, const int64_t* dims, int32_t ndims, int forced,
                                   const Choice& c, uint32_t* out, int32_t out_len) {
   if (out == nullptr) return B2B_ERR_NULL;
-  if (out_len < 60) return B2B_ERR_SHAPE;
+  if (out_len < 61) return B2B_ERR_SHAPE;
   ChainParams p;
   Regions r;
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
   if (b2b_status st = plan_for_kind(kind, dims, ndims, forced, p, r, smem, mode); st != B2B_OK)
     return st;
-  const uint32_t v[60] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[61] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -1946,7 +1954,8 @@ static b2b_status debug_plan_with(int32_t kind, const int64_t* dims, int32_t ndi
                           static_cast<uint32_t>(r.ncand), static_cast<uint32_t>(c.grid),
                           static_cast<uint32_t>(c.pf2), r.extend, p.off_w2, p.off_p1[0],
                           p.off_p1[1], p.d2_col[0], p.d2_col[1], p.p_split,
-                          static_cast<uint32_t>(p.w0_res), static_cast<uint32_t>(p.cta_pair)};
+                          static_cast<uint32_t>(p.w0_res), static_cast<uint32_t>(p.cta_pair),
+                          static_cast<uint32_t>(p.two_issuers)};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

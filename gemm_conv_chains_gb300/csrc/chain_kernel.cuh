@@ -152,6 +152,21 @@ __device__ __forceinline__ int local_tiles(const ChainParams& p) {
   return b < p.num_tiles ? (p.num_tiles - 1 - b) / g + 1 : 0;
 }
 
+// Two MMA issuers (two_issuers(MODE)): each takes the tiles of one parity and the ring is
+// split into two sub-rings, [0, S/2) for even tiles and [S/2, S) for odd ones, so that each
+// sub-ring has one consumer that takes its slots in order (a consumer further ahead than
+// one phase of a slot would alias the barrier's phase parity).  The tiles of one parity
+// take consecutive positions in their sub-ring; slot and phase of stage kc of tile it:
+__device__ __forceinline__ void subring_pos(const ChainParams& p, int it, int kc, int& slot,
+                                            uint32_t& phase) {
+  const int s0 = static_cast<int>(p.num_stages) >> 1;
+  const int odd = it & 1;
+  const int n = odd ? static_cast<int>(p.num_stages) - s0 : s0;
+  const int pos = (it >> 1) * p.kstages0 + kc;
+  slot = (odd ? s0 : 0) + pos % n;
+  phase = static_cast<uint32_t>(pos / n) & 1u;
+}
+
 // Buffer of the CTA's it-th tile and the phase parity of its barriers.
 __device__ __forceinline__ uint32_t buf_of(const ChainParams& p, int it) {
   return static_cast<uint32_t>(it) & ((1u << p.nbuf_log2) - 1u);
@@ -326,6 +341,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     const TileCoord tc = tile_coord<A4D>(p, t);
     KPos k;
     for (int kc = 0; kc < p.kstages0; ++kc) {
+      if (two_issuers(MODE) && p.two_issuers) subring_pos(p, it, kc, stage, phase);
       if (W0RES && it == 0) {
         // The resident W0, chunk by chunk beside the CTA's first tile, so that its first
         // MMAs wait for one chunk, not for the whole matrix.
@@ -480,10 +496,7 @@ __device__ __forceinline__ void issue_chunk(uint32_t lead, uint32_t d, uint64_t 
   constexpr uint64_t kAStep = 32u >> 4;
   constexpr uint64_t kBStep = BMN ? (2048u >> 4) : (32u >> 4);
   if (nks == 4) {
-    mma_f16_ss(lead, d, adesc, bdesc, idesc, first ? 0u : 1u);
-    mma_f16_ss(lead, d, adesc + kAStep, bdesc + kBStep, idesc, 1u);
-    mma_f16_ss(lead, d, adesc + 2 * kAStep, bdesc + 2 * kBStep, idesc, 1u);
-    mma_f16_ss(lead, d, adesc + 3 * kAStep, bdesc + 3 * kBStep, idesc, 1u);
+    mma_f16_ss_x4(lead, d, adesc, bdesc, kAStep, kBStep, idesc, first ? 0u : 1u);
   } else {
     for (int ks = 0; ks < nks; ++ks)
       mma_f16_ss(lead, d, adesc + ks * kAStep, bdesc + ks * kBStep, idesc,
@@ -505,13 +518,17 @@ __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE, bool PAIR, bool NOPAIR,
           bool W0RES>
 __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
-                         volatile uint32_t* abort_flag) {
+                         volatile uint32_t* abort_flag, int issuer = 0) {
   const bool resident = !PAIR && p.resident != 0;   // (as in the producer)
+  // two issuers: issuer 0 takes even tiles, 1 odd ones, each in its own sub-ring
+  const bool two = two_issuers(MODE) && p.two_issuers != 0;
   const uint32_t idesc0 = idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p);
   const uint32_t idesc1 = idesc_f16_f32(BF16 ? 1u : 0u, W1MN ? 1u : 0u, kBlockM, p.N1p);
   bool ok = true;
   const uint32_t lead = elect_one();
-  Tracer trace(p, 1, lead, 3);   // slots 0..2: the kernel's entry, setup and dependency events
+  // slots 0..2: the kernel's entry, setup and dependency events (the second issuer does
+  // not record)
+  Tracer trace(p, 1, issuer == 0 ? lead : 0u, 3);
   if (resident)
     ok = warp_mbar_wait(bars + 8u * BAR_WFULL, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
   bool bias_ready = false;   // the epilogue warps write the bias operands at the start
@@ -579,6 +596,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
   auto issue_g0 = [&](int it) -> bool {
     const int32_t t = blockIdx.x + it * gridDim.x;
     const uint32_t b = buf_of(p, it);
+
     if ((MODE != MODE_CHAIN && MODE != MODE_CHAIN3) || PAIR || (!NOPAIR && p.p_tmem)) {
       // The epilogue must have drained the buffer's previous tile (with P in TMEM: its
       // GEMM1 accumulator, the last thing read from the buffer).
@@ -595,6 +613,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     int cb = 0;       // channel block within the tap (4-D) / chunk index (2-D)
     int s_tap = 0;    // halo: the column tap of the stage
     for (int kc = 0; kc < p.kstages0; ++kc) {
+      if (two) subring_pos(p, it, kc, stage, phase);   // this issuer's sub-ring
       trace(EV_MMA_WAIT, kc, it);
       if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL, t))
         return false;
@@ -889,10 +908,11 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         if (ok && j + L < ntiles) ok = issue_g0(j + L);
       }
     } else {
-      for (int it = 0; ok && it < ntiles; ++it) ok = issue_g0(it);
+      for (int it = two ? issuer : 0; ok && it < ntiles; it += two ? 2 : 1) ok = issue_g0(it);
     }
   }
-  // Whatever happened, no MMA may still be running when TMEM is released.
+  // Whatever happened, no MMA may still be running when TMEM is released (with two
+  // issuers the barrier counts both commits).
   mma_commit(lead, bars + 8u * BAR_MMA_DONE);
   (void)mbar_wait(bars + 8u * BAR_MMA_DONE, 0u, p.wait_limit_ns, nullptr, p.err, p.kernel_id,
                   SITE_MMA_DRAIN, 0);
@@ -1813,7 +1833,7 @@ __device__ __forceinline__ void fill_w2(const ChainParams& p, uint8_t* dst, int 
 // ------------------------------------------------------------------------------------
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
           bool PAIR = false, bool NOPAIR = false, bool W0RES = false>
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(chain_threads(MODE), 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW0,
                  const __grid_constant__ CUtensorMap tmW1,
                  const __grid_constant__ CUtensorMap tmOut, const ChainParams p) {
@@ -1854,7 +1874,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         mbar_init(bars + 8u * (BAR_D2_FULL0 + a), 1);
       }
     }
-    mbar_init(bars + 8u * BAR_MMA_DONE, 1);
+    mbar_init(bars + 8u * BAR_MMA_DONE, two_issuers(MODE) && p.two_issuers ? 2u : 1u);
     mbar_init(bars + 8u * BAR_BIAS_READY, kNumEpiWarps);
     if (W0RES)
       for (uint32_t c = 0; c < static_cast<uint32_t>(kMaxW0Chunks); ++c)
@@ -1907,7 +1927,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>(p, base, bars, tmem_base,
-                                                                    abort_flag);
+                                                                    abort_flag, 0);
+    __syncwarp();
+  } else if (two_issuers(MODE) && warp == kSecondIssuerWarp) {
+    if (p.two_issuers)
+      mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>(p, base, bars, tmem_base,
+                                                                      abort_flag, 1);
     __syncwarp();
   } else {
     // The bias operands, off the producer's critical path; the MMA issuer waits for them

@@ -76,6 +76,16 @@ constexpr int kChunkK = 64;           // K elements per staged chunk (128 B rows
 constexpr int kNumEpiWarps = 8;       // two warpgroups of four (one per TMEM lane quadrant)
 constexpr int kNumEpiThreads = 32 * kNumEpiWarps;
 constexpr int kNumThreads = 64 + kNumEpiThreads;   // warp 0 TMA, warp 1 MMA + TMEM, 2..9 epilogue
+// The conv + pool kernel (MODE_POOL, one GEMM per tile) adds warp 10, a possible second MMA
+// issuer (ChainParams::two_issuers): warps 1 and 10 then take alternate tiles (each its own
+// accumulator), so that one issues while the other waits between ring stages.  With N = 64
+// the tensor core finishes an MMA in ~48 cycles and accepts only a short queue of them, so
+// every cycle a single issuer spends on barriers and bookkeeping leaves it idle.
+__host__ __device__ constexpr bool two_issuers(int mode) { return mode == 2; }
+__host__ __device__ constexpr int chain_threads(int mode) {
+  return kNumThreads + (two_issuers(mode) ? 32 : 0);
+}
+constexpr int kSecondIssuerWarp = kNumThreads / 32;
 constexpr int kMaxStages = 8;
 constexpr int kMaxBufs = 4;          // accumulator / P buffers per CTA
 constexpr int kMaxW0Chunks = 8;      // K chunks of a W0 kept resident beside streamed W1
@@ -158,6 +168,9 @@ struct ChainParams {
                                 //    W0 and of W1 (w0/w1_chunk_bytes are the halves' chunks)
   uint8_t* out_ptr;             // w0_res, cta_pair: the output D [M][out_ld] row-major
   int32_t out_ld;               // w0_res, cta_pair: elements per output row
+  int32_t two_issuers;          // (MODE_POOL) 1: warps 1 and 10 issue the MMAs
+                                //    of alternate tiles, the ring split into two sub-rings
+                                //    (subring_pos); 0: warp 1 alone, warp 10 idle
   int32_t out_stage;            // cta_pair: 1 if each epilogue warp stages its 32 rows' output
                                 //    64 columns at a time (4 KiB per warp from off_out[0],
                                 //    128B-swizzled) and stores them with TMA; 0: stored

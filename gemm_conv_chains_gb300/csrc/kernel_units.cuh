@@ -22,7 +22,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& w0, const CUtens
                        const CUtensorMap& out, const ChainParams& p, int grid, size_t smem,
                        cudaStream_t stream) {
   return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>, a, w0,
-                      w1, out, p, grid, smem, stream);
+                      w1, out, p, grid, smem, stream, chain_threads(MODE));
 }
 
 // 2-D A operand: GEMM chains (row-major weights) and 1x1 convs (K-major filters).

@@ -40,10 +40,10 @@ using ChainKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMa
 inline cudaError_t launch_chain(ChainKernelFn fn, const CUtensorMap& a, const CUtensorMap& w0,
                                 const CUtensorMap& w1, const CUtensorMap& out,
                                 const ChainParams& p, int grid, size_t smem,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, int threads = kNumThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(static_cast<unsigned>(kNumThreads));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

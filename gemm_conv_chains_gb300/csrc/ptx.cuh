@@ -319,6 +319,33 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t pred, uint32_t d_tmem, uint6
       : "memory");
 }
 
+// Four consecutive K steps of one 64-wide K chunk in one asm block: the descriptors of
+// step j are a + j * astep and b + j * bstep (16-byte units); the first step accumulates
+// when `accumulate` != 0, the others always.  One predicate setup and no compiler-visible
+// boundaries between the four issues: the issuing thread is otherwise the bottleneck for
+// N <= 64, whose MMAs the tensor core finishes in ~48 cycles.
+__device__ __forceinline__ void mma_f16_ss_x4(uint32_t pred, uint32_t d_tmem, uint64_t a,
+                                              uint64_t b, uint64_t astep, uint64_t bstep,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred q, p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 q, %0, 0;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "setp.eq.b32 t, %0, %0;\n\t"
+      "add.s64 a1, %2, %4;\n\t"
+      "add.s64 b1, %3, %5;\n\t"
+      "add.s64 a2, a1, %4;\n\t"
+      "add.s64 b2, b1, %5;\n\t"
+      "add.s64 a3, a2, %4;\n\t"
+      "add.s64 b3, b2, %5;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %6, p;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%1], a1, b1, %6, t;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%1], a2, b2, %6, t;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%1], a3, b3, %6, t;\n\t}" ::"r"(pred),
+      "r"(d_tmem), "l"(a), "l"(b), "l"(astep), "l"(bstep), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] x B[smem] ("TS" form): A is 128 lanes (rows) x 16 K elements packed
 // two per 32-bit column, 8 columns per K step.  Issued only where pred != 0.
 __device__ __forceinline__ void mma_f16_ts(uint32_t pred, uint32_t d_tmem, uint32_t a_tmem,

@@ -23,7 +23,7 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes",
           "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2", "d1_col3", "cand", "ncand",
           "grid_choice", "pf_choice", "ring_extend", "off_w2", "off_p1_0", "off_p1_1", "d2_col0",
-          "d2_col1", "p_split", "w0_res", "cta_pair"]
+          "d2_col1", "p_split", "w0_res", "cta_pair", "two_issuers"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4, "b2b_gemm3": 5}
@@ -458,3 +458,21 @@ def test_wide_chain_limits():
     assert plan("b2b_gemm", (1000, 64, 512, 136))[0] == 4     # N1 > 128 beside a wide N0
     assert plan("b2b_gemm", (1000, 64, 520, 64))[0] == 4      # N0 > 512
     assert plan("gemm_bias_act", (1000, 64, 264))[0] == 4     # single operators keep N <= 256
+
+
+def test_two_issuers_only_for_the_pooled_conv():
+    # the conv + pool kernel with N <= 64 whose ring holds two tiles' stages splits it
+    # between two MMA issuers; every other kernel keeps one
+    pool = check("conv_relu_maxpool", (32, 112, 112, 64, 64), False)
+    assert pool["two_issuers"] == 1 and pool["stages"] // 2 >= 3
+    for kind, dims, rm in (("conv_bias_act_nhwc", (32, 56, 56, 64, 64, 3, 3, 1), False),
+                           ("gemm_bias_act", (200704, 64, 64), True),
+                           ("gemm_bias_act", (32768, 256, 256), True),
+                           ("b2b_gemm", (1024, 64, 64, 64), True)):
+        assert check(kind, dims, rm)["two_issuers"] == 0
+    # the same pooled conv with streamed filters: nine stages per tile, one issuer
+    ops.set_choice("conv_relu_maxpool", (32, 112, 112, 64, 64), cand=1)
+    try:
+        assert check("conv_relu_maxpool", (32, 112, 112, 64, 64), False)["two_issuers"] == 0
+    finally:
+        ops.autotune_reset()
