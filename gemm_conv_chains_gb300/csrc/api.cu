@@ -198,7 +198,8 @@ struct Regions {
 
 // TMEM columns of the accumulators.  Chain: nbuf D0 buffers of round_up(N0p, 32) columns,
 // then nbuf D1 buffers of round_up(N1p, 32) columns (every buffer starts on a multiple of
-// 32 columns); single/pool: two accumulator buffers.  Returns the power-of-two allocation.
+// 32 columns); single/pool: two accumulator buffers, or four when nbuf is 4.  Returns the
+// power-of-two allocation.
 uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = false) {
   const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
   for (uint32_t b = 0; b < kMaxBufs; ++b) p.d0_col[b] = p.d1_col[b] = 0;
@@ -248,9 +249,10 @@ uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = fals
     }
     return pow2_at_least(nbuf * (s0 + s1));
   }
-  const uint32_t cols = pow2_at_least(2u * s0);
-  p.d0_col[0] = 0;
-  p.d0_col[1] = cols / 2u;
+  // single / pool: nbuf (2 or 4) accumulator buffers
+  const uint32_t n = nbuf >= 4u ? 4u : 2u;
+  const uint32_t cols = pow2_at_least(n * s0);
+  for (uint32_t b = 0; b < n; ++b) p.d0_col[b] = b * (cols / n);
   return cols;
 }
 
@@ -402,6 +404,14 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   // slower, so they keep one.
   p.two_issuers = mode == MODE_POOL && p.N0p <= 64 &&
                   p.num_stages / 2u >= static_cast<uint32_t>(p.kstages0) ? 1 : 0;
+  // ... and each issuer two accumulators, so that it starts its next tile while the
+  // epilogue drains the previous one (tile i takes buffer i & 3)
+  if (p.two_issuers && tmem_layout(p, mode, 4u) <= 512u) {
+    p.nbuf_log2 = 2;
+    p.tmem_cols = tmem_layout(p, mode, 4u);
+  } else {
+    p.tmem_cols = tmem_layout(p, mode, static_cast<uint32_t>(k.dual), k.p_tmem != 0);
+  }
   Regions r;
   r.cand = pick;
   r.ncand = nfeas;

@@ -114,8 +114,10 @@ def check(kind, dims, row_major_w):
         assert per >= 1 and per * w1_chunk <= p["stage_bytes"]
         assert -(-p["kchunks1"] // per) <= p["stages"]
     nbuf = p["nbuf"]
-    assert nbuf in (1, 2, 4) and (nbuf > 1) == dual and (mode == 0 or nbuf == 2)
-    assert nbuf != 4 or (mode == 0 and not p_tmem and groups == 2 and not p["alias"])
+    # (the pooled conv with two MMA issuers gives each issuer two accumulators)
+    assert nbuf in (1, 2, 4) and (nbuf > 1) == dual
+    assert mode == 0 or nbuf == 2 or (mode == 2 and p["two_issuers"] and nbuf == 4)
+    assert nbuf != 4 or mode == 2 or (mode == 0 and not p_tmem and groups == 2 and not p["alias"])
     # P buffers used: tile i -> P[i mod nbuf]; none when P is in TMEM
     pbufs = 0 if p_tmem else (nbuf if mode == 0 else 0)
     obufs = 2 if groups == 2 else 1
@@ -172,7 +174,7 @@ def check(kind, dims, row_major_w):
             spans.append((lo, hi))
         assert spans[0][1] <= spans[1][0] or spans[1][1] <= spans[0][0]
         return p
-    accs = [(f"d0_{b}", p[f"d0_col{b}"], N0p) for b in range(nbuf if mode == 0 else 2)]
+    accs = [(f"d0_{b}", p[f"d0_col{b}"], N0p) for b in range(nbuf)]
     if mode == 0:
         accs += [(f"d1_{b}", p[f"d1_col{b}"], N1p) for b in range(nbuf)]
     for name, col, n in accs:
