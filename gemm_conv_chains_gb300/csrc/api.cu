@@ -111,6 +111,7 @@ struct MapKey {
   uint64_t strides[3];
   uint32_t box[4];
   uint32_t elem_strides[4];
+  uint32_t swizzle128, pad;
   bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 struct MapKeyHash {
@@ -124,16 +125,19 @@ struct MapKeyHash {
 std::mutex g_map_mu;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-// A tiled, 128B-swizzled map with zero fill outside the tensor.  dims[0] is the
-// contiguous dimension; strides are in bytes for dims 1..rank-1.  elem_strides: the box
-// takes every elem_strides[i]-th element along dimension i (box[i] / elem_strides[i] of
-// them land in shared memory).
+// A tiled, 128B-swizzled (or, with swizzle128 false, unswizzled: the box lands densely,
+// dimension 0 fastest) map with zero fill outside the tensor.  dims[0] is the contiguous
+// dimension; strides are in bytes for dims 1..rank-1.  elem_strides: the box takes every
+// elem_strides[i]-th element along dimension i (box[i] / elem_strides[i] of them land in
+// shared memory).
 bool make_map(CUtensorMap* out, const void* ptr, int is_bf16, uint32_t rank,
               std::initializer_list<uint64_t> dims, std::initializer_list<uint64_t> strides,
               std::initializer_list<uint32_t> box,
-              std::initializer_list<uint32_t> elem_strides = {1, 1, 1, 1}) {
+              std::initializer_list<uint32_t> elem_strides = {1, 1, 1, 1},
+              bool swizzle128 = true) {
   MapKey key;
   std::memset(&key, 0, sizeof(key));
+  key.swizzle128 = swizzle128 ? 1u : 0u;
   key.ptr = ptr;
   key.rank = rank;
   key.is_bf16 = static_cast<uint32_t>(is_bf16);
@@ -162,7 +166,8 @@ bool make_map(CUtensorMap* out, const void* ptr, int is_bf16, uint32_t rank,
   CUtensorMap m;
   const CUresult r = fn(&m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         rank, const_cast<void*>(ptr), gdim, gstride, bdim, estride,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   std::lock_guard<std::mutex> lk(g_map_mu);
@@ -204,6 +209,7 @@ uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = fals
   const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
   for (uint32_t b = 0; b < kMaxBufs; ++b) p.d0_col[b] = p.d1_col[b] = 0;
   p.d2_col[0] = p.d2_col[1] = 0;
+  p.pt_col[0] = p.pt_col[1] = 0;
   p.p_split = 0;
   p.p_hi = 0;
   if (mode == MODE_CHAIN && p_tmem && p.N0p > 256) {
@@ -214,8 +220,8 @@ uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = fals
     // tile's first GEMM0 pass never touches the previous tile's D1.
     p.p_split = 256u;
     p.p_hi = 256u;
-    p.d0_col[0] = 0;
-    p.d0_col[1] = 256u;
+    p.d0_col[0] = p.pt_col[0] = 0;
+    p.d0_col[1] = p.pt_col[1] = 256u;
     p.d1_col[0] = 128u;
     p.d1_col[1] = 384u;
     return 512u;
@@ -231,12 +237,25 @@ uint32_t tmem_layout(ChainParams& p, int mode, uint32_t nbuf, bool p_tmem = fals
     }
     return pow2_at_least(2u * (s0 + s1 + s2));
   }
+  if (mode == MODE_CHAIN && p_tmem && p.two_issuers) {
+    // Two issuers: D0, P and D1 of both buffers apart -- [D0 0][D0 1][P 0][P 1][D1 0][D1 1]
+    // -- so that an issuer's next GEMM0 overwrites nothing its GEMM1 or the epilogue may
+    // still read.
+    const uint32_t sp = round_up(static_cast<uint32_t>(p.N0p) / 2u, 32u);
+    const uint32_t s1 = round_up(static_cast<uint32_t>(p.N1p), 32u);
+    for (uint32_t b = 0; b < 2; ++b) {
+      p.d0_col[b] = b * s0;
+      p.pt_col[b] = 2u * s0 + b * sp;
+      p.d1_col[b] = 2u * (s0 + sp) + b * s1;
+    }
+    return pow2_at_least(2u * (s0 + sp + s1));
+  }
   if (mode == MODE_CHAIN && p_tmem) {
     // Buffer b holds D0, then P (packed, N0p / 2 columns, over D0) and D1 after it.
     const uint32_t d1off = round_up(static_cast<uint32_t>(p.N0p) / 2u, 32u);
     const uint32_t buf = round_up(std::max(s0, d1off + static_cast<uint32_t>(p.N1p)), 32u);
-    p.d0_col[0] = 0;
-    p.d0_col[1] = buf;
+    p.d0_col[0] = p.pt_col[0] = 0;
+    p.d0_col[1] = p.pt_col[1] = buf;
     p.d1_col[0] = d1off;
     p.d1_col[1] = buf + d1off;
     return pow2_at_least(2u * buf);
@@ -277,6 +296,8 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   const uint32_t out_bytes = mode == MODE_CHAIN    ? n1blk * kPChunkBytes
                              : mode == MODE_SINGLE ? n0blk * kPChunkBytes
                                                    : n0blk * kPoolChunkBytes;
+  // (the two-issuer conv chain: one slot of 32 rows x 16 columns per epilogue warp)
+  const uint32_t slot_bytes = static_cast<uint32_t>(kNumEpiWarps) * kOutSlotBytes;
   // Bias operands: the ONES tile, then one BIAS block per 64-wide N block of each GEMM.
   const uint32_t bias_bytes =
       kOnesBytes + kBiasBlockBytes * (n0blk + (mode == MODE_CHAIN ? n1blk : 0u));
@@ -291,19 +312,28 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   // w0res: P in TMEM with W0 alone resident (row-major weights, at most kMaxW0Chunks K
   // chunks): the ring carries A and W1 chunks and the output goes from registers straight
   // to global memory, so the plan has no output staging.
-  struct Cand { int dual, groups, resident, alias, p_tmem, w0res = 0; };
+  // two: (convs with halo boxes, N0 <= 64) two MMA issuers over two sub-rings that each
+  // hold a whole tile's stages, resident filters, P in TMEM apart from D0 and D1, and the
+  // output staged 16 columns at a time in a 1 KiB slot per epilogue warp, so that the ring
+  // has room for both sub-rings.
+  struct Cand { int dual, groups, resident, alias, p_tmem, w0res = 0, two = 0; };
   Cand cands[16];
   int ncand = 0;
   if (mode == MODE_CHAIN) {
     ChainParams probe = p;
+    probe.two_issuers = 0;
     const bool tmem_quad_ok = tmem_layout(probe, mode, 4u) <= 512u;
     const bool tmem_dual_ok = tmem_layout(probe, mode, 2u) <= 512u;
     const bool tmem_p_ok = tmem_layout(probe, mode, 2u, true) <= 512u;
+    probe.two_issuers = 1;
+    const bool tmem_two_ok = tmem_layout(probe, mode, 2u, true) <= 512u;
     if (p.N0p > 256) {
       // Wide (256 < N0 <= 512, N1 <= 128): one tile in flight, P in TMEM, both
       // warpgroups on every tile, weights streamed.
       if (p.N1p <= 128) cands[ncand++] = {1, 1, 0, 0, 1};
     } else {
+      if (p.R > 1 && p.stride == 1 && p.N0p <= 64 && tmem_two_ok)
+        cands[ncand++] = {2, 2, 1, 0, 1, 0, 1};
       // Four tiles in flight (narrow chains): each epilogue group one tile ahead.
       if (tmem_quad_ok)
         for (int resident = 1; resident >= 0; --resident) cands[ncand++] = {4, 2, resident, 0, 0};
@@ -341,15 +371,16 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
           : k.w0res  ? round_up(std::max(kABytes, p.w1_chunk_bytes), 1024u)
                      : round_up(std::max(kABytes + p.w0_chunk_bytes, p.w1_chunk_bytes), 1024u);
       const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? static_cast<uint32_t>(k.dual) : 0u;
-      const uint32_t obufs = k.w0res ? 0u : (k.groups == 2 ? 2u : 1u);
+      const uint32_t obufs = k.w0res ? 0u : (k.groups == 2 && !k.two ? 2u : 1u);
       const uint32_t shared = k.alias ? pbufs * std::max(p_bytes, out_bytes)
-                                      : pbufs * p_bytes + obufs * out_bytes;
+                                      : pbufs * p_bytes + obufs * (k.two ? slot_bytes : out_bytes);
       const uint32_t w0_res_bytes = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
       const uint32_t fixed =
           (k.resident ? w_res : k.w0res ? w0_res_bytes : 0u) + shared + bias_bytes + bar_bytes;
       if (fixed >= budget) continue;
       const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / stage_bytes);
       if (stages < 2u) continue;
+      if (k.two && stages / 2u < static_cast<uint32_t>(p.S * p.kc_per_tap)) continue;
       feas[nfeas] = c;
       feas_stages[nfeas] = stages;
       feas_stage_bytes[nfeas++] = stage_bytes;
@@ -379,6 +410,8 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   p.halo = (k.resident && p.R > 1 && p.stride == 1) ? 1 : 0;
   p.a_stage_bytes = p.halo ? (7u + static_cast<uint32_t>(p.R)) * 2048u : kABytes;
   p.kstages0 = p.halo ? p.S * p.kc_per_tap : p.kchunks0;
+  p.two_issuers = k.two;
+  p.out_slots = k.two;
   p.tmem_cols = tmem_layout(p, mode, static_cast<uint32_t>(k.dual), k.p_tmem != 0);
   // P in TMEM with streamed weights: W1 is packed into as few ring stages as possible and
   // shared by the two tiles of a pair -- if those stages fit the ring at once.
@@ -402,11 +435,12 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   // busy, and sub-rings shallower than a tile starve both issuers; on the single GEMMs of
   // the unfused operators (also tried: N = 64 and N = 128-256) two issuers ran 2-10 %
   // slower, so they keep one.
-  p.two_issuers = mode == MODE_POOL && p.N0p <= 64 &&
-                  p.num_stages / 2u >= static_cast<uint32_t>(p.kstages0) ? 1 : 0;
+  if (mode == MODE_POOL)
+    p.two_issuers =
+        p.N0p <= 64 && p.num_stages / 2u >= static_cast<uint32_t>(p.kstages0) ? 1 : 0;
   // ... and each issuer two accumulators, so that it starts its next tile while the
   // epilogue drains the previous one (tile i takes buffer i & 3)
-  if (p.two_issuers && tmem_layout(p, mode, 4u) <= 512u) {
+  if (mode == MODE_POOL && p.two_issuers && tmem_layout(p, mode, 4u) <= 512u) {
     p.nbuf_log2 = 2;
     p.tmem_cols = tmem_layout(p, mode, 4u);
   } else {
@@ -419,10 +453,10 @@ bool plan_smem(ChainParams& p, int mode, bool w0mn, bool w1mn, size_t* smem_byte
   r.w_res = p.resident ? w_res : (k.w0res ? static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes : 0u);
   const uint32_t pbufs = (mode == MODE_CHAIN && !k.p_tmem) ? static_cast<uint32_t>(k.dual) : 0u;
   r.p_each = pbufs ? (p.out_alias_p ? std::max(p_bytes, out_bytes) : p_bytes) : 0u;
-  r.out_each = (p.out_alias_p || k.w0res) ? 0u : out_bytes;
+  r.out_each = (p.out_alias_p || k.w0res) ? 0u : (k.two ? slot_bytes : out_bytes);
   r.bias = bias_bytes;
   r.bar = bar_bytes;
-  const uint32_t obufs = k.w0res ? 0u : (k.groups == 2 ? 2u : 1u);
+  const uint32_t obufs = k.w0res ? 0u : (k.groups == 2 && !k.two ? 2u : 1u);
   uint32_t off = 0;
   p.off_ring = off;
   off += r.ring;
@@ -1065,7 +1099,18 @@ b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t
   p.pf_w0_bytes = static_cast<uint32_t>(static_cast<uint64_t>(C0) * R * S * C * e);
   p.pf_w1 = static_cast<const uint8_t*>(W1);
   p.pf_w1_bytes = mode == MODE_CHAIN ? static_cast<uint32_t>(static_cast<uint64_t>(C1) * C0 * e) : 0u;
-  const Variant v = mode == MODE_CHAIN    ? (p.p_tmem ? V_CONV_CHAIN : V_CONV_CHAIN_NP)
+  // The two-issuer chain stores each warp's 32 rows (two output rows of 16 pixels) 16
+  // channels at a time from its own 1 KiB slot.
+  if (p.out_slots)
+    ok = ok && make_map(&to, y, p.is_bf16, 4,
+                        {static_cast<uint64_t>(C1), static_cast<uint64_t>(Wo), static_cast<uint64_t>(Ho),
+                         static_cast<uint64_t>(N)},
+                        {C1 * e, static_cast<uint64_t>(Wo) * C1 * e, static_cast<uint64_t>(Ho) * Wo * C1 * e},
+                        {16, 16, 2, 1}, {1, 1, 1, 1}, false);
+  if (!ok) return B2B_ERR_CUDA;
+  const Variant v = mode == MODE_CHAIN    ? (p.two_issuers ? V_CONV_CHAIN_2I
+                                            : p.p_tmem    ? V_CONV_CHAIN
+                                                          : V_CONV_CHAIN_NP)
                     : mode == MODE_SINGLE ? V_CONV_SINGLE
                                           : V_CONV_POOL;
   return launch(v, d, ta, tw0, tw1, to, p, smem, grid, stream);
@@ -1940,14 +1985,14 @@ extern "C" {
 static b2b_status debug_plan_with(int32_t kind, const int64_t* dims, int32_t ndims, int forced,
                                   const Choice& c, uint32_t* out, int32_t out_len) {
   if (out == nullptr) return B2B_ERR_NULL;
-  if (out_len < 61) return B2B_ERR_SHAPE;
+  if (out_len < 64) return B2B_ERR_SHAPE;
   ChainParams p;
   Regions r;
   size_t smem = 0;
   int32_t mode = MODE_CHAIN;
   if (b2b_status st = plan_for_kind(kind, dims, ndims, forced, p, r, smem, mode); st != B2B_OK)
     return st;
-  const uint32_t v[61] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
+  const uint32_t v[64] = {static_cast<uint32_t>(smem), p.num_stages, p.stage_bytes,
                           static_cast<uint32_t>(p.resident), static_cast<uint32_t>(p.out_alias_p),
                           p.off_ring, r.ring, p.off_w0, p.off_w1, r.w_res, p.w0_chunk_bytes,
                           p.w1_chunk_bytes, p.off_p[0], p.off_p[1], r.p_each, p.off_out[0],
@@ -1965,7 +2010,8 @@ static b2b_status debug_plan_with(int32_t kind, const int64_t* dims, int32_t ndi
                           static_cast<uint32_t>(c.pf2), r.extend, p.off_w2, p.off_p1[0],
                           p.off_p1[1], p.d2_col[0], p.d2_col[1], p.p_split,
                           static_cast<uint32_t>(p.w0_res), static_cast<uint32_t>(p.cta_pair),
-                          static_cast<uint32_t>(p.two_issuers)};
+                          static_cast<uint32_t>(p.two_issuers),
+                          static_cast<uint32_t>(p.out_slots), p.pt_col[0], p.pt_col[1]};
   std::memcpy(out, v, sizeof(v));
   return B2B_OK;
 }

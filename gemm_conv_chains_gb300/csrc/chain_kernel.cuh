@@ -152,11 +152,12 @@ __device__ __forceinline__ int local_tiles(const ChainParams& p) {
   return b < p.num_tiles ? (p.num_tiles - 1 - b) / g + 1 : 0;
 }
 
-// Two MMA issuers (two_issuers(MODE)): each takes the tiles of one parity and the ring is
-// split into two sub-rings, [0, S/2) for even tiles and [S/2, S) for odd ones, so that each
-// sub-ring has one consumer that takes its slots in order (a consumer further ahead than
-// one phase of a slot would alias the barrier's phase parity).  The tiles of one parity
-// take consecutive positions in their sub-ring; slot and phase of stage kc of tile it:
+// Two MMA issuers (two_issuers(MODE, TWO)): each takes the tiles of one parity and the
+// ring is split into two sub-rings, [0, S/2) for even tiles and [S/2, S) for odd ones, so
+// that each sub-ring has one consumer that takes its slots in order (a consumer further
+// ahead than one phase of a slot would alias the barrier's phase parity).  The tiles of one
+// parity take consecutive positions in their sub-ring; slot and phase of stage kc of tile
+// it:
 __device__ __forceinline__ void subring_pos(const ChainParams& p, int it, int kc, int& slot,
                                             uint32_t& phase) {
   const int s0 = static_cast<int>(p.num_stages) >> 1;
@@ -289,7 +290,8 @@ __device__ __forceinline__ void prefetch_a_tile(const ChainParams& p, int32_t t)
   bulk_prefetch_l2(p.pf_a + off, static_cast<uint32_t>(n));
 }
 
-template <int MODE, bool A4D, bool W0MN, bool W1MN, bool WIDE, bool PAIR, bool NOPAIR, bool W0RES>
+template <int MODE, bool A4D, bool W0MN, bool W1MN, bool WIDE, bool PAIR, bool NOPAIR, bool W0RES,
+          bool TWO>
 __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
                               const CUtensorMap* tmW0, const CUtensorMap* tmW1, uint32_t base,
                               uint32_t bars, volatile uint32_t* abort_flag) {
@@ -341,7 +343,7 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     const TileCoord tc = tile_coord<A4D>(p, t);
     KPos k;
     for (int kc = 0; kc < p.kstages0; ++kc) {
-      if (two_issuers(MODE) && p.two_issuers) subring_pos(p, it, kc, stage, phase);
+      if (two_issuers(MODE, TWO) && p.two_issuers) subring_pos(p, it, kc, stage, phase);
       if (W0RES && it == 0) {
         // The resident W0, chunk by chunk beside the CTA's first tile, so that its first
         // MMAs wait for one chunk, not for the whole matrix.
@@ -516,12 +518,12 @@ __device__ __forceinline__ void issue_chunk_ts(uint32_t lead, uint32_t d, uint32
 }
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE, bool PAIR, bool NOPAIR,
-          bool W0RES>
+          bool W0RES, bool TWO>
 __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
                          volatile uint32_t* abort_flag, int issuer = 0) {
   const bool resident = !PAIR && p.resident != 0;   // (as in the producer)
   // two issuers: issuer 0 takes even tiles, 1 odd ones, each in its own sub-ring
-  const bool two = two_issuers(MODE) && p.two_issuers != 0;
+  const bool two = two_issuers(MODE, TWO) && p.two_issuers != 0;
   const uint32_t idesc0 = idesc_f16_f32(BF16 ? 1u : 0u, W0MN ? 1u : 0u, kBlockM, p.N0p);
   const uint32_t idesc1 = idesc_f16_f32(BF16 ? 1u : 0u, W1MN ? 1u : 0u, kBlockM, p.N1p);
   bool ok = true;
@@ -597,9 +599,11 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     const int32_t t = blockIdx.x + it * gridDim.x;
     const uint32_t b = buf_of(p, it);
 
-    if ((MODE != MODE_CHAIN && MODE != MODE_CHAIN3) || PAIR || (!NOPAIR && p.p_tmem)) {
+    if ((MODE != MODE_CHAIN && MODE != MODE_CHAIN3) || PAIR || (!NOPAIR && p.p_tmem && !two)) {
       // The epilogue must have drained the buffer's previous tile (with P in TMEM: its
-      // GEMM1 accumulator, the last thing read from the buffer).
+      // GEMM1 accumulator, the last thing read from the buffer).  (A chain with two
+      // issuers keeps P and D1 apart from D0: D0 was drained before that tile's P was
+      // published, which its GEMM1, issued before this GEMM0, waited for.)
       if (!warp_mbar_wait(bars + 8u * (BAR_ACC_EMPTY0 + b), use_of(p, it) ^ 1u, p, abort_flag,
                           SITE_MMA_ACC_EMPTY, t))
         return false;
@@ -686,8 +690,8 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
       }
       const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
       if (PAIR || (!NOPAIR && p.p_tmem)) {
-        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * static_cast<uint32_t>(kc1), bdesc, idesc1,
-                             nks1, kc1 == 0);
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.pt_col[b] + 32u * static_cast<uint32_t>(kc1),
+                             bdesc, idesc1, nks1, kc1 == 0);
       } else {
         // P buffer b, chunk kc1 (P buffers are whole 1 KiB multiples apart)
         const uint64_t adesc = p_desc0 + ((p.off_p[b] - p.off_p[0]) >> 4) +
@@ -761,7 +765,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         const uint64_t bdesc = ring_w1 + static_cast<uint64_t>(s) * stage_step +
                                static_cast<uint64_t>(slot) * w1_step;
         const int nks1 = kc1 == p.kchunks1 - 1 ? last_nks1 : 4;
-        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.d0_col[b] + 32u * kc1, bdesc, idesc1, nks1,
+        issue_chunk_ts<W1MN>(lead, d1, tmem_base + p.pt_col[b] + 32u * kc1, bdesc, idesc1, nks1,
                              kc1 == 0);
         trace(EV_MMA_ISSUED, 8 + kc1, jj);   // GEMM1 chunks: group 8 + chunk
       }
@@ -870,6 +874,14 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
         ok = issue_g0_half(it, f, false);
         if (ok) ok = issue_g0_half(it, f ^ 1, true);
         if (ok) ok = issue_g1_wide(it);
+      }
+    } else if (MODE == MODE_CHAIN && TWO && two) {
+      // Two issuers: this one takes the tiles issuer, issuer + 2, ..., each GEMM0 then
+      // GEMM1 into buffer `issuer`; while it waits for the epilogue's P, the other issuer's
+      // GEMM0 keeps the tensor core busy.
+      for (int j = issuer; ok && j < ntiles; j += 2) {
+        ok = issue_g0(j);
+        if (ok) ok = issue_g1(j);
       }
     } else if (MODE == MODE_CHAIN && (PAIR || (!NOPAIR && p.p_tmem))) {
       // Pairs of tiles: while the epilogue of one tile drains, the other tile's MMAs run.
@@ -1092,6 +1104,55 @@ __device__ __forceinline__ void drain_to_global(int act, uint32_t tm_lane, uint3
     drain_to_global_act<BF16, 1>(tm_lane, col0, ncols, dst, nvalid, row_ok);
   else
     drain_to_global_act<BF16, 0>(tm_lane, col0, ncols, dst, nvalid, row_ok);
+}
+
+// Accumulator columns [col0, col0 + ncols) of this thread's row (one output pixel) ->
+// act -> dtype -> the output, 16 columns at a time through the warp's 1 KiB slot (32 rows
+// x 32 B, row = lane): one TMA store per step of 16 channels x 16 x 2 pixels at (c, wo0, h0,
+// n), the warp's two output rows; lane 0 first waits until its previous store has read the
+// slot.  Columns at or past `nvalid` are not stored, nor anything if `store` is false (both
+// rows below the image; TMA clips the rest).  A small slot and short steps keep the kernel
+// within its 168-register cap, and TMA writes whole 32-byte sectors where stores from
+// registers (one lane per pixel, 256 bytes apart) take a cache line per lane.
+template <bool BF16, int ACT>
+__device__ __noinline__ void drain16_to_slot_act(uint32_t tm_lane, uint32_t col0, int ncols,
+                                                 int nvalid, uint32_t slot, const CUtensorMap* map,
+                                                 int32_t wo0, int32_t h0, int32_t n, bool store,
+                                                 int lane) {
+  const uint32_t rb = slot + static_cast<uint32_t>(lane) * 32u;
+  for (int c = 0; c < ncols; c += 16) {
+    uint32_t a[16], v[8];
+    tmem_ld16(tm_lane + col0 + c, a);
+    tmem_wait_ld(a);
+    convert16<BF16, ACT>(a, v);
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3])
+                 : "memory");
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + 16u), "r"(v[4]),
+                 "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && store && c < nvalid) {
+      tma_store_4d(map, slot, c, wo0, h0, n);
+      bulk_commit_group();
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void drain16_to_slot(int act, uint32_t tm_lane, uint32_t col0,
+                                                int ncols, int nvalid, uint32_t slot,
+                                                const CUtensorMap* map, int32_t wo0, int32_t h0,
+                                                int32_t n, bool store, int lane) {
+  if (act == 2)
+    drain16_to_slot_act<BF16, 2>(tm_lane, col0, ncols, nvalid, slot, map, wo0, h0, n, store, lane);
+  else if (act == 1)
+    drain16_to_slot_act<BF16, 1>(tm_lane, col0, ncols, nvalid, slot, map, wo0, h0, n, store, lane);
+  else
+    drain16_to_slot_act<BF16, 0>(tm_lane, col0, ncols, nvalid, slot, map, wo0, h0, n, store, lane);
 }
 
 // ------------------------------------------------------------------------------------
@@ -1516,7 +1577,7 @@ __device__ __forceinline__ bool warp_wait(bool alive, uint32_t bar, uint32_t par
 // Epilogue warps.  With epi_groups == 2 warpgroup g (warps 2+4g .. 5+4g) takes the
 // CTA's tiles i with i & 1 == g and owns buffer g; with epi_groups == 1 all eight warps
 // take every tile and warpgroup g drains the 32-column blocks 2k + g.
-template <int MODE, bool A4D, bool BF16, bool WIDE, bool PAIR, bool NOPAIR, bool W0RES>
+template <int MODE, bool A4D, bool BF16, bool WIDE, bool PAIR, bool NOPAIR, bool W0RES, bool TWO>
 __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, uint32_t base,
                               uint32_t bars, uint32_t tmem_base,
                               volatile uint32_t* abort_flag) {
@@ -1552,7 +1613,7 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
     }
     if (alive) {
       if (PAIR || (!NOPAIR && p.p_tmem))
-        drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b], p.N0p, p.d0_col[b]);
+        drain_to_tmem<BF16>(p.act0, tm_lane, p.d0_col[b], p.N0p, p.pt_col[b]);
       else
         drain_to_smem<BF16>(p.act0, tm_lane, p.d0_col[b], c_first, c_step, p.N0p, p_tile,
                             row, kPChunkBytes);
@@ -1586,6 +1647,21 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8u * (BAR_ACC_EMPTY0 + b));
+      if (elected) trace(EV_EPI_STORED, g, it);
+      return;
+    }
+    if constexpr (TWO && A4D) {
+      // (out_slots) Row 32q + lane of the 8 x 16 tile is pixel (ho0 + 2q + lane / 16,
+      // wo0 + lane % 16): each warp stores its two output rows from its own slot.  Nothing
+      // waits for this buffer's D1 but GEMM1 of the group's next tile, which follows the
+      // group's next P.
+      const int32_t h0 = tc.ho0 + 2 * q;
+      const uint32_t slot =
+          base + p.off_out[0] + static_cast<uint32_t>(warp - 2) * kOutSlotBytes;
+      if (alive)   // warp-uniform: the drain's TMEM loads are warp-collective
+        drain16_to_slot<BF16>(p.act1, tm_lane, p.d1_col[b], p.N1p, p.N1, slot, tmOut, tc.wo0,
+                              h0, tc.n, h0 < p.Ho && !*abort_flag, lane);
+      tc_fence_before_sync();
       if (elected) trace(EV_EPI_STORED, g, it);
       return;
     }
@@ -1756,8 +1832,8 @@ __device__ void epilogue_role(const ChainParams& p, const CUtensorMap* tmOut, ui
     }
   }
   // The staging tiles must outlive the stores' reads of them; the writes themselves are
-  // complete when the grid is.
-  if (elected) bulk_wait_read_all();
+  // complete when the grid is.  (Two-issuer chain: lane 0 of every warp stored.)
+  if (TWO ? lane == 0 : elected) bulk_wait_read_all();
 }
 
 // ------------------------------------------------------------------------------------
@@ -1832,8 +1908,8 @@ __device__ __forceinline__ void fill_w2(const ChainParams& p, uint8_t* dst, int 
 // the kernel
 // ------------------------------------------------------------------------------------
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false, bool NOPAIR = false, bool W0RES = false>
-__global__ void __launch_bounds__(chain_threads(MODE), 1)
+          bool PAIR = false, bool NOPAIR = false, bool W0RES = false, bool TWO = false>
+__global__ void __launch_bounds__(chain_threads(MODE, TWO), 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW0,
                  const __grid_constant__ CUtensorMap tmW1,
                  const __grid_constant__ CUtensorMap tmOut, const ChainParams p) {
@@ -1874,7 +1950,7 @@ __global__ void __launch_bounds__(chain_threads(MODE), 1)
         mbar_init(bars + 8u * (BAR_D2_FULL0 + a), 1);
       }
     }
-    mbar_init(bars + 8u * BAR_MMA_DONE, two_issuers(MODE) && p.two_issuers ? 2u : 1u);
+    mbar_init(bars + 8u * BAR_MMA_DONE, two_issuers(MODE, TWO) && p.two_issuers ? 2u : 1u);
     mbar_init(bars + 8u * BAR_BIAS_READY, kNumEpiWarps);
     if (W0RES)
       for (uint32_t c = 0; c < static_cast<uint32_t>(kMaxW0Chunks); ++c)
@@ -1922,16 +1998,16 @@ __global__ void __launch_bounds__(chain_threads(MODE), 1)
       }
     }
     __syncwarp();
-    producer_role<MODE, A4D, W0MN, W1MN, WIDE, PAIR, NOPAIR, W0RES>(p, &tmA, &tmW0, &tmW1, base,
+    producer_role<MODE, A4D, W0MN, W1MN, WIDE, PAIR, NOPAIR, W0RES, TWO>(p, &tmA, &tmW0, &tmW1, base,
                                                                    bars, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>(p, base, bars, tmem_base,
+    mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES, TWO>(p, base, bars, tmem_base,
                                                                     abort_flag, 0);
     __syncwarp();
-  } else if (two_issuers(MODE) && warp == kSecondIssuerWarp) {
+  } else if (two_issuers(MODE, TWO) && warp == kSecondIssuerWarp) {
     if (p.two_issuers)
-      mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>(p, base, bars, tmem_base,
+      mma_role<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES, TWO>(p, base, bars, tmem_base,
                                                                       abort_flag, 1);
     __syncwarp();
   } else {
@@ -1946,7 +2022,7 @@ __global__ void __launch_bounds__(chain_threads(MODE), 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8u * BAR_BIAS_READY);
-    epilogue_role<MODE, A4D, BF16, WIDE, PAIR, NOPAIR, W0RES>(p, &tmOut, base, bars, tmem_base,
+    epilogue_role<MODE, A4D, BF16, WIDE, PAIR, NOPAIR, W0RES, TWO>(p, &tmOut, base, bars, tmem_base,
                                                               abort_flag);
   }
 

@@ -76,14 +76,18 @@ constexpr int kChunkK = 64;           // K elements per staged chunk (128 B rows
 constexpr int kNumEpiWarps = 8;       // two warpgroups of four (one per TMEM lane quadrant)
 constexpr int kNumEpiThreads = 32 * kNumEpiWarps;
 constexpr int kNumThreads = 64 + kNumEpiThreads;   // warp 0 TMA, warp 1 MMA + TMEM, 2..9 epilogue
-// The conv + pool kernel (MODE_POOL, one GEMM per tile) adds warp 10, a possible second MMA
-// issuer (ChainParams::two_issuers): warps 1 and 10 then take alternate tiles (each its own
-// accumulator), so that one issues while the other waits between ring stages.  With N = 64
-// the tensor core finishes an MMA in ~48 cycles and accepts only a short queue of them, so
-// every cycle a single issuer spends on barriers and bookkeeping leaves it idle.
-__host__ __device__ constexpr bool two_issuers(int mode) { return mode == 2; }
-__host__ __device__ constexpr int chain_threads(int mode) {
-  return kNumThreads + (two_issuers(mode) ? 32 : 0);
+// The conv + pool kernel (MODE_POOL) and the conv chain's two-issuer instantiation (the
+// kernel's TWO template parameter, `two` below) add warp 10, a possible second MMA issuer
+// (ChainParams::two_issuers): warps 1 and 10 then take alternate tiles (each its own
+// accumulators), so that one issues while the other waits between ring stages or for its
+// epilogue.  With N = 64 the tensor core finishes an MMA in ~48 cycles and accepts only a
+// short queue of them, so every cycle a single issuer spends on barriers and bookkeeping
+// leaves it idle.
+__host__ __device__ constexpr bool two_issuers(int mode, bool two) {
+  return mode == 2 || (mode == 0 && two);
+}
+__host__ __device__ constexpr int chain_threads(int mode, bool two) {
+  return kNumThreads + (two_issuers(mode, two) ? 32 : 0);
 }
 constexpr int kSecondIssuerWarp = kNumThreads / 32;
 constexpr int kMaxStages = 8;
@@ -91,6 +95,7 @@ constexpr int kMaxBufs = 4;          // accumulator / P buffers per CTA
 constexpr int kMaxW0Chunks = 8;      // K chunks of a W0 kept resident beside streamed W1
 // Bias operands in shared memory (at off_bias): a 1 KiB ONES tile, then per GEMM one
 // 2 KiB BIAS block per 64-wide N block.
+constexpr uint32_t kOutSlotBytes = 1024;   // out_slots: 32 rows x 16 columns per warp
 constexpr uint32_t kOnesBytes = 1024;
 constexpr uint32_t kBiasBlockBytes = 2048;
 constexpr uint32_t kABytes = kBlockM * kChunkK * 2;   // 16 KiB A chunk
@@ -168,9 +173,16 @@ struct ChainParams {
                                 //    W0 and of W1 (w0/w1_chunk_bytes are the halves' chunks)
   uint8_t* out_ptr;             // w0_res, cta_pair: the output D [M][out_ld] row-major
   int32_t out_ld;               // w0_res, cta_pair: elements per output row
-  int32_t two_issuers;          // (MODE_POOL) 1: warps 1 and 10 issue the MMAs
-                                //    of alternate tiles, the ring split into two sub-rings
-                                //    (subring_pos); 0: warp 1 alone, warp 10 idle
+  int32_t two_issuers;          // (MODE_POOL; MODE_CHAIN with 4-D A, resident filters and
+                                //    P in TMEM) 1: warps 1 and 10 issue the MMAs of
+                                //    alternate tiles, the ring split into two sub-rings
+                                //    (subring_pos); 0: warp 1 alone, warp 10 idle.  A chain
+                                //    then keeps D1 apart from D0 / P in TMEM (buffer b =
+                                //    issuer b) and stores its output with out_slots
+  int32_t out_slots;            // (two-issuer conv chain) 1: each epilogue warp stages its 32
+                                //    rows' output 16 columns at a time in a 1 KiB slot of
+                                //    its own (kOutSlotBytes from off_out[0], unswizzled) and
+                                //    stores it with TMA (box of 16 channels x 16 x 2 pixels)
   int32_t out_stage;            // cta_pair: 1 if each epilogue warp stages its 32 rows' output
                                 //    64 columns at a time (4 KiB per warp from off_out[0],
                                 //    128B-swizzled) and stores them with TMA; 0: stored
@@ -189,6 +201,8 @@ struct ChainParams {
                                 // 1: both warpgroups split the columns of every tile
   uint32_t tmem_cols;
   uint32_t d0_col[kMaxBufs], d1_col[kMaxBufs];  // TMEM columns of the accumulator buffers
+  uint32_t pt_col[2];           // (P in TMEM) TMEM column of buffer b's packed P: over its D0
+                                //    (d0_col[b]), or, with two issuers, a region of its own
   uint64_t wait_limit_ns;
   uint32_t kernel_id;
   uint32_t* err;                // device error word {code, kernel, site, tile}

@@ -10,19 +10,19 @@ namespace b2b {
 namespace B2B_KNS {
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false, bool NOPAIR = false, bool W0RES = false>
+          bool PAIR = false, bool NOPAIR = false, bool W0RES = false, bool TWO = false>
 const void* kernel_ptr() {
   return reinterpret_cast<const void*>(
-      &chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>);
+      &chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES, TWO>);
 }
 
 template <int MODE, bool A4D, bool W0MN, bool W1MN, bool BF16, bool WIDE = false,
-          bool PAIR = false, bool NOPAIR = false, bool W0RES = false>
+          bool PAIR = false, bool NOPAIR = false, bool W0RES = false, bool TWO = false>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1,
                        const CUtensorMap& out, const ChainParams& p, int grid, size_t smem,
                        cudaStream_t stream) {
-  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES>, a, w0,
-                      w1, out, p, grid, smem, stream, chain_threads(MODE));
+  return launch_chain(chain_kernel<MODE, A4D, W0MN, W1MN, BF16, WIDE, PAIR, NOPAIR, W0RES, TWO>, a, w0,
+                      w1, out, p, grid, smem, stream, chain_threads(MODE, TWO));
 }
 
 // 2-D A operand: GEMM chains (row-major weights) and 1x1 convs (K-major filters).
@@ -89,6 +89,8 @@ const void* variant_func_a4d(Variant v) {
       return kernel_ptr<MODE_CHAIN, true, false, false, BF16, false, false, true>();
     case V_CONV_SINGLE: return kernel_ptr<MODE_SINGLE, true, false, false, BF16>();
     case V_CONV_POOL: return kernel_ptr<MODE_POOL, true, false, false, BF16>();
+    case V_CONV_CHAIN_2I:
+      return kernel_ptr<MODE_CHAIN, true, false, false, BF16, false, false, false, false, true>();
     default: return nullptr;
   }
 }
@@ -107,6 +109,9 @@ cudaError_t launch_variant_a4d(Variant v, const CUtensorMap& a, const CUtensorMa
       return launch_one<MODE_SINGLE, true, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
     case V_CONV_POOL:
       return launch_one<MODE_POOL, true, false, false, BF16>(a, w0, w1, out, p, grid, smem, s);
+    case V_CONV_CHAIN_2I:
+      return launch_one<MODE_CHAIN, true, false, false, BF16, false, false, false, false, true>(
+          a, w0, w1, out, p, grid, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }

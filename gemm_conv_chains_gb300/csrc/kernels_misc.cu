@@ -39,7 +39,8 @@ B2B_UNIT_DECLS
 #undef B2B_UNIT_DECLS
 
 static bool is_a4d(Variant v) {
-  return v == V_CONV_CHAIN || v == V_CONV_CHAIN_NP || v == V_CONV_SINGLE || v == V_CONV_POOL;
+  return v == V_CONV_CHAIN || v == V_CONV_CHAIN_NP || v == V_CONV_CHAIN_2I || v == V_CONV_SINGLE ||
+         v == V_CONV_POOL;
 }
 
 const void* variant_func(Variant v, bool bf16, bool trace) {

@@ -29,6 +29,8 @@ enum Variant : int {
   V_GEMM_CHAIN_PAIR_W0,   // tile pairs, P in TMEM, W0 resident, A and W1 streamed, output
                           //   stored from registers
   V_GEMM_CHAIN_CTA2,      // the chain over CTA pairs (chain_cta2_kernel.cuh)
+  V_CONV_CHAIN_2I,        // conv chain, two MMA issuers, P in TMEM, output stored from
+                          //   registers
   V_COUNT
 };
 

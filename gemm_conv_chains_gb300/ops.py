@@ -408,7 +408,7 @@ PLAN_FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring",
                "a_stage_bytes", "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2",
                "d1_col3", "cand", "ncand", "grid_choice", "pf_choice", "ring_extend", "off_w2",
                "off_p1_0", "off_p1_1", "d2_col0", "d2_col1", "p_split", "w0_res", "cta_pair",
-               "two_issuers"]
+               "two_issuers", "out_slots", "pt_col0", "pt_col1"]
 _SIGNED_PLAN_FIELDS = ("grid_choice", "pf_choice")
 PLAN_KINDS = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
               "conv_relu_maxpool": 4, "b2b_gemm3": 5}

@@ -285,7 +285,11 @@ def chain_buffers(plan: dict) -> List[Buffer]:
     out_cols = plan["N1p"] if chain else plan["N0p"]
     per_chunk = 32 * 128 if plan["mode"] == 2 else 128 * 128   # pooled: 4 x 8 pixels per tile
     out_bytes = (out_cols + 63) // 64 * per_chunk
-    # (W0 resident beside streamed W1: the output leaves from registers, no staging)
+    # (W0 resident beside streamed W1: the output leaves from registers, no staging; the
+    # conv chain's two-issuer layout: one 1 KiB slot per epilogue warp, `out` bytes in all)
+    if plan.get("out_slots"):
+        return bufs + [Buffer(f"P{i}", p_bytes, whole) for i in range(pbufs)] + \
+            [Buffer("out", plan["out"], whole)]
     obufs = 0 if plan.get("w0_res") else (2 if plan["groups"] == 2 else 1)
     paired = bool(plan["alias"]) and pbufs == obufs
     for i in range(pbufs):

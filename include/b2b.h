@@ -251,7 +251,7 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * filed per variant, since each dtype and epilogue pair runs its own kernel instantiation;
  * sizes alone address every variant (see b2b_set_choice).  Any other count of dims, or a
  * variant value out of range, returns B2B_ERR_SHAPE.
- * out (out_len >= 61) receives, in order: dynamic smem bytes, ring stages, stage bytes,
+ * out (out_len >= 64) receives, in order: dynamic smem bytes, ring stages, stage bytes,
  * weights resident (0/1), output staging aliases P (0/1), ring offset, ring bytes,
  * resident-weight offset, W1 offset, resident bytes, W0 chunk bytes, W1 chunk bytes,
  * P offsets [2], bytes per P buffer, staging offsets [2], bytes per staging buffer,
@@ -274,9 +274,12 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * else 0), and 1 if W0 alone stays resident while A and W1 stream through the ring (P in
  * TMEM, tile pairs; the output is then stored from registers, with no staging tile), and
  * 1 if the chain runs over CTA pairs (clusters of two CTAs sharing each MMA of 256 rows,
- * each holding half of W0 and W1; tiles then count 256 rows), and 1 if two warps issue
- * the MMAs of alternate tiles, each from its own half of the ring (single-GEMM and pool
- * kernels with N <= 128 and four or more ring stages).  A choice pinned,
+ * each holding half of W0 and W1; tiles then count 256 rows), 1 if two warps issue
+ * the MMAs of alternate tiles, each from its own half of the ring (the conv + pool kernel
+ * with N0 <= 64 when half the ring holds a tile's stages; conv chains with halo boxes and
+ * N0 <= 64 in their two-issuer layout), 1 if each epilogue warp stages its output 16
+ * columns at a time in a 1 KiB slot of its own (that two-issuer layout), and the TMEM
+ * columns of the two P buffers when P is kept in TMEM (else 0).  A choice pinned,
  * measured or ranked for these sizes is reflected; without one, the layout is the
  * tile-graph model's pick, as the entry point takes it (see b2b_set_autotune).
  * Returns the status the entry point would return for these sizes (B2B_OK if it would

@@ -23,7 +23,8 @@ FIELDS = ["smem", "stages", "stage_bytes", "resident", "alias", "off_ring", "rin
           "N0p", "N1p", "mode", "p_tmem", "w1_group", "w1_per_stage", "halo", "a_stage_bytes",
           "nbuf", "off_p2", "off_p3", "d0_col2", "d0_col3", "d1_col2", "d1_col3", "cand", "ncand",
           "grid_choice", "pf_choice", "ring_extend", "off_w2", "off_p1_0", "off_p1_1", "d2_col0",
-          "d2_col1", "p_split", "w0_res", "cta_pair", "two_issuers"]
+          "d2_col1", "p_split", "w0_res", "cta_pair", "two_issuers", "out_slots", "pt_col0",
+          "pt_col1"]
 SMEM_LIMIT = 227 * 1024
 KIND = {"b2b_gemm": 0, "gemm_bias_act": 1, "b2b_conv_nhwc": 2, "conv_bias_act_nhwc": 3,
         "conv_relu_maxpool": 4, "b2b_gemm3": 5}
@@ -126,11 +127,25 @@ def check(kind, dims, row_major_w):
         assert p["p"] >= need_p
         for b in range(pbufs):
             regions.append((f"p{b}", p[f"off_p{b}"], p["p"]))
+    slots = p["out_slots"] == 1
+    if slots:
+        # the conv chain's two-issuer layout: halo boxes over resident filters, P in TMEM,
+        # two sub-rings that each hold a whole tile's stages, and a 1 KiB output slot per
+        # epilogue warp (32 rows x 16 columns)
+        assert mode == 0 and p["two_issuers"] and p["halo"] and p["resident"] and p_tmem
+        assert dual and groups == 2 and nbuf == 2 and N0p <= 64 and not p["alias"]
+        assert p["stages"] // 2 >= p["kchunks0"] // R
+        assert p["out"] == 8 * 1024 and p["off_out0"] == p["off_out1"]
+        regions.append(("slots", p["off_out0"], p["out"]))
+    if p["two_issuers"] and mode == 0:
+        assert slots
     if p["alias"]:
         assert mode == 0
         # staging b (used by epilogue group b, which handles the tiles using P[b])
         for b in range(obufs):
             assert p[f"off_out{b}"] == p[f"off_p{b if dual else 0}"]
+    elif slots:
+        pass
     elif w0_res:
         assert p["out"] == 0
     else:
@@ -162,9 +177,22 @@ def check(kind, dims, row_major_w):
     assert p["tmem_cols"] in (32, 64, 128, 256, 512)
     if wide:
         return p
+    if p_tmem and slots:
+        # two issuers: D0, P (packed) and D1 of each buffer in disjoint column ranges
+        accs = []
+        for b in range(2):
+            accs += [(f"d0_{b}", p[f"d0_col{b}"], N0p), (f"p_{b}", p[f"pt_col{b}"], N0p // 2),
+                     (f"d1_{b}", p[f"d1_col{b}"], N1p)]
+        for name, col, n in accs:
+            assert col % 32 == 0 and col + n <= p["tmem_cols"], (name, col, n)
+        for (a, ca, na), (b, cb, nb) in itertools.combinations(accs, 2):
+            assert ca + na <= cb or cb + nb <= ca, (a, b)
+        return p
     if p_tmem:
         # buffer b: D0 [d0, d0 + N0p); P (packed) [d0, d0 + N0p/2); D1 [d1, d1 + N1p) after P
         spans = []
+        for b in range(2):
+            assert p[f"pt_col{b}"] == p[f"d0_col{b}"]
         for b in range(2):
             d0, d1 = p[f"d0_col{b}"], p[f"d1_col{b}"]
             assert d0 % 32 == 0 and d1 % 32 == 0
