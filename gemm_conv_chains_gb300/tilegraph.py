@@ -569,8 +569,8 @@ def bounds_report(measured_us: Optional[Dict[str, float]] = None) -> str:
     """Markdown table of launch_bounds for every workload, beside measured microseconds per
     launch where given (name -> us)."""
     measured_us = measured_us or {}
-    lines = ["| workload | tiles per CTA (max) | HBM us | L2 -> SM us | tensor us | floor | "
-             "measured us | floor / measured |", "|---|---|---|---|---|---|---|---|"]
+    lines = ["| workload | tiles per CTA or CTA pair (max) | HBM us | L2 -> SM us | tensor us "
+             "| floor | measured us | floor / measured |", "|---|---|---|---|---|---|---|---|"]
     for name, w in wl.WORKLOADS.items():
         plan = plan_of(w)
         b = launch_bounds(w, plan)
@@ -578,7 +578,8 @@ def bounds_report(measured_us: Optional[Dict[str, float]] = None) -> str:
         got = "" if m is None else f"{m:.2f}"
         frac = "" if m is None else f"{b['floor_us'] / m:.2f}"
         lines.append(
-            f"| {name} | {max(tiles_per_cta(plan['tiles'], 152))} | {b['hbm_us']:.2f} "
+            f"| {name} | {max(tiles_per_cta(plan['tiles'], 76 if plan.get('cta_pair') else 152))} "
+            f"| {b['hbm_us']:.2f} "
             f"| {b['l2_us']:.2f} | {b['tensor_us']:.2f} | {b['floor_us']:.2f} ({b['bound']}) "
             f"| {got} | {frac} |")
     return "\n".join(lines)
