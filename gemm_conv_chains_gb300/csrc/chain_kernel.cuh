@@ -1402,8 +1402,9 @@ __device__ __noinline__ void drain64_release_to_global_act(uint32_t tm_lane, uin
 // 64 packed output columns of this lane's row (v) -> the warp's staging slot (32 rows x
 // 128 B, 128B-swizzled: the output map's box of 64 columns x 32 rows) -> one TMA store at
 // output column `col`, rows row0 .. row0 + 31 (TMA clips rows past the output; a box whose
-// rows all lie past it is not issued).  Lane 0 first waits until its previous store has
-// read the slot.
+// rows all lie past it is not issued), marked evict-first in L2 (the output is not read
+// again here; measured ~1 % faster on the FFN-like chain over CTA pairs).  Lane 0 first
+// waits until its previous store has read the slot.
 __device__ __forceinline__ void stage_store64(const uint32_t (&v)[32], uint32_t slot,
                                               const CUtensorMap* map, int col, int32_t row0,
                                               int64_t rows, int lane) {
@@ -1419,7 +1420,7 @@ __device__ __forceinline__ void stage_store64(const uint32_t (&v)[32], uint32_t 
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0 && row0 < rows) {
-    tma_store_2d(map, slot, col, row0);
+    tma_store_2d_hint(map, slot, col, row0, l2_policy_evict_first());
     bulk_commit_group();
   }
 }
