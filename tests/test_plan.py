@@ -490,19 +490,31 @@ def test_wide_chain_limits():
     assert plan("gemm_bias_act", (1000, 64, 264))[0] == 4     # single operators keep N <= 256
 
 
-def test_two_issuers_only_for_the_pooled_conv():
+def test_two_issuers_only_for_the_n64_halo_convs():
     # the conv + pool kernel with N <= 64 whose ring holds two tiles' stages splits it
-    # between two MMA issuers; every other kernel keeps one
+    # between two MMA issuers, and so does the conv chain with halo boxes and N0 <= 64 in
+    # its own layout (P in TMEM, per-warp output slots, a six-stage ring); every other
+    # kernel keeps one
     pool = check("conv_relu_maxpool", (32, 112, 112, 64, 64), False)
     assert pool["two_issuers"] == 1 and pool["stages"] // 2 >= 3
+    chain = check("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128), False)
+    assert chain["two_issuers"] == 1 and chain["out_slots"] == 1 and chain["halo"] == 1
+    assert chain["stages"] == 6 and chain["p_tmem"] == 1 and chain["out"] == 8 * 1024
     for kind, dims, rm in (("conv_bias_act_nhwc", (32, 56, 56, 64, 64, 3, 3, 1), False),
                            ("gemm_bias_act", (200704, 64, 64), True),
                            ("gemm_bias_act", (32768, 256, 256), True),
-                           ("b2b_gemm", (1024, 64, 64, 64), True)):
+                           ("b2b_gemm", (1024, 64, 64, 64), True),
+                           # a 1x1 chain (no halo boxes), a halo chain with N0 = 128
+                           ("b2b_conv_nhwc", (64, 56, 56, 64, 64, 1, 1, 0, 64), False),
+                           ("b2b_conv_nhwc", (8, 28, 28, 64, 128, 3, 3, 1, 64), False)):
         assert check(kind, dims, rm)["two_issuers"] == 0
-    # the same pooled conv with streamed filters: nine stages per tile, one issuer
+    # the same pooled conv with streamed filters: nine stages per tile, one issuer; the
+    # chain's other layouts keep one issuer
     ops.set_choice("conv_relu_maxpool", (32, 112, 112, 64, 64), cand=1)
+    ops.set_choice("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128), cand=1)
     try:
         assert check("conv_relu_maxpool", (32, 112, 112, 64, 64), False)["two_issuers"] == 0
+        other = check("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128), False)
+        assert other["two_issuers"] == 0 and other["out_slots"] == 0
     finally:
         ops.autotune_reset()
