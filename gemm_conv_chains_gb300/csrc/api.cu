@@ -517,19 +517,29 @@ bool plan_smem_chain3(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   const uint32_t w_res = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes +
                          static_cast<uint32_t>(p.kchunks1) * p.w1_chunk_bytes +
                          static_cast<uint32_t>(p.kchunks2) * p.w2_chunk_bytes;
-  const uint64_t fixed = uint64_t{w_res} + 2u * (p0_bytes + p1_bytes + out_bytes) + bias_bytes +
-                         bar_bytes;
-  if (fixed >= budget) return false;
-  const uint32_t stages =
-      std::min<uint32_t>(kMaxStages, (budget - static_cast<uint32_t>(fixed)) / kABytes);
+  // The output staging of buffer b may share P0[b]'s space: the group that owns buffer b
+  // writes it only after GEMM2 of the tile (so GEMM1 has read P0[b]) and waits for the TMA
+  // store to have read it before its next tile's P0.  Taken when separate staging would
+  // leave fewer than three ring stages.
+  auto stages_for = [&](bool alias) -> uint32_t {
+    const uint64_t fixed = uint64_t{w_res} +
+                           2u * ((alias ? std::max(p0_bytes, out_bytes) : p0_bytes + out_bytes) +
+                                 p1_bytes) +
+                           bias_bytes + bar_bytes;
+    if (fixed >= budget) return 0u;
+    return std::min<uint32_t>(kMaxStages, (budget - static_cast<uint32_t>(fixed)) / kABytes);
+  };
+  const bool alias = stages_for(false) < 3u && stages_for(true) > stages_for(false);
+  const uint32_t stages = stages_for(alias);
   if (stages < 2u) return false;
+  const uint32_t p0_each = alias ? std::max(p0_bytes, out_bytes) : p0_bytes;
   p.tmem_cols = tmem_layout(p, MODE_CHAIN3, 2u);
   if (p.tmem_cols > 512u) return false;
   p.acc_dual = 1;
   p.nbuf_log2 = 1;
   p.epi_groups = 2;
   p.resident = 1;
-  p.out_alias_p = 0;
+  p.out_alias_p = alias ? 1 : 0;
   p.p_tmem = 0;
   p.halo = 0;
   p.num_stages = stages;
@@ -543,8 +553,8 @@ bool plan_smem_chain3(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   r.ncand = 1;
   r.ring = stages * kABytes;
   r.w_res = w_res;
-  r.p_each = p0_bytes;
-  r.out_each = out_bytes;
+  r.p_each = p0_each;
+  r.out_each = alias ? 0u : out_bytes;
   r.bias = bias_bytes;
   r.bar = bar_bytes;
   uint32_t off = 0;
@@ -554,12 +564,12 @@ bool plan_smem_chain3(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   p.off_w1 = p.off_w0 + static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
   p.off_w2 = p.off_w1 + static_cast<uint32_t>(p.kchunks1) * p.w1_chunk_bytes;
   off += w_res;
-  for (uint32_t b = 0; b < kMaxBufs; ++b) p.off_p[b] = off + (b & 1u) * p0_bytes;
-  off += 2u * p0_bytes;
+  for (uint32_t b = 0; b < kMaxBufs; ++b) p.off_p[b] = off + (b & 1u) * p0_each;
+  off += 2u * p0_each;
   for (uint32_t b = 0; b < 2; ++b) p.off_p1[b] = off + b * p1_bytes;
   off += 2u * p1_bytes;
-  for (uint32_t b = 0; b < 2; ++b) p.off_out[b] = off + b * out_bytes;
-  off += 2u * out_bytes;
+  for (uint32_t b = 0; b < 2; ++b) p.off_out[b] = alias ? p.off_p[b] : off + b * out_bytes;
+  if (!alias) off += 2u * out_bytes;
   p.off_bias = off;
   off += bias_bytes;
   p.off_bar = off;

@@ -273,11 +273,13 @@ def chain_buffers(plan: dict) -> List[Buffer]:
     if plan["resident"] or plan.get("w0_res"):
         bufs.append(Buffer("weights", plan["w_res"], whole))
     if plan["mode"] == 3:
-        # three-operator chain: two tiles in flight hold P0, P1 and the staging of both
+        # three-operator chain: two tiles in flight hold P0, P1 and the staging of both (with
+        # `alias`, staging b shares P0[b]'s space: the P0 buffers are then that size)
         p1 = (plan["off_p1_1"] - plan["off_p1_0"])
         for b in range(2):
-            bufs += [Buffer(f"P0{b}", plan["p"], whole), Buffer(f"P1{b}", p1, whole),
-                     Buffer(f"out{b}", plan["out"], whole)]
+            bufs += [Buffer(f"P0{b}", plan["p"], whole), Buffer(f"P1{b}", p1, whole)]
+            if not plan["alias"]:
+                bufs.append(Buffer(f"out{b}", plan["out"], whole))
         return bufs
     chain = plan["mode"] == 0
     pbufs = plan["nbuf"] if (chain and not plan["p_tmem"]) else 0

@@ -436,14 +436,21 @@ def test_gemm3_plans(dims):
     assert p["stages"] >= 2 and p["stage_bytes"] == 16384 and p["smem"] <= SMEM_LIMIT
     k0, k1, k2 = -(-K0 // 64), -(-r16(N0) // 64), -(-r16(N1) // 64)
     assert p["kchunks0"] == k0 and p["kchunks1"] == k1
+    p0 = max(n0b, n2b) * 16384 if p["alias"] else n0b * 16384
     regions = [("ring", p["off_ring"], p["ring"]),
                ("w0", p["off_w0"], k0 * n0b * 8192), ("w1", p["off_w1"], k1 * n1b * 8192),
                ("w2", p["off_w2"], k2 * n2b * 8192),
-               ("p0a", p["off_p0"], n0b * 16384), ("p0b", p["off_p1"], n0b * 16384),
+               ("p0a", p["off_p0"], p0), ("p0b", p["off_p1"], p0),
                ("p1a", p["off_p1_0"], n1b * 16384), ("p1b", p["off_p1_1"], n1b * 16384),
-               ("outa", p["off_out0"], n2b * 16384), ("outb", p["off_out1"], n2b * 16384),
                ("bias", p["off_bias"], 1024 + 2048 * (n0b + n1b + n2b)),
                ("bar", p["off_bar"], 8 * 43 + 8)]
+    if p["alias"]:
+        # output staging b shares P0[b]'s space, taken only where separate staging would
+        # leave fewer than three ring stages
+        assert p["off_out0"] == p["off_p0"] and p["off_out1"] == p["off_p1"] and p["out"] == 0
+        assert p["stages"] >= 3
+    else:
+        regions += [("outa", p["off_out0"], n2b * 16384), ("outb", p["off_out1"], n2b * 16384)]
     for name, off, size in regions:
         assert off % 1024 == 0 and off + size <= p["smem"] - 1024, name
     for (a, oa, sa), (b, ob, sb) in itertools.combinations(regions, 2):
@@ -453,6 +460,13 @@ def test_gemm3_plans(dims):
         assert c % 32 == 0 and c + n <= p["tmem_cols"] <= 512
     for (ca, na), (cb, nb) in itertools.combinations(cols, 2):
         assert ca + na <= cb or cb + nb <= ca
+
+
+def test_gemm3_mlp3_aliases_its_staging():
+    # the three-operator workload (128 -> 128 -> 64 -> 64): separate staging leaves two
+    # ring stages, sharing P0's space four
+    st, p = plan("b2b_gemm3", (32768, 128, 128, 64, 64))
+    assert st == 0 and p["alias"] == 1 and p["stages"] == 4
 
 
 def test_gemm3_limits():
