@@ -261,6 +261,7 @@ CONV_SHAPES = [
     ("f16", 2, 7, 9, 64, 64, 1, 1, 0, 64),     # the 1x1 path (GEMM over pixels)
     ("f16", 1, 6, 6, 16, 16, 1, 3, 1, 16),     # non-square filter, wider output
     ("bf16", 1, 5, 5, 8, 8, 1, 1, 1, 8),       # 1x1 with padding: zero border rows
+    ("bf16", 16, 30, 44, 64, 64, 3, 3, 1, 32),  # 192 ragged tiles: both MMA issuers busy
 ]
 
 
