@@ -41,11 +41,13 @@ struct DeviceState {
   int num_sms = 0;
   uint32_t* err = nullptr;                    // device address of g_error_word
   cudaError_t init_error = cudaSuccess;
-  std::atomic<uint64_t> attr_done{0};   // bit 2 (v + V_COUNT traced) + bf16: smem attribute set
+  // bit 2 (v + V_COUNT traced) + bf16 of the pair of words: smem attribute set
+  std::atomic<uint64_t> attr_done[2] = {0, 0};
   // CTA-pair kernel: resident clusters of two (per bf16 + 2 * traced), for the dynamic
   // shared memory size they were computed for; 0 = not yet known
-  std::atomic<int> cta2_clusters[4] = {0, 0, 0, 0};
-  std::atomic<size_t> cta2_smem[4] = {0, 0, 0, 0};
+  // per pair kernel (+4: conv + pool), dtype (+1: bf16) and build (+2: traced)
+  std::atomic<int> cta2_clusters[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  std::atomic<size_t> cta2_smem[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 };
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
@@ -659,6 +661,80 @@ bool plan_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   return *smem_bytes <= kSmemLimit;
 }
 
+// Shared-memory plan of the conv + pool kernel over CTA pairs (chain_cta2_pool_kernel.cuh;
+// stride 1, R > 1, N0p <= 128): per CTA a ring of halo boxes of its own 8 x 16 tile, its
+// half of the filters resident (N0p / 2 rows of every tap and channel block), one pooled
+// staging tile per epilogue warpgroup, the ONES tile and a K-major bias block of its half,
+// the barriers; four accumulators of N0p columns in TMEM.  At least one tile's ring stages
+// and one more.  p.num_tiles stays the count of 8 x 16 tiles (two per pair-tile).
+bool plan_pool_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
+  if (p.R < 2 || p.stride != 1 || p.N0p > 128 || p.N0p % 16 != 0) return false;
+  const uint32_t budget = kSmemLimit - 1024u;
+  const uint32_t half = static_cast<uint32_t>(p.N0p) / 2u;
+  p.w0_chunk_bytes = half * 128u;
+  const uint32_t w0b = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
+  const uint32_t nch = static_cast<uint32_t>((p.N0p + 63) / 64);
+  const uint32_t out_each = nch * kPoolChunkBytes;
+  const uint32_t bias_bytes = round_up(kOnesBytes + half * 128u, 1024u);
+  const uint32_t bar_bytes = 1024u;
+  const uint32_t a_bytes = (7u + static_cast<uint32_t>(p.R)) * 2048u;
+  const uint32_t kst = static_cast<uint32_t>(p.S * p.kc_per_tap);
+  const uint32_t fixed = round_up(w0b, 1024u) + 2u * out_each + bias_bytes + bar_bytes;
+  if (fixed >= budget) return false;
+  const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / a_bytes);
+  if (stages < kst + 1u) return false;
+  const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
+  p.tmem_cols = pow2_at_least(4u * s0);
+  if (p.tmem_cols > 512u) return false;
+  for (uint32_t b = 0; b < kMaxBufs; ++b) {
+    p.d0_col[b] = b * s0;
+    p.d1_col[b] = 0;
+  }
+  p.cta_pair = 1;
+  p.acc_dual = 1;
+  p.nbuf_log2 = 2;
+  p.epi_groups = 2;
+  p.resident = 1;
+  p.w0_res = 0;
+  p.out_alias_p = 0;
+  p.p_tmem = 0;
+  p.halo = 1;
+  // two MMA issuers in the leader, each over half of the ring, where half holds a tile
+  p.two_issuers = stages / 2u >= kst ? 1 : 0;
+  p.num_stages = stages;
+  p.stage_bytes = a_bytes;
+  p.a_stage_bytes = a_bytes;
+  p.kstages0 = static_cast<int32_t>(kst);
+  p.w1_group = 0;
+  p.w1_per_stage = 1;
+  uint32_t off = 0;
+  p.off_ring = off;
+  off += stages * a_bytes;
+  p.off_w0 = off;
+  p.off_w1 = off;
+  off += round_up(w0b, 1024u);
+  for (uint32_t b = 0; b < kMaxBufs; ++b) p.off_p[b] = 0;
+  p.off_out[0] = off;
+  p.off_out[1] = off + out_each;
+  off += 2u * out_each;
+  p.off_bias = off;
+  off += bias_bytes;
+  p.off_bar = off;
+  off += bar_bytes;
+  if (regions) {
+    Regions r;
+    r.ring = stages * a_bytes;
+    r.w_res = round_up(w0b, 1024u);
+    r.p_each = 0;
+    r.out_each = out_each;
+    r.bias = bias_bytes;
+    r.bar = bar_bytes;
+    *regions = r;
+  }
+  *smem_bytes = off + 1024u;
+  return *smem_bytes <= kSmemLimit;
+}
+
 void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const void* b1,
                  DeviceState* d, uint32_t kid) {
   p.is_bf16 = dt == B2B_BF16 ? 1 : 0;
@@ -677,16 +753,18 @@ void fill_common(ChainParams& p, int dt, int e0, int e1, const void* b0, const v
 
 // Lets the kernel of variant v (the launch's dtype and build) use the full shared memory.
 b2b_status ensure_smem_attribute(Variant v, DeviceState* d, bool bf16, bool traced) {
-  const uint64_t bit = 1ull << (2u * (static_cast<uint32_t>(v) + (traced ? V_COUNT : 0u)) +
-                                (bf16 ? 1u : 0u));
-  if ((d->attr_done.load() & bit) == 0u) {
+  const uint32_t idx = 2u * (static_cast<uint32_t>(v) + (traced ? V_COUNT : 0u)) + (bf16 ? 1u : 0u);
+  static_assert(4 * V_COUNT <= 128, "attribute bits");
+  std::atomic<uint64_t>& word = d->attr_done[idx >> 6];
+  const uint64_t bit = 1ull << (idx & 63u);
+  if ((word.load() & bit) == 0u) {
     if (cudaFuncSetAttribute(variant_func(v, bf16, traced),
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemLimit)) != cudaSuccess) {
       cudaGetLastError();
       return B2B_ERR_CUDA;
     }
-    d->attr_done.fetch_or(bit);
+    word.fetch_or(bit);
   }
   return B2B_OK;
 }
@@ -803,6 +881,32 @@ bool conv_params(ChainParams& p, int mode, int32_t N, int32_t H, int32_t W, int3
   const int64_t tiles = static_cast<int64_t>(N) * p.tiles_w * p.tiles_h;
   if (tiles > INT32_MAX) return false;
   p.num_tiles = static_cast<int32_t>(tiles);
+  // The conv + pool may also run over CTA pairs: one more feasible layout after the
+  // single-CTA ones (as for the b2b GEMM chain).
+  if (mode == MODE_POOL) {
+    ChainParams q = p;
+    size_t qs = 0;
+    Regions qr;
+    const bool single_ok = plan_smem(q, mode, false, false, &qs, &qr, -1);
+    const int nsingle = single_ok ? qr.ncand : 0;
+    ChainParams c = p;
+    size_t cs = 0;
+    Regions cr;
+    const bool pair_ok = plan_pool_cta2(c, &cs, &cr);
+    if (pair_ok && forced == nsingle) {
+      p = c;
+      *smem = cs;
+      if (regions) {
+        *regions = cr;
+        regions->cand = nsingle;
+        regions->ncand = nsingle + 1;
+      }
+      return true;
+    }
+    const bool ok = plan_smem(p, mode, false, false, smem, regions, forced);
+    if (ok && pair_ok && regions) regions->ncand += 1;
+    return ok;
+  }
   return plan_smem(p, mode, false, false, smem, regions, forced);
 }
 
@@ -1048,6 +1152,54 @@ b2b_status run_gemm3_with(const Choice& ch, Info* info, int dt, int64_t M, int32
 // ------------------------------------------------------------------------------------
 // conv-shaped entry points (4-D implicit-GEMM A operand)
 // ------------------------------------------------------------------------------------
+// The conv + pool over CTA pairs (plan_pool_cta2): clusters of two CTAs, at most as many
+// as can be resident at once; grid choices as for single CTAs, counted in pair-tiles.
+b2b_status run_pool_cta2(const Choice& ch, Info* info, const Regions& r, ChainParams& p,
+                         size_t smem, DeviceState* d, int32_t N, int32_t H, int32_t W, int32_t C,
+                         const void* x, const void* W0, int32_t C0, int32_t R, int32_t S, void* y,
+                         void* stream) {
+  const bool traced = p.trace != nullptr;
+  if (b2b_status st = ensure_smem_attribute(V_CONV_POOL_CTA2, d, p.is_bf16 != 0, traced);
+      st != B2B_OK)
+    return st;
+  const int ci = 4 + (p.is_bf16 ? 1 : 0) + (traced ? 2 : 0);
+  int clusters = d->cta2_clusters[ci].load();
+  if (clusters <= 0 || d->cta2_smem[ci].load() != smem) {
+    if (cta2_max_clusters(p.is_bf16 != 0, traced, smem, &clusters, true) != cudaSuccess ||
+        clusters < 1) {
+      cudaGetLastError();
+      return B2B_ERR_CUDA;
+    }
+    d->cta2_clusters[ci].store(clusters);
+    d->cta2_smem[ci].store(smem);
+  }
+  const int32_t pair_tiles = (p.num_tiles + 1) / 2;
+  const int pairs = grid_for(pair_tiles, clusters, ch.grid);
+  p.pf_second = 0;
+  if (info) *info = info_for(r, pair_tiles, clusters, false);
+  const uint64_t e = 2;
+  CUtensorMap ta, tw0, to;
+  // the halo box of each CTA's own tile, as the single-CTA kernel's
+  bool ok = make_map(&ta, x, p.is_bf16, 4,
+                     {static_cast<uint64_t>(C), static_cast<uint64_t>(W), static_cast<uint64_t>(H),
+                      static_cast<uint64_t>(N)},
+                     {C * e, static_cast<uint64_t>(W) * C * e, static_cast<uint64_t>(H) * W * C * e},
+                     {kChunkK, 16, static_cast<uint32_t>(8 + R - 1), 1});
+  // [C0][R*S][C]: half of the output channels (rows) of one tap's channel block per box
+  ok = ok && make_map(&tw0, W0, p.is_bf16, 3,
+                      {static_cast<uint64_t>(C), static_cast<uint64_t>(R) * S, static_cast<uint64_t>(C0)},
+                      {C * e, static_cast<uint64_t>(R) * S * C * e},
+                      {kChunkK, 1, static_cast<uint32_t>(p.N0p / 2)});
+  const int32_t Hp = H / 2, Wp = W / 2;
+  ok = ok && make_map(&to, y, p.is_bf16, 4,
+                      {static_cast<uint64_t>(C0), static_cast<uint64_t>(Wp), static_cast<uint64_t>(Hp),
+                       static_cast<uint64_t>(N)},
+                      {C0 * e, static_cast<uint64_t>(Wp) * C0 * e, static_cast<uint64_t>(Hp) * Wp * C0 * e},
+                      {64, 8, 4, 1});
+  if (!ok) return B2B_ERR_CUDA;
+  return launch(V_CONV_POOL_CTA2, d, ta, tw0, tw0, to, p, smem, 2 * pairs, stream);
+}
+
 b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t N, int32_t H,
                          int32_t W, int32_t C, const void* x, const void* W0, int32_t C0,
                          int32_t R, int32_t S, int32_t pad, int32_t stride, const void* b0, int e0,
@@ -1061,6 +1213,10 @@ b2b_status run_conv_with(const Choice& ch, Info* info, int mode, int dt, int32_t
   b2b_status st = B2B_OK;
   DeviceState* d = device_state(&st);
   if (d == nullptr) return st;
+  if (p.cta_pair) {
+    fill_common(p, dt, e0, e1, b0, b1, d, KID_CONV_POOL_CTA2);
+    return run_pool_cta2(ch, info, r, p, smem, d, N, H, W, C, x, W0, C0, R, S, y, stream);
+  }
   fill_common(p, dt, e0, e1, b0, b1, d, kid);
   const int grid = grid_for(p.num_tiles, d->num_sms, ch.grid);
   p.pf_second = 0;   // the implicit-GEMM A has no per-tile contiguous range to prefetch
@@ -1753,13 +1909,30 @@ struct ModelEval {
   bool shallow;       // fewer than three ring stages
 };
 
-// The problem's FLOPs, irreducible bytes, bias bytes per CTA, filter rows R and W2 bytes.
+// The problem's FLOPs, irreducible bytes, bias bytes per CTA, filter rows R and W2 bytes,
+// and each GEMM's FLOPs and N (the MMA's N, padded to 16).
 struct ModelProblem {
   double flops, floor_bytes, bias_cta, w2 = 0.0;
   int64_t R = 1;
   int32_t N0 = 0;
   bool three = false;
+  int ngemm = 0;
+  double gflops[3] = {0.0, 0.0, 0.0};
+  int32_t gn[3] = {0, 0, 0};
+  void gemm(double f, double n) {
+    gflops[ngemm] = f;
+    gn[ngemm++] = static_cast<int32_t>(round_up(static_cast<uint32_t>(n), 16u));
+  }
 };
+
+// Tensor-pipe cycles per MMA of 128 rows per SM are N / 2 at the bf16 peak; shorter MMAs
+// take a floor (measured on the GB300, operands resident: M128 x N64 x K16 48 cycles, the
+// pair's M256 x N64 x K16 43 cycles per SM's 128 rows; N >= 128 runs at the peak).  The
+// factor by which a GEMM of this N takes longer than the peak allows:
+double model_mma_factor(int32_t n, bool pair) {
+  const double ideal = std::max(1.0, n / 2.0), floor = pair ? 43.0 : 48.0;
+  return std::max(1.0, floor / ideal);
+}
 
 ModelProblem model_problem(int32_t kind, const int64_t* d, int32_t ndims) {
   ModelProblem m;
@@ -1768,6 +1941,8 @@ ModelProblem model_problem(int32_t kind, const int64_t* d, int32_t ndims) {
     case 0: {   // M, K0, N0, N1
       const double M = d[0], K0 = d[1], N0 = d[2], N1 = d[3];
       m.flops = 2.0 * M * (K0 * N0 + N0 * N1);
+      m.gemm(2.0 * M * K0 * N0, std::min(N0, 256.0));
+      m.gemm(2.0 * M * N0 * N1, N1);
       m.floor_bytes = e * (M * K0 + K0 * N0 + N0 * N1 + M * N1) + (N0 + N1) * e;
       m.bias_cta = (N0 + N1) * e;
       m.N0 = static_cast<int32_t>(d[2]);
@@ -1776,6 +1951,7 @@ ModelProblem model_problem(int32_t kind, const int64_t* d, int32_t ndims) {
     case 1: {   // M, K, N
       const double M = d[0], K = d[1], N = d[2];
       m.flops = 2.0 * M * (K * N);
+      m.gemm(m.flops, N);
       m.floor_bytes = e * (M * K + K * N + N + M * N);
       m.bias_cta = N * e;
       m.N0 = static_cast<int32_t>(d[2]);
@@ -1791,6 +1967,8 @@ ModelProblem model_problem(int32_t kind, const int64_t* d, int32_t ndims) {
       const double C1 = kind == 2 ? static_cast<double>(d[8]) : 0.0;
       const double x = static_cast<double>(d[0] * d[1] * d[2]) * C;
       m.flops = 2.0 * M * (RS * C * C0 + C0 * C1);
+      m.gemm(2.0 * M * RS * C * C0, C0);
+      if (kind == 2) m.gemm(2.0 * M * C0 * C1, C1);
       m.floor_bytes = kind == 2 ? e * (x + C0 * RS * C + C0 + C1 * C0 + C1 + M * C1)
                                 : e * (x + C0 * RS * C + C0 + M * C0);
       m.bias_cta = (C0 + C1) * e;
@@ -1801,6 +1979,7 @@ ModelProblem model_problem(int32_t kind, const int64_t* d, int32_t ndims) {
     case 4: {   // N, H, W, Cin, Cout
       const double N = d[0], H = d[1], W = d[2], Cin = d[3], Cout = d[4];
       m.flops = 2.0 * N * H * W * 9.0 * Cin * Cout;
+      m.gemm(m.flops, Cout);
       m.floor_bytes = e * (N * H * W * Cin + Cout * 9.0 * Cin + Cout +
                            N * static_cast<double>(d[1] / 2) * static_cast<double>(d[2] / 2) * Cout);
       m.bias_cta = Cout * e;
@@ -1811,6 +1990,9 @@ ModelProblem model_problem(int32_t kind, const int64_t* d, int32_t ndims) {
     default: {  // 5: M, K0, N0, N1, N2
       const double M = d[0], K0 = d[1], N0 = d[2], N1 = d[3], N2 = d[4];
       m.flops = 2.0 * M * (K0 * N0 + N0 * N1 + N1 * N2);
+      m.gemm(2.0 * M * K0 * N0, N0);
+      m.gemm(2.0 * M * N0 * N1, N1);
+      m.gemm(2.0 * M * N1 * N2, N2);
       m.floor_bytes = e * (M * K0 + K0 * N0 + N0 * N1 + N1 * N2 + N0 + N1 + N2 + M * N2);
       m.bias_cta = (N0 + N1 + N2) * e;
       m.w2 = N1 * N2 * e;
@@ -1839,7 +2021,22 @@ bool model_eval(int32_t kind, const int64_t* dims, int32_t ndims, int cand, Mode
   const double hbm = m.floor_bytes / (kModelHbmGBs * 1e3);
   double cta_bytes = 0.0, tensor = 0.0;
   int64_t n = 0;
-  if (p.cta_pair) {
+  // the problem's MMA time at the peak rate, stretched for short MMAs
+  double eff_flops = 0.0;
+  for (int g = 0; g < m.ngemm; ++g)
+    eff_flops += m.gflops[g] * model_mma_factor(m.gn[g], p.cta_pair != 0);
+  const double sm_rate = kModelTensorTF * 1e6 / kModelSms;
+  if (p.cta_pair && mode == MODE_POOL) {
+    // conv + pool pairs: each CTA its own 8 x 16 tile of every pair-tile (halo boxes),
+    // its half of the filters once, its half of the bias
+    const int64_t pair_tiles = (p.num_tiles + 1) / 2;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(pair_tiles, kModelSms / 2));
+    n = (pair_tiles + grid - 1) / grid;
+    const double nn = static_cast<double>(n);
+    cta_bytes = static_cast<double>(p.kstages0) * p.a_stage_bytes * nn +
+                static_cast<double>(p.kchunks0) * p.w0_chunk_bytes + (p.N0p / 2) * 2.0;
+    tensor = eff_flops / tiles * nn / sm_rate;
+  } else if (p.cta_pair) {
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(p.num_tiles, kModelSms / 2));
     n = (p.num_tiles + grid - 1) / grid;
     const double ctas = 2.0 * static_cast<double>(grid);
@@ -1848,7 +2045,7 @@ bool model_eval(int32_t kind, const int64_t* dims, int32_t ndims, int cand, Mode
     const double W1 = ctas * p.kchunks1 * p.w1_chunk_bytes;
     const double bias = ctas * (p.N0p / 2 + p.N1p / 2) * 2.0;
     cta_bytes = A / (2.0 * tiles) * static_cast<double>(n) + (W0 + W1 + bias) / ctas;
-    tensor = m.flops / (2.0 * tiles) * static_cast<double>(n) / (kModelTensorTF * 1e6 / kModelSms);
+    tensor = eff_flops / (2.0 * tiles) * static_cast<double>(n) / sm_rate;
   } else {
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(p.num_tiles, kModelSms));
     const int64_t q = p.num_tiles / grid, rem = p.num_tiles % grid;
@@ -1883,7 +2080,7 @@ bool model_eval(int32_t kind, const int64_t* dims, int32_t ndims, int cand, Mode
         cta_bytes += (tiles * w1) / tiles * nn;
       }
     }
-    tensor = m.flops / tiles * nn / (kModelTensorTF * 1e6 / kModelSms);
+    tensor = eff_flops / tiles * nn / sm_rate;
   }
   const double l2 = cta_bytes / (kModelL2BytesPerClk * kModelSmMHz);
   double d[3] = {hbm, l2, tensor};

@@ -24,6 +24,7 @@ enum KernelId : uint32_t {
   KID_CONV_POOL = 7,
   KID_GEMM_CHAIN3 = 8,
   KID_GEMM_CHAIN_CTA2 = 9,   // b2b GEMM chain over CTA pairs (cta_group::2)
+  KID_CONV_POOL_CTA2 = 10,   // conv + pool over CTA pairs
   KID_PROBE = 15,
 };
 

@@ -29,7 +29,15 @@ namespace b2b {
                           const CUtensorMap& out, const ChainParams& p, int grid, size_t smem, \
                           cudaStream_t s);                                                   \
   template <bool BF16>                                                                       \
-  cudaError_t cta2_clusters(size_t smem, int* clusters);
+  cudaError_t cta2_clusters(size_t smem, int* clusters);                                     \
+  template <bool BF16>                                                                       \
+  const void* pool2_func();                                                                  \
+  template <bool BF16>                                                                       \
+  cudaError_t pool2_launch(const CUtensorMap& a, const CUtensorMap& w0, const CUtensorMap& w1, \
+                           const CUtensorMap& out, const ChainParams& p, int grid, size_t smem, \
+                           cudaStream_t s);                                                  \
+  template <bool BF16>                                                                       \
+  cudaError_t pool2_clusters(size_t smem, int* clusters);
 namespace plain {
 B2B_UNIT_DECLS
 }
@@ -47,6 +55,10 @@ const void* variant_func(Variant v, bool bf16, bool trace) {
   if (v == V_GEMM_CHAIN_CTA2) {
     if (trace) return bf16 ? traced::cta2_func<true>() : traced::cta2_func<false>();
     return bf16 ? plain::cta2_func<true>() : plain::cta2_func<false>();
+  }
+  if (v == V_CONV_POOL_CTA2) {
+    if (trace) return bf16 ? traced::pool2_func<true>() : traced::pool2_func<false>();
+    return bf16 ? plain::pool2_func<true>() : plain::pool2_func<false>();
   }
   if (trace) {
     if (is_a4d(v)) return bf16 ? traced::variant_func_a4d<true>(v) : traced::variant_func_a4d<false>(v);
@@ -67,6 +79,13 @@ cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w
     return bf16 ? plain::cta2_launch<true>(a, w0, w1, out, p, grid, smem, stream)
                 : plain::cta2_launch<false>(a, w0, w1, out, p, grid, smem, stream);
   }
+  if (v == V_CONV_POOL_CTA2) {
+    if (p.trace != nullptr)
+      return bf16 ? traced::pool2_launch<true>(a, w0, w1, out, p, grid, smem, stream)
+                  : traced::pool2_launch<false>(a, w0, w1, out, p, grid, smem, stream);
+    return bf16 ? plain::pool2_launch<true>(a, w0, w1, out, p, grid, smem, stream)
+                : plain::pool2_launch<false>(a, w0, w1, out, p, grid, smem, stream);
+  }
   if (p.trace != nullptr) {
     if (is_a4d(v))
       return bf16 ? traced::launch_variant_a4d<true>(v, a, w0, w1, out, p, grid, smem, stream)
@@ -81,7 +100,14 @@ cudaError_t launch_variant(Variant v, const CUtensorMap& a, const CUtensorMap& w
               : plain::launch_variant_a2d<false>(v, a, w0, w1, out, p, grid, smem, stream);
 }
 
-cudaError_t cta2_max_clusters(bool bf16, bool trace, size_t smem, int* clusters) {
+cudaError_t cta2_max_clusters(bool bf16, bool trace, size_t smem, int* clusters, bool pool) {
+  if (pool) {
+    if (trace)
+      return bf16 ? traced::pool2_clusters<true>(smem, clusters)
+                  : traced::pool2_clusters<false>(smem, clusters);
+    return bf16 ? plain::pool2_clusters<true>(smem, clusters)
+                : plain::pool2_clusters<false>(smem, clusters);
+  }
   if (trace)
     return bf16 ? traced::cta2_clusters<true>(smem, clusters)
                 : traced::cta2_clusters<false>(smem, clusters);

@@ -29,8 +29,8 @@ enum Variant : int {
   V_GEMM_CHAIN_PAIR_W0,   // tile pairs, P in TMEM, W0 resident, A and W1 streamed, output
                           //   stored from registers
   V_GEMM_CHAIN_CTA2,      // the chain over CTA pairs (chain_cta2_kernel.cuh)
-  V_CONV_CHAIN_2I,        // conv chain, two MMA issuers, P in TMEM, output stored from
-                          //   registers
+  V_CONV_CHAIN_2I,        // conv chain, two MMA issuers, P in TMEM, output staged per warp
+  V_CONV_POOL_CTA2,       // conv + pool over CTA pairs (chain_cta2_pool_kernel.cuh)
   V_COUNT
 };
 
@@ -61,10 +61,10 @@ inline cudaError_t launch_chain(ChainKernelFn fn, const CUtensorMap& a, const CU
 inline cudaError_t launch_chain_cta2(ChainKernelFn fn, const CUtensorMap& a, const CUtensorMap& w0,
                                      const CUtensorMap& w1, const CUtensorMap& out,
                                      const ChainParams& p, int grid, size_t smem,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, int threads = kNumThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(static_cast<unsigned>(kNumThreads));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -79,10 +79,11 @@ inline cudaError_t launch_chain_cta2(ChainKernelFn fn, const CUtensorMap& a, con
   return cudaLaunchKernelEx(&cfg, fn, a, w0, w1, out, p);
 }
 
-// How many clusters of two CTAs of the CTA-pair kernel (dtype, build) can be resident at
-// once with `smem` bytes of dynamic shared memory each (its function attributes set), or
-// an error.
-cudaError_t cta2_max_clusters(bool bf16, bool trace, size_t smem, int* clusters);
+// How many clusters of two CTAs of a CTA-pair kernel (the b2b GEMM chain's, or with `pool`
+// the conv + pool one; dtype, build) can be resident at once with `smem` bytes of dynamic
+// shared memory each (its function attributes set), or an error.
+cudaError_t cta2_max_clusters(bool bf16, bool trace, size_t smem, int* clusters,
+                              bool pool = false);
 
 // Kernel function pointer of a variant, operand dtype and build (with or without the event
 // trace), for cudaFuncSetAttribute.

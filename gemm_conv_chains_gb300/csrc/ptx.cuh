@@ -554,6 +554,18 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t pred, uint32_t dst, co
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t pred, uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%1], [%2, {%4, %5, %6, %7}], [%3], %8;\n\t}" ::"r"(pred),
+      "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "l"(policy)
+      : "memory");
+}
+
 // TMEM allocation for the pair: one warp in EACH CTA executes it, and both get the same
 // columns.  Whole warp.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
@@ -581,6 +593,30 @@ __device__ __forceinline__ void mma_pair_ss(uint32_t pred, uint32_t d_tmem, uint
       "setp.ne.b32 p, %5, 0;\n\t"
       "@q tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %4, p;\n\t}" ::"r"(pred),
       "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four K steps of mma_pair_ss in one block (as mma_f16_ss_x4): the first accumulates when
+// `accumulate` != 0, the others always.
+__device__ __forceinline__ void mma_pair_ss_x4(uint32_t pred, uint32_t d_tmem, uint64_t a,
+                                               uint64_t b, uint64_t astep, uint64_t bstep,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred q, p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 q, %0, 0;\n\t"
+      "setp.ne.b32 p, %7, 0;\n\t"
+      "setp.eq.b32 t, %0, %0;\n\t"
+      "add.s64 a1, %2, %4;\n\t"
+      "add.s64 b1, %3, %5;\n\t"
+      "add.s64 a2, a1, %4;\n\t"
+      "add.s64 b2, b1, %5;\n\t"
+      "add.s64 a3, a2, %4;\n\t"
+      "add.s64 b3, b2, %5;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%1], %2, %3, %6, p;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%1], a1, b1, %6, t;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%1], a2, b2, %6, t;\n\t"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%1], a3, b3, %6, t;\n\t}" ::"r"(pred),
+      "r"(d_tmem), "l"(a), "l"(b), "l"(astep), "l"(bstep), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 

@@ -147,6 +147,16 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
     epilogue warps).  `A_in_bounds` (not in the total) is the part of A inside the
     tensor; A / A_in_bounds is the waste of ragged and halo tiles."""
     plan = plan or plan_of(w)
+    if _pool_pair(plan):
+        # conv + pool pairs: each CTA its own tile's halo boxes (an odd last pair-tile's
+        # empty second tile included), its half of the filters and of the bias once
+        pairs = len(tiles_per_cta(-(-plan["tiles"] // 2), num_sms // 2))
+        out = {"A": 2 * -(-plan["tiles"] // 2) * (plan["kchunks0"] // 3) * plan["a_stage_bytes"],
+               "W0": 2 * pairs * plan["kchunks0"] * plan["w0_chunk"],
+               "bias": 2 * pairs * plan["N0p"] // 2 * ELEM}
+        out["total"] = sum(out.values())
+        out["A_in_bounds"] = _conv_tile_input_bytes(w.N, w.H, w.W, w.Cin, 3, 3, 1, True)
+        return out
     if plan.get("cta_pair"):
         return _cta_pair_traffic(w, plan, num_sms)
     per_cta = tiles_per_cta(plan["tiles"], num_sms)
@@ -265,6 +275,11 @@ def chain_buffers(plan: dict) -> List[Buffer]:
     whole = (0, 5)
     bufs = [Buffer("ring", plan["ring"], whole), Buffer("bias", plan["bias"], whole),
             Buffer("bar", plan["bar"], whole)]
+    if _pool_pair(plan):
+        # conv + pool pairs: half of the filters resident, one pooled staging tile per
+        # epilogue warpgroup
+        return bufs + [Buffer("weights", plan["w_res"], whole), Buffer("out0", plan["out"], whole),
+                       Buffer("out1", plan["out"], whole)]
     if plan.get("cta_pair"):
         # CTA pairs: the halves of both weights resident, P in TMEM, and (when the ring keeps
         # five stages beside it) a 4 KiB output staging slot per epilogue warp
@@ -339,6 +354,43 @@ def read_ncu_raw_csv(path: str) -> Dict[str, float]:
 L2_TO_SM_BYTES_PER_CLK = 89.0
 
 
+def mma_factor(n: int, pair: bool = False) -> float:
+    """How much longer than the bf16 peak allows a GEMM of MMA width N takes: an MMA of
+    128 rows per SM needs N / 2 cycles at the peak, but short ones take a floor (measured,
+    operands resident: M128 x N64 x K16 48 cycles, a pair's M256 x N64 x K16 43 cycles per
+    SM's 128 rows; N >= 128 runs at the peak)."""
+    return max(1.0, (43.0 if pair else 48.0) / max(1.0, n / 2))
+
+
+def gemm_shapes(w) -> List[Tuple[float, int]]:
+    """Each GEMM of the workload's fused launch: its FLOPs and its MMA width N (padded to
+    16; GEMM0 of a wide chain runs in passes of at most 256)."""
+    r16 = lambda n: -(-n // 16) * 16
+    if isinstance(w, wl.GemmChain3):
+        return [(2.0 * w.M * w.K0 * w.N0, r16(w.N0)), (2.0 * w.M * w.N0 * w.N1, r16(w.N1)),
+                (2.0 * w.M * w.N1 * w.N2, r16(w.N2))]
+    if isinstance(w, wl.GemmChain):
+        out = [(2.0 * w.M * w.K0 * w.N0, r16(min(w.N0, 256)))]
+        if w.N1:
+            out.append((2.0 * w.M * w.N0 * w.N1, r16(w.N1)))
+        return out
+    if isinstance(w, wl.ConvChain):
+        out = [(2.0 * w.M * w.R * w.S * w.C * w.C0, r16(w.C0))]
+        if w.C1:
+            out.append((2.0 * w.M * w.C0 * w.C1, r16(w.C1)))
+        return out
+    return [(float(w.flops), r16(w.Cout))]
+
+
+def _mma_flops(w, pair: bool) -> float:
+    """The workload's FLOPs weighted by mma_factor: its MMA time at the peak rate."""
+    return sum(f * mma_factor(n, pair) for f, n in gemm_shapes(w))
+
+
+def _pool_pair(plan: dict) -> bool:
+    return bool(plan.get("cta_pair")) and plan["mode"] == 2
+
+
 def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
                   tensor_tflops: float = 1951.4, sm_mhz: float = 2070.0,
                   num_sms: int = 152) -> Dict[str, float]:
@@ -349,6 +401,19 @@ def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
     TMA ingress.  Tensor: the busiest CTA's share of the MMA FLOPs over one SM's share of
     the peak.  `floor` is the largest; `bound` names it."""
     plan = plan or plan_of(w)
+    if _pool_pair(plan):
+        # conv + pool pairs: per SM its own tile of each of its pair's pair-tiles (halo
+        # boxes), its half of the filters and of the bias, one tile's MMA FLOPs per pair-tile
+        n = max(tiles_per_cta(-(-plan["tiles"] // 2), num_sms // 2))
+        R = getattr(w, "R", 3)
+        cta_bytes = (plan["kchunks0"] // R * plan["a_stage_bytes"] * n
+                     + plan["kchunks0"] * plan["w0_chunk"] + plan["N0p"] // 2 * ELEM)
+        out = {"hbm_us": w.floor_bytes / (hbm_gbs * 1e3),
+               "l2_us": cta_bytes / (L2_TO_SM_BYTES_PER_CLK * sm_mhz),
+               "tensor_us": _mma_flops(w, True) / plan["tiles"] * n / (tensor_tflops * 1e6 / num_sms)}
+        out["bound"] = max(out, key=out.get)[:-3]
+        out["floor_us"] = max(out["hbm_us"], out["l2_us"], out["tensor_us"])
+        return out
     if plan.get("cta_pair"):
         # pairs of SMs share each 256-row tile; per SM: 128 rows of each of its pair's tiles,
         # its weight halves, half of each tile's MMA FLOPs
@@ -359,7 +424,8 @@ def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
         cta_bytes = (t["A"] / (2 * plan["tiles"]) * n + (t["W0"] + t["W1"] + t["bias"]) / ctas)
         out = {"hbm_us": w.floor_bytes / (hbm_gbs * 1e3),
                "l2_us": cta_bytes / (L2_TO_SM_BYTES_PER_CLK * sm_mhz),
-               "tensor_us": w.flops / (2 * plan["tiles"]) * n / (tensor_tflops * 1e6 / num_sms)}
+               "tensor_us": _mma_flops(w, True) / (2 * plan["tiles"]) * n
+               / (tensor_tflops * 1e6 / num_sms)}
         out["bound"] = max(out, key=out.get)[:-3]
         out["floor_us"] = max(out["hbm_us"], out["l2_us"], out["tensor_us"])
         return out
@@ -380,7 +446,7 @@ def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
     out = {
         "hbm_us": w.floor_bytes / (hbm_gbs * 1e3),
         "l2_us": cta_bytes / (L2_TO_SM_BYTES_PER_CLK * sm_mhz),
-        "tensor_us": w.flops / tiles * n / (tensor_tflops * 1e6 / num_sms),
+        "tensor_us": _mma_flops(w, False) / tiles * n / (tensor_tflops * 1e6 / num_sms),
     }
     out["bound"] = max(out, key=out.get)[:-3]
     out["floor_us"] = max(out["hbm_us"], out["l2_us"], out["tensor_us"])
@@ -517,12 +583,13 @@ def candidates(w, num_sms: int = 152) -> List[Candidate]:
         if not fits(plan):
             continue
         units = num_sms // 2 if plan.get("cta_pair") else num_sms
+        unit_tiles = -(-plan["tiles"] // 2) if _pool_pair(plan) else plan["tiles"]
         if plan["tiles"] == 0:
             b = {"hbm_us": 0.0, "l2_us": 0.0, "tensor_us": 0.0, "floor_us": 0.0, "bound": "hbm"}
             out.append(Candidate(c, plan, b, 0))
             continue
         out.append(Candidate(c, plan, launch_bounds(w, plan, num_sms=num_sms),
-                             max(tiles_per_cta(plan["tiles"], units))))
+                             max(tiles_per_cta(unit_tiles, units))))
     return out
 
 

@@ -213,6 +213,10 @@ def test_b2b_conv_guards(shape):
                                    ("bf16", 1, 20, 34, 32, 64)],
                          ids=lambda s: "-".join(map(str, s)))
 def test_conv_relu_maxpool_guards(shape):
+    _pool_guarded(shape)
+
+
+def _pool_guarded(shape):
     dt, N, H, W, Cin, Cout = shape
     w = wl.ConvPool("guard", dt, N, H, W, Cin, Cout)
     t = wl.pool_inputs(w, seed=33)
@@ -225,6 +229,22 @@ def test_conv_relu_maxpool_guards(shape):
     _slack_intact(obuf, int(np.prod(oshape)), OUT_FILL, "conv_relu_maxpool")
     ref = oracle.conv_relu_maxpool(dt, wl.to_bits(t["x"]), wl.to_bits(t["Wt"]), wl.to_bits(t["b"]))
     compare(dt, wl.to_bits(out.cpu()), ref, False, "conv_relu_maxpool guarded")
+
+
+@pytest.mark.parametrize("shape", [("f16", 1, 18, 20, 64, 64), ("bf16", 1, 20, 34, 32, 48)],
+                         ids=lambda s: "-".join(map(str, s)))
+def test_conv_relu_maxpool_cta_pair_guards(shape):
+    # the pair layout: each CTA stores its own pooled tile (an odd tile count leaves the
+    # last pair-tile's second tile empty: nothing stored past the output)
+    dt, N, H, W, Cin, Cout = shape
+    dims = (N, H, W, Cin, Cout)
+    n = ops.debug_plan("conv_relu_maxpool", dims, cand=0)["ncand"]
+    ops.set_choice("conv_relu_maxpool", dims, cand=n - 1)
+    try:
+        assert ops.debug_plan("conv_relu_maxpool", dims)["cta_pair"] == 1
+        _pool_guarded(shape)
+    finally:
+        ops.autotune_reset()
 
 
 def test_unfused_operators_guards():

@@ -428,6 +428,45 @@ def test_conv_relu_maxpool_random(shape):
     run_pool(*shape, False, seed=sum(shape[1:]) + 1)
 
 
+POOL_PAIR_SHAPES = [
+    # dtype, N, H, W, Cin, Cout over CTA pairs: an odd tile count (the last pair-tile's
+    # second tile empty), ragged tiles, N0 = 16 / 48 / 128, partial channel blocks, pairs
+    # with many pair-tiles (both MMA issuers busy)
+    ("f16", 1, 16, 16, 64, 64), ("f16", 3, 18, 20, 16, 48), ("bf16", 2, 32, 48, 64, 128),
+    ("f16", 1, 14, 30, 8, 16), ("bf16", 5, 36, 40, 64, 64), ("f16", 24, 56, 56, 64, 64),
+]
+
+
+@pytest.mark.parametrize("shape", POOL_PAIR_SHAPES, ids=lambda s: "-".join(map(str, s)))
+@pytest.mark.parametrize("integer", [True, False])
+def test_conv_relu_maxpool_cta_pair(shape, integer):
+    # the pair layout (pinned) against the oracle, and bit for bit against the single-CTA
+    # layout: the same products in the same order
+    dt, N, H, W, Cin, Cout = shape
+    dims = (N, H, W, Cin, Cout)
+    n = ops.debug_plan("conv_relu_maxpool", dims, cand=0)["ncand"]
+    w = wl.ConvPool("p2", dt, N, H, W, Cin, Cout)
+    t = wl.pool_inputs(w, seed=sum(dims) + integer, integer=integer)
+    args = (to_dev(t["x"]), to_dev(t["Wt"]), to_dev(t["b"]))
+    try:
+        ops.set_choice("conv_relu_maxpool", dims, cand=0)
+        assert ops.debug_plan("conv_relu_maxpool", dims)["cta_pair"] == 0
+        single = ops.conv_relu_maxpool(*args)
+        ops.set_choice("conv_relu_maxpool", dims, cand=n - 1)
+        assert ops.debug_plan("conv_relu_maxpool", dims)["cta_pair"] == 1
+        out = ops.conv_relu_maxpool(*args)
+        torch.cuda.synchronize()
+    finally:
+        ops.autotune_reset()
+    check_no_device_error()
+    got = wl.to_bits(out.cpu())
+    assert np.array_equal(got, wl.to_bits(single.cpu())), "pair and single-CTA layouts differ"
+    b = {k: wl.to_bits(v) for k, v in t.items()}
+    for i in sorted({0, N - 1}):
+        ref = oracle.conv_relu_maxpool(dt, b["x"][i:i + 1], b["Wt"], b["b"])
+        compare(dt, got[i:i + 1], ref, integer, f"conv_relu_maxpool pair image {i}")
+
+
 def test_conv_pool_workload_sampled_images():
     w = wl.CONV_POOL
     t = wl.pool_inputs(w, seed=0)

@@ -48,6 +48,8 @@ def check(kind, dims, row_major_w):
     if kind in ("b2b_conv_nhwc", "conv_bias_act_nhwc") and dims[5] == 1 and dims[6] == 1 and dims[7] == 0:
         R = 1   # a 1x1 pad-0 conv runs as a GEMM
     assert st == 0, (kind, dims, st)
+    if p["cta_pair"] and kind == "conv_relu_maxpool":
+        return check_pool_cta2(dims, p)
     if p["cta_pair"]:
         return check_cta2(kind, dims, p)
     mode = p["mode"]
@@ -210,6 +212,43 @@ def check(kind, dims, row_major_w):
     for (a, ca, na), (b, cb, nb) in itertools.combinations(accs, 2):
         assert ca + na <= cb or cb + nb <= ca, (a, b)
     assert N0p % 16 == 0 and 16 <= N0p <= 256 and N1p % 16 == 0 and N1p <= 256
+    return p
+
+
+def check_pool_cta2(dims, p):
+    """A conv + pool plan over CTA pairs: per CTA a ring of halo boxes ((8 + 2) x 16 pixels x
+    64 channels) of its own 8 x 16 tile, at least one tile's stages and one more; its half
+    of the filters resident (N0p / 2 rows x 128 B per tap and channel block); one 4 KiB
+    pooled staging tile per 64 channels for each epilogue warpgroup; the ONES tile and a
+    K-major bias block of its half; the barriers; four accumulators in TMEM; two MMA
+    issuers where half the ring holds a tile's stages."""
+    N, H, W, C, C0 = dims[:5]
+    N0p = p["N0p"]
+    assert p["mode"] == 2 and N0p % 16 == 0 and N0p <= 128
+    kc_tap = -(-C // 64)
+    assert p["kchunks0"] == 9 * kc_tap and p["halo"] == 1 and p["resident"] == 1
+    assert p["tiles"] == N * -(-H // 8) * -(-W // 16)
+    assert p["stage_bytes"] == p["a_stage_bytes"] == 10 * 16 * 128
+    assert p["ring"] == p["stages"] * p["stage_bytes"] and 3 * kc_tap + 1 <= p["stages"] <= 8
+    assert p["two_issuers"] == (1 if p["stages"] // 2 >= 3 * kc_tap else 0)
+    assert p["w0_chunk"] == N0p // 2 * 128 and p["w_res"] >= p["kchunks0"] * p["w0_chunk"]
+    nch = -(-N0p // 64)
+    assert p["out"] == nch * 4096 and p["off_out1"] == p["off_out0"] + p["out"]
+    assert p["bias"] >= 1024 + N0p // 2 * 128
+    assert p["nbuf"] == 4 and p["dual"] == 1 and p["groups"] == 2
+    regions = [("ring", p["off_ring"], p["ring"]), ("w0", p["off_w0"], p["w_res"]),
+               ("out", p["off_out0"], 2 * p["out"]), ("bias", p["off_bias"], p["bias"]),
+               ("bar", p["off_bar"], p["bar"])]
+    usable = p["smem"] - 1024
+    for name, off, size in regions:
+        assert off % 1024 == 0 and off + size <= usable, name
+    for (a, oa, sa), (b, ob, sb) in itertools.combinations(regions, 2):
+        assert oa + sa <= ob or ob + sb <= oa, (a, b)
+    assert p["smem"] <= SMEM_LIMIT
+    s0 = -(-N0p // 32) * 32
+    for b in range(4):
+        assert p[f"d0_col{b}"] == b * s0
+    assert 4 * s0 <= p["tmem_cols"] <= 512
     return p
 
 
