@@ -146,7 +146,11 @@ b2b_status b2b_conv_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_t W, 
  * through the (2,2,F) reuse tile; the conv output never reaches global memory).
  *   x  [N][H][W][Cin]     Wt [Cout][3][3][Cin]     b [Cout] or NULL
  *   y  [N][H/2][W/2][Cout] (output; an odd last row/column of the conv is dropped)
- * Limits: N >= 0; H, W >= 2; Cin >= 8; 8 <= Cout <= 256; Cin, Cout multiples of 8. */
+ * Limits: N >= 0; H, W >= 2; Cin >= 8; 8 <= Cout <= 256; Cin, Cout multiples of 8.
+ * For Cout <= 128 one more launch layout runs over CTA pairs (clusters of two CTAs, each
+ * MMA of 256 rows covering one 8 x 16 output tile per CTA, each CTA holding half of the
+ * filters; the last layout index, see b2b_debug_plan); the tile-graph model takes it where
+ * its bounds are lower and every pair runs three or more pairs of tiles. */
 b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t Cin,
                              const void* x, const void* Wt, const void* b, int32_t Cout,
                              void* y, void* stream);
@@ -273,13 +277,15 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * columns [2] (0 otherwise), the TMEM column split of a wide chain's two GEMM0 passes (256,
  * else 0), and 1 if W0 alone stays resident while A and W1 stream through the ring (P in
  * TMEM, tile pairs; the output is then stored from registers, with no staging tile), and
- * 1 if the chain runs over CTA pairs (clusters of two CTAs sharing each MMA of 256 rows,
- * each holding half of W0 and W1; tiles then count 256 rows), 1 if two warps issue
- * the MMAs of alternate tiles, each from its own half of the ring (the conv + pool kernel
- * with N0 <= 64 when half the ring holds a tile's stages; conv chains with halo boxes and
- * N0 <= 64 in their two-issuer layout), 1 if each epilogue warp stages its output 16
- * columns at a time in a 1 KiB slot of its own (that two-issuer layout), and the TMEM
- * columns of the two P buffers when P is kept in TMEM (else 0).  A choice pinned,
+ * 1 if the launch runs over CTA pairs (clusters of two CTAs sharing each MMA of 256 rows,
+ * each holding half of W0 (and W1); for the b2b GEMM chain tiles then count 256 rows, for
+ * the conv + pool they still count 8 x 16 tiles, two per MMA), 1 if two warps issue
+ * the MMAs of alternate tiles, each from its own half of the ring (the conv + pool kernels,
+ * single-CTA with N0 <= 64 or over CTA pairs, when half the ring holds a tile's stages;
+ * conv chains with halo boxes and N0 <= 64 in their two-issuer layout), 1 if each epilogue
+ * warp stages its output 16 columns at a time in a 1 KiB slot of its own (that two-issuer
+ * layout), and the TMEM columns of the two P buffers when P is kept in TMEM (else 0).  A
+ * choice pinned,
  * measured or ranked for these sizes is reflected; without one, the layout is the
  * tile-graph model's pick, as the entry point takes it (see b2b_set_autotune).
  * Returns the status the entry point would return for these sizes (B2B_OK if it would
