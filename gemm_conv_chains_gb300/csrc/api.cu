@@ -664,8 +664,8 @@ bool plan_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
 // Shared-memory plan of the conv + pool kernel over CTA pairs (chain_cta2_pool_kernel.cuh;
 // stride 1, R > 1, N0p <= 128): per CTA a ring of halo boxes of its own 8 x 16 tile, its
 // half of the filters resident (N0p / 2 rows of every tap and channel block), one pooled
-// staging tile per epilogue warpgroup, the ONES tile and a K-major bias block of its half,
-// the barriers; four accumulators of N0p columns in TMEM.  At least one tile's ring stages
+// staging tile per epilogue warpgroup, the bias of every channel (fp32), the barriers; two
+// accumulators of N0p columns in TMEM per MMA issuer.  At least one tile's ring stages
 // and one more.  p.num_tiles stays the count of 8 x 16 tiles (two per pair-tile).
 bool plan_pool_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   if (p.R < 2 || p.stride != 1 || p.N0p > 128 || p.N0p % 16 != 0) return false;
@@ -675,16 +675,21 @@ bool plan_pool_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   const uint32_t w0b = static_cast<uint32_t>(p.kchunks0) * p.w0_chunk_bytes;
   const uint32_t nch = static_cast<uint32_t>((p.N0p + 63) / 64);
   const uint32_t out_each = nch * kPoolChunkBytes;
-  const uint32_t bias_bytes = round_up(kOnesBytes + half * 128u, 1024u);
+  const uint32_t bias_bytes = 1024u;   // 256 fp32 words: the bias of every channel
   const uint32_t bar_bytes = 1024u;
   const uint32_t a_bytes = (7u + static_cast<uint32_t>(p.R)) * 2048u;
   const uint32_t kst = static_cast<uint32_t>(p.S * p.kc_per_tap);
   const uint32_t fixed = round_up(w0b, 1024u) + 2u * out_each + bias_bytes + bar_bytes;
   if (fixed >= budget) return false;
-  const uint32_t stages = std::min<uint32_t>(kMaxStages, (budget - fixed) / a_bytes);
+  const uint32_t stages = std::min<uint32_t>(kPool2MaxStages, (budget - fixed) / a_bytes);
   if (stages < kst + 1u) return false;
   const uint32_t s0 = round_up(static_cast<uint32_t>(p.N0p), 32u);
-  p.tmem_cols = pow2_at_least(4u * s0);
+  // MMA issuers in the leader, each over a sub-ring that holds a tile's stages, each with
+  // two accumulator buffers: three where six buffers fit TMEM, else two, else one
+  uint32_t issuers = std::min<uint32_t>(3u, stages / kst);
+  if (issuers == 3u && 6u * s0 > 512u) issuers = 2u;
+  if (issuers == 0u) issuers = 1u;
+  p.tmem_cols = pow2_at_least((issuers == 3u ? 6u : 4u) * s0);
   if (p.tmem_cols > 512u) return false;
   for (uint32_t b = 0; b < kMaxBufs; ++b) {
     p.d0_col[b] = b * s0;
@@ -699,8 +704,7 @@ bool plan_pool_cta2(ChainParams& p, size_t* smem_bytes, Regions* regions) {
   p.out_alias_p = 0;
   p.p_tmem = 0;
   p.halo = 1;
-  // two MMA issuers in the leader, each over half of the ring, where half holds a tile
-  p.two_issuers = stages / 2u >= kst ? 1 : 0;
+  p.two_issuers = static_cast<int32_t>(issuers) - 1;
   p.num_stages = stages;
   p.stage_bytes = a_bytes;
   p.a_stage_bytes = a_bytes;
@@ -2028,13 +2032,13 @@ bool model_eval(int32_t kind, const int64_t* dims, int32_t ndims, int cand, Mode
   const double sm_rate = kModelTensorTF * 1e6 / kModelSms;
   if (p.cta_pair && mode == MODE_POOL) {
     // conv + pool pairs: each CTA its own 8 x 16 tile of every pair-tile (halo boxes),
-    // its half of the filters once, its half of the bias
+    // its half of the filters once, the bias of every channel once
     const int64_t pair_tiles = (p.num_tiles + 1) / 2;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(pair_tiles, kModelSms / 2));
     n = (pair_tiles + grid - 1) / grid;
     const double nn = static_cast<double>(n);
     cta_bytes = static_cast<double>(p.kstages0) * p.a_stage_bytes * nn +
-                static_cast<double>(p.kchunks0) * p.w0_chunk_bytes + (p.N0p / 2) * 2.0;
+                static_cast<double>(p.kchunks0) * p.w0_chunk_bytes + p.N0p * 2.0;
     tensor = eff_flops / tiles * nn / sm_rate;
   } else if (p.cta_pair) {
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(p.num_tiles, kModelSms / 2));
@@ -2211,7 +2215,9 @@ static b2b_status debug_plan_with(int32_t kind, const int64_t* dims, int32_t ndi
                           static_cast<uint32_t>(p.N1p), static_cast<uint32_t>(mode),
                           static_cast<uint32_t>(p.p_tmem), static_cast<uint32_t>(p.w1_group),
                           p.w1_per_stage, static_cast<uint32_t>(p.halo), p.a_stage_bytes,
-                          1u << p.nbuf_log2, p.off_p[2], p.off_p[3], p.d0_col[2], p.d0_col[3],
+                          mode == MODE_POOL && p.cta_pair && p.two_issuers == 2 ? 6u
+                                                                              : 1u << p.nbuf_log2,
+                          p.off_p[2], p.off_p[3], p.d0_col[2], p.d0_col[3],
                           p.d1_col[2], p.d1_col[3], static_cast<uint32_t>(r.cand),
                           static_cast<uint32_t>(r.ncand), static_cast<uint32_t>(c.grid),
                           static_cast<uint32_t>(c.pf2), r.extend, p.off_w2, p.off_p1[0],

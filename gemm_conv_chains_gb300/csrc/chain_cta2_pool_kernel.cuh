@@ -16,18 +16,23 @@
 //               (once), completing on the LEADER CTA's barriers, which count both CTAs'
 //               bytes
 //   warp 1      TMEM (both CTAs allocate the pair's columns together); in the leader CTA
-//               only, the MMA issuer for both; its commits arrive on the barriers of both
+//               only, an MMA issuer for both; its commits arrive on the barriers of both
 //               CTAs at once
+//   warps 10,11 in the leader CTA, the second and third MMA issuers (p.two_issuers = 1,
+//               2): issuer j takes the pair-tiles i with i mod issuers = j from its own
+//               sub-ring of the ring, so that the others issue while one waits
 //   warps 2..9  epilogue, in both CTAs, two warpgroups taking alternate pair-tiles: the
-//               CTA's own 128 accumulator rows (bias included) -> ReLU, rounding -> 2x2
+//               CTA's own 128 accumulator rows + the bias (fp32) -> ReLU, rounding -> 2x2
 //               max in registers -> a 4 x 8 pooled tile staged in shared memory -> TMA
 //               store; each warp reports to the leader's barrier
 //
 // Pair q takes the pair-tiles q, q + pairs, ...; pair-tile u is the 8 x 16 output tiles 2u
 // (first CTA) and 2u + 1 (second).  An odd tile count leaves the last pair-tile's second
 // tile empty: its boxes lie past the last image (TMA reads zeros) and nothing is stored.
-// Four accumulator buffers per CTA: the i-th pair-tile of the pair uses buffer i & 3.
-// Limits (the host checks them): stride 1, R > 1 (halo boxes), N0p <= 128.
+// Two accumulator buffers per issuer (four, or six with three issuers): the i-th
+// pair-tile of the pair uses buffer i mod buffers.  Limits (the host checks them):
+// stride 1, R > 1 (halo boxes), N0p <= 128, and three issuers only where six buffers fit
+// the 512 TMEM columns.
 //
 // Every wait is bounded; a CTA that gives up leaves its loops, and both CTAs meet at one
 // cluster barrier before either exits.
@@ -38,19 +43,28 @@
 namespace b2b {
 namespace B2B_KNS {
 
-// Barrier slots at p.off_bar.  FULL, WFULL, ACC_EMPTY, BIAS_READY and MMA_DONE are used in
-// the leader CTA only; EMPTY and ACC_FULL in both (the leader's commits arrive on both).
+// Barrier slots at p.off_bar.  FULL, WFULL, ACC_EMPTY and MMA_DONE are used in the leader
+// CTA only; EMPTY and ACC_FULL in both (the leader's commits arrive on both).
 enum : uint32_t {
   QB_FULL0 = 0,
-  QB_EMPTY0 = kMaxStages,
-  QB_WFULL = 2 * kMaxStages,
+  QB_EMPTY0 = kPool2MaxStages,
+  QB_WFULL = 2 * kPool2MaxStages,
   QB_ACC_FULL0 = QB_WFULL + 1,
-  QB_ACC_EMPTY0 = QB_ACC_FULL0 + 4,
-  QB_BIAS_READY = QB_ACC_EMPTY0 + 4,
-  QB_MMA_DONE = QB_BIAS_READY + 1,
+  QB_ACC_EMPTY0 = QB_ACC_FULL0 + kPool2MaxBufs,
+  QB_MMA_DONE = QB_ACC_EMPTY0 + kPool2MaxBufs,
   QB_COUNT = QB_MMA_DONE + 1,
 };
 static_assert(8u * QB_COUNT + 8u <= kBarRegionBytes, "barrier region too small");
+
+// MMA issuers, accumulator buffers, and the TMEM column of buffer b (buffers are
+// p.d0_col[1] columns apart).
+__device__ __forceinline__ int pool2_issuers(const ChainParams& p) { return 1 + p.two_issuers; }
+__device__ __forceinline__ int pool2_bufs(const ChainParams& p) {
+  return p.two_issuers == 2 ? 6 : 4;
+}
+__device__ __forceinline__ uint32_t pool2_col(const ChainParams& p, uint32_t b) {
+  return b * static_cast<uint32_t>(p.d0_col[1]);
+}
 
 // Pair-tiles of the whole launch, and the number this pair processes.
 __device__ __forceinline__ int pool2_pairtiles(const ChainParams& p) {
@@ -67,30 +81,28 @@ __device__ __forceinline__ int32_t pool2_tile(int i, uint32_t rank) {
   return 2 * u + static_cast<int32_t>(rank);
 }
 
-// Bias operands of this CTA's half of the output channels: the ONES tile (as
-// fill_bias_operands), then a K-major B block of N0p / 2 rows x 128 B whose K element 0 in
-// row n is the bias of channel rank * N0p / 2 + n (all else zero) -- in the 128B-swizzled
-// layout, K element 0 of row n sits at byte n * 128 + (n & 7) * 16.  Every word is written
-// once, by one thread.
-__device__ __forceinline__ void fill_pool_bias_half(const ChainParams& p, uint8_t* region, int tid,
-                                                    int nthreads, uint32_t rank) {
-  const int half = p.N0p / 2;
-  const int nwords = (static_cast<int>(kOnesBytes) + half * 128) >> 2;
-  constexpr int kOnesWords = static_cast<int>(kOnesBytes) >> 2;
-  const uint32_t one = p.is_bf16 ? 0x3F80u : 0x3C00u;
-  uint32_t* words = reinterpret_cast<uint32_t*>(region);
-  for (int w = tid; w < nwords; w += nthreads) {
-    const int o = w << 2;
-    if (o < static_cast<int>(kOnesBytes)) {
-      words[w] = o == (o >> 7) * 144 ? one : 0u;
-    } else {
-      // the word of row n that holds K element 0 (low half: the bias; high half: 0)
-      const int e = w - kOnesWords, n = e >> 5;
-      const int col = static_cast<int>(rank) * half + n;
-      words[w] = (e & 31) == (n & 7) * 4 && col < p.N0 && p.b0 != nullptr
-                     ? static_cast<uint32_t>(p.b0[col])
-                     : 0u;
+// The sub-ring of issuer j of n: the ring's stages split as evenly as they go, issuer j
+// owning [start, end) and walking it in order (SubRing), so that every slot has one
+// consumer, never more than one phase ahead of its producer.
+__device__ __forceinline__ SubRing pool2_subring(const ChainParams& p, int j) {
+  const int n = pool2_issuers(p), S = static_cast<int>(p.num_stages);
+  const int per = S / n, extra = S % n;
+  const int start = j * per + min(j, extra);
+  return make_subring(start, start + per + (j < extra ? 1 : 0));
+}
+
+// The bias of every output channel as fp32 (zero past N0, and with no bias), 256 words
+// at `region`, one word per thread: the epilogue adds it to the accumulators.
+__device__ __forceinline__ void fill_pool_bias(const ChainParams& p, float* region, int tid,
+                                               int nthreads) {
+  for (int n = tid; n < 256; n += nthreads) {
+    float v = 0.0f;
+    if (n < p.N0 && p.b0 != nullptr) {
+      const uint16_t h = p.b0[n];
+      v = p.is_bf16 ? __uint_as_float(static_cast<uint32_t>(h) << 16)
+                    : __half2float(__ushort_as_half(h));
     }
+    region[n] = v;
   }
 }
 
@@ -117,9 +129,10 @@ __device__ void pool2_producer(const ChainParams& p, const CUtensorMap* tmA, con
                        leader_bar(QB_WFULL), k.cb * kChunkK, k.t,
                        static_cast<int32_t>(rank) * (p.N0p / 2), pol_keep);
   }
-  const int ntiles = pool2_local(p);
-  int stage = 0;
-  uint32_t phase = 0;
+  const int ntiles = pool2_local(p), nis = pool2_issuers(p);
+  // the walkers of the sub-rings of the current pair-tile's issuer (r0) and of the next
+  SubRing r0 = pool2_subring(p, 0), r1 = pool2_subring(p, min(1, nis - 1)),
+          r2 = pool2_subring(p, min(2, nis - 1));
   uint32_t issued = 0, issued_parity = 0;   // leader: per stage, a fill in flight and its parity
   bool ok = true;
   for (int i = 0; ok && i < ntiles; ++i) {
@@ -127,7 +140,8 @@ __device__ void pool2_producer(const ChainParams& p, const CUtensorMap* tmA, con
     const TileCoord tc = tile_coord<true>(p, t);   // past the last tile: an image past the end
     KPos k;
     for (int kc = 0; kc < p.kstages0; ++kc, k.next_halo(p)) {
-      if (p.two_issuers) subring_pos(p, i, kc, stage, phase);   // issuer i & 1's sub-ring
+      const int stage = r0.slot;
+      const uint32_t phase = r0.phase;
       if (!warp_mbar_wait(bars + 8u * (QB_EMPTY0 + stage), phase ^ 1u, p, abort_flag,
                           SITE_PRODUCER_EMPTY, t)) {
         ok = false;
@@ -142,7 +156,18 @@ __device__ void pool2_producer(const ChainParams& p, const CUtensorMap* tmA, con
       trace(EV_PROD_ISSUED, kc, i);
       issued |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+      advance_subring(r0);
+    }
+    // the next pair-tile belongs to the next issuer
+    if (nis == 2) {
+      const SubRing x = r0;
+      r0 = r1;
+      r1 = x;
+    } else if (nis == 3) {
+      const SubRing x = r0;
+      r0 = r1;
+      r1 = r2;
+      r2 = x;
     }
   }
   if (leader) {
@@ -159,40 +184,34 @@ __device__ void pool2_producer(const ChainParams& p, const CUtensorMap* tmA, con
   }
 }
 
-// Issuer `issuer` (0: warp 1; 1: warp 10, with p.two_issuers) of the leader CTA: with two
-// issuers each takes the pair-tiles of one parity (buffers issuer and issuer + 2) from its
-// own half of the ring, so that one issues while the other pauses between stages; the
-// epilogue warpgroup of the same parity drains them.
+// Issuer `issuer` (0: warp 1; 1, 2: warps 10, 11, with p.two_issuers) of the leader CTA:
+// it takes the pair-tiles i with i mod issuers = issuer, each into buffer i mod buffers,
+// from its own sub-ring of the ring; the epilogue warpgroup of i's parity drains them.
 template <bool BF16>
 __device__ void pool2_mma(const ChainParams& p, uint32_t base, uint32_t bars, uint32_t tmem_base,
                           volatile uint32_t* abort_flag, int issuer) {
   const uint32_t lead = elect_one();
   const uint32_t dt = BF16 ? 1u : 0u;
-  // M = 256 over the pair; the filters (B) and the bias block are K-major.
+  // M = 256 over the pair; the filters (B) are K-major.
   const uint32_t idesc0 = idesc_f16_f32(dt, 0u, 2 * kBlockM, p.N0p);
   const uint64_t ring_a = sdesc_sw128(base + p.off_ring, 16u, 1024u);
   const uint64_t res_w0 = sdesc_sw128(base + p.off_w0, 16u, 1024u);
-  const uint64_t ones_desc = sdesc_sw128(base + p.off_bias, 16u, 0u);
-  const uint64_t bias_desc = sdesc_sw128(base + p.off_bias + kOnesBytes, 16u, 1024u);
   const uint32_t stage_step = p.stage_bytes >> 4;
   const uint32_t w0_step = p.w0_chunk_bytes >> 4;
   constexpr uint64_t kStep = 32u >> 4;   // per 16-wide K step, K-major A and B
   const int last_rem = p.K0 - (p.kc_per_tap - 1) * kChunkK;
   const int last_nks = last_rem >= 64 ? 4 : (last_rem + 15) >> 4;
   const int ntiles = pool2_local(p);
+  const int nis = pool2_issuers(p), nbufs = pool2_bufs(p);
   Tracer trace(p, 1, issuer == 0 ? lead : 0u, 3);
-  const bool two = p.two_issuers != 0;
   bool ok = true;
-  int stage = 0;
-  uint32_t phase = 0;
+  SubRing ring = pool2_subring(p, issuer);   // this issuer's stages
+  uint32_t b = static_cast<uint32_t>(issuer), use = 0u;   // buffer i mod nbufs, its parity
   trace(EV_MMA_SETUP, 0, 0);
   grid_dependency_wait();
   trace(EV_DEP_READY, 0, 0);
   ok = warp_wait_tx(bars + 8u * QB_WFULL, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
-  if (ok)
-    ok = warp_wait_cl(true, bars + 8u * QB_BIAS_READY, 0u, p, abort_flag, SITE_MMA_WEIGHTS, 0);
-  for (int i = two ? issuer : 0; ok && i < ntiles; i += two ? 2 : 1) {
-    const uint32_t b = static_cast<uint32_t>(i) & 3u, use = (static_cast<uint32_t>(i) >> 2) & 1u;
+  for (int i = issuer; ok && i < ntiles; i += nis) {
     // both CTAs' epilogues have drained the buffer's previous pair-tile
     if (!warp_wait_cl(true, bars + 8u * (QB_ACC_EMPTY0 + b), use ^ 1u, p, abort_flag,
                       SITE_MMA_ACC_EMPTY, i)) {
@@ -201,10 +220,11 @@ __device__ void pool2_mma(const ChainParams& p, uint32_t base, uint32_t bars, ui
     }
     trace(EV_MMA_ACC_FREE, b, i);
     tc_fence_after_sync();
-    const uint32_t d0 = tmem_base + p.d0_col[b];
+    const uint32_t d0 = tmem_base + pool2_col(p, b);
     int cb = 0, s_tap = 0;
     for (int kc = 0; kc < p.kstages0; ++kc) {
-      if (two) subring_pos(p, i, kc, stage, phase);   // this issuer's sub-ring
+      const int stage = ring.slot;
+      const uint32_t phase = ring.phase;
       trace(EV_MMA_WAIT, kc, i);
       if (!warp_wait_tx(bars + 8u * (QB_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL, i)) {
         ok = false;
@@ -229,13 +249,17 @@ __device__ void pool2_mma(const ChainParams& p, uint32_t base, uint32_t bars, ui
       }
       trace(EV_MMA_ISSUED, kc, i);
       mma_commit_pair(lead, bars + 8u * (QB_EMPTY0 + stage), kBothCtas);   // frees both slots
-      if (++stage == static_cast<int>(p.num_stages)) { stage = 0; phase ^= 1u; }
+      advance_subring(ring);
       if (++cb == p.kc_per_tap) { cb = 0; ++s_tap; }
     }
     if (!ok) break;
-    mma_pair_ss(lead, d0, ones_desc, bias_desc, idesc0, 1u);   // D += bias
     mma_commit_pair(lead, bars + 8u * (QB_ACC_FULL0 + b), kBothCtas);
     trace(EV_MMA_G0_DONE, b, i);
+    b += static_cast<uint32_t>(nis);
+    if (b >= static_cast<uint32_t>(nbufs)) {
+      b -= static_cast<uint32_t>(nbufs);
+      use ^= 1u;
+    }
   }
   // Whatever happened, no MMA may still be running (reading either CTA's shared memory or
   // writing either CTA's TMEM) when the pair leaves.
@@ -243,6 +267,51 @@ __device__ void pool2_mma(const ChainParams& p, uint32_t base, uint32_t bars, ui
   (void)mbar_wait(bars + 8u * QB_MMA_DONE, 0u, p.wait_limit_ns, nullptr, p.err, p.kernel_id,
                   SITE_MMA_DRAIN, 0);
   __syncwarp();
+}
+
+// The CTA's 128 accumulator rows (the conv sums) of one pair-tile + the bias -> ReLU,
+// rounding -> 2x2 max -> the 4 x 8 pooled tile, 32 columns at a time (as drain_pool, with
+// the bias, 256 fp32 words at `bias`, added in fp32 before the rounding).
+template <bool BF16>
+__device__ __noinline__ void drain_pool_bias(uint32_t tm_lane, uint32_t col0, int ncols,
+                                             uint32_t bias, uint32_t tile, int q, int lane) {
+  const bool owner = (lane & 17) == 0;
+  const int prow = q * 8 + (lane >> 1);
+  for (int c = 0; c < ncols; c += 32) {
+    const bool two = c + 16 < ncols;
+    uint32_t a[16], b[16], v[8], w[8];
+    tmem_ld32(tm_lane + col0 + c, two, a, b);
+    float fa[16], fb[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 x = ld_shared_f4(bias + 4u * static_cast<uint32_t>(c + 4 * j));
+      const float4 y = ld_shared_f4(bias + 4u * static_cast<uint32_t>(c + 16 + 4 * j));
+      fa[4 * j] = x.x, fa[4 * j + 1] = x.y, fa[4 * j + 2] = x.z, fa[4 * j + 3] = x.w;
+      fb[4 * j] = y.x, fb[4 * j + 1] = y.y, fb[4 * j + 2] = y.z, fb[4 * j + 3] = y.w;
+    }
+    tmem_wait_ld(a, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = pack2<BF16, true>(__uint_as_float(a[2 * j]) + fa[2 * j],
+                               __uint_as_float(a[2 * j + 1]) + fa[2 * j + 1]);
+      w[j] = pack2<BF16, true>(__uint_as_float(b[2 * j]) + fb[2 * j],
+                               __uint_as_float(b[2 * j + 1]) + fb[2 * j + 1]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = max2<BF16>(v[j], __shfl_xor_sync(0xffffffffu, v[j], 1));
+      w[j] = max2<BF16>(w[j], __shfl_xor_sync(0xffffffffu, w[j], 1));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = max2<BF16>(v[j], __shfl_xor_sync(0xffffffffu, v[j], 16));
+      w[j] = max2<BF16>(w[j], __shfl_xor_sync(0xffffffffu, w[j], 16));
+    }
+    if (owner) {
+      st_row16_sw128(tile, prow, c, kPoolChunkBytes, v);
+      if (two) st_row16_sw128(tile, prow, c + 16, kPoolChunkBytes, w);
+    }
+  }
 }
 
 template <bool BF16>
@@ -260,9 +329,10 @@ __device__ void pool2_epilogue(const ChainParams& p, const CUtensorMap* tmOut, u
   const uint32_t out_tile = base + p.off_out[g];
   const int nch = (p.N0p + 63) >> 6;
   bool alive = true;
-  const int ntiles = pool2_local(p);
+  const int ntiles = pool2_local(p), nbufs = pool2_bufs(p);
+  const uint32_t bias = base + p.off_bias;
+  uint32_t b = static_cast<uint32_t>(g), use = 0u;   // buffer i mod nbufs, its parity
   for (int i = g; i < ntiles; i += 2) {
-    const uint32_t b = static_cast<uint32_t>(i) & 3u, use = (static_cast<uint32_t>(i) >> 2) & 1u;
     const int32_t t = pool2_tile(i, rank);
     const TileCoord tc = tile_coord<true>(p, t);
     alive = warp_wait_cl(alive, bars + 8u * (QB_ACC_FULL0 + b), use, p, abort_flag,
@@ -272,7 +342,7 @@ __device__ void pool2_epilogue(const ChainParams& p, const CUtensorMap* tmOut, u
     if (elected) bulk_wait_read_all();   // this group's staging is free again
     named_bar_sync(bar_id, 128u);
     if (elected) trace(EV_EPI_STAGING, g, i);
-    if (alive) drain_pool<BF16>(tm_lane, p.d0_col[b], p.N0p, out_tile, q, lane);
+    if (alive) drain_pool_bias<BF16>(tm_lane, pool2_col(p, b), p.N0p, bias, out_tile, q, lane);
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive_remote(leader_bar(QB_ACC_EMPTY0 + b));
@@ -285,13 +355,18 @@ __device__ void pool2_epilogue(const ChainParams& p, const CUtensorMap* tmOut, u
       bulk_commit_group();
       trace(EV_EPI_STORED, g, i);
     }
+    b += 2u;
+    if (b >= static_cast<uint32_t>(nbufs)) {
+      b -= static_cast<uint32_t>(nbufs);
+      use ^= 1u;
+    }
   }
   // the TMA engine has read every staged tile before the CTA can leave
   if (elected) bulk_wait_read_all();
 }
 
-// Warp 10 is the leader's second MMA issuer (p.two_issuers).
-constexpr int kPool2Threads = kNumThreads + 32;
+// Warps 10 and 11 are the leader's second and third MMA issuers (p.two_issuers).
+constexpr int kPool2Threads = kNumThreads + 64;
 
 template <bool BF16>
 __global__ void __launch_bounds__(kPool2Threads, 1)
@@ -323,12 +398,11 @@ __global__ void __launch_bounds__(kPool2Threads, 1)
       mbar_init(bars + 8u * (QB_EMPTY0 + s), 1);
     }
     mbar_init(bars + 8u * QB_WFULL, 1);
-    for (uint32_t b = 0; b < 4; ++b) {
+    for (int b = 0; b < pool2_bufs(p); ++b) {
       mbar_init(bars + 8u * (QB_ACC_FULL0 + b), 1);
       mbar_init(bars + 8u * (QB_ACC_EMPTY0 + b), 2 * 4);   // four warps of one group, per CTA
     }
-    mbar_init(bars + 8u * QB_BIAS_READY, 2 * kNumEpiWarps);
-    mbar_init(bars + 8u * QB_MMA_DONE, p.two_issuers ? 2u : 1u);
+    mbar_init(bars + 8u * QB_MMA_DONE, static_cast<uint32_t>(pool2_issuers(p)));
     *abort_flag = 0u;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -357,16 +431,16 @@ __global__ void __launch_bounds__(kPool2Threads, 1)
   } else if (warp == 1) {
     if (rank == 0) pool2_mma<BF16>(p, base, bars, tmem_base, abort_flag, 0);
     __syncwarp();
-  } else if (warp == kSecondIssuerWarp) {
-    if (rank == 0 && p.two_issuers) pool2_mma<BF16>(p, base, bars, tmem_base, abort_flag, 1);
+  } else if (warp >= kSecondIssuerWarp) {
+    const int issuer = warp - kSecondIssuerWarp + 1;
+    if (rank == 0 && issuer < pool2_issuers(p))
+      pool2_mma<BF16>(p, base, bars, tmem_base, abort_flag, issuer);
     __syncwarp();
   } else {
     grid_dependency_wait();
-    fill_pool_bias_half(p, base_ptr + p.off_bias, static_cast<int>(threadIdx.x) - 64,
-                        kNumEpiThreads, rank);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_cluster(mapa_shared(bars + 8u * QB_BIAS_READY, 0u));
+    fill_pool_bias(p, reinterpret_cast<float*>(base_ptr + p.off_bias),
+                   static_cast<int>(threadIdx.x) - 64, kNumEpiThreads);
+    named_bar_sync(4u, kNumEpiThreads);   // the bias words are written before any is read
     pool2_epilogue<BF16>(p, &tmOut, base, bars, tmem_base, rank, abort_flag);
   }
 

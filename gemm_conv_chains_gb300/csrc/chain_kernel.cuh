@@ -152,20 +152,37 @@ __device__ __forceinline__ int local_tiles(const ChainParams& p) {
   return b < p.num_tiles ? (p.num_tiles - 1 - b) / g + 1 : 0;
 }
 
+// A walker over the ring slots [start, end): the slot and phase parity of successive
+// stages, stepped by one per stage.  (No division per stage: with N = 64 the MMA issuers'
+// pauses between ring stages are what bounds a launch, and a slot computed from the tile
+// and stage index with two integer divisions made the conv + pool kernel ~10 % slower.)
+struct SubRing {
+  int start, end, slot;
+  uint32_t phase;
+};
+__device__ __forceinline__ SubRing make_subring(int start, int end) {
+  SubRing r;
+  r.start = start;
+  r.end = end;
+  r.slot = start;
+  r.phase = 0u;
+  return r;
+}
+__device__ __forceinline__ void advance_subring(SubRing& r) {
+  if (++r.slot == r.end) {
+    r.slot = r.start;
+    r.phase ^= 1u;
+  }
+}
+
 // Two MMA issuers (two_issuers(MODE, TWO)): each takes the tiles of one parity and the
 // ring is split into two sub-rings, [0, S/2) for even tiles and [S/2, S) for odd ones, so
 // that each sub-ring has one consumer that takes its slots in order (a consumer further
 // ahead than one phase of a slot would alias the barrier's phase parity).  The tiles of one
-// parity take consecutive positions in their sub-ring; slot and phase of stage kc of tile
-// it:
-__device__ __forceinline__ void subring_pos(const ChainParams& p, int it, int kc, int& slot,
-                                            uint32_t& phase) {
+// parity take consecutive positions in their sub-ring.
+__device__ __forceinline__ SubRing subring_of(const ChainParams& p, int parity) {
   const int s0 = static_cast<int>(p.num_stages) >> 1;
-  const int odd = it & 1;
-  const int n = odd ? static_cast<int>(p.num_stages) - s0 : s0;
-  const int pos = (it >> 1) * p.kstages0 + kc;
-  slot = (odd ? s0 : 0) + pos % n;
-  phase = static_cast<uint32_t>(pos / n) & 1u;
+  return parity ? make_subring(s0, static_cast<int>(p.num_stages)) : make_subring(0, s0);
 }
 
 // Buffer of the CTA's it-th tile and the phase parity of its barriers.
@@ -328,6 +345,9 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
 
   int stage = 0;
   uint32_t phase = 0;
+  // two issuers: the sub-rings of the next tile to load (its parity) and of the one after
+  const bool two = two_issuers(MODE, TWO) && p.two_issuers != 0;
+  SubRing sr_cur = subring_of(p, 0), sr_next = subring_of(p, 1);
   auto acquire = [&](int32_t t) -> bool {   // waits until ring slot `stage` is free
     return warp_mbar_wait(bars + 8u * (BAR_EMPTY0 + stage), phase ^ 1u, p, abort_flag,
                           SITE_PRODUCER_EMPTY, t);
@@ -343,7 +363,11 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
     const TileCoord tc = tile_coord<A4D>(p, t);
     KPos k;
     for (int kc = 0; kc < p.kstages0; ++kc) {
-      if (two_issuers(MODE, TWO) && p.two_issuers) subring_pos(p, it, kc, stage, phase);
+      if (two) {   // (tiles are loaded in order: it's parity is sr_cur's)
+        stage = sr_cur.slot;
+        phase = sr_cur.phase;
+        advance_subring(sr_cur);
+      }
       if (W0RES && it == 0) {
         // The resident W0, chunk by chunk beside the CTA's first tile, so that its first
         // MMAs wait for one chunk, not for the whole matrix.
@@ -368,6 +392,11 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
       if (kc == 0 && lead) prefetch_a_tile(p, t + 2 * static_cast<int32_t>(gridDim.x));
       trace(EV_PROD_ISSUED, kc, it);
       advance();
+    }
+    if (two) {
+      const SubRing x = sr_cur;
+      sr_cur = sr_next;
+      sr_next = x;
     }
     return true;
   };
@@ -587,6 +616,7 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
 
   int stage = 0;
   uint32_t phase = 0;
+  SubRing sr = subring_of(p, issuer);   // two issuers: this issuer's sub-ring
   const int ntiles = local_tiles(p);
   trace(EV_MMA_SETUP, 0, 0);
   // The setup above overlaps the previous grid's tail; no bounded wait below runs while
@@ -617,7 +647,11 @@ __device__ void mma_role(const ChainParams& p, uint32_t base, uint32_t bars, uin
     int cb = 0;       // channel block within the tap (4-D) / chunk index (2-D)
     int s_tap = 0;    // halo: the column tap of the stage
     for (int kc = 0; kc < p.kstages0; ++kc) {
-      if (two) subring_pos(p, it, kc, stage, phase);   // this issuer's sub-ring
+      if (two) {   // this issuer's sub-ring
+        stage = sr.slot;
+        phase = sr.phase;
+        advance_subring(sr);
+      }
       trace(EV_MMA_WAIT, kc, it);
       if (!warp_mbar_wait(bars + 8u * (BAR_FULL0 + stage), phase, p, abort_flag, SITE_MMA_FULL, t))
         return false;

@@ -93,6 +93,11 @@ __host__ __device__ constexpr int chain_threads(int mode, bool two) {
 constexpr int kSecondIssuerWarp = kNumThreads / 32;
 constexpr int kMaxStages = 8;
 constexpr int kMaxBufs = 4;          // accumulator / P buffers per CTA
+// The conv + pool kernel over CTA pairs: up to three MMA issuers (warps 1, 10 and 11),
+// each with two of up to six accumulators, over up to ten ring stages.
+constexpr int kPool2MaxStages = 10;
+constexpr int kPool2MaxBufs = 6;
+constexpr int kThirdIssuerWarp = kSecondIssuerWarp + 1;
 constexpr int kMaxW0Chunks = 8;      // K chunks of a W0 kept resident beside streamed W1
 // Bias operands in shared memory (at off_bias): a 1 KiB ONES tile, then per GEMM one
 // 2 KiB BIAS block per 64-wide N block.
@@ -177,9 +182,12 @@ struct ChainParams {
   int32_t two_issuers;          // (MODE_POOL; MODE_CHAIN with 4-D A, resident filters and
                                 //    P in TMEM) 1: warps 1 and 10 issue the MMAs of
                                 //    alternate tiles, the ring split into two sub-rings
-                                //    (subring_pos); 0: warp 1 alone, warp 10 idle.  A chain
+                                //    (subring_of); 0: warp 1 alone, warp 10 idle.  A chain
                                 //    then keeps D1 apart from D0 / P in TMEM (buffer b =
-                                //    issuer b) and stores its output with out_slots
+                                //    issuer b) and stores its output with out_slots; the conv
+                                //    + pool kernel over CTA pairs: the issuers beyond warp 1
+                                //    (0, 1 or 2: warps 10 and 11), each with its own
+                                //    sub-ring
   int32_t out_slots;            // (two-issuer conv chain) 1: each epilogue warp stages its 32
                                 //    rows' output 16 columns at a time in a 1 KiB slot of
                                 //    its own (kOutSlotBytes from off_out[0], unswizzled) and

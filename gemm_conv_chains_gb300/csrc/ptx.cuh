@@ -436,6 +436,16 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
                : "memory");
 }
 
+// Four consecutive fp32 words of shared memory at a 16-byte aligned address.
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // 32 consecutive columns in two x16 loads (the second only if `two`).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, bool two, uint32_t (&r)[16],
                                           uint32_t (&s)[16]) {

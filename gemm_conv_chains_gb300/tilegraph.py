@@ -149,11 +149,12 @@ def l2_to_smem_traffic(w, plan: Optional[dict] = None, num_sms: int = 152) -> Di
     plan = plan or plan_of(w)
     if _pool_pair(plan):
         # conv + pool pairs: each CTA its own tile's halo boxes (an odd last pair-tile's
-        # empty second tile included), its half of the filters and of the bias once
+        # empty second tile included), its half of the filters once and the bias of every
+        # channel once
         pairs = len(tiles_per_cta(-(-plan["tiles"] // 2), num_sms // 2))
         out = {"A": 2 * -(-plan["tiles"] // 2) * (plan["kchunks0"] // 3) * plan["a_stage_bytes"],
                "W0": 2 * pairs * plan["kchunks0"] * plan["w0_chunk"],
-               "bias": 2 * pairs * plan["N0p"] // 2 * ELEM}
+               "bias": 2 * pairs * plan["N0p"] * ELEM}
         out["total"] = sum(out.values())
         out["A_in_bounds"] = _conv_tile_input_bytes(w.N, w.H, w.W, w.Cin, 3, 3, 1, True)
         return out
@@ -403,11 +404,12 @@ def launch_bounds(w, plan: Optional[dict] = None, hbm_gbs: float = 6791.4,
     plan = plan or plan_of(w)
     if _pool_pair(plan):
         # conv + pool pairs: per SM its own tile of each of its pair's pair-tiles (halo
-        # boxes), its half of the filters and of the bias, one tile's MMA FLOPs per pair-tile
+        # boxes), its half of the filters, the bias of every channel, one tile's MMA FLOPs
+        # per pair-tile
         n = max(tiles_per_cta(-(-plan["tiles"] // 2), num_sms // 2))
         R = getattr(w, "R", 3)
         cta_bytes = (plan["kchunks0"] // R * plan["a_stage_bytes"] * n
-                     + plan["kchunks0"] * plan["w0_chunk"] + plan["N0p"] // 2 * ELEM)
+                     + plan["kchunks0"] * plan["w0_chunk"] + plan["N0p"] * ELEM)
         out = {"hbm_us": w.floor_bytes / (hbm_gbs * 1e3),
                "l2_us": cta_bytes / (L2_TO_SM_BYTES_PER_CLK * sm_mhz),
                "tensor_us": _mma_flops(w, True) / plan["tiles"] * n / (tensor_tflops * 1e6 / num_sms)}

@@ -219,23 +219,30 @@ def check_pool_cta2(dims, p):
     """A conv + pool plan over CTA pairs: per CTA a ring of halo boxes ((8 + 2) x 16 pixels x
     64 channels) of its own 8 x 16 tile, at least one tile's stages and one more; its half
     of the filters resident (N0p / 2 rows x 128 B per tap and channel block); one 4 KiB
-    pooled staging tile per 64 channels for each epilogue warpgroup; the ONES tile and a
-    K-major bias block of its half; the barriers; four accumulators in TMEM; two MMA
-    issuers where half the ring holds a tile's stages."""
+    pooled staging tile per 64 channels for each epilogue warpgroup; the bias of every
+    channel as 256 fp32 words; the barriers; MMA issuers in the leader as many as the ring
+    holds tiles' stages (up to three; three only where their six accumulators fit TMEM),
+    two accumulators in TMEM per issuer (four with fewer than three)."""
     N, H, W, C, C0 = dims[:5]
     N0p = p["N0p"]
     assert p["mode"] == 2 and N0p % 16 == 0 and N0p <= 128
     kc_tap = -(-C // 64)
+    kst = 3 * kc_tap
     assert p["kchunks0"] == 9 * kc_tap and p["halo"] == 1 and p["resident"] == 1
     assert p["tiles"] == N * -(-H // 8) * -(-W // 16)
     assert p["stage_bytes"] == p["a_stage_bytes"] == 10 * 16 * 128
-    assert p["ring"] == p["stages"] * p["stage_bytes"] and 3 * kc_tap + 1 <= p["stages"] <= 8
-    assert p["two_issuers"] == (1 if p["stages"] // 2 >= 3 * kc_tap else 0)
+    assert p["ring"] == p["stages"] * p["stage_bytes"] and kst + 1 <= p["stages"] <= 10
+    s0 = -(-N0p // 32) * 32
+    issuers = min(3, p["stages"] // kst)
+    if issuers == 3 and 6 * s0 > 512:
+        issuers = 2
+    assert p["two_issuers"] == issuers - 1
     assert p["w0_chunk"] == N0p // 2 * 128 and p["w_res"] >= p["kchunks0"] * p["w0_chunk"]
     nch = -(-N0p // 64)
     assert p["out"] == nch * 4096 and p["off_out1"] == p["off_out0"] + p["out"]
-    assert p["bias"] >= 1024 + N0p // 2 * 128
-    assert p["nbuf"] == 4 and p["dual"] == 1 and p["groups"] == 2
+    assert p["bias"] >= 256 * 4
+    nbuf = 6 if issuers == 3 else 4
+    assert p["nbuf"] == nbuf and p["dual"] == 1 and p["groups"] == 2
     regions = [("ring", p["off_ring"], p["ring"]), ("w0", p["off_w0"], p["w_res"]),
                ("out", p["off_out0"], 2 * p["out"]), ("bias", p["off_bias"], p["bias"]),
                ("bar", p["off_bar"], p["bar"])]
@@ -245,10 +252,9 @@ def check_pool_cta2(dims, p):
     for (a, oa, sa), (b, ob, sb) in itertools.combinations(regions, 2):
         assert oa + sa <= ob or ob + sb <= oa, (a, b)
     assert p["smem"] <= SMEM_LIMIT
-    s0 = -(-N0p // 32) * 32
     for b in range(4):
         assert p[f"d0_col{b}"] == b * s0
-    assert 4 * s0 <= p["tmem_cols"] <= 512
+    assert nbuf * s0 <= p["tmem_cols"] <= 512
     return p
 
 
@@ -545,11 +551,19 @@ def test_wide_chain_limits():
 
 def test_two_issuers_only_for_the_n64_halo_convs():
     # the conv + pool kernel with N <= 64 whose ring holds two tiles' stages splits it
-    # between two MMA issuers, and so does the conv chain with halo boxes and N0 <= 64 in
+    # between two MMA issuers (three over CTA pairs when it holds three), and so does the conv chain with halo boxes and N0 <= 64 in
     # its own layout (P in TMEM, per-warp output slots, a six-stage ring); every other
     # kernel keeps one
+    # (over CTA pairs, the model's pick for this pooled conv, the ring of nine stages holds
+    # three tiles' stages: three issuers)
     pool = check("conv_relu_maxpool", (32, 112, 112, 64, 64), False)
-    assert pool["two_issuers"] == 1 and pool["stages"] // 2 >= 3
+    assert pool["cta_pair"] == 1 and pool["two_issuers"] == 2 and pool["stages"] == 9
+    ops.set_choice("conv_relu_maxpool", (32, 112, 112, 64, 64), cand=0)
+    try:
+        pool = check("conv_relu_maxpool", (32, 112, 112, 64, 64), False)
+        assert pool["cta_pair"] == 0 and pool["two_issuers"] == 1 and pool["stages"] // 2 >= 3
+    finally:
+        ops.autotune_reset()
     chain = check("b2b_conv_nhwc", (32, 56, 56, 64, 64, 3, 3, 1, 128), False)
     assert chain["two_issuers"] == 1 and chain["out_slots"] == 1 and chain["halo"] == 1
     assert chain["stages"] == 6 and chain["p_tmem"] == 1 and chain["out"] == 8 * 1024
