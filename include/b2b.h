@@ -149,8 +149,11 @@ b2b_status b2b_conv_nhwc_strided(b2b_dtype dt, int32_t N, int32_t H, int32_t W, 
  * Limits: N >= 0; H, W >= 2; Cin >= 8; 8 <= Cout <= 256; Cin, Cout multiples of 8.
  * For Cout <= 128 one more launch layout runs over CTA pairs (clusters of two CTAs, each
  * MMA of 256 rows covering one 8 x 16 output tile per CTA, each CTA holding half of the
- * filters; the last layout index, see b2b_debug_plan); the tile-graph model takes it where
- * its bounds are lower and every pair runs three or more pairs of tiles. */
+ * filters, up to three MMA issuers; the bias is then added in fp32 after the sums rather
+ * than as a last MMA step, so that on non-integer data its outputs may differ from the
+ * single-CTA layout's in the last place, within the tolerance; the last layout index, see
+ * b2b_debug_plan); the tile-graph model takes it where its bounds are lower and every pair
+ * runs three or more pairs of tiles. */
 b2b_status conv_relu_maxpool(b2b_dtype dt, int32_t N, int32_t H, int32_t W, int32_t Cin,
                              const void* x, const void* Wt, const void* b, int32_t Cout,
                              void* y, void* stream);
@@ -266,7 +269,8 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * of shared memory (wide N0: GEMM1 then reads its A operand from TMEM), 1 if W1 is then
  * loaded once per pair of tiles into shared ring stages, the W1 chunks per stage, 1 if a
  * conv loads one halo box per column tap for all row taps, the A bytes per ring stage, the
- * number of accumulator buffers (tiles in flight: 1, 2 or 4), P offsets [2..3], GEMM0
+ * number of accumulator buffers (tiles in flight: 1, 2, 4, or 6 for the conv + pool over
+ * CTA pairs with three MMA issuers), P offsets [2..3], GEMM0
  * accumulator columns [2..3], GEMM1 accumulator columns [2..3], the layout taken (an
  * index into the feasible layouts, in the planner's order of preference), the number of
  * feasible layouts, and the pinned or measured grid and second-tile-prefetch choices
@@ -279,10 +283,12 @@ b2b_status b2b_probe_timeout(uint64_t limit_ns, void* stream);
  * TMEM, tile pairs; the output is then stored from registers, with no staging tile), and
  * 1 if the launch runs over CTA pairs (clusters of two CTAs sharing each MMA of 256 rows,
  * each holding half of W0 (and W1); for the b2b GEMM chain tiles then count 256 rows, for
- * the conv + pool they still count 8 x 16 tiles, two per MMA), 1 if two warps issue
- * the MMAs of alternate tiles, each from its own half of the ring (the conv + pool kernels,
- * single-CTA with N0 <= 64 or over CTA pairs, when half the ring holds a tile's stages;
- * conv chains with halo boxes and N0 <= 64 in their two-issuer layout), 1 if each epilogue
+ * the conv + pool they still count 8 x 16 tiles, two per MMA), the MMA issuers beyond the
+ * first: 1 if two warps issue the MMAs of alternate tiles, each from its own half of the
+ * ring (the single-CTA conv + pool kernel with N0 <= 64 when half the ring holds a tile's
+ * stages; conv chains with halo boxes and N0 <= 64 in their two-issuer layout), and for
+ * the conv + pool over CTA pairs 0, 1 or 2 (one issuer per tile's stages the ring holds,
+ * up to three; three only when their six accumulators fit TMEM), 1 if each epilogue
  * warp stages its output 16 columns at a time in a 1 KiB slot of its own (that two-issuer
  * layout), and the TMEM columns of the two P buffers when P is kept in TMEM (else 0).  A
  * choice pinned,
@@ -308,7 +314,8 @@ b2b_status b2b_debug_plan_candidate(int32_t kind, const int64_t* dims, int32_t n
  * one kernel, which compute the same products with the same
  * roundings: results are bit-identical, except that an R x S conv (R > 1) sums its taps
  * in another fp32 order when its filters are resident (halo loads) than when they are
- * streamed).
+ * streamed, and that the conv + pool over CTA pairs adds the bias in fp32 after the sums,
+ * not as a last MMA step).
  * The default layout of a problem is the pick of a tile-graph cost model (Welder notes,
  * "Scheduling policy": candidates are ordered by their traffic before any is profiled):
  * for each feasible layout it bounds the launch from below by HBM (the problem's
