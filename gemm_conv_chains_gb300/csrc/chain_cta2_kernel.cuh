@@ -153,7 +153,6 @@ __device__ void cta2_producer(const ChainParams& p, const CUtensorMap* tmA, cons
         mbar_arrive_expect_tx_if(lead, bars + 8u * (PB_FULL0 + stage), 2u * kABytes);
       tma_load_2d_pair(lead, base + p.off_ring + stage * p.stage_bytes, tmA,
                        leader_bar(PB_FULL0 + stage), kc * kChunkK, m0, pol_stream);
-      if (kc == 0 && lead) cta2_prefetch_rows(p, it + 2, rank);
       trace(EV_PROD_ISSUED, kc, it);
       issued |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -472,7 +471,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   if (warp == 0) {
     // This CTA's rows of the first two tiles into L2 while the previous kernel finishes
-    // (a hint only; see chain_kernel.cuh).
+    // (a hint only; see chain_kernel.cuh).  No further prefetches: prefetching tile it + 2
+    // behind tile it's first chunk made the FFN-like chain 4 % slower (42.6 against 40.8
+    // us at M = 262144), its bulk prefetches queueing beside the ring's own loads.
     if (lane == 0) {
       cta2_prefetch_rows(p, 0, rank);
       cta2_prefetch_rows(p, 1, rank);

@@ -386,10 +386,9 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
       if (stream_w0)
         load_w0_chunk<A4D, W0MN>(lead, p, tmW0, sbase + kABytes, k, fb, pol_keep);
       if (A4D && p.halo) k.next_halo(p); else k.next(p);
-      // Tile it + 2's A into L2 behind this tile's first chunk (tile 0, and tile 1 when
-      // the CTA has more tiles, were prefetched at the start), so that HBM stays busy
-      // ahead of the ring.
-      if (kc == 0 && lead) prefetch_a_tile(p, t + 2 * static_cast<int32_t>(gridDim.x));
+      // (Tile 0's A, and tile 1's when the CTA has more tiles, were prefetched into L2 at
+      // the start.  Prefetching tile it + 2 here as well measured 0-1.5 % slower on every
+      // workload: the ring's own loads keep HBM as busy.)
       trace(EV_PROD_ISSUED, kc, it);
       advance();
     }
@@ -435,8 +434,6 @@ __device__ void producer_role(const ChainParams& p, const CUtensorMap* tmA,
       mbar_arrive_expect_tx_if(lead, fb, kABytes + wbytes);
       load_a_chunk<MODE, A4D, W0MN, W1MN>(lead, p, tmA, sbase, tc, k, fb, pol_stream);
       load_w0_half(lead, p, tmW0, sbase + kABytes, kc, h, fb, pol_keep);
-      if (kc == 0 && h == (it & 1) && lead)
-        prefetch_a_tile(p, t + 2 * static_cast<int32_t>(gridDim.x));
       trace(EV_PROD_ISSUED, kc, it);
       advance();
     }
